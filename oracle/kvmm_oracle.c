@@ -1,0 +1,367 @@
+/*
+ * kvmm_oracle.c -- plain, slow CPU oracle for query-aware MinMax page
+ * selection followed by sparse paged GQA decode attention.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path links, loads or
+ * calls this file: it is used by the tests, by the smoke check and by the
+ * CPU-baseline leg of the benchmark.  It shares no code, header, table or
+ * helper with the CUDA library; the two only ever see the same input bytes.
+ *
+ * Every computation is written straight from its definition, one unit
+ * (batch b, layer l, KV head h) at a time, in double precision, with no
+ * blocking, fusion or reordering:
+ *
+ *   FlexiCache: Leveraging Temporal Stability of Attention Heads for
+ *   Efficient KV Cache Management (blog summary of the MLSys'26 paper)
+ *     - "Core method, 2. MinMax-metadata page scoring": every KV page keeps
+ *       the per-channel minimum and maximum of its keys; the query and these
+ *       bounds give an estimate of the largest dot product the page can
+ *       produce; the top-K pages are chosen per (layer, KV head).
+ *     - "Core method, 3. Periodic reranking and incremental promotion":
+ *       after a rerank only (current top-K minus previous top-K) is moved.
+ *     - "System design, head-level block table": the block table is
+ *       [batch, layer, head, logical_block]; evicted slots point at a null
+ *       block that is never dereferenced.
+ *     - "Core method, 1. Stability-differentiated placement": decode
+ *       attention runs over the top-K pages only.
+ *   KVDrive: A Holistic Multi-Tier KV Cache Management System for
+ *   Long-Context LLM Inference, "Background and key observations": Quest
+ *   multiplies the query with the keys' channel-wise min and max.
+ *
+ * Readings taken where the pages are silent (each is listed in the design doc):
+ *   - page score for one query head: sum_d max(q_d*min_d, q_d*max_d), the
+ *     exact maximum of q.k over the box [min, max];
+ *   - GQA: the KV head's score is the SUM of its query heads' scores
+ *     (group_reduce = 0); group_reduce = 1 takes the MAX instead;
+ *   - top-K ties go to the lower logical page index; if a unit has no more
+ *     than K pages, all of them are selected; the selection is emitted in
+ *     ascending page order;
+ *   - a partial last page uses only its valid tokens (< seq_len);
+ *   - min/max of bf16 values is taken in value order with -0 < +0, so the
+ *     result is a unique bf16 bit pattern;
+ *   - attention scale defaults to D^-1/2; output and log-sum-exp in double;
+ *     a unit with no valid token yields output 0 and lse = -inf.
+ *
+ * bf16 values are passed as their raw 16-bit patterns (uint16_t).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* Device-error bits, defined here on their own (same meaning as the
+ * library's): a selected logical page whose table entry is the null block,
+ * and a table entry outside the physical pool. */
+#define ORACLE_ERR_NULL_BLOCK 1
+#define ORACLE_ERR_OUT_OF_RANGE 2
+
+static double bf16_value(uint16_t bits)
+{
+    uint32_t u = (uint32_t)bits << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* a strictly before b in the order used for min/max: by value, and -0 < +0 */
+static int bf16_before(uint16_t a, uint16_t b)
+{
+    double x = bf16_value(a), y = bf16_value(b);
+    if (x < y) return 1;
+    if (x > y) return 0;
+    return (a & 0x8000u) && !(b & 0x8000u);
+}
+
+/* Resolve a logical page through the unit's block-table row.
+ * Returns the physical page, or -1 after setting the matching error bit. */
+static int64_t resolve_page(const int32_t* bt_row, int32_t logical, int64_t n_phys, int32_t* err)
+{
+    int32_t phys = bt_row[logical];
+    if (phys < 0) {
+        *err |= ORACLE_ERR_NULL_BLOCK;
+        return -1;
+    }
+    if ((int64_t)phys >= n_phys) {
+        *err |= ORACLE_ERR_OUT_OF_RANGE;
+        return -1;
+    }
+    return phys;
+}
+
+/* Number of valid tokens of logical page p in a sequence of seq_len tokens. */
+static int32_t valid_tokens(int32_t p, int32_t T, int32_t seq_len)
+{
+    int64_t first = (int64_t)p * T;
+    if (first >= seq_len) return 0;
+    int64_t n = (int64_t)seq_len - first;
+    return n < T ? (int32_t)n : T;
+}
+
+/* ---------------------------------------------------------------------------
+ * Append: write new token rows into their pages through the block table.
+ * Token tok_begin + j takes row j of new_k / new_v ([n][D]).
+ * Returns error bits; rows whose page is null or out of range are skipped.
+ */
+int32_t oracle_unit_append(uint16_t* k_pool, uint16_t* v_pool, int64_t n_phys, int32_t T, int32_t D,
+                           const int32_t* bt_row, int32_t tok_begin, int32_t tok_end,
+                           const uint16_t* new_k, const uint16_t* new_v)
+{
+    int32_t err = 0;
+    for (int32_t t = tok_begin; t < tok_end; ++t) {
+        int64_t phys = resolve_page(bt_row, t / T, n_phys, &err);
+        if (phys < 0) continue;
+        int64_t row = phys * T + (t % T);
+        for (int32_t d = 0; d < D; ++d) {
+            k_pool[row * D + d] = new_k[(int64_t)(t - tok_begin) * D + d];
+            v_pool[row * D + d] = new_v[(int64_t)(t - tok_begin) * D + d];
+        }
+    }
+    return err;
+}
+
+/* ---------------------------------------------------------------------------
+ * MinMax metadata of logical pages [page_begin, page_end) of one unit:
+ * meta[p][0][d] = min over the page's valid tokens of k[t][d],
+ * meta[p][1][d] = max over the same tokens.  Pages with no valid token and
+ * pages whose entry is null / out of range are left untouched.
+ */
+int32_t oracle_unit_minmax(const uint16_t* k_pool, int64_t n_phys, int32_t T, int32_t D,
+                           const int32_t* bt_row, int32_t seq_len, int32_t page_begin,
+                           int32_t page_end, uint16_t* meta)
+{
+    int32_t err = 0;
+    for (int32_t p = page_begin; p < page_end; ++p) {
+        int32_t n = valid_tokens(p, T, seq_len);
+        if (n == 0) continue;
+        int64_t phys = resolve_page(bt_row, p, n_phys, &err);
+        if (phys < 0) continue;
+        const uint16_t* page = k_pool + phys * T * D;
+        uint16_t* mn = meta + (int64_t)p * 2 * D;
+        uint16_t* mx = mn + D;
+        for (int32_t d = 0; d < D; ++d) {
+            uint16_t lo = page[d], hi = page[d];
+            for (int32_t r = 1; r < n; ++r) {
+                uint16_t x = page[(int64_t)r * D + d];
+                if (bf16_before(x, lo)) lo = x;
+                if (bf16_before(hi, x)) hi = x;
+            }
+            mn[d] = lo;
+            mx[d] = hi;
+        }
+    }
+    return err;
+}
+
+/* ---------------------------------------------------------------------------
+ * Page scores of one unit.  q is [G][D] (the query heads of the KV head's
+ * group), meta is [P][2][D].  For query head g:
+ *     s_g(p) = sum_d max(q[g][d] * min_p[d], q[g][d] * max_p[d])
+ * and the unit's score is sum_g s_g(p) (group_reduce 0) or max_g s_g(p)
+ * (group_reduce 1).
+ */
+void oracle_unit_scores(const uint16_t* q, int32_t G, int32_t D, const uint16_t* meta, int32_t P,
+                        int32_t group_reduce, double* scores)
+{
+    for (int32_t p = 0; p < P; ++p) {
+        const uint16_t* mn = meta + (int64_t)p * 2 * D;
+        const uint16_t* mx = mn + D;
+        double total = 0.0;
+        for (int32_t g = 0; g < G; ++g) {
+            double s = 0.0;
+            for (int32_t d = 0; d < D; ++d) {
+                double qd = bf16_value(q[(int64_t)g * D + d]);
+                double a = qd * bf16_value(mn[d]);
+                double b = qd * bf16_value(mx[d]);
+                s += (a > b) ? a : b;
+            }
+            if (group_reduce == 1)
+                total = (g == 0 || s > total) ? s : total;
+            else
+                total += s;
+        }
+        scores[p] = total;
+    }
+}
+
+/* ---------------------------------------------------------------------------
+ * Top-K: order the pages by (score descending, page index ascending), keep
+ * the first min(K, P), and return them in ascending page order.
+ */
+typedef struct {
+    double score;
+    int32_t page;
+} scored_page;
+
+static int by_score_then_page(const void* a, const void* b)
+{
+    const scored_page* x = (const scored_page*)a;
+    const scored_page* y = (const scored_page*)b;
+    if (x->score > y->score) return -1;
+    if (x->score < y->score) return 1;
+    return (x->page > y->page) - (x->page < y->page);
+}
+
+static int by_int(const void* a, const void* b)
+{
+    int32_t x = *(const int32_t*)a, y = *(const int32_t*)b;
+    return (x > y) - (x < y);
+}
+
+int32_t oracle_topk(const double* scores, int32_t P, int32_t K, int32_t* sel)
+{
+    if (P <= 0 || K <= 0) return 0;
+    scored_page* order = (scored_page*)malloc(sizeof(scored_page) * (size_t)P);
+    if (!order) return -1;
+    for (int32_t p = 0; p < P; ++p) {
+        order[p].score = scores[p];
+        order[p].page = p;
+    }
+    qsort(order, (size_t)P, sizeof(scored_page), by_score_then_page);
+    int32_t n = K < P ? K : P;
+    for (int32_t i = 0; i < n; ++i) sel[i] = order[i].page;
+    free(order);
+    qsort(sel, (size_t)n, sizeof(int32_t), by_int);
+    return n;
+}
+
+/* ---------------------------------------------------------------------------
+ * Set difference a \ b of two ascending lists, in ascending order.
+ * promoted = cur \ prev, evicted = prev \ cur.
+ */
+int32_t oracle_set_difference(const int32_t* a, int32_t na, const int32_t* b, int32_t nb, int32_t* out)
+{
+    int32_t n = 0;
+    for (int32_t i = 0; i < na; ++i) {
+        int found = 0;
+        for (int32_t j = 0; j < nb; ++j)
+            if (b[j] == a[i]) found = 1;
+        if (!found) out[n++] = a[i];
+    }
+    return n;
+}
+
+/* ---------------------------------------------------------------------------
+ * Softmax attention of G query heads over an explicit list of n key/value
+ * rows (row indices into the pools, in the order given):
+ *     z_t = scale * sum_d q[g][d] * k_t[d]
+ *     out[g] = sum_t exp(z_t - m) v_t / sum_t exp(z_t - m),   m = max_t z_t
+ *     lse[g] = m + log(sum_t exp(z_t - m))
+ */
+static void attend_rows(const uint16_t* q, int32_t G, int32_t D, const uint16_t* k_pool,
+                        const uint16_t* v_pool, const int64_t* rows, int64_t n, double scale,
+                        double* out, double* lse)
+{
+    double* z = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+    for (int32_t g = 0; g < G; ++g) {
+        double* o = out + (int64_t)g * D;
+        for (int32_t d = 0; d < D; ++d) o[d] = 0.0;
+        if (n == 0 || !z) {
+            lse[g] = -INFINITY;
+            continue;
+        }
+        double m = -INFINITY;
+        for (int64_t t = 0; t < n; ++t) {
+            double dot = 0.0;
+            for (int32_t d = 0; d < D; ++d)
+                dot += bf16_value(q[(int64_t)g * D + d]) * bf16_value(k_pool[rows[t] * D + d]);
+            z[t] = dot * scale;
+            if (z[t] > m) m = z[t];
+        }
+        double denom = 0.0;
+        for (int64_t t = 0; t < n; ++t) {
+            double w = exp(z[t] - m);
+            denom += w;
+            for (int32_t d = 0; d < D; ++d) o[d] += w * bf16_value(v_pool[rows[t] * D + d]);
+        }
+        for (int32_t d = 0; d < D; ++d) o[d] /= denom;
+        lse[g] = m + log(denom);
+    }
+    free(z);
+}
+
+/* Sparse decode attention of one unit over its selected logical pages
+ * sel[0..cnt), each resolved through the block-table row; tokens at or past
+ * seq_len are not attended; null / out-of-range entries set their error bit
+ * and contribute nothing.  scale <= 0 means D^-1/2. */
+int32_t oracle_unit_sparse_attention(const uint16_t* q, int32_t G, int32_t D, int32_t T,
+                                     const uint16_t* k_pool, const uint16_t* v_pool,
+                                     int64_t n_phys, const int32_t* bt_row, int32_t seq_len,
+                                     const int32_t* sel, int32_t cnt, double scale, double* out,
+                                     double* lse)
+{
+    int32_t err = 0;
+    if (scale <= 0.0) scale = 1.0 / sqrt((double)D);
+    int64_t* rows = (int64_t*)malloc(sizeof(int64_t) * ((size_t)cnt * T + 1));
+    int64_t n = 0;
+    for (int32_t i = 0; i < cnt; ++i) {
+        int32_t nv = valid_tokens(sel[i], T, seq_len);
+        if (nv == 0) continue;
+        int64_t phys = resolve_page(bt_row, sel[i], n_phys, &err);
+        if (phys < 0) continue;
+        for (int32_t r = 0; r < nv; ++r) rows[n++] = phys * T + r;
+    }
+    attend_rows(q, G, D, k_pool, v_pool, rows, n, scale, out, lse);
+    free(rows);
+    return err;
+}
+
+/* Dense decode attention of one unit: every token t < seq_len, in token
+ * order, each found through the block-table row. */
+int32_t oracle_unit_dense_attention(const uint16_t* q, int32_t G, int32_t D, int32_t T,
+                                    const uint16_t* k_pool, const uint16_t* v_pool,
+                                    int64_t n_phys, const int32_t* bt_row, int32_t seq_len,
+                                    double scale, double* out, double* lse)
+{
+    int32_t err = 0;
+    if (scale <= 0.0) scale = 1.0 / sqrt((double)D);
+    int64_t* rows = (int64_t*)malloc(sizeof(int64_t) * ((size_t)seq_len + 1));
+    int64_t n = 0;
+    for (int32_t t = 0; t < seq_len; ++t) {
+        int64_t phys = resolve_page(bt_row, t / T, n_phys, &err);
+        if (phys < 0) continue;
+        rows[n++] = phys * T + (t % T);
+    }
+    attend_rows(q, G, D, k_pool, v_pool, rows, n, scale, out, lse);
+    free(rows);
+    return err;
+}
+
+/* ---------------------------------------------------------------------------
+ * One decode step of one unit, in the method's order (the CPU baseline):
+ *   append the new token and refresh the MinMax of its page; if the unit is
+ *   rescored this step, score every page, select the top-K and list
+ *   promoted = cur \ prev and evicted = prev \ cur, then make cur the unit's
+ *   selection; otherwise keep the previous selection; finally run sparse
+ *   attention over the selection.
+ * sel / sel_cnt hold the previous selection on entry and the current one on
+ * return.  scores is caller scratch of P entries.
+ */
+int32_t oracle_unit_step(uint16_t* k_pool, uint16_t* v_pool, int64_t n_phys, int32_t T, int32_t D,
+                         const int32_t* bt_row, int32_t seq_len, const uint16_t* new_k,
+                         const uint16_t* new_v, uint16_t* meta, const uint16_t* q, int32_t G,
+                         int32_t rescore, int32_t K, int32_t group_reduce, int32_t* sel,
+                         int32_t* sel_cnt, int32_t* promoted, int32_t* n_promoted, int32_t* evicted,
+                         int32_t* n_evicted, double* scores, double scale, double* out, double* lse)
+{
+    int32_t err = 0;
+    int32_t P = (seq_len + T - 1) / T;
+    if (new_k && new_v && seq_len > 0) {
+        err |= oracle_unit_append(k_pool, v_pool, n_phys, T, D, bt_row, seq_len - 1, seq_len, new_k, new_v);
+        err |= oracle_unit_minmax(k_pool, n_phys, T, D, bt_row, seq_len, P - 1, P, meta);
+    }
+    *n_promoted = 0;
+    *n_evicted = 0;
+    if (rescore) {
+        int32_t* cur = (int32_t*)malloc(sizeof(int32_t) * (size_t)(K > 0 ? K : 1));
+        oracle_unit_scores(q, G, D, meta, P, group_reduce, scores);
+        int32_t n = oracle_topk(scores, P, K, cur);
+        *n_promoted = oracle_set_difference(cur, n, sel, *sel_cnt, promoted);
+        *n_evicted = oracle_set_difference(sel, *sel_cnt, cur, n, evicted);
+        memcpy(sel, cur, sizeof(int32_t) * (size_t)n);
+        *sel_cnt = n;
+        free(cur);
+    }
+    err |= oracle_unit_sparse_attention(q, G, D, T, k_pool, v_pool, n_phys, bt_row, seq_len, sel,
+                                        *sel_cnt, scale, out, lse);
+    return err;
+}
