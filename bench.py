@@ -1,0 +1,456 @@
+"""Benchmark: MinMax page selection + sparse paged decode attention on GB300.
+
+One step = one decode step of the Llama-3.1-8B-shaped 32K-context workload
+(32 layers, B=8, 32 query / 8 KV heads, head_dim 128, 16-token pages,
+budget 128 pages): per layer, append the new token and refresh its page's
+MinMax (kv_minmax_update), score every page and select the top-K
+(page_score_topk), list promoted pages (topk_promotion_diff) and attend over
+the selected pages (sparse_paged_decode_attn).  A layer-step is one layer of
+that step for the whole batch.
+
+Inputs are seeded synthetic tensors resident in HBM (32 GiB of K/V, 2 GiB of
+metadata); one step touches 4 GiB of distinct data, far more than the 129 MB
+L2, so no flush is needed between steps.  The step is captured once in a
+CUDA graph and replayed; CUDA events on the launching stream time the timed
+region and every launch of the scoring and attention kernels.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from paged_kv_cache_minmax_gb300 import workloads  # noqa: E402
+
+METRIC = "sparse decode attn+scoring: KV GB/s & % of HBM peak; layer-steps/s at 32K ctx"
+CFG = workloads.CONFIGS[2]
+FALLBACK_HBM_GBS = 6800.0
+
+
+# --------------------------------------------------------------------------- #
+# byte accounting                                                              #
+# --------------------------------------------------------------------------- #
+def algorithmic_bytes(cfg, rescored_units=None):
+    """Bytes one layer-step must move at minimum (all units of one layer).
+
+    meta   : MinMax rows of every page of every rescored unit (P * 2 * D * 2 B)
+    kv     : K and V rows of every selected page (K * T * D * 2 B each)
+    small  : q, selected table entries, selection lists (write + read), the
+             promotion diff, outputs, the appended token and its page's
+             re-read and metadata write.
+    """
+    units = cfg.B * cfg.Hkv
+    resc = units if rescored_units is None else rescored_units
+    P, K = cfg.P, min(cfg.K, cfg.P)
+    meta = resc * P * 2 * cfg.D * 2
+    kv = units * K * cfg.T * cfg.D * 2 * 2
+    page = cfg.T * cfg.D * 2
+    small = (cfg.B * cfg.Hq * cfg.D * 2 * 2          # q read by scoring and by attention
+             + units * K * 4                          # table entries of selected pages
+             + units * K * 4 * 3                      # selection written, read by diff and attention
+             + resc * K * 4 * 3                       # prev read, promoted written, prev committed
+             + cfg.B * cfg.Hq * (cfg.D + 1) * 4       # out + lse
+             + units * (2 * cfg.D * 2 + page + 2 * cfg.D * 2))  # new K/V row, page re-read, meta write
+    return {"meta": meta, "kv": kv, "small": small, "total": meta + kv + small,
+            "score_launch": meta + cfg.B * cfg.Hq * cfg.D * 2 + units * K * 4,
+            "attn_launch": kv + cfg.B * cfg.Hq * cfg.D * 2 + units * K * 8 + cfg.B * cfg.Hq * (cfg.D + 1) * 4}
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+# --------------------------------------------------------------------------- #
+# clocks during the timed region                                               #
+# --------------------------------------------------------------------------- #
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index=0, out_path=None):
+        self.out_path = out_path
+        self.proc = None
+        self.device_index = device_index
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.device_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+            if self.out_path:
+                with open(self.out_path, "w") as f:
+                    f.write(self.FIELDS + "\n" + "\n".join(self.lines) + "\n")
+
+    def summary(self):
+        if not getattr(self, "lines", None):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"], "samples": 0}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- #
+# CPU oracle timing (cpu_baseline and the reference arm)                      #
+# --------------------------------------------------------------------------- #
+def oracle_layer_sample(cfg, n_units, seed=2024, device=None):
+    """Host state for ``n_units`` units of one layer of ``cfg`` (compact pools)."""
+    import oracle
+
+    sub = workloads.scaled(cfg, B=max(1, -(-n_units // cfg.Hkv)), L=1, layers_alloc=None)
+    dev = device or ("cuda" if torch.cuda.is_available() else "cpu")
+    wl = workloads.generate(sub, device=dev, seed=seed)
+    nk, nv = workloads.step_tokens(wl, 0)
+    states = []
+    for u in range(n_units):
+        b, h = divmod(u, sub.Hkv)
+        row = wl.block_table[b, 0, h].cpu().numpy().astype(np.int32)
+        idx = torch.as_tensor(row[: sub.Pmax], dtype=torch.long, device=wl.k_pool.device)
+        kp = workloads.bf16_bits(wl.k_pool.index_select(0, idx))
+        vp = workloads.bf16_bits(wl.v_pool.index_select(0, idx))
+        local = np.arange(sub.Pmax, dtype=np.int32)
+        meta, _ = oracle.unit_minmax(kp, sub.T, local, int(wl.seq_len[b]))
+        stt = oracle.UnitState(kp, vp, sub.T, local, meta, sub.K)
+        qg = workloads.bf16_bits(wl.q[0, b, h * sub.G:(h + 1) * sub.G])
+        states.append((stt, int(wl.seq_len[b]), workloads.bf16_bits(nk[0, b, h]), workloads.bf16_bits(nv[0, b, h]),
+                       qg))
+    del wl
+    return states
+
+
+def run_oracle_units(states, threads):
+    """One decode step (rescored) of every unit in ``states``; returns seconds."""
+    import oracle
+    from concurrent.futures import ThreadPoolExecutor
+
+    def one(s):
+        stt, seq, nk, nv, qg = s
+        oracle.unit_step(stt, seq, nk, nv, qg, rescore=True)
+
+    t0 = time.perf_counter()
+    if threads <= 1:
+        for s in states:
+            one(s)
+    else:
+        with ThreadPoolExecutor(max_workers=threads) as ex:
+            list(ex.map(one, states))
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(cfg, target_seconds=12.0):
+    import oracle
+
+    oracle.build()
+    threads = os.cpu_count() or 1
+    units_per_layer = cfg.B * cfg.Hkv
+    states = oracle_layer_sample(cfg, min(units_per_layer, 16))
+    t1 = run_oracle_units(states, 1) / len(states)  # seconds of CPU per unit-step
+    reps = max(1, int(target_seconds / max(t1 * len(states), 1e-6)))
+    work = states * reps
+    wall = run_oracle_units(work, threads)
+    unit_steps = len(work)
+    ls_per_s = unit_steps / units_per_layer / wall
+    return {"value": ls_per_s, "unit": "layer-steps/s", "cores": threads, "kind": "oracle",
+            "sample": f"{unit_steps} unit-steps ({len(states)} distinct (batch, KV head) units of one layer of "
+                      f"{cfg.name}, each: append+MinMax, score all {cfg.P} pages, top-{cfg.K}, diff, attention) "
+                      f"on {threads} threads; {unit_steps / units_per_layer:.1f} layer-steps of work, "
+                      f"{t1 * unit_steps:.1f} s single-thread CPU"}
+
+
+def reference_arm(args):
+    """The oracle, as it stands, on the host cores: the slow reference program."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+
+    oracle.build()
+    cfg = CFG
+    threads = os.cpu_count() or 1
+    units = cfg.B * cfg.Hkv
+    states = oracle_layer_sample(cfg, units)
+    for _ in range(args.warmup):
+        run_oracle_units(states, threads)
+    times = [run_oracle_units(states, threads) for _ in range(args.steps)]
+    total = sum(times)
+    value = args.steps / total  # layer-steps per second
+    b = algorithmic_bytes(cfg)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "layer-steps/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded; stands in for Llama-3.1-8B long-context decode)",
+            "config": {"workload": cfg.name, "layer_step": f"one layer of one decode step, {units} units",
+                       "global_batch": cfg.B, "seq_len": cfg.S, "top_k_pages": cfg.K, "page_tokens": cfg.T},
+            "kv_gbs": b["total"] * value / 1e9,
+            "cpu_baseline": {"kind": "oracle", "cores": threads, "value": value, "unit": "layer-steps/s",
+                             "sample": f"each step = all {units} units of one layer (C oracle, double "
+                                       f"precision) on {threads} threads"},
+            "e2e": {"value": value, "unit": "layer-steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------- #
+# GPU arm                                                                      #
+# --------------------------------------------------------------------------- #
+def make_timing_events(n):
+    try:
+        return [torch.cuda.Event(enable_timing=True, external=True) for _ in range(n)], True
+    except TypeError:
+        return [torch.cuda.Event(enable_timing=True) for _ in range(n)], False
+
+
+def gpu_arm(args):
+    from paged_kv_cache_minmax_gb300 import build as kbuild
+    from paged_kv_cache_minmax_gb300 import kvmm
+    from paged_kv_cache_minmax_gb300.runtime import DecodeState
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl")
+    kbuild.build_library()
+    kvmm.load()
+
+    cfg = CFG
+    L = cfg.L
+    # replicas: every rank decodes its own batch (seeded per rank); no collective on the data path
+    wl = workloads.generate(cfg, device="cuda", seed=cfg.seed + 7919 * rank)
+    splits = kvmm.auto_splits(kvmm.make_shape(cfg.B, L, cfg.Hq, cfg.Hkv, cfg.D, cfg.T, cfg.Pmax, cfg.K,
+                                              wl.n_phys))
+    st = DecodeState.for_workload(wl, num_splits=splits)
+    st.build_metadata()
+    nk, nv = workloads.step_tokens(wl, 0)
+    # the current token sits at position seq_len - 1 and is rewritten every step
+    st.tok_begin.copy_(wl.seq_len - 1)
+    q_dev = wl.q.clone()
+    nk_dev, nv_dev = nk.clone(), nv.clone()
+    stream = torch.cuda.Stream()
+
+    ev_s, external = make_timing_events(4 * L)
+
+    def step(instrument):
+        for l in range(L):
+            kvmm.kv_minmax_update(st.shape, l, nk_dev[l], nv_dev[l], 1, st.tok_begin, st.seq_len, st.k_pool,
+                                  st.v_pool, st.block_table, st.meta, st.err)
+            if instrument:
+                ev_s[4 * l].record()
+            st.select(l, q_dev[l])
+            if instrument:
+                ev_s[4 * l + 1].record()
+            st.diff(l)
+            if instrument:
+                ev_s[4 * l + 2].record()
+            st.attend(l, q_dev[l])
+            if instrument:
+                ev_s[4 * l + 3].record()
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            step(False)
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    graph_instr = torch.cuda.CUDAGraph() if external else None
+    with torch.cuda.graph(graph, stream=stream):
+        step(False)
+    if external:
+        with torch.cuda.graph(graph_instr, stream=stream):
+            step(True)
+    st.err.zero_()
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            graph.replay()
+    stream.synchronize()
+
+    # ---- timed region (device-resident inputs) --------------------------------
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local_rank, os.path.join(ROOT, "gpurun_out", "clocks.csv")
+                          if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else None)
+    with clocks:
+        time.sleep(0.3)
+        with torch.cuda.stream(stream):
+            t0.record()
+            for i in range(args.steps):
+                if external and i == args.steps - 1:
+                    graph_instr.replay()  # the last step also stamps every kernel launch
+                else:
+                    graph.replay()
+            t1.record()
+        stream.synchronize()
+    torch.cuda.synchronize()
+    ms_total = t0.elapsed_time(t1)
+    if dist:
+        tt = torch.tensor([ms_total], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_total = float(tt)
+    err_word = st.read_err()
+
+    if not external:  # eager instrumented step: per-launch durations on the launching stream
+        with torch.cuda.stream(stream):
+            step(True)
+        stream.synchronize()
+    score_ms = [ev_s[4 * l].elapsed_time(ev_s[4 * l + 1]) for l in range(L)]
+    attn_ms = [ev_s[4 * l + 2].elapsed_time(ev_s[4 * l + 3]) for l in range(L)]
+
+    # ---- end to end: host buffers in, host results out ------------------------
+    q_host = wl.q.cpu().pin_memory()
+    nk_host, nv_host = nk.cpu().pin_memory(), nv.cpu().pin_memory()
+    out_host = torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory()
+    lse_host = torch.empty(st.lse.shape, dtype=st.lse.dtype).pin_memory()
+    prom_host = torch.empty(st.promoted_cnt.shape, dtype=torch.int32).pin_memory()
+    h2d = q_host.numel() * 2 + nk_host.numel() * 2 * 2
+    d2h = out_host.numel() * 4 + lse_host.numel() * 4 + prom_host.numel() * 4
+    e2e_steps = max(3, min(args.steps, 200))
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record()
+        for _ in range(e2e_steps):
+            q_dev.copy_(q_host, non_blocking=True)
+            nk_dev.copy_(nk_host, non_blocking=True)
+            nv_dev.copy_(nv_host, non_blocking=True)
+            graph.replay()
+            out_host.copy_(st.out, non_blocking=True)
+            lse_host.copy_(st.lse, non_blocking=True)
+            prom_host.copy_(st.promoted_cnt, non_blocking=True)
+        e1.record()
+    stream.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if dist:
+        tt = torch.tensor([e2e_ms], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt)
+
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return
+
+    acc = algorithmic_bytes(cfg)
+    n_ls = args.steps * L * world
+    secs = ms_total / 1e3
+    value = n_ls / secs
+    kv_gbs = acc["total"] * n_ls / secs / 1e9
+    peak, peak_kind = peaks()
+    s_ms, a_ms = statistics.mean(score_ms), statistics.mean(attn_ms)
+    dom = "sparse_attn_kernel" if a_ms >= s_ms else "score_topk_kernel"
+    dom_ms = max(a_ms, s_ms)
+    dom_bytes = acc["attn_launch"] if a_ms >= s_ms else acc["score_launch"]
+    achieved = dom_bytes / (dom_ms / 1e3) / 1e9
+    traffic = load_traffic(dom)
+    clk = clocks.summary()
+    line = {
+        "metric": METRIC, "value": value, "unit": "layer-steps/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_total / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16 in, fp32 accumulate",
+        "data": "synthetic (seeded; stands in for Llama-3.1-8B long-context decode)",
+        "config": {"workload": cfg.name, "layers": L, "global_batch": cfg.B * world, "seq_len": cfg.S,
+                   "q_heads": cfg.Hq, "kv_heads": cfg.Hkv, "head_dim": cfg.D, "page_tokens": cfg.T,
+                   "top_k_pages": cfg.K, "splits": splits, "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (4 GiB of distinct data per step, no flush)",
+                   "step": "one decode step = 32 layer-steps, CUDA graph replay"},
+        "kv_gbs": kv_gbs, "pct_hbm_peak": kv_gbs / peak,
+        "bytes_per_layer_step": acc["total"],
+        "kernel_ms": {"score_topk_kernel": s_ms, "sparse_attn_kernel": a_ms,
+                      "per_layer_step_ms": ms_total / args.steps / L},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic, "kernel": dom,
+                     "peak_source": f"{peak_kind} hbm_gbs (burst copy)",
+                     "achieved_bytes_per_launch": dom_bytes, "launch_ms": dom_ms,
+                     "launch_timing": "CUDA events around each launch in the last timed step"
+                                      if external else "CUDA events, eager instrumented step after timing"},
+        "e2e": {"value": e2e_steps * L * world / (e2e_ms / 1e3), "unit": "layer-steps/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "how": "pinned host q/new K,V -> device, graph replay, out/lse/promoted counts -> pinned host"},
+        "gpu_launches": 4 * L * args.steps,
+        "clocks": clk,
+        "device_err": err_word,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(cfg)
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def load_traffic(kernel):
+    """dram bytes per launch of ``kernel`` from the committed ncu summary, if current."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    return d.get(kernel)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="kvmm", choices=["kvmm", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    if args.impl == "reference":
+        reference_arm(args)
+    else:
+        gpu_arm(args)
+
+
+if __name__ == "__main__":
+    main()

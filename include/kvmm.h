@@ -1,0 +1,239 @@
+/*
+ * kvmm.h -- C ABI of libkvmm: query-aware MinMax page selection and sparse
+ * paged GQA decode attention on NVIDIA GB300 (sm_103a).
+ *
+ * The method follows two pages:
+ *   FlexiCache: Leveraging Temporal Stability of Attention Heads for
+ *   Efficient KV Cache Management (MLSys'26; blog summary), sections
+ *   "Core method, 2. MinMax-metadata page scoring",
+ *   "Core method, 3. Periodic reranking and incremental promotion",
+ *   "Core method, 1. Stability-differentiated placement" (attention over the
+ *   top-K pages only) and "System design, head-level block table";
+ *   KVDrive: A Holistic Multi-Tier KV Cache Management System for
+ *   Long-Context LLM Inference, "Background and key observations" (Quest
+ *   scores a page by multiplying the query with the keys' channel-wise
+ *   minimum and maximum).
+ *
+ * Terms.  A unit is one (batch b, layer l, KV head h).  Each unit owns a
+ * sequence of logical pages of T tokens; page p holds tokens
+ * [p*T, (p+1)*T).  A head-level block table maps (b, l, h, p) to a physical
+ * page of the shared K and V pools; the entry KVMM_NULL_BLOCK (-1) marks a
+ * page that is not resident and is never dereferenced.  The G = Hq / Hkv
+ * query heads h*G .. h*G+G-1 share KV head h.
+ *
+ * Conventions for every call:
+ *   - All array pointers are DEVICE pointers owned by the caller.  The
+ *     library allocates nothing; scratch comes from a caller workspace.
+ *   - Arrays are dense, row-major, in the layouts given below; bf16 values
+ *     are raw 16-bit patterns (kvmm_bf16).  bf16 arrays and workspaces must
+ *     be 16-byte aligned, int32 and float arrays 4-byte aligned; a
+ *     violation returns KVMM_INVALID_ARG.
+ *   - Work is enqueued on the caller's stream and runs asynchronously.  The
+ *     return value only reports host-side argument checks and launch
+ *     errors: KVMM_OK means the work was enqueued.
+ *   - Faults found on the device never trap: they OR a KVMM_ERR_* bit into
+ *     the caller's device word *err (which the caller zeroes and reads after
+ *     synchronising) and the offending page or row is skipped.
+ *   - NaN or Inf inputs are not supported; they give undefined values but
+ *     no fault.
+ *   - Calls that share a workspace, or write the same outputs, must not
+ *     run concurrently (calls on one stream never do).
+ */
+#ifndef KVMM_H
+#define KVMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t kvmm_bf16;              /* raw bf16 bit pattern */
+typedef struct CUstream_st* kvmm_stream; /* a cudaStream_t; NULL = legacy default stream */
+
+typedef enum kvmm_status {
+    KVMM_OK = 0,
+    KVMM_INVALID_ARG = 1,        /* null/misaligned pointer, index out of range, bad flag */
+    KVMM_UNSUPPORTED_SHAPE = 2,  /* shape outside the supported set (see kvmm_shape) */
+    KVMM_WORKSPACE_TOO_SMALL = 3,
+    KVMM_CUDA_ERROR = 4          /* a CUDA runtime call or kernel launch failed */
+} kvmm_status;
+
+/* Bits OR-ed into the caller's device error word. */
+#define KVMM_ERR_NULL_BLOCK 1   /* a page that had to be read maps to the null block */
+#define KVMM_ERR_OUT_OF_RANGE 2 /* a table entry >= n_phys, a selected page >= the unit's page
+                                   count, a sequence longer than Pmax*T, or more rows than given */
+#define KVMM_ERR_TIMEOUT 4      /* a bounded wait on an in-flight copy gave up (never expected) */
+
+#define KVMM_NULL_BLOCK (-1)
+
+/* Shape shared by all calls.
+ *   B      batch size                      L     layers held in the arrays
+ *   Hq     query heads per layer           Hkv   KV heads per layer (Hq % Hkv == 0, G <= 8)
+ *   D      head dimension (64 or 128)      T     tokens per page (16 or 32)
+ *   Pmax   logical pages per unit held by the block table and the metadata
+ *          (1 <= Pmax <= 32768)
+ *   Kmax   capacity of a unit's selection list (1 <= Kmax <= 32768)
+ *   n_phys physical pages in each of the K and V pools                    */
+typedef struct kvmm_shape {
+    int32_t B, L, Hq, Hkv, D, T, Pmax, Kmax;
+    int64_t n_phys;
+} kvmm_shape;
+
+/* Array layouts (all row-major):
+ *   k_pool, v_pool   [n_phys][T][D]            bf16
+ *   block_table      [B][L][Hkv][Pmax]         int32, -1 = null block
+ *   meta             [B][L][Hkv][Pmax][2][D]   bf16, [..][0][d] = min, [..][1][d] = max
+ *   q                [B][Hq][D]                bf16 (the layer being decoded)
+ *   seq_len          [B]                       int32, tokens in the sequence (<= Pmax*T)
+ *   rescore_mask     [L][Hkv]                  uint8, nonzero = rescore this step
+ *   sel_idx          [B][L][Hkv][Kmax]         int32 logical pages, ascending
+ *   sel_cnt          [B][L][Hkv]               int32
+ *   out              [B][Hq][D]                float
+ *   lse              [B][Hq]                   float (natural log)                 */
+
+/* ------------------------------------------------------------------------
+ * kv_minmax_update -- append token rows to their pages and refresh the
+ * per-page, per-channel key MinMax metadata of every page they touch.
+ *
+ * FlexiCache, "Core method, 2. MinMax-metadata page scoring": each KV page
+ * keeps the per-channel minimum and maximum of its keys; the metadata lives
+ * apart from the K/V pages (so it stays on the GPU even when the page does
+ * not) and is indexed by logical page.
+ *
+ * For each batch b, with n = tok_end[b] - tok_begin[b] (0 <= n <= n_new):
+ *   - if new_k and new_v are given ([B][Hkv][n_new][D] bf16 each), token
+ *     tok_begin[b] + j of every KV head of `layer` takes row j of new_k /
+ *     new_v, written into its physical page through block_table;
+ *   - if both are NULL nothing is written (metadata rebuild only; n_new is
+ *     then only an upper bound on n and may be as large as Pmax*T);
+ *   - for every logical page p with [p*T, (p+1)*T) meeting
+ *     [tok_begin[b], tok_end[b]), meta[b][layer][h][p] is recomputed over the
+ *     page's tokens below tok_end[b] (tok_end[b] is the sequence length after
+ *     the update).  min/max compare by value with -0 below +0.
+ * Null or out-of-range table entries set their error bit and are skipped;
+ * n > n_new sets KVMM_ERR_OUT_OF_RANGE and clamps n.
+ */
+kvmm_status kv_minmax_update(const kvmm_shape* shape, int32_t layer, const kvmm_bf16* new_k,
+                             const kvmm_bf16* new_v, int32_t n_new, const int32_t* tok_begin,
+                             const int32_t* tok_end, kvmm_bf16* k_pool, kvmm_bf16* v_pool,
+                             const int32_t* block_table, kvmm_bf16* meta, int32_t* err,
+                             kvmm_stream stream);
+
+/* ------------------------------------------------------------------------
+ * page_score_topk -- score every page of every rescored unit of `layer`
+ * against the query and keep the K best pages.
+ *
+ * FlexiCache, "Core method, 2. MinMax-metadata page scoring" (estimate from
+ * the page's key bounds the largest dot product the query can reach and keep
+ * the top-K pages per (layer, KV head)); KVDrive, "Background and key
+ * observations" (Quest: query times channel-wise key min and max).
+ *
+ * For a unit with P = ceil(seq_len[b] / T) pages and query heads g of its
+ * group, page p scores
+ *     s_g(p) = sum_d max(q_g[d] * min_p[d], q_g[d] * max_p[d])
+ * (the largest q_g.k over the box [min_p, max_p]); the unit's score is
+ * sum_g s_g(p) when group_reduce = 0 (the default) or max_g s_g(p) when
+ * group_reduce = 1.  Scores are computed in fp32.  The min(K, P) highest
+ * scoring pages are written to sel_idx[b][layer][h][0..) in ascending page
+ * order, ties going to the lower page index, and sel_cnt to their count.
+ *
+ * rescore_mask (may be NULL = every unit) selects the units scored this
+ * step; the others keep sel_idx / sel_cnt untouched (FlexiCache, "Core
+ * method, 3": stable heads reuse their previous top-K between reranks).
+ * scores_out, if not NULL, is [B][Hkv][Pmax] float and receives the fp32
+ * scores of rescored units (pages >= P are not written).
+ * workspace must hold kvmm_workspace_size(shape, 0) bytes, be zero-filled
+ * before its first use, and not be modified by the caller between calls
+ * (every call leaves its counters at zero again).
+ * Requires 1 <= K <= Kmax; a sequence longer than Pmax*T sets
+ * KVMM_ERR_OUT_OF_RANGE and is scored over its first Pmax pages.
+ */
+kvmm_status page_score_topk(const kvmm_shape* shape, int32_t layer, const kvmm_bf16* q,
+                            const kvmm_bf16* meta, const int32_t* seq_len,
+                            const uint8_t* rescore_mask, int32_t K, int32_t group_reduce,
+                            int32_t* sel_idx, int32_t* sel_cnt, float* scores_out,
+                            void* workspace, size_t workspace_bytes, int32_t* err,
+                            kvmm_stream stream);
+
+/* ------------------------------------------------------------------------
+ * sparse_paged_decode_attn -- GQA decode attention of every query head of
+ * `layer` over the valid tokens of its KV head's selected pages only.
+ *
+ * FlexiCache, "Core method, 1. Stability-differentiated placement" (decode
+ * attention runs over the top-K pages even where the full KV is resident)
+ * and "System design, head-level block table" (pages are found through
+ * [batch, layer, head, logical_block]; null entries are never read).
+ *
+ * For query head g of KV head h in batch b, over the tokens t < seq_len[b]
+ * of the pages sel_idx[b][layer][h][0 .. sel_cnt):
+ *     z_t = sm_scale * (q_g . k_t)
+ *     out[b][g]  = sum_t exp(z_t - m) v_t / sum_t exp(z_t - m),  m = max_t z_t
+ *     lse[b][g]  = m + log(sum_t exp(z_t - m))
+ * accumulated in fp32.  sm_scale <= 0 means 1/sqrt(D).  A unit with no
+ * valid token yields out = 0 and lse = -inf.  The selection is split over
+ * num_splits CTAs per unit (0 = chosen from the GPU's SM count) and the
+ * partial results are merged by their log-sum-exp.  A selected page whose
+ * entry is null or out of range, or whose index is >= the unit's page
+ * count, sets its error bit and contributes nothing.  lse may be NULL.
+ * workspace as for page_score_topk, of kvmm_workspace_size(shape,
+ * num_splits) bytes.
+ */
+kvmm_status sparse_paged_decode_attn(const kvmm_shape* shape, int32_t layer, const kvmm_bf16* q,
+                                     const kvmm_bf16* k_pool, const kvmm_bf16* v_pool,
+                                     const int32_t* block_table, const int32_t* seq_len,
+                                     const int32_t* sel_idx, const int32_t* sel_cnt,
+                                     float sm_scale, int32_t num_splits, float* out, float* lse,
+                                     void* workspace, size_t workspace_bytes, int32_t* err,
+                                     kvmm_stream stream);
+
+/* ------------------------------------------------------------------------
+ * topk_promotion_diff -- after a rerank, list the pages that entered and
+ * left each rescored unit's top-K.
+ *
+ * FlexiCache, "Core method, 3. Periodic reranking and incremental
+ * promotion": only (current top-K minus previous top-K) is transferred; and
+ * "System design, head-level block table" (physical blocks of evicted pages
+ * are reused for promoted pages), which the evicted list serves.
+ *
+ * For every unit of `layer` with rescore_mask set (NULL = all):
+ *     promoted = cur \ prev,   evicted = prev \ cur
+ * both ascending, from the ascending lists prev_idx[0..prev_cnt) and
+ * cur_idx[0..cur_cnt) (layouts of sel_idx / sel_cnt).  Units not rescored
+ * get promoted_cnt = evicted_cnt = 0.  evicted / evicted_cnt may be NULL.
+ * total_promoted, if not NULL, is a single device int32 to which the call
+ * atomically adds the number of promoted pages.  With commit != 0, prev is
+ * then overwritten by cur for the rescored units, so prev always holds the
+ * last committed selection.  Lists that are not strictly ascending, or
+ * counts outside [0, Kmax], set KVMM_ERR_OUT_OF_RANGE and the unit's output
+ * counts are 0.
+ */
+kvmm_status topk_promotion_diff(const kvmm_shape* shape, int32_t layer,
+                                const uint8_t* rescore_mask, int32_t* prev_idx,
+                                int32_t* prev_cnt, const int32_t* cur_idx,
+                                const int32_t* cur_cnt, int32_t commit, int32_t* promoted,
+                                int32_t* promoted_cnt, int32_t* evicted, int32_t* evicted_cnt,
+                                int32_t* total_promoted, int32_t* err, kvmm_stream stream);
+
+/* Workspace bytes that page_score_topk and sparse_paged_decode_attn (with
+ * this num_splits; 0 = automatic) need; one workspace serves both calls as
+ * long as they do not run concurrently.  Returns 0 for an unsupported shape. */
+size_t kvmm_workspace_size(const kvmm_shape* shape, int32_t num_splits);
+
+/* Number of splits per unit that sparse_paged_decode_attn uses for
+ * num_splits = 0 on the current device (0 for an unsupported shape). */
+int32_t kvmm_auto_splits(const kvmm_shape* shape);
+
+/* Static text for a status code. */
+const char* kvmm_status_string(kvmm_status status);
+
+/* Text of the CUDA error behind the calling thread's last KVMM_CUDA_ERROR
+ * ("no CUDA error" if there was none). */
+const char* kvmm_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVMM_H */

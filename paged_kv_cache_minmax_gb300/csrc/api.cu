@@ -1,0 +1,280 @@
+// api.cu -- the extern "C" entry points declared in include/kvmm.h.
+//
+// Host side only: synchronous argument checks, workspace carving and kernel
+// launches on the caller's stream.  No allocation, no synchronisation.
+#include <cmath>
+
+#include "kernels.h"
+
+namespace {
+
+using kvmm::AttnParams;
+using kvmm::DiffParams;
+using kvmm::ScoreParams;
+using kvmm::UpdateParams;
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// bf16 arrays and the workspace: present and 16-byte aligned (vector loads, bulk copies)
+bool req(const void* p) { return p != nullptr && aligned(p, 16); }
+bool opt(const void* p) { return p == nullptr || aligned(p, 16); }
+// int32 / float arrays: present (or NULL) and 4-byte aligned
+bool req4(const void* p) { return p != nullptr && aligned(p, 4); }
+bool opt4(const void* p) { return p == nullptr || aligned(p, 4); }
+
+kvmm_status check_shape(const kvmm_shape* s)
+{
+    if (s == nullptr) return KVMM_INVALID_ARG;
+    if (s->B < 1 || s->L < 1 || s->Hq < 1 || s->Hkv < 1 || s->Pmax < 1 || s->Kmax < 1 || s->n_phys < 1)
+        return KVMM_INVALID_ARG;
+    if (s->Hq % s->Hkv != 0) return KVMM_INVALID_ARG;
+    const int G = s->Hq / s->Hkv;
+    if (G > 8) return KVMM_UNSUPPORTED_SHAPE;
+    if (s->D != 64 && s->D != 128) return KVMM_UNSUPPORTED_SHAPE;
+    if (s->T != 16 && s->T != 32) return KVMM_UNSUPPORTED_SHAPE;
+    if (s->Pmax > 32768 || s->Kmax > 32768) return KVMM_UNSUPPORTED_SHAPE;
+    if (s->B > 65535 || s->Hkv > 65535) return KVMM_UNSUPPORTED_SHAPE;  // grid y/z limits
+    // every element index of the pools, tables and metadata fits in int64 and row ids in int64
+    if (s->n_phys > (int64_t(1) << 40)) return KVMM_UNSUPPORTED_SHAPE;
+    return KVMM_OK;
+}
+
+int resolve_splits(const kvmm_shape& s, int32_t num_splits)
+{
+    const int tiles = s.Kmax * (s.T / 16);
+    int splits = num_splits > 0 ? num_splits : kvmm::attention_slots_per_unit(s);
+    if (splits > tiles) splits = tiles;
+    if (splits < 1) splits = 1;
+    return splits;
+}
+
+size_t attention_ws_bytes(const kvmm_shape& s, int splits)
+{
+    const size_t units = size_t(s.B) * s.Hkv;
+    const int G = s.Hq / s.Hkv;
+    const size_t po = units * splits * G * s.D * sizeof(float);
+    const size_t pml = units * splits * G * 2 * sizeof(float);
+    return kvmm::ws_counter_bytes(s) + ((po + 255) & ~size_t(255)) + pml;
+}
+
+size_t score_ws_bytes(const kvmm_shape& s)
+{
+    return kvmm::ws_counter_bytes(s) + size_t(s.B) * s.Hkv * s.Pmax * sizeof(float);
+}
+
+thread_local cudaError_t g_last_cuda_error = cudaSuccess;
+
+kvmm_status launched(cudaError_t e)
+{
+    if (e == cudaSuccess) return KVMM_OK;
+    g_last_cuda_error = e;
+    return KVMM_CUDA_ERROR;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* kvmm_status_string(kvmm_status status)
+{
+    switch (status) {
+    case KVMM_OK: return "ok";
+    case KVMM_INVALID_ARG: return "invalid argument (null or misaligned pointer, index or flag out of range)";
+    case KVMM_UNSUPPORTED_SHAPE: return "unsupported shape (D in {64,128}, T in {16,32}, G <= 8, Pmax and Kmax <= 32768)";
+    case KVMM_WORKSPACE_TOO_SMALL: return "workspace too small (see kvmm_workspace_size)";
+    case KVMM_CUDA_ERROR: return "CUDA runtime or launch error";
+    }
+    return "unknown status";
+}
+
+const char* kvmm_last_cuda_error(void)
+{
+    return g_last_cuda_error == cudaSuccess ? "no CUDA error" : cudaGetErrorString(g_last_cuda_error);
+}
+
+int32_t kvmm_auto_splits(const kvmm_shape* shape)
+{
+    if (check_shape(shape) != KVMM_OK) return 0;
+    return resolve_splits(*shape, 0);
+}
+
+size_t kvmm_workspace_size(const kvmm_shape* shape, int32_t num_splits)
+{
+    if (check_shape(shape) != KVMM_OK || num_splits < 0) return 0;
+    const size_t a = attention_ws_bytes(*shape, resolve_splits(*shape, num_splits));
+    const size_t b = score_ws_bytes(*shape);
+    return a > b ? a : b;
+}
+
+kvmm_status kv_minmax_update(const kvmm_shape* shape, int32_t layer, const kvmm_bf16* new_k,
+                             const kvmm_bf16* new_v, int32_t n_new, const int32_t* tok_begin,
+                             const int32_t* tok_end, kvmm_bf16* k_pool, kvmm_bf16* v_pool,
+                             const int32_t* block_table, kvmm_bf16* meta, int32_t* err,
+                             kvmm_stream stream)
+{
+    kvmm_status st = check_shape(shape);
+    if (st != KVMM_OK) return st;
+    const kvmm_shape& s = *shape;
+    if (layer < 0 || layer >= s.L) return KVMM_INVALID_ARG;
+    if ((new_k == nullptr) != (new_v == nullptr)) return KVMM_INVALID_ARG;
+    if (!opt(new_k) || !opt(new_v) || !req4(tok_begin) || !req4(tok_end) || !req(k_pool) ||
+        !req4(block_table) || !req(meta) || !opt4(err))
+        return KVMM_INVALID_ARG;
+    if (new_k != nullptr && (n_new < 1 || !req(v_pool))) return KVMM_INVALID_ARG;
+    if (n_new < 0) return KVMM_INVALID_ARG;
+    UpdateParams p{};
+    p.B = s.B;
+    p.L = s.L;
+    p.Hkv = s.Hkv;
+    p.D = s.D;
+    p.T = s.T;
+    p.Pmax = s.Pmax;
+    p.layer = layer;
+    p.n_new = n_new;
+    p.n_phys = s.n_phys;
+    p.new_k = new_k;
+    p.new_v = new_v;
+    p.tok_begin = tok_begin;
+    p.tok_end = tok_end;
+    p.k_pool = k_pool;
+    p.v_pool = v_pool;
+    p.block_table = block_table;
+    p.meta = meta;
+    p.err = err;
+    return launched(kvmm::launch_minmax_update(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+kvmm_status page_score_topk(const kvmm_shape* shape, int32_t layer, const kvmm_bf16* q,
+                            const kvmm_bf16* meta, const int32_t* seq_len,
+                            const uint8_t* rescore_mask, int32_t K, int32_t group_reduce,
+                            int32_t* sel_idx, int32_t* sel_cnt, float* scores_out,
+                            void* workspace, size_t workspace_bytes, int32_t* err,
+                            kvmm_stream stream)
+{
+    kvmm_status st = check_shape(shape);
+    if (st != KVMM_OK) return st;
+    const kvmm_shape& s = *shape;
+    if (layer < 0 || layer >= s.L || K < 1 || K > s.Kmax) return KVMM_INVALID_ARG;
+    if (group_reduce != 0 && group_reduce != 1) return KVMM_INVALID_ARG;
+    if (!req(q) || !req(meta) || !req4(seq_len) || !req4(sel_idx) || !req4(sel_cnt) || !opt4(scores_out) ||
+        !req(workspace) || !opt4(err))
+        return KVMM_INVALID_ARG;
+    if (workspace_bytes < score_ws_bytes(s)) return KVMM_WORKSPACE_TOO_SMALL;
+    ScoreParams p{};
+    p.B = s.B;
+    p.L = s.L;
+    p.Hq = s.Hq;
+    p.Hkv = s.Hkv;
+    p.G = s.Hq / s.Hkv;
+    p.D = s.D;
+    p.T = s.T;
+    p.Pmax = s.Pmax;
+    p.Kmax = s.Kmax;
+    p.layer = layer;
+    p.K = K;
+    p.q = q;
+    p.meta = meta;
+    p.seq_len = seq_len;
+    p.rescore_mask = rescore_mask;
+    p.sel_idx = sel_idx;
+    p.sel_cnt = sel_cnt;
+    p.scores_out = scores_out;
+    p.counters = static_cast<int32_t*>(workspace);
+    p.scores_ws = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + kvmm::ws_counter_bytes(s));
+    p.err = err;
+    return launched(kvmm::launch_score_topk(p, group_reduce, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+kvmm_status sparse_paged_decode_attn(const kvmm_shape* shape, int32_t layer, const kvmm_bf16* q,
+                                     const kvmm_bf16* k_pool, const kvmm_bf16* v_pool,
+                                     const int32_t* block_table, const int32_t* seq_len,
+                                     const int32_t* sel_idx, const int32_t* sel_cnt,
+                                     float sm_scale, int32_t num_splits, float* out, float* lse,
+                                     void* workspace, size_t workspace_bytes, int32_t* err,
+                                     kvmm_stream stream)
+{
+    kvmm_status st = check_shape(shape);
+    if (st != KVMM_OK) return st;
+    const kvmm_shape& s = *shape;
+    if (layer < 0 || layer >= s.L || num_splits < 0 || !std::isfinite(sm_scale)) return KVMM_INVALID_ARG;
+    if (!req(q) || !req(k_pool) || !req(v_pool) || !req4(block_table) || !req4(seq_len) || !req4(sel_idx) ||
+        !req4(sel_cnt) || !req4(out) || !opt4(lse) || !opt4(err))
+        return KVMM_INVALID_ARG;
+    const int splits = resolve_splits(s, num_splits);
+    if (splits > 1 && !req(workspace)) return KVMM_INVALID_ARG;
+    if (splits > 1 && workspace_bytes < attention_ws_bytes(s, splits)) return KVMM_WORKSPACE_TOO_SMALL;
+    const int tiles = s.Kmax * (s.T / 16);
+    const int max_tiles = (tiles + splits - 1) / splits;
+    if (kvmm::attention_smem_bytes(s.D, max_tiles) > 227 * 1024) return KVMM_UNSUPPORTED_SHAPE;
+    AttnParams p{};
+    p.B = s.B;
+    p.L = s.L;
+    p.Hq = s.Hq;
+    p.Hkv = s.Hkv;
+    p.G = s.Hq / s.Hkv;
+    p.D = s.D;
+    p.T = s.T;
+    p.Pmax = s.Pmax;
+    p.Kmax = s.Kmax;
+    p.layer = layer;
+    p.splits = splits;
+    p.max_tiles = max_tiles;
+    p.n_phys = s.n_phys;
+    p.scale_log2 = (sm_scale > 0.f ? sm_scale : 1.0f / std::sqrt(static_cast<float>(s.D))) * 1.4426950408889634f;
+    p.q = q;
+    p.k_pool = k_pool;
+    p.v_pool = v_pool;
+    p.block_table = block_table;
+    p.seq_len = seq_len;
+    p.sel_idx = sel_idx;
+    p.sel_cnt = sel_cnt;
+    p.out = out;
+    p.lse = lse;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    p.counters = reinterpret_cast<int32_t*>(ws);
+    if (splits > 1) {
+        const size_t units = size_t(s.B) * s.Hkv;
+        const size_t po = units * splits * p.G * s.D * sizeof(float);
+        p.part_o = reinterpret_cast<float*>(ws + kvmm::ws_counter_bytes(s));
+        p.part_ml = reinterpret_cast<float*>(ws + kvmm::ws_counter_bytes(s) + ((po + 255) & ~size_t(255)));
+    }
+    p.err = err;
+    return launched(kvmm::launch_sparse_attention(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+kvmm_status topk_promotion_diff(const kvmm_shape* shape, int32_t layer,
+                                const uint8_t* rescore_mask, int32_t* prev_idx,
+                                int32_t* prev_cnt, const int32_t* cur_idx,
+                                const int32_t* cur_cnt, int32_t commit, int32_t* promoted,
+                                int32_t* promoted_cnt, int32_t* evicted, int32_t* evicted_cnt,
+                                int32_t* total_promoted, int32_t* err, kvmm_stream stream)
+{
+    kvmm_status st = check_shape(shape);
+    if (st != KVMM_OK) return st;
+    const kvmm_shape& s = *shape;
+    if (layer < 0 || layer >= s.L) return KVMM_INVALID_ARG;
+    if (!req4(prev_idx) || !req4(prev_cnt) || !req4(cur_idx) || !req4(cur_cnt) || !req4(promoted) ||
+        !req4(promoted_cnt) || !opt4(evicted) || !opt4(evicted_cnt) || !opt4(total_promoted) || !opt4(err))
+        return KVMM_INVALID_ARG;
+    DiffParams p{};
+    p.B = s.B;
+    p.L = s.L;
+    p.Hkv = s.Hkv;
+    p.Kmax = s.Kmax;
+    p.layer = layer;
+    p.commit = commit != 0;
+    p.rescore_mask = rescore_mask;
+    p.prev_idx = prev_idx;
+    p.prev_cnt = prev_cnt;
+    p.cur_idx = cur_idx;
+    p.cur_cnt = cur_cnt;
+    p.promoted = promoted;
+    p.promoted_cnt = promoted_cnt;
+    p.evicted = evicted;
+    p.evicted_cnt = evicted_cnt;
+    p.total_promoted = total_promoted;
+    p.err = err;
+    return launched(kvmm::launch_promotion_diff(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

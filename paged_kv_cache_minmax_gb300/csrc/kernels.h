@@ -1,0 +1,97 @@
+// kernels.h -- internal launch interface between the C-ABI layer (api.cu)
+// and the kernel translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "kvmm.h"
+
+namespace kvmm {
+
+// Workspace layout shared by page_score_topk and sparse_paged_decode_attn:
+// one int32 counter per (b, kv_head) of the layer, then the call's data.
+// Both kernels leave every counter at zero when they finish.
+inline size_t ws_counter_bytes(const kvmm_shape& s)
+{
+    size_t n = static_cast<size_t>(s.B) * s.Hkv * sizeof(int32_t);
+    return (n + 255) & ~static_cast<size_t>(255);
+}
+
+struct UpdateParams {
+    int32_t B, L, Hkv, D, T, Pmax, layer, n_new;
+    int64_t n_phys;
+    const kvmm_bf16* new_k;
+    const kvmm_bf16* new_v;
+    const int32_t* tok_begin;
+    const int32_t* tok_end;
+    kvmm_bf16* k_pool;
+    kvmm_bf16* v_pool;
+    const int32_t* block_table;
+    kvmm_bf16* meta;
+    int32_t* err;
+};
+
+struct ScoreParams {
+    int32_t B, L, Hq, Hkv, G, D, T, Pmax, Kmax, layer, K;
+    const kvmm_bf16* q;
+    const kvmm_bf16* meta;
+    const int32_t* seq_len;
+    const uint8_t* rescore_mask;
+    int32_t* sel_idx;
+    int32_t* sel_cnt;
+    float* scores_out;
+    int32_t* counters;  // workspace: [B*Hkv]
+    float* scores_ws;   // workspace: [B*Hkv][Pmax]
+    int32_t* err;
+};
+
+struct AttnParams {
+    int32_t B, L, Hq, Hkv, G, D, T, Pmax, Kmax, layer;
+    int32_t splits;      // CTAs per unit
+    int32_t max_tiles;   // upper bound of 16-token tiles handled by one CTA
+    int64_t n_phys;
+    float scale_log2;    // sm_scale * log2(e)
+    const kvmm_bf16* q;
+    const kvmm_bf16* k_pool;
+    const kvmm_bf16* v_pool;
+    const int32_t* block_table;
+    const int32_t* seq_len;
+    const int32_t* sel_idx;
+    const int32_t* sel_cnt;
+    float* out;
+    float* lse;
+    int32_t* counters;   // workspace: [B*Hkv]
+    float* part_o;       // workspace: [B*Hkv][splits][G][D]
+    float* part_ml;      // workspace: [B*Hkv][splits][G][2]
+    int32_t* err;
+};
+
+struct DiffParams {
+    int32_t B, L, Hkv, Kmax, layer, commit;
+    const uint8_t* rescore_mask;
+    int32_t* prev_idx;
+    int32_t* prev_cnt;
+    const int32_t* cur_idx;
+    const int32_t* cur_cnt;
+    int32_t* promoted;
+    int32_t* promoted_cnt;
+    int32_t* evicted;
+    int32_t* evicted_cnt;
+    int32_t* total_promoted;
+    int32_t* err;
+};
+
+// Launchers return cudaSuccess or the launch error.
+cudaError_t launch_minmax_update(const UpdateParams& p, cudaStream_t stream);
+cudaError_t launch_score_topk(const ScoreParams& p, int group_reduce, cudaStream_t stream);
+cudaError_t launch_sparse_attention(const AttnParams& p, cudaStream_t stream);
+cudaError_t launch_promotion_diff(const DiffParams& p, cudaStream_t stream);
+
+// Attention launch geometry for the current device.
+int attention_slots_per_unit(const kvmm_shape& s);  // automatic split count
+size_t attention_smem_bytes(int D, int max_tiles);
+
+}  // namespace kvmm

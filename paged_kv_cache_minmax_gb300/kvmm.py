@@ -1,0 +1,204 @@
+"""Thin Python binding of ``libkvmm.so`` (the C ABI declared in ``include/kvmm.h``).
+
+Argument marshalling only: every function checks the tensors it is given
+(device, dtype, contiguity, element count), turns them into raw device
+pointers and calls the C entry point of the same name on the current (or
+given) CUDA stream.  All computation happens in the library's kernels; there
+is no fallback, and a missing library raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+OK, INVALID_ARG, UNSUPPORTED_SHAPE, WORKSPACE_TOO_SMALL, CUDA_ERROR = range(5)
+ERR_NULL_BLOCK, ERR_OUT_OF_RANGE, ERR_TIMEOUT = 1, 2, 4
+NULL_BLOCK = -1
+
+EXPORTS = ("kv_minmax_update", "page_score_topk", "sparse_paged_decode_attn", "topk_promotion_diff",
+           "kvmm_workspace_size", "kvmm_auto_splits", "kvmm_status_string", "kvmm_last_cuda_error")
+
+
+class KvmmError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        msg = f"{fn}: {status_string(status)} (status {status})"
+        if status == CUDA_ERROR:
+            msg += f": {load().kvmm_last_cuda_error().decode()}"
+        super().__init__(msg)
+        self.status = status
+
+
+class Shape(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("L", ctypes.c_int32), ("Hq", ctypes.c_int32), ("Hkv", ctypes.c_int32),
+                ("D", ctypes.c_int32), ("T", ctypes.c_int32), ("Pmax", ctypes.c_int32), ("Kmax", ctypes.c_int32),
+                ("n_phys", ctypes.c_int64)]
+
+    @property
+    def G(self) -> int:
+        return self.Hq // self.Hkv
+
+    def __repr__(self) -> str:
+        return ("Shape(" + ", ".join(f"{n}={getattr(self, n)}" for n, _ in self._fields_) + ")")
+
+
+def make_shape(B, L, Hq, Hkv, D, T, Pmax, Kmax, n_phys) -> Shape:
+    return Shape(B, L, Hq, Hkv, D, T, Pmax, Kmax, n_phys)
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Load ``libkvmm.so`` (built by ``paged_kv_cache_minmax_gb300.build``); raises if absent."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    path = path or library_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"kvmm CUDA library not found at {path}: build it first "
+                           "(python -m paged_kv_cache_minmax_gb300.build)")
+    lib = ctypes.CDLL(path)
+    P, I32, F32, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float, ctypes.c_size_t
+    SP = ctypes.POINTER(Shape)
+    lib.kv_minmax_update.argtypes = [SP, I32, P, P, I32, P, P, P, P, P, P, P, P]
+    lib.page_score_topk.argtypes = [SP, I32, P, P, P, P, I32, I32, P, P, P, P, SZ, P, P]
+    lib.sparse_paged_decode_attn.argtypes = [SP, I32, P, P, P, P, P, P, P, F32, I32, P, P, P, SZ, P, P]
+    lib.topk_promotion_diff.argtypes = [SP, I32, P, P, P, P, P, I32, P, P, P, P, P, P, P]
+    for f in ("kv_minmax_update", "page_score_topk", "sparse_paged_decode_attn", "topk_promotion_diff"):
+        getattr(lib, f).restype = ctypes.c_int
+    lib.kvmm_workspace_size.argtypes = [SP, I32]
+    lib.kvmm_workspace_size.restype = SZ
+    lib.kvmm_auto_splits.argtypes = [SP]
+    lib.kvmm_auto_splits.restype = I32
+    lib.kvmm_status_string.argtypes = [ctypes.c_int]
+    lib.kvmm_status_string.restype = ctypes.c_char_p
+    lib.kvmm_last_cuda_error.argtypes = []
+    lib.kvmm_last_cuda_error.restype = ctypes.c_char_p
+    if path == library_path():
+        _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load().kvmm_status_string(status).decode()
+
+
+def _check(fn: str, status: int) -> None:
+    if status != OK:
+        raise KvmmError(fn, status)
+
+
+def _dev(t: torch.Tensor | None, name: str, dtype: torch.dtype, numel: int | None = None, optional=False):
+    if t is None:
+        if optional:
+            return None
+        raise ValueError(f"{name} is required")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if numel is not None and t.numel() < numel:
+        raise ValueError(f"{name} has {t.numel()} elements, needs {numel}")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+# --------------------------------------------------------------------------- #
+def workspace_size(shape: Shape, num_splits: int = 0) -> int:
+    return int(load().kvmm_workspace_size(ctypes.byref(shape), num_splits))
+
+
+def auto_splits(shape: Shape) -> int:
+    return int(load().kvmm_auto_splits(ctypes.byref(shape)))
+
+
+def alloc_workspace(shape: Shape, num_splits: int = 0, device="cuda") -> torch.Tensor:
+    """A zero-filled workspace (uint8) of ``workspace_size`` bytes, rounded to 16."""
+    n = workspace_size(shape, num_splits)
+    if n == 0:
+        raise KvmmError("kvmm_workspace_size", UNSUPPORTED_SHAPE)
+    return torch.zeros((n + 15) // 16 * 16, dtype=torch.uint8, device=device)
+
+
+def kv_minmax_update(shape: Shape, layer: int, new_k, new_v, n_new: int, tok_begin, tok_end, k_pool, v_pool,
+                     block_table, meta, err=None, stream=None) -> None:
+    s = shape
+    if (new_k is None) != (new_v is None):
+        raise ValueError("new_k and new_v are given together or not at all")
+    rows = s.B * s.Hkv * n_new * s.D
+    args = (ctypes.byref(s), layer,
+            _dev(new_k, "new_k", torch.bfloat16, rows, optional=True),
+            _dev(new_v, "new_v", torch.bfloat16, rows, optional=True), n_new,
+            _dev(tok_begin, "tok_begin", torch.int32, s.B), _dev(tok_end, "tok_end", torch.int32, s.B),
+            _dev(k_pool, "k_pool", torch.bfloat16, s.n_phys * s.T * s.D),
+            _dev(v_pool, "v_pool", torch.bfloat16, s.n_phys * s.T * s.D),
+            _dev(block_table, "block_table", torch.int32, s.B * s.L * s.Hkv * s.Pmax),
+            _dev(meta, "meta", torch.bfloat16, s.B * s.L * s.Hkv * s.Pmax * 2 * s.D),
+            _dev(err, "err", torch.int32, 1, optional=True), _stream(stream))
+    _check("kv_minmax_update", load().kv_minmax_update(*args))
+
+
+def page_score_topk(shape: Shape, layer: int, q, meta, seq_len, rescore_mask, K: int, sel_idx, sel_cnt,
+                    workspace, err=None, scores_out=None, group_reduce: int = 0, stream=None) -> None:
+    s = shape
+    units = s.B * s.L * s.Hkv
+    args = (ctypes.byref(s), layer, _dev(q, "q", torch.bfloat16, s.B * s.Hq * s.D),
+            _dev(meta, "meta", torch.bfloat16, units * s.Pmax * 2 * s.D),
+            _dev(seq_len, "seq_len", torch.int32, s.B),
+            _dev(rescore_mask, "rescore_mask", torch.uint8, s.L * s.Hkv, optional=True), K, group_reduce,
+            _dev(sel_idx, "sel_idx", torch.int32, units * s.Kmax), _dev(sel_cnt, "sel_cnt", torch.int32, units),
+            _dev(scores_out, "scores_out", torch.float32, s.B * s.Hkv * s.Pmax, optional=True),
+            _dev(workspace, "workspace", torch.uint8), workspace.numel(),
+            _dev(err, "err", torch.int32, 1, optional=True), _stream(stream))
+    _check("page_score_topk", load().page_score_topk(*args))
+
+
+def sparse_paged_decode_attn(shape: Shape, layer: int, q, k_pool, v_pool, block_table, seq_len, sel_idx, sel_cnt,
+                             out, workspace, lse=None, err=None, sm_scale: float = 0.0, num_splits: int = 0,
+                             stream=None) -> None:
+    s = shape
+    units = s.B * s.L * s.Hkv
+    args = (ctypes.byref(s), layer, _dev(q, "q", torch.bfloat16, s.B * s.Hq * s.D),
+            _dev(k_pool, "k_pool", torch.bfloat16, s.n_phys * s.T * s.D),
+            _dev(v_pool, "v_pool", torch.bfloat16, s.n_phys * s.T * s.D),
+            _dev(block_table, "block_table", torch.int32, units * s.Pmax),
+            _dev(seq_len, "seq_len", torch.int32, s.B),
+            _dev(sel_idx, "sel_idx", torch.int32, units * s.Kmax), _dev(sel_cnt, "sel_cnt", torch.int32, units),
+            float(sm_scale), num_splits, _dev(out, "out", torch.float32, s.B * s.Hq * s.D),
+            _dev(lse, "lse", torch.float32, s.B * s.Hq, optional=True),
+            _dev(workspace, "workspace", torch.uint8, optional=True),
+            0 if workspace is None else workspace.numel(),
+            _dev(err, "err", torch.int32, 1, optional=True), _stream(stream))
+    _check("sparse_paged_decode_attn", load().sparse_paged_decode_attn(*args))
+
+
+def topk_promotion_diff(shape: Shape, layer: int, rescore_mask, prev_idx, prev_cnt, cur_idx, cur_cnt, promoted,
+                        promoted_cnt, evicted=None, evicted_cnt=None, total_promoted=None, commit: bool = True,
+                        err=None, stream=None) -> None:
+    s = shape
+    units = s.B * s.L * s.Hkv
+    args = (ctypes.byref(s), layer,
+            _dev(rescore_mask, "rescore_mask", torch.uint8, s.L * s.Hkv, optional=True),
+            _dev(prev_idx, "prev_idx", torch.int32, units * s.Kmax), _dev(prev_cnt, "prev_cnt", torch.int32, units),
+            _dev(cur_idx, "cur_idx", torch.int32, units * s.Kmax), _dev(cur_cnt, "cur_cnt", torch.int32, units),
+            int(bool(commit)), _dev(promoted, "promoted", torch.int32, units * s.Kmax),
+            _dev(promoted_cnt, "promoted_cnt", torch.int32, units),
+            _dev(evicted, "evicted", torch.int32, units * s.Kmax, optional=True),
+            _dev(evicted_cnt, "evicted_cnt", torch.int32, units, optional=True),
+            _dev(total_promoted, "total_promoted", torch.int32, 1, optional=True),
+            _dev(err, "err", torch.int32, 1, optional=True), _stream(stream))
+    _check("topk_promotion_diff", load().topk_promotion_diff(*args))

@@ -1,0 +1,98 @@
+"""Decode-step driver over the four C-ABI calls.
+
+:class:`DecodeState` owns the device buffers one long-context decode needs
+beside the caller's pools (MinMax metadata, selections, the committed previous
+selections, promotion lists, outputs, workspace, error word) and issues, per
+layer and step, the calls in the method's order:
+
+  1. ``kv_minmax_update``          append the new token, refresh its page's MinMax
+  2. ``page_score_topk``           rescored units only (stable heads keep their top-K)
+  3. ``topk_promotion_diff``       promoted = cur \\ prev (commit cur as prev)
+  4. ``sparse_paged_decode_attn``  attention over the selected pages
+
+(FlexiCache, "Core method", sections 1-3.)  Everything runs on one CUDA
+stream; nothing here synchronises.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import kvmm
+
+
+class DecodeState:
+    def __init__(self, B, L, Hq, Hkv, D, T, Pmax, K, k_pool, v_pool, block_table, seq_len, num_splits=0,
+                 group_reduce=0, device="cuda"):
+        self.shape = kvmm.make_shape(B, L, Hq, Hkv, D, T, Pmax, K, k_pool.shape[0])
+        self.K = K
+        self.num_splits = num_splits
+        self.group_reduce = group_reduce
+        self.k_pool, self.v_pool, self.block_table, self.seq_len = k_pool, v_pool, block_table, seq_len
+        i32 = dict(dtype=torch.int32, device=device)
+        self.meta = torch.zeros(B, L, Hkv, Pmax, 2, D, dtype=torch.bfloat16, device=device)
+        self.sel_idx = torch.zeros(B, L, Hkv, K, **i32)
+        self.sel_cnt = torch.zeros(B, L, Hkv, **i32)
+        self.prev_idx = torch.zeros(B, L, Hkv, K, **i32)
+        self.prev_cnt = torch.zeros(B, L, Hkv, **i32)
+        self.promoted = torch.zeros(B, L, Hkv, K, **i32)
+        self.promoted_cnt = torch.zeros(B, L, Hkv, **i32)
+        self.evicted = torch.zeros(B, L, Hkv, K, **i32)
+        self.evicted_cnt = torch.zeros(B, L, Hkv, **i32)
+        self.total_promoted = torch.zeros(1, **i32)
+        self.out = torch.zeros(L, B, Hq, D, dtype=torch.float32, device=device)
+        self.lse = torch.zeros(L, B, Hq, dtype=torch.float32, device=device)
+        self.err = torch.zeros(1, **i32)
+        self.tok_begin = torch.zeros(B, **i32)
+        self.tok_end = torch.zeros(B, **i32)
+        self.workspace = kvmm.alloc_workspace(self.shape, num_splits, device=device)
+
+    @classmethod
+    def for_workload(cls, wl, K=None, **kw):
+        c = wl.cfg
+        return cls(c.B, c.L_alloc, c.Hq, c.Hkv, c.D, c.T, c.Pmax, K or c.K, wl.k_pool, wl.v_pool,
+                   wl.block_table, wl.seq_len, **kw)
+
+    # ------------------------------------------------------------------ #
+    def build_metadata(self, layers=None) -> None:
+        """Rebuild the MinMax of every page below seq_len (after a prefill)."""
+        s = self.shape
+        self.tok_begin.zero_()
+        for l in (range(s.L) if layers is None else layers):
+            kvmm.kv_minmax_update(s, l, None, None, 0, self.tok_begin, self.seq_len, self.k_pool, self.v_pool,
+                                  self.block_table, self.meta, self.err)
+
+    def append(self, layer, new_k, new_v) -> None:
+        """Write one new token per batch entry at position seq_len-1 of ``layer``.
+
+        new_k / new_v: ``[B, Hkv, 1, D]`` bf16; ``seq_len`` already counts the token.
+        """
+        torch.sub(self.seq_len, 1, out=self.tok_begin)
+        kvmm.kv_minmax_update(self.shape, layer, new_k, new_v, 1, self.tok_begin, self.seq_len, self.k_pool,
+                              self.v_pool, self.block_table, self.meta, self.err)
+
+    def select(self, layer, q, rescore_mask=None, scores_out=None) -> None:
+        kvmm.page_score_topk(self.shape, layer, q, self.meta, self.seq_len, rescore_mask, self.K, self.sel_idx,
+                             self.sel_cnt, self.workspace, self.err, scores_out=scores_out,
+                             group_reduce=self.group_reduce)
+
+    def diff(self, layer, rescore_mask=None, commit=True) -> None:
+        kvmm.topk_promotion_diff(self.shape, layer, rescore_mask, self.prev_idx, self.prev_cnt, self.sel_idx,
+                                 self.sel_cnt, self.promoted, self.promoted_cnt, self.evicted, self.evicted_cnt,
+                                 self.total_promoted, commit=commit, err=self.err)
+
+    def attend(self, layer, q, sm_scale=0.0) -> None:
+        kvmm.sparse_paged_decode_attn(self.shape, layer, q, self.k_pool, self.v_pool, self.block_table,
+                                      self.seq_len, self.sel_idx, self.sel_cnt, self.out[layer], self.workspace,
+                                      lse=self.lse[layer], err=self.err, sm_scale=sm_scale,
+                                      num_splits=self.num_splits)
+
+    def layer_step(self, layer, q, new_k=None, new_v=None, rescore_mask=None) -> None:
+        """One layer of one decode step: append, select, diff, attend."""
+        if new_k is not None:
+            self.append(layer, new_k, new_v)
+        self.select(layer, q, rescore_mask)
+        self.diff(layer, rescore_mask)
+        self.attend(layer, q)
+
+    def read_err(self) -> int:
+        return int(self.err.item())
