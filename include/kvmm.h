@@ -158,6 +158,34 @@ kvmm_status page_score_topk(const kvmm_shape* shape, int32_t layer, const kvmm_b
                             kvmm_stream stream);
 
 /* ------------------------------------------------------------------------
+ * page_score_topk_static_scratch -- page_score_topk without a caller
+ * workspace.  The pages have no counterpart to this call; it exists for
+ * callers that cannot allocate device memory when they need the selection:
+ * an engine whose pool allocator has already claimed all of HBM, a runtime
+ * with no device-allocation hook of its own, or a decode loop that must not
+ * pay cudaMalloc's implicit device synchronisation.  Those callers still own
+ * and pass every input and output; only the scratch moves into the library.
+ *
+ * Same arguments, semantics and results as page_score_topk, minus
+ * workspace / workspace_bytes.  The scratch is one fixed 4 MiB array in the
+ * library's own device memory (every GPU that loads libkvmm holds it until
+ * the process exits): up to 4096 (batch, KV head) units of a layer and
+ * B * Hkv * Pmax <= 1,044,480 scores; a larger shape returns
+ * KVMM_WORKSPACE_TOO_SMALL and nothing runs.  The first call on a device
+ * looks up the array's device address and zeroes its counters on `stream`;
+ * make that first call before any stream capture.  Every call on a device
+ * shares the one array and leaves its last contents in it, so calls whose
+ * kernels overlap on the GPU (different streams, or concurrent host
+ * threads) race and give wrong selections; serialise them (calls on one
+ * stream never overlap).
+ */
+kvmm_status page_score_topk_static_scratch(const kvmm_shape* shape, int32_t layer, const kvmm_bf16* q,
+                                           const kvmm_bf16* meta, const int32_t* seq_len,
+                                           const uint8_t* rescore_mask, int32_t K, int32_t group_reduce,
+                                           int32_t* sel_idx, int32_t* sel_cnt, float* scores_out,
+                                           int32_t* err, kvmm_stream stream);
+
+/* ------------------------------------------------------------------------
  * sparse_paged_decode_attn -- GQA decode attention of every query head of
  * `layer` over the valid tokens of its KV head's selected pages only.
  *

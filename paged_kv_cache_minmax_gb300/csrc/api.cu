@@ -185,6 +185,54 @@ kvmm_status page_score_topk(const kvmm_shape* shape, int32_t layer, const kvmm_b
     return launched(kvmm::launch_score_topk(p, group_reduce, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+kvmm_status page_score_topk_static_scratch(const kvmm_shape* shape, int32_t layer, const kvmm_bf16* q,
+                                           const kvmm_bf16* meta, const int32_t* seq_len,
+                                           const uint8_t* rescore_mask, int32_t K, int32_t group_reduce,
+                                           int32_t* sel_idx, int32_t* sel_cnt, float* scores_out,
+                                           int32_t* err, kvmm_stream stream)
+{
+    kvmm_status st = check_shape(shape);
+    if (st != KVMM_OK) return st;
+    const kvmm_shape& s = *shape;
+    if (layer < 0 || layer >= s.L || K < 1 || K > s.Kmax) return KVMM_INVALID_ARG;
+    if (group_reduce != 0 && group_reduce != 1) return KVMM_INVALID_ARG;
+    if (!req(q) || !req(meta) || !req4(seq_len) || !req4(sel_idx) || !req4(sel_cnt) || !opt4(scores_out) ||
+        !opt4(err))
+        return KVMM_INVALID_ARG;
+    // the shape must fit the fixed scratch: counters region, then B*Hkv*Pmax scores
+    const size_t units = size_t(s.B) * s.Hkv;
+    if (units * sizeof(int32_t) > kvmm::kStaticScratchCounterBytes ||
+        kvmm::kStaticScratchCounterBytes + units * s.Pmax * sizeof(float) > kvmm::kStaticScratchBytes)
+        return KVMM_WORKSPACE_TOO_SMALL;
+    void* scratch = nullptr;
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    const cudaError_t se = kvmm::static_scratch_for_current_device(&scratch, cs);
+    if (se != cudaSuccess) return launched(se);
+    ScoreParams p{};
+    p.B = s.B;
+    p.L = s.L;
+    p.Hq = s.Hq;
+    p.Hkv = s.Hkv;
+    p.G = s.Hq / s.Hkv;
+    p.D = s.D;
+    p.T = s.T;
+    p.Pmax = s.Pmax;
+    p.Kmax = s.Kmax;
+    p.layer = layer;
+    p.K = K;
+    p.q = q;
+    p.meta = meta;
+    p.seq_len = seq_len;
+    p.rescore_mask = rescore_mask;
+    p.sel_idx = sel_idx;
+    p.sel_cnt = sel_cnt;
+    p.scores_out = scores_out;
+    p.counters = static_cast<int32_t*>(scratch);
+    p.scores_ws = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + kvmm::kStaticScratchCounterBytes);
+    p.err = err;
+    return launched(kvmm::launch_score_topk(p, group_reduce, cs));
+}
+
 kvmm_status sparse_paged_decode_attn(const kvmm_shape* shape, int32_t layer, const kvmm_bf16* q,
                                      const kvmm_bf16* k_pool, const kvmm_bf16* v_pool,
                                      const int32_t* block_table, const int32_t* seq_len,

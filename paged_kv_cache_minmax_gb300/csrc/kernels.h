@@ -90,6 +90,14 @@ cudaError_t launch_score_topk(const ScoreParams& p, int group_reduce, cudaStream
 cudaError_t launch_sparse_attention(const AttnParams& p, cudaStream_t stream);
 cudaError_t launch_promotion_diff(const DiffParams& p, cudaStream_t stream);
 
+// Library-owned scratch of page_score_topk_static_scratch (score_topk.cu):
+// counters for up to kStaticScratchCounterBytes/4 units, then the scores.
+constexpr size_t kStaticScratchBytes = size_t(4) << 20;
+constexpr size_t kStaticScratchCounterBytes = size_t(16) << 10;
+// Device address of that scratch on the current device; the first call on a
+// device resolves it and zeroes the counters on `stream`.
+cudaError_t static_scratch_for_current_device(void** ptr, cudaStream_t stream);
+
 // Attention launch geometry for the current device.
 int attention_slots_per_unit(const kvmm_shape& s);  // automatic split count
 size_t attention_smem_bytes(int D, int max_tiles);

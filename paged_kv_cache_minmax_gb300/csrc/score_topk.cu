@@ -21,6 +21,7 @@
 // top-K with an exact 4-pass radix select on order-preserving keys and
 // writes the pages in ascending order, ties resolved to the lower index.
 #include <cfloat>
+#include <mutex>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -341,6 +342,42 @@ cudaError_t launch_score_topk(const ScoreParams& p, int group_reduce, cudaStream
 {
     if (p.D == 128) return group_reduce ? launch_one<128, 1>(p, stream) : launch_one<128, 0>(p, stream);
     return group_reduce ? launch_one<64, 1>(p, stream) : launch_one<64, 0>(p, stream);
+}
+
+// ---------------------------------------------------------------------------
+// Library-owned scratch for page_score_topk_static_scratch: a fixed array in
+// the module's device memory, so that call needs no workspace from its
+// caller and allocates nothing.  Every GPU that loads the library holds these
+// bytes until the process exits.  Layout as for a caller workspace: the
+// per-unit counters first, then the scores.
+namespace {
+__device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_static_mutex;
+void* g_static_ptr[kMaxDevices] = {};
+}  // namespace
+
+cudaError_t static_scratch_for_current_device(void** ptr, cudaStream_t stream)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_static_mutex);
+    if (g_static_ptr[dev] == nullptr) {
+        // first call on this device: resolve the array's device address (the
+        // host-side name is only a stand-in) and zero the counters, which
+        // every later call leaves at zero again
+        void* addr = nullptr;
+        e = cudaGetSymbolAddress(&addr, g_static_scratch);
+        if (e != cudaSuccess) return e;
+        e = cudaMemsetAsync(addr, 0, kStaticScratchCounterBytes, stream);
+        if (e != cudaSuccess) return e;
+        g_static_ptr[dev] = addr;
+    }
+    *ptr = g_static_ptr[dev];
+    return cudaSuccess;
 }
 
 }  // namespace kvmm

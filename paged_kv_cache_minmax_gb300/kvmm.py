@@ -20,7 +20,8 @@ ERR_NULL_BLOCK, ERR_OUT_OF_RANGE, ERR_TIMEOUT = 1, 2, 4
 NULL_BLOCK = -1
 
 EXPORTS = ("kv_minmax_update", "page_score_topk", "sparse_paged_decode_attn", "topk_promotion_diff",
-           "kvmm_workspace_size", "kvmm_auto_splits", "kvmm_status_string", "kvmm_last_cuda_error")
+           "kvmm_workspace_size", "kvmm_auto_splits", "kvmm_status_string", "kvmm_last_cuda_error",
+           "page_score_topk_static_scratch")
 
 
 class KvmmError(RuntimeError):
@@ -72,7 +73,9 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.page_score_topk.argtypes = [SP, I32, P, P, P, P, I32, I32, P, P, P, P, SZ, P, P]
     lib.sparse_paged_decode_attn.argtypes = [SP, I32, P, P, P, P, P, P, P, F32, I32, P, P, P, SZ, P, P]
     lib.topk_promotion_diff.argtypes = [SP, I32, P, P, P, P, P, I32, P, P, P, P, P, P, P]
-    for f in ("kv_minmax_update", "page_score_topk", "sparse_paged_decode_attn", "topk_promotion_diff"):
+    lib.page_score_topk_static_scratch.argtypes = [SP, I32, P, P, P, P, I32, I32, P, P, P, P, P]
+    for f in ("kv_minmax_update", "page_score_topk", "sparse_paged_decode_attn", "topk_promotion_diff",
+              "page_score_topk_static_scratch"):
         getattr(lib, f).restype = ctypes.c_int
     lib.kvmm_workspace_size.argtypes = [SP, I32]
     lib.kvmm_workspace_size.restype = SZ
@@ -165,6 +168,25 @@ def page_score_topk(shape: Shape, layer: int, q, meta, seq_len, rescore_mask, K:
             _dev(workspace, "workspace", torch.uint8), workspace.numel(),
             _dev(err, "err", torch.int32, 1, optional=True), _stream(stream))
     _check("page_score_topk", load().page_score_topk(*args))
+
+
+def page_score_topk_static_scratch(shape: Shape, layer: int, q, meta, seq_len, rescore_mask, K: int, sel_idx,
+                                   sel_cnt, err=None, scores_out=None, group_reduce: int = 0, stream=None) -> None:
+    """page_score_topk with the library's fixed device scratch instead of a caller workspace.
+
+    For callers that cannot allocate device memory at call time; the scratch
+    is shared by every call on a device, so calls must not overlap on the GPU.
+    """
+    s = shape
+    units = s.B * s.L * s.Hkv
+    args = (ctypes.byref(s), layer, _dev(q, "q", torch.bfloat16, s.B * s.Hq * s.D),
+            _dev(meta, "meta", torch.bfloat16, units * s.Pmax * 2 * s.D),
+            _dev(seq_len, "seq_len", torch.int32, s.B),
+            _dev(rescore_mask, "rescore_mask", torch.uint8, s.L * s.Hkv, optional=True), K, group_reduce,
+            _dev(sel_idx, "sel_idx", torch.int32, units * s.Kmax), _dev(sel_cnt, "sel_cnt", torch.int32, units),
+            _dev(scores_out, "scores_out", torch.float32, s.B * s.Hkv * s.Pmax, optional=True),
+            _dev(err, "err", torch.int32, 1, optional=True), _stream(stream))
+    _check("page_score_topk_static_scratch", load().page_score_topk_static_scratch(*args))
 
 
 def sparse_paged_decode_attn(shape: Shape, layer: int, q, k_pool, v_pool, block_table, seq_len, sel_idx, sel_cnt,
