@@ -24,7 +24,6 @@ import os
 import statistics
 import subprocess
 import sys
-import threading
 import time
 
 import numpy as np
@@ -261,6 +260,8 @@ def gpu_arm(args):
     kvmm.load()
 
     cfg = CFG
+    if args.batch or args.layers:
+        cfg = workloads.scaled(cfg, B=args.batch or cfg.B, L=args.layers or cfg.L)
     L = cfg.L
     # replicas: every rank decodes its own batch (seeded per rank); no collective on the data path
     wl = workloads.generate(cfg, device="cuda", seed=cfg.seed + 7919 * rank)
@@ -293,17 +294,27 @@ def gpu_arm(args):
             if instrument:
                 ev_s[4 * l + 3].record()
 
+    torch.cuda.empty_cache()
     with torch.cuda.stream(stream):
         for _ in range(3):
             step(False)
     stream.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    graph_instr = torch.cuda.CUDAGraph() if external else None
-    with torch.cuda.graph(graph, stream=stream):
-        step(False)
-    if external:
-        with torch.cuda.graph(graph_instr, stream=stream):
-            step(True)
+    if args.no_graph:  # eager launches (profiling): same kernels, host-issued every step
+        external = False
+
+        class _Eager:
+            def replay(self):
+                step(False)
+
+        graph, graph_instr = _Eager(), None
+    else:
+        graph = torch.cuda.CUDAGraph()
+        graph_instr = torch.cuda.CUDAGraph() if external else None
+        with torch.cuda.graph(graph, stream=stream):
+            step(False)
+        if external:
+            with torch.cuda.graph(graph_instr, stream=stream):
+                step(True)
     st.err.zero_()
 
     with torch.cuda.stream(stream):
@@ -402,7 +413,8 @@ def gpu_arm(args):
                    "q_heads": cfg.Hq, "kv_heads": cfg.Hkv, "head_dim": cfg.D, "page_tokens": cfg.T,
                    "top_k_pages": cfg.K, "splits": splits, "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (4 GiB of distinct data per step, no flush)",
-                   "step": "one decode step = 32 layer-steps, CUDA graph replay"},
+                   "step": f"one decode step = {L} layer-steps, " + ("eager launches" if args.no_graph
+                                                                     else "CUDA graph replay")},
         "kv_gbs": kv_gbs, "pct_hbm_peak": kv_gbs / peak,
         "bytes_per_layer_step": acc["total"],
         "kernel_ms": {"score_topk_kernel": s_ms, "sparse_attn_kernel": a_ms,
@@ -444,6 +456,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="kvmm", choices=["kvmm", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="launch eagerly (for profilers)")
+    ap.add_argument("--batch", type=int, default=0, help="override the batch (smaller profiling case)")
+    ap.add_argument("--layers", type=int, default=0, help="override the layer count (smaller profiling case)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.impl == "reference":

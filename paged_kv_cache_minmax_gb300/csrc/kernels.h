@@ -4,6 +4,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <utility>
 
 #include <cuda_runtime.h>
 
@@ -83,6 +84,42 @@ struct DiffParams {
     int32_t* total_promoted;
     int32_t* err;
 };
+
+// Launch `kernel` on `stream` with programmatic stream serialisation, so it
+// may be scheduled while its predecessor drains (it must griddepcontrol.wait
+// before using the predecessor's results).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// Raise a kernel's dynamic shared-memory limit to `bytes` (once per device and
+// size; the default 48 KiB limit counts static shared memory too).
+template <typename Kernel>
+cudaError_t allow_smem(Kernel kernel, size_t bytes, int& dev_cache, size_t& bytes_cache)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev_cache == dev && bytes_cache >= bytes) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+    if (e != cudaSuccess) return e;
+    dev_cache = dev;
+    bytes_cache = bytes;
+    return cudaSuccess;
+}
 
 // Launchers return cudaSuccess or the launch error.
 cudaError_t launch_minmax_update(const UpdateParams& p, cudaStream_t stream);

@@ -41,6 +41,8 @@ __global__ void __launch_bounds__(kUpdWarps * 32) minmax_update_kernel(const Upd
     const int h = blockIdx.y;
     const int b = blockIdx.z;
     const int T = p.T;
+    pdl_launch_dependents();
+    pdl_wait();  // the pools, table and metadata may be in use by the previous kernel
 
     int tb = p.tok_begin[b];
     int te = p.tok_end[b];
@@ -124,11 +126,8 @@ cudaError_t launch_minmax_update(const UpdateParams& p, cudaStream_t stream)
     const long long span = p.new_k ? (static_cast<long long>(p.n_new) + p.T - 1) / p.T + 1 : p.Pmax;
     const long long pages = span < p.Pmax ? span : p.Pmax;
     const dim3 grid(static_cast<unsigned>((pages + kUpdWarps - 1) / kUpdWarps), p.Hkv, p.B);
-    if (p.D == 128)
-        minmax_update_kernel<128><<<grid, kUpdWarps * 32, 0, stream>>>(p);
-    else
-        minmax_update_kernel<64><<<grid, kUpdWarps * 32, 0, stream>>>(p);
-    return cudaGetLastError();
+    if (p.D == 128) return launch_pdl(minmax_update_kernel<128>, grid, dim3(kUpdWarps * 32), 0, stream, p);
+    return launch_pdl(minmax_update_kernel<64>, grid, dim3(kUpdWarps * 32), 0, stream, p);
 }
 
 }  // namespace kvmm

@@ -66,6 +66,8 @@ __global__ void __launch_bounds__(kDiffThreads) promotion_diff_kernel(const Diff
     const int b = blockIdx.y;
     const int tid = threadIdx.x;
     const size_t unit = (static_cast<size_t>(b) * p.L + p.layer) * p.Hkv + h;
+    pdl_launch_dependents();
+    pdl_wait();  // the current selection comes from the preceding kernels
 
     if (p.rescore_mask != nullptr && p.rescore_mask[p.layer * p.Hkv + h] == 0) {
         if (tid == 0) {
@@ -115,9 +117,7 @@ __global__ void __launch_bounds__(kDiffThreads) promotion_diff_kernel(const Diff
 
 cudaError_t launch_promotion_diff(const DiffParams& p, cudaStream_t stream)
 {
-    const dim3 grid(p.Hkv, p.B);
-    promotion_diff_kernel<<<grid, kDiffThreads, 0, stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(promotion_diff_kernel, dim3(p.Hkv, p.B), dim3(kDiffThreads), 0, stream, p);
 }
 
 }  // namespace kvmm

@@ -7,19 +7,31 @@
 // multiplies the query with the channel-wise key min and max.
 //
 // Score of page p for query head g:  s_g(p) = sum_d max(q_gd*min_d, q_gd*max_d).
-// Since max(q*m, q*M) = max(q,0)*M + min(q,0)*m, the group SUM is a single
-// dot product of the page's [min | max] row (2D bf16) with the fixed weight
-// row [sum_g min(q_g,0) | sum_g max(q_g,0)] (fp32): one FMA per bf16 read,
-// the same real number as the definition up to fp32 rounding.  The MAX
-// group mode keeps one weight row per query head.
+// Since max(q*m, q*M) = min(q,0)*m + max(q,0)*M, and min(q,0), max(q,0) are
+// exact bf16 values, s_g(p) is the dot product of the page's [min | max] row
+// (2D bf16) with the head's weight row [min(q_g,0) | max(q_g,0)] (2D bf16):
+// bf16 x bf16 products are exact in fp32.  For 16 pages and the G <= 8 heads
+// of a KV head that is one [16 x 2D] x [2D x 8] product on the tensor cores
+// (mma.sync m16n8k16, fp32 accumulate); the unit's score is the sum (or, with
+// group_reduce = 1, the max) over the real heads of each row.
 //
-// Work split (HBM bound, 2D*2 bytes of metadata per page): one CTA scores a
-// chunk of kChunk pages of one unit, staged into shared memory by one
-// bulk copy (TMA) on an mbarrier; a warp reduces 4 pages at a time with a
-// transposed butterfly (6 shuffles per 4 pages).  Scores go to the
-// workspace; the last CTA of a unit (atomic ticket, no spinning) selects the
-// top-K with an exact 4-pass radix select on order-preserving keys and
-// writes the pages in ascending order, ties resolved to the lower index.
+// page_score_topk runs two kernels:
+//  1. score_pages_kernel -- a persistent, warp-specialised stream over the
+//     metadata (HBM bound, 2D*2 bytes per page).  Work items are chunks of
+//     kChunk pages of one unit; each CTA takes a contiguous run of items, so
+//     it rebuilds a unit's weight fragments only when the unit changes.  A
+//     producer warp keeps kStages chunks (and the unit's query group) in
+//     flight with 1-D bulk copies (TMA) on full/empty mbarriers; each
+//     consumer warp scores 16 pages of a chunk.
+//  2. select_topk_kernel -- one CTA per rescored unit selects the top K of
+//     the unit's P scores exactly: one pass buckets the scores into 2048 bins
+//     between their min and max (monotone in the value), a suffix scan finds
+//     the bin holding the K-th largest, the few scores in that bin are ranked
+//     exactly (value descending, page ascending), and an ordered compaction
+//     writes the pages in ascending order.  Degenerate inputs (a crowded
+//     threshold bin, a non-finite range) take an exact 4-pass radix select.
+// Both are launched with programmatic dependent launch so each is scheduled
+// while its predecessor drains.
 #include <cfloat>
 #include <mutex>
 
@@ -29,11 +41,19 @@
 namespace kvmm {
 namespace {
 
-constexpr int kScoreThreads = 128;
-constexpr int kScoreWarps = kScoreThreads / 32;
-constexpr int kChunk = 64;  // pages per CTA
+constexpr int kConsumerWarps = 4;
+constexpr int kScoreThreads = kConsumerWarps * 32 + 32;  // + one producer warp
+constexpr int kChunk = 16 * kConsumerWarps;               // pages per work item, 16 per consumer warp
+constexpr int kStages = 3;
+constexpr int kQBytes = 8 * 128 * 2;                      // largest query group (G <= 8, D <= 128)
 
-__host__ __device__ constexpr int chunk_bytes(int D) { return kChunk * 4 * D; }
+constexpr int kTopkThreads = 512;
+constexpr int kTopkWarps = kTopkThreads / 32;
+constexpr int kBins = 2048;
+constexpr int kCandMax = 1024;
+
+__host__ __device__ constexpr int stage_meta_bytes(int D) { return kChunk * 4 * D; }
+__host__ __device__ constexpr int stage_bytes(int D) { return stage_meta_bytes(D) + kQBytes; }
 
 // float -> unsigned key with the same order
 __device__ __forceinline__ uint32_t order_key(float f)
@@ -42,223 +62,216 @@ __device__ __forceinline__ uint32_t order_key(float f)
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-__device__ __forceinline__ float dot8(const uint4& v, const float (&w)[8])
+// per 16-bit half: keep negative values (min(x, 0)) or positive ones (max(x, 0))
+__device__ __forceinline__ uint32_t bf16x2_min0(uint32_t w)
 {
-    float s = bf16_lo(v.x) * w[0];
-    s = fmaf(bf16_hi(v.x), w[1], s);
-    s = fmaf(bf16_lo(v.y), w[2], s);
-    s = fmaf(bf16_hi(v.y), w[3], s);
-    s = fmaf(bf16_lo(v.z), w[4], s);
-    s = fmaf(bf16_hi(v.z), w[5], s);
-    s = fmaf(bf16_lo(v.w), w[6], s);
-    s = fmaf(bf16_hi(v.w), w[7], s);
-    return s;
+    const uint32_t neg = ((w >> 15) & 0x00010001u) * 0xffffu;
+    return w & neg;
+}
+__device__ __forceinline__ uint32_t bf16x2_max0(uint32_t w)
+{
+    const uint32_t neg = ((w >> 15) & 0x00010001u) * 0xffffu;
+    return w & ~neg;
 }
 
-// Sum four per-lane partials (one per page load j) over groups of LPP lanes.
-// Afterwards lane l holds the total of load j = 2*bit(LPP/2) + bit(LPP/4)
-// of its group; it is valid where (l % (LPP/4)) == 0.
-template <int LPP>
-__device__ __forceinline__ float reduce4(const float (&v)[4], int lane)
+// pages of sequence `seq_len[b]` clamped to the table, reporting overflow once
+__device__ __forceinline__ int unit_pages(const ScoreParams& p, int b, bool report_overflow)
 {
-    const bool up1 = lane & (LPP / 2);
-    float k0 = up1 ? v[2] : v[0];
-    float k1 = up1 ? v[3] : v[1];
-    const float s0 = up1 ? v[0] : v[2];
-    const float s1 = up1 ? v[1] : v[3];
-    k0 += __shfl_xor_sync(kFullMask, s0, LPP / 2);
-    k1 += __shfl_xor_sync(kFullMask, s1, LPP / 2);
-    const bool up2 = lane & (LPP / 4);
-    float k = up2 ? k1 : k0;
-    const float s = up2 ? k0 : k1;
-    k += __shfl_xor_sync(kFullMask, s, LPP / 4);
-#pragma unroll
-    for (int off = LPP / 8; off >= 1; off >>= 1) k += __shfl_xor_sync(kFullMask, k, off);
-    return k;
+    int seq = p.seq_len[b];
+    const int cap = p.Pmax * p.T;
+    if (seq < 0 || seq > cap) {
+        if (report_overflow) report(p.err, KVMM_ERR_OUT_OF_RANGE);
+        seq = seq < 0 ? 0 : cap;
+    }
+    return (seq + p.T - 1) / p.T;
 }
 
-struct TopkShared {
-    int hist[256];
-    int warp_tot[2][kScoreWarps];
-    int digit;
-    int remaining;
-    int last;
-};
-
+// ---------------------------------------------------------------------------
 template <int D, int MODE>
-__global__ void __launch_bounds__(kScoreThreads) score_topk_kernel(const ScoreParams p)
+__global__ void __launch_bounds__(kScoreThreads) score_pages_kernel(const ScoreParams p)
 {
-    constexpr int LPP = D / 4;      // lanes per page (16 bytes each)
-    constexpr int PPL = 32 / LPP;   // pages per warp-wide load
-    constexpr int kWRows = MODE == 0 ? 1 : 8;
+    constexpr int kRowChunks = 2 * D / 8;   // 16-byte chunks in a [min | max] row
+    constexpr int kR = kRowChunks / 4;      // chunk groups: lane tig takes chunk 4r + tig
     extern __shared__ __align__(128) uint8_t smem[];
-    __shared__ uint64_t bar;
-    __shared__ __align__(16) float w_s[kWRows][2 * D];
-    __shared__ TopkShared ts;
+    __shared__ uint64_t full_bar[kStages];
+    __shared__ uint64_t empty_bar[kStages];
+    __shared__ int4 info[kStages];  // {workspace unit, first page, pages (0 = skip), -}
 
     const int tid = threadIdx.x;
     const int lane = tid & 31;
     const int warp = tid >> 5;
-    const int chunk = blockIdx.x;
-    const int h = blockIdx.y;
-    const int b = blockIdx.z;
-
-    if (p.rescore_mask != nullptr && p.rescore_mask[p.layer * p.Hkv + h] == 0) return;
-
-    int seq = p.seq_len[b];
-    const int cap = p.Pmax * p.T;
-    if (seq > cap || seq < 0) {
-        if (chunk == 0 && tid == 0) report(p.err, KVMM_ERR_OUT_OF_RANGE);
-        seq = seq < 0 ? 0 : cap;
-    }
-    const int P = (seq + p.T - 1) / p.T;
-    const int n_chunks = (P + kChunk - 1) / kChunk;
-    const size_t unit = (static_cast<size_t>(b) * p.L + p.layer) * p.Hkv + h;  // table / meta / sel
-    const int wunit = b * p.Hkv + h;                                            // workspace slot
-
-    if (P == 0) {  // empty sequence: empty selection
-        if (chunk == 0 && tid == 0) p.sel_cnt[unit] = 0;
-        return;
-    }
-    if (chunk >= n_chunks) return;
-
-    const int page0 = chunk * kChunk;
-    const int npg = min(kChunk, P - page0);
-    const kvmm_bf16* src = p.meta + (unit * p.Pmax + page0) * 2 * D;
+    const int gid = lane >> 2, tig = lane & 3;
+    const int units = p.B * p.Hkv;
+    const int chunks = (p.Pmax + kChunk - 1) / kChunk;
+    const long long total = static_cast<long long>(units) * chunks;
+    const int item0 = static_cast<int>(total * blockIdx.x / gridDim.x);
+    const int item1 = static_cast<int>(total * (blockIdx.x + 1) / gridDim.x);
 
     if (tid == 0) {
-        mbar_init(&bar, 1);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full_bar[s], 1);
+            mbar_init(&empty_bar[s], kConsumerWarps);
+        }
         fence_barrier_init();
     }
     __syncthreads();
-    if (tid == 0) {
-        const uint32_t bytes = static_cast<uint32_t>(npg) * 4 * D;
-        mbar_arrive_expect_tx(&bar, bytes);
-        bulk_copy_g2s(smem, src, bytes, &bar);
-    }
+    pdl_launch_dependents();
+    pdl_wait();  // metadata and queries may come from the previous kernel
 
-    // weight rows while the copy is in flight
-    const kvmm_bf16* qb = p.q + (static_cast<size_t>(b) * p.Hq + static_cast<size_t>(h) * p.G) * D;
-    for (int d = tid; d < D; d += kScoreThreads) {
-        if (MODE == 0) {
-            float wn = 0.f, wx = 0.f;
-            for (int g = 0; g < p.G; ++g) {
-                const float x = __uint_as_float(static_cast<uint32_t>(qb[g * D + d]) << 16);
-                wn += fminf(x, 0.f);
-                wx += fmaxf(x, 0.f);
-            }
-            w_s[0][d] = wn;
-            w_s[0][D + d] = wx;
-        } else {
-            for (int g = 0; g < kWRows; ++g) {
-                const float x = g < p.G ? __uint_as_float(static_cast<uint32_t>(qb[g * D + d]) << 16) : 0.f;
-                w_s[g][d] = fminf(x, 0.f);
-                w_s[g][D + d] = fmaxf(x, 0.f);
-            }
-        }
-    }
-    __syncthreads();
-
-    const int sub = lane % LPP;  // 16-byte column of the page row: [min | max]
-    float w[kWRows][8];
-#pragma unroll
-    for (int g = 0; g < kWRows; ++g)
-#pragma unroll
-        for (int i = 0; i < 8; ++i) w[g][i] = w_s[g][8 * sub + i];
-
-    const bool ok = __syncthreads_and(mbar_wait_bounded(&bar, 0)) != 0;  // block-uniform
-    if (!ok && tid == 0) report(p.err, KVMM_ERR_TIMEOUT);
-
-    float* scores_ws = p.scores_ws + static_cast<size_t>(wunit) * p.Pmax;
-    float* scores_out = p.scores_out ? p.scores_out + static_cast<size_t>(wunit) * p.Pmax : nullptr;
-    if (ok) {
-        constexpr int kPagesPerIter = 4 * PPL;
-        for (int base = warp * kPagesPerIter; base < npg; base += kScoreWarps * kPagesPerIter) {
-            float part[kWRows][4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int pg = base + j * PPL + lane / LPP;
-                uint4 v = make_uint4(0u, 0u, 0u, 0u);
-                if (pg < npg) v = ld_shared_v4(smem + static_cast<size_t>(pg) * 4 * D + 16 * sub);
-#pragma unroll
-                for (int g = 0; g < kWRows; ++g) part[g][j] = dot8(v, w[g]);
-            }
-            float score;
-            if (MODE == 0) {
-                score = reduce4<LPP>(part[0], lane);
-            } else {
-                score = -FLT_MAX;
-#pragma unroll
-                for (int g = 0; g < kWRows; ++g) {
-                    const float sg = reduce4<LPP>(part[g], lane);
-                    if (g < p.G) score = fmaxf(score, sg);
+    if (warp == kConsumerWarps) {
+        // ---- producer ------------------------------------------------------
+        if (lane == 0) {
+            for (int item = item0, k = 0; item < item1; ++item, ++k) {
+                const int s = k % kStages;
+                if (k >= kStages && !mbar_wait_bounded(&empty_bar[s], ((k / kStages) - 1) & 1))
+                    report(p.err, KVMM_ERR_TIMEOUT);
+                const int wunit = item / chunks;
+                const int chunk = item - wunit * chunks;
+                const int b = wunit / p.Hkv, h = wunit - b * p.Hkv;
+                const int page0 = chunk * kChunk;
+                int npg = 0;
+                if (p.rescore_mask == nullptr || p.rescore_mask[p.layer * p.Hkv + h] != 0) {
+                    const int P = unit_pages(p, b, chunk == 0 && h == 0);
+                    npg = min(kChunk, P - page0);
+                    if (npg < 0) npg = 0;
+                }
+                info[s] = make_int4(wunit, page0, npg, 0);
+                if (npg > 0) {
+                    uint8_t* st = smem + static_cast<size_t>(s) * stage_bytes(D);
+                    const size_t unit = (static_cast<size_t>(b) * p.L + p.layer) * p.Hkv + h;
+                    const uint32_t mbytes = static_cast<uint32_t>(npg) * 4 * D;
+                    const uint32_t qbytes = static_cast<uint32_t>(p.G) * D * 2;
+                    mbar_arrive_expect_tx(&full_bar[s], mbytes + qbytes);
+                    bulk_copy_g2s(st, p.meta + (unit * p.Pmax + page0) * 2 * D, mbytes, &full_bar[s]);
+                    bulk_copy_g2s(st + stage_meta_bytes(D),
+                                  p.q + (static_cast<size_t>(b) * p.Hq + static_cast<size_t>(h) * p.G) * D,
+                                  qbytes, &full_bar[s]);
+                } else {
+                    mbar_arrive(&full_bar[s]);  // nothing to copy: consumers skip the item
                 }
             }
-            const int j = 2 * ((lane / (LPP / 2)) & 1) + ((lane / (LPP / 4)) & 1);
-            const int pg = base + j * PPL + lane / LPP;
-            if ((lane % (LPP / 4)) == 0 && pg < npg) {
-                scores_ws[page0 + pg] = score;
-                if (scores_out) scores_out[page0 + pg] = score;
-            }
         }
-    }
-
-    // ---- last CTA of the unit selects -----------------------------------
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) {
-        const int ticket = atomicAdd(p.counters + wunit, 1);
-        ts.last = (ticket == n_chunks - 1);
-        if (ts.last) p.counters[wunit] = 0;  // ready for the next call
-    }
-    __syncthreads();
-    if (!ts.last) return;
-    __threadfence();
-
-    int32_t* sel = p.sel_idx + unit * p.Kmax;
-    const int K = p.K;
-    if (K >= P) {
-        for (int i = tid; i < P; i += kScoreThreads) sel[i] = i;
-        if (tid == 0) p.sel_cnt[unit] = P;
         return;
     }
 
-    // keys in shared memory when they fit the staging buffer, else re-read from L2
-    const bool keys_in_smem = static_cast<size_t>(P) * 4 <= static_cast<size_t>(chunk_bytes(D));
-    uint32_t* keys = reinterpret_cast<uint32_t*>(smem);
-    if (keys_in_smem) {
-        for (int i = tid; i < P; i += kScoreThreads) keys[i] = order_key(__ldcg(scores_ws + i));
-        __syncthreads();
+    // ---- consumers: warp w scores pages [16w, 16w + 16) of each chunk ------
+    uint32_t wf[kR][4];  // weight B fragments of head gid: chunk 4r + tig of [min(q,0) | max(q,0)]
+    int cached_unit = -1;
+    const bool real_head = gid < p.G;
+    for (int item = item0, k = 0; item < item1; ++item, ++k) {
+        const int s = k % kStages;
+        if (!mbar_wait_bounded(&full_bar[s], (k / kStages) & 1) && lane == 0) report(p.err, KVMM_ERR_TIMEOUT);
+        const int4 inf = info[s];
+        const int npg = inf.z;
+        const uint8_t* st = smem + static_cast<size_t>(s) * stage_bytes(D);
+        if (npg > 0 && inf.x != cached_unit) {
+            const uint8_t* qs = st + stage_meta_bytes(D) + gid * (2 * D);
+#pragma unroll
+            for (int r = 0; r < kR; ++r) {
+                const int cc = 4 * r + tig;                 // chunk of the [min | max] row
+                const int qc = cc % (D / 8);                // source chunk of q
+                uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                if (real_head) v = ld_shared_v4(qs + 16 * qc);
+                const bool is_max = cc >= D / 8;
+                wf[r][0] = is_max ? bf16x2_max0(v.x) : bf16x2_min0(v.x);
+                wf[r][1] = is_max ? bf16x2_max0(v.y) : bf16x2_min0(v.y);
+                wf[r][2] = is_max ? bf16x2_max0(v.z) : bf16x2_min0(v.z);
+                wf[r][3] = is_max ? bf16x2_max0(v.w) : bf16x2_min0(v.w);
+            }
+            cached_unit = inf.x;
+        }
+        const int pg0 = warp * 16;
+        if (pg0 < npg) {
+            // C[page][head] over this warp's 16 pages: rows gid and gid + 8
+            const uint8_t* ra = st + static_cast<size_t>(pg0 + gid) * 4 * D;
+            const uint8_t* rb = ra + 8 * 4 * D;
+            float c[4] = {0.f, 0.f, 0.f, 0.f}, c2[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int r = 0; r < kR; ++r) {
+                const uint4 ka = ld_shared_v4(ra + 16 * (4 * r + tig));
+                const uint4 kb = ld_shared_v4(rb + 16 * (4 * r + tig));
+                mma_bf16_16816(c, ka.x, kb.x, ka.y, kb.y, wf[r][0], wf[r][1]);
+                mma_bf16_16816(c2, ka.z, kb.z, ka.w, kb.w, wf[r][2], wf[r][3]);
+            }
+            // c: [page gid][head 2tig], [gid][2tig+1], [gid+8][2tig], [gid+8][2tig+1]
+            float s_lo, s_hi;
+            if (MODE == 0) {
+                s_lo = (c[0] + c2[0]) + (c[1] + c2[1]);
+                s_hi = (c[2] + c2[2]) + (c[3] + c2[3]);
+                s_lo += __shfl_xor_sync(kFullMask, s_lo, 1);
+                s_hi += __shfl_xor_sync(kFullMask, s_hi, 1);
+                s_lo += __shfl_xor_sync(kFullMask, s_lo, 2);
+                s_hi += __shfl_xor_sync(kFullMask, s_hi, 2);
+            } else {
+                const bool h0 = 2 * tig < p.G, h1 = 2 * tig + 1 < p.G;
+                s_lo = fmaxf(h0 ? c[0] + c2[0] : -FLT_MAX, h1 ? c[1] + c2[1] : -FLT_MAX);
+                s_hi = fmaxf(h0 ? c[2] + c2[2] : -FLT_MAX, h1 ? c[3] + c2[3] : -FLT_MAX);
+                s_lo = fmaxf(s_lo, __shfl_xor_sync(kFullMask, s_lo, 1));
+                s_hi = fmaxf(s_hi, __shfl_xor_sync(kFullMask, s_hi, 1));
+                s_lo = fmaxf(s_lo, __shfl_xor_sync(kFullMask, s_lo, 2));
+                s_hi = fmaxf(s_hi, __shfl_xor_sync(kFullMask, s_hi, 2));
+            }
+            if (tig == 0) {
+                const size_t base = static_cast<size_t>(inf.x) * p.Pmax + inf.y + pg0;
+                if (pg0 + gid < npg) {
+                    p.scores_ws[base + gid] = s_lo;
+                    if (p.scores_out) p.scores_out[base + gid] = s_lo;
+                }
+                if (pg0 + gid + 8 < npg) {
+                    p.scores_ws[base + gid + 8] = s_hi;
+                    if (p.scores_out) p.scores_out[base + gid + 8] = s_hi;
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty_bar[s]);  // the stage may be refilled
     }
-    auto key_at = [&](int i) -> uint32_t {
-        return keys_in_smem ? keys[i] : order_key(__ldcg(scores_ws + i));
-    };
+}
 
-    // radix select of the K-th largest key, 8 bits per pass from the top
+// ---------------------------------------------------------------------------
+struct TopkShared {
+    int hist[kBins];
+    int cand[kCandMax];
+    float wmin[kTopkWarps];
+    float wmax[kTopkWarps];
+    int wsum[kTopkWarps];
+    int rhist[256];
+    int ncand;
+    int tb;
+    int need;
+    int cbin;
+    int digit;
+    int remaining;
+};
+
+// Exact top-K over all P keys by 4 radix passes; writes sel[0..K) ascending.
+// The general path, used when the binned pass cannot isolate the threshold.
+__device__ void radix_topk(const float* sc, int P, int K, int32_t* sel, TopkShared& ts)
+{
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     uint32_t prefix = 0, pmask = 0;
     int remaining = K;
-    const int P_round = (P + kScoreThreads - 1) / kScoreThreads * kScoreThreads;
+    const int P_round = (P + kTopkThreads - 1) / kTopkThreads * kTopkThreads;
     for (int shift = 24; shift >= 0; shift -= 8) {
-        for (int i = tid; i < 256; i += kScoreThreads) ts.hist[i] = 0;
+        for (int i = tid; i < 256; i += kTopkThreads) ts.rhist[i] = 0;
         __syncthreads();
-        for (int i = tid; i < P_round; i += kScoreThreads) {
-            const uint32_t k = i < P ? key_at(i) : 0u;
-            const bool cand = i < P && (k & pmask) == prefix;
+        for (int i = tid; i < P_round; i += kTopkThreads) {
+            const uint32_t key = i < P ? order_key(sc[i]) : 0u;
+            const bool cand = i < P && (key & pmask) == prefix;
             const unsigned active = __ballot_sync(kFullMask, cand);
             if (cand) {
-                const uint32_t digit = (k >> shift) & 255u;
+                const uint32_t digit = (key >> shift) & 255u;
                 const unsigned peers = __match_any_sync(active, digit);
-                if (lane == __ffs(peers) - 1) atomicAdd(&ts.hist[digit], __popc(peers));
+                if (lane == __ffs(peers) - 1) atomicAdd(&ts.rhist[digit], __popc(peers));
             }
         }
         __syncthreads();
         if (warp == 0) {
-            // lane l covers bins 255-8l .. 248-8l, scanned from the top
             int c[8];
             int tot = 0;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-                c[j] = ts.hist[255 - 8 * lane - j];
+                c[j] = ts.rhist[255 - 8 * lane - j];
                 tot += c[j];
             }
             int incl = tot;
@@ -268,8 +281,7 @@ __global__ void __launch_bounds__(kScoreThreads) score_topk_kernel(const ScorePa
                 if (lane >= off) incl += v;
             }
             const int excl = incl - tot;
-            const bool here = excl < remaining && remaining <= incl;
-            if (here) {
+            if (excl < remaining && remaining <= incl) {
                 int acc = excl;
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
@@ -288,34 +300,31 @@ __global__ void __launch_bounds__(kScoreThreads) score_topk_kernel(const ScorePa
         remaining = ts.remaining;
         __syncthreads();
     }
-    const uint32_t thr = prefix;  // the K-th largest key; `remaining` of its ties are taken
-
-    // emit in ascending page order: every key > thr, and the first `remaining` keys == thr
+    const uint32_t thr = prefix;
     int out_base = 0, eq_base = 0;
     const unsigned lt_mask = (1u << lane) - 1u;
-    for (int t0 = 0; t0 < P; t0 += kScoreThreads) {
+    for (int t0 = 0; t0 < P; t0 += kTopkThreads) {
         const int i = t0 + tid;
-        const uint32_t k = i < P ? key_at(i) : 0u;
-        const bool gt = i < P && k > thr;
-        const bool eq = i < P && k == thr;
+        const uint32_t key = i < P ? order_key(sc[i]) : 0u;
+        const bool gt = i < P && key > thr;
+        const bool eq = i < P && key == thr;
         const unsigned eqb = __ballot_sync(kFullMask, eq);
-        if (lane == 0) ts.warp_tot[0][warp] = __popc(eqb);
+        if (lane == 0) ts.wsum[warp] = __popc(eqb);
         __syncthreads();
         int eq_off = eq_base, eq_all = 0;
-#pragma unroll
-        for (int w2 = 0; w2 < kScoreWarps; ++w2) {
-            const int t = ts.warp_tot[0][w2];
+        for (int w2 = 0; w2 < kTopkWarps; ++w2) {
+            const int t = ts.wsum[w2];
             if (w2 < warp) eq_off += t;
             eq_all += t;
         }
+        __syncthreads();
         const bool take = gt || (eq && eq_off + __popc(eqb & lt_mask) < remaining);
         const unsigned tb = __ballot_sync(kFullMask, take);
-        if (lane == 0) ts.warp_tot[1][warp] = __popc(tb);
+        if (lane == 0) ts.wsum[warp] = __popc(tb);
         __syncthreads();
         int out_off = out_base, out_all = 0;
-#pragma unroll
-        for (int w2 = 0; w2 < kScoreWarps; ++w2) {
-            const int t = ts.warp_tot[1][w2];
+        for (int w2 = 0; w2 < kTopkWarps; ++w2) {
+            const int t = ts.wsum[w2];
             if (w2 < warp) out_off += t;
             out_all += t;
         }
@@ -324,24 +333,190 @@ __global__ void __launch_bounds__(kScoreThreads) score_topk_kernel(const ScorePa
         eq_base += eq_all;
         __syncthreads();
     }
+}
+
+__global__ void __launch_bounds__(kTopkThreads) select_topk_kernel(const ScoreParams p)
+{
+    extern __shared__ __align__(16) uint8_t tsm[];
+    __shared__ TopkShared ts;
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const int h = blockIdx.x;
+    const int b = blockIdx.y;
+    pdl_launch_dependents();
+    pdl_wait();  // the scores are written by the scoring kernel
+
+    if (p.rescore_mask != nullptr && p.rescore_mask[p.layer * p.Hkv + h] == 0) return;
+    const int P = unit_pages(p, b, false);
+    const size_t unit = (static_cast<size_t>(b) * p.L + p.layer) * p.Hkv + h;
+    const float* scores = p.scores_ws + static_cast<size_t>(b * p.Hkv + h) * p.Pmax;
+    int32_t* sel = p.sel_idx + unit * p.Kmax;
+    const int K = p.K;
+    if (K >= P) {
+        for (int i = tid; i < P; i += kTopkThreads) sel[i] = i;
+        if (tid == 0) p.sel_cnt[unit] = P;
+        return;
+    }
+    float* sc = reinterpret_cast<float*>(tsm);                                           // [P]
+    int16_t* bin = reinterpret_cast<int16_t*>(tsm + static_cast<size_t>(p.Pmax) * 4);  // [P]
+
+    // 1. scores to shared memory, their range, an empty histogram
+    float lo = FLT_MAX, hi = -FLT_MAX;
+    for (int i = tid; i < P; i += kTopkThreads) {
+        const float s = __ldcg(scores + i);
+        sc[i] = s;
+        lo = fminf(lo, s);
+        hi = fmaxf(hi, s);
+    }
+    for (int i = tid; i < kBins; i += kTopkThreads) ts.hist[i] = 0;
+    if (tid == 0) ts.ncand = 0;
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+        lo = fminf(lo, __shfl_xor_sync(kFullMask, lo, off));
+        hi = fmaxf(hi, __shfl_xor_sync(kFullMask, hi, off));
+    }
+    if (lane == 0) {
+        ts.wmin[warp] = lo;
+        ts.wmax[warp] = hi;
+    }
+    __syncthreads();
+    float mn = ts.wmin[0], mx = ts.wmax[0];
+    for (int w = 1; w < kTopkWarps; ++w) {
+        mn = fminf(mn, ts.wmin[w]);
+        mx = fmaxf(mx, ts.wmax[w]);
+    }
+    if (!(mx > mn)) {  // every score equal: the K lowest pages win the ties
+        for (int i = tid; i < K; i += kTopkThreads) sel[i] = i;
+        if (tid == 0) p.sel_cnt[unit] = K;
+        return;
+    }
+    const float scale = static_cast<float>(kBins) / (mx - mn);
+    if (!(scale < FLT_MAX)) {
+        radix_topk(sc, P, K, sel, ts);
+        if (tid == 0) p.sel_cnt[unit] = K;
+        return;
+    }
+
+    // 2. bucket every score: bin(s) = floor((s - mn) * scale) is monotone in s
+    for (int i = tid; i < P; i += kTopkThreads) {
+        const int bi = min(kBins - 1, static_cast<int>((sc[i] - mn) * scale));
+        bin[i] = static_cast<int16_t>(bi);
+        atomicAdd(&ts.hist[bi], 1);
+    }
+    __syncthreads();
+
+    // 3. the bin holding the K-th largest score: suffix sums over bins
+    constexpr int kBinsPerThread = kBins / kTopkThreads;
+    int local = 0;
+#pragma unroll
+    for (int j = 0; j < kBinsPerThread; ++j) local += ts.hist[kBinsPerThread * tid + j];
+    int incl = local;  // inclusive suffix within the warp (lanes >= this one)
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int v = __shfl_down_sync(kFullMask, incl, off);
+        if (lane + off < 32) incl += v;
+    }
+    if (lane == 0) ts.wsum[warp] = incl;
+    __syncthreads();
+    int above = incl - local;
+    for (int w = warp + 1; w < kTopkWarps; ++w) above += ts.wsum[w];
+    if (above < K && K <= above + local) {
+        int acc = above;
+        for (int j = kBinsPerThread - 1; j >= 0; --j) {
+            const int bj = kBinsPerThread * tid + j;
+            if (acc + ts.hist[bj] >= K) {
+                ts.tb = bj;
+                ts.need = K - acc;
+                ts.cbin = ts.hist[bj];
+                break;
+            }
+            acc += ts.hist[bj];
+        }
+    }
+    __syncthreads();
+    const int tb = ts.tb, need = ts.need, cbin = ts.cbin;
+    if (cbin > kCandMax) {  // crowded threshold bin: exact radix path
+        radix_topk(sc, P, K, sel, ts);
+        if (tid == 0) p.sel_cnt[unit] = K;
+        return;
+    }
+
+    // 4. rank the threshold bin's scores exactly; mark the winners above every bin
+    for (int i = tid; i < P; i += kTopkThreads)
+        if (bin[i] == tb) ts.cand[atomicAdd(&ts.ncand, 1)] = i;
+    __syncthreads();
+    for (int t = tid; t < cbin; t += kTopkThreads) {
+        const int i = ts.cand[t];
+        const float s = sc[i];
+        int rank = 0;
+        for (int j = 0; j < cbin; ++j) {
+            const int i2 = ts.cand[j];
+            const float s2 = sc[i2];
+            rank += (s2 > s) || (s2 == s && i2 < i);
+        }
+        if (rank < need) bin[i] = static_cast<int16_t>(kBins);
+    }
+    __syncthreads();
+
+    // 5. ordered compaction: thread t emits the winners among pages [t*m, t*m + m)
+    const int m = (P + kTopkThreads - 1) / kTopkThreads;
+    const int i0 = min(P, tid * m), i1 = min(P, i0 + m);
+    int mine = 0;
+    for (int i = i0; i < i1; ++i) mine += bin[i] > tb;
+    int pre = mine;  // inclusive prefix within the warp
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int v = __shfl_up_sync(kFullMask, pre, off);
+        if (lane >= off) pre += v;
+    }
+    if (lane == 31) ts.wsum[warp] = pre;
+    __syncthreads();
+    int pos = pre - mine;
+    for (int w = 0; w < warp; ++w) pos += ts.wsum[w];
+    for (int i = i0; i < i1; ++i)
+        if (bin[i] > tb) sel[pos++] = i;
     if (tid == 0) p.sel_cnt[unit] = K;
 }
 
-template <int D, int MODE>
-cudaError_t launch_one(const ScoreParams& p, cudaStream_t stream)
+// one opt-in cache for the (single) selection kernel, shared by every launcher
+cudaError_t allow_topk_smem(size_t bytes)
 {
-    const int smem = chunk_bytes(D);
-    const dim3 grid((p.Pmax + kChunk - 1) / kChunk, p.Hkv, p.B);
-    score_topk_kernel<D, MODE><<<grid, kScoreThreads, smem, stream>>>(p);
-    return cudaGetLastError();
+    static thread_local int dev_cache = -1;
+    static thread_local size_t bytes_cache = 0;
+    return allow_smem(select_topk_kernel, bytes, dev_cache, bytes_cache);
+}
+
+template <int D, int MODE>
+cudaError_t launch_score(const ScoreParams& p, cudaStream_t stream)
+{
+    static thread_local int dev_a = -1;
+    static thread_local size_t bytes_a = 0;
+    const size_t smem = static_cast<size_t>(kStages) * stage_bytes(D);
+    cudaError_t e = allow_smem(score_pages_kernel<D, MODE>, smem, dev_a, bytes_a);
+    if (e != cudaSuccess) return e;
+    int dev = 0, sms = 148, per_sm = 1;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, score_pages_kernel<D, MODE>, kScoreThreads, smem);
+    if (per_sm < 1) per_sm = 1;
+    const long long items = static_cast<long long>(p.B) * p.Hkv * ((p.Pmax + kChunk - 1) / kChunk);
+    const long long slots = static_cast<long long>(sms) * per_sm;
+    const long long grid = items < slots ? items : slots;
+    e = launch_pdl(score_pages_kernel<D, MODE>, dim3(static_cast<unsigned>(grid)), dim3(kScoreThreads), smem, stream, p);
+    if (e != cudaSuccess) return e;
+    const size_t ksmem = static_cast<size_t>(p.Pmax) * (sizeof(float) + sizeof(int16_t));
+    e = allow_topk_smem(ksmem);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(select_topk_kernel, dim3(p.Hkv, p.B), dim3(kTopkThreads), ksmem, stream, p);
 }
 
 }  // namespace
 
 cudaError_t launch_score_topk(const ScoreParams& p, int group_reduce, cudaStream_t stream)
 {
-    if (p.D == 128) return group_reduce ? launch_one<128, 1>(p, stream) : launch_one<128, 0>(p, stream);
-    return group_reduce ? launch_one<64, 1>(p, stream) : launch_one<64, 0>(p, stream);
+    if (p.D == 128) return group_reduce ? launch_score<128, 1>(p, stream) : launch_score<128, 0>(p, stream);
+    return group_reduce ? launch_score<64, 1>(p, stream) : launch_score<64, 0>(p, stream);
 }
 
 // ---------------------------------------------------------------------------

@@ -7,12 +7,14 @@
 // pages are found through [batch, layer, head, logical_block] and null
 // entries are never read.
 //
-// Design (sm_103a).  The unit of work is a 16-token tile of a selected page
-// (one tile per page at T = 16, two at T = 32).  The tiles of one (batch, KV
-// head) are split over `splits` CTAs; inside a CTA each warp walks its own
-// tiles through a private ring of shared-memory slots filled by 1-D bulk
-// copies (TMA, one for K and one for V per tile) on per-slot mbarriers, so
-// copies for the next tiles are in flight while the current one is computed.
+// Design (sm_103a).  The unit of transfer is a 16-token tile of a selected
+// page (one tile per page at T = 16, two at T = 32): its K rows and V rows,
+// each one contiguous 16*D*2-byte block, moved by two 1-D bulk copies (TMA)
+// into shared memory and completing on an mbarrier.  The tiles of one (batch,
+// KV head) are split over `splits` CTAs.  Each warp of a CTA walks its own
+// tiles through a private ring of kRing slots, refilling a slot as soon as it
+// is consumed, and computes two tiles per step (independent MMA chains,
+// one softmax update per 32 tokens).
 //
 // Per tile the GQA group is a small dense contraction and runs on the tensor
 // cores with mma.sync m16n8k16 (bf16 in, fp32 accumulate):
@@ -25,23 +27,40 @@
 // bf16 hi + lo parts (two MMAs) so the probabilities keep ~16 bits, and is
 // moved from the S^T accumulator layout to the B-operand layout with
 // movmatrix.  Softmax statistics are online per warp, merged across warps in
-// shared memory and across splits by the last CTA of the unit.
+// shared memory and across splits by the last CTA of the unit (an atomic
+// ticket; nothing spins).  The kernel is launched with programmatic
+// dependent launch and waits for its predecessor before reading any input.
 #include <cmath>
 
 #include "common.cuh"
 #include "kernels.h"
 
+#ifndef KVMM_ATTN_WARPS
+#define KVMM_ATTN_WARPS 4
+#endif
+#ifndef KVMM_ATTN_RING
+#define KVMM_ATTN_RING 4
+#endif
+
 namespace kvmm {
 namespace {
 
-constexpr int kAttnWarps = 4;
+constexpr int kAttnWarps = KVMM_ATTN_WARPS;
 constexpr int kAttnThreads = kAttnWarps * 32;
-constexpr int kRing = 2;      // slots per warp
-constexpr int kTileTok = 16;  // tokens per tile
+constexpr int kRing = KVMM_ATTN_RING;  // tile slots per warp (>= 2: two tiles per step)
+constexpr int kTileTok = 16;           // tokens per tile
+static_assert(kRing >= 2, "two tiles per step need two slots");
 
 __host__ __device__ constexpr int tile_bytes(int D) { return kTileTok * D * 2; }
 
 __host__ __device__ constexpr size_t ring_bytes(int D) { return size_t(kAttnWarps) * kRing * 2 * tile_bytes(D); }
+
+__host__ __device__ constexpr size_t combine_bytes(int D) { return size_t(kAttnWarps) * 8 * D * sizeof(float); }
+
+__host__ __device__ constexpr size_t ring_region(int D)
+{
+    return ring_bytes(D) > combine_bytes(D) ? ring_bytes(D) : combine_bytes(D);
+}
 
 struct AttnShared {
     uint64_t bar[kAttnWarps][kRing];
@@ -50,11 +69,78 @@ struct AttnShared {
     int last;
 };
 
+// S^T of one tile: c = K_tile Q^T over the head dimension, two MMA chains
+template <int D>
+__device__ __forceinline__ void tile_scores(const uint8_t* ks, const uint32_t (&qf)[D / 32][4], int gid, int tig,
+                                            float (&c)[4])
+{
+    float c2[4] = {0.f, 0.f, 0.f, 0.f};
+    c[0] = c[1] = c[2] = c[3] = 0.f;
+#pragma unroll
+    for (int r = 0; r < D / 32; ++r) {
+        const uint4 ka = ld_shared_v4(ks + gid * (2 * D) + 16 * (4 * r + tig));
+        const uint4 kb = ld_shared_v4(ks + (gid + 8) * (2 * D) + 16 * (4 * r + tig));
+        mma_bf16_16816(c, ka.x, kb.x, ka.y, kb.y, qf[r][0], qf[r][1]);
+        mma_bf16_16816(c2, ka.z, kb.z, ka.w, kb.w, qf[r][2], qf[r][3]);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) c[i] += c2[i];
+}
+
+// O^T += V_tile^T P^T with P split into bf16 hi / lo B fragments
+template <int D>
+__device__ __forceinline__ void tile_accumulate(const uint8_t* vs, int nv, int gid, int tig, uint32_t bh0,
+                                                uint32_t bh1, uint32_t bl0, uint32_t bl1, float (&o)[D / 16][4])
+{
+    constexpr int kDimsPerGroup = D / 8;
+    // lane reads tokens 2tig, 2tig+1, 2tig+8, 2tig+9 at dims [gid*D/8, +D/8)
+    uint32_t wv[4][kDimsPerGroup / 2];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const int tok = 2 * tig + (q & 1) + 8 * (q >> 1);
+        const uint8_t* rowp = vs + tok * (2 * D) + gid * (2 * kDimsPerGroup);
+#pragma unroll
+        for (int c16 = 0; c16 < kDimsPerGroup / 8; ++c16) {
+            const uint4 v = ld_shared_v4(rowp + 16 * c16);
+            wv[q][4 * c16 + 0] = v.x;
+            wv[q][4 * c16 + 1] = v.y;
+            wv[q][4 * c16 + 2] = v.z;
+            wv[q][4 * c16 + 3] = v.w;
+        }
+        if (nv < kTileTok && tok >= nv) {
+#pragma unroll
+            for (int i = 0; i < kDimsPerGroup / 2; ++i) wv[q][i] = 0u;
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < D / 16; ++i) {
+        // m-tile i rows: dim gid*D/8 + 2i (row gid) and +1 (row gid+8)
+        const uint32_t a0 = prmt(wv[0][i], wv[1][i], 0x5410);
+        const uint32_t a1 = prmt(wv[0][i], wv[1][i], 0x7632);
+        const uint32_t a2 = prmt(wv[2][i], wv[3][i], 0x5410);
+        const uint32_t a3 = prmt(wv[2][i], wv[3][i], 0x7632);
+        mma_bf16_16816(o[i], a0, a1, a2, a3, bh0, bh1);
+        mma_bf16_16816(o[i], a0, a1, a2, a3, bl0, bl1);
+    }
+}
+
+// P^T (tokens x heads) of a tile as bf16 hi/lo B fragments for the PV MMA
+__device__ __forceinline__ void p_fragments(float p0, float p1, float p2, float p3, uint32_t& bh0, uint32_t& bh1,
+                                            uint32_t& bl0, uint32_t& bl1)
+{
+    const uint32_t h01 = pack_bf16x2(p0, p1), h23 = pack_bf16x2(p2, p3);
+    const uint32_t r01 = pack_bf16x2(p0 - bf16_lo(h01), p1 - bf16_hi(h01));
+    const uint32_t r23 = pack_bf16x2(p2 - bf16_lo(h23), p3 - bf16_hi(h23));
+    bh0 = movmatrix_trans(h01);
+    bh1 = movmatrix_trans(h23);
+    bl0 = movmatrix_trans(r01);
+    bl1 = movmatrix_trans(r23);
+}
+
 template <int D>
 __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const AttnParams p)
 {
-    constexpr int kChunks = D / 32;   // 16-byte chunk groups per row for the QK fragments
-    constexpr int kMTiles = D / 16;   // m-tiles of O^T
+    constexpr int kMTiles = D / 16;  // m-tiles of O^T
     constexpr int kDimsPerGroup = D / 8;
     extern __shared__ __align__(1024) uint8_t smem[];
     __shared__ AttnShared sh;
@@ -72,12 +158,32 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const AttnPar
     const int tiles_per_page = T / kTileTok;
 
     uint8_t* ring = smem;
-    int64_t* t_row = reinterpret_cast<int64_t*>(smem + ring_bytes(D));
+    int64_t* t_row = reinterpret_cast<int64_t*>(smem + ring_region(D));
     int* t_nv = reinterpret_cast<int*>(t_row + p.max_tiles);
 
     const size_t unit = (static_cast<size_t>(b) * p.L + p.layer) * p.Hkv + h;
     const int wunit = b * p.Hkv + h;
 
+    if (tid < kAttnWarps * kRing) mbar_init(&sh.bar[tid / kRing][tid % kRing], 1);
+    fence_barrier_init();
+
+    pdl_launch_dependents();
+    pdl_wait();  // every input may come from the preceding kernels
+
+    // Q^T as B fragments: lane (gid, tig) holds head gid, 16-byte chunk 4r+tig
+    uint32_t qf[D / 32][4];
+    {
+        const kvmm_bf16* qh = p.q + (static_cast<size_t>(b) * p.Hq + static_cast<size_t>(h) * G + gid) * D;
+#pragma unroll
+        for (int r = 0; r < D / 32; ++r) {
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (gid < G) v = *reinterpret_cast<const uint4*>(qh + 8 * (4 * r + tig));
+            qf[r][0] = v.x;
+            qf[r][1] = v.y;
+            qf[r][2] = v.z;
+            qf[r][3] = v.w;
+        }
+    }
     int seq = p.seq_len[b];
     const int cap = p.Pmax * T;
     if (seq < 0 || seq > cap) {
@@ -118,24 +224,7 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const AttnPar
         t_row[i] = row;
         t_nv[i] = nv;
     }
-    if (tid < kAttnWarps * kRing) mbar_init(&sh.bar[tid / kRing][tid % kRing], 1);
-    fence_barrier_init();
     __syncthreads();
-
-    // Q^T as B fragments: lane (gid, tig) holds head gid, 16-byte chunk 4r+tig
-    uint32_t qf[kChunks][4];
-    {
-        const kvmm_bf16* qh = p.q + (static_cast<size_t>(b) * p.Hq + static_cast<size_t>(h) * G + gid) * D;
-#pragma unroll
-        for (int r = 0; r < kChunks; ++r) {
-            uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (gid < G) v = *reinterpret_cast<const uint4*>(qh + 8 * (4 * r + tig));
-            qf[r][0] = v.x;
-            qf[r][1] = v.y;
-            qf[r][2] = v.z;
-            qf[r][3] = v.w;
-        }
-    }
 
     float o[kMTiles][4];
 #pragma unroll
@@ -147,59 +236,69 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const AttnPar
         while (i < ntile && t_row[i] < 0) i += kAttnWarps;
         return i;
     };
-    auto issue = [&](int i, int slot) {
-        if (lane == 0) {
-            uint8_t* ks = my_ring + static_cast<size_t>(slot) * 2 * tile_bytes(D);
-            const size_t off = static_cast<size_t>(t_row[i]) * D;
-            mbar_arrive_expect_tx(&sh.bar[warp][slot], 2 * tile_bytes(D));
-            bulk_copy_g2s(ks, p.k_pool + off, tile_bytes(D), &sh.bar[warp][slot]);
-            bulk_copy_g2s(ks + tile_bytes(D), p.v_pool + off, tile_bytes(D), &sh.bar[warp][slot]);
+    auto slot_ptr = [&](int ordinal) { return my_ring + static_cast<size_t>(ordinal % kRing) * 2 * tile_bytes(D); };
+
+    // the warp's valid tiles, numbered 0, 1, ...: tile u lives in slot u % kRing
+    int issue_i = next_valid(warp);  // list index of the next tile to fetch
+    int issued = 0, consumed = 0;
+    auto refill = [&]() {
+        while (issued < consumed + kRing && issue_i < ntile) {
+            if (lane == 0) {
+                uint8_t* ks = slot_ptr(issued);
+                uint64_t* bar = &sh.bar[warp][issued % kRing];
+                const size_t off = static_cast<size_t>(t_row[issue_i]) * D;
+                mbar_arrive_expect_tx(bar, 2 * tile_bytes(D));
+                bulk_copy_g2s(ks, p.k_pool + off, tile_bytes(D), bar);
+                bulk_copy_g2s(ks + tile_bytes(D), p.v_pool + off, tile_bytes(D), bar);
+            }
+            ++issued;
+            issue_i = next_valid(issue_i + kAttnWarps);
         }
     };
-
-    int issue_i = warp;
-    int n_issued = 0;
-#pragma unroll
-    for (int s = 0; s < kRing; ++s) {
-        issue_i = next_valid(issue_i);
-        if (issue_i < ntile) {
-            issue(issue_i, s);
-            issue_i += kAttnWarps;
-            ++n_issued;
-        }
-    }
+    refill();
 
     bool timed_out = false;
     int cons_i = warp;
-    for (int v = 0; v < n_issued; ++v) {
-        cons_i = next_valid(cons_i);
-        const int slot = v % kRing;
-        const bool ok = mbar_wait_bounded(&sh.bar[warp][slot], (v / kRing) & 1);
+    while (consumed < issued) {
+        // up to two tiles this step
+        const int i0 = next_valid(cons_i);
+        const bool two = consumed + 1 < issued;
+        const int i1 = two ? next_valid(i0 + kAttnWarps) : i0;
+        bool ok = mbar_wait_bounded(&sh.bar[warp][consumed % kRing], (consumed / kRing) & 1);
+        if (two) ok = mbar_wait_bounded(&sh.bar[warp][(consumed + 1) % kRing], ((consumed + 1) / kRing) & 1) && ok;
         if (__any_sync(kFullMask, !ok)) {  // warp-uniform decision
             timed_out = true;
             break;
         }
-        const uint8_t* ks = my_ring + static_cast<size_t>(slot) * 2 * tile_bytes(D);
-        const uint8_t* vs = ks + tile_bytes(D);
-        const int nv = t_nv[cons_i];
+        const uint8_t* ks0 = slot_ptr(consumed);
+        const uint8_t* ks1 = slot_ptr(consumed + 1);
+        const int nv0 = t_nv[i0];
+        const int nv1 = two ? t_nv[i1] : 0;
 
-        // ---- S^T = K Q^T ------------------------------------------------
-        float c[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int r = 0; r < kChunks; ++r) {
-            const uint4 ka = ld_shared_v4(ks + gid * (2 * D) + 16 * (4 * r + tig));
-            const uint4 kb = ld_shared_v4(ks + (gid + 8) * (2 * D) + 16 * (4 * r + tig));
-            mma_bf16_16816(c, ka.x, kb.x, ka.y, kb.y, qf[r][0], qf[r][1]);
-            mma_bf16_16816(c, ka.z, kb.z, ka.w, kb.w, qf[r][2], qf[r][3]);
+        float ca[4], cb[4];
+        tile_scores<D>(ks0, qf, gid, tig, ca);
+        if (two) {
+            tile_scores<D>(ks1, qf, gid, tig, cb);
+        } else {
+            cb[0] = cb[1] = cb[2] = cb[3] = 0.f;
         }
         // c = S^T[tok gid][head 2tig], [gid][2tig+1], [gid+8][2tig], [gid+8][2tig+1]
-        float x0 = c[0] * p.scale_log2, x1 = c[1] * p.scale_log2;
-        float x2 = c[2] * p.scale_log2, x3 = c[3] * p.scale_log2;
-        if (nv < kTileTok) {
-            if (gid >= nv) x0 = x1 = -INFINITY;
-            if (gid + 8 >= nv) x2 = x3 = -INFINITY;
+        float x[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            x[i] = ca[i] * p.scale_log2;
+            x[4 + i] = cb[i] * p.scale_log2;
         }
-        float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+        if (nv0 < kTileTok) {
+            if (gid >= nv0) x[0] = x[1] = -INFINITY;
+            if (gid + 8 >= nv0) x[2] = x[3] = -INFINITY;
+        }
+        if (nv1 < kTileTok) {  // also masks the absent second tile (nv1 = 0)
+            if (gid >= nv1) x[4] = x[5] = -INFINITY;
+            if (gid + 8 >= nv1) x[6] = x[7] = -INFINITY;
+        }
+        float mx0 = fmaxf(fmaxf(x[0], x[2]), fmaxf(x[4], x[6]));
+        float mx1 = fmaxf(fmaxf(x[1], x[3]), fmaxf(x[5], x[7]));
 #pragma unroll
         for (int off = 4; off < 32; off <<= 1) {
             mx0 = fmaxf(mx0, __shfl_xor_sync(kFullMask, mx0, off));
@@ -209,10 +308,11 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const AttnPar
         const float ref0 = mn0 == -INFINITY ? 0.f : mn0;
         const float ref1 = mn1 == -INFINITY ? 0.f : mn1;
         const float a0 = exp2f(m0 - ref0), a1 = exp2f(m1 - ref1);
-        const float p0 = exp2f(x0 - ref0), p1 = exp2f(x1 - ref1);
-        const float p2 = exp2f(x2 - ref0), p3 = exp2f(x3 - ref1);
-        l0 = fmaf(l0, a0, p0 + p2);
-        l1 = fmaf(l1, a1, p1 + p3);
+        float pr[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) pr[i] = exp2f(x[i] - ((i & 1) ? ref1 : ref0));
+        l0 = fmaf(l0, a0, (pr[0] + pr[2]) + (pr[4] + pr[6]));
+        l1 = fmaf(l1, a1, (pr[1] + pr[3]) + (pr[5] + pr[7]));
         m0 = mn0;
         m1 = mn1;
         if (__any_sync(kFullMask, (a0 != 1.f) || (a1 != 1.f))) {
@@ -225,59 +325,26 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const AttnPar
             }
         }
 
-        // ---- P^T as bf16 hi + lo B fragments ----------------------------
-        const uint32_t h01 = pack_bf16x2(p0, p1), h23 = pack_bf16x2(p2, p3);
-        const uint32_t r01 = pack_bf16x2(p0 - bf16_lo(h01), p1 - bf16_hi(h01));
-        const uint32_t r23 = pack_bf16x2(p2 - bf16_lo(h23), p3 - bf16_hi(h23));
-        const uint32_t bh0 = movmatrix_trans(h01), bh1 = movmatrix_trans(h23);
-        const uint32_t bl0 = movmatrix_trans(r01), bl1 = movmatrix_trans(r23);
-
-        // ---- O^T += V^T P^T ---------------------------------------------
-        // lane reads tokens 2tig, 2tig+1, 2tig+8, 2tig+9 at dims [gid*D/8, +D/8)
-        uint32_t wv[4][kDimsPerGroup / 2];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int tok = 2 * tig + (q & 1) + 8 * (q >> 1);
-            const uint8_t* rowp = vs + tok * (2 * D) + gid * (2 * kDimsPerGroup);
-#pragma unroll
-            for (int c16 = 0; c16 < kDimsPerGroup / 8; ++c16) {
-                const uint4 v = ld_shared_v4(rowp + 16 * c16);
-                wv[q][4 * c16 + 0] = v.x;
-                wv[q][4 * c16 + 1] = v.y;
-                wv[q][4 * c16 + 2] = v.z;
-                wv[q][4 * c16 + 3] = v.w;
-            }
-            if (nv < kTileTok && tok >= nv) {
-#pragma unroll
-                for (int i = 0; i < kDimsPerGroup / 2; ++i) wv[q][i] = 0u;
-            }
-        }
-#pragma unroll
-        for (int i = 0; i < kMTiles; ++i) {
-            // m-tile i rows: dim gid*D/8 + 2i (row gid) and +1 (row gid+8)
-            const uint32_t a0r = prmt(wv[0][i], wv[1][i], 0x5410);
-            const uint32_t a1r = prmt(wv[0][i], wv[1][i], 0x7632);
-            const uint32_t a2r = prmt(wv[2][i], wv[3][i], 0x5410);
-            const uint32_t a3r = prmt(wv[2][i], wv[3][i], 0x7632);
-            mma_bf16_16816(o[i], a0r, a1r, a2r, a3r, bh0, bh1);
-            mma_bf16_16816(o[i], a0r, a1r, a2r, a3r, bl0, bl1);
+        uint32_t bh0, bh1, bl0, bl1;
+        p_fragments(pr[0], pr[1], pr[2], pr[3], bh0, bh1, bl0, bl1);
+        tile_accumulate<D>(ks0 + tile_bytes(D), nv0, gid, tig, bh0, bh1, bl0, bl1, o);
+        if (two) {
+            p_fragments(pr[4], pr[5], pr[6], pr[7], bh0, bh1, bl0, bl1);
+            tile_accumulate<D>(ks1 + tile_bytes(D), nv1, gid, tig, bh0, bh1, bl0, bl1, o);
         }
 
-        // ---- release the slot and refill it ------------------------------
+        // ---- release the slots and refill them ---------------------------
         __syncwarp();
         fence_proxy_async_shared();
-        issue_i = next_valid(issue_i);
-        if (issue_i < ntile) {
-            issue(issue_i, slot);
-            issue_i += kAttnWarps;
-            ++n_issued;
-        }
-        cons_i += kAttnWarps;
+        consumed += two ? 2 : 1;
+        cons_i = (two ? i1 : i0) + kAttnWarps;
+        refill();
     }
     if (timed_out) {
         if (lane == 0) report(p.err, KVMM_ERR_TIMEOUT);
         // let copies still in flight land before the CTA leaves (bounded)
-        for (int v = 0; v < n_issued; ++v) mbar_wait_bounded(&sh.bar[warp][v % kRing], (v / kRing) & 1, 100000000ull);
+        for (int v = consumed; v < issued; ++v)
+            mbar_wait_bounded(&sh.bar[warp][v % kRing], (v / kRing) & 1, 100000000ull);
     }
 
     // ---- merge the warps of this CTA ------------------------------------
@@ -338,16 +405,16 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const AttnPar
     if (single) return;
 
     // ---- last CTA of the unit merges the splits -------------------------
-    __threadfence();
     __syncthreads();
     if (tid == 0) {
+        __threadfence();  // the CTA's partial (ordered before by the barrier) is visible
         const int ticket = atomicAdd(p.counters + wunit, 1);
         sh.last = (ticket == p.splits - 1);
         if (sh.last) p.counters[wunit] = 0;
+        __threadfence();
     }
     __syncthreads();
     if (!sh.last) return;
-    __threadfence();
 
     const float* uo = p.part_o + static_cast<size_t>(wunit) * p.splits * G * D;
     const float* uml = p.part_ml + static_cast<size_t>(wunit) * p.splits * G * 2;
@@ -374,32 +441,19 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const AttnPar
 template <int D>
 cudaError_t launch_attn(const AttnParams& p, cudaStream_t stream)
 {
+    static thread_local int dev_cache = -1;
+    static thread_local size_t bytes_cache = 0;
     const size_t smem = attention_smem_bytes(D, p.max_tiles);
-    // opt in to the dynamic shared memory this launch needs (once per device and size)
-    static thread_local int configured_device = -1;
-    static thread_local size_t configured_bytes = 0;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (smem > 48 * 1024 && (configured_device != dev || configured_bytes < smem)) {
-        cudaError_t e = cudaFuncSetAttribute(sparse_attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(smem));
-        if (e != cudaSuccess) return e;
-        configured_device = dev;
-        configured_bytes = smem;
-    }
-    const dim3 grid(p.splits, p.Hkv, p.B);
-    sparse_attn_kernel<D><<<grid, kAttnThreads, smem, stream>>>(p);
-    return cudaGetLastError();
+    cudaError_t e = allow_smem(sparse_attn_kernel<D>, smem, dev_cache, bytes_cache);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(sparse_attn_kernel<D>, dim3(p.splits, p.Hkv, p.B), dim3(kAttnThreads), smem, stream, p);
 }
 
 }  // namespace
 
 size_t attention_smem_bytes(int D, int max_tiles)
 {
-    const size_t ring = ring_bytes(D);
-    const size_t combine = size_t(kAttnWarps) * 8 * D * sizeof(float);
-    const size_t base = ring > combine ? ring : combine;
-    return base + size_t(max_tiles) * (sizeof(int64_t) + sizeof(int));
+    return ring_region(D) + size_t(max_tiles) * (sizeof(int64_t) + sizeof(int));
 }
 
 int attention_slots_per_unit(const kvmm_shape& s)
@@ -409,10 +463,10 @@ int attention_slots_per_unit(const kvmm_shape& s)
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const int tiles = s.Kmax * (s.T / kTileTok);
     // CTAs resident per SM are bounded by the ring (shared memory) of each CTA
-    const size_t per_cta = attention_smem_bytes(s.D, tiles) + 1024;
+    const size_t per_cta = attention_smem_bytes(s.D, tiles) + sizeof(AttnShared) + 1024;
     int per_sm = static_cast<int>((228u * 1024u) / per_cta);
     if (per_sm < 1) per_sm = 1;
-    if (per_sm > 4) per_sm = 4;
+    if (per_sm > 8) per_sm = 8;
     const long long slots = static_cast<long long>(sms) * per_sm;
     const long long units = static_cast<long long>(s.B) * s.Hkv;
     long long splits = slots / units;
