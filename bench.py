@@ -277,8 +277,13 @@ def gpu_arm(args):
     stream = torch.cuda.Stream()
 
     ev_s, external = make_timing_events(4 * L)
+    # the promotion diff is not needed by attention: it runs on a side stream
+    # forked after each selection and joined at the end of the step
+    side = torch.cuda.Stream()
+    forks = [torch.cuda.Event() for _ in range(L)]
 
     def step(instrument):
+        main = torch.cuda.current_stream()
         for l in range(L):
             kvmm.kv_minmax_update(st.shape, l, nk_dev[l], nv_dev[l], 1, st.tok_begin, st.seq_len, st.k_pool,
                                   st.v_pool, st.block_table, st.meta, st.err)
@@ -287,12 +292,16 @@ def gpu_arm(args):
             st.select(l, q_dev[l])
             if instrument:
                 ev_s[4 * l + 1].record()
-            st.diff(l)
+            forks[l].record(main)
+            side.wait_event(forks[l])
+            with torch.cuda.stream(side):
+                st.diff(l)
             if instrument:
                 ev_s[4 * l + 2].record()
             st.attend(l, q_dev[l])
             if instrument:
                 ev_s[4 * l + 3].record()
+        main.wait_stream(side)
 
     torch.cuda.empty_cache()
     with torch.cuda.stream(stream):
@@ -428,7 +437,7 @@ def gpu_arm(args):
         "e2e": {"value": e2e_steps * L * world / (e2e_ms / 1e3), "unit": "layer-steps/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "how": "pinned host q/new K,V -> device, graph replay, out/lse/promoted counts -> pinned host"},
-        "gpu_launches": 4 * L * args.steps,
+        "gpu_launches": 5 * L * args.steps,  # update, score, top-K, diff, attention per layer
         "clocks": clk,
         "device_err": err_word,
     }

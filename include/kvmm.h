@@ -82,7 +82,9 @@ typedef struct kvmm_shape {
 } kvmm_shape;
 
 /* Array layouts (all row-major):
- *   k_pool, v_pool   [n_phys][T][D]            bf16
+ *   k_pool           [n_phys][T][D]            bf16, a page's keys token by token
+ *   v_pool           [n_phys][D][T]            bf16, a page's values dimension by dimension
+ *                                              (the value cache layout of paged serving engines)
  *   block_table      [B][L][Hkv][Pmax]         int32, -1 = null block
  *   meta             [B][L][Hkv][Pmax][2][D]   bf16, [..][0][d] = min, [..][1][d] = max
  *   q                [B][Hq][D]                bf16 (the layer being decoded)
@@ -103,9 +105,10 @@ typedef struct kvmm_shape {
  * not) and is indexed by logical page.
  *
  * For each batch b, with n = tok_end[b] - tok_begin[b] (0 <= n <= n_new):
- *   - if new_k and new_v are given ([B][Hkv][n_new][D] bf16 each), token
- *     tok_begin[b] + j of every KV head of `layer` takes row j of new_k /
- *     new_v, written into its physical page through block_table;
+ *   - if new_k and new_v are given ([B][Hkv][n_new][D] bf16 each, token by
+ *     token), token tok_begin[b] + j of every KV head of `layer` takes row j
+ *     of new_k / new_v, written into its physical page through block_table
+ *     (keys as a row of the page, values as a column of the page's [D][T]);
  *   - if both are NULL nothing is written (metadata rebuild only; n_new is
  *     then only an upper bound on n and may be as large as Pmax*T);
  *   - for every logical page p with [p*T, (p+1)*T) meeting
@@ -201,12 +204,14 @@ kvmm_status page_score_topk_static_scratch(const kvmm_shape* shape, int32_t laye
  *     lse[b][g]  = m + log(sum_t exp(z_t - m))
  * accumulated in fp32.  sm_scale <= 0 means 1/sqrt(D).  A unit with no
  * valid token yields out = 0 and lse = -inf.  The selection is split over
- * num_splits CTAs per unit (0 = chosen from the GPU's SM count) and the
- * partial results are merged by their log-sum-exp.  A selected page whose
- * entry is null or out of range, or whose index is >= the unit's page
- * count, sets its error bit and contributes nothing.  lse may be NULL.
- * workspace as for page_score_topk, of kvmm_workspace_size(shape,
- * num_splits) bytes.
+ * num_splits CTAs per unit, which form one thread-block cluster and merge
+ * their partial results by log-sum-exp in distributed shared memory
+ * (0 = chosen from the GPU's SM count; explicit values are clamped to
+ * [1, min(16, Kmax)], and a value the device cannot co-schedule returns
+ * KVMM_UNSUPPORTED_SHAPE).  A selected page whose entry is null or out of
+ * range, or whose index is >= the unit's page count, sets its error bit and
+ * contributes nothing.  lse may be NULL.  workspace / workspace_bytes are
+ * not used by this call (kept for the stable signature) and may be NULL / 0.
  */
 kvmm_status sparse_paged_decode_attn(const kvmm_shape* shape, int32_t layer, const kvmm_bf16* q,
                                      const kvmm_bf16* k_pool, const kvmm_bf16* v_pool,
@@ -244,9 +249,9 @@ kvmm_status topk_promotion_diff(const kvmm_shape* shape, int32_t layer,
                                 int32_t* promoted_cnt, int32_t* evicted, int32_t* evicted_cnt,
                                 int32_t* total_promoted, int32_t* err, kvmm_stream stream);
 
-/* Workspace bytes that page_score_topk and sparse_paged_decode_attn (with
- * this num_splits; 0 = automatic) need; one workspace serves both calls as
- * long as they do not run concurrently.  Returns 0 for an unsupported shape. */
+/* Workspace bytes that page_score_topk needs (sparse_paged_decode_attn needs
+ * none; num_splits is accepted for the stable signature and ignored).
+ * Returns 0 for an unsupported shape. */
 size_t kvmm_workspace_size(const kvmm_shape* shape, int32_t num_splits);
 
 /* Number of splits per unit that sparse_paged_decode_attn uses for

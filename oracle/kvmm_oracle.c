@@ -43,6 +43,10 @@
  *     a unit with no valid token yields output 0 and lse = -inf.
  *
  * bf16 values are passed as their raw 16-bit patterns (uint16_t).
+ *
+ * Pool layouts: k_pool is [n_phys][T][D] (token-major); v_pool is
+ * [n_phys][D][T] (each page's values stored dimension-major, as paged
+ * serving engines lay out the value cache).
  */
 #include <math.h>
 #include <stdint.h>
@@ -113,7 +117,7 @@ int32_t oracle_unit_append(uint16_t* k_pool, uint16_t* v_pool, int64_t n_phys, i
         int64_t row = phys * T + (t % T);
         for (int32_t d = 0; d < D; ++d) {
             k_pool[row * D + d] = new_k[(int64_t)(t - tok_begin) * D + d];
-            v_pool[row * D + d] = new_v[(int64_t)(t - tok_begin) * D + d];
+            v_pool[(phys * D + d) * T + (t % T)] = new_v[(int64_t)(t - tok_begin) * D + d];
         }
     }
     return err;
@@ -241,13 +245,13 @@ int32_t oracle_set_difference(const int32_t* a, int32_t na, const int32_t* b, in
 }
 
 /* ---------------------------------------------------------------------------
- * Softmax attention of G query heads over an explicit list of n key/value
- * rows (row indices into the pools, in the order given):
+ * Softmax attention of G query heads over an explicit list of n tokens
+ * (rows[t] = phys * T + r: token r of physical page phys, in the order given):
  *     z_t = scale * sum_d q[g][d] * k_t[d]
  *     out[g] = sum_t exp(z_t - m) v_t / sum_t exp(z_t - m),   m = max_t z_t
  *     lse[g] = m + log(sum_t exp(z_t - m))
  */
-static void attend_rows(const uint16_t* q, int32_t G, int32_t D, const uint16_t* k_pool,
+static void attend_rows(const uint16_t* q, int32_t G, int32_t D, int32_t T, const uint16_t* k_pool,
                         const uint16_t* v_pool, const int64_t* rows, int64_t n, double scale,
                         double* out, double* lse)
 {
@@ -271,7 +275,8 @@ static void attend_rows(const uint16_t* q, int32_t G, int32_t D, const uint16_t*
         for (int64_t t = 0; t < n; ++t) {
             double w = exp(z[t] - m);
             denom += w;
-            for (int32_t d = 0; d < D; ++d) o[d] += w * bf16_value(v_pool[rows[t] * D + d]);
+            int64_t phys = rows[t] / T, r = rows[t] % T;
+            for (int32_t d = 0; d < D; ++d) o[d] += w * bf16_value(v_pool[(phys * D + d) * T + r]);
         }
         for (int32_t d = 0; d < D; ++d) o[d] /= denom;
         lse[g] = m + log(denom);
@@ -300,7 +305,7 @@ int32_t oracle_unit_sparse_attention(const uint16_t* q, int32_t G, int32_t D, in
         if (phys < 0) continue;
         for (int32_t r = 0; r < nv; ++r) rows[n++] = phys * T + r;
     }
-    attend_rows(q, G, D, k_pool, v_pool, rows, n, scale, out, lse);
+    attend_rows(q, G, D, T, k_pool, v_pool, rows, n, scale, out, lse);
     free(rows);
     return err;
 }
@@ -321,7 +326,7 @@ int32_t oracle_unit_dense_attention(const uint16_t* q, int32_t G, int32_t D, int
         if (phys < 0) continue;
         rows[n++] = phys * T + (t % T);
     }
-    attend_rows(q, G, D, k_pool, v_pool, rows, n, scale, out, lse);
+    attend_rows(q, G, D, T, k_pool, v_pool, rows, n, scale, out, lse);
     free(rows);
     return err;
 }

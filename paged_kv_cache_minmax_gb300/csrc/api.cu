@@ -41,20 +41,11 @@ kvmm_status check_shape(const kvmm_shape* s)
 
 int resolve_splits(const kvmm_shape& s, int32_t num_splits)
 {
-    const int tiles = s.Kmax * (s.T / 16);
     int splits = num_splits > 0 ? num_splits : kvmm::attention_slots_per_unit(s);
-    if (splits > tiles) splits = tiles;
+    if (splits > kvmm::kAttnMaxSplits) splits = kvmm::kAttnMaxSplits;
+    if (splits > s.Kmax) splits = s.Kmax;
     if (splits < 1) splits = 1;
     return splits;
-}
-
-size_t attention_ws_bytes(const kvmm_shape& s, int splits)
-{
-    const size_t units = size_t(s.B) * s.Hkv;
-    const int G = s.Hq / s.Hkv;
-    const size_t po = units * splits * G * s.D * sizeof(float);
-    const size_t pml = units * splits * G * 2 * sizeof(float);
-    return kvmm::ws_counter_bytes(s) + ((po + 255) & ~size_t(255)) + pml;
 }
 
 size_t score_ws_bytes(const kvmm_shape& s)
@@ -101,9 +92,7 @@ int32_t kvmm_auto_splits(const kvmm_shape* shape)
 size_t kvmm_workspace_size(const kvmm_shape* shape, int32_t num_splits)
 {
     if (check_shape(shape) != KVMM_OK || num_splits < 0) return 0;
-    const size_t a = attention_ws_bytes(*shape, resolve_splits(*shape, num_splits));
-    const size_t b = score_ws_bytes(*shape);
-    return a > b ? a : b;
+    return score_ws_bytes(*shape);  // attention merges its splits on chip and needs none
 }
 
 kvmm_status kv_minmax_update(const kvmm_shape* shape, int32_t layer, const kvmm_bf16* new_k,
@@ -248,12 +237,12 @@ kvmm_status sparse_paged_decode_attn(const kvmm_shape* shape, int32_t layer, con
     if (!req(q) || !req(k_pool) || !req(v_pool) || !req4(block_table) || !req4(seq_len) || !req4(sel_idx) ||
         !req4(sel_cnt) || !req4(out) || !opt4(lse) || !opt4(err))
         return KVMM_INVALID_ARG;
+    (void)workspace;
+    (void)workspace_bytes;
     const int splits = resolve_splits(s, num_splits);
-    if (splits > 1 && !req(workspace)) return KVMM_INVALID_ARG;
-    if (splits > 1 && workspace_bytes < attention_ws_bytes(s, splits)) return KVMM_WORKSPACE_TOO_SMALL;
-    const int tiles = s.Kmax * (s.T / 16);
-    const int max_tiles = (tiles + splits - 1) / splits;
-    if (kvmm::attention_smem_bytes(s.D, max_tiles) > 227 * 1024) return KVMM_UNSUPPORTED_SHAPE;
+    if (num_splits > 0 && splits > kvmm::attention_max_splits(s)) return KVMM_UNSUPPORTED_SHAPE;
+    const int max_pages = (s.Kmax + splits - 1) / splits;  // selected pages one CTA may hold
+    if (kvmm::attention_smem_bytes(s.D, max_pages) > 200 * 1024) return KVMM_UNSUPPORTED_SHAPE;
     AttnParams p{};
     p.B = s.B;
     p.L = s.L;
@@ -266,7 +255,7 @@ kvmm_status sparse_paged_decode_attn(const kvmm_shape* shape, int32_t layer, con
     p.Kmax = s.Kmax;
     p.layer = layer;
     p.splits = splits;
-    p.max_tiles = max_tiles;
+    p.max_tiles = max_pages;
     p.n_phys = s.n_phys;
     p.scale_log2 = (sm_scale > 0.f ? sm_scale : 1.0f / std::sqrt(static_cast<float>(s.D))) * 1.4426950408889634f;
     p.q = q;
@@ -278,14 +267,6 @@ kvmm_status sparse_paged_decode_attn(const kvmm_shape* shape, int32_t layer, con
     p.sel_cnt = sel_cnt;
     p.out = out;
     p.lse = lse;
-    uint8_t* ws = static_cast<uint8_t*>(workspace);
-    p.counters = reinterpret_cast<int32_t*>(ws);
-    if (splits > 1) {
-        const size_t units = size_t(s.B) * s.Hkv;
-        const size_t po = units * splits * p.G * s.D * sizeof(float);
-        p.part_o = reinterpret_cast<float*>(ws + kvmm::ws_counter_bytes(s));
-        p.part_ml = reinterpret_cast<float*>(ws + kvmm::ws_counter_bytes(s) + ((po + 255) & ~size_t(255)));
-    }
     p.err = err;
     return launched(kvmm::launch_sparse_attention(p, reinterpret_cast<cudaStream_t>(stream)));
 }

@@ -111,6 +111,33 @@ __device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t threads
 }
 
 // ---------------------------------------------------------------------------
+// thread-block clusters and distributed shared memory
+__device__ __forceinline__ uint32_t cluster_ctarank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// every thread of every CTA of the cluster arrives and waits; release/acquire
+// make each CTA's earlier shared-memory writes visible to the others
+__device__ __forceinline__ void cluster_sync()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// load a float from the shared memory of CTA `rank` of the cluster, at the
+// address that `local` has in this CTA's shared memory
+__device__ __forceinline__ float ld_dsmem_f32(const void* local, uint32_t rank)
+{
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(local)), "r"(rank));
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+    return v;
+}
+
+// ---------------------------------------------------------------------------
 // programmatic dependent launch: the next kernel in the stream may be
 // scheduled once every CTA of this one has called launch_dependents; a kernel
 // must call wait before touching memory its predecessor writes (or reads).

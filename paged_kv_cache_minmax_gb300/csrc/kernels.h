@@ -51,8 +51,8 @@ struct ScoreParams {
 
 struct AttnParams {
     int32_t B, L, Hq, Hkv, G, D, T, Pmax, Kmax, layer;
-    int32_t splits;      // CTAs per unit
-    int32_t max_tiles;   // upper bound of 16-token tiles handled by one CTA
+    int32_t splits;      // CTAs per unit (one cluster)
+    int32_t max_tiles;   // upper bound of selected pages handled by one CTA
     int64_t n_phys;
     float scale_log2;    // sm_scale * log2(e)
     const kvmm_bf16* q;
@@ -64,9 +64,6 @@ struct AttnParams {
     const int32_t* sel_cnt;
     float* out;
     float* lse;
-    int32_t* counters;   // workspace: [B*Hkv]
-    float* part_o;       // workspace: [B*Hkv][splits][G][D]
-    float* part_ml;      // workspace: [B*Hkv][splits][G][2]
     int32_t* err;
 };
 
@@ -105,6 +102,29 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// As launch_pdl, with the grid tiled into thread-block clusters of
+// `cluster_x` x 1 x 1 CTAs.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                               unsigned cluster_x, Args&&... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = cluster_x;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 // Raise a kernel's dynamic shared-memory limit to `bytes` (once per device and
 // size; the default 48 KiB limit counts static shared memory too).
 template <typename Kernel>
@@ -136,7 +156,9 @@ constexpr size_t kStaticScratchCounterBytes = size_t(16) << 10;
 cudaError_t static_scratch_for_current_device(void** ptr, cudaStream_t stream);
 
 // Attention launch geometry for the current device.
+constexpr int kAttnMaxSplits = 16;                   // CTAs of a unit form one cluster
 int attention_slots_per_unit(const kvmm_shape& s);  // automatic split count
-size_t attention_smem_bytes(int D, int max_tiles);
+int attention_max_splits(const kvmm_shape& s);      // largest launchable cluster (<= kAttnMaxSplits)
+size_t attention_smem_bytes(int D, int max_pages);
 
 }  // namespace kvmm

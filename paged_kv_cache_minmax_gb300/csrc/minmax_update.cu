@@ -5,7 +5,8 @@
 // keys, in metadata held apart from the page itself.
 //
 // One warp owns one (batch, KV head, logical page) touched by the update.
-// It writes the new rows of that page through the head-level block table,
+// It writes the new rows of that page through the head-level block table
+// (keys as rows of the page's [T][D], values as columns of its [D][T]),
 // then re-reads the page's valid rows with 16-byte coalesced loads and
 // reduces them.  min/max run on order-preserving 16-bit keys (two channels
 // per 32-bit word, SIMD min/max), so -0 sorts below +0 and the result is a
@@ -84,7 +85,12 @@ __global__ void __launch_bounds__(kUpdWarps * 32) minmax_update_kernel(const Upd
             const uint4 kv = reinterpret_cast<const uint4*>(p.new_k + j * D)[sub];
             const uint4 vv = reinterpret_cast<const uint4*>(p.new_v + j * D)[sub];
             reinterpret_cast<uint4*>(kpage + static_cast<size_t>(r) * D)[sub] = kv;
-            reinterpret_cast<uint4*>(vpage + static_cast<size_t>(r) * D)[sub] = vv;
+            // values are stored dimension-major: channel d of token r at vpage[d * T + r]
+            const uint32_t vw[4] = {vv.x, vv.y, vv.z, vv.w};
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                vpage[static_cast<size_t>(8 * sub + e) * T + r] =
+                    static_cast<kvmm_bf16>((e & 1) ? (vw[e >> 1] >> 16) : (vw[e >> 1] & 0xffffu));
         }
         __syncwarp();  // the rows just written are read back below by other lanes
     }

@@ -7,29 +7,30 @@
 // pages are found through [batch, layer, head, logical_block] and null
 // entries are never read.
 //
-// Design (sm_103a).  The unit of transfer is a 16-token tile of a selected
-// page (one tile per page at T = 16, two at T = 32): its K rows and V rows,
-// each one contiguous 16*D*2-byte block, moved by two 1-D bulk copies (TMA)
-// into shared memory and completing on an mbarrier.  The tiles of one (batch,
-// KV head) are split over `splits` CTAs.  Each warp of a CTA walks its own
-// tiles through a private ring of kRing slots, refilling a slot as soon as it
-// is consumed, and computes two tiles per step (independent MMA chains,
-// one softmax update per 32 tokens).
+// Design (sm_103a).  The selected pages of one (batch, KV head) are split
+// over `splits` CTAs.  A CTA first resolves its pages through the block table
+// into a compacted list (null / out-of-range entries dropped and reported),
+// then its warps take steps of 32 tokens (two 16-token pages or one 32-token
+// page) round robin.  Each warp keeps two steps in flight in a private ring:
+// every page's K block ([T][D]) and V block ([D][T]) is one contiguous run of
+// bytes, moved by a 1-D bulk copy (TMA) into shared memory, the copies of a
+// step issued from different lanes and completing on one mbarrier.
 //
-// Per tile the GQA group is a small dense contraction and runs on the tensor
-// cores with mma.sync m16n8k16 (bf16 in, fp32 accumulate):
-//   S^T[16 tok x 8 head]  = K_tile[16 x D] * Q^T[D x 8]            (D/16 MMAs)
-//   O^T[D x 8 head]      += V_tile^T[D x 16] * P^T[16 x 8]          (2*D/16 MMAs)
-// The K and V fragments are read straight from the bulk-copied row-major
-// tile with 16-byte shared loads; the head dimension is visited in a fixed
-// permuted order that is the same for Q and K (so S is unchanged) and is
-// undone when O is written.  P = exp2(S*scale*log2e - m) is split into
-// bf16 hi + lo parts (two MMAs) so the probabilities keep ~16 bits, and is
-// moved from the S^T accumulator layout to the B-operand layout with
-// movmatrix.  Softmax statistics are online per warp, merged across warps in
-// shared memory and across splits by the last CTA of the unit (an atomic
-// ticket; nothing spins).  The kernel is launched with programmatic
-// dependent launch and waits for its predecessor before reading any input.
+// Per 16-token sub-tile the GQA group is a small dense contraction on the
+// tensor cores (mma.sync m16n8k16, bf16 in, fp32 accumulate):
+//   S^T[16 tok x 8 head] = K[16 x D] * Q^T[D x 8]          (D/16 MMAs)
+//   O^T[D x 8 head]     += V^T[D x 16] * P^T[16 x 8]        (2*D/16 MMAs)
+// Tokens and head dimensions are visited in fixed permuted orders (the same
+// on both sides of each contraction): a lane's K fragment is a 16-byte load
+// of two token rows, and, because values are stored dimension-major, a lane's
+// V^T fragments for both sub-tiles of a step are one 16-byte load per
+// dimension row.  P = exp2(S*scale*log2e - m) is split into bf16 hi + lo parts
+// (two MMAs) so the probabilities keep ~16 bits, and is moved from the S^T
+// accumulator layout to the B-operand layout with movmatrix.  Softmax
+// statistics are online per warp, merged across warps in shared memory and
+// across splits by the last CTA of the unit (an atomic ticket; nothing
+// spins).  The kernel is launched with programmatic dependent launch and
+// waits for its predecessor before reading any input.
 #include <cmath>
 
 #include "common.cuh"
@@ -38,8 +39,8 @@
 #ifndef KVMM_ATTN_WARPS
 #define KVMM_ATTN_WARPS 4
 #endif
-#ifndef KVMM_ATTN_RING
-#define KVMM_ATTN_RING 4
+#ifndef KVMM_ATTN_STEPS
+#define KVMM_ATTN_STEPS 2
 #endif
 
 namespace kvmm {
@@ -47,101 +48,49 @@ namespace {
 
 constexpr int kAttnWarps = KVMM_ATTN_WARPS;
 constexpr int kAttnThreads = kAttnWarps * 32;
-constexpr int kRing = KVMM_ATTN_RING;  // tile slots per warp (>= 2: two tiles per step)
-constexpr int kTileTok = 16;           // tokens per tile
-static_assert(kRing >= 2, "two tiles per step need two slots");
+constexpr int kSteps = KVMM_ATTN_STEPS;  // steps in flight per warp
+constexpr int kStepTok = 32;             // tokens per step (two 16-token sub-tiles)
+static_assert(kSteps >= 2, "double buffering needs two steps");
 
-__host__ __device__ constexpr int tile_bytes(int D) { return kTileTok * D * 2; }
-
-__host__ __device__ constexpr size_t ring_bytes(int D) { return size_t(kAttnWarps) * kRing * 2 * tile_bytes(D); }
-
+__host__ __device__ constexpr int step_bytes(int D) { return 2 * kStepTok * D * 2; }  // K then V
+__host__ __device__ constexpr size_t ring_bytes(int D) { return size_t(kAttnWarps) * kSteps * step_bytes(D); }
 __host__ __device__ constexpr size_t combine_bytes(int D) { return size_t(kAttnWarps) * 8 * D * sizeof(float); }
-
 __host__ __device__ constexpr size_t ring_region(int D)
 {
     return ring_bytes(D) > combine_bytes(D) ? ring_bytes(D) : combine_bytes(D);
 }
 
+constexpr int kMaxSplits = kAttnMaxSplits;  // CTAs of one unit = one thread-block cluster
+
 struct AttnShared {
-    uint64_t bar[kAttnWarps][kRing];
+    uint64_t bar[kAttnWarps][kSteps];
     float m[kAttnWarps][8];
     float l[kAttnWarps][8];
-    int last;
+    float f[kMaxSplits][kAttnWarps][8];  // weight of each partial in the merge
+    float inv_l[8];
+    float lse[8];
+    int wcount[kAttnWarps];
 };
 
-// S^T of one tile: c = K_tile Q^T over the head dimension, two MMA chains
-template <int D>
-__device__ __forceinline__ void tile_scores(const uint8_t* ks, const uint32_t (&qf)[D / 32][4], int gid, int tig,
-                                            float (&c)[4])
+__device__ __forceinline__ float fast_exp2(float x)
 {
-    float c2[4] = {0.f, 0.f, 0.f, 0.f};
-    c[0] = c[1] = c[2] = c[3] = 0.f;
-#pragma unroll
-    for (int r = 0; r < D / 32; ++r) {
-        const uint4 ka = ld_shared_v4(ks + gid * (2 * D) + 16 * (4 * r + tig));
-        const uint4 kb = ld_shared_v4(ks + (gid + 8) * (2 * D) + 16 * (4 * r + tig));
-        mma_bf16_16816(c, ka.x, kb.x, ka.y, kb.y, qf[r][0], qf[r][1]);
-        mma_bf16_16816(c2, ka.z, kb.z, ka.w, kb.w, qf[r][2], qf[r][3]);
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) c[i] += c2[i];
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
-// O^T += V_tile^T P^T with P split into bf16 hi / lo B fragments
-template <int D>
-__device__ __forceinline__ void tile_accumulate(const uint8_t* vs, int nv, int gid, int tig, uint32_t bh0,
-                                                uint32_t bh1, uint32_t bl0, uint32_t bl1, float (&o)[D / 16][4])
+// keep the bf16 halves of w whose tokens are valid
+__device__ __forceinline__ uint32_t keep_halves(uint32_t w, bool lo, bool hi)
 {
-    constexpr int kDimsPerGroup = D / 8;
-    // lane reads tokens 2tig, 2tig+1, 2tig+8, 2tig+9 at dims [gid*D/8, +D/8)
-    uint32_t wv[4][kDimsPerGroup / 2];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const int tok = 2 * tig + (q & 1) + 8 * (q >> 1);
-        const uint8_t* rowp = vs + tok * (2 * D) + gid * (2 * kDimsPerGroup);
-#pragma unroll
-        for (int c16 = 0; c16 < kDimsPerGroup / 8; ++c16) {
-            const uint4 v = ld_shared_v4(rowp + 16 * c16);
-            wv[q][4 * c16 + 0] = v.x;
-            wv[q][4 * c16 + 1] = v.y;
-            wv[q][4 * c16 + 2] = v.z;
-            wv[q][4 * c16 + 3] = v.w;
-        }
-        if (nv < kTileTok && tok >= nv) {
-#pragma unroll
-            for (int i = 0; i < kDimsPerGroup / 2; ++i) wv[q][i] = 0u;
-        }
-    }
-#pragma unroll
-    for (int i = 0; i < D / 16; ++i) {
-        // m-tile i rows: dim gid*D/8 + 2i (row gid) and +1 (row gid+8)
-        const uint32_t a0 = prmt(wv[0][i], wv[1][i], 0x5410);
-        const uint32_t a1 = prmt(wv[0][i], wv[1][i], 0x7632);
-        const uint32_t a2 = prmt(wv[2][i], wv[3][i], 0x5410);
-        const uint32_t a3 = prmt(wv[2][i], wv[3][i], 0x7632);
-        mma_bf16_16816(o[i], a0, a1, a2, a3, bh0, bh1);
-        mma_bf16_16816(o[i], a0, a1, a2, a3, bl0, bl1);
-    }
+    return w & ((lo ? 0x0000ffffu : 0u) | (hi ? 0xffff0000u : 0u));
 }
 
-// P^T (tokens x heads) of a tile as bf16 hi/lo B fragments for the PV MMA
-__device__ __forceinline__ void p_fragments(float p0, float p1, float p2, float p3, uint32_t& bh0, uint32_t& bh1,
-                                            uint32_t& bl0, uint32_t& bl1)
-{
-    const uint32_t h01 = pack_bf16x2(p0, p1), h23 = pack_bf16x2(p2, p3);
-    const uint32_t r01 = pack_bf16x2(p0 - bf16_lo(h01), p1 - bf16_hi(h01));
-    const uint32_t r23 = pack_bf16x2(p2 - bf16_lo(h23), p3 - bf16_hi(h23));
-    bh0 = movmatrix_trans(h01);
-    bh1 = movmatrix_trans(h23);
-    bl0 = movmatrix_trans(r01);
-    bl1 = movmatrix_trans(r23);
-}
-
-template <int D>
+template <int D, int T>
 __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const AttnParams p)
 {
-    constexpr int kMTiles = D / 16;  // m-tiles of O^T
-    constexpr int kDimsPerGroup = D / 8;
+    constexpr int kPPS = kStepTok / T;      // pages per step
+    constexpr int kPageBytes = T * D * 2;   // a page's K (or V) block
+    constexpr int kMTiles = D / 16;         // m-tiles of O^T
     extern __shared__ __align__(1024) uint8_t smem[];
     __shared__ AttnShared sh;
 
@@ -154,19 +103,16 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const AttnPar
     const int h = blockIdx.y;
     const int b = blockIdx.z;
     const int G = p.G;
-    const int T = p.T;
-    const int tiles_per_page = T / kTileTok;
 
     uint8_t* ring = smem;
-    int64_t* t_row = reinterpret_cast<int64_t*>(smem + ring_region(D));
-    int* t_nv = reinterpret_cast<int*>(t_row + p.max_tiles);
+    int64_t* pg_row = reinterpret_cast<int64_t*>(smem + ring_region(D));  // physical page of list entry
+    int* pg_nv = reinterpret_cast<int*>(pg_row + p.max_tiles);            // its valid tokens
 
     const size_t unit = (static_cast<size_t>(b) * p.L + p.layer) * p.Hkv + h;
     const int wunit = b * p.Hkv + h;
 
-    if (tid < kAttnWarps * kRing) mbar_init(&sh.bar[tid / kRing][tid % kRing], 1);
+    if (tid < kAttnWarps * kSteps) mbar_init(&sh.bar[tid / kSteps][tid % kSteps], 1);
     fence_barrier_init();
-
     pdl_launch_dependents();
     pdl_wait();  // every input may come from the preceding kernels
 
@@ -184,6 +130,7 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const AttnPar
             qf[r][3] = v.w;
         }
     }
+
     int seq = p.seq_len[b];
     const int cap = p.Pmax * T;
     if (seq < 0 || seq > cap) {
@@ -196,109 +143,125 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const AttnPar
         if (split == 0 && tid == 0) report(p.err, KVMM_ERR_OUT_OF_RANGE);
         cnt = cnt < 0 ? 0 : p.Kmax;
     }
-    const int tiles = cnt * tiles_per_page;
-    const int beg = static_cast<int>(static_cast<long long>(tiles) * split / p.splits);
-    const int end = static_cast<int>(static_cast<long long>(tiles) * (split + 1) / p.splits);
-    const int ntile = end - beg;
+    const int beg = static_cast<int>(static_cast<long long>(cnt) * split / p.splits);
+    const int end = static_cast<int>(static_cast<long long>(cnt) * (split + 1) / p.splits);
 
-    // resolve this CTA's tiles through the selection and the block table
-    for (int i = tid; i < ntile; i += kAttnThreads) {
-        const int t = beg + i;
-        const int lp = p.sel_idx[unit * p.Kmax + t / tiles_per_page];
-        const int first = lp * T + (t % tiles_per_page) * kTileTok;
+    // resolve this CTA's pages and compact the valid ones (in selection order)
+    int n_valid = 0;
+    for (int i0 = beg; i0 < end; i0 += kAttnThreads) {
+        const int i = i0 + tid;
         int64_t row = -1;
         int nv = 0;
-        if (lp < 0 || lp >= P) {
-            report(p.err, KVMM_ERR_OUT_OF_RANGE);
-        } else {
-            const int32_t phys = p.block_table[unit * p.Pmax + lp];
-            if (phys < 0) {
-                report(p.err, KVMM_ERR_NULL_BLOCK);
-            } else if (phys >= p.n_phys) {
+        if (i < end) {
+            const int lp = p.sel_idx[unit * p.Kmax + i];
+            if (lp < 0 || lp >= P) {
                 report(p.err, KVMM_ERR_OUT_OF_RANGE);
             } else {
-                nv = min(kTileTok, seq - first);
-                if (nv > 0) row = static_cast<int64_t>(phys) * T + (t % tiles_per_page) * kTileTok;
+                const int32_t phys = p.block_table[unit * p.Pmax + lp];
+                if (phys < 0) {
+                    report(p.err, KVMM_ERR_NULL_BLOCK);
+                } else if (phys >= p.n_phys) {
+                    report(p.err, KVMM_ERR_OUT_OF_RANGE);
+                } else {
+                    nv = min(T, seq - lp * T);
+                    if (nv > 0) row = phys;
+                }
             }
         }
-        t_row[i] = row;
-        t_nv[i] = nv;
+        const bool ok = row >= 0;
+        const unsigned bal = __ballot_sync(kFullMask, ok);
+        if (lane == 0) sh.wcount[warp] = __popc(bal);
+        __syncthreads();
+        int pos = n_valid, tot = 0;
+#pragma unroll
+        for (int w = 0; w < kAttnWarps; ++w) {
+            if (w < warp) pos += sh.wcount[w];
+            tot += sh.wcount[w];
+        }
+        if (ok) {
+            pos += __popc(bal & ((1u << lane) - 1u));
+            pg_row[pos] = row;
+            pg_nv[pos] = nv;
+        }
+        n_valid += tot;
+        __syncthreads();
     }
-    __syncthreads();
 
     float o[kMTiles][4];
 #pragma unroll
     for (int i = 0; i < kMTiles; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
 
-    uint8_t* my_ring = ring + static_cast<size_t>(warp) * kRing * 2 * tile_bytes(D);
-    auto next_valid = [&](int i) {
-        while (i < ntile && t_row[i] < 0) i += kAttnWarps;
-        return i;
-    };
-    auto slot_ptr = [&](int ordinal) { return my_ring + static_cast<size_t>(ordinal % kRing) * 2 * tile_bytes(D); };
+    // steps of this CTA: step s covers list entries [s*kPPS, s*kPPS + kPPS); warp w takes s = w, w + warps, ...
+    const int n_steps = (n_valid + kPPS - 1) / kPPS;
+    const int my_steps = n_steps > warp ? (n_steps - warp + kAttnWarps - 1) / kAttnWarps : 0;
+    uint8_t* my_ring = ring + static_cast<size_t>(warp) * kSteps * step_bytes(D);
 
-    // the warp's valid tiles, numbered 0, 1, ...: tile u lives in slot u % kRing
-    int issue_i = next_valid(warp);  // list index of the next tile to fetch
-    int issued = 0, consumed = 0;
-    auto refill = [&]() {
-        while (issued < consumed + kRing && issue_i < ntile) {
-            if (lane == 0) {
-                uint8_t* ks = slot_ptr(issued);
-                uint64_t* bar = &sh.bar[warp][issued % kRing];
-                const size_t off = static_cast<size_t>(t_row[issue_i]) * D;
-                mbar_arrive_expect_tx(bar, 2 * tile_bytes(D));
-                bulk_copy_g2s(ks, p.k_pool + off, tile_bytes(D), bar);
-                bulk_copy_g2s(ks + tile_bytes(D), p.v_pool + off, tile_bytes(D), bar);
-            }
-            ++issued;
-            issue_i = next_valid(issue_i + kAttnWarps);
+    auto issue = [&](int k) {  // fetch the warp's k-th step into slot k % kSteps
+        const int s = warp + k * kAttnWarps;
+        uint8_t* slot = my_ring + static_cast<size_t>(k % kSteps) * step_bytes(D);
+        uint64_t* bar = &sh.bar[warp][k % kSteps];
+        const int npages = min(kPPS, n_valid - s * kPPS);
+        if (lane == 0) mbar_arrive_expect_tx(bar, static_cast<uint32_t>(npages) * 2 * kPageBytes);
+        __syncwarp();
+        if (lane < 2 * npages) {  // lane 2j copies page j's keys, lane 2j+1 its values
+            const int j = lane >> 1;
+            const size_t off = static_cast<size_t>(pg_row[s * kPPS + j]) * T * D;
+            if ((lane & 1) == 0)
+                bulk_copy_g2s(slot + j * kPageBytes, p.k_pool + off, kPageBytes, bar);
+            else
+                bulk_copy_g2s(slot + kStepTok * D * 2 + j * kPageBytes, p.v_pool + off, kPageBytes, bar);
         }
     };
-    refill();
+#pragma unroll
+    for (int k = 0; k < kSteps; ++k)
+        if (k < my_steps) issue(k);
 
+    // token u of a step: page u / T (within the step), row u % T.  Sub-tile j,
+    // fragment row rho holds token 8*((rho&7)>>1) + 4j + 2*(rho>>3) + (rho&1).
+    const int ua0 = 8 * (gid >> 1) + (gid & 1);  // rows gid (+2 for gid+8), sub-tile 0 (+4 for sub-tile 1)
     bool timed_out = false;
-    int cons_i = warp;
-    while (consumed < issued) {
-        // up to two tiles this step
-        const int i0 = next_valid(cons_i);
-        const bool two = consumed + 1 < issued;
-        const int i1 = two ? next_valid(i0 + kAttnWarps) : i0;
-        bool ok = mbar_wait_bounded(&sh.bar[warp][consumed % kRing], (consumed / kRing) & 1);
-        if (two) ok = mbar_wait_bounded(&sh.bar[warp][(consumed + 1) % kRing], ((consumed + 1) / kRing) & 1) && ok;
+    int k_stop = my_steps;  // first step not consumed
+    for (int k = 0; k < my_steps; ++k) {
+        const int s = warp + k * kAttnWarps;
+        const bool ok = mbar_wait_bounded(&sh.bar[warp][k % kSteps], (k / kSteps) & 1);
         if (__any_sync(kFullMask, !ok)) {  // warp-uniform decision
             timed_out = true;
+            k_stop = k;
             break;
         }
-        const uint8_t* ks0 = slot_ptr(consumed);
-        const uint8_t* ks1 = slot_ptr(consumed + 1);
-        const int nv0 = t_nv[i0];
-        const int nv1 = two ? t_nv[i1] : 0;
+        const uint8_t* ks = my_ring + static_cast<size_t>(k % kSteps) * step_bytes(D);
+        const uint8_t* vs = ks + kStepTok * D * 2;
+        // valid tokens of the step's pages (a missing second page has none)
+        const int nv0 = pg_nv[s * kPPS];
+        const int nv1 = (kPPS == 2 && s * kPPS + 1 < n_valid) ? pg_nv[s * kPPS + 1] : 0;
+        const bool full = (kPPS == 2) ? (nv0 == T && nv1 == T) : (nv0 == T);
+        auto valid = [&](int u) { return kPPS == 2 ? ((u >> 4) ? (u & 15) < nv1 : u < nv0) : u < nv0; };
 
-        float ca[4], cb[4];
-        tile_scores<D>(ks0, qf, gid, tig, ca);
-        if (two) {
-            tile_scores<D>(ks1, qf, gid, tig, cb);
-        } else {
-            cb[0] = cb[1] = cb[2] = cb[3] = 0.f;
-        }
-        // c = S^T[tok gid][head 2tig], [gid][2tig+1], [gid+8][2tig], [gid+8][2tig+1]
-        float x[8];
+        // ---- S^T = K Q^T for both sub-tiles ------------------------------
+        float x[2][4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            x[i] = ca[i] * p.scale_log2;
-            x[4 + i] = cb[i] * p.scale_log2;
+        for (int j = 0; j < 2; ++j) {
+            const uint8_t* ra = ks + (ua0 + 4 * j) * (2 * D);
+            const uint8_t* rb = ra + 2 * (2 * D);
+            float c[4] = {0.f, 0.f, 0.f, 0.f}, c2[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int r = 0; r < D / 32; ++r) {
+                const uint4 ka = ld_shared_v4(ra + 16 * (4 * r + tig));
+                const uint4 kb = ld_shared_v4(rb + 16 * (4 * r + tig));
+                mma_bf16_16816(c, ka.x, kb.x, ka.y, kb.y, qf[r][0], qf[r][1]);
+                mma_bf16_16816(c2, ka.z, kb.z, ka.w, kb.w, qf[r][2], qf[r][3]);
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) x[j][i] = (c[i] + c2[i]) * p.scale_log2;
+            if (!full) {
+                if (!valid(ua0 + 4 * j)) x[j][0] = x[j][1] = -INFINITY;
+                if (!valid(ua0 + 4 * j + 2)) x[j][2] = x[j][3] = -INFINITY;
+            }
         }
-        if (nv0 < kTileTok) {
-            if (gid >= nv0) x[0] = x[1] = -INFINITY;
-            if (gid + 8 >= nv0) x[2] = x[3] = -INFINITY;
-        }
-        if (nv1 < kTileTok) {  // also masks the absent second tile (nv1 = 0)
-            if (gid >= nv1) x[4] = x[5] = -INFINITY;
-            if (gid + 8 >= nv1) x[6] = x[7] = -INFINITY;
-        }
-        float mx0 = fmaxf(fmaxf(x[0], x[2]), fmaxf(x[4], x[6]));
-        float mx1 = fmaxf(fmaxf(x[1], x[3]), fmaxf(x[5], x[7]));
+        // x[j]: [row gid][head 2tig], [gid][2tig+1], [gid+8][2tig], [gid+8][2tig+1]
+        float mx0 = fmaxf(fmaxf(x[0][0], x[0][2]), fmaxf(x[1][0], x[1][2]));
+        float mx1 = fmaxf(fmaxf(x[0][1], x[0][3]), fmaxf(x[1][1], x[1][3]));
 #pragma unroll
         for (int off = 4; off < 32; off <<= 1) {
             mx0 = fmaxf(mx0, __shfl_xor_sync(kFullMask, mx0, off));
@@ -307,12 +270,14 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const AttnPar
         const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
         const float ref0 = mn0 == -INFINITY ? 0.f : mn0;
         const float ref1 = mn1 == -INFINITY ? 0.f : mn1;
-        const float a0 = exp2f(m0 - ref0), a1 = exp2f(m1 - ref1);
-        float pr[8];
+        const float a0 = fast_exp2(m0 - ref0), a1 = fast_exp2(m1 - ref1);
+        float pr[2][4];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) pr[i] = exp2f(x[i] - ((i & 1) ? ref1 : ref0));
-        l0 = fmaf(l0, a0, (pr[0] + pr[2]) + (pr[4] + pr[6]));
-        l1 = fmaf(l1, a1, (pr[1] + pr[3]) + (pr[5] + pr[7]));
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) pr[j][i] = fast_exp2(x[j][i] - ((i & 1) ? ref1 : ref0));
+        l0 = fmaf(l0, a0, (pr[0][0] + pr[0][2]) + (pr[1][0] + pr[1][2]));
+        l1 = fmaf(l1, a1, (pr[0][1] + pr[0][3]) + (pr[1][1] + pr[1][3]));
         m0 = mn0;
         m1 = mn1;
         if (__any_sync(kFullMask, (a0 != 1.f) || (a1 != 1.f))) {
@@ -325,36 +290,67 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const AttnPar
             }
         }
 
-        uint32_t bh0, bh1, bl0, bl1;
-        p_fragments(pr[0], pr[1], pr[2], pr[3], bh0, bh1, bl0, bl1);
-        tile_accumulate<D>(ks0 + tile_bytes(D), nv0, gid, tig, bh0, bh1, bl0, bl1, o);
-        if (two) {
-            p_fragments(pr[4], pr[5], pr[6], pr[7], bh0, bh1, bl0, bl1);
-            tile_accumulate<D>(ks1 + tile_bytes(D), nv1, gid, tig, bh0, bh1, bl0, bl1, o);
+        // ---- P^T as bf16 hi + lo B fragments (k order = the token order above)
+        uint32_t bh[2][2], bl[2][2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const uint32_t h01 = pack_bf16x2(pr[j][0], pr[j][1]), h23 = pack_bf16x2(pr[j][2], pr[j][3]);
+            const uint32_t r01 = pack_bf16x2(pr[j][0] - bf16_lo(h01), pr[j][1] - bf16_hi(h01));
+            const uint32_t r23 = pack_bf16x2(pr[j][2] - bf16_lo(h23), pr[j][3] - bf16_hi(h23));
+            bh[j][0] = movmatrix_trans(h01);
+            bh[j][1] = movmatrix_trans(h23);
+            bl[j][0] = movmatrix_trans(r01);
+            bl[j][1] = movmatrix_trans(r23);
         }
 
-        // ---- release the slots and refill them ---------------------------
+        // ---- O^T += V^T P^T: lane reads tokens 8tig .. 8tig+7 of dims 16i+gid, 16i+gid+8
+        const int u0 = 8 * tig;
+        const uint8_t* vrow = vs + (u0 / T) * kPageBytes + (u0 % T) * 2;
+        bool vk[8];
+        if (!full) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) vk[e] = valid(u0 + e);
+        }
+#pragma unroll
+        for (int i = 0; i < kMTiles; ++i) {
+            uint4 wa = ld_shared_v4(vrow + (16 * i + gid) * (T * 2));
+            uint4 wb = ld_shared_v4(vrow + (16 * i + gid + 8) * (T * 2));
+            if (!full) {
+                wa = make_uint4(keep_halves(wa.x, vk[0], vk[1]), keep_halves(wa.y, vk[2], vk[3]),
+                                keep_halves(wa.z, vk[4], vk[5]), keep_halves(wa.w, vk[6], vk[7]));
+                wb = make_uint4(keep_halves(wb.x, vk[0], vk[1]), keep_halves(wb.y, vk[2], vk[3]),
+                                keep_halves(wb.z, vk[4], vk[5]), keep_halves(wb.w, vk[6], vk[7]));
+            }
+            // sub-tile 0: tokens u0..u0+3 (words x, y); sub-tile 1: u0+4..u0+7 (z, w)
+            mma_bf16_16816(o[i], wa.x, wb.x, wa.y, wb.y, bh[0][0], bh[0][1]);
+            mma_bf16_16816(o[i], wa.x, wb.x, wa.y, wb.y, bl[0][0], bl[0][1]);
+            mma_bf16_16816(o[i], wa.z, wb.z, wa.w, wb.w, bh[1][0], bh[1][1]);
+            mma_bf16_16816(o[i], wa.z, wb.z, wa.w, wb.w, bl[1][0], bl[1][1]);
+        }
+
+        // ---- release the slot and refill it ------------------------------
         __syncwarp();
         fence_proxy_async_shared();
-        consumed += two ? 2 : 1;
-        cons_i = (two ? i1 : i0) + kAttnWarps;
-        refill();
+        if (k + kSteps < my_steps) issue(k + kSteps);
     }
     if (timed_out) {
         if (lane == 0) report(p.err, KVMM_ERR_TIMEOUT);
         // let copies still in flight land before the CTA leaves (bounded)
-        for (int v = consumed; v < issued; ++v)
-            mbar_wait_bounded(&sh.bar[warp][v % kRing], (v / kRing) & 1, 100000000ull);
+        for (int k = k_stop; k < min(my_steps, k_stop + kSteps); ++k)
+            mbar_wait_bounded(&sh.bar[warp][k % kSteps], (k / kSteps) & 1, 100000000ull);
     }
 
-    // ---- merge the warps of this CTA ------------------------------------
+    // ---- merge: warps of the CTA, then the CTAs of the cluster ------------
+    // Each warp leaves (m, l) per head and its unnormalised O^T in its own
+    // ring slot; after a cluster barrier every CTA of the cluster (the unit's
+    // splits) combines an equal share of the outputs from all partials
+    // through distributed shared memory.
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) {
         l0 += __shfl_xor_sync(kFullMask, l0, off);
         l1 += __shfl_xor_sync(kFullMask, l1, off);
     }
-    __syncthreads();  // all warps done with the ring: reuse it for O
-    float* so = reinterpret_cast<float*>(ring);  // [warps][8 heads][D]
+    float* my_o = reinterpret_cast<float*>(my_ring);  // [8 heads][D]; this warp's copies are all consumed
     if (gid == 0) {
         sh.m[warp][2 * tig] = m0;
         sh.m[warp][2 * tig + 1] = m1;
@@ -363,122 +359,169 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const AttnPar
     }
 #pragma unroll
     for (int i = 0; i < kMTiles; ++i) {
-        const int d0 = gid * kDimsPerGroup + 2 * i;
-        float* w0 = so + (warp * 8 + 2 * tig) * D;
+        float* w0 = my_o + (2 * tig) * D;
         float* w1 = w0 + D;
-        w0[d0] = o[i][0];
-        w1[d0] = o[i][1];
-        w0[d0 + 1] = o[i][2];
-        w1[d0 + 1] = o[i][3];
+        w0[16 * i + gid] = o[i][0];
+        w1[16 * i + gid] = o[i][1];
+        w0[16 * i + gid + 8] = o[i][2];
+        w1[16 * i + gid + 8] = o[i][3];
     }
-    __syncthreads();
+    cluster_sync();
 
-    const bool single = p.splits == 1;
-    float* part_o = p.part_o + (static_cast<size_t>(wunit) * p.splits + split) * G * D;
-    float* part_ml = p.part_ml + (static_cast<size_t>(wunit) * p.splits + split) * G * 2;
-    for (int e = tid; e < G * D; e += kAttnThreads) {
-        const int g = e / D, d = e % D;
+    const int nsp = p.splits;  // CTAs in the cluster
+    const uint32_t rank = cluster_ctarank();
+    if (tid < G) {
+        const int g = tid;
         float M = -INFINITY;
+        for (int s = 0; s < nsp; ++s)
 #pragma unroll
-        for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, sh.m[w][g]);
-        float O = 0.f, Lsum = 0.f;
-        if (M != -INFINITY) {
+            for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, ld_dsmem_f32(&sh.m[w][g], s));
+        float L = 0.f;
+        for (int s = 0; s < nsp; ++s)
 #pragma unroll
             for (int w = 0; w < kAttnWarps; ++w) {
-                const float f = exp2f(sh.m[w][g] - M);
-                O = fmaf(so[(w * 8 + g) * D + d], f, O);
-                Lsum = fmaf(sh.l[w][g], f, Lsum);
+                const float mw = ld_dsmem_f32(&sh.m[w][g], s);
+                const float f = (mw == -INFINITY) ? 0.f : exp2f(mw - M);
+                sh.f[s][w][g] = f;
+                L = fmaf(ld_dsmem_f32(&sh.l[w][g], s), f, L);
             }
-        }
-        if (single) {
-            const size_t oi = (static_cast<size_t>(b) * p.Hq + static_cast<size_t>(h) * G + g);
-            p.out[oi * D + d] = Lsum > 0.f ? O / Lsum : 0.f;
-            if (d == 0 && p.lse) p.lse[oi] = Lsum > 0.f ? (M + log2f(Lsum)) * 0.6931471805599453f : -INFINITY;
-        } else {
-            part_o[e] = O;
-            if (d == 0) {
-                part_ml[2 * g] = M;
-                part_ml[2 * g + 1] = Lsum;
-            }
-        }
-    }
-    if (single) return;
-
-    // ---- last CTA of the unit merges the splits -------------------------
-    __syncthreads();
-    if (tid == 0) {
-        __threadfence();  // the CTA's partial (ordered before by the barrier) is visible
-        const int ticket = atomicAdd(p.counters + wunit, 1);
-        sh.last = (ticket == p.splits - 1);
-        if (sh.last) p.counters[wunit] = 0;
-        __threadfence();
+        sh.inv_l[g] = L > 0.f ? 1.f / L : 0.f;
+        sh.lse[g] = L > 0.f ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
     }
     __syncthreads();
-    if (!sh.last) return;
-
-    const float* uo = p.part_o + static_cast<size_t>(wunit) * p.splits * G * D;
-    const float* uml = p.part_ml + static_cast<size_t>(wunit) * p.splits * G * 2;
-    for (int e = tid; e < G * D; e += kAttnThreads) {
-        const int g = e / D, d = e % D;
-        float M = -INFINITY;
-        for (int s = 0; s < p.splits; ++s) M = fmaxf(M, __ldcg(uml + (s * G + g) * 2));
-        float O = 0.f, Lsum = 0.f;
-        if (M != -INFINITY) {
-            for (int s = 0; s < p.splits; ++s) {
-                const float ms = __ldcg(uml + (s * G + g) * 2);
-                if (ms == -INFINITY) continue;
-                const float f = exp2f(ms - M);
-                O = fmaf(__ldcg(uo + (static_cast<size_t>(s) * G + g) * D + d), f, O);
-                Lsum = fmaf(__ldcg(uml + (s * G + g) * 2 + 1), f, Lsum);
+    const int n_out = G * D;
+    for (int e = static_cast<int>(rank) * kAttnThreads + tid; e < n_out; e += nsp * kAttnThreads) {
+        const int g = e / D, d = e - g * D;
+        float O = 0.f;
+        for (int s = 0; s < nsp; ++s)
+#pragma unroll
+            for (int w = 0; w < kAttnWarps; ++w) {
+                const float* src = reinterpret_cast<const float*>(ring + static_cast<size_t>(w) * kSteps * step_bytes(D)) + g * D + d;
+                O = fmaf(sh.f[s][w][g], ld_dsmem_f32(src, s), O);
             }
-        }
         const size_t oi = static_cast<size_t>(b) * p.Hq + static_cast<size_t>(h) * G + g;
-        p.out[oi * D + d] = Lsum > 0.f ? O / Lsum : 0.f;
-        if (d == 0 && p.lse) p.lse[oi] = Lsum > 0.f ? (M + log2f(Lsum)) * 0.6931471805599453f : -INFINITY;
+        p.out[oi * D + d] = O * sh.inv_l[g];
+        if (d == 0 && p.lse) p.lse[oi] = sh.lse[g];
     }
+    cluster_sync();  // no CTA leaves while its partials may still be read
 }
 
-template <int D>
-cudaError_t launch_attn(const AttnParams& p, cudaStream_t stream)
+template <int D, int T>
+void (*attn_kernel())(AttnParams)
 {
-    static thread_local int dev_cache = -1;
-    static thread_local size_t bytes_cache = 0;
-    const size_t smem = attention_smem_bytes(D, p.max_tiles);
-    cudaError_t e = allow_smem(sparse_attn_kernel<D>, smem, dev_cache, bytes_cache);
+    return sparse_attn_kernel<D, T>;
+}
+
+void (*attn_kernel_for(int D, int T))(AttnParams)
+{
+    if (D == 128) return T == 16 ? attn_kernel<128, 16>() : attn_kernel<128, 32>();
+    return T == 16 ? attn_kernel<64, 16>() : attn_kernel<64, 32>();
+}
+
+// opt-ins of one kernel instantiation, once per device
+cudaError_t prepare_attn(void (*kernel)(AttnParams), size_t smem)
+{
+    struct Prepared {
+        void (*kernel)(AttnParams);
+        int dev;
+        size_t bytes;
+    };
+    static thread_local Prepared cache[4] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    return launch_pdl(sparse_attn_kernel<D>, dim3(p.splits, p.Hkv, p.B), dim3(kAttnThreads), smem, stream, p);
+    for (auto& c : cache)
+        if (c.kernel == kernel && c.dev == dev && c.bytes >= smem) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+    for (auto& c : cache)
+        if (c.kernel == kernel || c.kernel == nullptr) {
+            c = {kernel, dev, smem};
+            break;
+        }
+    return cudaSuccess;
+}
+
+size_t attention_smem_bytes_impl(int D, int max_pages)
+{
+    return ring_region(D) + size_t(max_pages) * (sizeof(int64_t) + sizeof(int));
+}
+
+// clusters of `c` attention CTAs the device holds at once (0 = not launchable)
+int active_clusters(const kvmm_shape& s, int c)
+{
+    void (*kernel)(AttnParams) = attn_kernel_for(s.D, s.T);
+    const size_t smem = attention_smem_bytes(s.D, (s.Kmax + c - 1) / c);
+    if (prepare_attn(kernel, smem) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(c, 1, 1);
+    cfg.blockDim = dim3(kAttnThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = c;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
+struct SplitCache {
+    int dev, D, T, Kmax, units, splits, max_splits;
+};
+thread_local SplitCache g_split_cache[8] = {};
+thread_local int g_split_next = 0;
+
+SplitCache& split_entry(const kvmm_shape& s)
+{
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const int units = s.B * s.Hkv;
+    for (auto& c : g_split_cache)
+        if (c.max_splits > 0 && c.dev == dev && c.D == s.D && c.T == s.T && c.Kmax == s.Kmax && c.units == units)
+            return c;
+    SplitCache& c = g_split_cache[g_split_next++ % 8];
+    c = {dev, s.D, s.T, s.Kmax, units, 1, 1};
+    // largest launchable cluster, and the largest split count whose clusters
+    // for every unit fit on the device in one wave
+    int best = 1;
+    for (int k = 2; k <= kMaxSplits && k <= s.Kmax; ++k) {
+        const int n = active_clusters(s, k);
+        if (n <= 0) break;
+        c.max_splits = k;
+        if (n >= units) best = k;
+    }
+    c.splits = best;
+    return c;
 }
 
 }  // namespace
 
-size_t attention_smem_bytes(int D, int max_tiles)
-{
-    return ring_region(D) + size_t(max_tiles) * (sizeof(int64_t) + sizeof(int));
-}
+int attention_max_splits(const kvmm_shape& s) { return split_entry(s).max_splits; }
 
-int attention_slots_per_unit(const kvmm_shape& s)
-{
-    int dev = 0, sms = 148;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const int tiles = s.Kmax * (s.T / kTileTok);
-    // CTAs resident per SM are bounded by the ring (shared memory) of each CTA
-    const size_t per_cta = attention_smem_bytes(s.D, tiles) + sizeof(AttnShared) + 1024;
-    int per_sm = static_cast<int>((228u * 1024u) / per_cta);
-    if (per_sm < 1) per_sm = 1;
-    if (per_sm > 8) per_sm = 8;
-    const long long slots = static_cast<long long>(sms) * per_sm;
-    const long long units = static_cast<long long>(s.B) * s.Hkv;
-    long long splits = slots / units;
-    if (splits < 1) splits = 1;
-    if (splits > tiles) splits = tiles;
-    if (splits > 64) splits = 64;
-    return static_cast<int>(splits);
-}
+int attention_slots_per_unit(const kvmm_shape& s) { return split_entry(s).splits; }
+
+size_t attention_smem_bytes(int D, int max_pages) { return attention_smem_bytes_impl(D, max_pages); }
 
 cudaError_t launch_sparse_attention(const AttnParams& p, cudaStream_t stream)
 {
-    return p.D == 128 ? launch_attn<128>(p, stream) : launch_attn<64>(p, stream);
+    void (*kernel)(AttnParams) = attn_kernel_for(p.D, p.T);
+    const size_t smem = attention_smem_bytes(p.D, p.max_tiles);
+    const cudaError_t e = prepare_attn(kernel, smem);
+    if (e != cudaSuccess) return e;
+    return launch_pdl_cluster(kernel, dim3(p.splits, p.Hkv, p.B), dim3(kAttnThreads), smem, stream,
+                              static_cast<unsigned>(p.splits), p);
 }
 
 }  // namespace kvmm

@@ -20,7 +20,8 @@ Recipe (every tensor is drawn from one ``torch.Generator`` seeded per config):
   * q ~ N(0, 1) in bf16 per layer; with drift, q_t = 0.9 q_{t-1} + 0.44 eps
     in fp32 (eps ~ N(0, 1)), rounded to bf16 for use.
   * physical pool: identity layout (unit-major, logical page order) or a
-    seeded random permutation of the physical pages.
+    seeded random permutation of the physical pages; K pages are stored
+    token by token ([T][D]), V pages dimension by dimension ([D][T]).
   * stable/unstable split: a seeded subset of ``unstable_frac`` of the
     (layer, KV head) pairs is unstable.
 """
@@ -100,8 +101,8 @@ def scaled(cfg: Config, **kw) -> Config:
 class Workload:
     cfg: Config
     q: torch.Tensor  # [L_alloc, B, Hq, D] bf16
-    k_pool: torch.Tensor  # [Nphys, T, D] bf16
-    v_pool: torch.Tensor  # [Nphys, T, D] bf16
+    k_pool: torch.Tensor  # [Nphys, T, D] bf16 (token-major pages)
+    v_pool: torch.Tensor  # [Nphys, D, T] bf16 (dimension-major pages)
     block_table: torch.Tensor  # [B, L_alloc, Hkv, Pmax] int32
     seq_len: torch.Tensor  # [B] int32
     unstable: torch.Tensor  # [L_alloc, Hkv] uint8
@@ -157,12 +158,12 @@ def generate(cfg: Config, device="cpu", seed: int | None = None, chunk_pages: in
     lh_of_phys[block_table.reshape(-1).long()] = lh_logical
 
     k_pool = torch.empty(n_phys, T, D, dtype=torch.bfloat16, device=device)
-    v_pool = torch.empty(n_phys, T, D, dtype=torch.bfloat16, device=device)
+    v_pool = torch.empty(n_phys, D, T, dtype=torch.bfloat16, device=device)
     flat_scale = key_scale.view(L * Hkv, D)
     for s in range(0, n_phys, chunk_pages):
         e = min(n_phys, s + chunk_pages)
         k_pool[s:e] = torch.randn(e - s, T, D, generator=gen, device=device).to(torch.bfloat16)
-        v_pool[s:e] = torch.randn(e - s, T, D, generator=gen, device=device).to(torch.bfloat16)
+        v_pool[s:e] = torch.randn(e - s, D, T, generator=gen, device=device).to(torch.bfloat16)
         if cfg.key_dist != "normal":
             _scale_keys(k_pool[s:e], flat_scale[lh_of_phys[s:e]])
 

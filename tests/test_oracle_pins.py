@@ -37,6 +37,11 @@ def random_pool(rs, n_phys, T, D, scale=1.0):
     return bf16_bits_of(rs.standard_normal((n_phys, T, D)) * scale)
 
 
+def to_v(vp_token_major):
+    """A [n][T][D] value pool in the oracle's value layout [n][D][T]."""
+    return np.ascontiguousarray(vp_token_major.transpose(0, 2, 1))
+
+
 def gather_tokens(pool_f64, bt_row, T, seq_len, pages):
     rows = []
     for p in pages:
@@ -237,7 +242,7 @@ def test_sparse_attention_matches_torch_softmax(oracle_mod):
     bt = rs.permutation(n_phys)[:P].astype(np.int32)
     q = bf16_bits_of(rs.standard_normal((G, D)))
     sel = np.array([0, 3, 4, 9], np.int32)  # includes the ragged last page
-    out, lse, err = oracle_mod.unit_sparse_attention(q, kp, vp, T, bt, seq_len, sel)
+    out, lse, err = oracle_mod.unit_sparse_attention(q, kp, to_v(vp), T, bt, seq_len, sel)
     assert err == 0
     kr = gather_tokens(bits_to_f64(kp), bt, T, seq_len, sel)
     vr = gather_tokens(bits_to_f64(vp), bt, T, seq_len, sel)
@@ -252,8 +257,8 @@ def test_all_pages_selected_equals_dense_attention(oracle_mod):
     kp, vp = random_pool(rs, P, T, D), random_pool(rs, P, T, D)
     bt = np.arange(P, dtype=np.int32)
     q = bf16_bits_of(rs.standard_normal((G, D)))
-    sparse, lse_s, _ = oracle_mod.unit_sparse_attention(q, kp, vp, T, bt, P * T, np.arange(P))
-    dense, lse_d, _ = oracle_mod.unit_dense_attention(q, kp, vp, T, bt, P * T)
+    sparse, lse_s, _ = oracle_mod.unit_sparse_attention(q, kp, to_v(vp), T, bt, P * T, np.arange(P))
+    dense, lse_d, _ = oracle_mod.unit_dense_attention(q, kp, to_v(vp), T, bt, P * T)
     assert np.array_equal(sparse, dense) and np.array_equal(lse_s, lse_d)
     ref, ref_lse = torch_attention(q, bits_to_f64(kp).reshape(-1, D), bits_to_f64(vp).reshape(-1, D), D ** -0.5)
     assert np.allclose(dense, ref, rtol=0, atol=1e-12)
@@ -265,11 +270,11 @@ def test_single_token_gives_its_value_and_equal_keys_give_the_mean(oracle_mod):
     T, D, G = 16, 32, 2
     kp, vp = random_pool(rs, 2, T, D), random_pool(rs, 2, T, D)
     q = bf16_bits_of(rs.standard_normal((G, D)))
-    out, lse, _ = oracle_mod.unit_sparse_attention(q, kp, vp, T, np.array([0], np.int32), 1, [0])
+    out, lse, _ = oracle_mod.unit_sparse_attention(q, kp, to_v(vp), T, np.array([0], np.int32), 1, [0])
     assert np.array_equal(out, np.repeat(bits_to_f64(vp[0, :1]), G, axis=0))
     assert np.allclose(lse, bits_to_f64(q) @ bits_to_f64(kp[0, 0]) * D ** -0.5, atol=1e-12)
     kp[1] = kp[1, 0]  # every key of page 1 identical -> uniform weights
-    out, _, _ = oracle_mod.unit_sparse_attention(q, kp, vp, T, np.array([1], np.int32), T, [0])
+    out, _, _ = oracle_mod.unit_sparse_attention(q, kp, to_v(vp), T, np.array([1], np.int32), T, [0])
     assert np.allclose(out, np.repeat(bits_to_f64(vp[1]).mean(axis=0)[None], G, axis=0), atol=1e-12)
 
 
@@ -277,7 +282,7 @@ def test_empty_selection_gives_zero_output(oracle_mod):
     rs = np.random.default_rng(11)
     kp, vp = random_pool(rs, 1, 4, 8), random_pool(rs, 1, 4, 8)
     q = bf16_bits_of(rs.standard_normal((2, 8)))
-    out, lse, err = oracle_mod.unit_sparse_attention(q, kp, vp, 4, np.array([0], np.int32), 4, [])
+    out, lse, err = oracle_mod.unit_sparse_attention(q, kp, to_v(vp), 4, np.array([0], np.int32), 4, [])
     assert err == 0 and not out.any() and np.all(np.isneginf(lse))
 
 
@@ -291,18 +296,18 @@ def test_permuted_pool_is_transparent_and_null_block_is_skipped(oracle_mod):
     kperm, vperm = np.empty_like(kp), np.empty_like(vp)
     kperm[perm], vperm[perm] = kp, vp  # logical page p lives at physical perm[p]
     sel = [1, 2, 6]
-    a, la, _ = oracle_mod.unit_sparse_attention(q, kp, vp, T, ident, P * T, sel)
-    b, lb, _ = oracle_mod.unit_sparse_attention(q, kperm, vperm, T, perm, P * T, sel)
+    a, la, _ = oracle_mod.unit_sparse_attention(q, kp, to_v(vp), T, ident, P * T, sel)
+    b, lb, _ = oracle_mod.unit_sparse_attention(q, kperm, to_v(vperm), T, perm, P * T, sel)
     assert np.array_equal(a, b) and np.array_equal(la, lb)
     # a null entry on an unselected page changes nothing
     bt_null = ident.copy()
     bt_null[4] = -1
-    c, _, err = oracle_mod.unit_sparse_attention(q, kp, vp, T, bt_null, P * T, sel)
+    c, _, err = oracle_mod.unit_sparse_attention(q, kp, to_v(vp), T, bt_null, P * T, sel)
     assert err == 0 and np.array_equal(a, c)
     # a selected null page is reported and contributes nothing
     bt_null[2] = -1
-    d, _, err = oracle_mod.unit_sparse_attention(q, kp, vp, T, bt_null, P * T, sel)
-    e, _, _ = oracle_mod.unit_sparse_attention(q, kp, vp, T, ident, P * T, [1, 6])
+    d, _, err = oracle_mod.unit_sparse_attention(q, kp, to_v(vp), T, bt_null, P * T, sel)
+    e, _, _ = oracle_mod.unit_sparse_attention(q, kp, to_v(vp), T, ident, P * T, [1, 6])
     assert err == oracle_mod.ERR_NULL_BLOCK and np.array_equal(d, e)
 
 
@@ -314,7 +319,7 @@ def test_unit_step_follows_the_rerank_schedule(oracle_mod):
     T, D, G, K = 16, 32, 4, 3
     S0, steps = 5 * T - 2, 6
     Pmax = -(-(S0 + steps) // T)
-    kp, vp = random_pool(rs, Pmax, T, D), random_pool(rs, Pmax, T, D)
+    kp, vp = random_pool(rs, Pmax, T, D), to_v(random_pool(rs, Pmax, T, D))
     bt = np.arange(Pmax, dtype=np.int32)
     meta, _ = oracle_mod.unit_minmax(kp, T, bt, S0)
     st = oracle_mod.UnitState(kp, vp, T, bt, meta, K)
@@ -329,6 +334,7 @@ def test_unit_step_follows_the_rerank_schedule(oracle_mod):
         assert err == 0
         # the new token landed and the metadata of its page covers it
         assert np.array_equal(st.k_pool[(seq - 1) // T, (seq - 1) % T], nk[0])
+        assert np.array_equal(st.v_pool[(seq - 1) // T, :, (seq - 1) % T], nv[0])
         full_meta, _ = oracle_mod.unit_minmax(st.k_pool, T, bt, seq)
         P = -(-seq // T)
         assert np.array_equal(st.meta[:P], full_meta[:P])
