@@ -4,8 +4,9 @@ One step = one decode step of the Llama-3.1-8B-shaped 32K-context workload
 (32 layers, B=8, 32 query / 8 KV heads, head_dim 128, 16-token pages,
 budget 128 pages): per layer, append the new token and refresh its page's
 MinMax (kv_minmax_update), score every page and select the top-K
-(page_score_topk), list promoted pages (topk_promotion_diff) and attend over
-the selected pages (sparse_paged_decode_attn).  A layer-step is one layer of
+(page_score_topk), attend over the selected pages (sparse_paged_decode_attn;
+--fused runs both as one page_score_topk_attn launch), and list promoted pages
+(topk_promotion_diff, on a side stream).  A layer-step is one layer of
 that step for the whole batch.
 
 Inputs are seeded synthetic tensors resident in HBM (32 GiB of K/V, 2 GiB of
@@ -65,7 +66,10 @@ def algorithmic_bytes(cfg, rescored_units=None):
              + units * (2 * cfg.D * 2 + page + 2 * cfg.D * 2))  # new K/V row, page re-read, meta write
     return {"meta": meta, "kv": kv, "small": small, "total": meta + kv + small,
             "score_launch": meta + cfg.B * cfg.Hq * cfg.D * 2 + units * K * 4,
-            "attn_launch": kv + cfg.B * cfg.Hq * cfg.D * 2 + units * K * 8 + cfg.B * cfg.Hq * (cfg.D + 1) * 4}
+            "attn_launch": kv + cfg.B * cfg.Hq * cfg.D * 2 + units * K * 8 + cfg.B * cfg.Hq * (cfg.D + 1) * 4,
+            # one launch: metadata, selected K/V, q, table entries, selection written and read, out + lse
+            "fused_launch": meta + kv + cfg.B * cfg.Hq * cfg.D * 2 + units * K * 4 * 3
+                            + cfg.B * cfg.Hq * (cfg.D + 1) * 4}
 
 
 def peaks():
@@ -282,6 +286,8 @@ def gpu_arm(args):
     side = torch.cuda.Stream()
     forks = [torch.cuda.Event() for _ in range(L)]
 
+    fused = args.fused
+
     def step(instrument):
         main = torch.cuda.current_stream()
         for l in range(L):
@@ -289,18 +295,22 @@ def gpu_arm(args):
                                   st.v_pool, st.block_table, st.meta, st.err)
             if instrument:
                 ev_s[4 * l].record()
-            st.select(l, q_dev[l])
+            if fused:  # scoring, selection and attention in one launch
+                st.select_attend(l, q_dev[l])
+            else:
+                st.select(l, q_dev[l])
             if instrument:
                 ev_s[4 * l + 1].record()
             forks[l].record(main)
             side.wait_event(forks[l])
             with torch.cuda.stream(side):
                 st.diff(l)
-            if instrument:
-                ev_s[4 * l + 2].record()
-            st.attend(l, q_dev[l])
-            if instrument:
-                ev_s[4 * l + 3].record()
+            if not fused:
+                if instrument:
+                    ev_s[4 * l + 2].record()
+                st.attend(l, q_dev[l])
+                if instrument:
+                    ev_s[4 * l + 3].record()
         main.wait_stream(side)
 
     torch.cuda.empty_cache()
@@ -362,7 +372,7 @@ def gpu_arm(args):
             step(True)
         stream.synchronize()
     score_ms = [ev_s[4 * l].elapsed_time(ev_s[4 * l + 1]) for l in range(L)]
-    attn_ms = [ev_s[4 * l + 2].elapsed_time(ev_s[4 * l + 3]) for l in range(L)]
+    attn_ms = [ev_s[4 * l + 2].elapsed_time(ev_s[4 * l + 3]) for l in range(L)] if not fused else [0.0]
 
     # ---- end to end: host buffers in, host results out ------------------------
     q_host = wl.q.cpu().pin_memory()
@@ -407,9 +417,15 @@ def gpu_arm(args):
     kv_gbs = acc["total"] * n_ls / secs / 1e9
     peak, peak_kind = peaks()
     s_ms, a_ms = statistics.mean(score_ms), statistics.mean(attn_ms)
-    dom = "sparse_attn_kernel" if a_ms >= s_ms else "score_topk_kernel"
-    dom_ms = max(a_ms, s_ms)
-    dom_bytes = acc["attn_launch"] if a_ms >= s_ms else acc["score_launch"]
+    if fused:
+        dom, dom_ms, dom_bytes = "fused_decode_kernel", s_ms, acc["fused_launch"]
+        kernel_ms = {"fused_decode_kernel": s_ms}
+    else:
+        dom = "sparse_attn_kernel" if a_ms >= s_ms else "score_topk_kernel"
+        dom_ms = max(a_ms, s_ms)
+        dom_bytes = acc["attn_launch"] if a_ms >= s_ms else acc["score_launch"]
+        kernel_ms = {"score_topk_kernel": s_ms, "sparse_attn_kernel": a_ms}
+    kernel_ms["per_layer_step_ms"] = ms_total / args.steps / L
     achieved = dom_bytes / (dom_ms / 1e3) / 1e9
     traffic = load_traffic(dom)
     clk = clocks.summary()
@@ -423,11 +439,12 @@ def gpu_arm(args):
                    "top_k_pages": cfg.K, "splits": splits, "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (4 GiB of distinct data per step, no flush)",
                    "step": f"one decode step = {L} layer-steps, " + ("eager launches" if args.no_graph
-                                                                     else "CUDA graph replay")},
+                                                                     else "CUDA graph replay"),
+                   "path": "page_score_topk_attn (one launch)" if fused
+                           else "page_score_topk + sparse_paged_decode_attn"},
         "kv_gbs": kv_gbs, "pct_hbm_peak": kv_gbs / peak,
         "bytes_per_layer_step": acc["total"],
-        "kernel_ms": {"score_topk_kernel": s_ms, "sparse_attn_kernel": a_ms,
-                      "per_layer_step_ms": ms_total / args.steps / L},
+        "kernel_ms": kernel_ms,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic, "kernel": dom,
                      "peak_source": f"{peak_kind} hbm_gbs (burst copy)",
@@ -437,7 +454,8 @@ def gpu_arm(args):
         "e2e": {"value": e2e_steps * L * world / (e2e_ms / 1e3), "unit": "layer-steps/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "how": "pinned host q/new K,V -> device, graph replay, out/lse/promoted counts -> pinned host"},
-        "gpu_launches": 5 * L * args.steps,  # update, score, top-K, diff, attention per layer
+        # per layer: update, fused select+attend, diff (fused) or update, score, top-K, diff, attention
+        "gpu_launches": (3 if fused else 5) * L * args.steps,
         "clocks": clk,
         "device_err": err_word,
     }
@@ -468,6 +486,8 @@ def main():
     ap.add_argument("--no-graph", action="store_true", help="launch eagerly (for profilers)")
     ap.add_argument("--batch", type=int, default=0, help="override the batch (smaller profiling case)")
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (smaller profiling case)")
+    ap.add_argument("--fused", action="store_true",
+                    help="one page_score_topk_attn launch per layer instead of page_score_topk + sparse_paged_decode_attn")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.impl == "reference":

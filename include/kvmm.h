@@ -249,9 +249,43 @@ kvmm_status topk_promotion_diff(const kvmm_shape* shape, int32_t layer,
                                 int32_t* promoted_cnt, int32_t* evicted, int32_t* evicted_cnt,
                                 int32_t* total_promoted, int32_t* err, kvmm_stream stream);
 
-/* Workspace bytes that page_score_topk needs (sparse_paged_decode_attn needs
- * none; num_splits is accepted for the stable signature and ignored).
- * Returns 0 for an unsupported shape. */
+/* ------------------------------------------------------------------------
+ * page_score_topk_attn -- page_score_topk followed by
+ * sparse_paged_decode_attn on the new selection, in one launch.
+ *
+ * FlexiCache, "Core method, 2. MinMax-metadata page scoring" (score every
+ * page from its key bounds, keep the top-K per layer and KV head) and
+ * "Core method, 1" / "System design, head-level block table" (attend over
+ * the selected pages only, through the head-level table).  The pages run
+ * these as successive steps of one decode step; this call computes the same
+ * results without a GPU-wide drain between them: while one unit selects,
+ * other units still stream metadata or K/V.
+ *
+ * Arguments, layouts and results are those of the two calls: sel_idx /
+ * sel_cnt / scores_out of rescored units as page_score_topk writes them (the
+ * others keep their selection, which the attention then uses), and out /
+ * lse as sparse_paged_decode_attn writes them.  The split of the selection
+ * over CTAs is internal (no num_splits); out must be 16-byte aligned
+ * (it is written with vector stores).  workspace must hold
+ * kvmm_workspace_size(shape, 0) bytes, be zero-filled before its first use
+ * and not be modified by the caller between calls; calls that share a
+ * workspace must not overlap on the GPU.  A wait that cannot end (which
+ * only a modified workspace or a broken device can cause) gives up after
+ * about a second with KVMM_ERR_TIMEOUT.  Up to Pmax = 2048 this is one
+ * kernel launch; longer tables run page_score_topk's kernels and then the
+ * attention kernel (same results).
+ */
+kvmm_status page_score_topk_attn(const kvmm_shape* shape, int32_t layer, const kvmm_bf16* q,
+                                 const kvmm_bf16* meta, const kvmm_bf16* k_pool, const kvmm_bf16* v_pool,
+                                 const int32_t* block_table, const int32_t* seq_len,
+                                 const uint8_t* rescore_mask, int32_t K, int32_t group_reduce,
+                                 float sm_scale, int32_t* sel_idx, int32_t* sel_cnt, float* scores_out,
+                                 float* out, float* lse, void* workspace, size_t workspace_bytes,
+                                 int32_t* err, kvmm_stream stream);
+
+/* Workspace bytes that page_score_topk and page_score_topk_attn need
+ * (sparse_paged_decode_attn needs none; num_splits is accepted for the
+ * stable signature and ignored).  Returns 0 for an unsupported shape. */
 size_t kvmm_workspace_size(const kvmm_shape* shape, int32_t num_splits);
 
 /* Number of splits per unit that sparse_paged_decode_attn uses for

@@ -48,10 +48,7 @@ int resolve_splits(const kvmm_shape& s, int32_t num_splits)
     return splits;
 }
 
-size_t score_ws_bytes(const kvmm_shape& s)
-{
-    return kvmm::ws_counter_bytes(s) + size_t(s.B) * s.Hkv * s.Pmax * sizeof(float);
-}
+size_t score_ws_bytes(const kvmm_shape& s) { return kvmm::ws_counter_bytes(s) + kvmm::ws_scores_bytes(s); }
 
 thread_local cudaError_t g_last_cuda_error = cudaSuccess;
 
@@ -92,7 +89,7 @@ int32_t kvmm_auto_splits(const kvmm_shape* shape)
 size_t kvmm_workspace_size(const kvmm_shape* shape, int32_t num_splits)
 {
     if (check_shape(shape) != KVMM_OK || num_splits < 0) return 0;
-    return score_ws_bytes(*shape);  // attention merges its splits on chip and needs none
+    return kvmm::ws_total_bytes(*shape);  // sparse_paged_decode_attn merges on chip and needs none
 }
 
 kvmm_status kv_minmax_update(const kvmm_shape* shape, int32_t layer, const kvmm_bf16* new_k,
@@ -269,6 +266,72 @@ kvmm_status sparse_paged_decode_attn(const kvmm_shape* shape, int32_t layer, con
     p.lse = lse;
     p.err = err;
     return launched(kvmm::launch_sparse_attention(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+kvmm_status page_score_topk_attn(const kvmm_shape* shape, int32_t layer, const kvmm_bf16* q,
+                                 const kvmm_bf16* meta, const kvmm_bf16* k_pool, const kvmm_bf16* v_pool,
+                                 const int32_t* block_table, const int32_t* seq_len,
+                                 const uint8_t* rescore_mask, int32_t K, int32_t group_reduce,
+                                 float sm_scale, int32_t* sel_idx, int32_t* sel_cnt, float* scores_out,
+                                 float* out, float* lse, void* workspace, size_t workspace_bytes,
+                                 int32_t* err, kvmm_stream stream)
+{
+    kvmm_status st = check_shape(shape);
+    if (st != KVMM_OK) return st;
+    const kvmm_shape& s = *shape;
+    if (layer < 0 || layer >= s.L || K < 1 || K > s.Kmax || !std::isfinite(sm_scale)) return KVMM_INVALID_ARG;
+    if (group_reduce != 0 && group_reduce != 1) return KVMM_INVALID_ARG;
+    if (!req(q) || !req(meta) || !req(k_pool) || !req(v_pool) || !req4(block_table) || !req4(seq_len) ||
+        !req4(sel_idx) || !req4(sel_cnt) || !opt4(scores_out) || !req(out) || !opt4(lse) || !req(workspace) ||
+        !opt4(err))
+        return KVMM_INVALID_ARG;
+    if (workspace_bytes < kvmm::ws_total_bytes(s)) return KVMM_WORKSPACE_TOO_SMALL;
+    if (s.Pmax > kvmm::kFusedMaxPages) {
+        // the one-launch selector holds a unit's scores in registers: longer tables
+        // run the scoring / selection kernels, then the attention kernel
+        st = page_score_topk(shape, layer, q, meta, seq_len, rescore_mask, K, group_reduce, sel_idx, sel_cnt,
+                             scores_out, workspace, workspace_bytes, err, stream);
+        if (st != KVMM_OK) return st;
+        return sparse_paged_decode_attn(shape, layer, q, k_pool, v_pool, block_table, seq_len, sel_idx, sel_cnt,
+                                        sm_scale, 0, out, lse, nullptr, 0, err, stream);
+    }
+    kvmm::FusedParams p{};
+    p.B = s.B;
+    p.L = s.L;
+    p.Hq = s.Hq;
+    p.Hkv = s.Hkv;
+    p.G = s.Hq / s.Hkv;
+    p.D = s.D;
+    p.T = s.T;
+    p.Pmax = s.Pmax;
+    p.Kmax = s.Kmax;
+    p.layer = layer;
+    p.K = K;
+    p.chunks = (s.Pmax + 127) / 128;
+    p.splits = kvmm::fused_splits(s);
+    p.pstride = kvmm::ws_score_stride(s);
+    // the work list is indexed by int32
+    if (static_cast<long long>(s.B) * s.Hkv * (p.chunks + p.splits) > (1LL << 30)) return KVMM_UNSUPPORTED_SHAPE;
+    p.n_phys = s.n_phys;
+    p.scale_log2 = (sm_scale > 0.f ? sm_scale : 1.0f / std::sqrt(static_cast<float>(s.D))) * 1.4426950408889634f;
+    p.q = q;
+    p.meta = meta;
+    p.k_pool = k_pool;
+    p.v_pool = v_pool;
+    p.block_table = block_table;
+    p.seq_len = seq_len;
+    p.rescore_mask = rescore_mask;
+    p.sel_idx = sel_idx;
+    p.sel_cnt = sel_cnt;
+    p.scores_out = scores_out;
+    p.out = out;
+    p.lse = lse;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    p.ctrl = reinterpret_cast<int32_t*>(ws);
+    p.scores = reinterpret_cast<float*>(ws + kvmm::ws_counter_bytes(s));
+    p.partials = reinterpret_cast<float*>(ws + kvmm::ws_counter_bytes(s) + kvmm::ws_scores_bytes(s));
+    p.err = err;
+    return launched(kvmm::launch_fused_decode(p, group_reduce, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 kvmm_status topk_promotion_diff(const kvmm_shape* shape, int32_t layer,

@@ -12,13 +12,42 @@
 
 namespace kvmm {
 
-// Workspace layout shared by page_score_topk and sparse_paged_decode_attn:
-// one int32 counter per (b, kv_head) of the layer, then the call's data.
-// Both kernels leave every counter at zero when they finish.
+// Workspace layout shared by every call that takes a workspace:
+//   [control words][scores: B*Hkv rows of Pmax fp32][attention partials]
+// The control words (zero before the first use; every launch of the fused
+// call leaves them zero again) are the fused call's queue counters, then
+// four per-unit arrays: score tickets [U], attention tickets [U], the select
+// queue [U] and the ready queue [U * splits].  page_score_topk uses only the
+// scores region.
+constexpr int kCtrlHead = 16;
+inline size_t round256(size_t n) { return (n + 255) & ~static_cast<size_t>(255); }
+// attention items per unit in the fused call: 256 tokens of selected pages each, at most 64
+inline int fused_splits(const kvmm_shape& s)
+{
+    const int item_pages = 256 / s.T;
+    int n = (s.Kmax + item_pages - 1) / item_pages;
+    return n < 1 ? 1 : (n > 64 ? 64 : n);
+}
 inline size_t ws_counter_bytes(const kvmm_shape& s)
 {
-    size_t n = static_cast<size_t>(s.B) * s.Hkv * sizeof(int32_t);
-    return (n + 255) & ~static_cast<size_t>(255);
+    const size_t units = static_cast<size_t>(s.B) * s.Hkv;
+    return round256((kCtrlHead + 3 * units + units * fused_splits(s)) * sizeof(int32_t));
+}
+// score rows of the fused call start 16-byte aligned: Pmax rounded up to 4
+inline int ws_score_stride(const kvmm_shape& s) { return (s.Pmax + 3) & ~3; }
+inline size_t ws_scores_bytes(const kvmm_shape& s)
+{
+    return round256(static_cast<size_t>(s.B) * s.Hkv * ws_score_stride(s) * sizeof(float));
+}
+// one partial per (unit, attention item): m[8], l[8], O[8][D] (fp32)
+inline size_t ws_partials_bytes(const kvmm_shape& s)
+{
+    return round256(static_cast<size_t>(s.B) * s.Hkv * fused_splits(s) * (16 + 8 * static_cast<size_t>(s.D)) *
+                    sizeof(float));
+}
+inline size_t ws_total_bytes(const kvmm_shape& s)
+{
+    return ws_counter_bytes(s) + ws_scores_bytes(s) + ws_partials_bytes(s);
 }
 
 struct UpdateParams {
@@ -64,6 +93,34 @@ struct AttnParams {
     const int32_t* sel_cnt;
     float* out;
     float* lse;
+    int32_t* err;
+};
+
+// page_score_topk_attn runs as one launch for page tables up to this long
+constexpr int kFusedMaxPages = 2048;
+
+struct FusedParams {
+    int32_t B, L, Hq, Hkv, G, D, T, Pmax, Kmax, layer, K;
+    int32_t chunks;  // score items per unit: ceil(Pmax / 128)
+    int32_t splits;  // attention items per unit
+    int32_t pstride; // floats between the workspace score rows of two units
+    int64_t n_phys;
+    float scale_log2;  // sm_scale * log2(e)
+    const kvmm_bf16* q;
+    const kvmm_bf16* meta;
+    const kvmm_bf16* k_pool;
+    const kvmm_bf16* v_pool;
+    const int32_t* block_table;
+    const int32_t* seq_len;
+    const uint8_t* rescore_mask;
+    int32_t* sel_idx;
+    int32_t* sel_cnt;
+    float* scores_out;
+    float* out;
+    float* lse;
+    int32_t* ctrl;      // workspace: control words
+    float* scores;      // workspace: [B*Hkv][pstride]
+    float* partials;    // workspace: [B*Hkv][splits][16 + 8*D]
     int32_t* err;
 };
 
@@ -146,6 +203,7 @@ cudaError_t launch_minmax_update(const UpdateParams& p, cudaStream_t stream);
 cudaError_t launch_score_topk(const ScoreParams& p, int group_reduce, cudaStream_t stream);
 cudaError_t launch_sparse_attention(const AttnParams& p, cudaStream_t stream);
 cudaError_t launch_promotion_diff(const DiffParams& p, cudaStream_t stream);
+cudaError_t launch_fused_decode(const FusedParams& p, int group_reduce, cudaStream_t stream);
 
 // Library-owned scratch of page_score_topk_static_scratch (score_topk.cu):
 // counters for up to kStaticScratchCounterBytes/4 units, then the scores.

@@ -41,13 +41,20 @@
 namespace kvmm {
 namespace {
 
-constexpr int kConsumerWarps = 4;
+#ifndef KVMM_SCORE_WARPS
+#define KVMM_SCORE_WARPS 4
+#endif
+#ifndef KVMM_SCORE_STAGES
+#define KVMM_SCORE_STAGES 3
+#endif
+
+constexpr int kConsumerWarps = KVMM_SCORE_WARPS;
 constexpr int kScoreThreads = kConsumerWarps * 32 + 32;  // + one producer warp
 constexpr int kChunk = 16 * kConsumerWarps;               // pages per work item, 16 per consumer warp
-constexpr int kStages = 3;
+constexpr int kStages = KVMM_SCORE_STAGES;
 constexpr int kQBytes = 8 * 128 * 2;                      // largest query group (G <= 8, D <= 128)
 
-constexpr int kTopkThreads = 512;
+constexpr int kTopkThreads = 1024;
 constexpr int kTopkWarps = kTopkThreads / 32;
 constexpr int kBins = 2048;
 constexpr int kCandMax = 1024;

@@ -109,7 +109,6 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const AttnPar
     int* pg_nv = reinterpret_cast<int*>(pg_row + p.max_tiles);            // its valid tokens
 
     const size_t unit = (static_cast<size_t>(b) * p.L + p.layer) * p.Hkv + h;
-    const int wunit = b * p.Hkv + h;
 
     if (tid < kAttnWarps * kSteps) mbar_init(&sh.bar[tid / kSteps][tid % kSteps], 1);
     fence_barrier_init();

@@ -21,7 +21,7 @@ NULL_BLOCK = -1
 
 EXPORTS = ("kv_minmax_update", "page_score_topk", "sparse_paged_decode_attn", "topk_promotion_diff",
            "kvmm_workspace_size", "kvmm_auto_splits", "kvmm_status_string", "kvmm_last_cuda_error",
-           "page_score_topk_static_scratch")
+           "page_score_topk_static_scratch", "page_score_topk_attn")
 
 
 class KvmmError(RuntimeError):
@@ -74,8 +74,9 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.sparse_paged_decode_attn.argtypes = [SP, I32, P, P, P, P, P, P, P, F32, I32, P, P, P, SZ, P, P]
     lib.topk_promotion_diff.argtypes = [SP, I32, P, P, P, P, P, I32, P, P, P, P, P, P, P]
     lib.page_score_topk_static_scratch.argtypes = [SP, I32, P, P, P, P, I32, I32, P, P, P, P, P]
+    lib.page_score_topk_attn.argtypes = [SP, I32, P, P, P, P, P, P, P, I32, I32, F32, P, P, P, P, P, P, SZ, P, P]
     for f in ("kv_minmax_update", "page_score_topk", "sparse_paged_decode_attn", "topk_promotion_diff",
-              "page_score_topk_static_scratch"):
+              "page_score_topk_static_scratch", "page_score_topk_attn"):
         getattr(lib, f).restype = ctypes.c_int
     lib.kvmm_workspace_size.argtypes = [SP, I32]
     lib.kvmm_workspace_size.restype = SZ
@@ -206,6 +207,29 @@ def sparse_paged_decode_attn(shape: Shape, layer: int, q, k_pool, v_pool, block_
             0 if workspace is None else workspace.numel(),
             _dev(err, "err", torch.int32, 1, optional=True), _stream(stream))
     _check("sparse_paged_decode_attn", load().sparse_paged_decode_attn(*args))
+
+
+def page_score_topk_attn(shape: Shape, layer: int, q, meta, k_pool, v_pool, block_table, seq_len, rescore_mask,
+                         K: int, sel_idx, sel_cnt, out, workspace, lse=None, err=None, scores_out=None,
+                         group_reduce: int = 0, sm_scale: float = 0.0, stream=None) -> None:
+    """page_score_topk then sparse_paged_decode_attn on the new selection, in one launch."""
+    s = shape
+    units = s.B * s.L * s.Hkv
+    args = (ctypes.byref(s), layer, _dev(q, "q", torch.bfloat16, s.B * s.Hq * s.D),
+            _dev(meta, "meta", torch.bfloat16, units * s.Pmax * 2 * s.D),
+            _dev(k_pool, "k_pool", torch.bfloat16, s.n_phys * s.T * s.D),
+            _dev(v_pool, "v_pool", torch.bfloat16, s.n_phys * s.T * s.D),
+            _dev(block_table, "block_table", torch.int32, units * s.Pmax),
+            _dev(seq_len, "seq_len", torch.int32, s.B),
+            _dev(rescore_mask, "rescore_mask", torch.uint8, s.L * s.Hkv, optional=True), K, group_reduce,
+            float(sm_scale),
+            _dev(sel_idx, "sel_idx", torch.int32, units * s.Kmax), _dev(sel_cnt, "sel_cnt", torch.int32, units),
+            _dev(scores_out, "scores_out", torch.float32, s.B * s.Hkv * s.Pmax, optional=True),
+            _dev(out, "out", torch.float32, s.B * s.Hq * s.D),
+            _dev(lse, "lse", torch.float32, s.B * s.Hq, optional=True),
+            _dev(workspace, "workspace", torch.uint8), workspace.numel(),
+            _dev(err, "err", torch.int32, 1, optional=True), _stream(stream))
+    _check("page_score_topk_attn", load().page_score_topk_attn(*args))
 
 
 def topk_promotion_diff(shape: Shape, layer: int, rescore_mask, prev_idx, prev_cnt, cur_idx, cur_cnt, promoted,

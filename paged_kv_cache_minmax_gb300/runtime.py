@@ -10,6 +10,8 @@ layer and step, the calls in the method's order:
   3. ``topk_promotion_diff``       promoted = cur \\ prev (commit cur as prev)
   4. ``sparse_paged_decode_attn``  attention over the selected pages
 
+or, with steps 2 and 4 in one launch, ``page_score_topk_attn`` then the diff.
+
 (FlexiCache, "Core method", sections 1-3.)  Everything runs on one CUDA
 stream; nothing here synchronises.
 """
@@ -86,13 +88,24 @@ class DecodeState:
                                       lse=self.lse[layer], err=self.err, sm_scale=sm_scale,
                                       num_splits=self.num_splits)
 
-    def layer_step(self, layer, q, new_k=None, new_v=None, rescore_mask=None) -> None:
-        """One layer of one decode step: append, select, diff, attend."""
+    def select_attend(self, layer, q, rescore_mask=None, scores_out=None, sm_scale=0.0) -> None:
+        """select + attend in one launch (page_score_topk_attn)."""
+        kvmm.page_score_topk_attn(self.shape, layer, q, self.meta, self.k_pool, self.v_pool, self.block_table,
+                                  self.seq_len, rescore_mask, self.K, self.sel_idx, self.sel_cnt, self.out[layer],
+                                  self.workspace, lse=self.lse[layer], err=self.err, scores_out=scores_out,
+                                  group_reduce=self.group_reduce, sm_scale=sm_scale)
+
+    def layer_step(self, layer, q, new_k=None, new_v=None, rescore_mask=None, fused=True) -> None:
+        """One layer of one decode step: append, select + attend, diff."""
         if new_k is not None:
             self.append(layer, new_k, new_v)
-        self.select(layer, q, rescore_mask)
-        self.diff(layer, rescore_mask)
-        self.attend(layer, q)
+        if fused:
+            self.select_attend(layer, q, rescore_mask)
+            self.diff(layer, rescore_mask)
+        else:
+            self.select(layer, q, rescore_mask)
+            self.diff(layer, rescore_mask)
+            self.attend(layer, q)
 
     def read_err(self) -> int:
         return int(self.err.item())

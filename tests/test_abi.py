@@ -84,6 +84,13 @@ def test_validation_rejects_before_any_launch(lib):
     # attention: non-finite scale
     assert lib.sparse_paged_decode_attn(ctypes.byref(s), 0, fake, fake, fake, fake, fake, fake, fake,
                                         float("nan"), 1, fake, None, None, 0, None, None) == kvmm.INVALID_ARG
+    # fused select + attend: null pointers, bad K, non-finite scale, small workspace
+    fa = [fake, fake, fake, fake, fake, fake, None, 8, 0, 0.0, fake, fake, None, fake, None, fake, 1 << 20, None,
+          None]
+    assert lib.page_score_topk_attn(ctypes.byref(s), 0, None, *fa[1:]) == kvmm.INVALID_ARG
+    assert lib.page_score_topk_attn(ctypes.byref(s), 0, *fa[:7], 9, *fa[8:]) == kvmm.INVALID_ARG
+    assert lib.page_score_topk_attn(ctypes.byref(s), 0, *fa[:9], float("inf"), *fa[10:]) == kvmm.INVALID_ARG
+    assert lib.page_score_topk_attn(ctypes.byref(s), 0, *fa[:16], 64, None, None) == kvmm.WORKSPACE_TOO_SMALL
     # diff: missing promoted list
     assert lib.topk_promotion_diff(ctypes.byref(s), 0, None, fake, fake, fake, fake, 1, None, fake, None, None,
                                    None, None, None) == kvmm.INVALID_ARG
