@@ -251,29 +251,25 @@ kvmm_status topk_promotion_diff(const kvmm_shape* shape, int32_t layer,
 
 /* ------------------------------------------------------------------------
  * page_score_topk_attn -- page_score_topk followed by
- * sparse_paged_decode_attn on the new selection, in one launch.
+ * sparse_paged_decode_attn on the new selection.
  *
  * FlexiCache, "Core method, 2. MinMax-metadata page scoring" (score every
  * page from its key bounds, keep the top-K per layer and KV head) and
  * "Core method, 1" / "System design, head-level block table" (attend over
- * the selected pages only, through the head-level table).  The pages run
- * these as successive steps of one decode step; this call computes the same
- * results without a GPU-wide drain between them: while one unit selects,
- * other units still stream metadata or K/V.
+ * the selected pages only, through the head-level table).  Two kernels
+ * instead of three: the scoring kernel, then the attention kernel, whose
+ * CTAs select their unit's pages from the scores themselves (every CTA of a
+ * unit's cluster computes the same exact top-K in shared memory) before
+ * streaming them, so the separate selection kernel and its round trip
+ * through global memory drop out.
  *
  * Arguments, layouts and results are those of the two calls: sel_idx /
  * sel_cnt / scores_out of rescored units as page_score_topk writes them (the
  * others keep their selection, which the attention then uses), and out /
- * lse as sparse_paged_decode_attn writes them.  The split of the selection
- * over CTAs is internal (no num_splits); out must be 16-byte aligned
- * (it is written with vector stores).  workspace must hold
- * kvmm_workspace_size(shape, 0) bytes, be zero-filled before its first use
- * and not be modified by the caller between calls; calls that share a
- * workspace must not overlap on the GPU.  A wait that cannot end (which
- * only a modified workspace or a broken device can cause) gives up after
- * about a second with KVMM_ERR_TIMEOUT.  Up to Pmax = 2048 this is one
- * kernel launch; longer tables run page_score_topk's kernels and then the
- * attention kernel (same results).
+ * lse as sparse_paged_decode_attn writes them with its automatic split
+ * count.  workspace as for page_score_topk.  When the selection does not fit
+ * the attention CTA's shared memory (Pmax beyond about 30,000 pages), the
+ * call runs page_score_topk and then sparse_paged_decode_attn (same results).
  */
 kvmm_status page_score_topk_attn(const kvmm_shape* shape, int32_t layer, const kvmm_bf16* q,
                                  const kvmm_bf16* meta, const kvmm_bf16* k_pool, const kvmm_bf16* v_pool,

@@ -39,9 +39,9 @@ kvmm_status check_shape(const kvmm_shape* s)
     return KVMM_OK;
 }
 
-int resolve_splits(const kvmm_shape& s, int32_t num_splits)
+int resolve_splits(const kvmm_shape& s, int32_t num_splits, bool select = false)
 {
-    int splits = num_splits > 0 ? num_splits : kvmm::attention_slots_per_unit(s);
+    int splits = num_splits > 0 ? num_splits : kvmm::attention_slots_per_unit(s, select);
     if (splits > kvmm::kAttnMaxSplits) splits = kvmm::kAttnMaxSplits;
     if (splits > s.Kmax) splits = s.Kmax;
     if (splits < 1) splits = 1;
@@ -253,6 +253,7 @@ kvmm_status sparse_paged_decode_attn(const kvmm_shape* shape, int32_t layer, con
     p.layer = layer;
     p.splits = splits;
     p.max_tiles = max_pages;
+    p.region0 = static_cast<int32_t>(kvmm::attention_region0(s.D, 0));
     p.n_phys = s.n_phys;
     p.scale_log2 = (sm_scale > 0.f ? sm_scale : 1.0f / std::sqrt(static_cast<float>(s.D))) * 1.4426950408889634f;
     p.q = q;
@@ -282,20 +283,48 @@ kvmm_status page_score_topk_attn(const kvmm_shape* shape, int32_t layer, const k
     if (layer < 0 || layer >= s.L || K < 1 || K > s.Kmax || !std::isfinite(sm_scale)) return KVMM_INVALID_ARG;
     if (group_reduce != 0 && group_reduce != 1) return KVMM_INVALID_ARG;
     if (!req(q) || !req(meta) || !req(k_pool) || !req(v_pool) || !req4(block_table) || !req4(seq_len) ||
-        !req4(sel_idx) || !req4(sel_cnt) || !opt4(scores_out) || !req(out) || !opt4(lse) || !req(workspace) ||
+        !req4(sel_idx) || !req4(sel_cnt) || !opt4(scores_out) || !req4(out) || !opt4(lse) || !req(workspace) ||
         !opt4(err))
         return KVMM_INVALID_ARG;
-    if (workspace_bytes < kvmm::ws_total_bytes(s)) return KVMM_WORKSPACE_TOO_SMALL;
-    if (s.Pmax > kvmm::kFusedMaxPages) {
-        // the one-launch selector holds a unit's scores in registers: longer tables
-        // run the scoring / selection kernels, then the attention kernel
+    if (workspace_bytes < score_ws_bytes(s)) return KVMM_WORKSPACE_TOO_SMALL;
+    const size_t scratch = kvmm::attention_select_scratch(s.Pmax, s.Kmax);
+    const int splits = resolve_splits(s, 0, true);
+    const int max_pages = (s.Kmax + splits - 1) / splits;
+    if (kvmm::attention_smem_bytes(s.D, max_pages, scratch) > 200 * 1024) {
+        // the selection does not fit the attention CTA's shared memory: separate kernels
         st = page_score_topk(shape, layer, q, meta, seq_len, rescore_mask, K, group_reduce, sel_idx, sel_cnt,
                              scores_out, workspace, workspace_bytes, err, stream);
         if (st != KVMM_OK) return st;
         return sparse_paged_decode_attn(shape, layer, q, k_pool, v_pool, block_table, seq_len, sel_idx, sel_cnt,
                                         sm_scale, 0, out, lse, nullptr, 0, err, stream);
     }
-    kvmm::FusedParams p{};
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    float* scores_ws = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + kvmm::ws_counter_bytes(s));
+    ScoreParams sp{};
+    sp.B = s.B;
+    sp.L = s.L;
+    sp.Hq = s.Hq;
+    sp.Hkv = s.Hkv;
+    sp.G = s.Hq / s.Hkv;
+    sp.D = s.D;
+    sp.T = s.T;
+    sp.Pmax = s.Pmax;
+    sp.Kmax = s.Kmax;
+    sp.layer = layer;
+    sp.K = K;
+    sp.q = q;
+    sp.meta = meta;
+    sp.seq_len = seq_len;
+    sp.rescore_mask = rescore_mask;
+    sp.sel_idx = sel_idx;
+    sp.sel_cnt = sel_cnt;
+    sp.scores_out = scores_out;
+    sp.counters = static_cast<int32_t*>(workspace);
+    sp.scores_ws = scores_ws;
+    sp.err = err;
+    const cudaError_t e = kvmm::launch_score_only(sp, group_reduce, cs);
+    if (e != cudaSuccess) return launched(e);
+    AttnParams p{};
     p.B = s.B;
     p.L = s.L;
     p.Hq = s.Hq;
@@ -306,32 +335,29 @@ kvmm_status page_score_topk_attn(const kvmm_shape* shape, int32_t layer, const k
     p.Pmax = s.Pmax;
     p.Kmax = s.Kmax;
     p.layer = layer;
+    p.splits = splits;
+    p.max_tiles = max_pages;
+    p.region0 = static_cast<int32_t>(kvmm::attention_region0(s.D, scratch));
+    p.select = 1;
     p.K = K;
-    p.chunks = (s.Pmax + 127) / 128;
-    p.splits = kvmm::fused_splits(s);
-    p.pstride = kvmm::ws_score_stride(s);
-    // the work list is indexed by int32
-    if (static_cast<long long>(s.B) * s.Hkv * (p.chunks + p.splits) > (1LL << 30)) return KVMM_UNSUPPORTED_SHAPE;
+    p.pstride = s.Pmax;
     p.n_phys = s.n_phys;
     p.scale_log2 = (sm_scale > 0.f ? sm_scale : 1.0f / std::sqrt(static_cast<float>(s.D))) * 1.4426950408889634f;
     p.q = q;
-    p.meta = meta;
     p.k_pool = k_pool;
     p.v_pool = v_pool;
     p.block_table = block_table;
     p.seq_len = seq_len;
-    p.rescore_mask = rescore_mask;
     p.sel_idx = sel_idx;
     p.sel_cnt = sel_cnt;
-    p.scores_out = scores_out;
     p.out = out;
     p.lse = lse;
-    uint8_t* ws = static_cast<uint8_t*>(workspace);
-    p.ctrl = reinterpret_cast<int32_t*>(ws);
-    p.scores = reinterpret_cast<float*>(ws + kvmm::ws_counter_bytes(s));
-    p.partials = reinterpret_cast<float*>(ws + kvmm::ws_counter_bytes(s) + kvmm::ws_scores_bytes(s));
+    p.scores = scores_ws;
+    p.rescore_mask = rescore_mask;
+    p.sel_out = sel_idx;
+    p.cnt_out = sel_cnt;
     p.err = err;
-    return launched(kvmm::launch_fused_decode(p, group_reduce, reinterpret_cast<cudaStream_t>(stream)));
+    return launched(kvmm::launch_sparse_attention(p, cs));
 }
 
 kvmm_status topk_promotion_diff(const kvmm_shape* shape, int32_t layer,

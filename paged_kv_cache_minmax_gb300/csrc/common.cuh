@@ -137,6 +137,16 @@ __device__ __forceinline__ float ld_dsmem_f32(const void* local, uint32_t rank)
     return v;
 }
 
+// store a float into the shared memory of CTA `rank` of the cluster, at the
+// address that `local` has in this CTA's shared memory (visible to that CTA
+// after the next cluster barrier)
+__device__ __forceinline__ void st_dsmem_f32(void* local, uint32_t rank, float v)
+{
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(local)), "r"(rank));
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
+}
+
 // ---------------------------------------------------------------------------
 // programmatic dependent launch: the next kernel in the stream may be
 // scheduled once every CTA of this one has called launch_dependents; a kernel

@@ -12,43 +12,19 @@
 
 namespace kvmm {
 
-// Workspace layout shared by every call that takes a workspace:
-//   [control words][scores: B*Hkv rows of Pmax fp32][attention partials]
-// The control words (zero before the first use; every launch of the fused
-// call leaves them zero again) are the fused call's queue counters, then
-// four per-unit arrays: score tickets [U], attention tickets [U], the select
-// queue [U] and the ready queue [U * splits].  page_score_topk uses only the
-// scores region.
-constexpr int kCtrlHead = 16;
+// Workspace layout shared by the calls that take one: one int32 counter per
+// (b, kv_head) of the layer (reserved; left at zero), then the unit's page
+// scores, B*Hkv rows of Pmax fp32.
 inline size_t round256(size_t n) { return (n + 255) & ~static_cast<size_t>(255); }
-// attention items per unit in the fused call: 256 tokens of selected pages each, at most 64
-inline int fused_splits(const kvmm_shape& s)
-{
-    const int item_pages = 256 / s.T;
-    int n = (s.Kmax + item_pages - 1) / item_pages;
-    return n < 1 ? 1 : (n > 64 ? 64 : n);
-}
 inline size_t ws_counter_bytes(const kvmm_shape& s)
 {
-    const size_t units = static_cast<size_t>(s.B) * s.Hkv;
-    return round256((kCtrlHead + 3 * units + units * fused_splits(s)) * sizeof(int32_t));
+    return round256(static_cast<size_t>(s.B) * s.Hkv * sizeof(int32_t));
 }
-// score rows of the fused call start 16-byte aligned: Pmax rounded up to 4
-inline int ws_score_stride(const kvmm_shape& s) { return (s.Pmax + 3) & ~3; }
 inline size_t ws_scores_bytes(const kvmm_shape& s)
 {
-    return round256(static_cast<size_t>(s.B) * s.Hkv * ws_score_stride(s) * sizeof(float));
+    return round256(static_cast<size_t>(s.B) * s.Hkv * s.Pmax * sizeof(float));
 }
-// one partial per (unit, attention item): m[8], l[8], O[8][D] (fp32)
-inline size_t ws_partials_bytes(const kvmm_shape& s)
-{
-    return round256(static_cast<size_t>(s.B) * s.Hkv * fused_splits(s) * (16 + 8 * static_cast<size_t>(s.D)) *
-                    sizeof(float));
-}
-inline size_t ws_total_bytes(const kvmm_shape& s)
-{
-    return ws_counter_bytes(s) + ws_scores_bytes(s) + ws_partials_bytes(s);
-}
+inline size_t ws_total_bytes(const kvmm_shape& s) { return ws_counter_bytes(s) + ws_scores_bytes(s); }
 
 struct UpdateParams {
     int32_t B, L, Hkv, D, T, Pmax, layer, n_new;
@@ -82,6 +58,10 @@ struct AttnParams {
     int32_t B, L, Hq, Hkv, G, D, T, Pmax, Kmax, layer;
     int32_t splits;      // CTAs per unit (one cluster)
     int32_t max_tiles;   // upper bound of selected pages handled by one CTA
+    int32_t region0;     // shared-memory bytes before the page lists (ring, or selection scratch)
+    int32_t select;      // 1: rescored units select their pages from `scores` first
+    int32_t K;           // select: pages to keep
+    int32_t pstride;     // select: floats between the score rows of two units
     int64_t n_phys;
     float scale_log2;    // sm_scale * log2(e)
     const kvmm_bf16* q;
@@ -93,34 +73,10 @@ struct AttnParams {
     const int32_t* sel_cnt;
     float* out;
     float* lse;
-    int32_t* err;
-};
-
-// page_score_topk_attn runs as one launch for page tables up to this long
-constexpr int kFusedMaxPages = 2048;
-
-struct FusedParams {
-    int32_t B, L, Hq, Hkv, G, D, T, Pmax, Kmax, layer, K;
-    int32_t chunks;  // score items per unit: ceil(Pmax / 128)
-    int32_t splits;  // attention items per unit
-    int32_t pstride; // floats between the workspace score rows of two units
-    int64_t n_phys;
-    float scale_log2;  // sm_scale * log2(e)
-    const kvmm_bf16* q;
-    const kvmm_bf16* meta;
-    const kvmm_bf16* k_pool;
-    const kvmm_bf16* v_pool;
-    const int32_t* block_table;
-    const int32_t* seq_len;
-    const uint8_t* rescore_mask;
-    int32_t* sel_idx;
-    int32_t* sel_cnt;
-    float* scores_out;
-    float* out;
-    float* lse;
-    int32_t* ctrl;      // workspace: control words
-    float* scores;      // workspace: [B*Hkv][pstride]
-    float* partials;    // workspace: [B*Hkv][splits][16 + 8*D]
+    const float* scores;          // select: [B*Hkv][pstride] page scores of the layer
+    const uint8_t* rescore_mask;  // select: [L][Hkv] or null (every unit)
+    int32_t* sel_out;             // select: where the new selections are written (sel_idx)
+    int32_t* cnt_out;             // select: ... and their counts (sel_cnt)
     int32_t* err;
 };
 
@@ -203,7 +159,8 @@ cudaError_t launch_minmax_update(const UpdateParams& p, cudaStream_t stream);
 cudaError_t launch_score_topk(const ScoreParams& p, int group_reduce, cudaStream_t stream);
 cudaError_t launch_sparse_attention(const AttnParams& p, cudaStream_t stream);
 cudaError_t launch_promotion_diff(const DiffParams& p, cudaStream_t stream);
-cudaError_t launch_fused_decode(const FusedParams& p, int group_reduce, cudaStream_t stream);
+// the scoring kernel alone (page_score_topk without its selection kernel)
+cudaError_t launch_score_only(const ScoreParams& p, int group_reduce, cudaStream_t stream);
 
 // Library-owned scratch of page_score_topk_static_scratch (score_topk.cu):
 // counters for up to kStaticScratchCounterBytes/4 units, then the scores.
@@ -215,8 +172,13 @@ cudaError_t static_scratch_for_current_device(void** ptr, cudaStream_t stream);
 
 // Attention launch geometry for the current device.
 constexpr int kAttnMaxSplits = 16;                   // CTAs of a unit form one cluster
-int attention_slots_per_unit(const kvmm_shape& s);  // automatic split count
-int attention_max_splits(const kvmm_shape& s);      // largest launchable cluster (<= kAttnMaxSplits)
-size_t attention_smem_bytes(int D, int max_pages);
+// `select`: the attention kernel that selects its own pages (page_score_topk_attn)
+int attention_slots_per_unit(const kvmm_shape& s, bool select = false);  // automatic split count
+int attention_max_splits(const kvmm_shape& s, bool select = false);      // largest launchable cluster
+// dynamic shared memory of one attention CTA; `scratch`: the selection scratch (0 without selection)
+size_t attention_smem_bytes(int D, int max_pages, size_t scratch = 0);
+size_t attention_region0(int D, size_t scratch);
+// selection scratch of the selecting attention kernel for a shape
+size_t attention_select_scratch(int Pmax, int Kmax);
 
 }  // namespace kvmm

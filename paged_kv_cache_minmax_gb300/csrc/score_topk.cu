@@ -23,13 +23,10 @@
 //     producer warp keeps kStages chunks (and the unit's query group) in
 //     flight with 1-D bulk copies (TMA) on full/empty mbarriers; each
 //     consumer warp scores 16 pages of a chunk.
-//  2. select_topk_kernel -- one CTA per rescored unit selects the top K of
-//     the unit's P scores exactly: one pass buckets the scores into 2048 bins
-//     between their min and max (monotone in the value), a suffix scan finds
-//     the bin holding the K-th largest, the few scores in that bin are ranked
-//     exactly (value descending, page ascending), and an ordered compaction
-//     writes the pages in ascending order.  Degenerate inputs (a crowded
-//     threshold bin, a non-finite range) take an exact 4-pass radix select.
+//  2. select_topk_kernel -- one 512-thread CTA per rescored unit selects the
+//     top K of the unit's P scores exactly (block_topk, topk_block.cuh: a
+//     binned pass with an exact rank of the threshold bin, or a radix
+//     select for degenerate inputs) and writes them in ascending page order.
 // Both are launched with programmatic dependent launch so each is scheduled
 // while its predecessor drains.
 #include <cfloat>
@@ -37,6 +34,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "topk_block.cuh"
 
 namespace kvmm {
 namespace {
@@ -54,20 +52,11 @@ constexpr int kChunk = 16 * kConsumerWarps;               // pages per work item
 constexpr int kStages = KVMM_SCORE_STAGES;
 constexpr int kQBytes = 8 * 128 * 2;                      // largest query group (G <= 8, D <= 128)
 
-constexpr int kTopkThreads = 1024;
-constexpr int kTopkWarps = kTopkThreads / 32;
-constexpr int kBins = 2048;
-constexpr int kCandMax = 1024;
+constexpr int kTopkThreads = 512;
 
 __host__ __device__ constexpr int stage_meta_bytes(int D) { return kChunk * 4 * D; }
 __host__ __device__ constexpr int stage_bytes(int D) { return stage_meta_bytes(D) + kQBytes; }
 
-// float -> unsigned key with the same order
-__device__ __forceinline__ uint32_t order_key(float f)
-{
-    const uint32_t u = __float_as_uint(f);
-    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
 
 // per 16-bit half: keep negative values (min(x, 0)) or positive ones (max(x, 0))
 __device__ __forceinline__ uint32_t bf16x2_min0(uint32_t w)
@@ -236,119 +225,10 @@ __global__ void __launch_bounds__(kScoreThreads) score_pages_kernel(const ScoreP
 }
 
 // ---------------------------------------------------------------------------
-struct TopkShared {
-    int hist[kBins];
-    int cand[kCandMax];
-    float wmin[kTopkWarps];
-    float wmax[kTopkWarps];
-    int wsum[kTopkWarps];
-    int rhist[256];
-    int ncand;
-    int tb;
-    int need;
-    int cbin;
-    int digit;
-    int remaining;
-};
-
-// Exact top-K over all P keys by 4 radix passes; writes sel[0..K) ascending.
-// The general path, used when the binned pass cannot isolate the threshold.
-__device__ void radix_topk(const float* sc, int P, int K, int32_t* sel, TopkShared& ts)
-{
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    uint32_t prefix = 0, pmask = 0;
-    int remaining = K;
-    const int P_round = (P + kTopkThreads - 1) / kTopkThreads * kTopkThreads;
-    for (int shift = 24; shift >= 0; shift -= 8) {
-        for (int i = tid; i < 256; i += kTopkThreads) ts.rhist[i] = 0;
-        __syncthreads();
-        for (int i = tid; i < P_round; i += kTopkThreads) {
-            const uint32_t key = i < P ? order_key(sc[i]) : 0u;
-            const bool cand = i < P && (key & pmask) == prefix;
-            const unsigned active = __ballot_sync(kFullMask, cand);
-            if (cand) {
-                const uint32_t digit = (key >> shift) & 255u;
-                const unsigned peers = __match_any_sync(active, digit);
-                if (lane == __ffs(peers) - 1) atomicAdd(&ts.rhist[digit], __popc(peers));
-            }
-        }
-        __syncthreads();
-        if (warp == 0) {
-            int c[8];
-            int tot = 0;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                c[j] = ts.rhist[255 - 8 * lane - j];
-                tot += c[j];
-            }
-            int incl = tot;
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const int v = __shfl_up_sync(kFullMask, incl, off);
-                if (lane >= off) incl += v;
-            }
-            const int excl = incl - tot;
-            if (excl < remaining && remaining <= incl) {
-                int acc = excl;
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    if (acc + c[j] >= remaining) {
-                        ts.digit = 255 - 8 * lane - j;
-                        ts.remaining = remaining - acc;
-                        break;
-                    }
-                    acc += c[j];
-                }
-            }
-        }
-        __syncthreads();
-        prefix |= static_cast<uint32_t>(ts.digit) << shift;
-        pmask |= 255u << shift;
-        remaining = ts.remaining;
-        __syncthreads();
-    }
-    const uint32_t thr = prefix;
-    int out_base = 0, eq_base = 0;
-    const unsigned lt_mask = (1u << lane) - 1u;
-    for (int t0 = 0; t0 < P; t0 += kTopkThreads) {
-        const int i = t0 + tid;
-        const uint32_t key = i < P ? order_key(sc[i]) : 0u;
-        const bool gt = i < P && key > thr;
-        const bool eq = i < P && key == thr;
-        const unsigned eqb = __ballot_sync(kFullMask, eq);
-        if (lane == 0) ts.wsum[warp] = __popc(eqb);
-        __syncthreads();
-        int eq_off = eq_base, eq_all = 0;
-        for (int w2 = 0; w2 < kTopkWarps; ++w2) {
-            const int t = ts.wsum[w2];
-            if (w2 < warp) eq_off += t;
-            eq_all += t;
-        }
-        __syncthreads();
-        const bool take = gt || (eq && eq_off + __popc(eqb & lt_mask) < remaining);
-        const unsigned tb = __ballot_sync(kFullMask, take);
-        if (lane == 0) ts.wsum[warp] = __popc(tb);
-        __syncthreads();
-        int out_off = out_base, out_all = 0;
-        for (int w2 = 0; w2 < kTopkWarps; ++w2) {
-            const int t = ts.wsum[w2];
-            if (w2 < warp) out_off += t;
-            out_all += t;
-        }
-        if (take) sel[out_off + __popc(tb & lt_mask)] = i;
-        out_base += out_all;
-        eq_base += eq_all;
-        __syncthreads();
-    }
-}
-
 __global__ void __launch_bounds__(kTopkThreads) select_topk_kernel(const ScoreParams p)
 {
     extern __shared__ __align__(16) uint8_t tsm[];
-    __shared__ TopkShared ts;
-    const int tid = threadIdx.x;
-    const int lane = tid & 31;
-    const int warp = tid >> 5;
+    __shared__ BlockTopkShared<kTopkThreads> ts;
     const int h = blockIdx.x;
     const int b = blockIdx.y;
     pdl_launch_dependents();
@@ -357,133 +237,11 @@ __global__ void __launch_bounds__(kTopkThreads) select_topk_kernel(const ScorePa
     if (p.rescore_mask != nullptr && p.rescore_mask[p.layer * p.Hkv + h] == 0) return;
     const int P = unit_pages(p, b, false);
     const size_t unit = (static_cast<size_t>(b) * p.L + p.layer) * p.Hkv + h;
-    const float* scores = p.scores_ws + static_cast<size_t>(b * p.Hkv + h) * p.Pmax;
-    int32_t* sel = p.sel_idx + unit * p.Kmax;
-    const int K = p.K;
-    if (K >= P) {
-        for (int i = tid; i < P; i += kTopkThreads) sel[i] = i;
-        if (tid == 0) p.sel_cnt[unit] = P;
-        return;
-    }
     float* sc = reinterpret_cast<float*>(tsm);                                           // [P]
     int16_t* bin = reinterpret_cast<int16_t*>(tsm + static_cast<size_t>(p.Pmax) * 4);  // [P]
-
-    // 1. scores to shared memory, their range, an empty histogram
-    float lo = FLT_MAX, hi = -FLT_MAX;
-    for (int i = tid; i < P; i += kTopkThreads) {
-        const float s = __ldcg(scores + i);
-        sc[i] = s;
-        lo = fminf(lo, s);
-        hi = fmaxf(hi, s);
-    }
-    for (int i = tid; i < kBins; i += kTopkThreads) ts.hist[i] = 0;
-    if (tid == 0) ts.ncand = 0;
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) {
-        lo = fminf(lo, __shfl_xor_sync(kFullMask, lo, off));
-        hi = fmaxf(hi, __shfl_xor_sync(kFullMask, hi, off));
-    }
-    if (lane == 0) {
-        ts.wmin[warp] = lo;
-        ts.wmax[warp] = hi;
-    }
-    __syncthreads();
-    float mn = ts.wmin[0], mx = ts.wmax[0];
-    for (int w = 1; w < kTopkWarps; ++w) {
-        mn = fminf(mn, ts.wmin[w]);
-        mx = fmaxf(mx, ts.wmax[w]);
-    }
-    if (!(mx > mn)) {  // every score equal: the K lowest pages win the ties
-        for (int i = tid; i < K; i += kTopkThreads) sel[i] = i;
-        if (tid == 0) p.sel_cnt[unit] = K;
-        return;
-    }
-    const float scale = static_cast<float>(kBins) / (mx - mn);
-    if (!(scale < FLT_MAX)) {
-        radix_topk(sc, P, K, sel, ts);
-        if (tid == 0) p.sel_cnt[unit] = K;
-        return;
-    }
-
-    // 2. bucket every score: bin(s) = floor((s - mn) * scale) is monotone in s
-    for (int i = tid; i < P; i += kTopkThreads) {
-        const int bi = min(kBins - 1, static_cast<int>((sc[i] - mn) * scale));
-        bin[i] = static_cast<int16_t>(bi);
-        atomicAdd(&ts.hist[bi], 1);
-    }
-    __syncthreads();
-
-    // 3. the bin holding the K-th largest score: suffix sums over bins
-    constexpr int kBinsPerThread = kBins / kTopkThreads;
-    int local = 0;
-#pragma unroll
-    for (int j = 0; j < kBinsPerThread; ++j) local += ts.hist[kBinsPerThread * tid + j];
-    int incl = local;  // inclusive suffix within the warp (lanes >= this one)
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const int v = __shfl_down_sync(kFullMask, incl, off);
-        if (lane + off < 32) incl += v;
-    }
-    if (lane == 0) ts.wsum[warp] = incl;
-    __syncthreads();
-    int above = incl - local;
-    for (int w = warp + 1; w < kTopkWarps; ++w) above += ts.wsum[w];
-    if (above < K && K <= above + local) {
-        int acc = above;
-        for (int j = kBinsPerThread - 1; j >= 0; --j) {
-            const int bj = kBinsPerThread * tid + j;
-            if (acc + ts.hist[bj] >= K) {
-                ts.tb = bj;
-                ts.need = K - acc;
-                ts.cbin = ts.hist[bj];
-                break;
-            }
-            acc += ts.hist[bj];
-        }
-    }
-    __syncthreads();
-    const int tb = ts.tb, need = ts.need, cbin = ts.cbin;
-    if (cbin > kCandMax) {  // crowded threshold bin: exact radix path
-        radix_topk(sc, P, K, sel, ts);
-        if (tid == 0) p.sel_cnt[unit] = K;
-        return;
-    }
-
-    // 4. rank the threshold bin's scores exactly; mark the winners above every bin
-    for (int i = tid; i < P; i += kTopkThreads)
-        if (bin[i] == tb) ts.cand[atomicAdd(&ts.ncand, 1)] = i;
-    __syncthreads();
-    for (int t = tid; t < cbin; t += kTopkThreads) {
-        const int i = ts.cand[t];
-        const float s = sc[i];
-        int rank = 0;
-        for (int j = 0; j < cbin; ++j) {
-            const int i2 = ts.cand[j];
-            const float s2 = sc[i2];
-            rank += (s2 > s) || (s2 == s && i2 < i);
-        }
-        if (rank < need) bin[i] = static_cast<int16_t>(kBins);
-    }
-    __syncthreads();
-
-    // 5. ordered compaction: thread t emits the winners among pages [t*m, t*m + m)
-    const int m = (P + kTopkThreads - 1) / kTopkThreads;
-    const int i0 = min(P, tid * m), i1 = min(P, i0 + m);
-    int mine = 0;
-    for (int i = i0; i < i1; ++i) mine += bin[i] > tb;
-    int pre = mine;  // inclusive prefix within the warp
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const int v = __shfl_up_sync(kFullMask, pre, off);
-        if (lane >= off) pre += v;
-    }
-    if (lane == 31) ts.wsum[warp] = pre;
-    __syncthreads();
-    int pos = pre - mine;
-    for (int w = 0; w < warp; ++w) pos += ts.wsum[w];
-    for (int i = i0; i < i1; ++i)
-        if (bin[i] > tb) sel[pos++] = i;
-    if (tid == 0) p.sel_cnt[unit] = K;
+    const int n = block_topk<kTopkThreads>(p.scores_ws + static_cast<size_t>(b * p.Hkv + h) * p.Pmax, P, p.K,
+                                           p.sel_idx + unit * p.Kmax, sc, bin, ts);
+    if (threadIdx.x == 0) p.sel_cnt[unit] = n;
 }
 
 // one opt-in cache for the (single) selection kernel, shared by every launcher
@@ -495,7 +253,7 @@ cudaError_t allow_topk_smem(size_t bytes)
 }
 
 template <int D, int MODE>
-cudaError_t launch_score(const ScoreParams& p, cudaStream_t stream)
+cudaError_t launch_score(const ScoreParams& p, cudaStream_t stream, bool with_select)
 {
     static thread_local int dev_a = -1;
     static thread_local size_t bytes_a = 0;
@@ -511,7 +269,7 @@ cudaError_t launch_score(const ScoreParams& p, cudaStream_t stream)
     const long long slots = static_cast<long long>(sms) * per_sm;
     const long long grid = items < slots ? items : slots;
     e = launch_pdl(score_pages_kernel<D, MODE>, dim3(static_cast<unsigned>(grid)), dim3(kScoreThreads), smem, stream, p);
-    if (e != cudaSuccess) return e;
+    if (e != cudaSuccess || !with_select) return e;
     const size_t ksmem = static_cast<size_t>(p.Pmax) * (sizeof(float) + sizeof(int16_t));
     e = allow_topk_smem(ksmem);
     if (e != cudaSuccess) return e;
@@ -522,8 +280,16 @@ cudaError_t launch_score(const ScoreParams& p, cudaStream_t stream)
 
 cudaError_t launch_score_topk(const ScoreParams& p, int group_reduce, cudaStream_t stream)
 {
-    if (p.D == 128) return group_reduce ? launch_score<128, 1>(p, stream) : launch_score<128, 0>(p, stream);
-    return group_reduce ? launch_score<64, 1>(p, stream) : launch_score<64, 0>(p, stream);
+    if (p.D == 128)
+        return group_reduce ? launch_score<128, 1>(p, stream, true) : launch_score<128, 0>(p, stream, true);
+    return group_reduce ? launch_score<64, 1>(p, stream, true) : launch_score<64, 0>(p, stream, true);
+}
+
+cudaError_t launch_score_only(const ScoreParams& p, int group_reduce, cudaStream_t stream)
+{
+    if (p.D == 128)
+        return group_reduce ? launch_score<128, 1>(p, stream, false) : launch_score<128, 0>(p, stream, false);
+    return group_reduce ? launch_score<64, 1>(p, stream, false) : launch_score<64, 0>(p, stream, false);
 }
 
 // ---------------------------------------------------------------------------

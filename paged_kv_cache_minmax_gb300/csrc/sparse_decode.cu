@@ -28,13 +28,17 @@
 // (two MMAs) so the probabilities keep ~16 bits, and is moved from the S^T
 // accumulator layout to the B-operand layout with movmatrix.  Softmax
 // statistics are online per warp, merged across warps in shared memory and
-// across splits by the last CTA of the unit (an atomic ticket; nothing
-// spins).  The kernel is launched with programmatic dependent launch and
-// waits for its predecessor before reading any input.
+// across the splits of a unit (one thread-block cluster) by remote
+// shared-memory stores and one cluster barrier.  With `select`, rescored
+// units first pick their pages from the layer's scores (block_topk, every CTA
+// of the cluster computing the same selection).  The kernel is launched with
+// programmatic dependent launch and waits for its predecessor before reading
+// any input.
 #include <cmath>
 
 #include "common.cuh"
 #include "kernels.h"
+#include "topk_block.cuh"
 
 #ifndef KVMM_ATTN_WARPS
 #define KVMM_ATTN_WARPS 4
@@ -62,13 +66,27 @@ __host__ __device__ constexpr size_t ring_region(int D)
 
 constexpr int kMaxSplits = kAttnMaxSplits;  // CTAs of one unit = one thread-block cluster
 
+// selection scratch, laid over the ring before streaming starts:
+// [BlockTopkShared][scores: Pmax fp32][bins: Pmax int16][selection: Kmax int32]
+__host__ __device__ constexpr size_t align16(size_t n) { return (n + 15) & ~static_cast<size_t>(15); }
+__host__ __device__ constexpr size_t select_scratch_offset_scores()
+{
+    return align16(sizeof(BlockTopkShared<kAttnThreads>));
+}
+__host__ __device__ constexpr size_t select_scratch_offset_sel(int Pmax)
+{
+    return align16(select_scratch_offset_scores() + size_t(Pmax) * (sizeof(float) + sizeof(int16_t)));
+}
+
 struct AttnShared {
     uint64_t bar[kAttnWarps][kSteps];
     float m[kAttnWarps][8];
     float l[kAttnWarps][8];
-    float f[kMaxSplits][kAttnWarps][8];  // weight of each partial in the merge
+    float fw[kAttnWarps][8];          // weight of each warp's partial in the CTA's
+    float fc[kMaxSplits][8];          // weight of each CTA's partial in the unit's
     float inv_l[8];
-    float lse[8];
+    float rstat[kMaxSplits][16];      // received: (m, l) per head of every CTA of the cluster
+    float ro[8 * 128 + kMaxSplits];   // received: every CTA's partial of this CTA's output slice
     int wcount[kAttnWarps];
 };
 
@@ -85,7 +103,7 @@ __device__ __forceinline__ uint32_t keep_halves(uint32_t w, bool lo, bool hi)
     return w & ((lo ? 0x0000ffffu : 0u) | (hi ? 0xffff0000u : 0u));
 }
 
-template <int D, int T>
+template <int D, int T, bool SELECT>
 __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const AttnParams p)
 {
     constexpr int kPPS = kStepTok / T;      // pages per step
@@ -105,8 +123,9 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const AttnPar
     const int G = p.G;
 
     uint8_t* ring = smem;
-    int64_t* pg_row = reinterpret_cast<int64_t*>(smem + ring_region(D));  // physical page of list entry
-    int* pg_nv = reinterpret_cast<int*>(pg_row + p.max_tiles);            // its valid tokens
+    // the ring (or, before streaming, the selection scratch) spans p.region0 bytes
+    int64_t* pg_row = reinterpret_cast<int64_t*>(smem + p.region0);  // physical page of list entry
+    int* pg_nv = reinterpret_cast<int*>(pg_row + p.max_tiles);       // its valid tokens
 
     const size_t unit = (static_cast<size_t>(b) * p.L + p.layer) * p.Hkv + h;
 
@@ -137,10 +156,28 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const AttnPar
         seq = seq < 0 ? 0 : cap;
     }
     const int P = (seq + T - 1) / T;
-    int cnt = p.sel_cnt[unit];
-    if (cnt < 0 || cnt > p.Kmax) {
-        if (split == 0 && tid == 0) report(p.err, KVMM_ERR_OUT_OF_RANGE);
-        cnt = cnt < 0 ? 0 : p.Kmax;
+    const int32_t* sel_src = p.sel_idx + unit * p.Kmax;
+    int cnt;
+    if (SELECT && (p.rescore_mask == nullptr || p.rescore_mask[p.layer * p.Hkv + h] != 0)) {
+        // select this unit's pages from its scores (every CTA of the cluster
+        // computes the same selection; split 0 also writes it out)
+        auto& ts = *reinterpret_cast<BlockTopkShared<kAttnThreads>*>(smem);
+        float* sc_s = reinterpret_cast<float*>(smem + select_scratch_offset_scores());
+        int16_t* bin_s = reinterpret_cast<int16_t*>(sc_s + p.Pmax);
+        int32_t* sel_s = reinterpret_cast<int32_t*>(smem + select_scratch_offset_sel(p.Pmax));
+        cnt = block_topk<kAttnThreads>(p.scores + static_cast<size_t>(b * p.Hkv + h) * p.pstride, P, p.K, sel_s,
+                                       sc_s, bin_s, ts);
+        if (split == 0) {
+            for (int i = tid; i < cnt; i += kAttnThreads) p.sel_out[unit * p.Kmax + i] = sel_s[i];
+            if (tid == 0) p.cnt_out[unit] = cnt;
+        }
+        sel_src = sel_s;
+    } else {
+        cnt = p.sel_cnt[unit];
+        if (cnt < 0 || cnt > p.Kmax) {
+            if (split == 0 && tid == 0) report(p.err, KVMM_ERR_OUT_OF_RANGE);
+            cnt = cnt < 0 ? 0 : p.Kmax;
+        }
     }
     const int beg = static_cast<int>(static_cast<long long>(cnt) * split / p.splits);
     const int end = static_cast<int>(static_cast<long long>(cnt) * (split + 1) / p.splits);
@@ -152,7 +189,7 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const AttnPar
         int64_t row = -1;
         int nv = 0;
         if (i < end) {
-            const int lp = p.sel_idx[unit * p.Kmax + i];
+            const int lp = sel_src[i];
             if (lp < 0 || lp >= P) {
                 report(p.err, KVMM_ERR_OUT_OF_RANGE);
             } else {
@@ -339,11 +376,12 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const AttnPar
             mbar_wait_bounded(&sh.bar[warp][k % kSteps], (k / kSteps) & 1, 100000000ull);
     }
 
-    // ---- merge: warps of the CTA, then the CTAs of the cluster ------------
+    // ---- merge: the CTA's warps, then the cluster's CTAs -------------------
     // Each warp leaves (m, l) per head and its unnormalised O^T in its own
-    // ring slot; after a cluster barrier every CTA of the cluster (the unit's
-    // splits) combines an equal share of the outputs from all partials
-    // through distributed shared memory.
+    // ring slot; the CTA combines them into one partial and stores into every
+    // CTA of the cluster (the unit's splits) the slice of the outputs that CTA
+    // owns (remote shared-memory stores).  After one cluster barrier every CTA
+    // combines the partials of its slice locally and writes it out.
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) {
         l0 += __shfl_xor_sync(kFullMask, l0, off);
@@ -365,56 +403,79 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const AttnPar
         w0[16 * i + gid + 8] = o[i][2];
         w1[16 * i + gid + 8] = o[i][3];
     }
-    cluster_sync();
+    __syncthreads();
 
     const int nsp = p.splits;  // CTAs in the cluster
     const uint32_t rank = cluster_ctarank();
+    const int n_out = G * D;
+    const int slice = (n_out + nsp - 1) / nsp;  // outputs owned by each CTA
     if (tid < G) {
-        const int g = tid;
         float M = -INFINITY;
-        for (int s = 0; s < nsp; ++s)
 #pragma unroll
-            for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, ld_dsmem_f32(&sh.m[w][g], s));
+        for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, sh.m[w][tid]);
         float L = 0.f;
-        for (int s = 0; s < nsp; ++s)
 #pragma unroll
-            for (int w = 0; w < kAttnWarps; ++w) {
-                const float mw = ld_dsmem_f32(&sh.m[w][g], s);
-                const float f = (mw == -INFINITY) ? 0.f : exp2f(mw - M);
-                sh.f[s][w][g] = f;
-                L = fmaf(ld_dsmem_f32(&sh.l[w][g], s), f, L);
-            }
-        sh.inv_l[g] = L > 0.f ? 1.f / L : 0.f;
-        sh.lse[g] = L > 0.f ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
+        for (int w = 0; w < kAttnWarps; ++w) {
+            const float mw = sh.m[w][tid];
+            const float f = (mw == -INFINITY) ? 0.f : exp2f(mw - M);
+            sh.fw[w][tid] = f;
+            L = fmaf(sh.l[w][tid], f, L);
+        }
+        for (int r = 0; r < nsp; ++r) {
+            st_dsmem_f32(&sh.rstat[rank][tid], r, M);
+            st_dsmem_f32(&sh.rstat[rank][8 + tid], r, L);
+        }
     }
     __syncthreads();
-    const int n_out = G * D;
-    for (int e = static_cast<int>(rank) * kAttnThreads + tid; e < n_out; e += nsp * kAttnThreads) {
-        const int g = e / D, d = e - g * D;
+    for (int e = tid; e < n_out; e += kAttnThreads) {
+        const int g = e / D;
         float O = 0.f;
-        for (int s = 0; s < nsp; ++s)
 #pragma unroll
-            for (int w = 0; w < kAttnWarps; ++w) {
-                const float* src = reinterpret_cast<const float*>(ring + static_cast<size_t>(w) * kSteps * step_bytes(D)) + g * D + d;
-                O = fmaf(sh.f[s][w][g], ld_dsmem_f32(src, s), O);
-            }
-        const size_t oi = static_cast<size_t>(b) * p.Hq + static_cast<size_t>(h) * G + g;
-        p.out[oi * D + d] = O * sh.inv_l[g];
-        if (d == 0 && p.lse) p.lse[oi] = sh.lse[g];
+        for (int w = 0; w < kAttnWarps; ++w)
+            O = fmaf(sh.fw[w][g], reinterpret_cast<const float*>(ring + static_cast<size_t>(w) * kSteps * step_bytes(D))[e], O);
+        const int r = e / slice;
+        st_dsmem_f32(&sh.ro[rank * slice + (e - r * slice)], r, O);
     }
-    cluster_sync();  // no CTA leaves while its partials may still be read
+    cluster_sync();  // every CTA's partial of every slice has arrived
+
+    if (tid < G) {
+        float M = -INFINITY;
+        for (int c = 0; c < nsp; ++c) M = fmaxf(M, sh.rstat[c][tid]);
+        float L = 0.f;
+        for (int c = 0; c < nsp; ++c) {
+            const float mc = sh.rstat[c][tid];
+            const float f = (mc == -INFINITY) ? 0.f : exp2f(mc - M);
+            sh.fc[c][tid] = f;
+            L = fmaf(sh.rstat[c][8 + tid], f, L);
+        }
+        sh.inv_l[tid] = L > 0.f ? 1.f / L : 0.f;
+        if (rank == 0 && p.lse) {
+            const size_t oi = static_cast<size_t>(b) * p.Hq + static_cast<size_t>(h) * G + tid;
+            p.lse[oi] = L > 0.f ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
+        }
+    }
+    __syncthreads();
+    const int e0 = static_cast<int>(rank) * slice;
+    const int e1 = min(n_out, e0 + slice);
+    float* ob = p.out + (static_cast<size_t>(b) * p.Hq + static_cast<size_t>(h) * G) * D;
+    for (int e = e0 + tid; e < e1; e += kAttnThreads) {
+        const int g = e / D;
+        float O = 0.f;
+        for (int c = 0; c < nsp; ++c) O = fmaf(sh.fc[c][g], sh.ro[c * slice + (e - e0)], O);
+        ob[e] = O * sh.inv_l[g];
+    }
 }
 
 template <int D, int T>
-void (*attn_kernel())(AttnParams)
+void (*attn_kernel(bool select))(AttnParams)
 {
-    return sparse_attn_kernel<D, T>;
+    return select ? sparse_attn_kernel<D, T, true> : sparse_attn_kernel<D, T, false>;
 }
 
-void (*attn_kernel_for(int D, int T))(AttnParams)
+void (*attn_kernel_for(int D, int T, bool select))(AttnParams)
 {
-    if (D == 128) return T == 16 ? attn_kernel<128, 16>() : attn_kernel<128, 32>();
-    return T == 16 ? attn_kernel<64, 16>() : attn_kernel<64, 32>();
+    if (D == 128) return T == 16 ? attn_kernel<128, 16>(select) : attn_kernel<128, 32>(select);
+    return T == 16 ? attn_kernel<64, 16>(select) : attn_kernel<64, 32>(select);
 }
 
 // opt-ins of one kernel instantiation, once per device
@@ -425,7 +486,7 @@ cudaError_t prepare_attn(void (*kernel)(AttnParams), size_t smem)
         int dev;
         size_t bytes;
     };
-    static thread_local Prepared cache[4] = {};
+    static thread_local Prepared cache[8] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -443,16 +504,23 @@ cudaError_t prepare_attn(void (*kernel)(AttnParams), size_t smem)
     return cudaSuccess;
 }
 
-size_t attention_smem_bytes_impl(int D, int max_pages)
+size_t region0_bytes(int D, size_t scratch)
 {
-    return ring_region(D) + size_t(max_pages) * (sizeof(int64_t) + sizeof(int));
+    const size_t r = ring_region(D) > scratch ? ring_region(D) : scratch;
+    return (r + 15) & ~static_cast<size_t>(15);
+}
+
+size_t attention_smem_bytes_impl(int D, int max_pages, size_t scratch)
+{
+    return region0_bytes(D, scratch) + size_t(max_pages) * (sizeof(int64_t) + sizeof(int));
 }
 
 // clusters of `c` attention CTAs the device holds at once (0 = not launchable)
-int active_clusters(const kvmm_shape& s, int c)
+int active_clusters(const kvmm_shape& s, int c, bool select)
 {
-    void (*kernel)(AttnParams) = attn_kernel_for(s.D, s.T);
-    const size_t smem = attention_smem_bytes(s.D, (s.Kmax + c - 1) / c);
+    void (*kernel)(AttnParams) = attn_kernel_for(s.D, s.T, select);
+    const size_t smem =
+        attention_smem_bytes(s.D, (s.Kmax + c - 1) / c, select ? attention_select_scratch(s.Pmax, s.Kmax) : 0);
     if (prepare_attn(kernel, smem) != cudaSuccess) {
         cudaGetLastError();
         return 0;
@@ -477,26 +545,28 @@ int active_clusters(const kvmm_shape& s, int c)
 }
 
 struct SplitCache {
-    int dev, D, T, Kmax, units, splits, max_splits;
+    int dev, D, T, Kmax, Pmax, units, select, splits, max_splits;
 };
 thread_local SplitCache g_split_cache[8] = {};
 thread_local int g_split_next = 0;
 
-SplitCache& split_entry(const kvmm_shape& s)
+SplitCache& split_entry(const kvmm_shape& s, bool select)
 {
     int dev = 0;
     cudaGetDevice(&dev);
     const int units = s.B * s.Hkv;
+    const int pm = select ? s.Pmax : 0;  // the selecting kernel's scratch depends on Pmax
     for (auto& c : g_split_cache)
-        if (c.max_splits > 0 && c.dev == dev && c.D == s.D && c.T == s.T && c.Kmax == s.Kmax && c.units == units)
+        if (c.max_splits > 0 && c.dev == dev && c.D == s.D && c.T == s.T && c.Kmax == s.Kmax && c.Pmax == pm &&
+            c.units == units && c.select == int(select))
             return c;
     SplitCache& c = g_split_cache[g_split_next++ % 8];
-    c = {dev, s.D, s.T, s.Kmax, units, 1, 1};
+    c = {dev, s.D, s.T, s.Kmax, pm, units, int(select), 1, 1};
     // largest launchable cluster, and the largest split count whose clusters
     // for every unit fit on the device in one wave
     int best = 1;
     for (int k = 2; k <= kMaxSplits && k <= s.Kmax; ++k) {
-        const int n = active_clusters(s, k);
+        const int n = active_clusters(s, k, select);
         if (n <= 0) break;
         c.max_splits = k;
         if (n >= units) best = k;
@@ -507,16 +577,26 @@ SplitCache& split_entry(const kvmm_shape& s)
 
 }  // namespace
 
-int attention_max_splits(const kvmm_shape& s) { return split_entry(s).max_splits; }
+int attention_max_splits(const kvmm_shape& s, bool select) { return split_entry(s, select).max_splits; }
 
-int attention_slots_per_unit(const kvmm_shape& s) { return split_entry(s).splits; }
+int attention_slots_per_unit(const kvmm_shape& s, bool select) { return split_entry(s, select).splits; }
 
-size_t attention_smem_bytes(int D, int max_pages) { return attention_smem_bytes_impl(D, max_pages); }
+size_t attention_smem_bytes(int D, int max_pages, size_t scratch)
+{
+    return attention_smem_bytes_impl(D, max_pages, scratch);
+}
+
+size_t attention_region0(int D, size_t scratch) { return region0_bytes(D, scratch); }
+
+size_t attention_select_scratch(int Pmax, int Kmax)
+{
+    return select_scratch_offset_sel(Pmax) + size_t(Kmax) * sizeof(int32_t);
+}
 
 cudaError_t launch_sparse_attention(const AttnParams& p, cudaStream_t stream)
 {
-    void (*kernel)(AttnParams) = attn_kernel_for(p.D, p.T);
-    const size_t smem = attention_smem_bytes(p.D, p.max_tiles);
+    void (*kernel)(AttnParams) = attn_kernel_for(p.D, p.T, p.select != 0);
+    const size_t smem = static_cast<size_t>(p.region0) + size_t(p.max_tiles) * (sizeof(int64_t) + sizeof(int));
     const cudaError_t e = prepare_attn(kernel, smem);
     if (e != cudaSuccess) return e;
     return launch_pdl_cluster(kernel, dim3(p.splits, p.Hkv, p.B), dim3(kAttnThreads), smem, stream,

@@ -1,0 +1,290 @@
+// topk_block.cuh -- exact top-K page selection by one thread block.
+//
+// FlexiCache (MLSys'26 blog summary), "Core method, 2. MinMax-metadata page
+// scoring": the K highest-scoring pages of a (layer, KV head) are kept.
+// Ties go to the lower page index; the K pages are emitted in ascending
+// page order (the layout of sel_idx).
+//
+// One pass buckets the unit's P scores into kTopkBins bins between their
+// minimum and maximum (the bin is monotone in the score), a suffix scan
+// finds the bin holding the K-th largest score, the few scores in that bin
+// are ranked exactly (value descending, page ascending), and an ordered
+// compaction writes the winners.  Degenerate inputs (a crowded threshold
+// bin, a non-finite range) take an exact 4-pass radix select over
+// order-preserving keys.  Used with 512 threads by the selection kernel and
+// with the attention CTA's 128 threads when attention selects its own pages.
+#pragma once
+
+#include <cfloat>
+
+#include "common.cuh"
+
+namespace kvmm {
+
+constexpr int kTopkBins = 2048;
+constexpr int kTopkCandMax = 1024;
+
+template <int THREADS>
+struct BlockTopkShared {
+    static constexpr int kWarps = THREADS / 32;
+    int hist[kTopkBins];
+    int cand[kTopkCandMax];
+    float wmin[kWarps];
+    float wmax[kWarps];
+    int wsum[kWarps];
+    int rhist[256];
+    int ncand;
+    int tb;
+    int need;
+    int cbin;
+    int digit;
+    int remaining;
+};
+
+// float -> unsigned key with the same order
+__device__ __forceinline__ uint32_t topk_order_key(float f)
+{
+    const uint32_t u = __float_as_uint(f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Exact top-K over the P scores in sc[] by 4 radix passes; writes sel[0..K) ascending.
+template <int THREADS>
+__device__ void block_radix_topk(const float* sc, int P, int K, int32_t* sel, BlockTopkShared<THREADS>& ts)
+{
+    constexpr int kWarps = THREADS / 32;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    uint32_t prefix = 0, pmask = 0;
+    int remaining = K;
+    const int P_round = (P + THREADS - 1) / THREADS * THREADS;
+    for (int shift = 24; shift >= 0; shift -= 8) {
+        for (int i = tid; i < 256; i += THREADS) ts.rhist[i] = 0;
+        __syncthreads();
+        for (int i = tid; i < P_round; i += THREADS) {
+            const uint32_t key = i < P ? topk_order_key(sc[i]) : 0u;
+            const bool cand = i < P && (key & pmask) == prefix;
+            const unsigned active = __ballot_sync(kFullMask, cand);
+            if (cand) {
+                const uint32_t digit = (key >> shift) & 255u;
+                const unsigned peers = __match_any_sync(active, digit);
+                if (lane == __ffs(peers) - 1) atomicAdd(&ts.rhist[digit], __popc(peers));
+            }
+        }
+        __syncthreads();
+        if (warp == 0) {
+            int c[8];
+            int tot = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                c[j] = ts.rhist[255 - 8 * lane - j];
+                tot += c[j];
+            }
+            int incl = tot;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int v = __shfl_up_sync(kFullMask, incl, off);
+                if (lane >= off) incl += v;
+            }
+            const int excl = incl - tot;
+            if (excl < remaining && remaining <= incl) {
+                int acc = excl;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    if (acc + c[j] >= remaining) {
+                        ts.digit = 255 - 8 * lane - j;
+                        ts.remaining = remaining - acc;
+                        break;
+                    }
+                    acc += c[j];
+                }
+            }
+        }
+        __syncthreads();
+        prefix |= static_cast<uint32_t>(ts.digit) << shift;
+        pmask |= 255u << shift;
+        remaining = ts.remaining;
+        __syncthreads();
+    }
+    const uint32_t thr = prefix;
+    int out_base = 0, eq_base = 0;
+    const unsigned lt_mask = (1u << lane) - 1u;
+    for (int t0 = 0; t0 < P; t0 += THREADS) {
+        const int i = t0 + tid;
+        const uint32_t key = i < P ? topk_order_key(sc[i]) : 0u;
+        const bool gt = i < P && key > thr;
+        const bool eq = i < P && key == thr;
+        const unsigned eqb = __ballot_sync(kFullMask, eq);
+        if (lane == 0) ts.wsum[warp] = __popc(eqb);
+        __syncthreads();
+        int eq_off = eq_base, eq_all = 0;
+        for (int w2 = 0; w2 < kWarps; ++w2) {
+            const int t = ts.wsum[w2];
+            if (w2 < warp) eq_off += t;
+            eq_all += t;
+        }
+        __syncthreads();
+        const bool take = gt || (eq && eq_off + __popc(eqb & lt_mask) < remaining);
+        const unsigned tb = __ballot_sync(kFullMask, take);
+        if (lane == 0) ts.wsum[warp] = __popc(tb);
+        __syncthreads();
+        int out_off = out_base, out_all = 0;
+        for (int w2 = 0; w2 < kWarps; ++w2) {
+            const int t = ts.wsum[w2];
+            if (w2 < warp) out_off += t;
+            out_all += t;
+        }
+        if (take) sel[out_off + __popc(tb & lt_mask)] = i;
+        out_base += out_all;
+        eq_base += eq_all;
+        __syncthreads();
+    }
+}
+
+// Selects the top K of the P scores at `scores` (global memory, read through
+// L2) into sel[] (shared or global memory) and returns the count, min(K, P).
+// sc (P floats) and bin (P int16) are shared-memory scratch.  Every thread of
+// the block must call it; sel[] is complete for every thread on return.
+template <int THREADS>
+__device__ int block_topk(const float* scores, int P, int K, int32_t* sel, float* sc, int16_t* bin,
+                          BlockTopkShared<THREADS>& ts)
+{
+    constexpr int kWarps = THREADS / 32;
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    if (K >= P) {
+        for (int i = tid; i < P; i += THREADS) sel[i] = i;
+        __syncthreads();
+        return P;
+    }
+
+    // 1. scores to shared memory (16 loads in flight per thread), their range, an empty histogram
+    constexpr int kBatch = 16;
+    float lo = FLT_MAX, hi = -FLT_MAX;
+    for (int c0 = 0; c0 < P; c0 += THREADS * kBatch) {
+        float v[kBatch];
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j) {
+            const int i = c0 + j * THREADS + tid;
+            v[j] = i < P ? __ldcg(scores + i) : 0.f;
+        }
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j) {
+            const int i = c0 + j * THREADS + tid;
+            if (i < P) {
+                sc[i] = v[j];
+                lo = fminf(lo, v[j]);
+                hi = fmaxf(hi, v[j]);
+            }
+        }
+    }
+    for (int i = tid; i < kTopkBins; i += THREADS) ts.hist[i] = 0;
+    if (tid == 0) ts.ncand = 0;
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+        lo = fminf(lo, __shfl_xor_sync(kFullMask, lo, off));
+        hi = fmaxf(hi, __shfl_xor_sync(kFullMask, hi, off));
+    }
+    if (lane == 0) {
+        ts.wmin[warp] = lo;
+        ts.wmax[warp] = hi;
+    }
+    __syncthreads();
+    float mn = ts.wmin[0], mx = ts.wmax[0];
+    for (int w = 1; w < kWarps; ++w) {
+        mn = fminf(mn, ts.wmin[w]);
+        mx = fmaxf(mx, ts.wmax[w]);
+    }
+    if (!(mx > mn)) {  // every score equal: the K lowest pages win the ties
+        for (int i = tid; i < K; i += THREADS) sel[i] = i;
+        __syncthreads();
+        return K;
+    }
+    const float scale = static_cast<float>(kTopkBins) / (mx - mn);
+    if (!(scale < FLT_MAX)) {
+        block_radix_topk<THREADS>(sc, P, K, sel, ts);
+        return K;
+    }
+
+    // 2. bucket every score: bin(s) = floor((s - mn) * scale) is monotone in s
+    for (int i = tid; i < P; i += THREADS) {
+        const int bi = min(kTopkBins - 1, static_cast<int>((sc[i] - mn) * scale));
+        bin[i] = static_cast<int16_t>(bi);
+        atomicAdd(&ts.hist[bi], 1);
+    }
+    __syncthreads();
+
+    // 3. the bin holding the K-th largest score: suffix sums over bins
+    constexpr int kBinsPerThread = kTopkBins / THREADS;
+    int local = 0;
+#pragma unroll
+    for (int j = 0; j < kBinsPerThread; ++j) local += ts.hist[kBinsPerThread * tid + j];
+    int incl = local;  // inclusive suffix within the warp (lanes >= this one)
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int v = __shfl_down_sync(kFullMask, incl, off);
+        if (lane + off < 32) incl += v;
+    }
+    if (lane == 0) ts.wsum[warp] = incl;
+    __syncthreads();
+    int above = incl - local;
+    for (int w = warp + 1; w < kWarps; ++w) above += ts.wsum[w];
+    if (above < K && K <= above + local) {
+        int acc = above;
+        for (int j = kBinsPerThread - 1; j >= 0; --j) {
+            const int bj = kBinsPerThread * tid + j;
+            if (acc + ts.hist[bj] >= K) {
+                ts.tb = bj;
+                ts.need = K - acc;
+                ts.cbin = ts.hist[bj];
+                break;
+            }
+            acc += ts.hist[bj];
+        }
+    }
+    __syncthreads();
+    const int tb = ts.tb, need = ts.need, cbin = ts.cbin;
+    if (cbin > kTopkCandMax) {  // crowded threshold bin: exact radix path
+        block_radix_topk<THREADS>(sc, P, K, sel, ts);
+        return K;
+    }
+
+    // 4. rank the threshold bin's scores exactly; mark the winners above every bin
+    for (int i = tid; i < P; i += THREADS)
+        if (bin[i] == tb) ts.cand[atomicAdd(&ts.ncand, 1)] = i;
+    __syncthreads();
+    for (int t = tid; t < cbin; t += THREADS) {
+        const int i = ts.cand[t];
+        const float s = sc[i];
+        int rank = 0;
+        for (int j = 0; j < cbin; ++j) {
+            const int i2 = ts.cand[j];
+            const float s2 = sc[i2];
+            rank += (s2 > s) || (s2 == s && i2 < i);
+        }
+        if (rank < need) bin[i] = static_cast<int16_t>(kTopkBins);
+    }
+    __syncthreads();
+
+    // 5. ordered compaction: thread t emits the winners among pages [t*m, t*m + m)
+    const int m = (P + THREADS - 1) / THREADS;
+    const int i0 = min(P, tid * m), i1 = min(P, i0 + m);
+    int mine = 0;
+    for (int i = i0; i < i1; ++i) mine += bin[i] > tb;
+    int pre = mine;  // inclusive prefix within the warp
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int v = __shfl_up_sync(kFullMask, pre, off);
+        if (lane >= off) pre += v;
+    }
+    if (lane == 31) ts.wsum[warp] = pre;
+    __syncthreads();
+    int pos = pre - mine;
+    for (int w = 0; w < warp; ++w) pos += ts.wsum[w];
+    for (int i = i0; i < i1; ++i)
+        if (bin[i] > tb) sel[pos++] = i;
+    __syncthreads();
+    return K;
+}
+
+}  // namespace kvmm
