@@ -3,9 +3,10 @@
 One step = one decode step of the Llama-3.1-8B-shaped 32K-context workload
 (32 layers, B=8, 32 query / 8 KV heads, head_dim 128, 16-token pages,
 budget 128 pages): per layer, append the new token and refresh its page's
-MinMax (kv_minmax_update), score every page and select the top-K
-(page_score_topk), attend over the selected pages (sparse_paged_decode_attn;
---fused runs both as one page_score_topk_attn launch), and list promoted pages
+MinMax (kv_minmax_update), score every page, select the top-K and attend over
+the selected pages (page_score_topk_attn: the scoring kernel, then the
+attention kernel that selects its own pages; --unfused runs page_score_topk
+and sparse_paged_decode_attn instead), and list promoted pages
 (topk_promotion_diff, on a side stream).  A layer-step is one layer of
 that step for the whole batch.
 
@@ -286,7 +287,7 @@ def gpu_arm(args):
     side = torch.cuda.Stream()
     forks = [torch.cuda.Event() for _ in range(L)]
 
-    fused = args.fused
+    fused = not args.unfused
 
     def step(instrument):
         main = torch.cuda.current_stream()
@@ -295,7 +296,7 @@ def gpu_arm(args):
                                   st.v_pool, st.block_table, st.meta, st.err)
             if instrument:
                 ev_s[4 * l].record()
-            if fused:  # scoring, selection and attention in one launch
+            if fused:  # scoring, then attention that selects its own pages
                 st.select_attend(l, q_dev[l])
             else:
                 st.select(l, q_dev[l])
@@ -418,8 +419,8 @@ def gpu_arm(args):
     peak, peak_kind = peaks()
     s_ms, a_ms = statistics.mean(score_ms), statistics.mean(attn_ms)
     if fused:
-        dom, dom_ms, dom_bytes = "fused_decode_kernel", s_ms, acc["fused_launch"]
-        kernel_ms = {"fused_decode_kernel": s_ms}
+        dom, dom_ms, dom_bytes = "page_score_topk_attn", s_ms, acc["fused_launch"]
+        kernel_ms = {"page_score_topk_attn": s_ms}
     else:
         dom = "sparse_attn_kernel" if a_ms >= s_ms else "score_topk_kernel"
         dom_ms = max(a_ms, s_ms)
@@ -440,7 +441,7 @@ def gpu_arm(args):
                    "l2": "inputs larger than L2 (4 GiB of distinct data per step, no flush)",
                    "step": f"one decode step = {L} layer-steps, " + ("eager launches" if args.no_graph
                                                                      else "CUDA graph replay"),
-                   "path": "page_score_topk_attn (one launch)" if fused
+                   "path": "page_score_topk_attn (scoring kernel + selecting attention kernel)" if fused
                            else "page_score_topk + sparse_paged_decode_attn"},
         "kv_gbs": kv_gbs, "pct_hbm_peak": kv_gbs / peak,
         "bytes_per_layer_step": acc["total"],
@@ -454,8 +455,8 @@ def gpu_arm(args):
         "e2e": {"value": e2e_steps * L * world / (e2e_ms / 1e3), "unit": "layer-steps/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "how": "pinned host q/new K,V -> device, graph replay, out/lse/promoted counts -> pinned host"},
-        # per layer: update, fused select+attend, diff (fused) or update, score, top-K, diff, attention
-        "gpu_launches": (3 if fused else 5) * L * args.steps,
+        # per layer: update, score, selecting attention, diff (fused) or update, score, top-K, diff, attention
+        "gpu_launches": (4 if fused else 5) * L * args.steps,
         "clocks": clk,
         "device_err": err_word,
     }
@@ -486,8 +487,8 @@ def main():
     ap.add_argument("--no-graph", action="store_true", help="launch eagerly (for profilers)")
     ap.add_argument("--batch", type=int, default=0, help="override the batch (smaller profiling case)")
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (smaller profiling case)")
-    ap.add_argument("--fused", action="store_true",
-                    help="one page_score_topk_attn launch per layer instead of page_score_topk + sparse_paged_decode_attn")
+    ap.add_argument("--unfused", action="store_true",
+                    help="page_score_topk + sparse_paged_decode_attn instead of page_score_topk_attn")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.impl == "reference":

@@ -290,7 +290,11 @@ kvmm_status page_score_topk_attn(const kvmm_shape* shape, int32_t layer, const k
     const size_t scratch = kvmm::attention_select_scratch(s.Pmax, s.Kmax);
     const int splits = resolve_splits(s, 0, true);
     const int max_pages = (s.Kmax + splits - 1) / splits;
-    if (kvmm::attention_smem_bytes(s.D, max_pages, scratch) > 200 * 1024) {
+    // the unit's block-table row in shared memory too, when its rows are 16-byte aligned and short
+    const bool bt_prefetch = s.Pmax % 4 == 0 && s.Pmax <= 4096;
+    const size_t base_smem = kvmm::attention_smem_bytes(s.D, max_pages, scratch);
+    const size_t bt_offset = (base_smem + 15) & ~static_cast<size_t>(15);
+    if (bt_offset + (bt_prefetch ? size_t(s.Pmax) * 4 : 0) > 200 * 1024) {
         // the selection does not fit the attention CTA's shared memory: separate kernels
         st = page_score_topk(shape, layer, q, meta, seq_len, rescore_mask, K, group_reduce, sel_idx, sel_cnt,
                              scores_out, workspace, workspace_bytes, err, stream);
@@ -341,6 +345,8 @@ kvmm_status page_score_topk_attn(const kvmm_shape* shape, int32_t layer, const k
     p.select = 1;
     p.K = K;
     p.pstride = s.Pmax;
+    p.bt_prefetch = bt_prefetch ? 1 : 0;
+    p.bt_offset = static_cast<int32_t>(bt_offset);
     p.n_phys = s.n_phys;
     p.scale_log2 = (sm_scale > 0.f ? sm_scale : 1.0f / std::sqrt(static_cast<float>(s.D))) * 1.4426950408889634f;
     p.q = q;

@@ -62,6 +62,8 @@ struct AttnParams {
     int32_t select;      // 1: rescored units select their pages from `scores` first
     int32_t K;           // select: pages to keep
     int32_t pstride;     // select: floats between the score rows of two units
+    int32_t bt_prefetch; // select: copy each unit's block-table row to shared memory (16-byte aligned rows)
+    int32_t bt_offset;   // select: its shared-memory offset
     int64_t n_phys;
     float scale_log2;    // sm_scale * log2(e)
     const kvmm_bf16* q;

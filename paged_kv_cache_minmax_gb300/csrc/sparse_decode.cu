@@ -11,7 +11,8 @@
 // over `splits` CTAs.  A CTA first resolves its pages through the block table
 // into a compacted list (null / out-of-range entries dropped and reported),
 // then its warps take steps of 32 tokens (two 16-token pages or one 32-token
-// page) round robin.  Each warp keeps two steps in flight in a private ring:
+// page) round robin.  Each warp keeps kSteps steps in flight in a private ring
+// (eight warps of one step: 128 KiB per CTA at D = 128):
 // every page's K block ([T][D]) and V block ([D][T]) is one contiguous run of
 // bytes, moved by a 1-D bulk copy (TMA) into shared memory, the copies of a
 // step issued from different lanes and completing on one mbarrier.
@@ -41,10 +42,10 @@
 #include "topk_block.cuh"
 
 #ifndef KVMM_ATTN_WARPS
-#define KVMM_ATTN_WARPS 4
+#define KVMM_ATTN_WARPS 8
 #endif
 #ifndef KVMM_ATTN_STEPS
-#define KVMM_ATTN_STEPS 2
+#define KVMM_ATTN_STEPS 1
 #endif
 
 namespace kvmm {
@@ -54,7 +55,7 @@ constexpr int kAttnWarps = KVMM_ATTN_WARPS;
 constexpr int kAttnThreads = kAttnWarps * 32;
 constexpr int kSteps = KVMM_ATTN_STEPS;  // steps in flight per warp
 constexpr int kStepTok = 32;             // tokens per step (two 16-token sub-tiles)
-static_assert(kSteps >= 2, "double buffering needs two steps");
+static_assert(kSteps >= 1, "at least one step in flight per warp");
 
 __host__ __device__ constexpr int step_bytes(int D) { return 2 * kStepTok * D * 2; }  // K then V
 __host__ __device__ constexpr size_t ring_bytes(int D) { return size_t(kAttnWarps) * kSteps * step_bytes(D); }
@@ -80,6 +81,7 @@ __host__ __device__ constexpr size_t select_scratch_offset_sel(int Pmax)
 
 struct AttnShared {
     uint64_t bar[kAttnWarps][kSteps];
+    uint64_t bt_bar;                  // the unit's block-table row (selecting kernel)
     float m[kAttnWarps][8];
     float l[kAttnWarps][8];
     float fw[kAttnWarps][8];          // weight of each warp's partial in the CTA's
@@ -130,6 +132,7 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const AttnPar
     const size_t unit = (static_cast<size_t>(b) * p.L + p.layer) * p.Hkv + h;
 
     if (tid < kAttnWarps * kSteps) mbar_init(&sh.bar[tid / kSteps][tid % kSteps], 1);
+    if (tid == 0) mbar_init(&sh.bt_bar, 1);
     fence_barrier_init();
     pdl_launch_dependents();
     pdl_wait();  // every input may come from the preceding kernels
@@ -157,8 +160,17 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const AttnPar
     }
     const int P = (seq + T - 1) / T;
     const int32_t* sel_src = p.sel_idx + unit * p.Kmax;
+    const bool selecting = SELECT && (p.rescore_mask == nullptr || p.rescore_mask[p.layer * p.Hkv + h] != 0);
+    // the selecting kernel fetches the unit's block-table row while it selects
+    const bool bt_prefetch = selecting && p.bt_prefetch && P > 0;
+    int32_t* bt_s = reinterpret_cast<int32_t*>(smem + p.bt_offset);
+    if (bt_prefetch && tid == 0) {
+        const uint32_t bytes = static_cast<uint32_t>((P + 3) / 4) * 16;  // within the 16-byte aligned row
+        mbar_arrive_expect_tx(&sh.bt_bar, bytes);
+        bulk_copy_g2s(bt_s, p.block_table + unit * p.Pmax, bytes, &sh.bt_bar);
+    }
     int cnt;
-    if (SELECT && (p.rescore_mask == nullptr || p.rescore_mask[p.layer * p.Hkv + h] != 0)) {
+    if (selecting) {
         // select this unit's pages from its scores (every CTA of the cluster
         // computes the same selection; split 0 also writes it out)
         auto& ts = *reinterpret_cast<BlockTopkShared<kAttnThreads>*>(smem);
@@ -182,6 +194,10 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const AttnPar
     const int beg = static_cast<int>(static_cast<long long>(cnt) * split / p.splits);
     const int end = static_cast<int>(static_cast<long long>(cnt) * (split + 1) / p.splits);
 
+    bool bt_ok = bt_prefetch;
+    if (bt_prefetch) bt_ok = __syncthreads_and(mbar_wait_bounded(&sh.bt_bar, 0)) != 0;
+    if (bt_prefetch && !bt_ok && tid == 0) report(p.err, KVMM_ERR_TIMEOUT);  // read the table directly instead
+
     // resolve this CTA's pages and compact the valid ones (in selection order)
     int n_valid = 0;
     for (int i0 = beg; i0 < end; i0 += kAttnThreads) {
@@ -193,7 +209,7 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const AttnPar
             if (lp < 0 || lp >= P) {
                 report(p.err, KVMM_ERR_OUT_OF_RANGE);
             } else {
-                const int32_t phys = p.block_table[unit * p.Pmax + lp];
+                const int32_t phys = bt_ok ? bt_s[lp] : p.block_table[unit * p.Pmax + lp];
                 if (phys < 0) {
                     report(p.err, KVMM_ERR_NULL_BLOCK);
                 } else if (phys >= p.n_phys) {
@@ -596,7 +612,8 @@ size_t attention_select_scratch(int Pmax, int Kmax)
 cudaError_t launch_sparse_attention(const AttnParams& p, cudaStream_t stream)
 {
     void (*kernel)(AttnParams) = attn_kernel_for(p.D, p.T, p.select != 0);
-    const size_t smem = static_cast<size_t>(p.region0) + size_t(p.max_tiles) * (sizeof(int64_t) + sizeof(int));
+    size_t smem = static_cast<size_t>(p.region0) + size_t(p.max_tiles) * (sizeof(int64_t) + sizeof(int));
+    if (p.bt_prefetch) smem = static_cast<size_t>(p.bt_offset) + size_t(p.Pmax) * sizeof(int32_t);
     const cudaError_t e = prepare_attn(kernel, smem);
     if (e != cudaSuccess) return e;
     return launch_pdl_cluster(kernel, dim3(p.splits, p.Hkv, p.B), dim3(kAttnThreads), smem, stream,

@@ -26,6 +26,8 @@ constexpr int kTopkCandMax = 1024;
 
 template <int THREADS>
 struct BlockTopkShared {
+    static_assert(THREADS % 32 == 0 && kTopkBins % THREADS == 0 && THREADS <= kTopkBins,
+                  "the bins are split evenly over the block's threads");
     static constexpr int kWarps = THREADS / 32;
     int hist[kTopkBins];
     int cand[kTopkCandMax];
