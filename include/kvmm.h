@@ -279,6 +279,37 @@ kvmm_status page_score_topk_attn(const kvmm_shape* shape, int32_t layer, const k
                                  float* out, float* lse, void* workspace, size_t workspace_bytes,
                                  int32_t* err, kvmm_stream stream);
 
+/* ------------------------------------------------------------------------
+ * decode_layer -- one layer of a decode step in one launch: append the new
+ * tokens and refresh their pages' MinMax (kv_minmax_update), score every
+ * page and select the top K (page_score_topk), attend over the selected
+ * pages (sparse_paged_decode_attn).
+ *
+ * FlexiCache, "Core method, 2. MinMax-metadata page scoring" (the bounds are
+ * kept up to date as pages fill; every page is scored; the top-K pages of
+ * each layer and KV head are kept) and "Core method, 1" / "System design,
+ * head-level block table" (attention over the selected pages only).
+ *
+ * Arguments and results are those of the three calls: new_k / new_v
+ * ([B][Hkv][n_new][D], or both NULL to append nothing), n_new, tok_begin,
+ * tok_end as for kv_minmax_update (the appended rows are written to the
+ * pools and their pages' MinMax refreshed before those pages are scored);
+ * rescore_mask, K, group_reduce, sel_idx, sel_cnt, scores_out as for
+ * page_score_topk; sm_scale, out, lse as for sparse_paged_decode_attn.
+ * seq_len already counts the appended tokens.  Two units (batch, KV head)
+ * share one thread-block cluster, which scores, selects and attends entirely
+ * on chip: no workspace.  For shapes whose buffers do not fit one CTA's shared
+ * memory (long page tables), the call runs kv_minmax_update and then
+ * page_score_topk_attn instead, which need workspace (as for page_score_topk;
+ * otherwise workspace may be NULL and is not used).
+ */
+kvmm_status decode_layer(const kvmm_shape* shape, int32_t layer, const kvmm_bf16* q, const kvmm_bf16* new_k,
+                         const kvmm_bf16* new_v, int32_t n_new, const int32_t* tok_begin, const int32_t* tok_end,
+                         kvmm_bf16* k_pool, kvmm_bf16* v_pool, const int32_t* block_table, kvmm_bf16* meta,
+                         const int32_t* seq_len, const uint8_t* rescore_mask, int32_t K, int32_t group_reduce,
+                         float sm_scale, int32_t* sel_idx, int32_t* sel_cnt, float* scores_out, float* out,
+                         float* lse, void* workspace, size_t workspace_bytes, int32_t* err, kvmm_stream stream);
+
 /* Workspace bytes that page_score_topk and page_score_topk_attn need
  * (sparse_paged_decode_attn needs none; num_splits is accepted for the
  * stable signature and ignored).  Returns 0 for an unsupported shape. */

@@ -366,6 +366,75 @@ kvmm_status page_score_topk_attn(const kvmm_shape* shape, int32_t layer, const k
     return launched(kvmm::launch_sparse_attention(p, cs));
 }
 
+kvmm_status decode_layer(const kvmm_shape* shape, int32_t layer, const kvmm_bf16* q, const kvmm_bf16* new_k,
+                         const kvmm_bf16* new_v, int32_t n_new, const int32_t* tok_begin, const int32_t* tok_end,
+                         kvmm_bf16* k_pool, kvmm_bf16* v_pool, const int32_t* block_table, kvmm_bf16* meta,
+                         const int32_t* seq_len, const uint8_t* rescore_mask, int32_t K, int32_t group_reduce,
+                         float sm_scale, int32_t* sel_idx, int32_t* sel_cnt, float* scores_out, float* out,
+                         float* lse, void* workspace, size_t workspace_bytes, int32_t* err, kvmm_stream stream)
+{
+    kvmm_status st = check_shape(shape);
+    if (st != KVMM_OK) return st;
+    const kvmm_shape& s = *shape;
+    if (layer < 0 || layer >= s.L || K < 1 || K > s.Kmax || !std::isfinite(sm_scale)) return KVMM_INVALID_ARG;
+    if (group_reduce != 0 && group_reduce != 1) return KVMM_INVALID_ARG;
+    if ((new_k == nullptr) != (new_v == nullptr)) return KVMM_INVALID_ARG;
+    if (new_k != nullptr && (n_new < 1 || !req(new_k) || !req(new_v) || !req4(tok_begin) || !req4(tok_end)))
+        return KVMM_INVALID_ARG;
+    if (!req(q) || !req(meta) || !req(k_pool) || !req(v_pool) || !req4(block_table) || !req4(seq_len) ||
+        !req4(sel_idx) || !req4(sel_cnt) || !opt4(scores_out) || !req4(out) || !opt4(lse) || !opt(workspace) ||
+        !opt4(err))
+        return KVMM_INVALID_ARG;
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    const int C = kvmm::decode_layer_cluster(s);
+    if (kvmm::decode_layer_smem(s.D, s.T, s.Pmax, s.Kmax, C) > 220 * 1024) {
+        // the one-launch kernel's buffers do not fit: append, then the two-kernel call
+        if (workspace == nullptr || workspace_bytes < score_ws_bytes(s)) return KVMM_WORKSPACE_TOO_SMALL;
+        if (new_k != nullptr) {
+            st = kv_minmax_update(shape, layer, new_k, new_v, n_new, tok_begin, tok_end, k_pool, v_pool,
+                                  block_table, meta, err, stream);
+            if (st != KVMM_OK) return st;
+        }
+        return page_score_topk_attn(shape, layer, q, meta, k_pool, v_pool, block_table, seq_len, rescore_mask, K,
+                                    group_reduce, sm_scale, sel_idx, sel_cnt, scores_out, out, lse, workspace,
+                                    workspace_bytes, err, stream);
+    }
+    kvmm::DecodeParams p{};
+    p.B = s.B;
+    p.L = s.L;
+    p.Hq = s.Hq;
+    p.Hkv = s.Hkv;
+    p.G = s.Hq / s.Hkv;
+    p.D = s.D;
+    p.T = s.T;
+    p.Pmax = s.Pmax;
+    p.Kmax = s.Kmax;
+    p.layer = layer;
+    p.K = K;
+    p.C = C;
+    p.n_new = new_k != nullptr ? n_new : 0;
+    p.n_phys = s.n_phys;
+    p.scale_log2 = (sm_scale > 0.f ? sm_scale : 1.0f / std::sqrt(static_cast<float>(s.D))) * 1.4426950408889634f;
+    p.q = q;
+    p.new_k = new_k;
+    p.new_v = new_v;
+    p.tok_begin = tok_begin;
+    p.tok_end = tok_end;
+    p.k_pool = k_pool;
+    p.v_pool = v_pool;
+    p.block_table = block_table;
+    p.meta = meta;
+    p.seq_len = seq_len;
+    p.rescore_mask = rescore_mask;
+    p.sel_idx = sel_idx;
+    p.sel_cnt = sel_cnt;
+    p.scores_out = scores_out;
+    p.out = out;
+    p.lse = lse;
+    p.err = err;
+    return launched(kvmm::launch_decode_layer(p, group_reduce, cs));
+}
+
 kvmm_status topk_promotion_diff(const kvmm_shape* shape, int32_t layer,
                                 const uint8_t* rescore_mask, int32_t* prev_idx,
                                 int32_t* prev_cnt, const int32_t* cur_idx,

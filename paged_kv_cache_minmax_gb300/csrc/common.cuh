@@ -147,6 +147,20 @@ __device__ __forceinline__ void st_dsmem_f32(void* local, uint32_t rank, float v
     asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
 }
 
+// asynchronous store of v to the float at `local`'s address in CTA `rank` of
+// the cluster, completing 4 bytes of transaction on the mbarrier at
+// `local_bar`'s address in that CTA.  A thread that sees the barrier's phase
+// complete sees the value; the sender needs no fence.
+__device__ __forceinline__ void st_async_f32(void* local, uint64_t* local_bar, uint32_t rank, float v)
+{
+    uint32_t ra, rb;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_addr(local)), "r"(rank));
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rb) : "r"(smem_addr(local_bar)), "r"(rank));
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(ra),
+                 "r"(__float_as_uint(v)), "r"(rb)
+                 : "memory");
+}
+
 // ---------------------------------------------------------------------------
 // programmatic dependent launch: the next kernel in the stream may be
 // scheduled once every CTA of this one has called launch_dependents; a kernel
@@ -162,6 +176,13 @@ __device__ __forceinline__ uint4 ld_shared_v4(const void* p)
     asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                  : "r"(smem_addr(p)));
+    return v;
+}
+
+__device__ __forceinline__ uint2 ld_shared_v2(const void* p)
+{
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(smem_addr(p)));
     return v;
 }
 

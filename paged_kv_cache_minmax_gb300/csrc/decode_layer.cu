@@ -1,0 +1,1061 @@
+// decode_layer.cu -- one launch per layer: append the new tokens and refresh
+// their pages' MinMax, score every page, select the top K, attend over the
+// selected pages.
+//
+// FlexiCache (MLSys'26 blog summary), "Core method, 2. MinMax-metadata page
+// scoring" (per-page key bounds, kept up to date as pages fill; the query and
+// the bounds give each page's score; the top-K pages of every (layer, KV
+// head) are kept) and "Core method, 1. Stability-differentiated placement" /
+// "System design, head-level block table" (attention over the selected pages
+// only, found through [batch, layer, head, logical_block]).  The results
+// equal kv_minmax_update (appending) followed by page_score_topk_attn.
+//
+// Design (sm_103a).  A thread-block cluster of C CTAs owns two units (batch,
+// KV head).  Every CTA of it streams, in this order, its share of unit 0's
+// MinMax rows, its share of unit 1's, its share of unit 0's selected K/V
+// pages, its share of unit 1's:
+//   - 8 consumer warps each keep their own slots in flight (1-D bulk copies,
+//     TMA, one mbarrier per slot; two slots a warp for pages of 16 tokens, one
+//     for pages of 32).  A slot holds one page of K and V (an attention step)
+//     or the [min | max] rows of T consecutive pages (a score item): the same
+//     bytes.  A score item is scored on the tensor cores (mma.sync m16n8k16)
+//     and every score sent to every CTA of the cluster as an asynchronous
+//     remote store that completes on the receiver's mbarrier; a page of the
+//     item that receives new tokens first has its bounds widened by them.  An
+//     attention step runs S^T = K Q^T, the online softmax and O^T += V^T P^T
+//     with P as bf16 hi + lo.  At the end of a unit the warps combine their
+//     softmax partials and send every CTA its slice of the outputs, while
+//     their slots already fetch the next unit's pages;
+//   - 8 selector warps first take the bounds of the rows a partly filled page
+//     already holds (for the consumer that widens it) and append the new
+//     tokens (rows, and the MinMax of the pages this CTA owns); then, as soon
+//     as all of a unit's scores have arrived, they select the unit's top K
+//     exactly (block_topk) and resolve this CTA's share of the pages through
+//     the block table -- unit 0's selection overlaps the streaming of unit 1's
+//     rows, unit 1's overlaps unit 0's attention -- and finally combine each
+//     unit's partials into out and lse.
+// All exchange stays on chip (asynchronous remote shared-memory stores and
+// mbarriers), with no fence on the way: a consumer attending over a page that
+// receives tokens takes those rows from new_k / new_v rather than waiting for
+// the selectors' pool writes, which are for later launches.  Every wait is
+// bounded (KVMM_ERR_TIMEOUT, then the kernel runs to its end).
+#include <cfloat>
+#include <cmath>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "topk_block.cuh"
+
+namespace kvmm {
+namespace {
+
+constexpr int kDCons = 8;                      // consumer warps
+constexpr int kDSel0 = kDCons;                 // first selector warp
+constexpr int kDSelWarps = 8;
+constexpr int kDSelThreads = kDSelWarps * 32;
+constexpr int kDThreads = (kDCons + kDSelWarps) * 32;
+constexpr int kDUnits = 2;                     // units per cluster
+constexpr int kDSelBar = 1;                    // the selector warps' named barrier
+constexpr int kDRingMax = 2;
+
+// slots per consumer warp; a slot is one page of K and V (4TD bytes)
+__host__ __device__ constexpr int d_ring(int T) { return T == 16 ? 2 : 1; }
+
+using SelGroup = WarpGroup<kDSelBar, kDSel0 * 32, kDSelThreads>;
+
+constexpr uint64_t kDWaitNs = 1000000000ull;   // 1 s: far beyond any legitimate wait
+constexpr uint64_t kDAbortNs = 1000000ull;
+
+// one unit of the cluster as this CTA sees it, read from global memory once
+struct DUnit {
+    size_t ufull;   // its row of the [B][L][Hkv] arrays
+    int b, h;
+    int seq, P;     // sequence length (clamped to Pmax*T) and its pages
+    int lo, hi;     // the pages this CTA scores
+    int rescored;
+    int tb, te;     // tokens this launch appends (te <= tb: none)
+    int pb, pe;     // pages holding appended tokens that this CTA owns (the last CTA also owns those
+                    // at or past the unit's page count)
+};
+
+struct DecodeShared {
+    uint64_t full[kDCons][kDRingMax];  // a consumer warp's slot has landed
+    uint64_t qbar;            // the query groups of the cluster's units
+    uint64_t sbar[kDUnits];   // all of the unit's scores are here (asynchronous remote stores, 4 bytes each)
+    uint64_t selr[kDUnits];   // this CTA's share of the unit's pages is resolved
+    uint64_t rbar[kDUnits];   // every CTA's partial of this CTA's output slice is here (likewise)
+    uint64_t gbar;            // consumer-group barrier (kDCons arrivals per use)
+    uint64_t pbar;            // prior bounds written (one arrival per selector warp)
+    DUnit ud[kDUnits];
+    int resn[kDUnits];        // resolved pages of this CTA's share
+    int wcount[kDSelWarps];
+    float mm[kDCons][8];
+    float ml[kDCons][8];
+    float fw[kDCons][8];
+    float fc[kDMaxCluster][8];
+    float inv_l[8];
+    uint32_t prior[kDUnits][128];  // per unit: key-ordered bounds of the rows the first appended page
+                                   // already holds, [min | max], two channels a word (D <= 128)
+    int abort_flag;
+};
+
+__device__ __forceinline__ uint32_t bf16x2_min0(uint32_t w)
+{
+    const uint32_t neg = ((w >> 15) & 0x00010001u) * 0xffffu;
+    return w & neg;
+}
+__device__ __forceinline__ uint32_t bf16x2_max0(uint32_t w)
+{
+    const uint32_t neg = ((w >> 15) & 0x00010001u) * 0xffffu;
+    return w & ~neg;
+}
+
+__device__ __forceinline__ float fast_exp2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint32_t keep_halves(uint32_t w, bool lo, bool hi)
+{
+    return w & ((lo ? 0x0000ffffu : 0u) | (hi ? 0xffff0000u : 0u));
+}
+
+// bf16 pair -> pair of unsigned 16-bit keys ordered like the values
+__device__ __forceinline__ uint32_t to_key2(uint32_t w)
+{
+    const uint32_t neg = (w >> 15) & 0x00010001u;
+    return w ^ ((neg * 0xffffu) | 0x80008000u);
+}
+__device__ __forceinline__ uint32_t from_key2(uint32_t k)
+{
+    const uint32_t neg = ((~k) >> 15) & 0x00010001u;
+    return k ^ ((neg * 0xffffu) | 0x80008000u);
+}
+
+__device__ __forceinline__ int ld_volatile(const int* p) { return *reinterpret_cast<const volatile int*>(p); }
+
+// the shared-memory plan, identical on host and device
+struct DLayout {
+    size_t ring, part, qbuf, sbuf, bins, ts, selv, res, recv, total;
+    int pstride, slice, recv_stride;
+};
+__host__ __device__ inline size_t d_align(size_t n) { return (n + 127) & ~static_cast<size_t>(127); }
+__host__ __device__ inline DLayout d_layout(int D, int T, int Pmax, int Kmax, int C, int maxp)
+{
+    DLayout l{};
+    l.pstride = (Pmax + 3) & ~3;
+    l.slice = (8 * D + C - 1) / C;
+    l.recv_stride = 16 * C + l.slice * C;
+    l.ring = 0;
+    l.part = d_align(l.ring + size_t(kDCons) * d_ring(T) * 4 * T * D);
+    l.qbuf = d_align(l.part + size_t(kDCons) * 8 * D * sizeof(float));
+    l.sbuf = d_align(l.qbuf + size_t(kDUnits) * 8 * D * 2);
+    l.bins = d_align(l.sbuf + size_t(kDUnits) * l.pstride * sizeof(float));
+    l.ts = d_align(l.bins + size_t(Pmax) * sizeof(int16_t));
+    l.selv = d_align(l.ts + sizeof(BlockTopkShared<kDSelThreads>));
+    l.res = d_align(l.selv + size_t(Kmax) * sizeof(int32_t));
+    l.recv = d_align(l.res + size_t(kDUnits) * maxp * 2 * sizeof(int32_t));
+    l.total = d_align(l.recv + size_t(kDUnits) * l.recv_stride * sizeof(float));
+    return l;
+}
+
+// ---------------------------------------------------------------------------
+template <int D, int T, int MODE>
+__global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const DecodeParams p)
+{
+    constexpr int kSub = T / 16;                // 16-token sub-tiles of a page
+    constexpr int kRing = d_ring(T);            // slots per consumer warp
+    constexpr int kRowBytes = 4 * D;            // a page's [min | max] row
+    constexpr int kPageBytes = 2 * T * D;       // a page's K (or V) block
+    constexpr int kSlot = 2 * kPageBytes;       // one page of K and V, or the rows of T pages
+    constexpr int kPiece = kSlot / kRowBytes;   // pages per score item
+    constexpr int kMTiles = D / 16;
+    constexpr int kR = (2 * D / 8) / 4;         // 16-byte chunk groups of a [min | max] row
+    static_assert(kPiece == 16 * kSub, "a score item is kSub groups of 16 pages");
+    static_assert(kRing <= kDRingMax, "slot count");
+    extern __shared__ __align__(1024) uint8_t smem[];
+    __shared__ DecodeShared sh;
+
+    const int C = p.C;
+    const DLayout lay = d_layout(D, T, p.Pmax, p.Kmax, C, p.maxp);
+    uint8_t* rings = smem + lay.ring;
+    float* part = reinterpret_cast<float*>(smem + lay.part);
+    uint8_t* qbuf = smem + lay.qbuf;
+    float* sbuf = reinterpret_cast<float*>(smem + lay.sbuf);
+    int16_t* bins = reinterpret_cast<int16_t*>(smem + lay.bins);
+    auto& ts = *reinterpret_cast<BlockTopkShared<kDSelThreads>*>(smem + lay.ts);
+    int32_t* selv = reinterpret_cast<int32_t*>(smem + lay.selv);
+    int2* res = reinterpret_cast<int2*>(smem + lay.res);
+    float* recv = reinterpret_cast<float*>(smem + lay.recv);
+
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const uint32_t rank = cluster_ctarank();
+    const int cluster = blockIdx.x / C;
+    const int U = p.B * p.Hkv;
+    const int nunits = min(kDUnits, U - cluster * kDUnits);
+    const int G = p.G;
+    const int n_out = G * D;
+
+    if (tid == 0) {
+        for (int w = 0; w < kDCons; ++w)
+            for (int b2 = 0; b2 < kDRingMax; ++b2) mbar_init(&sh.full[w][b2], 1);
+        mbar_init(&sh.qbar, 1);
+        for (int j = 0; j < kDUnits; ++j) {
+            mbar_init(&sh.sbar[j], 1);
+            mbar_init(&sh.selr[j], 1);
+            mbar_init(&sh.rbar[j], 1);
+            sh.resn[j] = 0;
+        }
+        mbar_init(&sh.gbar, kDCons);
+        mbar_init(&sh.pbar, kDSelWarps);
+        sh.abort_flag = 0;
+        fence_barrier_init();
+    }
+    cluster_sync();  // every CTA's barriers exist before the first remote arrival
+    pdl_launch_dependents();
+    pdl_wait();  // every input may come from the preceding kernels
+
+    auto aborting = [&]() { return ld_volatile(&sh.abort_flag) != 0; };
+    auto set_abort = [&]() {
+        *reinterpret_cast<volatile int*>(&sh.abort_flag) = 1;
+        report(p.err, KVMM_ERR_TIMEOUT);
+    };
+    auto wait_bar_warp = [&](uint64_t* bar, uint32_t parity) {  // every lane of a warp, one outcome
+        const bool ok = __all_sync(kFullMask, mbar_wait_bounded(bar, parity, aborting() ? kDAbortNs : kDWaitNs));
+        if (!ok && lane == 0) set_abort();
+        return ok;
+    };
+
+    if (tid == 0) {  // the query groups of the cluster's units
+        const uint32_t qbytes = static_cast<uint32_t>(G) * D * 2;
+        mbar_arrive_expect_tx(&sh.qbar, qbytes * nunits);
+        for (int j = 0; j < nunits; ++j) {
+            const int wunit = cluster * kDUnits + j;
+            const int b = wunit / p.Hkv, h = wunit - (wunit / p.Hkv) * p.Hkv;
+            bulk_copy_g2s(qbuf + size_t(j) * 8 * D * 2,
+                          p.q + (static_cast<size_t>(b) * p.Hq + static_cast<size_t>(h) * G) * D, qbytes, &sh.qbar);
+        }
+    }
+    if (tid < nunits) {  // this CTA's view of unit tid
+        DUnit u;
+        const int wunit = cluster * kDUnits + tid;
+        u.b = wunit / p.Hkv;
+        u.h = wunit - u.b * p.Hkv;
+        u.ufull = (static_cast<size_t>(u.b) * p.L + p.layer) * p.Hkv + u.h;
+        const int cap = p.Pmax * T;
+        const bool first_of_batch = rank == 0 && u.h == 0;  // reports a batch's range errors once
+        int seq = p.seq_len[u.b];
+        if (seq < 0 || seq > cap) {
+            if (first_of_batch) report(p.err, KVMM_ERR_OUT_OF_RANGE);
+            seq = seq < 0 ? 0 : cap;
+        }
+        u.seq = seq;
+        u.P = (seq + T - 1) / T;
+        u.lo = static_cast<int>(static_cast<long long>(u.P) * rank / C);
+        u.hi = static_cast<int>(static_cast<long long>(u.P) * (rank + 1) / C);
+        u.rescored = p.rescore_mask == nullptr || p.rescore_mask[p.layer * p.Hkv + u.h] != 0;
+        u.tb = u.te = u.pb = u.pe = 0;
+        if (p.new_k != nullptr) {
+            const int tb = p.tok_begin[u.b], te = p.tok_end[u.b];
+            if (first_of_batch && (tb < 0 || te < tb || tb > cap || te > cap || te - tb > p.n_new))
+                report(p.err, KVMM_ERR_OUT_OF_RANGE);
+            if (tb >= 0 && te >= tb && tb <= cap) {
+                const int te2 = min(min(te, cap), tb + p.n_new);
+                if (te2 > tb) {
+                    u.tb = tb;
+                    u.te = te2;
+                    const int own_hi = rank == static_cast<uint32_t>(C - 1) ? p.Pmax : u.hi;
+                    u.pb = max(tb / T, u.lo);
+                    u.pe = max(u.pb, min((te2 - 1) / T + 1, own_hi));
+                }
+            }
+        }
+        sh.ud[tid] = u;
+    }
+    __syncthreads();
+
+    if (warp >= kDSel0) {
+        // ================= selectors =======================================
+        const int stid = tid - kDSel0 * 32;
+        const int swarp = stid >> 5;
+        constexpr int kLanesPerRow = D / 8;  // 16 bytes (8 channels) per lane
+        constexpr int kRowsPerPass = 32 / kLanesPerRow;
+        const int sub = lane % kLanesPerRow;
+        if (stid == 0) {
+            // the bytes this CTA receives: every score of a rescored unit (one float a page), and from
+            // each CTA its (m, l) of every head and its partial of this CTA's slice of the outputs.  A
+            // remote store that lands before its barrier is told to expect it leaves the transaction
+            // count negative; the pending arrival keeps the phase open until the count is set.
+            const int e0 = static_cast<int>(rank) * lay.slice;
+            const int own = max(0, min(n_out, e0 + lay.slice) - e0);
+            for (int j = 0; j < nunits; ++j) {
+                const DUnit& u = sh.ud[j];
+                mbar_arrive_expect_tx(&sh.sbar[j], u.rescored ? static_cast<uint32_t>(u.P) * 4u : 0u);
+                mbar_arrive_expect_tx(&sh.rbar[j], static_cast<uint32_t>(C * (2 * G + own)) * 4u);
+            }
+        }
+        // 0. a page the new tokens only partly fill gets its MinMax over all its rows below tok_end: the
+        //    bounds of the rows it already holds, for the consumer warp that scores and widens it
+        if (swarp < nunits) {
+            const DUnit& u = sh.ud[swarp];
+            const int pg = u.tb / T, r0 = u.tb - pg * T;
+            if (u.te > u.tb && u.rescored && r0 > 0 && u.pb <= pg && pg < min(u.pe, u.hi)) {
+                const int32_t phys = p.block_table[u.ufull * p.Pmax + pg];
+                if (phys >= 0 && phys < p.n_phys) {  // else the page is skipped, and reported below
+                    const kvmm_bf16* kpage = p.k_pool + static_cast<size_t>(phys) * T * D;
+                    uint32_t lo[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
+                    uint32_t hi[4] = {0u, 0u, 0u, 0u};
+#pragma unroll 4
+                    for (int r = lane / kLanesPerRow; r < r0; r += kRowsPerPass) {
+                        const uint4 v = reinterpret_cast<const uint4*>(kpage + static_cast<size_t>(r) * D)[sub];
+                        const uint32_t w4[4] = {to_key2(v.x), to_key2(v.y), to_key2(v.z), to_key2(v.w)};
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            lo[i] = __vminu2(lo[i], w4[i]);
+                            hi[i] = __vmaxu2(hi[i], w4[i]);
+                        }
+                    }
+#pragma unroll
+                    for (int off = kLanesPerRow; off < 32; off <<= 1) {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            lo[i] = __vminu2(lo[i], __shfl_xor_sync(kFullMask, lo[i], off));
+                            hi[i] = __vmaxu2(hi[i], __shfl_xor_sync(kFullMask, hi[i], off));
+                        }
+                    }
+                    if (lane < kLanesPerRow) {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            sh.prior[swarp][4 * sub + i] = lo[i];
+                            sh.prior[swarp][D / 2 + 4 * sub + i] = hi[i];
+                        }
+                    }
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh.pbar);  // release: the bounds above
+        // 1. the appended tokens of the pages this CTA owns: rows, then the pages' MinMax from all
+        //    their rows (a consumer scoring such a page widens its own copy of the bounds)
+        if (p.new_k != nullptr) {
+            for (int j = 0; j < nunits; ++j) {
+                const DUnit& u = sh.ud[j];
+                const int tb = u.tb, te = u.te;
+                for (int page = u.pb + swarp; page < u.pe; page += kDSelWarps) {
+                    const int32_t phys = p.block_table[u.ufull * p.Pmax + page];
+                    if (phys < 0 || phys >= p.n_phys) {
+                        if (lane == 0) report(p.err, phys < 0 ? KVMM_ERR_NULL_BLOCK : KVMM_ERR_OUT_OF_RANGE);
+                        continue;
+                    }
+                    kvmm_bf16* kpage = p.k_pool + static_cast<size_t>(phys) * T * D;
+                    kvmm_bf16* vpage = p.v_pool + static_cast<size_t>(phys) * T * D;
+                    const int first = page * T;
+                    const int r0 = max(tb - first, 0);
+                    const int r1 = min(te - first, T);
+                    const size_t src_base = (static_cast<size_t>(u.b) * p.Hkv + u.h) * p.n_new;
+                    for (int r = r0 + lane / kLanesPerRow; r < r1; r += kRowsPerPass) {
+                        const size_t jj = src_base + (first + r - tb);
+                        const uint4 kv = reinterpret_cast<const uint4*>(p.new_k + jj * D)[sub];
+                        const uint4 vv = reinterpret_cast<const uint4*>(p.new_v + jj * D)[sub];
+                        reinterpret_cast<uint4*>(kpage + static_cast<size_t>(r) * D)[sub] = kv;
+                        const uint32_t vw[4] = {vv.x, vv.y, vv.z, vv.w};
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)  // values are dimension-major: channel d of token r at [d*T + r]
+                            vpage[static_cast<size_t>(8 * sub + e) * T + r] =
+                                static_cast<kvmm_bf16>((e & 1) ? (vw[e >> 1] >> 16) : (vw[e >> 1] & 0xffffu));
+                    }
+                    __syncwarp();  // the rows just written are read back below by other lanes
+                    const int n_valid = min(T, te - first);
+                    uint32_t lo[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
+                    uint32_t hi[4] = {0u, 0u, 0u, 0u};
+                    for (int r = lane / kLanesPerRow; r < n_valid; r += kRowsPerPass) {
+                        const uint4 v = reinterpret_cast<const uint4*>(kpage + static_cast<size_t>(r) * D)[sub];
+                        const uint32_t w4[4] = {to_key2(v.x), to_key2(v.y), to_key2(v.z), to_key2(v.w)};
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            lo[i] = __vminu2(lo[i], w4[i]);
+                            hi[i] = __vmaxu2(hi[i], w4[i]);
+                        }
+                    }
+#pragma unroll
+                    for (int off = kLanesPerRow; off < 32; off <<= 1) {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            lo[i] = __vminu2(lo[i], __shfl_xor_sync(kFullMask, lo[i], off));
+                            hi[i] = __vmaxu2(hi[i], __shfl_xor_sync(kFullMask, hi[i], off));
+                        }
+                    }
+                    if (lane < kLanesPerRow) {
+                        kvmm_bf16* m = p.meta + (u.ufull * p.Pmax + page) * 2 * D;
+                        reinterpret_cast<uint4*>(m)[lane] = make_uint4(from_key2(lo[0]), from_key2(lo[1]),
+                                                                       from_key2(lo[2]), from_key2(lo[3]));
+                        reinterpret_cast<uint4*>(m + D)[lane] = make_uint4(from_key2(hi[0]), from_key2(hi[1]),
+                                                                           from_key2(hi[2]), from_key2(hi[3]));
+                    }
+                }
+            }
+            // later launches read these rows and bounds; this one never waits for them: the consumer
+            // that attends over such a page takes the new rows from new_k / new_v itself
+        }
+
+        // 2. each unit's selection, then this CTA's share of its pages through the block table
+        for (int j = 0; j < nunits; ++j) {
+            const DUnit u = sh.ud[j];
+            int cnt;
+            const int32_t* src;
+            if (u.rescored) {
+                // every score of the unit is here
+                if (!mbar_wait_bounded(&sh.sbar[j], 0, aborting() ? kDAbortNs : kDWaitNs)) set_abort();
+                cnt = block_topk<kDSelThreads, SelGroup>(nullptr, u.P, p.K, selv, sbuf + size_t(j) * lay.pstride,
+                                                         bins, ts);
+                if (rank == 0) {
+                    for (int i = stid; i < cnt; i += kDSelThreads) p.sel_idx[u.ufull * p.Kmax + i] = selv[i];
+                    if (stid == 0) p.sel_cnt[u.ufull] = cnt;
+                }
+                src = selv;
+            } else {
+                cnt = p.sel_cnt[u.ufull];
+                if (cnt < 0 || cnt > p.Kmax) {
+                    if (rank == 0 && stid == 0) report(p.err, KVMM_ERR_OUT_OF_RANGE);
+                    cnt = cnt < 0 ? 0 : p.Kmax;
+                }
+                src = p.sel_idx + u.ufull * p.Kmax;
+            }
+            const int beg = static_cast<int>(static_cast<long long>(cnt) * rank / C);
+            const int end = static_cast<int>(static_cast<long long>(cnt) * (rank + 1) / C);
+            int2* rl = res + size_t(j) * p.maxp;
+            int nres = 0;
+            for (int i0 = beg; i0 < end; i0 += kDSelThreads) {
+                const int i = i0 + stid;
+                int phys = -1;
+                int lp = 0;
+                if (i < end) {
+                    lp = src[i];
+                    if (lp < 0 || lp >= u.P) {
+                        report(p.err, KVMM_ERR_OUT_OF_RANGE);
+                    } else {
+                        const int32_t ph = p.block_table[u.ufull * p.Pmax + lp];
+                        if (ph < 0) {
+                            report(p.err, KVMM_ERR_NULL_BLOCK);
+                        } else if (ph >= p.n_phys) {
+                            report(p.err, KVMM_ERR_OUT_OF_RANGE);
+                        } else if (u.seq > lp * T) {
+                            phys = ph;
+                        }
+                    }
+                }
+                const bool ok = phys >= 0;
+                const unsigned bal = __ballot_sync(kFullMask, ok);
+                if (lane == 0) sh.wcount[swarp] = __popc(bal);
+                SelGroup::sync();
+                int pos = nres, tot = 0;
+#pragma unroll
+                for (int w = 0; w < kDSelWarps; ++w) {
+                    if (w < swarp) pos += sh.wcount[w];
+                    tot += sh.wcount[w];
+                }
+                if (ok) rl[pos + __popc(bal & ((1u << lane) - 1u))] = make_int2(phys, lp);
+                nres += tot;
+                SelGroup::sync();
+            }
+            if (stid == 0) {
+                sh.resn[j] = nres;
+                mbar_arrive(&sh.selr[j]);  // release: the list above, then the consumers
+            }
+        }
+
+        // 3. each unit's output slice: combine the partials of every CTA of the cluster
+        for (int j = 0; j < nunits; ++j) {
+            const DUnit& u = sh.ud[j];
+            if (!mbar_wait_bounded(&sh.rbar[j], 0, aborting() ? kDAbortNs : kDWaitNs)) set_abort();
+            const float* rj = recv + size_t(j) * lay.recv_stride;  // [C][16] (m, l), then [C][slice] outputs
+            if (stid < G) {
+                float M = -INFINITY;
+                for (int c = 0; c < C; ++c) M = fmaxf(M, rj[16 * c + stid]);
+                float L = 0.f;
+                for (int c = 0; c < C; ++c) {
+                    const float mc = rj[16 * c + stid];
+                    const float f = mc == -INFINITY ? 0.f : exp2f(mc - M);
+                    sh.fc[c][stid] = f;
+                    L = fmaf(rj[16 * c + 8 + stid], f, L);
+                }
+                sh.inv_l[stid] = L > 0.f ? 1.f / L : 0.f;
+                if (rank == 0 && p.lse) {
+                    const size_t oi = static_cast<size_t>(u.b) * p.Hq + static_cast<size_t>(u.h) * G + stid;
+                    p.lse[oi] = L > 0.f ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
+                }
+            }
+            SelGroup::sync();
+            const int e0 = static_cast<int>(rank) * lay.slice;
+            const int e1 = min(n_out, e0 + lay.slice);
+            const float* ro = rj + 16 * C;
+            float* ob = p.out + (static_cast<size_t>(u.b) * p.Hq + static_cast<size_t>(u.h) * G) * D;
+            for (int e = e0 + stid; e < e1; e += kDSelThreads) {
+                const int g = e / D;
+                float O = 0.f;
+                for (int c = 0; c < C; ++c) O = fmaf(sh.fc[c][g], ro[c * lay.slice + (e - e0)], O);
+                ob[e] = O * sh.inv_l[g];
+            }
+            SelGroup::sync();
+        }
+    } else {
+        // ================= consumers =======================================
+        const int w = warp;
+        const int gid = lane >> 2, tig = lane & 3;
+        const bool real_head = gid < G;
+        uint32_t wf[kR][4];      // score weights of head gid: [min(q,0) | max(q,0)] chunk 4r + tig
+        uint32_t qf[D / 32][4];  // attention Q^T B fragments of head gid
+        int frag = -1;           // which fragments are loaded: 2*unit + (0 score, 1 attention)
+        bool have_q = false;
+        uint32_t gsync_n = 0;
+        auto group_sync = [&]() {  // the consumer warps
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sh.gbar);
+            wait_bar_warp(&sh.gbar, gsync_n & 1);
+            ++gsync_n;
+        };
+        uint8_t* my_ring = rings + size_t(w) * kRing * kSlot;
+        // what each slot holds: held, unit, item; and the phase its mbarrier waits for
+        bool held[kRing];
+        int hj[kRing], hs[kRing];
+        uint32_t par[kRing];
+#pragma unroll
+        for (int b2 = 0; b2 < kRing; ++b2) {
+            held[b2] = false;
+            hj[b2] = hs[b2] = 0;
+            par[b2] = 0u;
+        }
+        auto land = [&](int b2) {  // b2 is a compile-time index wherever this is called
+            const bool ok = wait_bar_warp(&sh.full[w][b2], par[b2]);
+            par[b2] ^= 1u;
+            return ok;
+        };
+        auto load_frags = [&](int j, bool att) {
+            const int want = 2 * j + (att ? 1 : 0);
+            if (want == frag) return;
+            if (!have_q) {
+                wait_bar_warp(&sh.qbar, 0);
+                have_q = true;
+            }
+            const uint8_t* qe = qbuf + size_t(j) * 8 * D * 2 + gid * (2 * D);
+            if (!att) {
+#pragma unroll
+                for (int r = 0; r < kR; ++r) {
+                    const int c = 4 * r + tig;  // chunk of the [min | max] row
+                    const int qc = c % (D / 8);
+                    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                    if (real_head) v = ld_shared_v4(qe + 16 * qc);
+                    const bool is_max = c >= D / 8;
+                    wf[r][0] = is_max ? bf16x2_max0(v.x) : bf16x2_min0(v.x);
+                    wf[r][1] = is_max ? bf16x2_max0(v.y) : bf16x2_min0(v.y);
+                    wf[r][2] = is_max ? bf16x2_max0(v.z) : bf16x2_min0(v.z);
+                    wf[r][3] = is_max ? bf16x2_max0(v.w) : bf16x2_min0(v.w);
+                }
+            } else {
+#pragma unroll
+                for (int r = 0; r < D / 32; ++r) {
+                    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                    if (real_head) v = ld_shared_v4(qe + 16 * (4 * r + tig));
+                    qf[r][0] = v.x;
+                    qf[r][1] = v.y;
+                    qf[r][2] = v.z;
+                    qf[r][3] = v.w;
+                }
+            }
+            frag = want;
+        };
+
+        // ---- 1. scores: this warp's items (T pages each) s = w, w + 8, ... of each rescored unit ----
+        int nsl[kDUnits] = {0, 0};
+        for (int j = 0; j < nunits; ++j) {
+            const DUnit& u = sh.ud[j];
+            nsl[j] = u.rescored ? (u.hi - u.lo + kPiece - 1) / kPiece : 0;
+        }
+        // advance (j, sl) to this warp's next score item; false when there is none
+        auto next_score = [&](int& j, int& sl) {
+            sl += kDCons;
+            while (j < nunits && sl >= nsl[j]) {
+                ++j;
+                sl = w;
+            }
+            return j < nunits;
+        };
+        auto issue_score = [&](int b2, int j, int sl) {
+            const int lo = sh.ud[j].lo, hi = sh.ud[j].hi;
+            const size_t ufull = sh.ud[j].ufull;
+            const int page0 = lo + sl * kPiece;
+            const int npg = min(kPiece, hi - page0);
+            if (lane == 0) mbar_arrive_expect_tx(&sh.full[w][b2], static_cast<uint32_t>(npg) * kRowBytes);
+            __syncwarp();
+            if (8 * lane < npg) {  // lane i copies rows 8i .. 8i+7
+                const int rows = min(8, npg - 8 * lane);
+                bulk_copy_g2s(my_ring + size_t(b2) * kSlot + size_t(8 * lane) * kRowBytes,
+                              p.meta + (ufull * p.Pmax + page0 + 8 * lane) * 2 * D,
+                              static_cast<uint32_t>(rows) * kRowBytes, &sh.full[w][b2]);
+            }
+            held[b2] = true;
+            hj[b2] = j;
+            hs[b2] = sl;
+        };
+        // page `pg` of unit j receives tokens in this launch: its bounds in `staged` (the page's
+        // [min | max] row in shared memory) become those of all its rows below tok_end -- the rows it
+        // already holds (bounds from the selector warps) and the new ones.  The selector warps write
+        // the rows and the metadata; a page they skip (null or out-of-range table entry) keeps its
+        // bounds here too.
+        bool have_prior = false;
+        auto widen_page = [&](int j, int pg, uint8_t* staged) {
+            constexpr int kLanesPerRow = D / 8;  // 16 bytes (8 channels) per lane
+            const DUnit& u = sh.ud[j];
+            const int tb = u.tb, te = u.te;
+            const int first = pg * T;
+            const int r0 = max(tb - first, 0), r1 = min(te - first, T);
+            const int32_t phys = p.block_table[u.ufull * p.Pmax + pg];
+            if (phys < 0 || phys >= p.n_phys || r1 <= r0) return;
+            if (r0 > 0 && !have_prior) {  // the selector warps' bounds of rows [0, r0)
+                wait_bar_warp(&sh.pbar, 0);
+                have_prior = true;
+            }
+            const size_t src_base = (static_cast<size_t>(u.b) * p.Hkv + u.h) * p.n_new;
+            const int half = lane / kLanesPerRow;  // 0: min, 1: max
+            const int sub = lane % kLanesPerRow;
+            if (half < 2) {
+                uint32_t acc[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    acc[i] = r0 > 0 ? sh.prior[j][half * (D / 2) + 4 * sub + i] : (half == 0 ? 0xffffffffu : 0u);
+                for (int r = r0; r < r1; ++r) {
+                    const uint4 kv = reinterpret_cast<const uint4*>(p.new_k + (src_base + (first + r - tb)) * D)[sub];
+                    const uint32_t k4[4] = {to_key2(kv.x), to_key2(kv.y), to_key2(kv.z), to_key2(kv.w)};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        acc[i] = half == 0 ? __vminu2(acc[i], k4[i]) : __vmaxu2(acc[i], k4[i]);
+                }
+                *reinterpret_cast<uint4*>(staged + half * 2 * D + 16 * sub) =
+                    make_uint4(from_key2(acc[0]), from_key2(acc[1]), from_key2(acc[2]), from_key2(acc[3]));
+            }
+            __syncwarp();
+        };
+        auto score_slot = [&](const uint8_t* slot, int j, int page0, int npg) {
+            float* sb = sbuf + size_t(j) * lay.pstride + page0;
+            float* orow = p.scores_out ? p.scores_out + static_cast<size_t>(cluster * kDUnits + j) * p.Pmax + page0
+                                       : nullptr;
+#pragma unroll
+            for (int grp = 0; grp < kSub; ++grp) {
+                if (16 * grp < npg) {
+                    const uint8_t* ra = slot + static_cast<size_t>(16 * grp + gid) * kRowBytes;
+                    const uint8_t* rb = ra + 8 * kRowBytes;
+                    float c[4] = {0.f, 0.f, 0.f, 0.f}, c2[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int r = 0; r < kR; ++r) {
+                        const uint4 ka = ld_shared_v4(ra + 16 * (4 * r + tig));
+                        const uint4 kb = ld_shared_v4(rb + 16 * (4 * r + tig));
+                        mma_bf16_16816(c, ka.x, kb.x, ka.y, kb.y, wf[r][0], wf[r][1]);
+                        mma_bf16_16816(c2, ka.z, kb.z, ka.w, kb.w, wf[r][2], wf[r][3]);
+                    }
+                    float s_lo, s_hi;
+                    if (MODE == 0) {
+                        s_lo = (c[0] + c2[0]) + (c[1] + c2[1]);
+                        s_hi = (c[2] + c2[2]) + (c[3] + c2[3]);
+                        s_lo += __shfl_xor_sync(kFullMask, s_lo, 1);
+                        s_hi += __shfl_xor_sync(kFullMask, s_hi, 1);
+                        s_lo += __shfl_xor_sync(kFullMask, s_lo, 2);
+                        s_hi += __shfl_xor_sync(kFullMask, s_hi, 2);
+                    } else {
+                        const bool h0 = 2 * tig < G, h1 = 2 * tig + 1 < G;
+                        s_lo = fmaxf(h0 ? c[0] + c2[0] : -FLT_MAX, h1 ? c[1] + c2[1] : -FLT_MAX);
+                        s_hi = fmaxf(h0 ? c[2] + c2[2] : -FLT_MAX, h1 ? c[3] + c2[3] : -FLT_MAX);
+                        s_lo = fmaxf(s_lo, __shfl_xor_sync(kFullMask, s_lo, 1));
+                        s_hi = fmaxf(s_hi, __shfl_xor_sync(kFullMask, s_hi, 1));
+                        s_lo = fmaxf(s_lo, __shfl_xor_sync(kFullMask, s_lo, 2));
+                        s_hi = fmaxf(s_hi, __shfl_xor_sync(kFullMask, s_hi, 2));
+                    }
+                    // lanes tig = 0..3 of a row group send the two scores to CTAs tig, tig + 4, ...
+                    const int r0 = 16 * grp + gid;
+                    for (int r = tig; r < C; r += 4) {
+                        if (r0 < npg) st_async_f32(sb + r0, &sh.sbar[j], static_cast<uint32_t>(r), s_lo);
+                        if (r0 + 8 < npg) st_async_f32(sb + r0 + 8, &sh.sbar[j], static_cast<uint32_t>(r), s_hi);
+                    }
+                    if (orow && tig == 0) {
+                        if (r0 < npg) orow[r0] = s_lo;
+                        if (r0 + 8 < npg) orow[r0 + 8] = s_hi;
+                    }
+                }
+            }
+        };
+        {
+            int ij = 0, isl = w - kDCons;  // the last issued item
+            bool more = next_score(ij, isl);
+#pragma unroll
+            for (int b2 = 0; b2 < kRing; ++b2) {
+                if (more) {
+                    issue_score(b2, ij, isl);
+                    more = next_score(ij, isl);
+                }
+            }
+            // slots are used in turn, so they are consumed in the order they were filled
+            for (bool any = true; any;) {
+                any = false;
+#pragma unroll
+                for (int b2 = 0; b2 < kRing; ++b2) {
+                    if (!held[b2]) continue;
+                    any = true;
+                    const int j = hj[b2];
+                    const int page0 = sh.ud[j].lo + hs[b2] * kPiece;
+                    const int npg = min(kPiece, sh.ud[j].hi - page0);
+                    land(b2);
+                    load_frags(j, false);
+                    uint8_t* slot = my_ring + size_t(b2) * kSlot;
+                    const int pe = min(sh.ud[j].pe, page0 + npg);
+                    for (int pg = max(sh.ud[j].pb, page0); pg < pe; ++pg)  // pages receiving new tokens
+                        widen_page(j, pg, slot + size_t(pg - page0) * kRowBytes);
+                    score_slot(slot, j, page0, npg);
+                    __syncwarp();
+                    fence_proxy_async_shared();  // this slot's reads, then the next copy into it
+                    held[b2] = false;
+                    if (more) {
+                        issue_score(b2, ij, isl);
+                        more = next_score(ij, isl);
+                    }
+                }
+            }
+        }
+
+        // ---- 2. attention: this warp's steps (one page each) s = w, w + 8, ... of each unit, then the
+        //         unit's merge; once a unit's steps are all issued, the freed slots fetch the next unit's
+        float o[kMTiles][4];
+        float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+#pragma unroll
+        for (int i = 0; i < kMTiles; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+        // token of fragment row rho of sub-tile jj: 4*kSub*((rho&7)>>1) + 4*jj + 2*(rho>>3) + (rho&1), so
+        // that lane tig's k-slots of the P^T fragment are tokens 4*kSub*tig .. 4*kSub*tig + 4*kSub - 1
+        const int ua0 = 4 * kSub * (gid >> 1) + (gid & 1);
+        auto att_step = [&](const uint8_t* slot, int nv) {
+            const bool full = nv == T;
+            const uint8_t* ks = slot;
+            const uint8_t* vs = slot + kPageBytes;
+            float x[kSub][4];
+#pragma unroll
+            for (int jj = 0; jj < kSub; ++jj) {
+                const uint8_t* ra = ks + (ua0 + 4 * jj) * (2 * D);
+                const uint8_t* rb = ra + 2 * (2 * D);
+                float c[4] = {0.f, 0.f, 0.f, 0.f}, c2[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int r = 0; r < D / 32; ++r) {
+                    const uint4 ka = ld_shared_v4(ra + 16 * (4 * r + tig));
+                    const uint4 kb = ld_shared_v4(rb + 16 * (4 * r + tig));
+                    mma_bf16_16816(c, ka.x, kb.x, ka.y, kb.y, qf[r][0], qf[r][1]);
+                    mma_bf16_16816(c2, ka.z, kb.z, ka.w, kb.w, qf[r][2], qf[r][3]);
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i) x[jj][i] = (c[i] + c2[i]) * p.scale_log2;
+                if (!full) {
+                    if (ua0 + 4 * jj >= nv) x[jj][0] = x[jj][1] = -INFINITY;
+                    if (ua0 + 4 * jj + 2 >= nv) x[jj][2] = x[jj][3] = -INFINITY;
+                }
+            }
+            float mx0 = fmaxf(x[0][0], x[0][2]), mx1 = fmaxf(x[0][1], x[0][3]);
+#pragma unroll
+            for (int jj = 1; jj < kSub; ++jj) {
+                mx0 = fmaxf(mx0, fmaxf(x[jj][0], x[jj][2]));
+                mx1 = fmaxf(mx1, fmaxf(x[jj][1], x[jj][3]));
+            }
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(kFullMask, mx0, off));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(kFullMask, mx1, off));
+            }
+            const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+            const float ref0 = mn0 == -INFINITY ? 0.f : mn0;
+            const float ref1 = mn1 == -INFINITY ? 0.f : mn1;
+            const float a0 = fast_exp2(m0 - ref0), a1 = fast_exp2(m1 - ref1);
+            float pr[kSub][4];
+            float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+            for (int jj = 0; jj < kSub; ++jj) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) pr[jj][i] = fast_exp2(x[jj][i] - ((i & 1) ? ref1 : ref0));
+                ps0 += pr[jj][0] + pr[jj][2];
+                ps1 += pr[jj][1] + pr[jj][3];
+            }
+            l0 = fmaf(l0, a0, ps0);
+            l1 = fmaf(l1, a1, ps1);
+            m0 = mn0;
+            m1 = mn1;
+            if (__any_sync(kFullMask, (a0 != 1.f) || (a1 != 1.f))) {
+#pragma unroll
+                for (int i = 0; i < kMTiles; ++i) {
+                    o[i][0] *= a0;
+                    o[i][1] *= a1;
+                    o[i][2] *= a0;
+                    o[i][3] *= a1;
+                }
+            }
+            uint32_t bh[kSub][2], bl[kSub][2];
+#pragma unroll
+            for (int jj = 0; jj < kSub; ++jj) {
+                const uint32_t h01 = pack_bf16x2(pr[jj][0], pr[jj][1]), h23 = pack_bf16x2(pr[jj][2], pr[jj][3]);
+                const uint32_t r01 = pack_bf16x2(pr[jj][0] - bf16_lo(h01), pr[jj][1] - bf16_hi(h01));
+                const uint32_t r23 = pack_bf16x2(pr[jj][2] - bf16_lo(h23), pr[jj][3] - bf16_hi(h23));
+                bh[jj][0] = movmatrix_trans(h01);
+                bh[jj][1] = movmatrix_trans(h23);
+                bl[jj][0] = movmatrix_trans(r01);
+                bl[jj][1] = movmatrix_trans(r23);
+            }
+            // O^T += V^T P^T: lane reads tokens u0 .. u0 + 4*kSub - 1 of dims 16i+gid, 16i+gid+8
+            const int u0 = 4 * kSub * tig;
+            const uint8_t* vrow = vs + u0 * 2;
+            bool vk[4 * kSub];
+            if (!full) {
+#pragma unroll
+                for (int e = 0; e < 4 * kSub; ++e) vk[e] = u0 + e < nv;
+            }
+#pragma unroll
+            for (int i = 0; i < kMTiles; ++i) {
+                if constexpr (kSub == 2) {
+                    uint4 wa = ld_shared_v4(vrow + (16 * i + gid) * (T * 2));
+                    uint4 wb = ld_shared_v4(vrow + (16 * i + gid + 8) * (T * 2));
+                    if (!full) {
+                        wa = make_uint4(keep_halves(wa.x, vk[0], vk[1]), keep_halves(wa.y, vk[2], vk[3]),
+                                        keep_halves(wa.z, vk[4], vk[5]), keep_halves(wa.w, vk[6], vk[7]));
+                        wb = make_uint4(keep_halves(wb.x, vk[0], vk[1]), keep_halves(wb.y, vk[2], vk[3]),
+                                        keep_halves(wb.z, vk[4], vk[5]), keep_halves(wb.w, vk[6], vk[7]));
+                    }
+                    mma_bf16_16816(o[i], wa.x, wb.x, wa.y, wb.y, bh[0][0], bh[0][1]);
+                    mma_bf16_16816(o[i], wa.x, wb.x, wa.y, wb.y, bl[0][0], bl[0][1]);
+                    mma_bf16_16816(o[i], wa.z, wb.z, wa.w, wb.w, bh[1][0], bh[1][1]);
+                    mma_bf16_16816(o[i], wa.z, wb.z, wa.w, wb.w, bl[1][0], bl[1][1]);
+                } else {
+                    uint2 wa = ld_shared_v2(vrow + (16 * i + gid) * (T * 2));
+                    uint2 wb = ld_shared_v2(vrow + (16 * i + gid + 8) * (T * 2));
+                    if (!full) {
+                        wa = make_uint2(keep_halves(wa.x, vk[0], vk[1]), keep_halves(wa.y, vk[2], vk[3]));
+                        wb = make_uint2(keep_halves(wb.x, vk[0], vk[1]), keep_halves(wb.y, vk[2], vk[3]));
+                    }
+                    mma_bf16_16816(o[i], wa.x, wb.x, wa.y, wb.y, bh[0][0], bh[0][1]);
+                    mma_bf16_16816(o[i], wa.x, wb.x, wa.y, wb.y, bl[0][0], bl[0][1]);
+                }
+            }
+        };
+        // a page receiving tokens in this launch may have been copied before or after the selector
+        // warps wrote them to the pools: its slot takes those rows from new_k / new_v
+        auto patch_page = [&](int j, int lp, uint8_t* slot) {
+            constexpr int kDimsPerLane = D / 32;
+            const DUnit& u = sh.ud[j];
+            const int first = lp * T;
+            const int r0 = max(u.tb - first, 0), r1 = min(u.te - first, T);
+            const size_t src_base = (static_cast<size_t>(u.b) * p.Hkv + u.h) * p.n_new;
+            kvmm_bf16* vt = reinterpret_cast<kvmm_bf16*>(slot + kPageBytes);  // value d of token r at [d*T + r]
+            for (int r = r0; r < r1; ++r) {
+                const size_t jj = src_base + (first + r - u.tb);
+                if (lane < D / 8)
+                    *reinterpret_cast<uint4*>(slot + static_cast<size_t>(r) * 2 * D + 16 * lane) =
+                        reinterpret_cast<const uint4*>(p.new_k + jj * D)[lane];
+                const kvmm_bf16* vsrc = p.new_v + jj * D + kDimsPerLane * lane;
+#pragma unroll
+                for (int e = 0; e < kDimsPerLane; ++e) vt[static_cast<size_t>(kDimsPerLane * lane + e) * T + r] = vsrc[e];
+            }
+            __syncwarp();
+        };
+        auto issue_att = [&](int b2, int j, int s) {  // step s of unit j: page s of this CTA's share
+            if (lane == 0) mbar_arrive_expect_tx(&sh.full[w][b2], 2u * kPageBytes);
+            __syncwarp();
+            if (lane < 2) {  // lane 0 copies the page's keys, lane 1 its values
+                uint8_t* dst = my_ring + size_t(b2) * kSlot + lane * kPageBytes;
+                const size_t off = static_cast<size_t>(res[size_t(j) * p.maxp + s].x) * T * D;
+                bulk_copy_g2s(dst, (lane ? p.v_pool : p.k_pool) + off, kPageBytes, &sh.full[w][b2]);
+            }
+            held[b2] = true;
+            hj[b2] = j;
+            hs[b2] = s;
+        };
+        bool next_known = false;  // the next unit's pages are resolved and its steps may be fetched
+        int next_nx = w;          // the next unit's next step to fetch
+        for (int j = 0; j < nunits; ++j) {
+            if (!(j > 0 && next_known)) wait_bar_warp(&sh.selr[j], 0);
+            const int n = sh.resn[j];
+            int nx = j > 0 && next_known ? next_nx : w;
+            next_known = false;
+            next_nx = w;
+            load_frags(j, true);
+#pragma unroll
+            for (int b2 = 0; b2 < kRing; ++b2) {
+                if (!held[b2] && nx < n) {
+                    issue_att(b2, j, nx);
+                    nx += kDCons;
+                }
+            }
+            const int jn = j + 1;
+            for (bool any = true; any;) {
+                any = false;
+#pragma unroll
+                for (int b2 = 0; b2 < kRing; ++b2) {
+                    if (!held[b2] || hj[b2] != j) continue;
+                    any = true;
+                    const int lp = res[size_t(j) * p.maxp + hs[b2]].y;
+                    const int nv = min(T, sh.ud[j].seq - lp * T);
+                    uint8_t* slot = my_ring + size_t(b2) * kSlot;
+                    land(b2);
+                    if (sh.ud[j].te > lp * T && sh.ud[j].tb < (lp + 1) * T) patch_page(j, lp, slot);
+                    att_step(slot, nv);
+                    __syncwarp();
+                    fence_proxy_async_shared();  // this slot's reads, then the next copy into it
+                    held[b2] = false;
+                    if (nx < n) {
+                        issue_att(b2, j, nx);
+                        nx += kDCons;
+                    } else if (jn < nunits) {
+                        if (!next_known && __all_sync(kFullMask, mbar_try_wait(&sh.selr[jn], 0))) next_known = true;
+                        if (next_known && next_nx < sh.resn[jn]) {
+                            issue_att(b2, jn, next_nx);
+                            next_nx += kDCons;
+                        }
+                    }
+                }
+            }
+
+            // ---- end of the unit: the warps' partials -> this CTA's, sent to the cluster
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+                l0 += __shfl_xor_sync(kFullMask, l0, off);
+                l1 += __shfl_xor_sync(kFullMask, l1, off);
+            }
+            if (gid == 0) {
+                sh.mm[w][2 * tig] = m0;
+                sh.mm[w][2 * tig + 1] = m1;
+                sh.ml[w][2 * tig] = l0;
+                sh.ml[w][2 * tig + 1] = l1;
+            }
+            float* mw = part + size_t(w) * 8 * D;  // [8 heads][D]
+#pragma unroll
+            for (int i = 0; i < kMTiles; ++i) {
+                float* w0 = mw + (2 * tig) * D;
+                float* w1 = w0 + D;
+                w0[16 * i + gid] = o[i][0];
+                w1[16 * i + gid] = o[i][1];
+                w0[16 * i + gid + 8] = o[i][2];
+                w1[16 * i + gid + 8] = o[i][3];
+            }
+            group_sync();
+            const int gt = w * 32 + lane;  // 0 .. 255 over the consumer group
+            float* rj = recv + size_t(j) * lay.recv_stride;
+            if (gt < G) {
+                float M = -INFINITY;
+#pragma unroll
+                for (int ww = 0; ww < kDCons; ++ww) M = fmaxf(M, sh.mm[ww][gt]);
+                float L = 0.f;
+#pragma unroll
+                for (int ww = 0; ww < kDCons; ++ww) {
+                    const float mw2 = sh.mm[ww][gt];
+                    const float f = mw2 == -INFINITY ? 0.f : exp2f(mw2 - M);
+                    sh.fw[ww][gt] = f;
+                    L = fmaf(sh.ml[ww][gt], f, L);
+                }
+                for (int r = 0; r < C; ++r) {
+                    st_async_f32(rj + 16 * rank + gt, &sh.rbar[j], static_cast<uint32_t>(r), M);
+                    st_async_f32(rj + 16 * rank + 8 + gt, &sh.rbar[j], static_cast<uint32_t>(r), L);
+                }
+            }
+            group_sync();
+            for (int e = gt; e < n_out; e += kDCons * 32) {
+                const int g = e / D;
+                float O = 0.f;
+#pragma unroll
+                for (int ww = 0; ww < kDCons; ++ww) O = fmaf(sh.fw[ww][g], part[size_t(ww) * 8 * D + e], O);
+                const int r = e / lay.slice;
+                st_async_f32(rj + 16 * C + rank * lay.slice + (e - r * lay.slice), &sh.rbar[j], static_cast<uint32_t>(r),
+                             O);
+            }
+            group_sync();  // every warp's partial read before the next unit's merge writes its own
+#pragma unroll
+            for (int i = 0; i < kMTiles; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+            m0 = m1 = -INFINITY;
+            l0 = l1 = 0.f;
+        }
+        // only after a time-out can a slot still be in flight here: let it land before the CTA exits
+#pragma unroll
+        for (int b2 = 0; b2 < kRing; ++b2)
+            if (held[b2]) land(b2);
+    }
+    __syncthreads();
+    cluster_sync();  // no CTA leaves while another may still address its shared memory
+}
+
+template <int D, int T, int MODE>
+void (*decode_kernel())(DecodeParams)
+{
+    return decode_layer_kernel<D, T, MODE>;
+}
+
+void (*decode_kernel_for(int D, int T, int mode))(DecodeParams)
+{
+    if (D == 128) {
+        if (T == 16) return mode ? decode_kernel<128, 16, 1>() : decode_kernel<128, 16, 0>();
+        return mode ? decode_kernel<128, 32, 1>() : decode_kernel<128, 32, 0>();
+    }
+    if (T == 16) return mode ? decode_kernel<64, 16, 1>() : decode_kernel<64, 16, 0>();
+    return mode ? decode_kernel<64, 32, 1>() : decode_kernel<64, 32, 0>();
+}
+
+// opt-ins of one instantiation, once per device and size
+cudaError_t prepare_decode(void (*kernel)(DecodeParams), size_t smem)
+{
+    struct Prepared {
+        void (*kernel)(DecodeParams);
+        int dev;
+        size_t bytes;
+    };
+    static thread_local Prepared cache[8] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    for (auto& c : cache)
+        if (c.kernel == kernel && c.dev == dev && c.bytes >= smem) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+    for (auto& c : cache)
+        if (c.kernel == kernel || c.kernel == nullptr) {
+            c = {kernel, dev, smem};
+            break;
+        }
+    return cudaSuccess;
+}
+
+}  // namespace
+
+size_t decode_layer_smem(int D, int T, int Pmax, int Kmax, int C)
+{
+    const int maxp = (Kmax + C - 1) / C;
+    return d_layout(D, T, Pmax, Kmax, C, maxp).total;
+}
+
+int decode_layer_cluster(const kvmm_shape& s)
+{
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int clusters = (s.B * s.Hkv + kDUnits - 1) / kDUnits;
+    int c = sms / clusters;
+    if (c > kDMaxCluster) c = kDMaxCluster;
+    if (c < 1) c = 1;
+    return c;
+}
+
+cudaError_t launch_decode_layer(DecodeParams p, int group_reduce, cudaStream_t stream)
+{
+    void (*kernel)(DecodeParams) = decode_kernel_for(p.D, p.T, group_reduce);
+    p.maxp = (p.Kmax + p.C - 1) / p.C;
+    const size_t smem = decode_layer_smem(p.D, p.T, p.Pmax, p.Kmax, p.C);
+    cudaError_t e = prepare_decode(kernel, smem);
+    if (e != cudaSuccess) return e;
+    const int clusters = (p.B * p.Hkv + kDUnits - 1) / kDUnits;
+    return launch_pdl_cluster(kernel, dim3(static_cast<unsigned>(clusters * p.C)), dim3(kDThreads), smem, stream,
+                              static_cast<unsigned>(p.C), p);
+}
+
+}  // namespace kvmm

@@ -82,6 +82,34 @@ struct AttnParams {
     int32_t* err;
 };
 
+// one-launch decode layer (decode_layer.cu): a cluster of C CTAs per two units
+constexpr int kDMaxCluster = 8;
+struct DecodeParams {
+    int32_t B, L, Hq, Hkv, G, D, T, Pmax, Kmax, layer, K;
+    int32_t C;      // CTAs per cluster
+    int32_t maxp;   // selected pages one CTA attends over at most: ceil(Kmax / C)
+    int32_t n_new;  // appended tokens per batch entry (rows of new_k / new_v)
+    int64_t n_phys;
+    float scale_log2;  // sm_scale * log2(e)
+    const kvmm_bf16* q;
+    const kvmm_bf16* new_k;  // null: nothing appended
+    const kvmm_bf16* new_v;
+    const int32_t* tok_begin;
+    const int32_t* tok_end;
+    kvmm_bf16* k_pool;
+    kvmm_bf16* v_pool;
+    const int32_t* block_table;
+    kvmm_bf16* meta;
+    const int32_t* seq_len;
+    const uint8_t* rescore_mask;
+    int32_t* sel_idx;
+    int32_t* sel_cnt;
+    float* scores_out;
+    float* out;
+    float* lse;
+    int32_t* err;
+};
+
 struct DiffParams {
     int32_t B, L, Hkv, Kmax, layer, commit;
     const uint8_t* rescore_mask;
@@ -161,6 +189,9 @@ cudaError_t launch_minmax_update(const UpdateParams& p, cudaStream_t stream);
 cudaError_t launch_score_topk(const ScoreParams& p, int group_reduce, cudaStream_t stream);
 cudaError_t launch_sparse_attention(const AttnParams& p, cudaStream_t stream);
 cudaError_t launch_promotion_diff(const DiffParams& p, cudaStream_t stream);
+cudaError_t launch_decode_layer(DecodeParams p, int group_reduce, cudaStream_t stream);
+size_t decode_layer_smem(int D, int T, int Pmax, int Kmax, int C);  // dynamic shared memory of one CTA
+int decode_layer_cluster(const kvmm_shape& s);                 // CTAs per cluster for a shape
 // the scoring kernel alone (page_score_topk without its selection kernel)
 cudaError_t launch_score_only(const ScoreParams& p, int group_reduce, cudaStream_t stream);
 

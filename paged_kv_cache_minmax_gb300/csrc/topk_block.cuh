@@ -43,6 +43,19 @@ struct BlockTopkShared {
     int remaining;
 };
 
+// The threads that run one selection: the whole CTA, or a group of N threads
+// (whole warps) starting at thread FIRST that synchronises on named barrier BAR.
+struct CtaGroup {
+    static constexpr int kFirst = 0;
+    __device__ static void sync() { __syncthreads(); }
+};
+template <int BAR, int FIRST, int N>
+struct WarpGroup {
+    static_assert(FIRST % 32 == 0 && N % 32 == 0, "whole warps");
+    static constexpr int kFirst = FIRST;
+    __device__ static void sync() { asm volatile("bar.sync %0, %1;" ::"r"(BAR), "r"(N) : "memory"); }
+};
+
 // float -> unsigned key with the same order
 __device__ __forceinline__ uint32_t topk_order_key(float f)
 {
@@ -51,17 +64,17 @@ __device__ __forceinline__ uint32_t topk_order_key(float f)
 }
 
 // Exact top-K over the P scores in sc[] by 4 radix passes; writes sel[0..K) ascending.
-template <int THREADS>
+template <int THREADS, class Group = CtaGroup>
 __device__ void block_radix_topk(const float* sc, int P, int K, int32_t* sel, BlockTopkShared<THREADS>& ts)
 {
     constexpr int kWarps = THREADS / 32;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int tid = static_cast<int>(threadIdx.x) - Group::kFirst, lane = tid & 31, warp = tid >> 5;
     uint32_t prefix = 0, pmask = 0;
     int remaining = K;
     const int P_round = (P + THREADS - 1) / THREADS * THREADS;
     for (int shift = 24; shift >= 0; shift -= 8) {
         for (int i = tid; i < 256; i += THREADS) ts.rhist[i] = 0;
-        __syncthreads();
+        Group::sync();
         for (int i = tid; i < P_round; i += THREADS) {
             const uint32_t key = i < P ? topk_order_key(sc[i]) : 0u;
             const bool cand = i < P && (key & pmask) == prefix;
@@ -72,7 +85,7 @@ __device__ void block_radix_topk(const float* sc, int P, int K, int32_t* sel, Bl
                 if (lane == __ffs(peers) - 1) atomicAdd(&ts.rhist[digit], __popc(peers));
             }
         }
-        __syncthreads();
+        Group::sync();
         if (warp == 0) {
             int c[8];
             int tot = 0;
@@ -101,11 +114,11 @@ __device__ void block_radix_topk(const float* sc, int P, int K, int32_t* sel, Bl
                 }
             }
         }
-        __syncthreads();
+        Group::sync();
         prefix |= static_cast<uint32_t>(ts.digit) << shift;
         pmask |= 255u << shift;
         remaining = ts.remaining;
-        __syncthreads();
+        Group::sync();
     }
     const uint32_t thr = prefix;
     int out_base = 0, eq_base = 0;
@@ -117,18 +130,18 @@ __device__ void block_radix_topk(const float* sc, int P, int K, int32_t* sel, Bl
         const bool eq = i < P && key == thr;
         const unsigned eqb = __ballot_sync(kFullMask, eq);
         if (lane == 0) ts.wsum[warp] = __popc(eqb);
-        __syncthreads();
+        Group::sync();
         int eq_off = eq_base, eq_all = 0;
         for (int w2 = 0; w2 < kWarps; ++w2) {
             const int t = ts.wsum[w2];
             if (w2 < warp) eq_off += t;
             eq_all += t;
         }
-        __syncthreads();
+        Group::sync();
         const bool take = gt || (eq && eq_off + __popc(eqb & lt_mask) < remaining);
         const unsigned tb = __ballot_sync(kFullMask, take);
         if (lane == 0) ts.wsum[warp] = __popc(tb);
-        __syncthreads();
+        Group::sync();
         int out_off = out_base, out_all = 0;
         for (int w2 = 0; w2 < kWarps; ++w2) {
             const int t = ts.wsum[w2];
@@ -138,32 +151,39 @@ __device__ void block_radix_topk(const float* sc, int P, int K, int32_t* sel, Bl
         if (take) sel[out_off + __popc(tb & lt_mask)] = i;
         out_base += out_all;
         eq_base += eq_all;
-        __syncthreads();
+        Group::sync();
     }
 }
 
 // Selects the top K of the P scores at `scores` (global memory, read through
-// L2) into sel[] (shared or global memory) and returns the count, min(K, P).
-// sc (P floats) and bin (P int16) are shared-memory scratch.  Every thread of
-// the block must call it; sel[] is complete for every thread on return.
-template <int THREADS>
+// L2; or null when sc[] already holds them) into sel[] (shared or global
+// memory) and returns the count, min(K, P).  sc (P floats) and bin (P int16)
+// are shared-memory scratch.  Every thread of the group must call it; sel[]
+// is complete for every thread of the group on return.
+template <int THREADS, class Group = CtaGroup>
 __device__ int block_topk(const float* scores, int P, int K, int32_t* sel, float* sc, int16_t* bin,
                           BlockTopkShared<THREADS>& ts)
 {
     constexpr int kWarps = THREADS / 32;
-    const int tid = threadIdx.x;
+    const int tid = static_cast<int>(threadIdx.x) - Group::kFirst;
     const int lane = tid & 31;
     const int warp = tid >> 5;
     if (K >= P) {
         for (int i = tid; i < P; i += THREADS) sel[i] = i;
-        __syncthreads();
+        Group::sync();
         return P;
     }
 
     // 1. scores to shared memory (16 loads in flight per thread), their range, an empty histogram
     constexpr int kBatch = 16;
     float lo = FLT_MAX, hi = -FLT_MAX;
-    for (int c0 = 0; c0 < P; c0 += THREADS * kBatch) {
+    if (scores == nullptr) {
+        for (int i = tid; i < P; i += THREADS) {
+            lo = fminf(lo, sc[i]);
+            hi = fmaxf(hi, sc[i]);
+        }
+    }
+    for (int c0 = 0; scores != nullptr && c0 < P; c0 += THREADS * kBatch) {
         float v[kBatch];
 #pragma unroll
         for (int j = 0; j < kBatch; ++j) {
@@ -191,7 +211,7 @@ __device__ int block_topk(const float* scores, int P, int K, int32_t* sel, float
         ts.wmin[warp] = lo;
         ts.wmax[warp] = hi;
     }
-    __syncthreads();
+    Group::sync();
     float mn = ts.wmin[0], mx = ts.wmax[0];
     for (int w = 1; w < kWarps; ++w) {
         mn = fminf(mn, ts.wmin[w]);
@@ -199,12 +219,12 @@ __device__ int block_topk(const float* scores, int P, int K, int32_t* sel, float
     }
     if (!(mx > mn)) {  // every score equal: the K lowest pages win the ties
         for (int i = tid; i < K; i += THREADS) sel[i] = i;
-        __syncthreads();
+        Group::sync();
         return K;
     }
     const float scale = static_cast<float>(kTopkBins) / (mx - mn);
     if (!(scale < FLT_MAX)) {
-        block_radix_topk<THREADS>(sc, P, K, sel, ts);
+        block_radix_topk<THREADS, Group>(sc, P, K, sel, ts);
         return K;
     }
 
@@ -214,7 +234,7 @@ __device__ int block_topk(const float* scores, int P, int K, int32_t* sel, float
         bin[i] = static_cast<int16_t>(bi);
         atomicAdd(&ts.hist[bi], 1);
     }
-    __syncthreads();
+    Group::sync();
 
     // 3. the bin holding the K-th largest score: suffix sums over bins
     constexpr int kBinsPerThread = kTopkBins / THREADS;
@@ -228,7 +248,7 @@ __device__ int block_topk(const float* scores, int P, int K, int32_t* sel, float
         if (lane + off < 32) incl += v;
     }
     if (lane == 0) ts.wsum[warp] = incl;
-    __syncthreads();
+    Group::sync();
     int above = incl - local;
     for (int w = warp + 1; w < kWarps; ++w) above += ts.wsum[w];
     if (above < K && K <= above + local) {
@@ -244,17 +264,17 @@ __device__ int block_topk(const float* scores, int P, int K, int32_t* sel, float
             acc += ts.hist[bj];
         }
     }
-    __syncthreads();
+    Group::sync();
     const int tb = ts.tb, need = ts.need, cbin = ts.cbin;
     if (cbin > kTopkCandMax) {  // crowded threshold bin: exact radix path
-        block_radix_topk<THREADS>(sc, P, K, sel, ts);
+        block_radix_topk<THREADS, Group>(sc, P, K, sel, ts);
         return K;
     }
 
     // 4. rank the threshold bin's scores exactly; mark the winners above every bin
     for (int i = tid; i < P; i += THREADS)
         if (bin[i] == tb) ts.cand[atomicAdd(&ts.ncand, 1)] = i;
-    __syncthreads();
+    Group::sync();
     for (int t = tid; t < cbin; t += THREADS) {
         const int i = ts.cand[t];
         const float s = sc[i];
@@ -266,7 +286,7 @@ __device__ int block_topk(const float* scores, int P, int K, int32_t* sel, float
         }
         if (rank < need) bin[i] = static_cast<int16_t>(kTopkBins);
     }
-    __syncthreads();
+    Group::sync();
 
     // 5. ordered compaction: thread t emits the winners among pages [t*m, t*m + m)
     const int m = (P + THREADS - 1) / THREADS;
@@ -280,12 +300,12 @@ __device__ int block_topk(const float* scores, int P, int K, int32_t* sel, float
         if (lane >= off) pre += v;
     }
     if (lane == 31) ts.wsum[warp] = pre;
-    __syncthreads();
+    Group::sync();
     int pos = pre - mine;
     for (int w = 0; w < warp; ++w) pos += ts.wsum[w];
     for (int i = i0; i < i1; ++i)
         if (bin[i] > tb) sel[pos++] = i;
-    __syncthreads();
+    Group::sync();
     return K;
 }
 

@@ -21,7 +21,7 @@ NULL_BLOCK = -1
 
 EXPORTS = ("kv_minmax_update", "page_score_topk", "sparse_paged_decode_attn", "topk_promotion_diff",
            "kvmm_workspace_size", "kvmm_auto_splits", "kvmm_status_string", "kvmm_last_cuda_error",
-           "page_score_topk_static_scratch", "page_score_topk_attn")
+           "page_score_topk_static_scratch", "page_score_topk_attn", "decode_layer")
 
 
 class KvmmError(RuntimeError):
@@ -75,8 +75,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.topk_promotion_diff.argtypes = [SP, I32, P, P, P, P, P, I32, P, P, P, P, P, P, P]
     lib.page_score_topk_static_scratch.argtypes = [SP, I32, P, P, P, P, I32, I32, P, P, P, P, P]
     lib.page_score_topk_attn.argtypes = [SP, I32, P, P, P, P, P, P, P, I32, I32, F32, P, P, P, P, P, P, SZ, P, P]
+    lib.decode_layer.argtypes = [SP, I32, P, P, P, I32, P, P, P, P, P, P, P, P, I32, I32, F32, P, P, P, P, P, P, SZ,
+                                 P, P]
     for f in ("kv_minmax_update", "page_score_topk", "sparse_paged_decode_attn", "topk_promotion_diff",
-              "page_score_topk_static_scratch", "page_score_topk_attn"):
+              "page_score_topk_static_scratch", "page_score_topk_attn", "decode_layer"):
         getattr(lib, f).restype = ctypes.c_int
     lib.kvmm_workspace_size.argtypes = [SP, I32]
     lib.kvmm_workspace_size.restype = SZ
@@ -230,6 +232,38 @@ def page_score_topk_attn(shape: Shape, layer: int, q, meta, k_pool, v_pool, bloc
             _dev(workspace, "workspace", torch.uint8), workspace.numel(),
             _dev(err, "err", torch.int32, 1, optional=True), _stream(stream))
     _check("page_score_topk_attn", load().page_score_topk_attn(*args))
+
+
+def decode_layer(shape: Shape, layer: int, q, new_k, new_v, n_new: int, tok_begin, tok_end, k_pool, v_pool,
+                 block_table, meta, seq_len, rescore_mask, K: int, sel_idx, sel_cnt, out, lse=None, err=None,
+                 scores_out=None, group_reduce: int = 0, sm_scale: float = 0.0, workspace=None,
+                 stream=None) -> None:
+    """Append (optional), score, select and attend for one layer in one launch."""
+    s = shape
+    units = s.B * s.L * s.Hkv
+    if (new_k is None) != (new_v is None):
+        raise ValueError("new_k and new_v are given together or not at all")
+    app = new_k is not None
+    args = (ctypes.byref(s), layer, _dev(q, "q", torch.bfloat16, s.B * s.Hq * s.D),
+            _dev(new_k, "new_k", torch.bfloat16, s.B * s.Hkv * max(n_new, 1) * s.D, optional=True),
+            _dev(new_v, "new_v", torch.bfloat16, s.B * s.Hkv * max(n_new, 1) * s.D, optional=True),
+            int(n_new) if app else 0,
+            _dev(tok_begin, "tok_begin", torch.int32, s.B, optional=not app),
+            _dev(tok_end, "tok_end", torch.int32, s.B, optional=not app),
+            _dev(k_pool, "k_pool", torch.bfloat16, s.n_phys * s.T * s.D),
+            _dev(v_pool, "v_pool", torch.bfloat16, s.n_phys * s.T * s.D),
+            _dev(block_table, "block_table", torch.int32, units * s.Pmax),
+            _dev(meta, "meta", torch.bfloat16, units * s.Pmax * 2 * s.D),
+            _dev(seq_len, "seq_len", torch.int32, s.B),
+            _dev(rescore_mask, "rescore_mask", torch.uint8, s.L * s.Hkv, optional=True), K, group_reduce,
+            float(sm_scale),
+            _dev(sel_idx, "sel_idx", torch.int32, units * s.Kmax), _dev(sel_cnt, "sel_cnt", torch.int32, units),
+            _dev(scores_out, "scores_out", torch.float32, s.B * s.Hkv * s.Pmax, optional=True),
+            _dev(out, "out", torch.float32, s.B * s.Hq * s.D),
+            _dev(lse, "lse", torch.float32, s.B * s.Hq, optional=True),
+            _dev(workspace, "workspace", torch.uint8, optional=True), 0 if workspace is None else workspace.numel(),
+            _dev(err, "err", torch.int32, 1, optional=True), _stream(stream))
+    _check("decode_layer", load().decode_layer(*args))
 
 
 def topk_promotion_diff(shape: Shape, layer: int, rescore_mask, prev_idx, prev_cnt, cur_idx, cur_cnt, promoted,

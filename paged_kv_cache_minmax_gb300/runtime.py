@@ -95,6 +95,15 @@ class DecodeState:
                                   self.workspace, lse=self.lse[layer], err=self.err, scores_out=scores_out,
                                   group_reduce=self.group_reduce, sm_scale=sm_scale)
 
+    def decode(self, layer, q, new_k=None, new_v=None, rescore_mask=None, scores_out=None, sm_scale=0.0) -> None:
+        """decode_layer: append (new_k/new_v [B, Hkv, 1, D] at seq_len - 1), score, select, attend."""
+        if new_k is not None:
+            torch.sub(self.seq_len, 1, out=self.tok_begin)
+        kvmm.decode_layer(self.shape, layer, q, new_k, new_v, 1, self.tok_begin, self.seq_len, self.k_pool,
+                          self.v_pool, self.block_table, self.meta, self.seq_len, rescore_mask, self.K, self.sel_idx,
+                          self.sel_cnt, self.out[layer], lse=self.lse[layer], err=self.err, scores_out=scores_out,
+                          group_reduce=self.group_reduce, sm_scale=sm_scale, workspace=self.workspace)
+
     def layer_step(self, layer, q, new_k=None, new_v=None, rescore_mask=None, fused=True) -> None:
         """One layer of one decode step: append, select + attend, diff."""
         if new_k is not None:

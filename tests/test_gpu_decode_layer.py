@@ -1,0 +1,187 @@
+"""GPU parity of decode_layer (append, score, select and attend in one launch).
+
+It must leave exactly what kv_minmax_update followed by page_score_topk_attn
+leaves: the appended rows in the pools and their pages' MinMax bit-exact, the
+scores, selections and counts bit-exact, and the attention within the
+attention tolerance of the oracle (and within 2e-5 of the separate calls).
+Cases cover both group reductions, every (D, T), an odd number of units (a
+cluster with one unit), short and empty sequences, partial rescore masks,
+null blocks and no append at all.
+"""
+import pytest
+import torch
+
+from paged_kv_cache_minmax_gb300 import kvmm, workloads
+from paged_kv_cache_minmax_gb300.runtime import DecodeState
+from paged_kv_cache_minmax_gb300.workloads import CONFIGS, scaled
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    assert torch.cuda.is_available(), "GPU tests need CUDA"
+    from paged_kv_cache_minmax_gb300 import build
+
+    build.build_library()
+    kvmm.load()
+    yield
+    torch.cuda.empty_cache()
+
+
+CASES = {
+    "tiny": CONFIGS[1],
+    "llama-ragged": scaled(CONFIGS[2], B=2, L=2, S=4096, K=32, n_planted=16, ragged=True),
+    "odd-units": workloads.Config("odd", B=3, L=1, Hq=12, Hkv=3, D=128, T=16, S=2000, K=20, ragged=True, seed=81),
+    "permuted": scaled(CONFIGS[3], B=2, L=1, S=8192 + 5, K=64, n_planted=32),
+    "gqa5-t32": scaled(CONFIGS[5], B=2, L=2, S=4096 - 7, K=16, n_planted=8, ragged=True, layers_alloc=None),
+    "d64-g8": workloads.Config("d64-g8", B=2, L=1, Hq=16, Hkv=2, D=64, T=16, S=1500, K=12, key_dist="chanscale",
+                               n_planted=6, ragged=True, permuted_pool=True, seed=77),
+    "d64-t32": workloads.Config("d64-t32", B=3, L=1, Hq=8, Hkv=2, D=64, T=32, S=3000, K=40, ragged=True, seed=79),
+    "g1-d128-t32": workloads.Config("g1-d128", B=1, L=1, Hq=4, Hkv=4, D=128, T=32, S=777, K=5, seed=78),
+    "big-k": scaled(CONFIGS[2], B=1, L=1, S=32768, K=1000, n_planted=64),
+}
+
+
+def twin_states(cfg, group_reduce=0):
+    """Two identical workloads and states: one for decode_layer, one for the separate calls."""
+    out = []
+    for _ in range(2):
+        wl = workloads.generate(cfg, device="cuda")
+        st = DecodeState.for_workload(wl, group_reduce=group_reduce)
+        st.build_metadata()
+        out.append((wl, st))
+    torch.cuda.synchronize()
+    return out
+
+
+def run_both(a, b, layer, q, nk=None, nv=None, mask=None):
+    (wa, sa), (wb, sb) = a, b
+    cfg = wa.cfg
+    sca = torch.full((cfg.B, cfg.Hkv, cfg.Pmax), float("nan"), device="cuda")
+    scb = torch.full((cfg.B, cfg.Hkv, cfg.Pmax), float("nan"), device="cuda")
+    sa.decode(layer, q, nk, nv, rescore_mask=mask, scores_out=sca)
+    if nk is not None:
+        sb.append(layer, nk, nv)
+    sb.select(layer, q, rescore_mask=mask, scores_out=scb)
+    sb.attend(layer, q)
+    torch.cuda.synchronize()
+    return sca, scb
+
+
+def assert_same(a, b, sca, scb, layer):
+    (wa, sa), (wb, sb) = a, b
+    assert torch.equal(wa.k_pool, wb.k_pool), "appended key rows differ"
+    assert torch.equal(wa.v_pool, wb.v_pool), "appended value rows differ"
+    assert torch.equal(sa.meta, sb.meta), "MinMax metadata differs"
+    assert torch.equal(sa.sel_cnt, sb.sel_cnt)
+    for idx in torch.nonzero(torch.ones_like(sa.sel_cnt)).tolist():
+        n = int(sa.sel_cnt[tuple(idx)])
+        assert torch.equal(sa.sel_idx[tuple(idx)][:n], sb.sel_idx[tuple(idx)][:n]), idx
+    assert torch.equal(torch.nan_to_num(sca, nan=7.0), torch.nan_to_num(scb, nan=7.0)), "scores differ"
+    d = (sa.out[layer] - sb.out[layer]).abs().max().item()
+    assert d <= 2e-5, f"attention differs by {d}"
+    fa, fb = torch.isfinite(sa.lse[layer]), torch.isfinite(sb.lse[layer])
+    assert torch.equal(fa, fb)
+    assert (sa.lse[layer][fa] - sb.lse[layer][fb]).abs().max().item() <= 2e-5 if fa.any() else True
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_decode_layer_matches_separate_calls_and_oracle(name):
+    cfg = CASES[name]
+    a, b = twin_states(cfg)
+    wl, st = a
+    nk, nv = workloads.step_tokens(wl, 0)
+    stats = parity.Stats()
+    for l in range(cfg.L_alloc):
+        sca, scb = run_both(a, b, l, wl.q[l], nk[l], nv[l])
+        assert st.read_err() == 0 and b[1].read_err() == 0
+        assert_same(a, b, sca, scb, l)
+        for bb in range(cfg.B):
+            for h in range(cfg.Hkv):
+                parity.check_unit(wl, st, l, bb, h, wl.q[l], sca, stats)
+    stats.check()
+    print(name, "units", stats.units, "ties", stats.ties, "max-abs", stats.max_abs)
+
+
+def test_without_append_equals_page_score_topk_attn():
+    cfg = CASES["llama-ragged"]
+    a, b = twin_states(cfg)
+    for l in range(cfg.L):
+        sca, scb = run_both(a, b, l, a[0].q[l])
+        assert a[1].read_err() == 0
+        assert_same(a, b, sca, scb, l)
+
+
+def test_group_max_mode():
+    cfg = CASES["gqa5-t32"]
+    a, b = twin_states(cfg, group_reduce=1)
+    nk, nv = workloads.step_tokens(a[0], 1)
+    for l in range(cfg.L_alloc):
+        sca, scb = run_both(a, b, l, a[0].q[l], nk[l], nv[l])
+        assert a[1].read_err() == 0
+        assert_same(a, b, sca, scb, l)
+
+
+def test_repeated_steps_and_partial_rescore_mask():
+    cfg = CASES["llama-ragged"]
+    a, b = twin_states(cfg)
+    qs = workloads.drift_queries(a[0], 4)
+    for step in range(4):
+        mask = None
+        if step % 2 == 1:
+            mask = torch.zeros(cfg.L_alloc, cfg.Hkv, dtype=torch.uint8, device="cuda")
+            mask[:, 1::3] = 1
+        nk, nv = workloads.step_tokens(a[0], step)
+        for l in range(cfg.L):
+            sca, scb = run_both(a, b, l, qs[step][l], nk[l], nv[l], mask=mask)
+            assert a[1].read_err() == 0
+            assert_same(a, b, sca, scb, l)
+
+
+def test_short_and_empty_units():
+    cfg = workloads.Config("short", B=3, L=1, Hq=8, Hkv=2, D=128, T=16, S=40, K=8, seed=5)
+    a, b = twin_states(cfg)
+    for wl, st in (a, b):
+        wl.seq_len.copy_(torch.tensor([40, 1, 0], dtype=torch.int32))
+        st.build_metadata()
+    nk, nv = workloads.step_tokens(a[0], 0)
+    # no append for the empty sequence: decode without new tokens
+    sca, scb = run_both(a, b, 0, a[0].q[0])
+    assert a[1].read_err() == 0
+    assert_same(a, b, sca, scb, 0)
+    assert a[1].sel_cnt[:, 0].tolist() == [[3, 3], [1, 1], [0, 0]]
+    assert torch.all(a[1].out[0, 2] == 0)
+    assert torch.all(torch.isneginf(a[1].lse[0, 2]))
+
+
+def test_null_blocks_outside_the_selection_are_never_read():
+    cfg = CASES["llama-ragged"]
+    a, b = twin_states(cfg)
+    wl, st = a
+    for l in range(cfg.L):
+        st.decode(l, wl.q[l])
+    torch.cuda.synchronize()
+    ref = st.out.clone()
+    sel_mask = torch.zeros(cfg.B, cfg.L, cfg.Hkv, cfg.Pmax, dtype=torch.bool, device="cuda")
+    for bb in range(cfg.B):
+        for l in range(cfg.L):
+            for h in range(cfg.Hkv):
+                n = int(st.sel_cnt[bb, l, h])
+                sel_mask[bb, l, h, st.sel_idx[bb, l, h, :n].long()] = True
+    wl.block_table.masked_fill_(~sel_mask, kvmm.NULL_BLOCK)
+    for l in range(cfg.L):
+        st.decode(l, wl.q[l])
+    torch.cuda.synchronize()
+    assert st.read_err() == 0
+    assert torch.equal(st.out, ref)
+    victim = int(st.sel_idx[0, 0, 0, 3])
+    wl.block_table[0, 0, 0, victim] = kvmm.NULL_BLOCK
+    st.decode(0, wl.q[0])
+    torch.cuda.synchronize()
+    assert st.read_err() & kvmm.ERR_NULL_BLOCK
+    assert not st.read_err() & kvmm.ERR_TIMEOUT
+    stats = parity.Stats()
+    parity.check_unit(wl, st, 0, 0, 0, wl.q[0], None, stats, check_meta=False)
+    stats.check()
