@@ -23,17 +23,18 @@
 //     remote store that completes on the receiver's mbarrier; a page of the
 //     item that receives new tokens first has its bounds widened by them.  An
 //     attention step runs S^T = K Q^T, the online softmax and O^T += V^T P^T
-//     with P as bf16 hi + lo.  At the end of a unit the warps combine their
-//     softmax partials and send every CTA its slice of the outputs, while
-//     their slots already fetch the next unit's pages;
+//     with P as bf16 hi + lo.  At the end of a unit each warp leaves its
+//     softmax partial in shared memory and goes on with the next unit's
+//     pages, already in flight;
 //   - 8 selector warps first take the bounds of the rows a partly filled page
 //     already holds (for the consumer that widens it) and append the new
 //     tokens (rows, and the MinMax of the pages this CTA owns); then, as soon
 //     as all of a unit's scores have arrived, they select the unit's top K
 //     exactly (block_topk) and resolve this CTA's share of the pages through
 //     the block table -- unit 0's selection overlaps the streaming of unit 1's
-//     rows, unit 1's overlaps unit 0's attention -- and finally combine each
-//     unit's partials into out and lse.
+//     rows, unit 1's overlaps unit 0's attention -- and for each unit combine
+//     the consumer warps' partials into the CTA's, send every CTA its slice,
+//     and combine the slices they receive into out and lse.
 // All exchange stays on chip (asynchronous remote shared-memory stores and
 // mbarriers), with no fence on the way: a consumer attending over a page that
 // receives tokens takes those rows from new_k / new_v rather than waiting for
@@ -84,8 +85,9 @@ struct DecodeShared {
     uint64_t sbar[kDUnits];   // all of the unit's scores are here (asynchronous remote stores, 4 bytes each)
     uint64_t selr[kDUnits];   // this CTA's share of the unit's pages is resolved
     uint64_t rbar[kDUnits];   // every CTA's partial of this CTA's output slice is here (likewise)
-    uint64_t gbar;            // consumer-group barrier (kDCons arrivals per use)
     uint64_t pbar;            // prior bounds written (one arrival per selector warp)
+    uint64_t pready[kDUnits]; // every consumer warp's partial of the unit is written (kDCons arrivals)
+    uint64_t pfree;           // the selector warps have read the consumers' partials of unit 0
     DUnit ud[kDUnits];
     int resn[kDUnits];        // resolved pages of this CTA's share
     int wcount[kDSelWarps];
@@ -94,8 +96,10 @@ struct DecodeShared {
     float fw[kDCons][8];
     float fc[kDMaxCluster][8];
     float inv_l[8];
-    uint32_t prior[kDUnits][128];  // per unit: key-ordered bounds of the rows the first appended page
-                                   // already holds, [min | max], two channels a word (D <= 128)
+    uint32_t wide[kDUnits][128];   // per unit: key-ordered bounds of all rows below tok_end of the first
+                                   // page the new tokens reach, [min | max], two channels a word (D <= 128)
+    int wide_ok[kDUnits];          // those bounds are set (the page has a valid table entry)
+    uint4 nrow[kDUnits][32];       // per unit, for a one-token append: the token's key row, then its value row
     int abort_flag;
 };
 
@@ -136,6 +140,19 @@ __device__ __forceinline__ uint32_t from_key2(uint32_t k)
 
 __device__ __forceinline__ int ld_volatile(const int* p) { return *reinterpret_cast<const volatile int*>(p); }
 
+// a long wait of an idle warp: poll with short sleeps so that it leaves the issue slots and the
+// shared-memory pipe to the warps that stream
+__device__ __forceinline__ bool mbar_wait_sleepy(uint64_t* bar, uint32_t parity, uint64_t limit_ns)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        __nanosleep(200);
+        if (global_timer_ns() - t0 > limit_ns) return false;
+    }
+    return true;
+}
+
 // the shared-memory plan, identical on host and device
 struct DLayout {
     size_t ring, part, qbuf, sbuf, bins, ts, selv, res, recv, total;
@@ -150,7 +167,7 @@ __host__ __device__ inline DLayout d_layout(int D, int T, int Pmax, int Kmax, in
     l.recv_stride = 16 * C + l.slice * C;
     l.ring = 0;
     l.part = d_align(l.ring + size_t(kDCons) * d_ring(T) * 4 * T * D);
-    l.qbuf = d_align(l.part + size_t(kDCons) * 8 * D * sizeof(float));
+    l.qbuf = d_align(l.part + size_t(kDCons) * 8 * (D + 4) * sizeof(float));
     l.sbuf = d_align(l.qbuf + size_t(kDUnits) * 8 * D * 2);
     l.bins = d_align(l.sbuf + size_t(kDUnits) * l.pstride * sizeof(float));
     l.ts = d_align(l.bins + size_t(Pmax) * sizeof(int16_t));
@@ -210,8 +227,9 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
             mbar_init(&sh.rbar[j], 1);
             sh.resn[j] = 0;
         }
-        mbar_init(&sh.gbar, kDCons);
         mbar_init(&sh.pbar, kDSelWarps);
+        for (int j = 0; j < kDUnits; ++j) mbar_init(&sh.pready[j], kDCons);
+        mbar_init(&sh.pfree, 1);
         sh.abort_flag = 0;
         fence_barrier_init();
     }
@@ -298,47 +316,60 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
                 mbar_arrive_expect_tx(&sh.rbar[j], static_cast<uint32_t>(C * (2 * G + own)) * 4u);
             }
         }
-        // 0. a page the new tokens only partly fill gets its MinMax over all its rows below tok_end: the
-        //    bounds of the rows it already holds, for the consumer warp that scores and widens it
+        // 0. for the consumer warps, well before they need them: the finished bounds of the first page the
+        //    new tokens reach, if this CTA scores it (all its rows below tok_end, old and new), and for a
+        //    one-token append the token's key and value rows
         if (swarp < nunits) {
-            const DUnit& u = sh.ud[swarp];
-            const int pg = u.tb / T, r0 = u.tb - pg * T;
-            if (u.te > u.tb && u.rescored && r0 > 0 && u.pb <= pg && pg < min(u.pe, u.hi)) {
-                const int32_t phys = p.block_table[u.ufull * p.Pmax + pg];
-                if (phys >= 0 && phys < p.n_phys) {  // else the page is skipped, and reported below
-                    const kvmm_bf16* kpage = p.k_pool + static_cast<size_t>(phys) * T * D;
-                    uint32_t lo[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
-                    uint32_t hi[4] = {0u, 0u, 0u, 0u};
+            const int j = swarp;
+            const DUnit& u = sh.ud[j];
+            if (u.te > u.tb) {
+                const size_t src = (static_cast<size_t>(u.b) * p.Hkv + u.h) * p.n_new;  // token tb's row
+                if (u.te - u.tb == 1 && lane < D / 8) {
+                    sh.nrow[j][lane] = reinterpret_cast<const uint4*>(p.new_k + src * D)[lane];
+                    sh.nrow[j][D / 8 + lane] = reinterpret_cast<const uint4*>(p.new_v + src * D)[lane];
+                }
+                const int pg = u.tb / T, r0 = u.tb - pg * T, r1 = min(u.te - pg * T, T);
+                if (u.rescored && u.pb <= pg && pg < min(u.pe, u.hi)) {
+                    const int32_t phys = p.block_table[u.ufull * p.Pmax + pg];
+                    const bool ok = phys >= 0 && phys < p.n_phys;  // else the page is skipped, and reported below
+                    if (ok) {
+                        const kvmm_bf16* kpage = p.k_pool + static_cast<size_t>(phys) * T * D;
+                        uint32_t lo[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
+                        uint32_t hi[4] = {0u, 0u, 0u, 0u};
 #pragma unroll 4
-                    for (int r = lane / kLanesPerRow; r < r0; r += kRowsPerPass) {
-                        const uint4 v = reinterpret_cast<const uint4*>(kpage + static_cast<size_t>(r) * D)[sub];
-                        const uint32_t w4[4] = {to_key2(v.x), to_key2(v.y), to_key2(v.z), to_key2(v.w)};
+                        for (int r = lane / kLanesPerRow; r < r1; r += kRowsPerPass) {
+                            const kvmm_bf16* row = r < r0 ? kpage + static_cast<size_t>(r) * D
+                                                          : p.new_k + (src + (r - r0)) * D;
+                            const uint4 v = reinterpret_cast<const uint4*>(row)[sub];
+                            const uint32_t w4[4] = {to_key2(v.x), to_key2(v.y), to_key2(v.z), to_key2(v.w)};
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            lo[i] = __vminu2(lo[i], w4[i]);
-                            hi[i] = __vmaxu2(hi[i], w4[i]);
+                            for (int i = 0; i < 4; ++i) {
+                                lo[i] = __vminu2(lo[i], w4[i]);
+                                hi[i] = __vmaxu2(hi[i], w4[i]);
+                            }
+                        }
+#pragma unroll
+                        for (int off = kLanesPerRow; off < 32; off <<= 1) {
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                lo[i] = __vminu2(lo[i], __shfl_xor_sync(kFullMask, lo[i], off));
+                                hi[i] = __vmaxu2(hi[i], __shfl_xor_sync(kFullMask, hi[i], off));
+                            }
+                        }
+                        if (lane < kLanesPerRow) {
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                sh.wide[j][4 * sub + i] = lo[i];
+                                sh.wide[j][D / 2 + 4 * sub + i] = hi[i];
+                            }
                         }
                     }
-#pragma unroll
-                    for (int off = kLanesPerRow; off < 32; off <<= 1) {
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            lo[i] = __vminu2(lo[i], __shfl_xor_sync(kFullMask, lo[i], off));
-                            hi[i] = __vmaxu2(hi[i], __shfl_xor_sync(kFullMask, hi[i], off));
-                        }
-                    }
-                    if (lane < kLanesPerRow) {
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            sh.prior[swarp][4 * sub + i] = lo[i];
-                            sh.prior[swarp][D / 2 + 4 * sub + i] = hi[i];
-                        }
-                    }
+                    if (lane == 0) sh.wide_ok[j] = ok ? 1 : 0;
                 }
             }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sh.pbar);  // release: the bounds above
+        if (lane == 0) mbar_arrive(&sh.pbar);  // release: the bounds and rows above
         // 1. the appended tokens of the pages this CTA owns: rows, then the pages' MinMax from all
         //    their rows (a consumer scoring such a page widens its own copy of the bounds)
         if (p.new_k != nullptr) {
@@ -409,7 +440,7 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
             const int32_t* src;
             if (u.rescored) {
                 // every score of the unit is here
-                if (!mbar_wait_bounded(&sh.sbar[j], 0, aborting() ? kDAbortNs : kDWaitNs)) set_abort();
+                if (!mbar_wait_sleepy(&sh.sbar[j], 0, aborting() ? kDAbortNs : kDWaitNs)) set_abort();
                 cnt = block_topk<kDSelThreads, SelGroup>(nullptr, u.P, p.K, selv, sbuf + size_t(j) * lay.pstride,
                                                          bins, ts);
                 if (rank == 0) {
@@ -468,11 +499,44 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
             }
         }
 
-        // 3. each unit's output slice: combine the partials of every CTA of the cluster
+        // 3. each unit's outputs: the consumer warps' partials -> this CTA's, sent to every CTA of the
+        //    cluster (each gets its slice); then this CTA's slice from every CTA's partial
         for (int j = 0; j < nunits; ++j) {
             const DUnit& u = sh.ud[j];
-            if (!mbar_wait_bounded(&sh.rbar[j], 0, aborting() ? kDAbortNs : kDWaitNs)) set_abort();
-            const float* rj = recv + size_t(j) * lay.recv_stride;  // [C][16] (m, l), then [C][slice] outputs
+            if (!mbar_wait_sleepy(&sh.pready[j], 0, aborting() ? kDAbortNs : kDWaitNs)) set_abort();
+            float* rj = recv + size_t(j) * lay.recv_stride;  // [C][16] (m, l), then [C][slice] outputs
+            if (stid < G) {
+                float M = -INFINITY;
+#pragma unroll
+                for (int ww = 0; ww < kDCons; ++ww) M = fmaxf(M, sh.mm[ww][stid]);
+                float L = 0.f;
+#pragma unroll
+                for (int ww = 0; ww < kDCons; ++ww) {
+                    const float mw2 = sh.mm[ww][stid];
+                    const float f = mw2 == -INFINITY ? 0.f : exp2f(mw2 - M);
+                    sh.fw[ww][stid] = f;
+                    L = fmaf(sh.ml[ww][stid], f, L);
+                }
+                for (int r = 0; r < C; ++r) {
+                    st_async_f32(rj + 16 * rank + stid, &sh.rbar[j], static_cast<uint32_t>(r), M);
+                    st_async_f32(rj + 16 * rank + 8 + stid, &sh.rbar[j], static_cast<uint32_t>(r), L);
+                }
+            }
+            SelGroup::sync();
+            for (int e = stid; e < n_out; e += kDSelThreads) {
+                const int g = e / D;
+                float O = 0.f;
+#pragma unroll
+                for (int ww = 0; ww < kDCons; ++ww)
+                    O = fmaf(sh.fw[ww][g], part[size_t(ww) * 8 * (D + 4) + g * (D + 4) + (e - g * D)], O);
+                const int r = e / lay.slice;
+                st_async_f32(rj + 16 * C + rank * lay.slice + (e - r * lay.slice), &sh.rbar[j], static_cast<uint32_t>(r),
+                             O);
+            }
+            SelGroup::sync();  // the consumer warps' partials are read
+            if (stid == 0 && j + 1 < nunits) mbar_arrive(&sh.pfree);
+
+            if (!mbar_wait_sleepy(&sh.rbar[j], 0, aborting() ? kDAbortNs : kDWaitNs)) set_abort();
             if (stid < G) {
                 float M = -INFINITY;
                 for (int c = 0; c < C; ++c) M = fmaxf(M, rj[16 * c + stid]);
@@ -511,27 +575,26 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
         uint32_t qf[D / 32][4];  // attention Q^T B fragments of head gid
         int frag = -1;           // which fragments are loaded: 2*unit + (0 score, 1 attention)
         bool have_q = false;
-        uint32_t gsync_n = 0;
-        auto group_sync = [&]() {  // the consumer warps
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sh.gbar);
-            wait_bar_warp(&sh.gbar, gsync_n & 1);
-            ++gsync_n;
-        };
         uint8_t* my_ring = rings + size_t(w) * kRing * kSlot;
-        // what each slot holds: held, unit, item; and the phase its mbarrier waits for
-        bool held[kRing];
-        int hj[kRing], hs[kRing];
-        uint32_t par[kRing];
-#pragma unroll
-        for (int b2 = 0; b2 < kRing; ++b2) {
-            held[b2] = false;
-            hj[b2] = hs[b2] = 0;
-            par[b2] = 0u;
-        }
-        auto land = [&](int b2) {  // b2 is a compile-time index wherever this is called
-            const bool ok = wait_bar_warp(&sh.full[w][b2], par[b2]);
-            par[b2] ^= 1u;
+        // the slots: bit b of `held` -- slot b has a copy in flight; bit b of `par` -- the phase its
+        // mbarrier completes next; (hj, hs) -- the unit and item it holds
+        uint32_t held = 0u, par = 0u;
+        int hj0 = 0, hj1 = 0, hs0 = 0, hs1 = 0;
+        auto set_slot = [&](int b, int j, int s) {
+            held |= 1u << b;
+            if (b) {
+                hj1 = j;
+                hs1 = s;
+            } else {
+                hj0 = j;
+                hs0 = s;
+            }
+        };
+        auto in_flight = [&](int b) { return ((held >> b) & 1u) != 0u; };
+        auto land = [&](int b) {
+            const bool ok = wait_bar_warp(&sh.full[w][b], (par >> b) & 1u);
+            par ^= 1u << b;
+            held &= ~(1u << b);
             return ok;
         };
         auto load_frags = [&](int j, bool att) {
@@ -597,38 +660,46 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
                               p.meta + (ufull * p.Pmax + page0 + 8 * lane) * 2 * D,
                               static_cast<uint32_t>(rows) * kRowBytes, &sh.full[w][b2]);
             }
-            held[b2] = true;
-            hj[b2] = j;
-            hs[b2] = sl;
+            set_slot(b2, j, sl);
         };
         // page `pg` of unit j receives tokens in this launch: its bounds in `staged` (the page's
-        // [min | max] row in shared memory) become those of all its rows below tok_end -- the rows it
-        // already holds (bounds from the selector warps) and the new ones.  The selector warps write
-        // the rows and the metadata; a page they skip (null or out-of-range table entry) keeps its
-        // bounds here too.
-        bool have_prior = false;
-        auto widen_page = [&](int j, int pg, uint8_t* staged) {
-            constexpr int kLanesPerRow = D / 8;  // 16 bytes (8 channels) per lane
-            const DUnit& u = sh.ud[j];
-            const int tb = u.tb, te = u.te;
-            const int first = pg * T;
-            const int r0 = max(tb - first, 0), r1 = min(te - first, T);
-            const int32_t phys = p.block_table[u.ufull * p.Pmax + pg];
-            if (phys < 0 || phys >= p.n_phys || r1 <= r0) return;
-            if (r0 > 0 && !have_prior) {  // the selector warps' bounds of rows [0, r0)
+        // [min | max] row in shared memory) become those of all its rows below tok_end.  The selector warps
+        // have them ready for the first such page; a later page of a multi-token append holds new rows
+        // only.  (The selector warps write the rows and the metadata; a page they skip -- null or
+        // out-of-range table entry -- keeps its bounds here too.)
+        bool have_prep = false;  // the selector warps' preparations are visible
+        auto wait_prep = [&]() {
+            if (!have_prep) {
                 wait_bar_warp(&sh.pbar, 0);
-                have_prior = true;
+                have_prep = true;
             }
+        };
+        auto widen_page = [&](int j, int pg, uint8_t* staged) {
+            const DUnit& u = sh.ud[j];
+            if (pg == u.tb / T) {
+                wait_prep();
+                if (sh.wide_ok[j] && lane < D / 4) {
+                    const uint32_t* wv = sh.wide[j] + 4 * lane;
+                    *reinterpret_cast<uint4*>(staged + 16 * lane) =
+                        make_uint4(from_key2(wv[0]), from_key2(wv[1]), from_key2(wv[2]), from_key2(wv[3]));
+                }
+                __syncwarp();
+                return;
+            }
+            constexpr int kLanesPerRow = D / 8;  // 16 bytes (8 channels) per lane
+            const int first = pg * T;
+            const int r1 = min(u.te - first, T);
+            const int32_t phys = p.block_table[u.ufull * p.Pmax + pg];
+            if (phys < 0 || phys >= p.n_phys || r1 <= 0) return;
             const size_t src_base = (static_cast<size_t>(u.b) * p.Hkv + u.h) * p.n_new;
             const int half = lane / kLanesPerRow;  // 0: min, 1: max
             const int sub = lane % kLanesPerRow;
             if (half < 2) {
                 uint32_t acc[4];
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    acc[i] = r0 > 0 ? sh.prior[j][half * (D / 2) + 4 * sub + i] : (half == 0 ? 0xffffffffu : 0u);
-                for (int r = r0; r < r1; ++r) {
-                    const uint4 kv = reinterpret_cast<const uint4*>(p.new_k + (src_base + (first + r - tb)) * D)[sub];
+                for (int i = 0; i < 4; ++i) acc[i] = half == 0 ? 0xffffffffu : 0u;
+                for (int r = 0; r < r1; ++r) {
+                    const uint4 kv = reinterpret_cast<const uint4*>(p.new_k + (src_base + (first + r - u.tb)) * D)[sub];
                     const uint32_t k4[4] = {to_key2(kv.x), to_key2(kv.y), to_key2(kv.z), to_key2(kv.w)};
 #pragma unroll
                     for (int i = 0; i < 4; ++i)
@@ -689,37 +760,28 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
         {
             int ij = 0, isl = w - kDCons;  // the last issued item
             bool more = next_score(ij, isl);
-#pragma unroll
-            for (int b2 = 0; b2 < kRing; ++b2) {
-                if (more) {
-                    issue_score(b2, ij, isl);
-                    more = next_score(ij, isl);
-                }
+            for (int b = 0; b < kRing && more; ++b) {
+                issue_score(b, ij, isl);
+                more = next_score(ij, isl);
             }
-            // slots are used in turn, so they are consumed in the order they were filled
-            for (bool any = true; any;) {
-                any = false;
-#pragma unroll
-                for (int b2 = 0; b2 < kRing; ++b2) {
-                    if (!held[b2]) continue;
-                    any = true;
-                    const int j = hj[b2];
-                    const int page0 = sh.ud[j].lo + hs[b2] * kPiece;
-                    const int npg = min(kPiece, sh.ud[j].hi - page0);
-                    land(b2);
-                    load_frags(j, false);
-                    uint8_t* slot = my_ring + size_t(b2) * kSlot;
-                    const int pe = min(sh.ud[j].pe, page0 + npg);
-                    for (int pg = max(sh.ud[j].pb, page0); pg < pe; ++pg)  // pages receiving new tokens
-                        widen_page(j, pg, slot + size_t(pg - page0) * kRowBytes);
-                    score_slot(slot, j, page0, npg);
-                    __syncwarp();
-                    fence_proxy_async_shared();  // this slot's reads, then the next copy into it
-                    held[b2] = false;
-                    if (more) {
-                        issue_score(b2, ij, isl);
-                        more = next_score(ij, isl);
-                    }
+            // a slot is refilled as soon as it is consumed, and the slots are consumed in turn: in the
+            // order they were filled
+            for (int b = 0; in_flight(b); b = (b + 1) % kRing) {
+                const int j = b ? hj1 : hj0;
+                const int page0 = sh.ud[j].lo + (b ? hs1 : hs0) * kPiece;
+                const int npg = min(kPiece, sh.ud[j].hi - page0);
+                land(b);
+                load_frags(j, false);
+                uint8_t* slot = my_ring + size_t(b) * kSlot;
+                const int pe = min(sh.ud[j].pe, page0 + npg);
+                for (int pg = max(sh.ud[j].pb, page0); pg < pe; ++pg)  // pages receiving new tokens
+                    widen_page(j, pg, slot + size_t(pg - page0) * kRowBytes);
+                score_slot(slot, j, page0, npg);
+                __syncwarp();
+                fence_proxy_async_shared();  // this slot's reads, then the next copy into it
+                if (more) {
+                    issue_score(b, ij, isl);
+                    more = next_score(ij, isl);
                 }
             }
         }
@@ -849,6 +911,16 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
             const int r0 = max(u.tb - first, 0), r1 = min(u.te - first, T);
             const size_t src_base = (static_cast<size_t>(u.b) * p.Hkv + u.h) * p.n_new;
             kvmm_bf16* vt = reinterpret_cast<kvmm_bf16*>(slot + kPageBytes);  // value d of token r at [d*T + r]
+            if (u.te - u.tb == 1) {  // the token's rows, staged by the selector warps
+                wait_prep();
+                if (lane < D / 8)
+                    *reinterpret_cast<uint4*>(slot + static_cast<size_t>(r0) * 2 * D + 16 * lane) = sh.nrow[j][lane];
+                const kvmm_bf16* vsrc = reinterpret_cast<const kvmm_bf16*>(&sh.nrow[j][D / 8]) + kDimsPerLane * lane;
+#pragma unroll
+                for (int e = 0; e < kDimsPerLane; ++e) vt[static_cast<size_t>(kDimsPerLane * lane + e) * T + r0] = vsrc[e];
+                __syncwarp();
+                return;
+            }
             for (int r = r0; r < r1; ++r) {
                 const size_t jj = src_base + (first + r - u.tb);
                 if (lane < D / 8)
@@ -868,12 +940,11 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
                 const size_t off = static_cast<size_t>(res[size_t(j) * p.maxp + s].x) * T * D;
                 bulk_copy_g2s(dst, (lane ? p.v_pool : p.k_pool) + off, kPageBytes, &sh.full[w][b2]);
             }
-            held[b2] = true;
-            hj[b2] = j;
-            hs[b2] = s;
+            set_slot(b2, j, s);
         };
         bool next_known = false;  // the next unit's pages are resolved and its steps may be fetched
         int next_nx = w;          // the next unit's next step to fetch
+        int b = 0;                // the slot consumed next: the oldest in flight, if any is
         for (int j = 0; j < nunits; ++j) {
             if (!(j > 0 && next_known)) wait_bar_warp(&sh.selr[j], 0);
             const int n = sh.resn[j];
@@ -881,104 +952,70 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
             next_known = false;
             next_nx = w;
             load_frags(j, true);
-#pragma unroll
-            for (int b2 = 0; b2 < kRing; ++b2) {
-                if (!held[b2] && nx < n) {
-                    issue_att(b2, j, nx);
+            if (kRing == 2 && !in_flight(b) && in_flight(b ^ 1)) b ^= 1;
+            for (int t = 0; t < kRing; ++t) {
+                const int bb = (b + t) % kRing;
+                if (!in_flight(bb) && nx < n) {
+                    issue_att(bb, j, nx);
                     nx += kDCons;
                 }
             }
             const int jn = j + 1;
-            for (bool any = true; any;) {
-                any = false;
-#pragma unroll
-                for (int b2 = 0; b2 < kRing; ++b2) {
-                    if (!held[b2] || hj[b2] != j) continue;
-                    any = true;
-                    const int lp = res[size_t(j) * p.maxp + hs[b2]].y;
-                    const int nv = min(T, sh.ud[j].seq - lp * T);
-                    uint8_t* slot = my_ring + size_t(b2) * kSlot;
-                    land(b2);
-                    if (sh.ud[j].te > lp * T && sh.ud[j].tb < (lp + 1) * T) patch_page(j, lp, slot);
-                    att_step(slot, nv);
-                    __syncwarp();
-                    fence_proxy_async_shared();  // this slot's reads, then the next copy into it
-                    held[b2] = false;
-                    if (nx < n) {
-                        issue_att(b2, j, nx);
-                        nx += kDCons;
-                    } else if (jn < nunits) {
-                        if (!next_known && __all_sync(kFullMask, mbar_try_wait(&sh.selr[jn], 0))) next_known = true;
-                        if (next_known && next_nx < sh.resn[jn]) {
-                            issue_att(b2, jn, next_nx);
-                            next_nx += kDCons;
-                        }
+            for (; in_flight(b) && (b ? hj1 : hj0) == j; b = (b + 1) % kRing) {
+                const int lp = res[size_t(j) * p.maxp + (b ? hs1 : hs0)].y;
+                const int nv = min(T, sh.ud[j].seq - lp * T);
+                uint8_t* slot = my_ring + size_t(b) * kSlot;
+                land(b);
+                if (sh.ud[j].te > lp * T && sh.ud[j].tb < (lp + 1) * T) patch_page(j, lp, slot);
+                att_step(slot, nv);
+                __syncwarp();
+                fence_proxy_async_shared();  // this slot's reads, then the next copy into it
+                if (nx < n) {
+                    issue_att(b, j, nx);
+                    nx += kDCons;
+                } else if (jn < nunits) {
+                    if (!next_known && __all_sync(kFullMask, mbar_try_wait(&sh.selr[jn], 0))) next_known = true;
+                    if (next_known && next_nx < sh.resn[jn]) {
+                        issue_att(b, jn, next_nx);
+                        next_nx += kDCons;
                     }
                 }
             }
 
-            // ---- end of the unit: the warps' partials -> this CTA's, sent to the cluster
+            // ---- end of the unit: this warp's partial, which the selector warps combine
 #pragma unroll
             for (int off = 4; off < 32; off <<= 1) {
                 l0 += __shfl_xor_sync(kFullMask, l0, off);
                 l1 += __shfl_xor_sync(kFullMask, l1, off);
             }
+            if (j > 0) wait_bar_warp(&sh.pfree, 0);  // the previous unit's partials have been read
             if (gid == 0) {
                 sh.mm[w][2 * tig] = m0;
                 sh.mm[w][2 * tig + 1] = m1;
                 sh.ml[w][2 * tig] = l0;
                 sh.ml[w][2 * tig + 1] = l1;
             }
-            float* mw = part + size_t(w) * 8 * D;  // [8 heads][D]
+            // [8 heads][D + 4]: the padding spreads the four tig lanes over distinct banks
+            float* mw = part + size_t(w) * 8 * (D + 4);
 #pragma unroll
             for (int i = 0; i < kMTiles; ++i) {
-                float* w0 = mw + (2 * tig) * D;
-                float* w1 = w0 + D;
+                float* w0 = mw + (2 * tig) * (D + 4);
+                float* w1 = w0 + (D + 4);
                 w0[16 * i + gid] = o[i][0];
                 w1[16 * i + gid] = o[i][1];
                 w0[16 * i + gid + 8] = o[i][2];
                 w1[16 * i + gid + 8] = o[i][3];
             }
-            group_sync();
-            const int gt = w * 32 + lane;  // 0 .. 255 over the consumer group
-            float* rj = recv + size_t(j) * lay.recv_stride;
-            if (gt < G) {
-                float M = -INFINITY;
-#pragma unroll
-                for (int ww = 0; ww < kDCons; ++ww) M = fmaxf(M, sh.mm[ww][gt]);
-                float L = 0.f;
-#pragma unroll
-                for (int ww = 0; ww < kDCons; ++ww) {
-                    const float mw2 = sh.mm[ww][gt];
-                    const float f = mw2 == -INFINITY ? 0.f : exp2f(mw2 - M);
-                    sh.fw[ww][gt] = f;
-                    L = fmaf(sh.ml[ww][gt], f, L);
-                }
-                for (int r = 0; r < C; ++r) {
-                    st_async_f32(rj + 16 * rank + gt, &sh.rbar[j], static_cast<uint32_t>(r), M);
-                    st_async_f32(rj + 16 * rank + 8 + gt, &sh.rbar[j], static_cast<uint32_t>(r), L);
-                }
-            }
-            group_sync();
-            for (int e = gt; e < n_out; e += kDCons * 32) {
-                const int g = e / D;
-                float O = 0.f;
-#pragma unroll
-                for (int ww = 0; ww < kDCons; ++ww) O = fmaf(sh.fw[ww][g], part[size_t(ww) * 8 * D + e], O);
-                const int r = e / lay.slice;
-                st_async_f32(rj + 16 * C + rank * lay.slice + (e - r * lay.slice), &sh.rbar[j], static_cast<uint32_t>(r),
-                             O);
-            }
-            group_sync();  // every warp's partial read before the next unit's merge writes its own
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sh.pready[j]);  // release: the partial above
 #pragma unroll
             for (int i = 0; i < kMTiles; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
             m0 = m1 = -INFINITY;
             l0 = l1 = 0.f;
         }
         // only after a time-out can a slot still be in flight here: let it land before the CTA exits
-#pragma unroll
-        for (int b2 = 0; b2 < kRing; ++b2)
-            if (held[b2]) land(b2);
+        for (int bb = 0; bb < kRing; ++bb)
+            if (in_flight(bb)) land(bb);
     }
     __syncthreads();
     cluster_sync();  // no CTA leaves while another may still address its shared memory
