@@ -3,18 +3,19 @@
 One step = one decode step of the Llama-3.1-8B-shaped 32K-context workload
 (32 layers, B=8, 32 query / 8 KV heads, head_dim 128, 16-token pages,
 budget 128 pages): per layer, append the new token and refresh its page's
-MinMax (kv_minmax_update), score every page, select the top-K and attend over
-the selected pages (page_score_topk_attn: the scoring kernel, then the
-attention kernel that selects its own pages; --unfused runs page_score_topk
-and sparse_paged_decode_attn instead), and list promoted pages
-(topk_promotion_diff, on a side stream).  A layer-step is one layer of
-that step for the whole batch.
+MinMax, score every page, select the top-K and attend over the selected
+pages -- decode_layer, one launch -- and list promoted pages
+(topk_promotion_diff, on a side stream).  --path fused runs
+kv_minmax_update and page_score_topk_attn (scoring kernel, then the attention
+kernel that selects its own pages) instead; --path unfused runs
+kv_minmax_update, page_score_topk and sparse_paged_decode_attn.  A
+layer-step is one layer of that step for the whole batch.
 
 Inputs are seeded synthetic tensors resident in HBM (32 GiB of K/V, 2 GiB of
 metadata); one step touches 4 GiB of distinct data, far more than the 129 MB
 L2, so no flush is needed between steps.  The step is captured once in a
 CUDA graph and replayed; CUDA events on the launching stream time the timed
-region and every launch of the scoring and attention kernels.
+region and every launch of the decode (or scoring and attention) kernels.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 """
@@ -70,7 +71,11 @@ def algorithmic_bytes(cfg, rescored_units=None):
             "attn_launch": kv + cfg.B * cfg.Hq * cfg.D * 2 + units * K * 8 + cfg.B * cfg.Hq * (cfg.D + 1) * 4,
             # one launch: metadata, selected K/V, q, table entries, selection written and read, out + lse
             "fused_launch": meta + kv + cfg.B * cfg.Hq * cfg.D * 2 + units * K * 4 * 3
-                            + cfg.B * cfg.Hq * (cfg.D + 1) * 4}
+                            + cfg.B * cfg.Hq * (cfg.D + 1) * 4,
+            # decode_layer: the above, plus the append (new K/V row read, the page's earlier rows re-read,
+            # its metadata row written)
+            "decode_launch": meta + kv + cfg.B * cfg.Hq * cfg.D * 2 + units * K * 4 * 3
+                             + cfg.B * cfg.Hq * (cfg.D + 1) * 4 + units * (2 * cfg.D * 2 + page + 2 * cfg.D * 2)}
 
 
 def peaks():
@@ -287,16 +292,22 @@ def gpu_arm(args):
     side = torch.cuda.Stream()
     forks = [torch.cuda.Event() for _ in range(L)]
 
-    fused = not args.unfused
+    path = args.path
+    fused = path != "unfused"  # one timed launch group per layer (decode_layer, or scoring + attention)
 
     def step(instrument):
         main = torch.cuda.current_stream()
         for l in range(L):
-            kvmm.kv_minmax_update(st.shape, l, nk_dev[l], nv_dev[l], 1, st.tok_begin, st.seq_len, st.k_pool,
-                                  st.v_pool, st.block_table, st.meta, st.err)
+            if path != "decode_layer":
+                kvmm.kv_minmax_update(st.shape, l, nk_dev[l], nv_dev[l], 1, st.tok_begin, st.seq_len, st.k_pool,
+                                      st.v_pool, st.block_table, st.meta, st.err)
             if instrument:
                 ev_s[4 * l].record()
-            if fused:  # scoring, then attention that selects its own pages
+            if path == "decode_layer":  # append, score, select and attend in one launch
+                kvmm.decode_layer(st.shape, l, q_dev[l], nk_dev[l], nv_dev[l], 1, st.tok_begin, st.seq_len,
+                                  st.k_pool, st.v_pool, st.block_table, st.meta, st.seq_len, None, st.K, st.sel_idx,
+                                  st.sel_cnt, st.out[l], lse=st.lse[l], err=st.err, workspace=st.workspace)
+            elif path == "fused":  # scoring, then attention that selects its own pages
                 st.select_attend(l, q_dev[l])
             else:
                 st.select(l, q_dev[l])
@@ -418,7 +429,10 @@ def gpu_arm(args):
     kv_gbs = acc["total"] * n_ls / secs / 1e9
     peak, peak_kind = peaks()
     s_ms, a_ms = statistics.mean(score_ms), statistics.mean(attn_ms)
-    if fused:
+    if path == "decode_layer":
+        dom, dom_ms, dom_bytes = "decode_layer", s_ms, acc["decode_launch"]
+        kernel_ms = {"decode_layer": s_ms}
+    elif fused:
         dom, dom_ms, dom_bytes = "page_score_topk_attn", s_ms, acc["fused_launch"]
         kernel_ms = {"page_score_topk_attn": s_ms}
     else:
@@ -441,8 +455,10 @@ def gpu_arm(args):
                    "l2": "inputs larger than L2 (4 GiB of distinct data per step, no flush)",
                    "step": f"one decode step = {L} layer-steps, " + ("eager launches" if args.no_graph
                                                                      else "CUDA graph replay"),
-                   "path": "page_score_topk_attn (scoring kernel + selecting attention kernel)" if fused
-                           else "page_score_topk + sparse_paged_decode_attn"},
+                   "path": {"decode_layer": "decode_layer (append, score, select, attend: one launch)",
+                            "fused": "kv_minmax_update + page_score_topk_attn (scoring kernel + selecting "
+                                     "attention kernel)",
+                            "unfused": "kv_minmax_update + page_score_topk + sparse_paged_decode_attn"}[path]},
         "kv_gbs": kv_gbs, "pct_hbm_peak": kv_gbs / peak,
         "bytes_per_layer_step": acc["total"],
         "kernel_ms": kernel_ms,
@@ -455,8 +471,9 @@ def gpu_arm(args):
         "e2e": {"value": e2e_steps * L * world / (e2e_ms / 1e3), "unit": "layer-steps/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "how": "pinned host q/new K,V -> device, graph replay, out/lse/promoted counts -> pinned host"},
-        # per layer: update, score, selecting attention, diff (fused) or update, score, top-K, diff, attention
-        "gpu_launches": (4 if fused else 5) * L * args.steps,
+        # per layer: decode_layer, diff; or update, score, selecting attention, diff (fused); or update,
+        # score, top-K, diff, attention (unfused)
+        "gpu_launches": {"decode_layer": 2, "fused": 4, "unfused": 5}[path] * L * args.steps,
         "clocks": clk,
         "device_err": err_word,
     }
@@ -487,8 +504,9 @@ def main():
     ap.add_argument("--no-graph", action="store_true", help="launch eagerly (for profilers)")
     ap.add_argument("--batch", type=int, default=0, help="override the batch (smaller profiling case)")
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (smaller profiling case)")
-    ap.add_argument("--unfused", action="store_true",
-                    help="page_score_topk + sparse_paged_decode_attn instead of page_score_topk_attn")
+    ap.add_argument("--path", default="decode_layer", choices=["decode_layer", "fused", "unfused"],
+                    help="decode_layer (one launch per layer), fused (kv_minmax_update + page_score_topk_attn) "
+                         "or unfused (kv_minmax_update + page_score_topk + sparse_paged_decode_attn)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.impl == "reference":
