@@ -140,6 +140,12 @@ __device__ __forceinline__ uint32_t from_key2(uint32_t k)
 
 __device__ __forceinline__ int ld_volatile(const int* p) { return *reinterpret_cast<const volatile int*>(p); }
 
+// start fetching `bytes` (a multiple of 16, from a 16-byte aligned address) into L2
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // a long wait of an idle warp: poll with short sleeps so that it leaves the issue slots and the
 // shared-memory pipe to the warps that stream
 __device__ __forceinline__ bool mbar_wait_sleepy(uint64_t* bar, uint32_t parity, uint64_t limit_ns)
@@ -147,7 +153,7 @@ __device__ __forceinline__ bool mbar_wait_sleepy(uint64_t* bar, uint32_t parity,
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     while (!mbar_try_wait(bar, parity)) {
-        __nanosleep(200);
+        __nanosleep(64);
         if (global_timer_ns() - t0 > limit_ns) return false;
     }
     return true;
@@ -303,6 +309,11 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
         constexpr int kLanesPerRow = D / 8;  // 16 bytes (8 channels) per lane
         constexpr int kRowsPerPass = 32 / kLanesPerRow;
         const int sub = lane % kLanesPerRow;
+        if (stid == 0 && (p.Pmax & 3) == 0) {
+            // the units' block-table rows, read when this CTA's share of the selection is resolved
+            for (int j = 0; j < nunits; ++j)
+                prefetch_l2(p.block_table + sh.ud[j].ufull * p.Pmax, static_cast<uint32_t>(p.Pmax) * 4u);
+        }
         if (stid == 0) {
             // the bytes this CTA receives: every score of a rescored unit (one float a page), and from
             // each CTA its (m, l) of every head and its partial of this CTA's slice of the outputs.  A
@@ -1017,8 +1028,9 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
         for (int bb = 0; bb < kRing; ++bb)
             if (in_flight(bb)) land(bb);
     }
-    __syncthreads();
-    cluster_sync();  // no CTA leaves while another may still address its shared memory
+    // No final cluster barrier: every access another CTA makes to this one's shared memory is an
+    // asynchronous store counted by one of this CTA's mbarriers (scores, partials), and the selector
+    // warps have waited for all of them by now.
 }
 
 template <int D, int T, int MODE>
