@@ -9,9 +9,12 @@
 // minimum and maximum (the bin is monotone in the score), a suffix scan
 // finds the bin holding the K-th largest score, the few scores in that bin
 // are ranked exactly (value descending, page ascending), and an ordered
-// compaction writes the winners.  Degenerate inputs (a crowded threshold
-// bin, a non-finite range) take an exact 4-pass radix select over
-// order-preserving keys.  Used with 512 threads by the selection kernel and
+// compaction writes the winners; when every thread can hold its share of the
+// scores in registers, all of this runs on registers (block_topk_reg).
+// Degenerate inputs (a crowded threshold bin, a non-finite range) take an
+// exact 4-pass radix select over order-preserving keys.  The selections are out-of-line
+// functions: called once per unit, they would otherwise share register
+// allocation and scheduling with the caller's streaming loops.  Used with 512 threads by the selection kernel and
 // with the attention CTA's 128 threads when attention selects its own pages.
 #pragma once
 
@@ -65,7 +68,7 @@ __device__ __forceinline__ uint32_t topk_order_key(float f)
 
 // Exact top-K over the P scores in sc[] by 4 radix passes; writes sel[0..K) ascending.
 template <int THREADS, class Group = CtaGroup>
-__device__ void block_radix_topk(const float* sc, int P, int K, int32_t* sel, BlockTopkShared<THREADS>& ts)
+__device__ __noinline__ void block_radix_topk(const float* sc, int P, int K, int32_t* sel, BlockTopkShared<THREADS>& ts)
 {
     constexpr int kWarps = THREADS / 32;
     const int tid = static_cast<int>(threadIdx.x) - Group::kFirst, lane = tid & 31, warp = tid >> 5;
@@ -155,13 +158,167 @@ __device__ void block_radix_topk(const float* sc, int P, int K, int32_t* sel, Bl
     }
 }
 
+// The same selection when every thread can hold its share of the scores in
+// registers (P <= 8 * THREADS): thread t owns pages [8t, 8t + 8), reads them
+// once, bins them and emits its winners in order itself.  The threshold bin's
+// pages are ranked one per thread, as in block_topk, and marked in a bitmask
+// (the radix histogram's space) that their owners read back.  Same bins, same
+// threshold, same result.
+template <int THREADS, class Group = CtaGroup>
+__device__ __noinline__ int block_topk_reg(const float* scores, int P, int K, int32_t* sel, float* sc,
+                              BlockTopkShared<THREADS>& ts)
+{
+    constexpr int kPer = 8;
+    constexpr int kWarps = THREADS / 32;
+    const int tid = static_cast<int>(threadIdx.x) - Group::kFirst;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const int i0 = kPer * tid;
+
+    // 1. this thread's scores, their range, an empty histogram
+    float v[kPer];
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) {
+        const int i = i0 + e;
+        v[e] = i < P ? (scores != nullptr ? __ldcg(scores + i) : sc[i]) : 0.f;
+    }
+    float lo = FLT_MAX, hi = -FLT_MAX;
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) {
+        if (i0 + e < P) {
+            if (scores != nullptr) sc[i0 + e] = v[e];  // the ranking and the radix path read them here
+            lo = fminf(lo, v[e]);
+            hi = fmaxf(hi, v[e]);
+        }
+    }
+    for (int i = tid; i < kTopkBins; i += THREADS) ts.hist[i] = 0;
+    uint32_t* winbits = reinterpret_cast<uint32_t*>(ts.rhist);  // bit i: page i of the threshold bin wins
+    static_assert(8 * THREADS / 32 <= 256, "the winner bitmask fits the radix histogram");
+    for (int i = tid; i < 8 * THREADS / 32; i += THREADS) winbits[i] = 0u;
+    if (tid == 0) ts.ncand = 0;
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+        lo = fminf(lo, __shfl_xor_sync(kFullMask, lo, off));
+        hi = fmaxf(hi, __shfl_xor_sync(kFullMask, hi, off));
+    }
+    if (lane == 0) {
+        ts.wmin[warp] = lo;
+        ts.wmax[warp] = hi;
+    }
+    Group::sync();
+    float mn = ts.wmin[0], mx = ts.wmax[0];
+#pragma unroll
+    for (int w = 1; w < kWarps; ++w) {
+        mn = fminf(mn, ts.wmin[w]);
+        mx = fmaxf(mx, ts.wmax[w]);
+    }
+    if (!(mx > mn)) {  // every score equal: the K lowest pages win the ties
+        for (int i = tid; i < K; i += THREADS) sel[i] = i;
+        Group::sync();
+        return K;
+    }
+    const float scale = static_cast<float>(kTopkBins) / (mx - mn);
+    if (!(scale < FLT_MAX)) {
+        block_radix_topk<THREADS, Group>(sc, P, K, sel, ts);
+        return K;
+    }
+
+    // 2. bins, monotone in the score
+    int b[kPer];
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) {
+        b[e] = -1;
+        if (i0 + e < P) {
+            b[e] = min(kTopkBins - 1, static_cast<int>((v[e] - mn) * scale));
+            atomicAdd(&ts.hist[b[e]], 1);
+        }
+    }
+    Group::sync();
+
+    // 3. the bin holding the K-th largest score: suffix sums over bins
+    constexpr int kBinsPerThread = kTopkBins / THREADS;
+    int local = 0;
+#pragma unroll
+    for (int j = 0; j < kBinsPerThread; ++j) local += ts.hist[kBinsPerThread * tid + j];
+    int incl = local;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int x = __shfl_down_sync(kFullMask, incl, off);
+        if (lane + off < 32) incl += x;
+    }
+    if (lane == 0) ts.wsum[warp] = incl;
+    Group::sync();
+    int above = incl - local;
+    for (int w = warp + 1; w < kWarps; ++w) above += ts.wsum[w];
+    if (above < K && K <= above + local) {
+        int acc = above;
+        for (int j = kBinsPerThread - 1; j >= 0; --j) {
+            const int bj = kBinsPerThread * tid + j;
+            if (acc + ts.hist[bj] >= K) {
+                ts.tb = bj;
+                ts.need = K - acc;
+                ts.cbin = ts.hist[bj];
+                break;
+            }
+            acc += ts.hist[bj];
+        }
+    }
+    Group::sync();
+    const int tb = ts.tb, need = ts.need, cbin = ts.cbin;
+    if (cbin > kTopkCandMax) {  // crowded threshold bin: exact radix path
+        block_radix_topk<THREADS, Group>(sc, P, K, sel, ts);
+        return K;
+    }
+
+    // 4. rank the threshold bin's pages exactly (value descending, page ascending), one per thread
+#pragma unroll
+    for (int e = 0; e < kPer; ++e)
+        if (b[e] == tb) ts.cand[atomicAdd(&ts.ncand, 1)] = i0 + e;
+    Group::sync();
+    for (int t = tid; t < cbin; t += THREADS) {
+        const int i = ts.cand[t];
+        const float s = sc[i];
+        int rank = 0;
+        for (int j = 0; j < cbin; ++j) {
+            const int i2 = ts.cand[j];
+            const float s2 = sc[i2];
+            rank += (s2 > s) || (s2 == s && i2 < i);
+        }
+        if (rank < need) atomicOr(&winbits[i >> 5], 1u << (i & 31));
+    }
+    Group::sync();
+    const uint32_t tw = winbits[i0 >> 5] >> (i0 & 31);  // this thread's 8 pages share one word
+    uint32_t win = 0u;
+#pragma unroll
+    for (int e = 0; e < kPer; ++e)
+        if (b[e] > tb || (b[e] == tb && ((tw >> e) & 1u))) win |= 1u << e;
+
+    // 5. ordered compaction: thread t's winners follow those of threads below t
+    const int mine = __popc(win);
+    int pre = mine;  // inclusive prefix within the warp
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int x = __shfl_up_sync(kFullMask, pre, off);
+        if (lane >= off) pre += x;
+    }
+    if (lane == 31) ts.wsum[warp] = pre;
+    Group::sync();
+    int pos = pre - mine;
+    for (int w = 0; w < warp; ++w) pos += ts.wsum[w];
+#pragma unroll
+    for (int e = 0; e < kPer; ++e)
+        if ((win >> e) & 1u) sel[pos++] = i0 + e;
+    Group::sync();
+    return K;
+}
+
 // Selects the top K of the P scores at `scores` (global memory, read through
 // L2; or null when sc[] already holds them) into sel[] (shared or global
 // memory) and returns the count, min(K, P).  sc (P floats) and bin (P int16)
 // are shared-memory scratch.  Every thread of the group must call it; sel[]
 // is complete for every thread of the group on return.
 template <int THREADS, class Group = CtaGroup>
-__device__ int block_topk(const float* scores, int P, int K, int32_t* sel, float* sc, int16_t* bin,
+__device__ __noinline__ int block_topk(const float* scores, int P, int K, int32_t* sel, float* sc, int16_t* bin,
                           BlockTopkShared<THREADS>& ts)
 {
     constexpr int kWarps = THREADS / 32;
@@ -173,6 +330,7 @@ __device__ int block_topk(const float* scores, int P, int K, int32_t* sel, float
         Group::sync();
         return P;
     }
+    if (P <= 8 * THREADS) return block_topk_reg<THREADS, Group>(scores, P, K, sel, sc, ts);
 
     // 1. scores to shared memory (16 loads in flight per thread), their range, an empty histogram
     constexpr int kBatch = 16;
