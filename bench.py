@@ -484,6 +484,73 @@ def gpu_arm(args):
         dist.destroy_process_group()
 
 
+def stability_arm(args):
+    """Head-stability profiling at the 8B-32K shape (B 8, L 32, Hkv 8, K 128): record one decode step's
+    selections of every layer into a W-step ring, then the RCO of every unit over the window and the
+    classification.  Timed with CUDA events on the launching stream; latency-bound kernels, reported in us."""
+    from paged_kv_cache_minmax_gb300 import build as kbuild
+    from paged_kv_cache_minmax_gb300 import kvmm
+    from paged_kv_cache_minmax_gb300.runtime import StabilityProfiler
+
+    kbuild.build_library()
+    kvmm.load()
+    cfg, W = CFG, 16
+    shape = kvmm.make_shape(cfg.B, cfg.L, cfg.Hq, cfg.Hkv, cfg.D, cfg.T, cfg.Pmax, cfg.K, 1)
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(cfg.seed + 17)
+    units = cfg.B * cfg.L * cfg.Hkv
+    sel = torch.rand(units, cfg.P, generator=gen, device="cuda").topk(cfg.K, dim=1).indices.sort(dim=1).values
+    sel_idx = sel.to(torch.int32).view(cfg.B, cfg.L, cfg.Hkv, cfg.K).contiguous()
+    sel_cnt = torch.full((cfg.B, cfg.L, cfg.Hkv), cfg.K, dtype=torch.int32, device="cuda")
+    seq_len = torch.full((cfg.B,), cfg.S, dtype=torch.int32, device="cuda")
+
+    class _State:
+        pass
+
+    state = _State()
+    state.sel_idx, state.sel_cnt, state.seq_len = sel_idx, sel_cnt, seq_len
+    prof = StabilityProfiler(shape, W)
+    for _ in range(W):
+        prof.record(state)
+    # each call is captured in a CUDA graph and replayed, so the events time the device, not the host
+    stream = torch.cuda.Stream()
+    e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    reps = max(args.steps, 20)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            prof.record(state)
+            prof.classify(lag=1)
+    stream.synchronize()
+    g_rec, g_rco = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_rec, stream=stream):
+        prof.record(state)
+    with torch.cuda.graph(g_rco, stream=stream):
+        prof.classify(lag=1)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            g_rec.replay()
+            g_rco.replay()
+        e[0].record()
+        for _ in range(reps):
+            g_rec.replay()
+        e[1].record()
+        for _ in range(reps):
+            g_rco.replay()
+        e[2].record()
+    stream.synchronize()
+    rec_us = e[0].elapsed_time(e[1]) * 1e3 / reps
+    rco_us = e[1].elapsed_time(e[2]) * 1e3 / reps
+    pairs = W - 1
+    rco_bytes = (W * units * (cfg.K + 1) * 4 + W * cfg.B * 4) + units * 4 + cfg.L * cfg.Hkv * 5
+    print(json.dumps({
+        "metric": "head-stability profiling: RCO over a W-step window, 8B-32K shape", "unit": "us",
+        "higher_is_better": False, "record_step_us": rec_us, "rco_classify_us": rco_us,
+        "config": {"workload": cfg.name, "units": units, "window": W, "pairs_per_unit": pairs, "top_k": cfg.K,
+                   "layers": cfg.L},
+        "rco_bytes_read": rco_bytes, "rco_gbs": rco_bytes / (rco_us * 1e-6) / 1e9,
+        "device_err": int(prof.err.item())}), flush=True)
+
+
 def load_traffic(kernel):
     """dram bytes per launch of ``kernel`` from the committed ncu summary, if current."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
@@ -504,6 +571,8 @@ def main():
     ap.add_argument("--no-graph", action="store_true", help="launch eagerly (for profilers)")
     ap.add_argument("--batch", type=int, default=0, help="override the batch (smaller profiling case)")
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (smaller profiling case)")
+    ap.add_argument("--stability", action="store_true",
+                    help="time head-stability profiling (history record, RCO and classification) instead")
     ap.add_argument("--path", default="decode_layer", choices=["decode_layer", "fused", "unfused"],
                     help="decode_layer (one launch per layer), fused (kv_minmax_update + page_score_topk_attn) "
                          "or unfused (kv_minmax_update + page_score_topk + sparse_paged_decode_attn)")
@@ -511,6 +580,8 @@ def main():
     args.warmup = max(args.warmup, 3)
     if args.impl == "reference":
         reference_arm(args)
+    elif args.stability:
+        stability_arm(args)
     else:
         gpu_arm(args)
 

@@ -310,6 +310,65 @@ kvmm_status decode_layer(const kvmm_shape* shape, int32_t layer, const kvmm_bf16
                          float sm_scale, int32_t* sel_idx, int32_t* sel_cnt, float* scores_out, float* out,
                          float* lse, void* workspace, size_t workspace_bytes, int32_t* err, kvmm_stream stream);
 
+/* ------------------------------------------------------------------------
+ * Temporal stability of each (layer, KV head): offline profiling that
+ * classifies heads as stable or unstable.
+ *
+ * FlexiCache, "Core insight: attention heads differ in temporal stability":
+ * the top-K page set of each head is recorded at every decode step; sets a
+ * few steps apart are compared with the Random-Corrected Overlap (RCO),
+ * which is 1 for identical sets and 0 for the overlap random sets would
+ * have; RCO is aggregated over a window of W steps into a per-head
+ * stability score, and the least stable 25% of the heads are classed
+ * unstable (they are rescored every step, see rescore_mask).
+ *
+ * The pages print no formula.  The reading used here: for sets A, B drawn
+ * from P pages,
+ *     RCO(A, B) = (|A n B| - |A||B|/P) / (min(|A|, |B|) - |A||B|/P)
+ * where |A||B|/P is the expected overlap of random subsets of those sizes
+ * and min(|A|, |B|) the largest possible one; RCO = 1 when the two are
+ * equal (every page selected, or P = 0).  When the sequence grew between
+ * the two steps, P is the later (larger) page count.
+ * ------------------------------------------------------------------------
+ *
+ * topk_history_record -- store layer `layer`'s current selections (every
+ * layer's when layer = -1, in one launch) in slot `slot` (0 <= slot < W) of
+ * a history ring of W steps:
+ *     hist_idx   [W][B][L][Hkv][Kmax] int32   <- sel_idx  (ascending pages)
+ *     hist_cnt   [W][B][L][Hkv]       int32   <- sel_cnt
+ *     hist_pages [W][B]               int32   <- ceil(seq_len[b] / T), the
+ *                page count the selections were taken over (seq_len clamped
+ *                to [0, Pmax*T], out-of-range values set KVMM_ERR_OUT_OF_RANGE
+ *                when err is given).
+ * A decode step records every layer into the same slot (step mod W).
+ */
+kvmm_status topk_history_record(const kvmm_shape* shape, int32_t layer, const int32_t* sel_idx,
+                                const int32_t* sel_cnt, const int32_t* seq_len, int32_t W, int32_t slot,
+                                int32_t* hist_idx, int32_t* hist_cnt, int32_t* hist_pages, int32_t* err,
+                                kvmm_stream stream);
+
+/* topk_stability_rco -- stability of every unit and head from the last n
+ * recorded steps of the ring (the newest in slot `head`, the one before in
+ * slot head - 1 mod W, ...), comparing selections `lag` steps apart.
+ *     rco_unit  [B][L][Hkv] float: the mean of RCO(S_t, S_{t+lag}) over the
+ *               n - lag pairs t = 0 .. n - lag - 1 (t steps before the newest);
+ *     stability [L][Hkv] float (may be NULL): the mean of rco_unit over b;
+ *     unstable  [L][Hkv] uint8 (may be NULL): 1 for the round(unstable_frac *
+ *               L * Hkv) heads of lowest stability (ties: lower l * Hkv + h
+ *               first), else 0.
+ * Requires 1 <= n <= W, 0 <= head < W, 1 <= lag < n, 0 <= unstable_frac <= 1
+ * (else KVMM_INVALID_ARG), n <= 1024 and L * Hkv <= 4096 (else
+ * KVMM_UNSUPPORTED_SHAPE).
+ * A recorded count outside [0, Kmax], or a page count outside [0, Pmax], sets
+ * KVMM_ERR_OUT_OF_RANGE and is clamped; a recorded page outside [0, Pmax)
+ * sets it and is not counted.  Selections must be ascending and distinct (as
+ * sel_idx is); their overlap is counted exactly.  Sums run in double.
+ */
+kvmm_status topk_stability_rco(const kvmm_shape* shape, const int32_t* hist_idx, const int32_t* hist_cnt,
+                               const int32_t* hist_pages, int32_t W, int32_t n, int32_t head, int32_t lag,
+                               float unstable_frac, float* rco_unit, float* stability, uint8_t* unstable,
+                               int32_t* err, kvmm_stream stream);
+
 /* Workspace bytes that page_score_topk and page_score_topk_attn need
  * (sparse_paged_decode_attn needs none; num_splits is accepted for the
  * stable signature and ignored).  Returns 0 for an unsupported shape. */

@@ -67,6 +67,12 @@ def _load():
         lib.oracle_unit_sparse_attention.restype = I32
         lib.oracle_unit_dense_attention.argtypes = [P, I32, I32, I32, P, P, I64, P, I32, D, P, P]
         lib.oracle_unit_dense_attention.restype = I32
+        lib.oracle_rco.argtypes = [P, I32, P, I32, I32]
+        lib.oracle_rco.restype = D
+        lib.oracle_unit_stability.argtypes = [P, P, P, I32, I32, I32]
+        lib.oracle_unit_stability.restype = D
+        lib.oracle_classify.argtypes = [P, I32, D, P]
+        lib.oracle_classify.restype = None
         lib.oracle_unit_step.argtypes = [P, P, I64, I32, I32, P, I32, P, P, P, P, I32, I32, I32, I32,
                                          P, P, P, P, P, P, P, D, P, P]
         lib.oracle_unit_step.restype = I32
@@ -143,6 +149,28 @@ def set_difference(a, b) -> np.ndarray:
     out = np.zeros(max(len(a), 1), dtype=np.int32)
     n = _load().oracle_set_difference(_ptr(a), len(a), _ptr(b), len(b), _ptr(out))
     return out[:n].copy()
+
+
+def rco(a, b, P) -> float:
+    """Random-Corrected Overlap of page sets a and b drawn from P pages (FlexiCache, "Core insight")."""
+    a, b = _i32(a), _i32(b)
+    return float(_load().oracle_rco(_ptr(a), len(a), _ptr(b), len(b), int(P)))
+
+
+def unit_stability(idx, cnt, pages, lag) -> float:
+    """Mean RCO of steps ``lag`` apart over a window given newest first: idx [n, kmax], cnt [n], pages [n]."""
+    idx = np.ascontiguousarray(idx, dtype=np.int32)
+    cnt, pages = _i32(cnt), _i32(pages)
+    n, kmax = idx.shape
+    return float(_load().oracle_unit_stability(_ptr(idx), _ptr(cnt), _ptr(pages), kmax, n, int(lag)))
+
+
+def classify(stability, frac) -> np.ndarray:
+    """1 for the round(frac * n) entries of lowest stability (ties: lower index first)."""
+    st = np.ascontiguousarray(stability, dtype=np.float64).ravel()
+    out = np.zeros(max(st.size, 1), dtype=np.uint8)
+    _load().oracle_classify(_ptr(st), st.size, float(frac), _ptr(out))
+    return out[:st.size].copy()
 
 
 def unit_sparse_attention(q, k_pool, v_pool, T, bt_row, seq_len, sel, scale=0.0):

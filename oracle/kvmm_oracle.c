@@ -24,6 +24,11 @@
  *       block that is never dereferenced.
  *     - "Core method, 1. Stability-differentiated placement": decode
  *       attention runs over the top-K pages only.
+ *     - "Core insight: attention heads differ in temporal stability": the
+ *       top-K sets of a head are compared a few steps apart with the
+ *       Random-Corrected Overlap (1 = identical sets, 0 = the overlap of
+ *       random sets), aggregated over a window W; the least stable quarter
+ *       of the heads is unstable.
  *   KVDrive: A Holistic Multi-Tier KV Cache Management System for
  *   Long-Context LLM Inference, "Background and key observations": Quest
  *   multiplies the query with the keys' channel-wise min and max.
@@ -41,6 +46,15 @@
  *     result is a unique bf16 bit pattern;
  *   - attention scale defaults to D^-1/2; output and log-sum-exp in double;
  *     a unit with no valid token yields output 0 and lse = -inf.
+ *   - RCO(A, B) = (|A n B| - |A||B|/P) / (min(|A|,|B|) - |A||B|/P): the
+ *     overlap minus that of random subsets of the same sizes among P pages,
+ *     over its largest possible value (evaluated as the ratio of the exact
+ *     integers P|A n B| - |A||B| and P min(|A|,|B|) - |A||B|); 1 when the two
+ *     are equal (every page selected, or P = 0); P is the later (larger) page
+ *     count of the two
+ *     steps; a head's stability is the mean over the window's pairs (and
+ *     over the batch); round(frac * heads) heads of lowest stability are
+ *     unstable, ties to the lower index.
  *
  * bf16 values are passed as their raw 16-bit patterns (uint16_t).
  *
@@ -369,4 +383,66 @@ int32_t oracle_unit_step(uint16_t* k_pool, uint16_t* v_pool, int64_t n_phys, int
     err |= oracle_unit_sparse_attention(q, G, D, T, k_pool, v_pool, n_phys, bt_row, seq_len, sel,
                                         *sel_cnt, scale, out, lse);
     return err;
+}
+
+/* ------------------------------------------------------------------------
+ * Temporal stability (FlexiCache, "Core insight: attention heads differ in
+ * temporal stability").
+ */
+
+/* |A n B| of two sets of distinct page indices, in any order: every pair. */
+static int32_t overlap_count(const int32_t* a, int32_t na, const int32_t* b, int32_t nb)
+{
+    int32_t n = 0;
+    for (int32_t i = 0; i < na; ++i)
+        for (int32_t j = 0; j < nb; ++j)
+            if (a[i] == b[j]) {
+                ++n;
+                break;
+            }
+    return n;
+}
+
+/* Random-Corrected Overlap of sets A and B drawn from P pages:
+ *   (|A n B| - |A||B|/P) / (min(|A|,|B|) - |A||B|/P),
+ * |A||B|/P the expected overlap of random subsets of those sizes, min the
+ * largest possible.  Numerator and denominator are multiplied by P > 0, so
+ * both are exact integers and the value is one correctly rounded division. */
+double oracle_rco(const int32_t* a, int32_t na, const int32_t* b, int32_t nb, int32_t P)
+{
+    if (P <= 0) return 1.0;
+    const int64_t chance_p = (int64_t)na * nb;         /* P * expected overlap */
+    const int64_t best_p = (int64_t)(na < nb ? na : nb) * P; /* P * largest overlap */
+    if (best_p - chance_p <= 0) return 1.0;
+    return (double)((int64_t)overlap_count(a, na, b, nb) * P - chance_p) / (double)(best_p - chance_p);
+}
+
+/* A unit's stability over a window of n recorded steps, newest first: step t
+ * holds cnt[t] pages at idx + t * kmax, taken over pages[t] pages.  The mean
+ * of RCO(step t, step t + lag) over t = 0 .. n - lag - 1, P the larger of the
+ * two page counts.  NaN when there is no pair. */
+double oracle_unit_stability(const int32_t* idx, const int32_t* cnt, const int32_t* pages, int32_t kmax,
+                             int32_t n, int32_t lag)
+{
+    double sum = 0.0;
+    int32_t pairs = 0;
+    for (int32_t t = 0; t + lag < n; ++t) {
+        const int32_t P = pages[t] > pages[t + lag] ? pages[t] : pages[t + lag];
+        sum += oracle_rco(idx + (int64_t)t * kmax, cnt[t], idx + (int64_t)(t + lag) * kmax, cnt[t + lag], P);
+        ++pairs;
+    }
+    return pairs ? sum / (double)pairs : NAN;
+}
+
+/* unstable[i] = 1 for the round(frac * n) entries of lowest stability (ties:
+ * lower index first), else 0.  round() rounds half up: floor(x + 0.5). */
+void oracle_classify(const double* stability, int32_t n, double frac, uint8_t* unstable)
+{
+    const int32_t k = (int32_t)floor(frac * (double)n + 0.5);
+    for (int32_t i = 0; i < n; ++i) {
+        int32_t rank = 0;
+        for (int32_t j = 0; j < n; ++j)
+            if (stability[j] < stability[i] || (stability[j] == stability[i] && j < i)) ++rank;
+        unstable[i] = rank < k ? 1 : 0;
+    }
 }

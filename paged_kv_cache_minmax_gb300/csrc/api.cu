@@ -470,4 +470,73 @@ kvmm_status topk_promotion_diff(const kvmm_shape* shape, int32_t layer,
     return launched(kvmm::launch_promotion_diff(p, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+kvmm_status topk_history_record(const kvmm_shape* shape, int32_t layer, const int32_t* sel_idx,
+                                const int32_t* sel_cnt, const int32_t* seq_len, int32_t W, int32_t slot,
+                                int32_t* hist_idx, int32_t* hist_cnt, int32_t* hist_pages, int32_t* err,
+                                kvmm_stream stream)
+{
+    kvmm_status st = check_shape(shape);
+    if (st != KVMM_OK) return st;
+    const kvmm_shape& s = *shape;
+    if (layer < -1 || layer >= s.L || W < 1 || slot < 0 || slot >= W) return KVMM_INVALID_ARG;
+    if (!req4(sel_idx) || !req4(sel_cnt) || !req4(seq_len) || !req4(hist_idx) || !req4(hist_cnt) ||
+        !req4(hist_pages) || !opt4(err))
+        return KVMM_INVALID_ARG;
+    kvmm::StabilityParams p{};
+    p.B = s.B;
+    p.L = s.L;
+    p.Hkv = s.Hkv;
+    p.T = s.T;
+    p.Pmax = s.Pmax;
+    p.Kmax = s.Kmax;
+    p.W = W;
+    p.layer = layer;
+    p.slot = slot;
+    p.sel_idx = sel_idx;
+    p.sel_cnt = sel_cnt;
+    p.seq_len = seq_len;
+    p.hist_idx = hist_idx;
+    p.hist_cnt = hist_cnt;
+    p.hist_pages = hist_pages;
+    p.err = err;
+    return launched(kvmm::launch_history_record(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+kvmm_status topk_stability_rco(const kvmm_shape* shape, const int32_t* hist_idx, const int32_t* hist_cnt,
+                               const int32_t* hist_pages, int32_t W, int32_t n, int32_t head, int32_t lag,
+                               float unstable_frac, float* rco_unit, float* stability, uint8_t* unstable,
+                               int32_t* err, kvmm_stream stream)
+{
+    kvmm_status st = check_shape(shape);
+    if (st != KVMM_OK) return st;
+    const kvmm_shape& s = *shape;
+    if (W < 1 || n < 1 || n > W || head < 0 || head >= W || lag < 1 || lag >= n) return KVMM_INVALID_ARG;
+    if (n > 1024) return KVMM_UNSUPPORTED_SHAPE;  // the window's per-step values live in shared memory
+    if (!(unstable_frac >= 0.f && unstable_frac <= 1.f)) return KVMM_INVALID_ARG;
+    if (static_cast<size_t>(s.L) * s.Hkv > kvmm::stability_max_heads()) return KVMM_UNSUPPORTED_SHAPE;
+    if (!req4(hist_idx) || !req4(hist_cnt) || !req4(hist_pages) || !req4(rco_unit) || !opt4(stability) ||
+        !opt4(err))
+        return KVMM_INVALID_ARG;
+    kvmm::StabilityParams p{};
+    p.B = s.B;
+    p.L = s.L;
+    p.Hkv = s.Hkv;
+    p.T = s.T;
+    p.Pmax = s.Pmax;
+    p.Kmax = s.Kmax;
+    p.W = W;
+    p.n = n;
+    p.head = head;
+    p.lag = lag;
+    p.unstable_frac = unstable_frac;
+    p.hist_idx = const_cast<int32_t*>(hist_idx);
+    p.hist_cnt = const_cast<int32_t*>(hist_cnt);
+    p.hist_pages = const_cast<int32_t*>(hist_pages);
+    p.rco_unit = rco_unit;
+    p.stability = stability;
+    p.unstable = unstable;
+    p.err = err;
+    return launched(kvmm::launch_stability_rco(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"

@@ -185,10 +185,31 @@ cudaError_t allow_smem(Kernel kernel, size_t bytes, int& dev_cache, size_t& byte
 }
 
 // Launchers return cudaSuccess or the launch error.
+// topk_history_record / topk_stability_rco
+struct StabilityParams {
+    int B, L, Hkv, T, Pmax, Kmax;
+    int W, n, head, lag;  // ring size; steps used, slot of the newest, distance of compared steps
+    int layer, slot;      // recording: the layer and the ring slot it goes to
+    float unstable_frac;
+    const int32_t* sel_idx;
+    const int32_t* sel_cnt;
+    const int32_t* seq_len;
+    int32_t* hist_idx;    // [W][B][L][Hkv][Kmax]
+    int32_t* hist_cnt;    // [W][B][L][Hkv]
+    int32_t* hist_pages;  // [W][B]
+    float* rco_unit;      // [B][L][Hkv]
+    float* stability;     // [L][Hkv] or null
+    uint8_t* unstable;    // [L][Hkv] or null
+    int32_t* err;
+};
+
 cudaError_t launch_minmax_update(const UpdateParams& p, cudaStream_t stream);
 cudaError_t launch_score_topk(const ScoreParams& p, int group_reduce, cudaStream_t stream);
 cudaError_t launch_sparse_attention(const AttnParams& p, cudaStream_t stream);
 cudaError_t launch_promotion_diff(const DiffParams& p, cudaStream_t stream);
+cudaError_t launch_history_record(const StabilityParams& p, cudaStream_t stream);
+cudaError_t launch_stability_rco(const StabilityParams& p, cudaStream_t stream);
+size_t stability_max_heads();  // largest L * Hkv the classification handles
 cudaError_t launch_decode_layer(DecodeParams p, int group_reduce, cudaStream_t stream);
 size_t decode_layer_smem(int D, int T, int Pmax, int Kmax, int C);  // dynamic shared memory of one CTA
 int decode_layer_cluster(const kvmm_shape& s);                 // CTAs per cluster for a shape

@@ -21,7 +21,8 @@ NULL_BLOCK = -1
 
 EXPORTS = ("kv_minmax_update", "page_score_topk", "sparse_paged_decode_attn", "topk_promotion_diff",
            "kvmm_workspace_size", "kvmm_auto_splits", "kvmm_status_string", "kvmm_last_cuda_error",
-           "page_score_topk_static_scratch", "page_score_topk_attn", "decode_layer")
+           "page_score_topk_static_scratch", "page_score_topk_attn", "decode_layer", "topk_history_record",
+           "topk_stability_rco")
 
 
 class KvmmError(RuntimeError):
@@ -77,8 +78,11 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.page_score_topk_attn.argtypes = [SP, I32, P, P, P, P, P, P, P, I32, I32, F32, P, P, P, P, P, P, SZ, P, P]
     lib.decode_layer.argtypes = [SP, I32, P, P, P, I32, P, P, P, P, P, P, P, P, I32, I32, F32, P, P, P, P, P, P, SZ,
                                  P, P]
+    lib.topk_history_record.argtypes = [SP, I32, P, P, P, I32, I32, P, P, P, P, P]
+    lib.topk_stability_rco.argtypes = [SP, P, P, P, I32, I32, I32, I32, F32, P, P, P, P, P]
     for f in ("kv_minmax_update", "page_score_topk", "sparse_paged_decode_attn", "topk_promotion_diff",
-              "page_score_topk_static_scratch", "page_score_topk_attn", "decode_layer"):
+              "page_score_topk_static_scratch", "page_score_topk_attn", "decode_layer", "topk_history_record",
+              "topk_stability_rco"):
         getattr(lib, f).restype = ctypes.c_int
     lib.kvmm_workspace_size.argtypes = [SP, I32]
     lib.kvmm_workspace_size.restype = SZ
@@ -282,3 +286,34 @@ def topk_promotion_diff(shape: Shape, layer: int, rescore_mask, prev_idx, prev_c
             _dev(total_promoted, "total_promoted", torch.int32, 1, optional=True),
             _dev(err, "err", torch.int32, 1, optional=True), _stream(stream))
     _check("topk_promotion_diff", load().topk_promotion_diff(*args))
+
+
+def topk_history_record(shape: Shape, layer: int, sel_idx, sel_cnt, seq_len, slot: int, hist_idx, hist_cnt,
+                        hist_pages, err=None, stream=None) -> None:
+    """Store ``layer``'s selections in ring slot ``slot`` (hist_idx [W,B,L,Hkv,Kmax], hist_cnt [W,B,L,Hkv],
+    hist_pages [W,B], all int32; W is taken from hist_pages)."""
+    s = shape
+    units = s.B * s.L * s.Hkv
+    W = hist_pages.shape[0]
+    args = (ctypes.byref(s), layer, _dev(sel_idx, "sel_idx", torch.int32, units * s.Kmax),
+            _dev(sel_cnt, "sel_cnt", torch.int32, units), _dev(seq_len, "seq_len", torch.int32, s.B), W, slot,
+            _dev(hist_idx, "hist_idx", torch.int32, W * units * s.Kmax),
+            _dev(hist_cnt, "hist_cnt", torch.int32, W * units), _dev(hist_pages, "hist_pages", torch.int32, W * s.B),
+            _dev(err, "err", torch.int32, 1, optional=True), _stream(stream))
+    _check("topk_history_record", load().topk_history_record(*args))
+
+
+def topk_stability_rco(shape: Shape, hist_idx, hist_cnt, hist_pages, n: int, head: int, lag: int, rco_unit,
+                       stability=None, unstable=None, unstable_frac: float = 0.25, err=None, stream=None) -> None:
+    """Per-unit mean RCO of selections ``lag`` steps apart over the last ``n`` recorded steps (newest in slot
+    ``head``), the per-head stability and the unstable mask; see kvmm.h."""
+    s = shape
+    units = s.B * s.L * s.Hkv
+    W = hist_pages.shape[0]
+    args = (ctypes.byref(s), _dev(hist_idx, "hist_idx", torch.int32, W * units * s.Kmax),
+            _dev(hist_cnt, "hist_cnt", torch.int32, W * units), _dev(hist_pages, "hist_pages", torch.int32, W * s.B),
+            W, n, head, lag, float(unstable_frac), _dev(rco_unit, "rco_unit", torch.float32, units),
+            _dev(stability, "stability", torch.float32, s.L * s.Hkv, optional=True),
+            _dev(unstable, "unstable", torch.uint8, s.L * s.Hkv, optional=True),
+            _dev(err, "err", torch.int32, 1, optional=True), _stream(stream))
+    _check("topk_stability_rco", load().topk_stability_rco(*args))

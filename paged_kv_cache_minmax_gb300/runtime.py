@@ -118,3 +118,38 @@ class DecodeState:
 
     def read_err(self) -> int:
         return int(self.err.item())
+
+
+class StabilityProfiler:
+    """Offline profiling of head stability: a ring of the last W steps' selections of every (batch, layer,
+    KV head) and the Random-Corrected Overlap classification (FlexiCache, "Core insight: attention heads
+    differ in temporal stability").  ``record(state)`` stores one decode step of every layer; ``classify``
+    returns (rco per unit [B, L, Hkv], stability [L, Hkv], unstable mask [L, Hkv])."""
+
+    def __init__(self, shape, W: int, device="cuda"):
+        s = shape
+        i32 = dict(dtype=torch.int32, device=device)
+        self.shape, self.W = s, W
+        self.hist_idx = torch.zeros(W, s.B, s.L, s.Hkv, s.Kmax, **i32)
+        self.hist_cnt = torch.zeros(W, s.B, s.L, s.Hkv, **i32)
+        self.hist_pages = torch.zeros(W, s.B, **i32)
+        self.rco_unit = torch.zeros(s.B, s.L, s.Hkv, dtype=torch.float32, device=device)
+        self.stability = torch.zeros(s.L, s.Hkv, dtype=torch.float32, device=device)
+        self.unstable = torch.zeros(s.L, s.Hkv, dtype=torch.uint8, device=device)
+        self.err = torch.zeros(1, **i32)
+        self.steps = 0
+
+    def record(self, state, layers=None) -> None:
+        """Store this step's selections of ``layers`` (default: all) in slot steps mod W, then advance."""
+        slot = self.steps % self.W
+        for l in [-1] if layers is None else layers:  # -1: every layer in one launch
+            kvmm.topk_history_record(self.shape, l, state.sel_idx, state.sel_cnt, state.seq_len, slot,
+                                     self.hist_idx, self.hist_cnt, self.hist_pages, err=self.err)
+        self.steps += 1
+
+    def classify(self, lag: int = 1, unstable_frac: float = 0.25, n: int | None = None):
+        n = min(self.steps, self.W) if n is None else n
+        kvmm.topk_stability_rco(self.shape, self.hist_idx, self.hist_cnt, self.hist_pages, n,
+                                (self.steps - 1) % self.W, lag, self.rco_unit, self.stability, self.unstable,
+                                unstable_frac, err=self.err)
+        return self.rco_unit, self.stability, self.unstable

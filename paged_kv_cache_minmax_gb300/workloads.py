@@ -230,6 +230,29 @@ def drift_queries(wl: Workload, steps: int) -> torch.Tensor:
     return out
 
 
+def drift_queries_by_stability(wl: Workload, steps: int, keep_stable: float = 0.99,
+                               keep_unstable: float = 0.3) -> torch.Tensor:
+    """Queries ``[steps, L_alloc, B, Hq, D]`` (bf16) whose drift depends on the seeded stable/unstable split:
+    q_t = a q_{t-1} + sqrt(1 - a^2) eps_t (fp32; same stationary scale), with a = keep_unstable for the query
+    heads of an unstable (layer, KV head) and keep_stable otherwise.  q_0 is the workload's q."""
+    cfg = wl.cfg
+    device = wl.q.device
+    gen = torch.Generator(device=device)
+    gen.manual_seed(cfg.seed * 7 + 5)
+    unst = wl.unstable.bool().repeat_interleave(cfg.G, dim=1)  # [L_alloc, Hq]
+    a = torch.where(unst, torch.tensor(keep_unstable, device=device), torch.tensor(keep_stable, device=device))
+    a = a[:, None, :, None]  # [L, 1, Hq, 1]
+    out = torch.empty((steps,) + tuple(wl.q.shape), dtype=torch.bfloat16, device=device)
+    state = wl.q.float()
+    scale = state.std()
+    for t in range(steps):
+        if t > 0:
+            eps = torch.randn(state.shape, generator=gen, device=device) * scale
+            state = a * state + torch.sqrt(1 - a * a) * eps
+        out[t] = state.to(torch.bfloat16)
+    return out
+
+
 def bf16_bits(t: torch.Tensor):
     """Raw bf16 bit patterns of a (CPU or CUDA) tensor as a numpy uint16 array."""
     import numpy as np

@@ -94,6 +94,19 @@ def test_validation_rejects_before_any_launch(lib):
     # diff: missing promoted list
     assert lib.topk_promotion_diff(ctypes.byref(s), 0, None, fake, fake, fake, fake, 1, None, fake, None, None,
                                    None, None, None) == kvmm.INVALID_ARG
+    # history record: slot outside the ring, missing history
+    assert lib.topk_history_record(ctypes.byref(s), 0, fake, fake, fake, 4, 4, fake, fake, fake, None,
+                                   None) == kvmm.INVALID_ARG
+    assert lib.topk_history_record(ctypes.byref(s), 0, fake, fake, fake, 4, 0, None, fake, fake, None,
+                                   None) == kvmm.INVALID_ARG
+    # stability: lag must be below the window, the window inside the ring, the fraction in [0, 1]
+    ok = (fake, fake, fake, 8, 8, 7, 1)
+    assert lib.topk_stability_rco(ctypes.byref(s), *ok[:6], 8, 0.25, fake, None, None, None,
+                                  None) == kvmm.INVALID_ARG
+    assert lib.topk_stability_rco(ctypes.byref(s), *ok[:4], 9, 7, 1, 0.25, fake, None, None, None,
+                                  None) == kvmm.INVALID_ARG
+    assert lib.topk_stability_rco(ctypes.byref(s), *ok, 1.5, fake, None, None, None, None) == kvmm.INVALID_ARG
+    assert lib.topk_stability_rco(ctypes.byref(s), *ok, 0.25, None, None, None, None, None) == kvmm.INVALID_ARG
 
 
 def test_binding_fails_loudly_without_library(tmp_path):
