@@ -551,6 +551,80 @@ def stability_arm(args):
         "device_err": int(prof.err.item())}), flush=True)
 
 
+def promote_arm(args):
+    """Promotion transfer at the 8B-32K shape, one layer: every unit (64) brings 38 pages (30% of its top-128,
+    within the 23-35% the FlexiCache summary reports per rerank) from a pinned host store into the blocks of
+    38 evicted pages.  Calls alternate between two selections so that every call moves the same pages; each
+    pair of calls is one CUDA graph replay.  Reported per grid bound: GB/s of K/V moved over the host link."""
+    from paged_kv_cache_minmax_gb300 import build as kbuild
+    from paged_kv_cache_minmax_gb300 import kvmm
+
+    kbuild.build_library()
+    kvmm.load()
+    cfg = CFG
+    B, Hkv, T, D, Pmax, K = cfg.B, cfg.Hkv, cfg.T, cfg.D, cfg.Pmax, cfg.K
+    n_move = 38
+    units = B * Hkv
+    gen = torch.Generator()
+    gen.manual_seed(cfg.seed + 23)
+    host_k = torch.empty(B, 1, Hkv, Pmax, T, D, dtype=torch.bfloat16).pin_memory()
+    host_v = torch.empty(B, 1, Hkv, Pmax, D, T, dtype=torch.bfloat16).pin_memory()
+    host_k.view(torch.int16).random_(generator=gen)
+    host_v.view(torch.int16).random_(generator=gen)
+    n_phys = units * K
+    shape = kvmm.make_shape(B, 1, cfg.Hq, Hkv, D, T, Pmax, K, n_phys)
+    k_pool = torch.zeros(n_phys, T, D, dtype=torch.bfloat16, device="cuda")
+    v_pool = torch.zeros(n_phys, D, T, dtype=torch.bfloat16, device="cuda")
+    # selection A: pages [0, K); selection B: the same with the first n_move replaced by [K, K + n_move)
+    bt = torch.full((B, 1, Hkv, Pmax), -1, dtype=torch.int32)
+    bt[..., :K] = torch.arange(n_phys, dtype=torch.int32).view(B, 1, Hkv, K)
+    bt = bt.cuda()
+    ab = torch.arange(K, K + n_move, dtype=torch.int32).expand(B, 1, Hkv, n_move)
+    ba = torch.arange(0, n_move, dtype=torch.int32).expand(B, 1, Hkv, n_move)
+    lists = {}
+    for name, t in (("ab", ab), ("ba", ba)):
+        full = torch.zeros(B, 1, Hkv, K, dtype=torch.int32)
+        full[..., :n_move] = t
+        lists[name] = full.cuda()
+    cnt = torch.full((B, 1, Hkv), n_move, dtype=torch.int32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    moved = torch.zeros(B, 1, Hkv, dtype=torch.int32, device="cuda")
+    bytes_per_call = units * n_move * 2 * T * D * 2
+    stream = torch.cuda.Stream()
+    results = {}
+    for ctas in (4, 8, 16, 32, 64, 152):
+        def pair():
+            kvmm.promote_pages(shape, 0, None, lists["ab"], cnt, lists["ba"], cnt, host_k, host_v, k_pool, v_pool,
+                               bt, moved=moved, max_ctas=ctas, err=err)
+            kvmm.promote_pages(shape, 0, None, lists["ba"], cnt, lists["ab"], cnt, host_k, host_v, k_pool, v_pool,
+                               bt, moved=moved, max_ctas=ctas, err=err)
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                pair()
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            pair()
+        reps = max(10, min(args.steps, 100))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            g.replay()
+            e0.record()
+            for _ in range(reps):
+                g.replay()
+            e1.record()
+        stream.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / (2 * reps)
+        results[str(ctas)] = {"us_per_call": us, "gbs": bytes_per_call / (us * 1e-6) / 1e9}
+    ok = int(err.item()) == 0 and int(moved.min()) == n_move
+    print(json.dumps({
+        "metric": "promotion transfer: K/V moved from pinned host memory into recycled blocks", "unit": "GB/s",
+        "higher_is_better": True, "bytes_per_call": bytes_per_call, "by_max_ctas": results,
+        "config": {"workload": cfg.name, "units": units, "pages_per_unit": n_move, "top_k": K,
+                   "page_bytes_kv": 2 * T * D * 2, "host_store": "pinned (cudaHostAlloc through torch)"},
+        "device_err": int(err.item()), "all_moved": ok}), flush=True)
+
+
 def load_traffic(kernel):
     """dram bytes per launch of ``kernel`` from the committed ncu summary, if current."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
@@ -571,6 +645,8 @@ def main():
     ap.add_argument("--no-graph", action="store_true", help="launch eagerly (for profilers)")
     ap.add_argument("--batch", type=int, default=0, help="override the batch (smaller profiling case)")
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (smaller profiling case)")
+    ap.add_argument("--promote", action="store_true",
+                    help="time the promotion transfer from pinned host memory instead")
     ap.add_argument("--stability", action="store_true",
                     help="time head-stability profiling (history record, RCO and classification) instead")
     ap.add_argument("--path", default="decode_layer", choices=["decode_layer", "fused", "unfused"],
@@ -582,6 +658,8 @@ def main():
         reference_arm(args)
     elif args.stability:
         stability_arm(args)
+    elif args.promote:
+        promote_arm(args)
     else:
         gpu_arm(args)
 

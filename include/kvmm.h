@@ -311,6 +311,47 @@ kvmm_status decode_layer(const kvmm_shape* shape, int32_t layer, const kvmm_bf16
                          float* lse, void* workspace, size_t workspace_bytes, int32_t* err, kvmm_stream stream);
 
 /* ------------------------------------------------------------------------
+ * promote_pages -- after a rerank, bring each rescored unit's promoted pages
+ * from the host KV store into the GPU pools, in the physical blocks its
+ * evicted pages free, and rewrite the block table.
+ *
+ * FlexiCache, "Core method, 3. Periodic reranking and incremental
+ * promotion" (only the promoted pages are transferred), "Core method, 4.
+ * Overlapping transfer and compute" (a UVA kernel reads the pinned host KV
+ * directly, with a bounded grid, so that it leaves the SMs to decoding) and
+ * "System design, head-level block table" (physical block reuse: evicted
+ * pages' blocks go to promoted pages; evicted entries keep their place and
+ * point at the null block).
+ *
+ * For every unit of `layer` with rescore_mask set (NULL = all), promoted
+ * [0..np) and evicted [0..ne) ascending (as topk_promotion_diff writes
+ * them, same layouts as sel_idx / sel_cnt), m = min(np, ne):
+ *   - i < m: phys = block_table[evicted[i]]; block_table[evicted[i]] = -1;
+ *     block_table[promoted[i]] = phys; logical page promoted[i] of the host
+ *     store is copied into pool page phys;
+ *   - i >= m of evicted: block_table[evicted[i]] = -1, and its block is
+ *     returned in freed[i - m] (when given; -1 if the entry was skipped),
+ *     freed_cnt = ne - m;
+ *   - i >= m of promoted: no block is free; the entry is left as it was.
+ * moved [B][L][Hkv] (may be NULL) receives m minus the skipped pairs.
+ * host_k / host_v: [B][L][Hkv][Pmax][T][D] / [B][L][Hkv][Pmax][D][T] bf16
+ * (each logical page laid out as a pool page), in host memory the device
+ * can address: pinned, or pageable where the device reads pageable host
+ * memory (a coherent host link).  freed [B][L][Hkv][Kmax] and freed_cnt
+ * [B][L][Hkv] may be NULL.  max_ctas bounds the grid (0: 16).
+ * An evicted entry that is null or outside the pool sets
+ * KVMM_ERR_NULL_BLOCK / KVMM_ERR_OUT_OF_RANGE and its pair moves nothing;
+ * pages outside [0, Pmax) or counts outside [0, Kmax] set
+ * KVMM_ERR_OUT_OF_RANGE.  Decode of the same units must not run
+ * concurrently (stream order suffices).
+ */
+kvmm_status promote_pages(const kvmm_shape* shape, int32_t layer, const uint8_t* rescore_mask,
+                          const int32_t* promoted, const int32_t* promoted_cnt, const int32_t* evicted,
+                          const int32_t* evicted_cnt, const kvmm_bf16* host_k, const kvmm_bf16* host_v,
+                          kvmm_bf16* k_pool, kvmm_bf16* v_pool, int32_t* block_table, int32_t* moved,
+                          int32_t* freed, int32_t* freed_cnt, int32_t max_ctas, int32_t* err, kvmm_stream stream);
+
+/* ------------------------------------------------------------------------
  * Temporal stability of each (layer, KV head): offline profiling that
  * classifies heads as stable or unstable.
  *

@@ -67,6 +67,8 @@ def _load():
         lib.oracle_unit_sparse_attention.restype = I32
         lib.oracle_unit_dense_attention.argtypes = [P, I32, I32, I32, P, P, I64, P, I32, D, P, P]
         lib.oracle_unit_dense_attention.restype = I32
+        lib.oracle_unit_promote.argtypes = [P, I32, I64, P, I32, P, I32, P, P, P, P, I32, I32, P, P]
+        lib.oracle_unit_promote.restype = I32
         lib.oracle_rco.argtypes = [P, I32, P, I32, I32]
         lib.oracle_rco.restype = D
         lib.oracle_unit_stability.argtypes = [P, P, P, I32, I32, I32]
@@ -149,6 +151,22 @@ def set_difference(a, b) -> np.ndarray:
     out = np.zeros(max(len(a), 1), dtype=np.int32)
     n = _load().oracle_set_difference(_ptr(a), len(a), _ptr(b), len(b), _ptr(out))
     return out[:n].copy()
+
+
+def unit_promote(bt_row, n_phys, promoted, evicted, host_k, host_v, k_pool, v_pool, T):
+    """Promotion of one unit in place: bt_row (int32 [Pmax]) and the pools (uint16 bf16 bits [n_phys, T*D]) are
+    updated from the unit's host pages (uint16 [Pmax, T*D]).  Returns (err, moved, freed)."""
+    bt = np.ascontiguousarray(bt_row, dtype=np.int32)
+    assert bt_row.flags["C_CONTIGUOUS"] and bt_row.dtype == np.int32 and bt.ctypes.data == bt_row.ctypes.data
+    pr, ev = _i32(promoted), _i32(evicted)
+    D = host_k.shape[-1] // T
+    freed = np.zeros(max(len(ev), 1), dtype=np.int32)
+    moved = np.zeros(1, dtype=np.int32)
+    err = _load().oracle_unit_promote(_ptr(bt), len(bt), int(n_phys), _ptr(pr), len(pr), _ptr(ev), len(ev),
+                                      _ptr(_u16(host_k)), _ptr(_u16(host_v)), _ptr(k_pool), _ptr(v_pool), T, D,
+                                      _ptr(freed), _ptr(moved))
+    m = min(len(pr), len(ev))
+    return int(err), int(moved[0]), freed[:max(0, len(ev) - m)].copy()
 
 
 def rco(a, b, P) -> float:

@@ -22,6 +22,9 @@
  *     - "System design, head-level block table": the block table is
  *       [batch, layer, head, logical_block]; evicted slots point at a null
  *       block that is never dereferenced.
+ *     - "Core method, 4" and "System design" (physical block reuse): after a
+ *       rerank the promoted pages are brought from the host KV into the
+ *       physical blocks of the evicted pages.
  *     - "Core method, 1. Stability-differentiated placement": decode
  *       attention runs over the top-K pages only.
  *     - "Core insight: attention heads differ in temporal stability": the
@@ -46,6 +49,10 @@
  *     result is a unique bf16 bit pattern;
  *   - attention scale defaults to D^-1/2; output and log-sum-exp in double;
  *     a unit with no valid token yields output 0 and lse = -inf.
+ *   - promotion pairs promoted[i] with evicted[i] (both ascending) for
+ *     i < min(np, ne): the evicted page's block goes to the promoted page,
+ *     the evicted entry becomes the null block; surplus evicted blocks are
+ *     freed in order, surplus promoted pages stay unplaced;
  *   - RCO(A, B) = (|A n B| - |A||B|/P) / (min(|A|,|B|) - |A||B|/P): the
  *     overlap minus that of random subsets of the same sizes among P pages,
  *     over its largest possible value (evaluated as the ratio of the exact
@@ -445,4 +452,59 @@ void oracle_classify(const double* stability, int32_t n, double frac, uint8_t* u
             if (stability[j] < stability[i] || (stability[j] == stability[i] && j < i)) ++rank;
         unstable[i] = rank < k ? 1 : 0;
     }
+}
+
+/* ------------------------------------------------------------------------
+ * Promotion of one unit (FlexiCache, "Core method, 3" / "Core method, 4" /
+ * "System design, head-level block table"): the pairs i < m = min(np, ne)
+ * move the block of evicted[i] to promoted[i] and copy the host store's page
+ * promoted[i] (keys [T][D] and values [D][T], host_k/host_v hold the unit's
+ * Pmax pages) into it; evicted entries become -1; the blocks of evicted[i],
+ * i >= m, are returned in freed[i - m] (-1 for a skipped entry).  A pair
+ * whose evicted entry is null / out of range, or whose pages lie outside
+ * [0, Pmax), moves nothing and sets its error bit.  Returns the error bits;
+ * *moved receives the pages moved.
+ */
+int32_t oracle_unit_promote(int32_t* bt_row, int32_t Pmax, int64_t n_phys, const int32_t* promoted, int32_t np,
+                            const int32_t* evicted, int32_t ne, const uint16_t* host_k, const uint16_t* host_v,
+                            uint16_t* k_pool, uint16_t* v_pool, int32_t T, int32_t D, int32_t* freed,
+                            int32_t* moved)
+{
+    int32_t err = 0;
+    const int32_t m = np < ne ? np : ne;
+    const int64_t page = (int64_t)T * D;
+    int64_t* block = (int64_t*)malloc(sizeof(int64_t) * (size_t)(ne > 0 ? ne : 1));
+    /* the evicted entries: read their blocks, then null them */
+    for (int32_t i = 0; i < ne; ++i) {
+        block[i] = -1;
+        if (evicted[i] < 0 || evicted[i] >= Pmax) {
+            err |= ORACLE_ERR_OUT_OF_RANGE;
+            continue;
+        }
+        const int32_t ph = bt_row[evicted[i]];
+        if (ph < 0)
+            err |= ORACLE_ERR_NULL_BLOCK;
+        else if (ph >= n_phys)
+            err |= ORACLE_ERR_OUT_OF_RANGE;
+        else
+            block[i] = ph;
+        bt_row[evicted[i]] = -1;
+    }
+    int32_t n = 0;
+    for (int32_t i = 0; i < m; ++i) {
+        if (promoted[i] < 0 || promoted[i] >= Pmax) {
+            err |= ORACLE_ERR_OUT_OF_RANGE;
+            continue;
+        }
+        if (block[i] < 0) continue;
+        bt_row[promoted[i]] = (int32_t)block[i];
+        memcpy(k_pool + block[i] * page, host_k + (int64_t)promoted[i] * page, sizeof(uint16_t) * (size_t)page);
+        memcpy(v_pool + block[i] * page, host_v + (int64_t)promoted[i] * page, sizeof(uint16_t) * (size_t)page);
+        ++n;
+    }
+    for (int32_t i = m; i < ne; ++i)
+        if (freed) freed[i - m] = (int32_t)block[i];
+    free(block);
+    *moved = n;
+    return err;
 }

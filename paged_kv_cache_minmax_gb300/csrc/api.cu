@@ -22,6 +22,26 @@ bool opt(const void* p) { return p == nullptr || aligned(p, 16); }
 bool req4(const void* p) { return p != nullptr && aligned(p, 4); }
 bool opt4(const void* p) { return p == nullptr || aligned(p, 4); }
 
+// The device address of host memory the device can read (the same address under unified addressing),
+// or null: pinned or managed memory, or pageable memory where the device reads pageable host memory.
+const void* device_view_of_host(const void* h)
+{
+    cudaPointerAttributes a{};
+    if (cudaPointerGetAttributes(&a, h) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    if (a.type == cudaMemoryTypeHost || a.type == cudaMemoryTypeManaged || a.type == cudaMemoryTypeDevice)
+        return a.devicePointer != nullptr ? a.devicePointer : h;
+    int dev = 0, pageable = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&pageable, cudaDevAttrPageableMemoryAccess, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    return pageable ? h : nullptr;
+}
+
 kvmm_status check_shape(const kvmm_shape* s)
 {
     if (s == nullptr) return KVMM_INVALID_ARG;
@@ -468,6 +488,50 @@ kvmm_status topk_promotion_diff(const kvmm_shape* shape, int32_t layer,
     p.total_promoted = total_promoted;
     p.err = err;
     return launched(kvmm::launch_promotion_diff(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+kvmm_status promote_pages(const kvmm_shape* shape, int32_t layer, const uint8_t* rescore_mask,
+                          const int32_t* promoted, const int32_t* promoted_cnt, const int32_t* evicted,
+                          const int32_t* evicted_cnt, const kvmm_bf16* host_k, const kvmm_bf16* host_v,
+                          kvmm_bf16* k_pool, kvmm_bf16* v_pool, int32_t* block_table, int32_t* moved,
+                          int32_t* freed, int32_t* freed_cnt, int32_t max_ctas, int32_t* err, kvmm_stream stream)
+{
+    kvmm_status st = check_shape(shape);
+    if (st != KVMM_OK) return st;
+    const kvmm_shape& s = *shape;
+    if (layer < 0 || layer >= s.L || max_ctas < 0) return KVMM_INVALID_ARG;
+    if (!req4(promoted) || !req4(promoted_cnt) || !req4(evicted) || !req4(evicted_cnt) || !req(host_k) ||
+        !req(host_v) || !req(k_pool) || !req(v_pool) || !req4(block_table) || !opt4(moved) || !opt4(freed) ||
+        !opt4(freed_cnt) || !opt4(err))
+        return KVMM_INVALID_ARG;
+    const void* hk = device_view_of_host(host_k);
+    const void* hv = device_view_of_host(host_v);
+    if (hk == nullptr || hv == nullptr) return KVMM_INVALID_ARG;  // host memory the device cannot read
+    kvmm::PromoteParams p{};
+    p.B = s.B;
+    p.L = s.L;
+    p.Hkv = s.Hkv;
+    p.T = s.T;
+    p.D = s.D;
+    p.Pmax = s.Pmax;
+    p.Kmax = s.Kmax;
+    p.layer = layer;
+    p.n_phys = s.n_phys;
+    p.rescore_mask = rescore_mask;
+    p.promoted = promoted;
+    p.promoted_cnt = promoted_cnt;
+    p.evicted = evicted;
+    p.evicted_cnt = evicted_cnt;
+    p.host_k = static_cast<const kvmm_bf16*>(hk);
+    p.host_v = static_cast<const kvmm_bf16*>(hv);
+    p.k_pool = k_pool;
+    p.v_pool = v_pool;
+    p.block_table = block_table;
+    p.moved = moved;
+    p.freed = freed;
+    p.freed_cnt = freed_cnt;
+    p.err = err;
+    return launched(kvmm::launch_promote(p, max_ctas, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 kvmm_status topk_history_record(const kvmm_shape* shape, int32_t layer, const int32_t* sel_idx,

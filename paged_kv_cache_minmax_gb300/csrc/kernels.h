@@ -185,6 +185,26 @@ cudaError_t allow_smem(Kernel kernel, size_t bytes, int& dev_cache, size_t& byte
 }
 
 // Launchers return cudaSuccess or the launch error.
+// promote_pages
+struct PromoteParams {
+    int B, L, Hkv, T, D, Pmax, Kmax, layer;
+    int64_t n_phys;
+    const uint8_t* rescore_mask;
+    const int32_t* promoted;
+    const int32_t* promoted_cnt;
+    const int32_t* evicted;
+    const int32_t* evicted_cnt;
+    const kvmm_bf16* host_k;  // device-addressable host memory
+    const kvmm_bf16* host_v;
+    kvmm_bf16* k_pool;
+    kvmm_bf16* v_pool;
+    int32_t* block_table;
+    int32_t* moved;
+    int32_t* freed;
+    int32_t* freed_cnt;
+    int32_t* err;
+};
+
 // topk_history_record / topk_stability_rco
 struct StabilityParams {
     int B, L, Hkv, T, Pmax, Kmax;
@@ -207,6 +227,7 @@ cudaError_t launch_minmax_update(const UpdateParams& p, cudaStream_t stream);
 cudaError_t launch_score_topk(const ScoreParams& p, int group_reduce, cudaStream_t stream);
 cudaError_t launch_sparse_attention(const AttnParams& p, cudaStream_t stream);
 cudaError_t launch_promotion_diff(const DiffParams& p, cudaStream_t stream);
+cudaError_t launch_promote(const PromoteParams& p, int max_ctas, cudaStream_t stream);
 cudaError_t launch_history_record(const StabilityParams& p, cudaStream_t stream);
 cudaError_t launch_stability_rco(const StabilityParams& p, cudaStream_t stream);
 size_t stability_max_heads();  // largest L * Hkv the classification handles

@@ -22,7 +22,7 @@ NULL_BLOCK = -1
 EXPORTS = ("kv_minmax_update", "page_score_topk", "sparse_paged_decode_attn", "topk_promotion_diff",
            "kvmm_workspace_size", "kvmm_auto_splits", "kvmm_status_string", "kvmm_last_cuda_error",
            "page_score_topk_static_scratch", "page_score_topk_attn", "decode_layer", "topk_history_record",
-           "topk_stability_rco")
+           "topk_stability_rco", "promote_pages")
 
 
 class KvmmError(RuntimeError):
@@ -80,9 +80,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
                                  P, P]
     lib.topk_history_record.argtypes = [SP, I32, P, P, P, I32, I32, P, P, P, P, P]
     lib.topk_stability_rco.argtypes = [SP, P, P, P, I32, I32, I32, I32, F32, P, P, P, P, P]
+    lib.promote_pages.argtypes = [SP, I32, P, P, P, P, P, P, P, P, P, P, P, P, P, I32, P, P]
     for f in ("kv_minmax_update", "page_score_topk", "sparse_paged_decode_attn", "topk_promotion_diff",
               "page_score_topk_static_scratch", "page_score_topk_attn", "decode_layer", "topk_history_record",
-              "topk_stability_rco"):
+              "topk_stability_rco", "promote_pages"):
         getattr(lib, f).restype = ctypes.c_int
     lib.kvmm_workspace_size.argtypes = [SP, I32]
     lib.kvmm_workspace_size.restype = SZ
@@ -317,3 +318,37 @@ def topk_stability_rco(shape: Shape, hist_idx, hist_cnt, hist_pages, n: int, hea
             _dev(unstable, "unstable", torch.uint8, s.L * s.Hkv, optional=True),
             _dev(err, "err", torch.int32, 1, optional=True), _stream(stream))
     _check("topk_stability_rco", load().topk_stability_rco(*args))
+
+
+def _host(t: torch.Tensor, name: str, numel: int):
+    """A host-side bf16 store (pinned, or pageable where the device reads pageable memory)."""
+    if t.is_cuda:
+        raise ValueError(f"{name} must be a host tensor")
+    if t.dtype != torch.bfloat16 or not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous bfloat16")
+    if t.numel() < numel:
+        raise ValueError(f"{name} has {t.numel()} elements, needs {numel}")
+    return t.data_ptr()
+
+
+def promote_pages(shape: Shape, layer: int, rescore_mask, promoted, promoted_cnt, evicted, evicted_cnt, host_k,
+                  host_v, k_pool, v_pool, block_table, moved=None, freed=None, freed_cnt=None, max_ctas: int = 0,
+                  err=None, stream=None) -> None:
+    """Promoted pages from the host store (host_k [B,L,Hkv,Pmax,T,D], host_v [B,L,Hkv,Pmax,D,T], bf16) into the
+    blocks of evicted pages, and the table rewrite; see kvmm.h."""
+    s = shape
+    units = s.B * s.L * s.Hkv
+    page = s.T * s.D
+    args = (ctypes.byref(s), layer, _dev(rescore_mask, "rescore_mask", torch.uint8, s.L * s.Hkv, optional=True),
+            _dev(promoted, "promoted", torch.int32, units * s.Kmax),
+            _dev(promoted_cnt, "promoted_cnt", torch.int32, units),
+            _dev(evicted, "evicted", torch.int32, units * s.Kmax), _dev(evicted_cnt, "evicted_cnt", torch.int32, units),
+            _host(host_k, "host_k", units * s.Pmax * page), _host(host_v, "host_v", units * s.Pmax * page),
+            _dev(k_pool, "k_pool", torch.bfloat16, s.n_phys * page), _dev(v_pool, "v_pool", torch.bfloat16, s.n_phys * page),
+            _dev(block_table, "block_table", torch.int32, units * s.Pmax),
+            _dev(moved, "moved", torch.int32, units, optional=True),
+            _dev(freed, "freed", torch.int32, units * s.Kmax, optional=True),
+            _dev(freed_cnt, "freed_cnt", torch.int32, units, optional=True), int(max_ctas),
+            _dev(err, "err", torch.int32, 1, optional=True), _stream(stream))
+    _check("promote_pages", load().promote_pages(*args))
+

@@ -94,6 +94,13 @@ def test_validation_rejects_before_any_launch(lib):
     # diff: missing promoted list
     assert lib.topk_promotion_diff(ctypes.byref(s), 0, None, fake, fake, fake, fake, 1, None, fake, None, None,
                                    None, None, None) == kvmm.INVALID_ARG
+    # promotion: missing host store, negative grid bound
+    pa = (None, fake, fake, fake, fake, fake, fake, fake, fake, fake, None, None, None)
+    assert lib.promote_pages(ctypes.byref(s), 0, *pa, 0, None, None) == kvmm.INVALID_ARG
+    assert lib.promote_pages(ctypes.byref(s), 0, None, fake, fake, fake, fake, None, fake, fake, fake, fake, None,
+                             None, None, 0, None, None) == kvmm.INVALID_ARG
+    assert lib.promote_pages(ctypes.byref(s), 0, None, fake, fake, fake, fake, fake, fake, fake, fake, fake, None,
+                             None, None, -1, None, None) == kvmm.INVALID_ARG
     # history record: slot outside the ring, missing history
     assert lib.topk_history_record(ctypes.byref(s), 0, fake, fake, fake, 4, 4, fake, fake, fake, None,
                                    None) == kvmm.INVALID_ARG
