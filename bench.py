@@ -625,6 +625,63 @@ def promote_arm(args):
         "device_err": int(err.item()), "all_moved": ok}), flush=True)
 
 
+def table_update_arm(args):
+    """Dirty-tracked block-table synchronisation at the 8B-32K shape: one rerank of every unit of every layer
+    changes 76 entries per unit (38 promoted pages take blocks, 38 evicted pages become null), 155,648 entries
+    of the 4 Mi-entry table.  Timed: block_table_update reading those entries from pinned host memory, against
+    copying the whole table from pinned host memory; each as a CUDA graph replay."""
+    from paged_kv_cache_minmax_gb300 import build as kbuild
+    from paged_kv_cache_minmax_gb300 import kvmm
+
+    kbuild.build_library()
+    kvmm.load()
+    cfg = CFG
+    B, L, Hkv, Pmax = cfg.B, cfg.L, cfg.Hkv, cfg.Pmax
+    units = B * L * Hkv
+    n_phys = units * cfg.K
+    shape = kvmm.make_shape(B, L, cfg.Hq, Hkv, cfg.D, cfg.T, Pmax, cfg.K, n_phys)
+    gen = torch.Generator()
+    gen.manual_seed(cfg.seed + 29)
+    table = torch.full((B, L, Hkv, Pmax), -1, dtype=torch.int32, device="cuda")
+    host_table = torch.empty(B, L, Hkv, Pmax, dtype=torch.int32).pin_memory()
+    host_table.copy_(table.cpu())
+    per_unit = 76
+    cols = torch.stack([torch.randperm(Pmax, generator=gen)[:per_unit] for _ in range(units)])  # [units, 76]
+    idx = (torch.arange(units, dtype=torch.int64)[:, None] * Pmax + cols).reshape(-1).contiguous().pin_memory()
+    val = torch.randint(-1, n_phys, (idx.numel(),), generator=gen, dtype=torch.int32).pin_memory()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.Stream()
+
+    def timed(fn, reps):
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                fn()
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            g.replay()
+            e0.record()
+            for _ in range(reps):
+                g.replay()
+            e1.record()
+        stream.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / reps
+
+    reps = max(10, min(args.steps, 200))
+    delta_us = timed(lambda: kvmm.block_table_update(shape, idx, val, table, err=err), reps)
+    full_us = timed(lambda: table.copy_(host_table, non_blocking=True), reps)
+    print(json.dumps({
+        "metric": "block-table synchronisation per rerank step: changed entries vs the whole table", "unit": "us",
+        "higher_is_better": False, "delta_us": delta_us, "full_table_copy_us": full_us,
+        "delta_bytes": idx.numel() * 12, "table_bytes": table.numel() * 4, "changed_entries": idx.numel(),
+        "config": {"workload": cfg.name, "units": units, "changed_per_unit": per_unit,
+                   "deltas": "pinned host memory, read by the kernel"},
+        "device_err": int(err.item())}), flush=True)
+
+
 def load_traffic(kernel):
     """dram bytes per launch of ``kernel`` from the committed ncu summary, if current."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
@@ -645,6 +702,8 @@ def main():
     ap.add_argument("--no-graph", action="store_true", help="launch eagerly (for profilers)")
     ap.add_argument("--batch", type=int, default=0, help="override the batch (smaller profiling case)")
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (smaller profiling case)")
+    ap.add_argument("--table-update", action="store_true",
+                    help="time dirty-tracked block-table synchronisation instead")
     ap.add_argument("--promote", action="store_true",
                     help="time the promotion transfer from pinned host memory instead")
     ap.add_argument("--stability", action="store_true",
@@ -660,6 +719,8 @@ def main():
         stability_arm(args)
     elif args.promote:
         promote_arm(args)
+    elif args.table_update:
+        table_update_arm(args)
     else:
         gpu_arm(args)
 

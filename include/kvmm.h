@@ -311,6 +311,25 @@ kvmm_status decode_layer(const kvmm_shape* shape, int32_t layer, const kvmm_bf16
                          float* lse, void* workspace, size_t workspace_bytes, int32_t* err, kvmm_stream stream);
 
 /* ------------------------------------------------------------------------
+ * block_table_update -- apply the changed entries of the head-level block
+ * table: block_table[idx[i]] = val[i], i = 0 .. n-1.
+ *
+ * FlexiCache, "System design, head-level block table": with dirty tracking
+ * only the changed regions of the [batch, layer, head, logical_block] table
+ * are synchronised, not the whole four-dimensional table every step.  Here
+ * the changed entries themselves are the delta: idx (int64 flat indices into
+ * [B][L][Hkv][Pmax]) and val (a physical block, or -1 for the null block)
+ * may live in device memory or in host memory the device can read (a pinned
+ * staging buffer filled by the host scheduler), so only those 12 bytes per
+ * entry cross the host link.  Indices must be distinct (a dirty set); with
+ * repeats the entry takes one of the values.  An index outside the table or
+ * a value outside [-1, n_phys) sets KVMM_ERR_OUT_OF_RANGE and that update is
+ * skipped.  n = 0 launches nothing.
+ */
+kvmm_status block_table_update(const kvmm_shape* shape, const int64_t* idx, const int32_t* val, int32_t n,
+                               int32_t* block_table, int32_t* err, kvmm_stream stream);
+
+/* ------------------------------------------------------------------------
  * promote_pages -- after a rerank, bring each rescored unit's promoted pages
  * from the host KV store into the GPU pools, in the physical blocks its
  * evicted pages free, and rewrite the block table.

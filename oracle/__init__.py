@@ -69,6 +69,8 @@ def _load():
         lib.oracle_unit_dense_attention.restype = I32
         lib.oracle_unit_promote.argtypes = [P, I32, I64, P, I32, P, I32, P, P, P, P, I32, I32, P, P]
         lib.oracle_unit_promote.restype = I32
+        lib.oracle_table_update.argtypes = [P, I64, I64, P, P, I64]
+        lib.oracle_table_update.restype = I32
         lib.oracle_rco.argtypes = [P, I32, P, I32, I32]
         lib.oracle_rco.restype = D
         lib.oracle_unit_stability.argtypes = [P, P, P, I32, I32, I32]
@@ -167,6 +169,14 @@ def unit_promote(bt_row, n_phys, promoted, evicted, host_k, host_v, k_pool, v_po
                                       _ptr(freed), _ptr(moved))
     m = min(len(pr), len(ev))
     return int(err), int(moved[0]), freed[:max(0, len(ev) - m)].copy()
+
+
+def table_update(table, n_phys, idx, val) -> int:
+    """table (int32, C-contiguous, updated in place).flat[idx[i]] = val[i] in order; returns the error bits."""
+    assert table.dtype == np.int32 and table.flags["C_CONTIGUOUS"]
+    idx = np.ascontiguousarray(idx, dtype=np.int64)
+    val = _i32(val)
+    return int(_load().oracle_table_update(_ptr(table), table.size, int(n_phys), _ptr(idx), _ptr(val), len(idx)))
 
 
 def rco(a, b, P) -> float:

@@ -508,3 +508,21 @@ int32_t oracle_unit_promote(int32_t* bt_row, int32_t Pmax, int64_t n_phys, const
     *moved = n;
     return err;
 }
+
+/* Changed entries of a block table (FlexiCache, "System design, head-level
+ * block table": dirty tracking synchronises only what changed):
+ * table[idx[i]] = val[i] in order; an index outside [0, entries) or a value
+ * outside [-1, n_phys) is skipped and sets ORACLE_ERR_OUT_OF_RANGE. */
+int32_t oracle_table_update(int32_t* table, int64_t entries, int64_t n_phys, const int64_t* idx,
+                            const int32_t* val, int64_t n)
+{
+    int32_t err = 0;
+    for (int64_t i = 0; i < n; ++i) {
+        if (idx[i] < 0 || idx[i] >= entries || val[i] < -1 || val[i] >= n_phys) {
+            err |= ORACLE_ERR_OUT_OF_RANGE;
+            continue;
+        }
+        table[idx[i]] = val[i];
+    }
+    return err;
+}

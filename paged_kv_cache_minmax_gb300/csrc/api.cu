@@ -490,6 +490,29 @@ kvmm_status topk_promotion_diff(const kvmm_shape* shape, int32_t layer,
     return launched(kvmm::launch_promotion_diff(p, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+kvmm_status block_table_update(const kvmm_shape* shape, const int64_t* idx, const int32_t* val, int32_t n,
+                               int32_t* block_table, int32_t* err, kvmm_stream stream)
+{
+    kvmm_status st = check_shape(shape);
+    if (st != KVMM_OK) return st;
+    const kvmm_shape& s = *shape;
+    if (n < 0 || !req4(block_table) || !opt4(err)) return KVMM_INVALID_ARG;
+    if (n == 0) return KVMM_OK;
+    if (idx == nullptr || val == nullptr || !aligned(idx, 8) || !aligned(val, 4)) return KVMM_INVALID_ARG;
+    const void* di = device_view_of_host(idx);
+    const void* dv = device_view_of_host(val);
+    if (di == nullptr || dv == nullptr) return KVMM_INVALID_ARG;  // memory the device cannot read
+    kvmm::TableUpdateParams p{};
+    p.n = n;
+    p.entries = static_cast<long long>(s.B) * s.L * s.Hkv * s.Pmax;
+    p.n_phys = s.n_phys;
+    p.idx = static_cast<const int64_t*>(di);
+    p.val = static_cast<const int32_t*>(dv);
+    p.block_table = block_table;
+    p.err = err;
+    return launched(kvmm::launch_table_update(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 kvmm_status promote_pages(const kvmm_shape* shape, int32_t layer, const uint8_t* rescore_mask,
                           const int32_t* promoted, const int32_t* promoted_cnt, const int32_t* evicted,
                           const int32_t* evicted_cnt, const kvmm_bf16* host_k, const kvmm_bf16* host_v,

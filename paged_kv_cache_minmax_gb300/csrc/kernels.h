@@ -185,6 +185,17 @@ cudaError_t allow_smem(Kernel kernel, size_t bytes, int& dev_cache, size_t& byte
 }
 
 // Launchers return cudaSuccess or the launch error.
+// block_table_update
+struct TableUpdateParams {
+    long long n;
+    long long entries;  // B * L * Hkv * Pmax
+    int64_t n_phys;
+    const int64_t* idx;  // device-addressable
+    const int32_t* val;
+    int32_t* block_table;
+    int32_t* err;
+};
+
 // promote_pages
 struct PromoteParams {
     int B, L, Hkv, T, D, Pmax, Kmax, layer;
@@ -228,6 +239,7 @@ cudaError_t launch_score_topk(const ScoreParams& p, int group_reduce, cudaStream
 cudaError_t launch_sparse_attention(const AttnParams& p, cudaStream_t stream);
 cudaError_t launch_promotion_diff(const DiffParams& p, cudaStream_t stream);
 cudaError_t launch_promote(const PromoteParams& p, int max_ctas, cudaStream_t stream);
+cudaError_t launch_table_update(const TableUpdateParams& p, cudaStream_t stream);
 cudaError_t launch_history_record(const StabilityParams& p, cudaStream_t stream);
 cudaError_t launch_stability_rco(const StabilityParams& p, cudaStream_t stream);
 size_t stability_max_heads();  // largest L * Hkv the classification handles

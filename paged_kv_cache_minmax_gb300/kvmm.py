@@ -22,7 +22,7 @@ NULL_BLOCK = -1
 EXPORTS = ("kv_minmax_update", "page_score_topk", "sparse_paged_decode_attn", "topk_promotion_diff",
            "kvmm_workspace_size", "kvmm_auto_splits", "kvmm_status_string", "kvmm_last_cuda_error",
            "page_score_topk_static_scratch", "page_score_topk_attn", "decode_layer", "topk_history_record",
-           "topk_stability_rco", "promote_pages")
+           "topk_stability_rco", "promote_pages", "block_table_update")
 
 
 class KvmmError(RuntimeError):
@@ -81,9 +81,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.topk_history_record.argtypes = [SP, I32, P, P, P, I32, I32, P, P, P, P, P]
     lib.topk_stability_rco.argtypes = [SP, P, P, P, I32, I32, I32, I32, F32, P, P, P, P, P]
     lib.promote_pages.argtypes = [SP, I32, P, P, P, P, P, P, P, P, P, P, P, P, P, I32, P, P]
+    lib.block_table_update.argtypes = [SP, P, P, I32, P, P, P]
     for f in ("kv_minmax_update", "page_score_topk", "sparse_paged_decode_attn", "topk_promotion_diff",
               "page_score_topk_static_scratch", "page_score_topk_attn", "decode_layer", "topk_history_record",
-              "topk_stability_rco", "promote_pages"):
+              "topk_stability_rco", "promote_pages", "block_table_update"):
         getattr(lib, f).restype = ctypes.c_int
     lib.kvmm_workspace_size.argtypes = [SP, I32]
     lib.kvmm_workspace_size.restype = SZ
@@ -351,4 +352,19 @@ def promote_pages(shape: Shape, layer: int, rescore_mask, promoted, promoted_cnt
             _dev(freed_cnt, "freed_cnt", torch.int32, units, optional=True), int(max_ctas),
             _dev(err, "err", torch.int32, 1, optional=True), _stream(stream))
     _check("promote_pages", load().promote_pages(*args))
+
+
+def block_table_update(shape: Shape, idx, val, block_table, err=None, stream=None) -> None:
+    """block_table.view(-1)[idx[i]] = val[i]; idx (int64) and val (int32) on the device or in pinned host memory."""
+    s = shape
+    n = int(idx.numel())
+    if int(val.numel()) != n:
+        raise ValueError("idx and val differ in length")
+    for t, name, dt in ((idx, "idx", torch.int64), (val, "val", torch.int32)):
+        if t.dtype != dt or not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous {dt}")
+    args = (ctypes.byref(s), idx.data_ptr() if n else None, val.data_ptr() if n else None, n,
+            _dev(block_table, "block_table", torch.int32, s.B * s.L * s.Hkv * s.Pmax),
+            _dev(err, "err", torch.int32, 1, optional=True), _stream(stream))
+    _check("block_table_update", load().block_table_update(*args))
 

@@ -111,3 +111,20 @@ def test_a_null_evicted_entry_is_reported_and_moves_nothing():
     bt[2] = -1  # the evicted page was already null
     err, moved, _ = oracle.unit_promote(bt, n_phys, [6], [2], hk, hv, kp, vp, T)
     assert err & 1 and moved == 0 and bt[6] == -1
+
+
+def test_table_update_applies_exactly_the_changed_entries():
+    # FlexiCache, "System design, head-level block table" (dirty tracking): the entries where two tables differ,
+    # applied to the first, give the second; invalid updates are skipped and reported
+    rng = np.random.default_rng(9)
+    old = rng.integers(-1, 500, size=(2, 3, 4, 64)).astype(np.int32)
+    new = old.copy()
+    pick = rng.random(new.shape) < 0.05
+    new[pick] = rng.integers(-1, 500, size=int(pick.sum()))
+    idx = np.flatnonzero(old != new)
+    t = old.copy()
+    assert oracle.table_update(t, 500, idx, new.ravel()[idx]) == 0
+    assert np.array_equal(t, new)
+    t2 = old.copy()
+    err = oracle.table_update(t2, 500, np.array([0, old.size, 5], dtype=np.int64), np.array([7, 1, 500], dtype=np.int32))
+    assert err == 2 and t2.ravel()[0] == 7 and np.array_equal(t2.ravel()[1:], old.ravel()[1:])
