@@ -682,6 +682,81 @@ def table_update_arm(args):
         "device_err": int(err.item())}), flush=True)
 
 
+def meankey_arm(args):
+    """KVDrive's mean-key scorer beside MinMax at the 8B-32K shape (one layer, 64 units, K = 128): the time of
+    scoring + top-K for each (CUDA-graph replays; the mean rows are half the bytes), and, over a sample of units,
+    the dense attention mass their selections capture (oracle, fp64), next to the best possible: the K pages of
+    most mass."""
+    import oracle
+    from paged_kv_cache_minmax_gb300 import build as kbuild
+    from paged_kv_cache_minmax_gb300 import kvmm
+    from paged_kv_cache_minmax_gb300.runtime import DecodeState
+    from paged_kv_cache_minmax_gb300.workloads import bf16_bits
+
+    kbuild.build_library()
+    kvmm.load()
+    oracle.build()
+    cfg = workloads.scaled(CFG, L=1)
+    wl = workloads.generate(cfg, device="cuda")
+    st = DecodeState.for_workload(wl)
+    st.build_metadata()
+    shape = st.shape
+    mean = torch.zeros(cfg.B, 1, cfg.Hkv, cfg.Pmax, cfg.D, dtype=torch.bfloat16, device="cuda")
+    kvmm.kv_meankey_update(shape, 0, None, wl.seq_len, wl.k_pool, wl.block_table, mean, err=st.err)
+    sel_mm = torch.zeros_like(st.sel_idx)
+    cnt_mm = torch.zeros_like(st.sel_cnt)
+    sel_mk = torch.zeros_like(st.sel_idx)
+    cnt_mk = torch.zeros_like(st.sel_cnt)
+    stream = torch.cuda.Stream()
+
+    def timed(fn, reps):
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                fn()
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            g.replay()
+            e0.record()
+            for _ in range(reps):
+                g.replay()
+            e1.record()
+        stream.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / reps
+
+    reps = max(10, min(args.steps, 200))
+    mm_us = timed(lambda: kvmm.page_score_topk(shape, 0, wl.q[0], st.meta, wl.seq_len, None, cfg.K, sel_mm, cnt_mm,
+                                               st.workspace, st.err), reps)
+    mk_us = timed(lambda: kvmm.page_score_topk_mean(shape, 0, wl.q[0], mean, wl.seq_len, None, cfg.K, sel_mk,
+                                                    cnt_mk, st.workspace, st.err), reps)
+    torch.cuda.synchronize()
+    kp, qb = bf16_bits(wl.k_pool).reshape(-1, cfg.T, cfg.D), bf16_bits(wl.q[0])
+    captured = {"minmax": [], "meankey": [], "best": []}
+    sample = [(b, h) for b in range(cfg.B) for h in range(0, cfg.Hkv, 4)][:max(2, min(16, args.steps))]
+    for b, h in sample:
+        row = wl.block_table[b, 0, h].cpu().numpy()
+        seq = int(wl.seq_len[b])
+        mass = oracle.unit_page_mass(qb[b, h * cfg.G:(h + 1) * cfg.G], kp, cfg.T, row, seq).mean(axis=0)
+        for name, sel, cnt in (("minmax", sel_mm, cnt_mm), ("meankey", sel_mk, cnt_mk)):
+            pages = sel[b, 0, h, :int(cnt[b, 0, h])].cpu().numpy()
+            captured[name].append(float(mass[pages].sum()))
+        captured["best"].append(float(np.sort(mass)[::-1][:cfg.K].sum()))
+    meta_bytes = cfg.B * cfg.Hkv * cfg.P * 2 * cfg.D * 2
+    print(json.dumps({
+        "metric": "page scorers: MinMax bounds vs mean key (KVDrive); time and dense attention mass captured",
+        "unit": "us", "higher_is_better": False,
+        "score_topk_us": {"minmax": mm_us, "meankey": mk_us},
+        "metadata_bytes": {"minmax": meta_bytes, "meankey": meta_bytes // 2},
+        "attention_mass_captured_mean": {k: float(np.mean(v)) for k, v in captured.items()},
+        "attention_mass_captured_min": {k: float(np.min(v)) for k, v in captured.items()},
+        "config": {"workload": cfg.name, "units": cfg.B * cfg.Hkv, "top_k": cfg.K, "pages": cfg.P,
+                   "sampled_units": len(sample), "keys": cfg.key_dist, "planted_pages": cfg.n_planted},
+        "device_err": st.read_err()}), flush=True)
+
+
 def load_traffic(kernel):
     """dram bytes per launch of ``kernel`` from the committed ncu summary, if current."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
@@ -702,6 +777,8 @@ def main():
     ap.add_argument("--no-graph", action="store_true", help="launch eagerly (for profilers)")
     ap.add_argument("--batch", type=int, default=0, help="override the batch (smaller profiling case)")
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (smaller profiling case)")
+    ap.add_argument("--meankey", action="store_true",
+                    help="compare the mean-key scorer with MinMax (time, attention mass captured) instead")
     ap.add_argument("--table-update", action="store_true",
                     help="time dirty-tracked block-table synchronisation instead")
     ap.add_argument("--promote", action="store_true",
@@ -721,6 +798,8 @@ def main():
         promote_arm(args)
     elif args.table_update:
         table_update_arm(args)
+    elif args.meankey:
+        meankey_arm(args)
     else:
         gpu_arm(args)
 

@@ -311,6 +311,35 @@ kvmm_status decode_layer(const kvmm_shape* shape, int32_t layer, const kvmm_bf16
                          float* lse, void* workspace, size_t workspace_bytes, int32_t* err, kvmm_stream stream);
 
 /* ------------------------------------------------------------------------
+ * The mean-key scorer: KVDrive's page representative, beside MinMax.
+ *
+ * KVDrive, "Method details": the KV cache is split into blocks and each
+ * page's mean key is its representative in the index (higher-level
+ * centroids then group similar pages).  The score of page p for query head
+ * g is q_g . mean_p, on D channels where MinMax reads 2D.
+ *
+ * kv_meankey_update -- mean [B][L][Hkv][Pmax][D] bf16: for every logical
+ * page meeting [tok_begin[b], tok_end[b]) (tok_begin NULL = from 0), the
+ * mean of the page's keys below tok_end[b]: their fp32 sum in token order,
+ * divided by their count, rounded to bf16 (nearest even).  Null or
+ * out-of-range table entries set their error bit and the page is skipped;
+ * a range outside [0, Pmax*T] sets KVMM_ERR_OUT_OF_RANGE and is clamped.
+ */
+kvmm_status kv_meankey_update(const kvmm_shape* shape, int32_t layer, const int32_t* tok_begin,
+                              const int32_t* tok_end, const kvmm_bf16* k_pool, const int32_t* block_table,
+                              kvmm_bf16* mean, int32_t* err, kvmm_stream stream);
+
+/* page_score_topk_mean -- page_score_topk with the mean key as the page's
+ * row: s_g(p) = q_g . mean_p (fp32), group sum (or max), top K with the same
+ * ties, order, rescore mask, scores_out and workspace as page_score_topk.
+ */
+kvmm_status page_score_topk_mean(const kvmm_shape* shape, int32_t layer, const kvmm_bf16* q,
+                                 const kvmm_bf16* mean, const int32_t* seq_len, const uint8_t* rescore_mask,
+                                 int32_t K, int32_t group_reduce, int32_t* sel_idx, int32_t* sel_cnt,
+                                 float* scores_out, void* workspace, size_t workspace_bytes, int32_t* err,
+                                 kvmm_stream stream);
+
+/* ------------------------------------------------------------------------
  * block_table_update -- apply the changed entries of the head-level block
  * table: block_table[idx[i]] = val[i], i = 0 .. n-1.
  *

@@ -71,6 +71,12 @@ def _load():
         lib.oracle_unit_promote.restype = I32
         lib.oracle_table_update.argtypes = [P, I64, I64, P, P, I64]
         lib.oracle_table_update.restype = I32
+        lib.oracle_unit_meankey.argtypes = [P, I64, I32, I32, P, I32, I32, I32, P]
+        lib.oracle_unit_meankey.restype = I32
+        lib.oracle_unit_mean_scores.argtypes = [P, I32, I32, P, I32, I32, P]
+        lib.oracle_unit_mean_scores.restype = None
+        lib.oracle_unit_page_mass.argtypes = [P, I32, I32, I32, P, I64, P, I32, D, P]
+        lib.oracle_unit_page_mass.restype = I32
         lib.oracle_rco.argtypes = [P, I32, P, I32, I32]
         lib.oracle_rco.restype = D
         lib.oracle_unit_stability.argtypes = [P, P, P, I32, I32, I32]
@@ -177,6 +183,40 @@ def table_update(table, n_phys, idx, val) -> int:
     idx = np.ascontiguousarray(idx, dtype=np.int64)
     val = _i32(val)
     return int(_load().oracle_table_update(_ptr(table), table.size, int(n_phys), _ptr(idx), _ptr(val), len(idx)))
+
+
+def unit_meankey(k_pool, T, bt_row, seq_len, page_begin=0, page_end=None, mean=None):
+    """Mean keys (uint16 bf16 bits [Pmax, D]) of pages [page_begin, page_end); returns (mean, err)."""
+    k_pool = _u16(k_pool)
+    bt = _i32(bt_row)
+    D = k_pool.shape[-1]
+    n_phys = k_pool.size // (T * D)
+    P = len(bt)
+    if mean is None:
+        mean = np.zeros((P, D), dtype=np.uint16)
+    err = _load().oracle_unit_meankey(_ptr(k_pool), n_phys, T, D, _ptr(bt), int(seq_len), int(page_begin),
+                                      P if page_end is None else int(page_end), _ptr(mean))
+    return mean, int(err)
+
+
+def unit_mean_scores(q, mean, P, group_reduce=0) -> np.ndarray:
+    q, mean = _u16(q), _u16(mean)
+    G, D = q.shape
+    out = np.zeros(max(P, 1), dtype=np.float64)
+    _load().oracle_unit_mean_scores(_ptr(q), G, D, _ptr(mean), int(P), int(group_reduce), _ptr(out))
+    return out[:P].copy()
+
+
+def unit_page_mass(q, k_pool, T, bt_row, seq_len, scale=0.0) -> np.ndarray:
+    """Dense attention mass [G, P] of every page (softmax over every token below seq_len)."""
+    q, k_pool, bt = _u16(q), _u16(k_pool), _i32(bt_row)
+    G, D = q.shape
+    n_phys = k_pool.size // (T * D)
+    P = (int(seq_len) + T - 1) // T
+    out = np.zeros((G, max(P, 1)), dtype=np.float64)
+    _load().oracle_unit_page_mass(_ptr(q), G, D, T, _ptr(k_pool), n_phys, _ptr(bt), int(seq_len), float(scale),
+                                  _ptr(out))
+    return out[:, :P].copy()
 
 
 def rco(a, b, P) -> float:

@@ -35,6 +35,8 @@
  *   KVDrive: A Holistic Multi-Tier KV Cache Management System for
  *   Long-Context LLM Inference, "Background and key observations": Quest
  *   multiplies the query with the keys' channel-wise min and max.
+ *   KVDrive, "Method details": each page's mean key is its representative
+ *   in the index; the mean-key scorer ranks pages by q . mean.
  *
  * Readings taken where the pages are silent (each is listed in the design doc):
  *   - page score for one query head: sum_d max(q_d*min_d, q_d*max_d), the
@@ -49,6 +51,10 @@
  *     result is a unique bf16 bit pattern;
  *   - attention scale defaults to D^-1/2; output and log-sum-exp in double;
  *     a unit with no valid token yields output 0 and lse = -inf.
+ *   - a page's mean key is its keys' fp32 sum in token order over their
+ *     count, rounded to bf16 nearest-even (the rounding decides the stored
+ *     code, so it is taken in the kernel's precision); its score for head g
+ *     is q_g . mean in double;
  *   - promotion pairs promoted[i] with evicted[i] (both ascending) for
  *     i < min(np, ne): the evicted page's block goes to the promoted page,
  *     the evicted entry becomes the null block; surplus evicted blocks are
@@ -524,5 +530,100 @@ int32_t oracle_table_update(int32_t* table, int64_t entries, int64_t n_phys, con
         }
         table[idx[i]] = val[i];
     }
+    return err;
+}
+
+/* ------------------------------------------------------------------------
+ * The mean-key scorer (KVDrive, "Method details": each page's mean key is
+ * its representative).
+ */
+
+/* float -> bf16 bit pattern, rounding to nearest, ties to even (finite x) */
+static uint16_t bf16_round_nearest_even(float x)
+{
+    uint32_t u;
+    memcpy(&u, &x, sizeof(u));
+    const uint32_t lsb = (u >> 16) & 1u;
+    u += 0x7fffu + lsb;
+    return (uint16_t)(u >> 16);
+}
+
+/* mean[p][d] for logical pages [page_begin, page_end) with valid tokens:
+ * the fp32 sum of k[t][d] over the page's valid tokens in token order,
+ * divided by their count, rounded to bf16.  Null / out-of-range entries
+ * set their error bit and the page is left untouched. */
+int32_t oracle_unit_meankey(const uint16_t* k_pool, int64_t n_phys, int32_t T, int32_t D, const int32_t* bt_row,
+                            int32_t seq_len, int32_t page_begin, int32_t page_end, uint16_t* mean)
+{
+    int32_t err = 0;
+    for (int32_t p = page_begin; p < page_end; ++p) {
+        const int32_t n = valid_tokens(p, T, seq_len);
+        if (n == 0) continue;
+        const int64_t phys = resolve_page(bt_row, p, n_phys, &err);
+        if (phys < 0) continue;
+        const uint16_t* page = k_pool + phys * T * D;
+        for (int32_t d = 0; d < D; ++d) {
+            float acc = 0.0f;
+            for (int32_t r = 0; r < n; ++r) acc += (float)bf16_value(page[(int64_t)r * D + d]);
+            mean[(int64_t)p * D + d] = bf16_round_nearest_even(acc / (float)n);
+        }
+    }
+    return err;
+}
+
+/* s(p) = sum_g q_g . mean_p (group_reduce 0) or max_g (group_reduce 1), in double */
+void oracle_unit_mean_scores(const uint16_t* q, int32_t G, int32_t D, const uint16_t* mean, int32_t P,
+                             int32_t group_reduce, double* scores)
+{
+    for (int32_t p = 0; p < P; ++p) {
+        double heads = 0.0; /* the group's reduction */
+        for (int32_t g = 0; g < G; ++g) {
+            double s = 0.0;
+            for (int32_t d = 0; d < D; ++d)
+                s += bf16_value(q[(int64_t)g * D + d]) * bf16_value(mean[(int64_t)p * D + d]);
+            if (group_reduce == 1)
+                heads = (g == 0 || s > heads) ? s : heads;
+            else
+                heads = heads + s;
+        }
+        scores[p] = heads;
+    }
+}
+
+/* Dense attention mass of every page: mass[g][p] = sum over the page's valid
+ * tokens of softmax_t(scale * q_g . k_t), the softmax taken over every token
+ * below seq_len (through the block table).  A page whose entry is null
+ * contributes 0.  scale <= 0 means D^-1/2. */
+int32_t oracle_unit_page_mass(const uint16_t* q, int32_t G, int32_t D, int32_t T, const uint16_t* k_pool,
+                              int64_t n_phys, const int32_t* bt_row, int32_t seq_len, double scale, double* mass)
+{
+    int32_t err = 0;
+    if (scale <= 0.0) scale = 1.0 / sqrt((double)D);
+    const int32_t P = (seq_len + T - 1) / T;
+    double* z = (double*)malloc(sizeof(double) * (size_t)(seq_len > 0 ? seq_len : 1));
+    int64_t* row = (int64_t*)malloc(sizeof(int64_t) * (size_t)(seq_len > 0 ? seq_len : 1));
+    for (int32_t t = 0; t < seq_len; ++t) {
+        const int64_t phys = resolve_page(bt_row, t / T, n_phys, &err);
+        row[t] = phys < 0 ? -1 : phys * T + t % T;
+    }
+    for (int32_t g = 0; g < G; ++g) {
+        double m = -INFINITY;
+        for (int32_t t = 0; t < seq_len; ++t) {
+            z[t] = -INFINITY;
+            if (row[t] < 0) continue;
+            double dot = 0.0;
+            for (int32_t d = 0; d < D; ++d)
+                dot += bf16_value(q[(int64_t)g * D + d]) * bf16_value(k_pool[row[t] * D + d]);
+            z[t] = dot * scale;
+            if (z[t] > m) m = z[t];
+        }
+        double denom = 0.0;
+        for (int32_t t = 0; t < seq_len; ++t) denom += (row[t] < 0) ? 0.0 : exp(z[t] - m);
+        for (int32_t p = 0; p < P; ++p) mass[(int64_t)g * P + p] = 0.0;
+        for (int32_t t = 0; t < seq_len; ++t)
+            if (row[t] >= 0) mass[(int64_t)g * P + t / T] += exp(z[t] - m) / denom;
+    }
+    free(z);
+    free(row);
     return err;
 }

@@ -150,12 +150,12 @@ kvmm_status kv_minmax_update(const kvmm_shape* shape, int32_t layer, const kvmm_
     return launched(kvmm::launch_minmax_update(p, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-kvmm_status page_score_topk(const kvmm_shape* shape, int32_t layer, const kvmm_bf16* q,
-                            const kvmm_bf16* meta, const int32_t* seq_len,
-                            const uint8_t* rescore_mask, int32_t K, int32_t group_reduce,
-                            int32_t* sel_idx, int32_t* sel_cnt, float* scores_out,
-                            void* workspace, size_t workspace_bytes, int32_t* err,
-                            kvmm_stream stream)
+// page_score_topk and page_score_topk_mean: the same arguments, MinMax bounds or mean keys as rows
+static kvmm_status score_topk_call(const kvmm_shape* shape, int32_t layer, const kvmm_bf16* q,
+                                   const kvmm_bf16* meta, const int32_t* seq_len, const uint8_t* rescore_mask,
+                                   int32_t K, int32_t group_reduce, int32_t* sel_idx, int32_t* sel_cnt,
+                                   float* scores_out, void* workspace, size_t workspace_bytes, int32_t* err,
+                                   kvmm_stream stream, bool mean)
 {
     kvmm_status st = check_shape(shape);
     if (st != KVMM_OK) return st;
@@ -188,7 +188,57 @@ kvmm_status page_score_topk(const kvmm_shape* shape, int32_t layer, const kvmm_b
     p.counters = static_cast<int32_t*>(workspace);
     p.scores_ws = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + kvmm::ws_counter_bytes(s));
     p.err = err;
-    return launched(kvmm::launch_score_topk(p, group_reduce, reinterpret_cast<cudaStream_t>(stream)));
+    return launched(mean ? kvmm::launch_score_topk_mean(p, group_reduce, reinterpret_cast<cudaStream_t>(stream))
+                         : kvmm::launch_score_topk(p, group_reduce, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+kvmm_status page_score_topk(const kvmm_shape* shape, int32_t layer, const kvmm_bf16* q,
+                            const kvmm_bf16* meta, const int32_t* seq_len,
+                            const uint8_t* rescore_mask, int32_t K, int32_t group_reduce,
+                            int32_t* sel_idx, int32_t* sel_cnt, float* scores_out,
+                            void* workspace, size_t workspace_bytes, int32_t* err,
+                            kvmm_stream stream)
+{
+    return score_topk_call(shape, layer, q, meta, seq_len, rescore_mask, K, group_reduce, sel_idx, sel_cnt,
+                           scores_out, workspace, workspace_bytes, err, stream, false);
+}
+
+kvmm_status page_score_topk_mean(const kvmm_shape* shape, int32_t layer, const kvmm_bf16* q,
+                                 const kvmm_bf16* mean, const int32_t* seq_len, const uint8_t* rescore_mask,
+                                 int32_t K, int32_t group_reduce, int32_t* sel_idx, int32_t* sel_cnt,
+                                 float* scores_out, void* workspace, size_t workspace_bytes, int32_t* err,
+                                 kvmm_stream stream)
+{
+    return score_topk_call(shape, layer, q, mean, seq_len, rescore_mask, K, group_reduce, sel_idx, sel_cnt,
+                           scores_out, workspace, workspace_bytes, err, stream, true);
+}
+
+kvmm_status kv_meankey_update(const kvmm_shape* shape, int32_t layer, const int32_t* tok_begin,
+                              const int32_t* tok_end, const kvmm_bf16* k_pool, const int32_t* block_table,
+                              kvmm_bf16* mean, int32_t* err, kvmm_stream stream)
+{
+    kvmm_status st = check_shape(shape);
+    if (st != KVMM_OK) return st;
+    const kvmm_shape& s = *shape;
+    if (layer < 0 || layer >= s.L) return KVMM_INVALID_ARG;
+    if (!opt4(tok_begin) || !req4(tok_end) || !req(k_pool) || !req4(block_table) || !req(mean) || !opt4(err))
+        return KVMM_INVALID_ARG;
+    kvmm::MeanParams p{};
+    p.B = s.B;
+    p.L = s.L;
+    p.Hkv = s.Hkv;
+    p.T = s.T;
+    p.D = s.D;
+    p.Pmax = s.Pmax;
+    p.layer = layer;
+    p.n_phys = s.n_phys;
+    p.tok_begin = tok_begin;
+    p.tok_end = tok_end;
+    p.k_pool = k_pool;
+    p.block_table = block_table;
+    p.mean = mean;
+    p.err = err;
+    return launched(kvmm::launch_meankey(p, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 kvmm_status page_score_topk_static_scratch(const kvmm_shape* shape, int32_t layer, const kvmm_bf16* q,

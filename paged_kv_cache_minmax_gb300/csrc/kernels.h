@@ -185,6 +185,18 @@ cudaError_t allow_smem(Kernel kernel, size_t bytes, int& dev_cache, size_t& byte
 }
 
 // Launchers return cudaSuccess or the launch error.
+// kv_meankey_update
+struct MeanParams {
+    int B, L, Hkv, T, D, Pmax, layer;
+    int64_t n_phys;
+    const int32_t* tok_begin;  // or null: 0
+    const int32_t* tok_end;
+    const kvmm_bf16* k_pool;
+    const int32_t* block_table;
+    kvmm_bf16* mean;  // [B][L][Hkv][Pmax][D]
+    int32_t* err;
+};
+
 // block_table_update
 struct TableUpdateParams {
     long long n;
@@ -240,6 +252,7 @@ cudaError_t launch_sparse_attention(const AttnParams& p, cudaStream_t stream);
 cudaError_t launch_promotion_diff(const DiffParams& p, cudaStream_t stream);
 cudaError_t launch_promote(const PromoteParams& p, int max_ctas, cudaStream_t stream);
 cudaError_t launch_table_update(const TableUpdateParams& p, cudaStream_t stream);
+cudaError_t launch_meankey(const MeanParams& p, cudaStream_t stream);
 cudaError_t launch_history_record(const StabilityParams& p, cudaStream_t stream);
 cudaError_t launch_stability_rco(const StabilityParams& p, cudaStream_t stream);
 size_t stability_max_heads();  // largest L * Hkv the classification handles
@@ -248,6 +261,7 @@ size_t decode_layer_smem(int D, int T, int Pmax, int Kmax, int C);  // dynamic s
 int decode_layer_cluster(const kvmm_shape& s);                 // CTAs per cluster for a shape
 // the scoring kernel alone (page_score_topk without its selection kernel)
 cudaError_t launch_score_only(const ScoreParams& p, int group_reduce, cudaStream_t stream);
+cudaError_t launch_score_topk_mean(const ScoreParams& p, int group_reduce, cudaStream_t stream);  // mean-key rows
 
 // Library-owned scratch of page_score_topk_static_scratch (score_topk.cu):
 // counters for up to kStaticScratchCounterBytes/4 units, then the scores.

@@ -83,11 +83,15 @@ __device__ __forceinline__ int unit_pages(const ScoreParams& p, int b, bool repo
 }
 
 // ---------------------------------------------------------------------------
-template <int D, int MODE>
+// KIND 0: a page's row is its [min | max] key bounds (2D channels), weighted by [min(q,0) | max(q,0)];
+// KIND 1: a page's row is its mean key (D channels), weighted by q (KVDrive's mean-key representative).
+template <int D, int MODE, int KIND>
 __global__ void __launch_bounds__(kScoreThreads) score_pages_kernel(const ScoreParams p)
 {
-    constexpr int kRowChunks = 2 * D / 8;   // 16-byte chunks in a [min | max] row
-    constexpr int kR = kRowChunks / 4;      // chunk groups: lane tig takes chunk 4r + tig
+    constexpr int kRowCh = KIND == 0 ? 2 * D : D;  // channels of a page's row
+    constexpr int kRowBytes = 2 * kRowCh;
+    constexpr int kRowChunks = kRowCh / 8;         // 16-byte chunks in a row
+    constexpr int kR = kRowChunks / 4;             // chunk groups: lane tig takes chunk 4r + tig
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ uint64_t full_bar[kStages];
     __shared__ uint64_t empty_bar[kStages];
@@ -135,10 +139,10 @@ __global__ void __launch_bounds__(kScoreThreads) score_pages_kernel(const ScoreP
                 if (npg > 0) {
                     uint8_t* st = smem + static_cast<size_t>(s) * stage_bytes(D);
                     const size_t unit = (static_cast<size_t>(b) * p.L + p.layer) * p.Hkv + h;
-                    const uint32_t mbytes = static_cast<uint32_t>(npg) * 4 * D;
+                    const uint32_t mbytes = static_cast<uint32_t>(npg) * kRowBytes;
                     const uint32_t qbytes = static_cast<uint32_t>(p.G) * D * 2;
                     mbar_arrive_expect_tx(&full_bar[s], mbytes + qbytes);
-                    bulk_copy_g2s(st, p.meta + (unit * p.Pmax + page0) * 2 * D, mbytes, &full_bar[s]);
+                    bulk_copy_g2s(st, p.meta + (unit * p.Pmax + page0) * kRowCh, mbytes, &full_bar[s]);
                     bulk_copy_g2s(st + stage_meta_bytes(D),
                                   p.q + (static_cast<size_t>(b) * p.Hq + static_cast<size_t>(h) * p.G) * D,
                                   qbytes, &full_bar[s]);
@@ -164,23 +168,30 @@ __global__ void __launch_bounds__(kScoreThreads) score_pages_kernel(const ScoreP
             const uint8_t* qs = st + stage_meta_bytes(D) + gid * (2 * D);
 #pragma unroll
             for (int r = 0; r < kR; ++r) {
-                const int cc = 4 * r + tig;                 // chunk of the [min | max] row
+                const int cc = 4 * r + tig;                 // chunk of the row
                 const int qc = cc % (D / 8);                // source chunk of q
                 uint4 v = make_uint4(0u, 0u, 0u, 0u);
                 if (real_head) v = ld_shared_v4(qs + 16 * qc);
-                const bool is_max = cc >= D / 8;
-                wf[r][0] = is_max ? bf16x2_max0(v.x) : bf16x2_min0(v.x);
-                wf[r][1] = is_max ? bf16x2_max0(v.y) : bf16x2_min0(v.y);
-                wf[r][2] = is_max ? bf16x2_max0(v.z) : bf16x2_min0(v.z);
-                wf[r][3] = is_max ? bf16x2_max0(v.w) : bf16x2_min0(v.w);
+                if (KIND == 1) {  // mean key: the query itself
+                    wf[r][0] = v.x;
+                    wf[r][1] = v.y;
+                    wf[r][2] = v.z;
+                    wf[r][3] = v.w;
+                } else {
+                    const bool is_max = cc >= D / 8;
+                    wf[r][0] = is_max ? bf16x2_max0(v.x) : bf16x2_min0(v.x);
+                    wf[r][1] = is_max ? bf16x2_max0(v.y) : bf16x2_min0(v.y);
+                    wf[r][2] = is_max ? bf16x2_max0(v.z) : bf16x2_min0(v.z);
+                    wf[r][3] = is_max ? bf16x2_max0(v.w) : bf16x2_min0(v.w);
+                }
             }
             cached_unit = inf.x;
         }
         const int pg0 = warp * 16;
         if (pg0 < npg) {
             // C[page][head] over this warp's 16 pages: rows gid and gid + 8
-            const uint8_t* ra = st + static_cast<size_t>(pg0 + gid) * 4 * D;
-            const uint8_t* rb = ra + 8 * 4 * D;
+            const uint8_t* ra = st + static_cast<size_t>(pg0 + gid) * kRowBytes;
+            const uint8_t* rb = ra + 8 * kRowBytes;
             float c[4] = {0.f, 0.f, 0.f, 0.f}, c2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int r = 0; r < kR; ++r) {
@@ -252,23 +263,24 @@ cudaError_t allow_topk_smem(size_t bytes)
     return allow_smem(select_topk_kernel, bytes, dev_cache, bytes_cache);
 }
 
-template <int D, int MODE>
+template <int D, int MODE, int KIND = 0>
 cudaError_t launch_score(const ScoreParams& p, cudaStream_t stream, bool with_select)
 {
     static thread_local int dev_a = -1;
     static thread_local size_t bytes_a = 0;
     const size_t smem = static_cast<size_t>(kStages) * stage_bytes(D);
-    cudaError_t e = allow_smem(score_pages_kernel<D, MODE>, smem, dev_a, bytes_a);
+    cudaError_t e = allow_smem(score_pages_kernel<D, MODE, KIND>, smem, dev_a, bytes_a);
     if (e != cudaSuccess) return e;
     int dev = 0, sms = 148, per_sm = 1;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, score_pages_kernel<D, MODE>, kScoreThreads, smem);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, score_pages_kernel<D, MODE, KIND>, kScoreThreads, smem);
     if (per_sm < 1) per_sm = 1;
     const long long items = static_cast<long long>(p.B) * p.Hkv * ((p.Pmax + kChunk - 1) / kChunk);
     const long long slots = static_cast<long long>(sms) * per_sm;
     const long long grid = items < slots ? items : slots;
-    e = launch_pdl(score_pages_kernel<D, MODE>, dim3(static_cast<unsigned>(grid)), dim3(kScoreThreads), smem, stream, p);
+    e = launch_pdl(score_pages_kernel<D, MODE, KIND>, dim3(static_cast<unsigned>(grid)), dim3(kScoreThreads), smem,
+                   stream, p);
     if (e != cudaSuccess || !with_select) return e;
     const size_t ksmem = static_cast<size_t>(p.Pmax) * (sizeof(float) + sizeof(int16_t));
     e = allow_topk_smem(ksmem);
@@ -283,6 +295,13 @@ cudaError_t launch_score_topk(const ScoreParams& p, int group_reduce, cudaStream
     if (p.D == 128)
         return group_reduce ? launch_score<128, 1>(p, stream, true) : launch_score<128, 0>(p, stream, true);
     return group_reduce ? launch_score<64, 1>(p, stream, true) : launch_score<64, 0>(p, stream, true);
+}
+
+cudaError_t launch_score_topk_mean(const ScoreParams& p, int group_reduce, cudaStream_t stream)
+{
+    if (p.D == 128)
+        return group_reduce ? launch_score<128, 1, 1>(p, stream, true) : launch_score<128, 0, 1>(p, stream, true);
+    return group_reduce ? launch_score<64, 1, 1>(p, stream, true) : launch_score<64, 0, 1>(p, stream, true);
 }
 
 cudaError_t launch_score_only(const ScoreParams& p, int group_reduce, cudaStream_t stream)

@@ -22,7 +22,8 @@ NULL_BLOCK = -1
 EXPORTS = ("kv_minmax_update", "page_score_topk", "sparse_paged_decode_attn", "topk_promotion_diff",
            "kvmm_workspace_size", "kvmm_auto_splits", "kvmm_status_string", "kvmm_last_cuda_error",
            "page_score_topk_static_scratch", "page_score_topk_attn", "decode_layer", "topk_history_record",
-           "topk_stability_rco", "promote_pages", "block_table_update")
+           "topk_stability_rco", "promote_pages", "block_table_update", "kv_meankey_update",
+           "page_score_topk_mean")
 
 
 class KvmmError(RuntimeError):
@@ -82,9 +83,12 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.topk_stability_rco.argtypes = [SP, P, P, P, I32, I32, I32, I32, F32, P, P, P, P, P]
     lib.promote_pages.argtypes = [SP, I32, P, P, P, P, P, P, P, P, P, P, P, P, P, I32, P, P]
     lib.block_table_update.argtypes = [SP, P, P, I32, P, P, P]
+    lib.kv_meankey_update.argtypes = [SP, I32, P, P, P, P, P, P, P]
+    lib.page_score_topk_mean.argtypes = [SP, I32, P, P, P, P, I32, I32, P, P, P, P, SZ, P, P]
     for f in ("kv_minmax_update", "page_score_topk", "sparse_paged_decode_attn", "topk_promotion_diff",
               "page_score_topk_static_scratch", "page_score_topk_attn", "decode_layer", "topk_history_record",
-              "topk_stability_rco", "promote_pages", "block_table_update"):
+              "topk_stability_rco", "promote_pages", "block_table_update", "kv_meankey_update",
+              "page_score_topk_mean"):
         getattr(lib, f).restype = ctypes.c_int
     lib.kvmm_workspace_size.argtypes = [SP, I32]
     lib.kvmm_workspace_size.restype = SZ
@@ -367,4 +371,33 @@ def block_table_update(shape: Shape, idx, val, block_table, err=None, stream=Non
             _dev(block_table, "block_table", torch.int32, s.B * s.L * s.Hkv * s.Pmax),
             _dev(err, "err", torch.int32, 1, optional=True), _stream(stream))
     _check("block_table_update", load().block_table_update(*args))
+
+
+def kv_meankey_update(shape: Shape, layer: int, tok_begin, tok_end, k_pool, block_table, mean, err=None,
+                      stream=None) -> None:
+    """Mean key of every page meeting [tok_begin, tok_end) (tok_begin None = 0) into mean [B,L,Hkv,Pmax,D]."""
+    s = shape
+    units = s.B * s.L * s.Hkv
+    args = (ctypes.byref(s), layer, _dev(tok_begin, "tok_begin", torch.int32, s.B, optional=True),
+            _dev(tok_end, "tok_end", torch.int32, s.B), _dev(k_pool, "k_pool", torch.bfloat16, s.n_phys * s.T * s.D),
+            _dev(block_table, "block_table", torch.int32, units * s.Pmax),
+            _dev(mean, "mean", torch.bfloat16, units * s.Pmax * s.D), _dev(err, "err", torch.int32, 1, optional=True),
+            _stream(stream))
+    _check("kv_meankey_update", load().kv_meankey_update(*args))
+
+
+def page_score_topk_mean(shape: Shape, layer: int, q, mean, seq_len, rescore_mask, K: int, sel_idx, sel_cnt,
+                         workspace, err=None, scores_out=None, group_reduce: int = 0, stream=None) -> None:
+    """page_score_topk with the mean key (mean [B,L,Hkv,Pmax,D]) as the page's row."""
+    s = shape
+    units = s.B * s.L * s.Hkv
+    args = (ctypes.byref(s), layer, _dev(q, "q", torch.bfloat16, s.B * s.Hq * s.D),
+            _dev(mean, "mean", torch.bfloat16, units * s.Pmax * s.D),
+            _dev(seq_len, "seq_len", torch.int32, s.B),
+            _dev(rescore_mask, "rescore_mask", torch.uint8, s.L * s.Hkv, optional=True), K, group_reduce,
+            _dev(sel_idx, "sel_idx", torch.int32, units * s.Kmax), _dev(sel_cnt, "sel_cnt", torch.int32, units),
+            _dev(scores_out, "scores_out", torch.float32, s.B * s.Hkv * s.Pmax, optional=True),
+            _dev(workspace, "workspace", torch.uint8), workspace.numel(),
+            _dev(err, "err", torch.int32, 1, optional=True), _stream(stream))
+    _check("page_score_topk_mean", load().page_score_topk_mean(*args))
 

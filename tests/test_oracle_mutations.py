@@ -12,7 +12,7 @@ import tempfile
 import pytest
 
 import oracle
-from tests import test_oracle_pins as pins
+from tests import test_oracle_meankey, test_oracle_pins as pins, test_oracle_promote, test_oracle_stability
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "kvmm_oracle.c")
 
@@ -38,9 +38,27 @@ MUTATIONS = {
     "table-null-not-skipped": ("if (phys < 0) {\n        *err |= ORACLE_ERR_NULL_BLOCK;\n        return -1;",
                                "if (phys < 0) {\n        *err |= ORACLE_ERR_NULL_BLOCK;\n        return 0;"),
     "append-wrong-row": ("int64_t row = phys * T + (t % T);", "int64_t row = phys * T + ((t + 1) % T);"),
+    # temporal stability (RCO) and classification
+    "rco-chance-without-the-product": ("const int64_t chance_p = (int64_t)na * nb;",
+                                       "const int64_t chance_p = (int64_t)(na < nb ? na : nb);"),
+    "rco-best-is-the-larger-set": ("const int64_t best_p = (int64_t)(na < nb ? na : nb) * P;",
+                                   "const int64_t best_p = (int64_t)(na > nb ? na : nb) * P;"),
+    "rco-window-skips-a-pair": ("for (int32_t t = 0; t + lag < n; ++t) {", "for (int32_t t = 1; t + lag < n; ++t) {"),
+    "classify-ties-to-the-higher-index": ("(stability[j] == stability[i] && j < i)",
+                                          "(stability[j] == stability[i] && j > i)"),
+    # promotion
+    "promote-copies-the-evicted-page": ("host_k + (int64_t)promoted[i] * page", "host_k + (int64_t)evicted[i] * page"),
+    "promote-keeps-evicted-entries": ("        bt_row[evicted[i]] = -1;\n    }", "    }"),
+    # mean key and page mass
+    "meankey-divides-by-the-page-size": ("mean[(int64_t)p * D + d] = bf16_round_nearest_even(acc / (float)n);",
+                                         "mean[(int64_t)p * D + d] = bf16_round_nearest_even(acc / (float)T);"),
+    "meankey-truncates": ("    u += 0x7fffu + lsb;\n", ""),
+    "page-mass-skips-the-softmax-max": ("mass[(int64_t)g * P + t / T] += exp(z[t] - m) / denom;",
+                                        "mass[(int64_t)g * P + t / T] += exp(z[t]) / denom;"),
 }
 
-PIN_TESTS = [getattr(pins, n) for n in dir(pins) if n.startswith("test_")]
+PIN_TESTS = [getattr(m, n) for m in (pins, test_oracle_stability, test_oracle_promote, test_oracle_meankey)
+             for n in dir(m) if n.startswith("test_")]
 
 
 @pytest.mark.parametrize("name", sorted(MUTATIONS))
