@@ -587,6 +587,7 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
         int frag = -1;           // which fragments are loaded: 2*unit + (0 score, 1 attention)
         bool have_q = false;
         uint8_t* my_ring = rings + size_t(w) * kRing * kSlot;
+        const uint64_t stream_policy = l2_policy_evict_first();  // metadata and pages: read once
         // the slots: bit b of `held` -- slot b has a copy in flight; bit b of `par` -- the phase its
         // mbarrier completes next; (hj, hs) -- the unit and item it holds
         uint32_t held = 0u, par = 0u;
@@ -667,9 +668,9 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
             __syncwarp();
             if (8 * lane < npg) {  // lane i copies rows 8i .. 8i+7
                 const int rows = min(8, npg - 8 * lane);
-                bulk_copy_g2s(my_ring + size_t(b2) * kSlot + size_t(8 * lane) * kRowBytes,
-                              p.meta + (ufull * p.Pmax + page0 + 8 * lane) * 2 * D,
-                              static_cast<uint32_t>(rows) * kRowBytes, &sh.full[w][b2]);
+                bulk_copy_g2s_hint(my_ring + size_t(b2) * kSlot + size_t(8 * lane) * kRowBytes,
+                                   p.meta + (ufull * p.Pmax + page0 + 8 * lane) * 2 * D,
+                                   static_cast<uint32_t>(rows) * kRowBytes, &sh.full[w][b2], stream_policy);
             }
             set_slot(b2, j, sl);
         };
@@ -949,7 +950,8 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
             if (lane < 2) {  // lane 0 copies the page's keys, lane 1 its values
                 uint8_t* dst = my_ring + size_t(b2) * kSlot + lane * kPageBytes;
                 const size_t off = static_cast<size_t>(res[size_t(j) * p.maxp + s].x) * T * D;
-                bulk_copy_g2s(dst, (lane ? p.v_pool : p.k_pool) + off, kPageBytes, &sh.full[w][b2]);
+                bulk_copy_g2s_hint(dst, (lane ? p.v_pool : p.k_pool) + off, kPageBytes, &sh.full[w][b2],
+                                   stream_policy);
             }
             set_slot(b2, j, s);
         };
