@@ -181,6 +181,26 @@ __device__ __forceinline__ void st_async_f32(void* local, uint64_t* local_bar, u
                  : "memory");
 }
 
+// asynchronous atomic min (MAX = false) or max (MAX = true) of v into the
+// unsigned word at `local`'s address in CTA `rank` of the cluster, completing
+// 4 bytes of transaction on the mbarrier at `local_bar`'s address in that
+// CTA, like st_async_f32
+template <bool MAX>
+__device__ __forceinline__ void red_async_minmax_u32(uint32_t* local, uint64_t* local_bar, uint32_t rank, uint32_t v)
+{
+    uint32_t ra, rb;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_addr(local)), "r"(rank));
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rb) : "r"(smem_addr(local_bar)), "r"(rank));
+    if (MAX)
+        asm volatile("red.async.relaxed.cluster.shared::cluster.mbarrier::complete_tx::bytes.max.u32 [%0], %1, [%2];" ::"r"(ra),
+                     "r"(v), "r"(rb)
+                     : "memory");
+    else
+        asm volatile("red.async.relaxed.cluster.shared::cluster.mbarrier::complete_tx::bytes.min.u32 [%0], %1, [%2];" ::"r"(ra),
+                     "r"(v), "r"(rb)
+                     : "memory");
+}
+
 // ---------------------------------------------------------------------------
 // programmatic dependent launch: the next kernel in the stream may be
 // scheduled once every CTA of this one has called launch_dependents; a kernel

@@ -82,7 +82,8 @@ struct DUnit {
 struct DecodeShared {
     uint64_t full[kDCons][kDRingMax];  // a consumer warp's slot has landed
     uint64_t qbar;            // the query groups of the cluster's units
-    uint64_t sbar[kDUnits];   // all of the unit's scores are here (asynchronous remote stores, 4 bytes each)
+    uint64_t sbar[kDUnits];   // all of the unit's scores and its range are here (asynchronous remote stores
+                              // and reductions, 4 bytes each)
     uint64_t selr[kDUnits];   // this CTA's share of the unit's pages is resolved
     uint64_t rbar[kDUnits];   // every CTA's partial of this CTA's output slice is here (likewise)
     uint64_t pbar;            // prior bounds written (one arrival per selector warp)
@@ -100,6 +101,7 @@ struct DecodeShared {
                                    // page the new tokens reach, [min | max], two channels a word (D <= 128)
     int wide_ok[kDUnits];          // those bounds are set (the page has a valid table entry)
     uint4 nrow[kDUnits][32];       // per unit, for a one-token append: the token's key row, then its value row
+    uint32_t rkey[kDUnits][2];     // per unit: order keys of its smallest and largest score (remote reductions)
     int abort_flag;
 };
 
@@ -232,6 +234,8 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
             mbar_init(&sh.selr[j], 1);
             mbar_init(&sh.rbar[j], 1);
             sh.resn[j] = 0;
+            sh.rkey[j][0] = 0xffffffffu;
+            sh.rkey[j][1] = 0u;
         }
         mbar_init(&sh.pbar, kDSelWarps);
         for (int j = 0; j < kDUnits; ++j) mbar_init(&sh.pready[j], kDCons);
@@ -315,7 +319,8 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
                 prefetch_l2(p.block_table + sh.ud[j].ufull * p.Pmax, static_cast<uint32_t>(p.Pmax) * 4u);
         }
         if (stid == 0) {
-            // the bytes this CTA receives: every score of a rescored unit (one float a page), and from
+            // the bytes this CTA receives: every score of a rescored unit (one float a page) and from every
+            // consumer warp of every CTA the unit's score range (a min and a max reduction), and from
             // each CTA its (m, l) of every head and its partial of this CTA's slice of the outputs.  A
             // remote store that lands before its barrier is told to expect it leaves the transaction
             // count negative; the pending arrival keeps the phase open until the count is set.
@@ -323,7 +328,8 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
             const int own = max(0, min(n_out, e0 + lay.slice) - e0);
             for (int j = 0; j < nunits; ++j) {
                 const DUnit& u = sh.ud[j];
-                mbar_arrive_expect_tx(&sh.sbar[j], u.rescored ? static_cast<uint32_t>(u.P) * 4u : 0u);
+                mbar_arrive_expect_tx(&sh.sbar[j],
+                                      u.rescored ? static_cast<uint32_t>(u.P) * 4u + static_cast<uint32_t>(C * kDCons * 8) : 0u);
                 mbar_arrive_expect_tx(&sh.rbar[j], static_cast<uint32_t>(C * (2 * G + own)) * 4u);
             }
         }
@@ -450,10 +456,11 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
             int cnt;
             const int32_t* src;
             if (u.rescored) {
-                // every score of the unit is here
+                // every score of the unit and its range are here (the histogram is cleared meanwhile)
+                block_topk_prepare<kDSelThreads, SelGroup>(ts);
                 if (!mbar_wait_sleepy(&sh.sbar[j], 0, aborting() ? kDAbortNs : kDWaitNs)) set_abort();
                 cnt = block_topk<kDSelThreads, SelGroup>(nullptr, u.P, p.K, selv, sbuf + size_t(j) * lay.pstride,
-                                                         bins, ts);
+                                                         bins, ts, sh.rkey[j]);
                 if (rank == 0) {
                     for (int i = stid; i < cnt; i += kDSelThreads) p.sel_idx[u.ufull * p.Kmax + i] = selv[i];
                     if (stid == 0) p.sel_cnt[u.ufull] = cnt;
@@ -722,6 +729,23 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
             }
             __syncwarp();
         };
+        // the order keys of the smallest and largest score this lane has computed of unit rj; at the end of
+        // the unit every CTA of the cluster gets the warp's (for the selection's bins)
+        uint32_t kmin = 0xffffffffu, kmax = 0u;
+        int rj = 0;
+        auto flush_range = [&]() {
+            if (sh.ud[rj].rescored) {
+                kmin = __reduce_min_sync(kFullMask, kmin);
+                kmax = __reduce_max_sync(kFullMask, kmax);
+                if (lane < C) {
+                    red_async_minmax_u32<false>(&sh.rkey[rj][0], &sh.sbar[rj], static_cast<uint32_t>(lane), kmin);
+                    red_async_minmax_u32<true>(&sh.rkey[rj][1], &sh.sbar[rj], static_cast<uint32_t>(lane), kmax);
+                }
+            }
+            kmin = 0xffffffffu;
+            kmax = 0u;
+            ++rj;
+        };
         auto score_slot = [&](const uint8_t* slot, int j, int page0, int npg) {
             float* sb = sbuf + size_t(j) * lay.pstride + page0;
             float* orow = p.scores_out ? p.scores_out + static_cast<size_t>(cluster * kDUnits + j) * p.Pmax + page0
@@ -758,6 +782,14 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
                     }
                     // lanes tig = 0..3 of a row group send the two scores to CTAs tig, tig + 4, ...
                     const int r0 = 16 * grp + gid;
+                    if (r0 < npg) {
+                        kmin = min(kmin, topk_order_key(s_lo));
+                        kmax = max(kmax, topk_order_key(s_lo));
+                    }
+                    if (r0 + 8 < npg) {
+                        kmin = min(kmin, topk_order_key(s_hi));
+                        kmax = max(kmax, topk_order_key(s_hi));
+                    }
                     for (int r = tig; r < C; r += 4) {
                         if (r0 < npg) st_async_f32(sb + r0, &sh.sbar[j], static_cast<uint32_t>(r), s_lo);
                         if (r0 + 8 < npg) st_async_f32(sb + r0 + 8, &sh.sbar[j], static_cast<uint32_t>(r), s_hi);
@@ -782,6 +814,7 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
                 const int j = b ? hj1 : hj0;
                 const int page0 = sh.ud[j].lo + (b ? hs1 : hs0) * kPiece;
                 const int npg = min(kPiece, sh.ud[j].hi - page0);
+                while (rj < j) flush_range();  // the units before j are done
                 land(b);
                 load_frags(j, false);
                 uint8_t* slot = my_ring + size_t(b) * kSlot;
@@ -796,6 +829,7 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
                     more = next_score(ij, isl);
                 }
             }
+            while (rj < nunits) flush_range();
         }
 
         // ---- 2. attention: this warp's steps (one page each) s = w, w + 8, ... of each unit, then the

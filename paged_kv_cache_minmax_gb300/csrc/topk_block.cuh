@@ -66,6 +66,25 @@ __device__ __forceinline__ uint32_t topk_order_key(float f)
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// the float of an order key
+__device__ __forceinline__ float topk_key_float(uint32_t k)
+{
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// Clears what block_topk(..., range) expects cleared: the histogram, the winner bitmask and the
+// candidate count.  A caller that knows the scores' range ahead calls it before the scores are
+// complete (every thread of the group); the group syncs at its end.
+template <int THREADS, class Group = CtaGroup>
+__device__ __forceinline__ void block_topk_prepare(BlockTopkShared<THREADS>& ts)
+{
+    const int tid = static_cast<int>(threadIdx.x) - Group::kFirst;
+    for (int i = tid; i < kTopkBins; i += THREADS) ts.hist[i] = 0;
+    for (int i = tid; i < 256; i += THREADS) ts.rhist[i] = 0;
+    if (tid == 0) ts.ncand = 0;
+    Group::sync();
+}
+
 // Exact top-K over the P scores in sc[] by 4 radix passes; writes sel[0..K) ascending.
 template <int THREADS, class Group = CtaGroup>
 __device__ __noinline__ void block_radix_topk(const float* sc, int P, int K, int32_t* sel, BlockTopkShared<THREADS>& ts)
@@ -166,7 +185,7 @@ __device__ __noinline__ void block_radix_topk(const float* sc, int P, int K, int
 // threshold, same result.
 template <int THREADS, class Group = CtaGroup>
 __device__ __noinline__ int block_topk_reg(const float* scores, int P, int K, int32_t* sel, float* sc,
-                              BlockTopkShared<THREADS>& ts)
+                              BlockTopkShared<THREADS>& ts, const uint32_t* range)
 {
     constexpr int kPer = 8;
     constexpr int kWarps = THREADS / 32;
@@ -182,35 +201,42 @@ __device__ __noinline__ int block_topk_reg(const float* scores, int P, int K, in
         const int i = i0 + e;
         v[e] = i < P ? (scores != nullptr ? __ldcg(scores + i) : sc[i]) : 0.f;
     }
-    float lo = FLT_MAX, hi = -FLT_MAX;
-#pragma unroll
-    for (int e = 0; e < kPer; ++e) {
-        if (i0 + e < P) {
-            if (scores != nullptr) sc[i0 + e] = v[e];  // the ranking and the radix path read them here
-            lo = fminf(lo, v[e]);
-            hi = fmaxf(hi, v[e]);
-        }
-    }
-    for (int i = tid; i < kTopkBins; i += THREADS) ts.hist[i] = 0;
     uint32_t* winbits = reinterpret_cast<uint32_t*>(ts.rhist);  // bit i: page i of the threshold bin wins
     static_assert(8 * THREADS / 32 <= 256, "the winner bitmask fits the radix histogram");
-    for (int i = tid; i < 8 * THREADS / 32; i += THREADS) winbits[i] = 0u;
-    if (tid == 0) ts.ncand = 0;
+    float mn, mx;
+    if (range != nullptr) {  // known range; block_topk_prepare has cleared the histogram and the bitmask
+        mn = topk_key_float(range[0]);
+        mx = topk_key_float(range[1]);
+    } else {
+        float lo = FLT_MAX, hi = -FLT_MAX;
 #pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) {
-        lo = fminf(lo, __shfl_xor_sync(kFullMask, lo, off));
-        hi = fmaxf(hi, __shfl_xor_sync(kFullMask, hi, off));
-    }
-    if (lane == 0) {
-        ts.wmin[warp] = lo;
-        ts.wmax[warp] = hi;
-    }
-    Group::sync();
-    float mn = ts.wmin[0], mx = ts.wmax[0];
+        for (int e = 0; e < kPer; ++e) {
+            if (i0 + e < P) {
+                if (scores != nullptr) sc[i0 + e] = v[e];  // the ranking and the radix path read them here
+                lo = fminf(lo, v[e]);
+                hi = fmaxf(hi, v[e]);
+            }
+        }
+        for (int i = tid; i < kTopkBins; i += THREADS) ts.hist[i] = 0;
+        for (int i = tid; i < 8 * THREADS / 32; i += THREADS) winbits[i] = 0u;
+        if (tid == 0) ts.ncand = 0;
 #pragma unroll
-    for (int w = 1; w < kWarps; ++w) {
-        mn = fminf(mn, ts.wmin[w]);
-        mx = fmaxf(mx, ts.wmax[w]);
+        for (int off = 16; off >= 1; off >>= 1) {
+            lo = fminf(lo, __shfl_xor_sync(kFullMask, lo, off));
+            hi = fmaxf(hi, __shfl_xor_sync(kFullMask, hi, off));
+        }
+        if (lane == 0) {
+            ts.wmin[warp] = lo;
+            ts.wmax[warp] = hi;
+        }
+        Group::sync();
+        mn = ts.wmin[0];
+        mx = ts.wmax[0];
+#pragma unroll
+        for (int w = 1; w < kWarps; ++w) {
+            mn = fminf(mn, ts.wmin[w]);
+            mx = fmaxf(mx, ts.wmax[w]);
+        }
     }
     if (!(mx > mn)) {  // every score equal: the K lowest pages win the ties
         for (int i = tid; i < K; i += THREADS) sel[i] = i;
@@ -316,10 +342,13 @@ __device__ __noinline__ int block_topk_reg(const float* scores, int P, int K, in
 // L2; or null when sc[] already holds them) into sel[] (shared or global
 // memory) and returns the count, min(K, P).  sc (P floats) and bin (P int16)
 // are shared-memory scratch.  Every thread of the group must call it; sel[]
-// is complete for every thread of the group on return.
+// is complete for every thread of the group on return.  `range`, if not
+// null, holds the order keys (topk_order_key) of the scores' minimum and
+// maximum, and block_topk_prepare ran before: the selection then skips its
+// own range pass.
 template <int THREADS, class Group = CtaGroup>
 __device__ __noinline__ int block_topk(const float* scores, int P, int K, int32_t* sel, float* sc, int16_t* bin,
-                          BlockTopkShared<THREADS>& ts)
+                          BlockTopkShared<THREADS>& ts, const uint32_t* range = nullptr)
 {
     constexpr int kWarps = THREADS / 32;
     const int tid = static_cast<int>(threadIdx.x) - Group::kFirst;
@@ -330,7 +359,8 @@ __device__ __noinline__ int block_topk(const float* scores, int P, int K, int32_
         Group::sync();
         return P;
     }
-    if (P <= 8 * THREADS) return block_topk_reg<THREADS, Group>(scores, P, K, sel, sc, ts);
+    if (P <= 8 * THREADS) return block_topk_reg<THREADS, Group>(scores, P, K, sel, sc, ts, range);
+    // (the general path below finds the range itself)
 
     // 1. scores to shared memory (16 loads in flight per thread), their range, an empty histogram
     constexpr int kBatch = 16;
