@@ -276,7 +276,14 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
         u.ufull = (static_cast<size_t>(u.b) * p.L + p.layer) * p.Hkv + u.h;
         const int cap = p.Pmax * T;
         const bool first_of_batch = rank == 0 && u.h == 0;  // reports a batch's range errors once
+        // the four loads are independent: issue them together (an absent array reads seq_len, unused)
+        const int* tbp = p.new_k != nullptr ? p.tok_begin + u.b : p.seq_len + u.b;
+        const int* tep = p.new_k != nullptr ? p.tok_end + u.b : p.seq_len + u.b;
+        const uint8_t* mkp = p.rescore_mask != nullptr ? p.rescore_mask + p.layer * p.Hkv + u.h
+                                                       : reinterpret_cast<const uint8_t*>(p.seq_len + u.b);
         int seq = p.seq_len[u.b];
+        const int tb_in = *tbp, te_in = *tep;
+        const uint8_t mk_in = *mkp;
         if (seq < 0 || seq > cap) {
             if (first_of_batch) report(p.err, KVMM_ERR_OUT_OF_RANGE);
             seq = seq < 0 ? 0 : cap;
@@ -285,10 +292,10 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
         u.P = (seq + T - 1) / T;
         u.lo = static_cast<int>(static_cast<long long>(u.P) * rank / C);
         u.hi = static_cast<int>(static_cast<long long>(u.P) * (rank + 1) / C);
-        u.rescored = p.rescore_mask == nullptr || p.rescore_mask[p.layer * p.Hkv + u.h] != 0;
+        u.rescored = p.rescore_mask == nullptr || mk_in != 0;
         u.tb = u.te = u.pb = u.pe = 0;
         if (p.new_k != nullptr) {
-            const int tb = p.tok_begin[u.b], te = p.tok_end[u.b];
+            const int tb = tb_in, te = te_in;
             if (first_of_batch && (tb < 0 || te < tb || tb > cap || te > cap || te - tb > p.n_new))
                 report(p.err, KVMM_ERR_OUT_OF_RANGE);
             if (tb >= 0 && te >= tb && tb <= cap) {
