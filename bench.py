@@ -278,6 +278,12 @@ def gpu_arm(args):
     splits = kvmm.auto_splits(kvmm.make_shape(cfg.B, L, cfg.Hq, cfg.Hkv, cfg.D, cfg.T, cfg.Pmax, cfg.K,
                                               wl.n_phys))
     st = DecodeState.for_workload(wl, num_splits=splits)
+    if args.path == "decode_layer":
+        launch_shape = {"units_per_cluster": 2,
+                        "cluster_ctas": kvmm.decode_layer_cluster(kvmm.make_shape(
+                            cfg.B, L, cfg.Hq, cfg.Hkv, cfg.D, cfg.T, cfg.Pmax, cfg.K, wl.n_phys))}
+    else:
+        launch_shape = {"splits": splits}
     st.build_metadata()
     nk, nv = workloads.step_tokens(wl, 0)
     # the current token sits at position seq_len - 1 and is rewritten every step
@@ -295,6 +301,11 @@ def gpu_arm(args):
     path = args.path
     fused = path != "unfused"  # one timed launch group per layer (decode_layer, or scoring + attention)
 
+    def decode_layer_call(l):
+        kvmm.decode_layer(st.shape, l, q_dev[l], nk_dev[l], nv_dev[l], 1, st.tok_begin, st.seq_len,
+                          st.k_pool, st.v_pool, st.block_table, st.meta, st.seq_len, None, st.K, st.sel_idx,
+                          st.sel_cnt, st.out[l], lse=st.lse[l], err=st.err, workspace=st.workspace)
+
     def step(instrument):
         main = torch.cuda.current_stream()
         for l in range(L):
@@ -304,9 +315,7 @@ def gpu_arm(args):
             if instrument:
                 ev_s[4 * l].record()
             if path == "decode_layer":  # append, score, select and attend in one launch
-                kvmm.decode_layer(st.shape, l, q_dev[l], nk_dev[l], nv_dev[l], 1, st.tok_begin, st.seq_len,
-                                  st.k_pool, st.v_pool, st.block_table, st.meta, st.seq_len, None, st.K, st.sel_idx,
-                                  st.sel_cnt, st.out[l], lse=st.lse[l], err=st.err, workspace=st.workspace)
+                decode_layer_call(l)
             elif path == "fused":  # scoring, then attention that selects its own pages
                 st.select_attend(l, q_dev[l])
             else:
@@ -383,6 +392,26 @@ def gpu_arm(args):
         with torch.cuda.stream(stream):
             step(True)
         stream.synchronize()
+    # the dominant kernel alone, in the bench's launch configuration: the L decode_layer launches of a step
+    # back to back in one graph (no event between launches, so programmatic dependent launch still lets
+    # each launch's CTAs be scheduled while its predecessor drains); per launch = region / launches
+    dl_ms = None
+    if path == "decode_layer" and not args.no_graph:
+        g_dl = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_dl, stream=stream):
+            for l in range(L):
+                decode_layer_call(l)
+        reps = max(3, min(args.steps, 100))
+        d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                g_dl.replay()
+            d0.record()
+            for _ in range(reps):
+                g_dl.replay()
+            d1.record()
+        stream.synchronize()
+        dl_ms = d0.elapsed_time(d1) / (reps * L)
     score_ms = [ev_s[4 * l].elapsed_time(ev_s[4 * l + 1]) for l in range(L)]
     attn_ms = [ev_s[4 * l + 2].elapsed_time(ev_s[4 * l + 3]) for l in range(L)] if not fused else [0.0]
 
@@ -430,8 +459,8 @@ def gpu_arm(args):
     peak, peak_kind = peaks()
     s_ms, a_ms = statistics.mean(score_ms), statistics.mean(attn_ms)
     if path == "decode_layer":
-        dom, dom_ms, dom_bytes = "decode_layer", s_ms, acc["decode_launch"]
-        kernel_ms = {"decode_layer": s_ms}
+        dom, dom_ms, dom_bytes = "decode_layer", (dl_ms if dl_ms is not None else s_ms), acc["decode_launch"]
+        kernel_ms = {"decode_layer": dom_ms, "decode_layer_event_bracketed": s_ms}
     elif fused:
         dom, dom_ms, dom_bytes = "page_score_topk_attn", s_ms, acc["fused_launch"]
         kernel_ms = {"page_score_topk_attn": s_ms}
@@ -451,7 +480,7 @@ def gpu_arm(args):
         "data": "synthetic (seeded; stands in for Llama-3.1-8B long-context decode)",
         "config": {"workload": cfg.name, "layers": L, "global_batch": cfg.B * world, "seq_len": cfg.S,
                    "q_heads": cfg.Hq, "kv_heads": cfg.Hkv, "head_dim": cfg.D, "page_tokens": cfg.T,
-                   "top_k_pages": cfg.K, "splits": splits, "parallelism": f"replicas x{world}",
+                   "top_k_pages": cfg.K, **launch_shape, "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (4 GiB of distinct data per step, no flush)",
                    "step": f"one decode step = {L} layer-steps, " + ("eager launches" if args.no_graph
                                                                      else "CUDA graph replay"),
@@ -466,8 +495,11 @@ def gpu_arm(args):
                      "frac": achieved / peak, "traffic": traffic, "kernel": dom,
                      "peak_source": f"{peak_kind} hbm_gbs (burst copy)",
                      "achieved_bytes_per_launch": dom_bytes, "launch_ms": dom_ms,
-                     "launch_timing": "CUDA events around each launch in the last timed step"
-                                      if external else "CUDA events, eager instrumented step after timing"},
+                     "launch_timing": (f"CUDA events around {L}-launch graph replays of decode_layer alone, "
+                                       "back to back; per launch = region / launches"
+                                       if dl_ms is not None else
+                                       "CUDA events around each launch in the last timed step"
+                                       if external else "CUDA events, eager instrumented step after timing")},
         "e2e": {"value": e2e_steps * L * world / (e2e_ms / 1e3), "unit": "layer-steps/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "how": "pinned host q/new K,V -> device, graph replay, out/lse/promoted counts -> pinned host"},

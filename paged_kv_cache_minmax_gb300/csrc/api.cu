@@ -106,6 +106,13 @@ int32_t kvmm_auto_splits(const kvmm_shape* shape)
     return resolve_splits(*shape, 0);
 }
 
+int32_t kvmm_decode_layer_cluster(const kvmm_shape* shape)
+{
+    if (check_shape(shape) != KVMM_OK) return 0;
+    const int C = kvmm::decode_layer_cluster(*shape);
+    return kvmm::decode_layer_smem(shape->D, shape->T, shape->Pmax, shape->Kmax, C) > 220 * 1024 ? 0 : C;
+}
+
 size_t kvmm_workspace_size(const kvmm_shape* shape, int32_t num_splits)
 {
     if (check_shape(shape) != KVMM_OK || num_splits < 0) return 0;

@@ -680,10 +680,12 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
             const int npg = min(kPiece, hi - page0);
             if (lane == 0) mbar_arrive_expect_tx(&sh.full[w][b2], static_cast<uint32_t>(npg) * kRowBytes);
             __syncwarp();
-            if (8 * lane < npg) {  // lane i copies rows 8i .. 8i+7
-                const int rows = min(8, npg - 8 * lane);
-                bulk_copy_g2s_hint(my_ring + size_t(b2) * kSlot + size_t(8 * lane) * kRowBytes,
-                                   p.meta + (ufull * p.Pmax + page0 + 8 * lane) * 2 * D,
+            // each slot has its own copying lanes: a thread's bulk copies complete one after another
+            const int cl = lane - (kPiece / 8) * b2;
+            if (cl >= 0 && 8 * cl < npg) {  // lane cl copies rows 8cl .. 8cl+7
+                const int rows = min(8, npg - 8 * cl);
+                bulk_copy_g2s_hint(my_ring + size_t(b2) * kSlot + size_t(8 * cl) * kRowBytes,
+                                   p.meta + (ufull * p.Pmax + page0 + 8 * cl) * 2 * D,
                                    static_cast<uint32_t>(rows) * kRowBytes, &sh.full[w][b2], stream_policy);
             }
             set_slot(b2, j, sl);
@@ -988,10 +990,11 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
         auto issue_att = [&](int b2, int j, int s) {  // step s of unit j: page s of this CTA's share
             if (lane == 0) mbar_arrive_expect_tx(&sh.full[w][b2], 2u * kPageBytes);
             __syncwarp();
-            if (lane < 2) {  // lane 0 copies the page's keys, lane 1 its values
-                uint8_t* dst = my_ring + size_t(b2) * kSlot + lane * kPageBytes;
+            const int cl = lane - 2 * b2;  // the slot's own copying lanes, as for the scores
+            if (cl == 0 || cl == 1) {  // lane cl = 0 copies the page's keys, cl = 1 its values
+                uint8_t* dst = my_ring + size_t(b2) * kSlot + cl * kPageBytes;
                 const size_t off = static_cast<size_t>(res[size_t(j) * p.maxp + s].x) * T * D;
-                bulk_copy_g2s_hint(dst, (lane ? p.v_pool : p.k_pool) + off, kPageBytes, &sh.full[w][b2],
+                bulk_copy_g2s_hint(dst, (cl ? p.v_pool : p.k_pool) + off, kPageBytes, &sh.full[w][b2],
                                    stream_policy);
             }
             set_slot(b2, j, s);
@@ -1126,15 +1129,54 @@ size_t decode_layer_smem(int D, int T, int Pmax, int Kmax, int C)
     return d_layout(D, T, Pmax, Kmax, C, maxp).total;
 }
 
+// CTAs per cluster: as many as the SMs allow for one wave of all the launch's clusters.  Clusters are
+// placed within a GPC, so SMs / clusters can overestimate; the occupancy query decides (a launch whose
+// clusters do not all fit at once runs in two waves).  The query must leave room for an eighth more
+// clusters: with programmatic dependent launch the next launch's first clusters take the SMs this one
+// leaves free before it ends, and a launch that needs every cluster place the GPU has was measured to
+// run part of its grid in a second wave.  Cached per device and shape.
 int decode_layer_cluster(const kvmm_shape& s)
 {
+    struct Choice {
+        int dev, D, T, Pmax, Kmax, units, C;
+    };
+    static thread_local Choice cache[8] = {};
+    static thread_local int next = 0;
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
+    const int units = s.B * s.Hkv;
+    for (const auto& c : cache)
+        if (c.C > 0 && c.dev == dev && c.D == s.D && c.T == s.T && c.Pmax == s.Pmax && c.Kmax == s.Kmax &&
+            c.units == units)
+            return c.C;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const int clusters = (s.B * s.Hkv + kDUnits - 1) / kDUnits;
+    const int clusters = (units + kDUnits - 1) / kDUnits;
     int c = sms / clusters;
     if (c > kDMaxCluster) c = kDMaxCluster;
     if (c < 1) c = 1;
+    void (*kernel)(DecodeParams) = decode_kernel_for(s.D, s.T, 0);  // both reductions: same resources
+    for (; c > 1; --c) {
+        const size_t smem = decode_layer_smem(s.D, s.T, s.Pmax, s.Kmax, c);
+        if (prepare_decode(kernel, smem) != cudaSuccess) break;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(clusters * c));
+        cfg.blockDim = dim3(kDThreads);
+        cfg.dynamicSmemBytes = smem;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = static_cast<unsigned>(c);
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) {
+            cudaGetLastError();
+            continue;
+        }
+        if (n >= clusters + (clusters + 7) / 8) break;
+    }
+    cache[next++ % 8] = {dev, s.D, s.T, s.Pmax, s.Kmax, units, c};
     return c;
 }
 

@@ -82,8 +82,9 @@ struct AttnParams {
     int32_t* err;
 };
 
-// one-launch decode layer (decode_layer.cu): a cluster of C CTAs per two units
-constexpr int kDMaxCluster = 8;
+// one-launch decode layer (decode_layer.cu): a cluster of C CTAs per two units (C up to the
+// non-portable cluster size 16)
+constexpr int kDMaxCluster = 16;
 struct DecodeParams {
     int32_t B, L, Hq, Hkv, G, D, T, Pmax, Kmax, layer, K;
     int32_t C;      // CTAs per cluster
