@@ -764,26 +764,31 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
                 if (16 * grp < npg) {
                     const uint8_t* ra = slot + static_cast<size_t>(16 * grp + gid) * kRowBytes;
                     const uint8_t* rb = ra + 8 * kRowBytes;
+                    // four independent accumulation chains (even / odd r, low / high half of the chunk); the scoring
+                    // kernels of every path sum them in this same order, so their scores agree bit for bit
                     float c[4] = {0.f, 0.f, 0.f, 0.f}, c2[4] = {0.f, 0.f, 0.f, 0.f};
+                    float c3[4] = {0.f, 0.f, 0.f, 0.f}, c4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                     for (int r = 0; r < kR; ++r) {
                         const uint4 ka = ld_shared_v4(ra + 16 * (4 * r + tig));
                         const uint4 kb = ld_shared_v4(rb + 16 * (4 * r + tig));
-                        mma_bf16_16816(c, ka.x, kb.x, ka.y, kb.y, wf[r][0], wf[r][1]);
-                        mma_bf16_16816(c2, ka.z, kb.z, ka.w, kb.w, wf[r][2], wf[r][3]);
+                        mma_bf16_16816((r & 1) ? c3 : c, ka.x, kb.x, ka.y, kb.y, wf[r][0], wf[r][1]);
+                        mma_bf16_16816((r & 1) ? c4 : c2, ka.z, kb.z, ka.w, kb.w, wf[r][2], wf[r][3]);
                     }
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) c[i] = (c[i] + c3[i]) + (c2[i] + c4[i]);
                     float s_lo, s_hi;
                     if (MODE == 0) {
-                        s_lo = (c[0] + c2[0]) + (c[1] + c2[1]);
-                        s_hi = (c[2] + c2[2]) + (c[3] + c2[3]);
+                        s_lo = c[0] + c[1];
+                        s_hi = c[2] + c[3];
                         s_lo += __shfl_xor_sync(kFullMask, s_lo, 1);
                         s_hi += __shfl_xor_sync(kFullMask, s_hi, 1);
                         s_lo += __shfl_xor_sync(kFullMask, s_lo, 2);
                         s_hi += __shfl_xor_sync(kFullMask, s_hi, 2);
                     } else {
                         const bool h0 = 2 * tig < G, h1 = 2 * tig + 1 < G;
-                        s_lo = fmaxf(h0 ? c[0] + c2[0] : -FLT_MAX, h1 ? c[1] + c2[1] : -FLT_MAX);
-                        s_hi = fmaxf(h0 ? c[2] + c2[2] : -FLT_MAX, h1 ? c[3] + c2[3] : -FLT_MAX);
+                        s_lo = fmaxf(h0 ? c[0] : -FLT_MAX, h1 ? c[1] : -FLT_MAX);
+                        s_hi = fmaxf(h0 ? c[2] : -FLT_MAX, h1 ? c[3] : -FLT_MAX);
                         s_lo = fmaxf(s_lo, __shfl_xor_sync(kFullMask, s_lo, 1));
                         s_hi = fmaxf(s_hi, __shfl_xor_sync(kFullMask, s_hi, 1));
                         s_lo = fmaxf(s_lo, __shfl_xor_sync(kFullMask, s_lo, 2));
@@ -859,36 +864,61 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
             for (int jj = 0; jj < kSub; ++jj) {
                 const uint8_t* ra = ks + (ua0 + 4 * jj) * (2 * D);
                 const uint8_t* rb = ra + 2 * (2 * D);
+                // four independent accumulation chains (even / odd r, low / high half of the chunk)
                 float c[4] = {0.f, 0.f, 0.f, 0.f}, c2[4] = {0.f, 0.f, 0.f, 0.f};
+                float c3[4] = {0.f, 0.f, 0.f, 0.f}, c4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int r = 0; r < D / 32; ++r) {
                     const uint4 ka = ld_shared_v4(ra + 16 * (4 * r + tig));
                     const uint4 kb = ld_shared_v4(rb + 16 * (4 * r + tig));
-                    mma_bf16_16816(c, ka.x, kb.x, ka.y, kb.y, qf[r][0], qf[r][1]);
-                    mma_bf16_16816(c2, ka.z, kb.z, ka.w, kb.w, qf[r][2], qf[r][3]);
+                    mma_bf16_16816((r & 1) ? c3 : c, ka.x, kb.x, ka.y, kb.y, qf[r][0], qf[r][1]);
+                    mma_bf16_16816((r & 1) ? c4 : c2, ka.z, kb.z, ka.w, kb.w, qf[r][2], qf[r][3]);
                 }
 #pragma unroll
-                for (int i = 0; i < 4; ++i) x[jj][i] = (c[i] + c2[i]) * p.scale_log2;
+                for (int i = 0; i < 4; ++i) x[jj][i] = ((c[i] + c3[i]) + (c2[i] + c4[i])) * p.scale_log2;
                 if (!full) {
                     if (ua0 + 4 * jj >= nv) x[jj][0] = x[jj][1] = -INFINITY;
                     if (ua0 + 4 * jj + 2 >= nv) x[jj][2] = x[jj][3] = -INFINITY;
                 }
             }
+            // this lane's largest scores of its two heads
             float mx0 = fmaxf(x[0][0], x[0][2]), mx1 = fmaxf(x[0][1], x[0][3]);
 #pragma unroll
             for (int jj = 1; jj < kSub; ++jj) {
                 mx0 = fmaxf(mx0, fmaxf(x[jj][0], x[jj][2]));
                 mx1 = fmaxf(mx1, fmaxf(x[jj][1], x[jj][3]));
             }
+            // The probabilities are taken against a reference per head (m0, m1): kept from the earlier steps
+            // while no score of this step exceeds it by more than kSlack (one vote instead of a reduction),
+            // else raised to the running maximum, with the sums so far rescaled.  A probability is then at
+            // most 2^kSlack, which the fp32 sums and the bf16 hi + lo split carry to the same precision;
+            // (m, l, O) stay consistent, which is all the merge and lse use.
+            constexpr float kSlack = 8.f;
+            if (!__all_sync(kFullMask, mx0 <= m0 + kSlack && mx1 <= m1 + kSlack)) {
 #pragma unroll
-            for (int off = 4; off < 32; off <<= 1) {
-                mx0 = fmaxf(mx0, __shfl_xor_sync(kFullMask, mx0, off));
-                mx1 = fmaxf(mx1, __shfl_xor_sync(kFullMask, mx1, off));
+                for (int off = 4; off < 32; off <<= 1) {
+                    mx0 = fmaxf(mx0, __shfl_xor_sync(kFullMask, mx0, off));
+                    mx1 = fmaxf(mx1, __shfl_xor_sync(kFullMask, mx1, off));
+                }
+                const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+                const float a0 = mn0 == -INFINITY ? 1.f : fast_exp2(m0 - mn0);
+                const float a1 = mn1 == -INFINITY ? 1.f : fast_exp2(m1 - mn1);
+                l0 *= a0;
+                l1 *= a1;
+                if (__any_sync(kFullMask, (a0 != 1.f) || (a1 != 1.f))) {
+#pragma unroll
+                    for (int i = 0; i < kMTiles; ++i) {
+                        o[i][0] *= a0;
+                        o[i][1] *= a1;
+                        o[i][2] *= a0;
+                        o[i][3] *= a1;
+                    }
+                }
+                m0 = mn0;
+                m1 = mn1;
             }
-            const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-            const float ref0 = mn0 == -INFINITY ? 0.f : mn0;
-            const float ref1 = mn1 == -INFINITY ? 0.f : mn1;
-            const float a0 = fast_exp2(m0 - ref0), a1 = fast_exp2(m1 - ref1);
+            const float ref0 = m0 == -INFINITY ? 0.f : m0;
+            const float ref1 = m1 == -INFINITY ? 0.f : m1;
             float pr[kSub][4];
             float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
@@ -898,19 +928,8 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
                 ps0 += pr[jj][0] + pr[jj][2];
                 ps1 += pr[jj][1] + pr[jj][3];
             }
-            l0 = fmaf(l0, a0, ps0);
-            l1 = fmaf(l1, a1, ps1);
-            m0 = mn0;
-            m1 = mn1;
-            if (__any_sync(kFullMask, (a0 != 1.f) || (a1 != 1.f))) {
-#pragma unroll
-                for (int i = 0; i < kMTiles; ++i) {
-                    o[i][0] *= a0;
-                    o[i][1] *= a1;
-                    o[i][2] *= a0;
-                    o[i][3] *= a1;
-                }
-            }
+            l0 += ps0;
+            l1 += ps1;
             uint32_t bh[kSub][2], bl[kSub][2];
 #pragma unroll
             for (int jj = 0; jj < kSub; ++jj) {

@@ -192,27 +192,32 @@ __global__ void __launch_bounds__(kScoreThreads) score_pages_kernel(const ScoreP
             // C[page][head] over this warp's 16 pages: rows gid and gid + 8
             const uint8_t* ra = st + static_cast<size_t>(pg0 + gid) * kRowBytes;
             const uint8_t* rb = ra + 8 * kRowBytes;
+            // four independent accumulation chains (even / odd r, low / high half of the chunk); the scoring
+            // kernels of every path sum them in this same order, so their scores agree bit for bit
             float c[4] = {0.f, 0.f, 0.f, 0.f}, c2[4] = {0.f, 0.f, 0.f, 0.f};
+            float c3[4] = {0.f, 0.f, 0.f, 0.f}, c4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int r = 0; r < kR; ++r) {
                 const uint4 ka = ld_shared_v4(ra + 16 * (4 * r + tig));
                 const uint4 kb = ld_shared_v4(rb + 16 * (4 * r + tig));
-                mma_bf16_16816(c, ka.x, kb.x, ka.y, kb.y, wf[r][0], wf[r][1]);
-                mma_bf16_16816(c2, ka.z, kb.z, ka.w, kb.w, wf[r][2], wf[r][3]);
+                mma_bf16_16816((r & 1) ? c3 : c, ka.x, kb.x, ka.y, kb.y, wf[r][0], wf[r][1]);
+                mma_bf16_16816((r & 1) ? c4 : c2, ka.z, kb.z, ka.w, kb.w, wf[r][2], wf[r][3]);
             }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) c[i] = (c[i] + c3[i]) + (c2[i] + c4[i]);
             // c: [page gid][head 2tig], [gid][2tig+1], [gid+8][2tig], [gid+8][2tig+1]
             float s_lo, s_hi;
             if (MODE == 0) {
-                s_lo = (c[0] + c2[0]) + (c[1] + c2[1]);
-                s_hi = (c[2] + c2[2]) + (c[3] + c2[3]);
+                s_lo = c[0] + c[1];
+                s_hi = c[2] + c[3];
                 s_lo += __shfl_xor_sync(kFullMask, s_lo, 1);
                 s_hi += __shfl_xor_sync(kFullMask, s_hi, 1);
                 s_lo += __shfl_xor_sync(kFullMask, s_lo, 2);
                 s_hi += __shfl_xor_sync(kFullMask, s_hi, 2);
             } else {
                 const bool h0 = 2 * tig < p.G, h1 = 2 * tig + 1 < p.G;
-                s_lo = fmaxf(h0 ? c[0] + c2[0] : -FLT_MAX, h1 ? c[1] + c2[1] : -FLT_MAX);
-                s_hi = fmaxf(h0 ? c[2] + c2[2] : -FLT_MAX, h1 ? c[3] + c2[3] : -FLT_MAX);
+                s_lo = fmaxf(h0 ? c[0] : -FLT_MAX, h1 ? c[1] : -FLT_MAX);
+                s_hi = fmaxf(h0 ? c[2] : -FLT_MAX, h1 ? c[3] : -FLT_MAX);
                 s_lo = fmaxf(s_lo, __shfl_xor_sync(kFullMask, s_lo, 1));
                 s_hi = fmaxf(s_hi, __shfl_xor_sync(kFullMask, s_hi, 1));
                 s_lo = fmaxf(s_lo, __shfl_xor_sync(kFullMask, s_lo, 2));

@@ -296,51 +296,65 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const AttnPar
         for (int j = 0; j < 2; ++j) {
             const uint8_t* ra = ks + (ua0 + 4 * j) * (2 * D);
             const uint8_t* rb = ra + 2 * (2 * D);
+            // four independent accumulation chains (even / odd r, low / high half of the chunk)
             float c[4] = {0.f, 0.f, 0.f, 0.f}, c2[4] = {0.f, 0.f, 0.f, 0.f};
+            float c3[4] = {0.f, 0.f, 0.f, 0.f}, c4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int r = 0; r < D / 32; ++r) {
                 const uint4 ka = ld_shared_v4(ra + 16 * (4 * r + tig));
                 const uint4 kb = ld_shared_v4(rb + 16 * (4 * r + tig));
-                mma_bf16_16816(c, ka.x, kb.x, ka.y, kb.y, qf[r][0], qf[r][1]);
-                mma_bf16_16816(c2, ka.z, kb.z, ka.w, kb.w, qf[r][2], qf[r][3]);
+                mma_bf16_16816((r & 1) ? c3 : c, ka.x, kb.x, ka.y, kb.y, qf[r][0], qf[r][1]);
+                mma_bf16_16816((r & 1) ? c4 : c2, ka.z, kb.z, ka.w, kb.w, qf[r][2], qf[r][3]);
             }
 #pragma unroll
-            for (int i = 0; i < 4; ++i) x[j][i] = (c[i] + c2[i]) * p.scale_log2;
+            for (int i = 0; i < 4; ++i) x[j][i] = ((c[i] + c3[i]) + (c2[i] + c4[i])) * p.scale_log2;
             if (!full) {
                 if (!valid(ua0 + 4 * j)) x[j][0] = x[j][1] = -INFINITY;
                 if (!valid(ua0 + 4 * j + 2)) x[j][2] = x[j][3] = -INFINITY;
             }
         }
         // x[j]: [row gid][head 2tig], [gid][2tig+1], [gid+8][2tig], [gid+8][2tig+1]
+        // this lane's largest scores of its two heads
         float mx0 = fmaxf(fmaxf(x[0][0], x[0][2]), fmaxf(x[1][0], x[1][2]));
         float mx1 = fmaxf(fmaxf(x[0][1], x[0][3]), fmaxf(x[1][1], x[1][3]));
+        // The probabilities are taken against a reference per head (m0, m1): kept from the earlier steps
+        // while no score of this step exceeds it by more than kSlack (one vote instead of a reduction),
+        // else raised to the running maximum, with the sums so far rescaled.  A probability is then at
+        // most 2^kSlack, which the fp32 sums and the bf16 hi + lo split carry to the same precision;
+        // (m, l, O) stay consistent, which is all the merge and lse use.
+        constexpr float kSlack = 8.f;
+        if (!__all_sync(kFullMask, mx0 <= m0 + kSlack && mx1 <= m1 + kSlack)) {
 #pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-            mx0 = fmaxf(mx0, __shfl_xor_sync(kFullMask, mx0, off));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(kFullMask, mx1, off));
+            for (int off = 4; off < 32; off <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(kFullMask, mx0, off));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(kFullMask, mx1, off));
+            }
+            const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+            const float a0 = mn0 == -INFINITY ? 1.f : fast_exp2(m0 - mn0);
+            const float a1 = mn1 == -INFINITY ? 1.f : fast_exp2(m1 - mn1);
+            l0 *= a0;
+            l1 *= a1;
+            if (__any_sync(kFullMask, (a0 != 1.f) || (a1 != 1.f))) {
+#pragma unroll
+                for (int i = 0; i < kMTiles; ++i) {
+                    o[i][0] *= a0;
+                    o[i][1] *= a1;
+                    o[i][2] *= a0;
+                    o[i][3] *= a1;
+                }
+            }
+            m0 = mn0;
+            m1 = mn1;
         }
-        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-        const float ref0 = mn0 == -INFINITY ? 0.f : mn0;
-        const float ref1 = mn1 == -INFINITY ? 0.f : mn1;
-        const float a0 = fast_exp2(m0 - ref0), a1 = fast_exp2(m1 - ref1);
+        const float ref0 = m0 == -INFINITY ? 0.f : m0;
+        const float ref1 = m1 == -INFINITY ? 0.f : m1;
         float pr[2][4];
 #pragma unroll
         for (int j = 0; j < 2; ++j)
 #pragma unroll
             for (int i = 0; i < 4; ++i) pr[j][i] = fast_exp2(x[j][i] - ((i & 1) ? ref1 : ref0));
-        l0 = fmaf(l0, a0, (pr[0][0] + pr[0][2]) + (pr[1][0] + pr[1][2]));
-        l1 = fmaf(l1, a1, (pr[0][1] + pr[0][3]) + (pr[1][1] + pr[1][3]));
-        m0 = mn0;
-        m1 = mn1;
-        if (__any_sync(kFullMask, (a0 != 1.f) || (a1 != 1.f))) {
-#pragma unroll
-            for (int i = 0; i < kMTiles; ++i) {
-                o[i][0] *= a0;
-                o[i][1] *= a1;
-                o[i][2] *= a0;
-                o[i][3] *= a1;
-            }
-        }
+        l0 += (pr[0][0] + pr[0][2]) + (pr[1][0] + pr[1][2]);
+        l1 += (pr[0][1] + pr[0][3]) + (pr[1][1] + pr[1][3]);
 
         // ---- P^T as bf16 hi + lo B fragments (k order = the token order above)
         uint32_t bh[2][2], bl[2][2];
