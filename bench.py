@@ -218,7 +218,7 @@ def reference_arm(args):
     import oracle
 
     oracle.build()
-    cfg = CFG
+    cfg = workloads.CONFIGS[args.config]
     threads = os.cpu_count() or 1
     units = cfg.B * cfg.Hkv
     states = oracle_layer_sample(cfg, units)
@@ -269,21 +269,29 @@ def gpu_arm(args):
     kbuild.build_library()
     kvmm.load()
 
-    cfg = CFG
+    cfg = workloads.CONFIGS[args.config]
     if args.batch or args.layers:
         cfg = workloads.scaled(cfg, B=args.batch or cfg.B, L=args.layers or cfg.L)
-    L = cfg.L
+    L = cfg.L_alloc  # a step rotates over the allocated layers
     # replicas: every rank decodes its own batch (seeded per rank); no collective on the data path
     wl = workloads.generate(cfg, device="cuda", seed=cfg.seed + 7919 * rank)
     splits = kvmm.auto_splits(kvmm.make_shape(cfg.B, L, cfg.Hq, cfg.Hkv, cfg.D, cfg.T, cfg.Pmax, cfg.K,
                                               wl.n_phys))
     st = DecodeState.for_workload(wl, num_splits=splits)
+    one_launch = True  # decode_layer runs its one-launch kernel (else its two-kernel fallback)
     if args.path == "decode_layer":
-        launch_shape = {"units_per_cluster": 2,
-                        "cluster_ctas": kvmm.decode_layer_cluster(kvmm.make_shape(
-                            cfg.B, L, cfg.Hq, cfg.Hkv, cfg.D, cfg.T, cfg.Pmax, cfg.K, wl.n_phys))}
+        c_ctas = kvmm.decode_layer_cluster(kvmm.make_shape(cfg.B, L, cfg.Hq, cfg.Hkv, cfg.D, cfg.T, cfg.Pmax,
+                                                           cfg.K, wl.n_phys))
+        one_launch = c_ctas > 0
+        launch_shape = ({"units_per_cluster": 2, "cluster_ctas": c_ctas} if one_launch else
+                        {"splits": splits, "decode_layer": "falls back to kv_minmax_update + page_score_topk_attn "
+                                                           "(per-CTA buffers exceed shared memory)"})
     else:
         launch_shape = {"splits": splits}
+    # the rerank schedule: with an unstable share, a step rescores every unit every `rerank_period` steps and
+    # only the unstable heads' units otherwise (the others keep their selection)
+    mask_unstable = wl.unstable.contiguous() if cfg.unstable_frac > 0 else None
+    period = cfg.rerank_period if mask_unstable is not None else 1
     st.build_metadata()
     nk, nv = workloads.step_tokens(wl, 0)
     # the current token sits at position seq_len - 1 and is rewritten every step
@@ -301,12 +309,12 @@ def gpu_arm(args):
     path = args.path
     fused = path != "unfused"  # one timed launch group per layer (decode_layer, or scoring + attention)
 
-    def decode_layer_call(l):
+    def decode_layer_call(l, mask=None):
         kvmm.decode_layer(st.shape, l, q_dev[l], nk_dev[l], nv_dev[l], 1, st.tok_begin, st.seq_len,
-                          st.k_pool, st.v_pool, st.block_table, st.meta, st.seq_len, None, st.K, st.sel_idx,
+                          st.k_pool, st.v_pool, st.block_table, st.meta, st.seq_len, mask, st.K, st.sel_idx,
                           st.sel_cnt, st.out[l], lse=st.lse[l], err=st.err, workspace=st.workspace)
 
-    def step(instrument):
+    def step(instrument, mask=None):
         main = torch.cuda.current_stream()
         for l in range(L):
             if path != "decode_layer":
@@ -315,17 +323,17 @@ def gpu_arm(args):
             if instrument:
                 ev_s[4 * l].record()
             if path == "decode_layer":  # append, score, select and attend in one launch
-                decode_layer_call(l)
+                decode_layer_call(l, mask)
             elif path == "fused":  # scoring, then attention that selects its own pages
-                st.select_attend(l, q_dev[l])
+                st.select_attend(l, q_dev[l], rescore_mask=mask)
             else:
-                st.select(l, q_dev[l])
+                st.select(l, q_dev[l], rescore_mask=mask)
             if instrument:
                 ev_s[4 * l + 1].record()
             forks[l].record(main)
             side.wait_event(forks[l])
             with torch.cuda.stream(side):
-                st.diff(l)
+                st.diff(l, rescore_mask=mask)
             if not fused:
                 if instrument:
                     ev_s[4 * l + 2].record()
@@ -349,17 +357,25 @@ def gpu_arm(args):
         graph, graph_instr = _Eager(), None
     else:
         graph = torch.cuda.CUDAGraph()
+        external = external and period == 1  # with a rerank schedule the roofline uses the graph below
         graph_instr = torch.cuda.CUDAGraph() if external else None
         with torch.cuda.graph(graph, stream=stream):
             step(False)
+        if mask_unstable is not None:  # the steps between reranks: only the unstable heads rescore
+            graph_u = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph_u, stream=stream):
+                step(False, mask_unstable)
         if external:
             with torch.cuda.graph(graph_instr, stream=stream):
                 step(True)
     st.err.zero_()
 
+    def replay(i):  # step i of the rerank schedule
+        (graph if i % period == 0 or args.no_graph else graph_u).replay()
+
     with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
-            graph.replay()
+        for i in range(args.warmup):
+            replay(i)
     stream.synchronize()
 
     # ---- timed region (device-resident inputs) --------------------------------
@@ -377,7 +393,7 @@ def gpu_arm(args):
                 if external and i == args.steps - 1:
                     graph_instr.replay()  # the last step also stamps every kernel launch
                 else:
-                    graph.replay()
+                    replay(i)
             t1.record()
         stream.synchronize()
     torch.cuda.synchronize()
@@ -430,11 +446,11 @@ def gpu_arm(args):
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         e0.record()
-        for _ in range(e2e_steps):
+        for i in range(e2e_steps):
             q_dev.copy_(q_host, non_blocking=True)
             nk_dev.copy_(nk_host, non_blocking=True)
             nv_dev.copy_(nv_host, non_blocking=True)
-            graph.replay()
+            replay(i)
             out_host.copy_(st.out, non_blocking=True)
             lse_host.copy_(st.lse, non_blocking=True)
             prom_host.copy_(st.promoted_cnt, non_blocking=True)
@@ -451,7 +467,10 @@ def gpu_arm(args):
             dist.destroy_process_group()
         return
 
-    acc = algorithmic_bytes(cfg)
+    acc = acc_all = algorithmic_bytes(cfg)
+    if mask_unstable is not None:  # average over the schedule: every unit on a rerank step, else the unstable
+        n_u = float(wl.unstable.sum()) * cfg.B / L
+        acc = algorithmic_bytes(cfg, rescored_units=(cfg.B * cfg.Hkv + (period - 1) * n_u) / period)
     n_ls = args.steps * L * world
     secs = ms_total / 1e3
     value = n_ls / secs
@@ -459,15 +478,15 @@ def gpu_arm(args):
     peak, peak_kind = peaks()
     s_ms, a_ms = statistics.mean(score_ms), statistics.mean(attn_ms)
     if path == "decode_layer":
-        dom, dom_ms, dom_bytes = "decode_layer", (dl_ms if dl_ms is not None else s_ms), acc["decode_launch"]
+        dom, dom_ms, dom_bytes = "decode_layer", (dl_ms if dl_ms is not None else s_ms), acc_all["decode_launch"]
         kernel_ms = {"decode_layer": dom_ms, "decode_layer_event_bracketed": s_ms}
     elif fused:
-        dom, dom_ms, dom_bytes = "page_score_topk_attn", s_ms, acc["fused_launch"]
+        dom, dom_ms, dom_bytes = "page_score_topk_attn", s_ms, acc_all["fused_launch"]
         kernel_ms = {"page_score_topk_attn": s_ms}
     else:
         dom = "sparse_attn_kernel" if a_ms >= s_ms else "score_topk_kernel"
         dom_ms = max(a_ms, s_ms)
-        dom_bytes = acc["attn_launch"] if a_ms >= s_ms else acc["score_launch"]
+        dom_bytes = acc_all["attn_launch"] if a_ms >= s_ms else acc_all["score_launch"]
         kernel_ms = {"score_topk_kernel": s_ms, "sparse_attn_kernel": a_ms}
     kernel_ms["per_layer_step_ms"] = ms_total / args.steps / L
     achieved = dom_bytes / (dom_ms / 1e3) / 1e9
@@ -481,7 +500,8 @@ def gpu_arm(args):
         "config": {"workload": cfg.name, "layers": L, "global_batch": cfg.B * world, "seq_len": cfg.S,
                    "q_heads": cfg.Hq, "kv_heads": cfg.Hkv, "head_dim": cfg.D, "page_tokens": cfg.T,
                    "top_k_pages": cfg.K, **launch_shape, "parallelism": f"replicas x{world}",
-                   "l2": "inputs larger than L2 (4 GiB of distinct data per step, no flush)",
+                   "l2": f"inputs larger than L2 ({L * (acc_all['meta'] + acc_all['kv']) / 2**30:.1f} GiB of distinct "
+                         "data per step, no flush)",
                    "step": f"one decode step = {L} layer-steps, " + ("eager launches" if args.no_graph
                                                                      else "CUDA graph replay"),
                    "path": {"decode_layer": "decode_layer (append, score, select, attend: one launch)",
@@ -505,7 +525,7 @@ def gpu_arm(args):
                 "how": "pinned host q/new K,V -> device, graph replay, out/lse/promoted counts -> pinned host"},
         # per layer: decode_layer, diff; or update, score, selecting attention, diff (fused); or update,
         # score, top-K, diff, attention (unfused)
-        "gpu_launches": {"decode_layer": 2, "fused": 4, "unfused": 5}[path] * L * args.steps,
+        "gpu_launches": {"decode_layer": 2 if one_launch else 4, "fused": 4, "unfused": 5}[path] * L * args.steps,
         "clocks": clk,
         "device_err": err_word,
     }
@@ -806,6 +826,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="kvmm", choices=["kvmm", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--config", type=int, default=2, choices=sorted(workloads.CONFIGS),
+                    help="workload (default: the 8B-shape 32K-context decode step)")
     ap.add_argument("--no-graph", action="store_true", help="launch eagerly (for profilers)")
     ap.add_argument("--batch", type=int, default=0, help="override the batch (smaller profiling case)")
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (smaller profiling case)")

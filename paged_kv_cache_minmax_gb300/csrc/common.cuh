@@ -146,6 +146,10 @@ __device__ __forceinline__ void cluster_sync()
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// the two halves of cluster_sync, for work that needs neither in between
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+
 // load a float from the shared memory of CTA `rank` of the cluster, at the
 // address that `local` has in this CTA's shared memory
 __device__ __forceinline__ float ld_dsmem_f32(const void* local, uint32_t rank)

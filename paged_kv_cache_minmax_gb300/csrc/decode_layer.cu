@@ -243,7 +243,9 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
         sh.abort_flag = 0;
         fence_barrier_init();
     }
-    cluster_sync();  // every CTA's barriers exist before the first remote arrival
+    // every CTA's barriers exist before the first remote arrival: the cluster barrier is passed before
+    // anything reaches another CTA, and meanwhile the queries and the unit descriptors are fetched
+    cluster_arrive();
     pdl_launch_dependents();
     pdl_wait();  // every input may come from the preceding kernels
 
@@ -311,7 +313,9 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
         }
         sh.ud[tid] = u;
     }
-    __syncthreads();
+    __syncwarp();  // converged for the aligned barrier
+    cluster_wait();
+    __syncthreads();  // the descriptors above
 
     if (warp >= kDSel0) {
         // ================= selectors =======================================
