@@ -110,7 +110,10 @@ int32_t kvmm_decode_layer_cluster(const kvmm_shape* shape)
 {
     if (check_shape(shape) != KVMM_OK) return 0;
     const int C = kvmm::decode_layer_cluster(*shape);
-    return kvmm::decode_layer_smem(shape->D, shape->T, shape->Pmax, shape->Kmax, C) > 220 * 1024 ? 0 : C;
+    return kvmm::decode_layer_smem(shape->D, shape->T, shape->Pmax, shape->Kmax, C, shape->Hq / shape->Hkv) >
+                   kvmm::kDSmemLimit
+               ? 0
+               : C;
 }
 
 size_t kvmm_workspace_size(const kvmm_shape* shape, int32_t num_splits)
@@ -464,7 +467,7 @@ kvmm_status decode_layer(const kvmm_shape* shape, int32_t layer, const kvmm_bf16
         return KVMM_INVALID_ARG;
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     const int C = kvmm::decode_layer_cluster(s);
-    if (kvmm::decode_layer_smem(s.D, s.T, s.Pmax, s.Kmax, C) > 220 * 1024) {
+    if (kvmm::decode_layer_smem(s.D, s.T, s.Pmax, s.Kmax, C, s.Hq / s.Hkv) > kvmm::kDSmemLimit) {
         // the one-launch kernel's buffers do not fit: append, then the two-kernel call
         if (workspace == nullptr || workspace_bytes < score_ws_bytes(s)) return KVMM_WORKSPACE_TOO_SMALL;
         if (new_k != nullptr) {

@@ -82,6 +82,7 @@ struct DUnit {
 struct DecodeShared {
     uint64_t full[kDCons][kDRingMax];  // a consumer warp's slot has landed
     uint64_t qbar;            // the query groups of the cluster's units
+    uint64_t btbar;           // the units' block-table rows are in btab (bt_smem)
     uint64_t sbar[kDUnits];   // all of the unit's scores and its range are here (asynchronous remote stores
                               // and reductions, 4 bytes each)
     uint64_t selr[kDUnits];   // this CTA's share of the unit's pages is resolved
@@ -163,11 +164,12 @@ __device__ __forceinline__ bool mbar_wait_sleepy(uint64_t* bar, uint32_t parity,
 
 // the shared-memory plan, identical on host and device
 struct DLayout {
-    size_t ring, part, qbuf, sbuf, bins, ts, selv, res, recv, total;
+    size_t ring, part, qbuf, sbuf, bins, ts, selv, res, recv, btab, total;
     int pstride, slice, recv_stride;
 };
 __host__ __device__ inline size_t d_align(size_t n) { return (n + 127) & ~static_cast<size_t>(127); }
-__host__ __device__ inline DLayout d_layout(int D, int T, int Pmax, int Kmax, int C, int maxp)
+// bt: the units' block-table rows are copied to shared memory (btab), for the selection's page lookups
+__host__ __device__ inline DLayout d_layout(int D, int T, int Pmax, int Kmax, int C, int maxp, int G, bool bt)
 {
     DLayout l{};
     l.pstride = (Pmax + 3) & ~3;
@@ -175,14 +177,15 @@ __host__ __device__ inline DLayout d_layout(int D, int T, int Pmax, int Kmax, in
     l.recv_stride = 16 * C + l.slice * C;
     l.ring = 0;
     l.part = d_align(l.ring + size_t(kDCons) * d_ring(T) * 4 * T * D);
-    l.qbuf = d_align(l.part + size_t(kDCons) * 8 * (D + 4) * sizeof(float));
+    l.qbuf = d_align(l.part + size_t(kDCons) * G * (D + 4) * sizeof(float));
     l.sbuf = d_align(l.qbuf + size_t(kDUnits) * 8 * D * 2);
     l.bins = d_align(l.sbuf + size_t(kDUnits) * l.pstride * sizeof(float));
     l.ts = d_align(l.bins + size_t(Pmax) * sizeof(int16_t));
     l.selv = d_align(l.ts + sizeof(BlockTopkShared<kDSelThreads>));
     l.res = d_align(l.selv + size_t(Kmax) * sizeof(int32_t));
     l.recv = d_align(l.res + size_t(kDUnits) * maxp * 2 * sizeof(int32_t));
-    l.total = d_align(l.recv + size_t(kDUnits) * l.recv_stride * sizeof(float));
+    l.btab = d_align(l.recv + size_t(kDUnits) * l.recv_stride * sizeof(float));
+    l.total = d_align(l.btab + (bt ? size_t(kDUnits) * Pmax * sizeof(int32_t) : 0));
     return l;
 }
 
@@ -204,7 +207,7 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
     __shared__ DecodeShared sh;
 
     const int C = p.C;
-    const DLayout lay = d_layout(D, T, p.Pmax, p.Kmax, C, p.maxp);
+    const DLayout lay = d_layout(D, T, p.Pmax, p.Kmax, C, p.maxp, p.G, p.bt_smem != 0);
     uint8_t* rings = smem + lay.ring;
     float* part = reinterpret_cast<float*>(smem + lay.part);
     uint8_t* qbuf = smem + lay.qbuf;
@@ -214,6 +217,7 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
     int32_t* selv = reinterpret_cast<int32_t*>(smem + lay.selv);
     int2* res = reinterpret_cast<int2*>(smem + lay.res);
     float* recv = reinterpret_cast<float*>(smem + lay.recv);
+    int32_t* btab = reinterpret_cast<int32_t*>(smem + lay.btab);
 
     const int tid = threadIdx.x;
     const int lane = tid & 31;
@@ -229,6 +233,7 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
         for (int w = 0; w < kDCons; ++w)
             for (int b2 = 0; b2 < kDRingMax; ++b2) mbar_init(&sh.full[w][b2], 1);
         mbar_init(&sh.qbar, 1);
+        mbar_init(&sh.btbar, 1);
         for (int j = 0; j < kDUnits; ++j) {
             mbar_init(&sh.sbar[j], 1);
             mbar_init(&sh.selr[j], 1);
@@ -325,9 +330,16 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
         constexpr int kRowsPerPass = 32 / kLanesPerRow;
         const int sub = lane % kLanesPerRow;
         if (stid == 0 && (p.Pmax & 3) == 0) {
-            // the units' block-table rows, read when this CTA's share of the selection is resolved
-            for (int j = 0; j < nunits; ++j)
-                prefetch_l2(p.block_table + sh.ud[j].ufull * p.Pmax, static_cast<uint32_t>(p.Pmax) * 4u);
+            // the units' block-table rows, read when this CTA's share of the selection is resolved: into
+            // shared memory when there is room, else into L2
+            const uint32_t row = static_cast<uint32_t>(p.Pmax) * 4u;
+            if (p.bt_smem) mbar_arrive_expect_tx(&sh.btbar, row * nunits);
+            for (int j = 0; j < nunits; ++j) {
+                if (p.bt_smem)
+                    bulk_copy_g2s(btab + size_t(j) * p.Pmax, p.block_table + sh.ud[j].ufull * p.Pmax, row, &sh.btbar);
+                else
+                    prefetch_l2(p.block_table + sh.ud[j].ufull * p.Pmax, row);
+            }
         }
         if (stid == 0) {
             // the bytes this CTA receives: every score of a rescored unit (one float a page) and from every
@@ -487,6 +499,8 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
             }
             const int beg = static_cast<int>(static_cast<long long>(cnt) * rank / C);
             const int end = static_cast<int>(static_cast<long long>(cnt) * (rank + 1) / C);
+            // the rows in shared memory have long landed by now; after a time-out the table is read directly
+            const bool bt_here = p.bt_smem && mbar_wait_bounded(&sh.btbar, 0, aborting() ? kDAbortNs : kDWaitNs);
             int2* rl = res + size_t(j) * p.maxp;
             int nres = 0;
             for (int i0 = beg; i0 < end; i0 += kDSelThreads) {
@@ -498,7 +512,7 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
                     if (lp < 0 || lp >= u.P) {
                         report(p.err, KVMM_ERR_OUT_OF_RANGE);
                     } else {
-                        const int32_t ph = p.block_table[u.ufull * p.Pmax + lp];
+                        const int32_t ph = bt_here ? btab[size_t(j) * p.Pmax + lp] : p.block_table[u.ufull * p.Pmax + lp];
                         if (ph < 0) {
                             report(p.err, KVMM_ERR_NULL_BLOCK);
                         } else if (ph >= p.n_phys) {
@@ -557,7 +571,7 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
                 float O = 0.f;
 #pragma unroll
                 for (int ww = 0; ww < kDCons; ++ww)
-                    O = fmaf(sh.fw[ww][g], part[size_t(ww) * 8 * (D + 4) + g * (D + 4) + (e - g * D)], O);
+                    O = fmaf(sh.fw[ww][g], part[size_t(ww) * G * (D + 4) + g * (D + 4) + (e - g * D)], O);
                 const int r = e / lay.slice;
                 st_async_f32(rj + 16 * C + rank * lay.slice + (e - r * lay.slice), &sh.rbar[j], static_cast<uint32_t>(r),
                              O);
@@ -1075,16 +1089,21 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
                 sh.ml[w][2 * tig] = l0;
                 sh.ml[w][2 * tig + 1] = l1;
             }
-            // [8 heads][D + 4]: the padding spreads the four tig lanes over distinct banks
-            float* mw = part + size_t(w) * 8 * (D + 4);
+            // [G heads][D + 4]: the padding spreads the four tig lanes over distinct banks
+            float* mw = part + size_t(w) * G * (D + 4);
+            const bool h0 = 2 * tig < G, h1 = 2 * tig + 1 < G;
 #pragma unroll
             for (int i = 0; i < kMTiles; ++i) {
                 float* w0 = mw + (2 * tig) * (D + 4);
                 float* w1 = w0 + (D + 4);
-                w0[16 * i + gid] = o[i][0];
-                w1[16 * i + gid] = o[i][1];
-                w0[16 * i + gid + 8] = o[i][2];
-                w1[16 * i + gid + 8] = o[i][3];
+                if (h0) {
+                    w0[16 * i + gid] = o[i][0];
+                    w0[16 * i + gid + 8] = o[i][2];
+                }
+                if (h1) {
+                    w1[16 * i + gid] = o[i][1];
+                    w1[16 * i + gid + 8] = o[i][3];
+                }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&sh.pready[j]);  // release: the partial above
@@ -1146,10 +1165,17 @@ cudaError_t prepare_decode(void (*kernel)(DecodeParams), size_t smem)
 
 }  // namespace
 
-size_t decode_layer_smem(int D, int T, int Pmax, int Kmax, int C)
+// the units' block-table rows go to shared memory when the launch still fits the limit with them
+bool decode_layer_bt(int D, int T, int Pmax, int Kmax, int C, int G)
 {
     const int maxp = (Kmax + C - 1) / C;
-    return d_layout(D, T, Pmax, Kmax, C, maxp).total;
+    return Pmax % 4 == 0 && d_layout(D, T, Pmax, Kmax, C, maxp, G, true).total <= kDSmemLimit;
+}
+
+size_t decode_layer_smem(int D, int T, int Pmax, int Kmax, int C, int G)
+{
+    const int maxp = (Kmax + C - 1) / C;
+    return d_layout(D, T, Pmax, Kmax, C, maxp, G, decode_layer_bt(D, T, Pmax, Kmax, C, G)).total;
 }
 
 // CTAs per cluster: as many as the SMs allow for one wave of all the launch's clusters.  Clusters are
@@ -1179,7 +1205,7 @@ int decode_layer_cluster(const kvmm_shape& s)
     if (c < 1) c = 1;
     void (*kernel)(DecodeParams) = decode_kernel_for(s.D, s.T, 0);  // both reductions: same resources
     for (; c > 1; --c) {
-        const size_t smem = decode_layer_smem(s.D, s.T, s.Pmax, s.Kmax, c);
+        const size_t smem = decode_layer_smem(s.D, s.T, s.Pmax, s.Kmax, c, s.Hq / s.Hkv);
         if (prepare_decode(kernel, smem) != cudaSuccess) break;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(static_cast<unsigned>(clusters * c));
@@ -1207,7 +1233,8 @@ cudaError_t launch_decode_layer(DecodeParams p, int group_reduce, cudaStream_t s
 {
     void (*kernel)(DecodeParams) = decode_kernel_for(p.D, p.T, group_reduce);
     p.maxp = (p.Kmax + p.C - 1) / p.C;
-    const size_t smem = decode_layer_smem(p.D, p.T, p.Pmax, p.Kmax, p.C);
+    p.bt_smem = decode_layer_bt(p.D, p.T, p.Pmax, p.Kmax, p.C, p.G) ? 1 : 0;
+    const size_t smem = decode_layer_smem(p.D, p.T, p.Pmax, p.Kmax, p.C, p.G);
     cudaError_t e = prepare_decode(kernel, smem);
     if (e != cudaSuccess) return e;
     const int clusters = (p.B * p.Hkv + kDUnits - 1) / kDUnits;
