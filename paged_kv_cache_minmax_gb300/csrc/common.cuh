@@ -185,6 +185,19 @@ __device__ __forceinline__ void st_async_f32(void* local, uint64_t* local_bar, u
                  : "memory");
 }
 
+// st_async_f32 of four consecutive floats (16 bytes of transaction); `local` 16-byte aligned
+__device__ __forceinline__ void st_async_v4_f32(void* local, uint64_t* local_bar, uint32_t rank, float a, float b,
+                                                float c, float d)
+{
+    uint32_t ra, rb;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_addr(local)), "r"(rank));
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rb) : "r"(smem_addr(local_bar)), "r"(rank));
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(ra),
+                 "r"(__float_as_uint(a)), "r"(__float_as_uint(b)), "r"(__float_as_uint(c)), "r"(__float_as_uint(d)),
+                 "r"(rb)
+                 : "memory");
+}
+
 // asynchronous atomic min (MAX = false) or max (MAX = true) of v into the
 // unsigned word at `local`'s address in CTA `rank` of the cluster, completing
 // 4 bytes of transaction on the mbarrier at `local_bar`'s address in that

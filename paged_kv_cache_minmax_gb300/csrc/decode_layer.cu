@@ -173,7 +173,7 @@ __host__ __device__ inline DLayout d_layout(int D, int T, int Pmax, int Kmax, in
 {
     DLayout l{};
     l.pstride = (Pmax + 3) & ~3;
-    l.slice = (8 * D + C - 1) / C;
+    l.slice = ((G * D + C - 1) / C + 3) & ~3;  // outputs a CTA combines: a multiple of 4 (16-byte stores)
     l.recv_stride = 16 * C + l.slice * C;
     l.ring = 0;
     l.part = d_align(l.ring + size_t(kDCons) * d_ring(T) * 4 * T * D);
@@ -566,15 +566,22 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
                 }
             }
             SelGroup::sync();
-            for (int e = stid; e < n_out; e += kDSelThreads) {
-                const int g = e / D;
-                float O = 0.f;
+            for (int e4 = 4 * stid; e4 < n_out; e4 += 4 * kDSelThreads) {  // four outputs of one head a thread
+                const int g = e4 / D;
+                float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-                for (int ww = 0; ww < kDCons; ++ww)
-                    O = fmaf(sh.fw[ww][g], part[size_t(ww) * G * (D + 4) + g * (D + 4) + (e - g * D)], O);
-                const int r = e / lay.slice;
-                st_async_f32(rj + 16 * C + rank * lay.slice + (e - r * lay.slice), &sh.rbar[j], static_cast<uint32_t>(r),
-                             O);
+                for (int ww = 0; ww < kDCons; ++ww) {
+                    const float f = sh.fw[ww][g];
+                    const float4 v =
+                        *reinterpret_cast<const float4*>(part + size_t(ww) * G * (D + 4) + g * (D + 4) + (e4 - g * D));
+                    O.x = fmaf(f, v.x, O.x);
+                    O.y = fmaf(f, v.y, O.y);
+                    O.z = fmaf(f, v.z, O.z);
+                    O.w = fmaf(f, v.w, O.w);
+                }
+                const int r = e4 / lay.slice;
+                st_async_v4_f32(rj + 16 * C + rank * lay.slice + (e4 - r * lay.slice), &sh.rbar[j],
+                                static_cast<uint32_t>(r), O.x, O.y, O.z, O.w);
             }
             SelGroup::sync();  // the consumer warps' partials are read
             if (stid == 0 && j + 1 < nunits) mbar_arrive(&sh.pfree);
