@@ -283,7 +283,9 @@ def gpu_arm(args):
         c_ctas = kvmm.decode_layer_cluster(kvmm.make_shape(cfg.B, L, cfg.Hq, cfg.Hkv, cfg.D, cfg.T, cfg.Pmax,
                                                            cfg.K, wl.n_phys))
         one_launch = c_ctas > 0
-        launch_shape = ({"units_per_cluster": 2, "cluster_ctas": c_ctas} if one_launch else
+        launch_shape = ({"units_per_cluster": kvmm.decode_layer_units(kvmm.make_shape(
+                             cfg.B, L, cfg.Hq, cfg.Hkv, cfg.D, cfg.T, cfg.Pmax, cfg.K, wl.n_phys)),
+                         "cluster_ctas": c_ctas} if one_launch else
                         {"splits": splits, "decode_layer": "falls back to kv_minmax_update + page_score_topk_attn "
                                                            "(per-CTA buffers exceed shared memory)"})
     else:

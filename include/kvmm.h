@@ -467,13 +467,16 @@ size_t kvmm_workspace_size(const kvmm_shape* shape, int32_t num_splits);
  * num_splits = 0 on the current device (0 for an unsupported shape). */
 int32_t kvmm_auto_splits(const kvmm_shape* shape);
 
-/* CTAs per thread-block cluster that decode_layer launches for this shape on
- * the current device: the most whose clusters (one per two (batch, KV head)
- * units) are all resident at once.  0 when decode_layer does not launch its
- * one-launch kernel for the shape (an unsupported shape, or per-CTA buffers
- * that do not fit shared memory; it then runs kv_minmax_update and
- * page_score_topk_attn). */
+/* The launch shape of decode_layer's one-launch kernel for this shape on the
+ * current device.  kvmm_decode_layer_units: (batch, KV head) units a cluster
+ * of CTAs takes, 2 when their buffers fit shared memory, else 1 (long
+ * sequences: the scores of a unit take 4 bytes a page).
+ * kvmm_decode_layer_cluster: CTAs per cluster, the most whose clusters are
+ * all resident at once.  Both are 0 when decode_layer does not launch that
+ * kernel for the shape (an unsupported shape, or buffers that do not fit
+ * even for one unit; it then runs kv_minmax_update and page_score_topk_attn). */
 int32_t kvmm_decode_layer_cluster(const kvmm_shape* shape);
+int32_t kvmm_decode_layer_units(const kvmm_shape* shape);
 
 /* Static text for a status code. */
 const char* kvmm_status_string(kvmm_status status);

@@ -109,11 +109,13 @@ int32_t kvmm_auto_splits(const kvmm_shape* shape)
 int32_t kvmm_decode_layer_cluster(const kvmm_shape* shape)
 {
     if (check_shape(shape) != KVMM_OK) return 0;
-    const int C = kvmm::decode_layer_cluster(*shape);
-    return kvmm::decode_layer_smem(shape->D, shape->T, shape->Pmax, shape->Kmax, C, shape->Hq / shape->Hkv) >
-                   kvmm::kDSmemLimit
-               ? 0
-               : C;
+    return kvmm::decode_layer_grid(*shape).c;
+}
+
+int32_t kvmm_decode_layer_units(const kvmm_shape* shape)
+{
+    if (check_shape(shape) != KVMM_OK) return 0;
+    return kvmm::decode_layer_grid(*shape).nu;
 }
 
 size_t kvmm_workspace_size(const kvmm_shape* shape, int32_t num_splits)
@@ -466,8 +468,8 @@ kvmm_status decode_layer(const kvmm_shape* shape, int32_t layer, const kvmm_bf16
         !opt4(err))
         return KVMM_INVALID_ARG;
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-    const int C = kvmm::decode_layer_cluster(s);
-    if (kvmm::decode_layer_smem(s.D, s.T, s.Pmax, s.Kmax, C, s.Hq / s.Hkv) > kvmm::kDSmemLimit) {
+    const kvmm::DecodeGrid grid = kvmm::decode_layer_grid(s);
+    if (grid.nu == 0) {
         // the one-launch kernel's buffers do not fit: append, then the two-kernel call
         if (workspace == nullptr || workspace_bytes < score_ws_bytes(s)) return KVMM_WORKSPACE_TOO_SMALL;
         if (new_k != nullptr) {
@@ -491,7 +493,8 @@ kvmm_status decode_layer(const kvmm_shape* shape, int32_t layer, const kvmm_bf16
     p.Kmax = s.Kmax;
     p.layer = layer;
     p.K = K;
-    p.C = C;
+    p.C = grid.c;
+    p.NU = grid.nu;
     p.n_new = new_k != nullptr ? n_new : 0;
     p.n_phys = s.n_phys;
     p.scale_log2 = (sm_scale > 0.f ? sm_scale : 1.0f / std::sqrt(static_cast<float>(s.D))) * 1.4426950408889634f;

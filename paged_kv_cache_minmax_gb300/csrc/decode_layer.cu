@@ -55,7 +55,7 @@ constexpr int kDSel0 = kDCons;                 // first selector warp
 constexpr int kDSelWarps = 8;
 constexpr int kDSelThreads = kDSelWarps * 32;
 constexpr int kDThreads = (kDCons + kDSelWarps) * 32;
-constexpr int kDUnits = 2;                     // units per cluster
+constexpr int kDUnits = 2;                     // units per cluster at most (DecodeParams::NU: 1 or 2)
 constexpr int kDSelBar = 1;                    // the selector warps' named barrier
 constexpr int kDRingMax = 2;
 
@@ -169,7 +169,7 @@ struct DLayout {
 };
 __host__ __device__ inline size_t d_align(size_t n) { return (n + 127) & ~static_cast<size_t>(127); }
 // bt: the units' block-table rows are copied to shared memory (btab), for the selection's page lookups
-__host__ __device__ inline DLayout d_layout(int D, int T, int Pmax, int Kmax, int C, int maxp, int G, bool bt)
+__host__ __device__ inline DLayout d_layout(int D, int T, int Pmax, int Kmax, int C, int maxp, int G, bool bt, int NU)
 {
     DLayout l{};
     l.pstride = (Pmax + 3) & ~3;
@@ -178,21 +178,22 @@ __host__ __device__ inline DLayout d_layout(int D, int T, int Pmax, int Kmax, in
     l.ring = 0;
     l.part = d_align(l.ring + size_t(kDCons) * d_ring(T) * 4 * T * D);
     l.qbuf = d_align(l.part + size_t(kDCons) * G * (D + 4) * sizeof(float));
-    l.sbuf = d_align(l.qbuf + size_t(kDUnits) * 8 * D * 2);
-    l.bins = d_align(l.sbuf + size_t(kDUnits) * l.pstride * sizeof(float));
+    l.sbuf = d_align(l.qbuf + size_t(NU) * 8 * D * 2);
+    l.bins = d_align(l.sbuf + size_t(NU) * l.pstride * sizeof(float));
     l.ts = d_align(l.bins + size_t(Pmax) * sizeof(int16_t));
     l.selv = d_align(l.ts + sizeof(BlockTopkShared<kDSelThreads>));
     l.res = d_align(l.selv + size_t(Kmax) * sizeof(int32_t));
-    l.recv = d_align(l.res + size_t(kDUnits) * maxp * 2 * sizeof(int32_t));
-    l.btab = d_align(l.recv + size_t(kDUnits) * l.recv_stride * sizeof(float));
-    l.total = d_align(l.btab + (bt ? size_t(kDUnits) * Pmax * sizeof(int32_t) : 0));
+    l.recv = d_align(l.res + size_t(NU) * maxp * 2 * sizeof(int32_t));
+    l.btab = d_align(l.recv + size_t(NU) * l.recv_stride * sizeof(float));
+    l.total = d_align(l.btab + (bt ? size_t(NU) * Pmax * sizeof(int32_t) : 0));
     return l;
 }
 
 // ---------------------------------------------------------------------------
-template <int D, int T, int MODE>
+template <int D, int T, int MODE, int NU>
 __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const DecodeParams p)
 {
+    static_assert(NU >= 1 && NU <= kDUnits, "units per cluster");
     constexpr int kSub = T / 16;                // 16-token sub-tiles of a page
     constexpr int kRing = d_ring(T);            // slots per consumer warp
     constexpr int kRowBytes = 4 * D;            // a page's [min | max] row
@@ -207,7 +208,7 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
     __shared__ DecodeShared sh;
 
     const int C = p.C;
-    const DLayout lay = d_layout(D, T, p.Pmax, p.Kmax, C, p.maxp, p.G, p.bt_smem != 0);
+    const DLayout lay = d_layout(D, T, p.Pmax, p.Kmax, C, p.maxp, p.G, p.bt_smem != 0, NU);
     uint8_t* rings = smem + lay.ring;
     float* part = reinterpret_cast<float*>(smem + lay.part);
     uint8_t* qbuf = smem + lay.qbuf;
@@ -225,7 +226,7 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
     const uint32_t rank = cluster_ctarank();
     const int cluster = blockIdx.x / C;
     const int U = p.B * p.Hkv;
-    const int nunits = min(kDUnits, U - cluster * kDUnits);
+    const int nunits = min(NU, U - cluster * NU);
     const int G = p.G;
     const int n_out = G * D;
 
@@ -269,7 +270,7 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
         const uint32_t qbytes = static_cast<uint32_t>(G) * D * 2;
         mbar_arrive_expect_tx(&sh.qbar, qbytes * nunits);
         for (int j = 0; j < nunits; ++j) {
-            const int wunit = cluster * kDUnits + j;
+            const int wunit = cluster * NU + j;
             const int b = wunit / p.Hkv, h = wunit - (wunit / p.Hkv) * p.Hkv;
             bulk_copy_g2s(qbuf + size_t(j) * 8 * D * 2,
                           p.q + (static_cast<size_t>(b) * p.Hq + static_cast<size_t>(h) * G) * D, qbytes, &sh.qbar);
@@ -277,7 +278,7 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
     }
     if (tid < nunits) {  // this CTA's view of unit tid
         DUnit u;
-        const int wunit = cluster * kDUnits + tid;
+        const int wunit = cluster * NU + tid;
         u.b = wunit / p.Hkv;
         u.h = wunit - u.b * p.Hkv;
         u.ufull = (static_cast<size_t>(u.b) * p.L + p.layer) * p.Hkv + u.h;
@@ -782,7 +783,7 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
         };
         auto score_slot = [&](const uint8_t* slot, int j, int page0, int npg) {
             float* sb = sbuf + size_t(j) * lay.pstride + page0;
-            float* orow = p.scores_out ? p.scores_out + static_cast<size_t>(cluster * kDUnits + j) * p.Pmax + page0
+            float* orow = p.scores_out ? p.scores_out + static_cast<size_t>(cluster * NU + j) * p.Pmax + page0
                                        : nullptr;
 #pragma unroll
             for (int grp = 0; grp < kSub; ++grp) {
@@ -1129,19 +1130,19 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
 }
 
 template <int D, int T, int MODE>
-void (*decode_kernel())(DecodeParams)
+void (*decode_kernel(int nu))(DecodeParams)
 {
-    return decode_layer_kernel<D, T, MODE>;
+    return nu == 1 ? decode_layer_kernel<D, T, MODE, 1> : decode_layer_kernel<D, T, MODE, 2>;
 }
 
-void (*decode_kernel_for(int D, int T, int mode))(DecodeParams)
+void (*decode_kernel_for(int D, int T, int mode, int nu))(DecodeParams)
 {
     if (D == 128) {
-        if (T == 16) return mode ? decode_kernel<128, 16, 1>() : decode_kernel<128, 16, 0>();
-        return mode ? decode_kernel<128, 32, 1>() : decode_kernel<128, 32, 0>();
+        if (T == 16) return mode ? decode_kernel<128, 16, 1>(nu) : decode_kernel<128, 16, 0>(nu);
+        return mode ? decode_kernel<128, 32, 1>(nu) : decode_kernel<128, 32, 0>(nu);
     }
-    if (T == 16) return mode ? decode_kernel<64, 16, 1>() : decode_kernel<64, 16, 0>();
-    return mode ? decode_kernel<64, 32, 1>() : decode_kernel<64, 32, 0>();
+    if (T == 16) return mode ? decode_kernel<64, 16, 1>(nu) : decode_kernel<64, 16, 0>(nu);
+    return mode ? decode_kernel<64, 32, 1>(nu) : decode_kernel<64, 32, 0>(nu);
 }
 
 // opt-ins of one instantiation, once per device and size
@@ -1173,78 +1174,85 @@ cudaError_t prepare_decode(void (*kernel)(DecodeParams), size_t smem)
 }  // namespace
 
 // the units' block-table rows go to shared memory when the launch still fits the limit with them
-bool decode_layer_bt(int D, int T, int Pmax, int Kmax, int C, int G)
+bool decode_layer_bt(int D, int T, int Pmax, int Kmax, int C, int G, int NU)
 {
     const int maxp = (Kmax + C - 1) / C;
-    return Pmax % 4 == 0 && d_layout(D, T, Pmax, Kmax, C, maxp, G, true).total <= kDSmemLimit;
+    return Pmax % 4 == 0 && d_layout(D, T, Pmax, Kmax, C, maxp, G, true, NU).total <= kDSmemLimit;
 }
 
-size_t decode_layer_smem(int D, int T, int Pmax, int Kmax, int C, int G)
+size_t decode_layer_smem(int D, int T, int Pmax, int Kmax, int C, int G, int NU)
 {
     const int maxp = (Kmax + C - 1) / C;
-    return d_layout(D, T, Pmax, Kmax, C, maxp, G, decode_layer_bt(D, T, Pmax, Kmax, C, G)).total;
+    return d_layout(D, T, Pmax, Kmax, C, maxp, G, decode_layer_bt(D, T, Pmax, Kmax, C, G, NU), NU).total;
 }
 
-// CTAs per cluster: as many as the SMs allow for one wave of all the launch's clusters.  Clusters are
+// Units per cluster and CTAs per cluster.  Two units a cluster when their buffers fit shared memory, else
+// one (long sequences: a unit's scores take 4 bytes a page), else none ({0, 0}: the two-kernel path).  The
+// cluster size is as many CTAs as the SMs allow for one wave of all the launch's clusters.  Clusters are
 // placed within a GPC, so SMs / clusters can overestimate; the occupancy query decides (a launch whose
 // clusters do not all fit at once runs in two waves).  The query must leave room for an eighth more
 // clusters: with programmatic dependent launch the next launch's first clusters take the SMs this one
 // leaves free before it ends, and a launch that needs every cluster place the GPU has was measured to
 // run part of its grid in a second wave.  Cached per device and shape.
-int decode_layer_cluster(const kvmm_shape& s)
+DecodeGrid decode_layer_grid(const kvmm_shape& s)
 {
     struct Choice {
-        int dev, D, T, Pmax, Kmax, units, C;
+        int dev, D, T, Pmax, Kmax, units, G;
+        DecodeGrid g;
     };
     static thread_local Choice cache[8] = {};
     static thread_local int next = 0;
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
-    const int units = s.B * s.Hkv;
+    const int units = s.B * s.Hkv, G = s.Hq / s.Hkv;
     for (const auto& c : cache)
-        if (c.C > 0 && c.dev == dev && c.D == s.D && c.T == s.T && c.Pmax == s.Pmax && c.Kmax == s.Kmax &&
-            c.units == units)
-            return c.C;
+        if (c.g.nu > 0 && c.dev == dev && c.D == s.D && c.T == s.T && c.Pmax == s.Pmax && c.Kmax == s.Kmax &&
+            c.units == units && c.G == G)
+            return c.g;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const int clusters = (units + kDUnits - 1) / kDUnits;
-    int c = sms / clusters;
-    if (c > kDMaxCluster) c = kDMaxCluster;
-    if (c < 1) c = 1;
-    void (*kernel)(DecodeParams) = decode_kernel_for(s.D, s.T, 0);  // both reductions: same resources
-    for (; c > 1; --c) {
-        const size_t smem = decode_layer_smem(s.D, s.T, s.Pmax, s.Kmax, c, s.Hq / s.Hkv);
-        if (prepare_decode(kernel, smem) != cudaSuccess) break;
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(static_cast<unsigned>(clusters * c));
-        cfg.blockDim = dim3(kDThreads);
-        cfg.dynamicSmemBytes = smem;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = static_cast<unsigned>(c);
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) {
-            cudaGetLastError();
-            continue;
+    DecodeGrid g{0, 0};
+    for (int nu = kDUnits; nu >= 1 && g.nu == 0; --nu) {
+        void (*kernel)(DecodeParams) = decode_kernel_for(s.D, s.T, 0, nu);  // both reductions: same resources
+        const int clusters = (units + nu - 1) / nu;
+        int c = sms / clusters;
+        if (c > kDMaxCluster) c = kDMaxCluster;
+        if (c < 1) c = 1;
+        for (; c > 1; --c) {
+            const size_t smem = decode_layer_smem(s.D, s.T, s.Pmax, s.Kmax, c, G, nu);
+            if (smem > kDSmemLimit || prepare_decode(kernel, smem) != cudaSuccess) continue;
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(static_cast<unsigned>(clusters * c));
+            cfg.blockDim = dim3(kDThreads);
+            cfg.dynamicSmemBytes = smem;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = static_cast<unsigned>(c);
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            int n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) {
+                cudaGetLastError();
+                continue;
+            }
+            if (n >= clusters + (clusters + 7) / 8) break;
         }
-        if (n >= clusters + (clusters + 7) / 8) break;
+        if (decode_layer_smem(s.D, s.T, s.Pmax, s.Kmax, c, G, nu) <= kDSmemLimit) g = {nu, c};
     }
-    cache[next++ % 8] = {dev, s.D, s.T, s.Pmax, s.Kmax, units, c};
-    return c;
+    if (g.nu > 0) cache[next++ % 8] = {dev, s.D, s.T, s.Pmax, s.Kmax, units, G, g};
+    return g;
 }
 
 cudaError_t launch_decode_layer(DecodeParams p, int group_reduce, cudaStream_t stream)
 {
-    void (*kernel)(DecodeParams) = decode_kernel_for(p.D, p.T, group_reduce);
+    void (*kernel)(DecodeParams) = decode_kernel_for(p.D, p.T, group_reduce, p.NU);
     p.maxp = (p.Kmax + p.C - 1) / p.C;
-    p.bt_smem = decode_layer_bt(p.D, p.T, p.Pmax, p.Kmax, p.C, p.G) ? 1 : 0;
-    const size_t smem = decode_layer_smem(p.D, p.T, p.Pmax, p.Kmax, p.C, p.G);
+    p.bt_smem = decode_layer_bt(p.D, p.T, p.Pmax, p.Kmax, p.C, p.G, p.NU) ? 1 : 0;
+    const size_t smem = decode_layer_smem(p.D, p.T, p.Pmax, p.Kmax, p.C, p.G, p.NU);
     cudaError_t e = prepare_decode(kernel, smem);
     if (e != cudaSuccess) return e;
-    const int clusters = (p.B * p.Hkv + kDUnits - 1) / kDUnits;
+    const int clusters = (p.B * p.Hkv + p.NU - 1) / p.NU;
     return launch_pdl_cluster(kernel, dim3(static_cast<unsigned>(clusters * p.C)), dim3(kDThreads), smem, stream,
                               static_cast<unsigned>(p.C), p);
 }

@@ -82,14 +82,15 @@ struct AttnParams {
     int32_t* err;
 };
 
-// one-launch decode layer (decode_layer.cu): a cluster of C CTAs per two units (C up to the
-// non-portable cluster size 16)
+// one-launch decode layer (decode_layer.cu): a cluster of C CTAs per NU units (C up to the non-portable
+// cluster size 16, NU 1 or 2)
 constexpr int kDMaxCluster = 16;
 struct DecodeParams {
     int32_t B, L, Hq, Hkv, G, D, T, Pmax, Kmax, layer, K;
     int32_t C;      // CTAs per cluster
     int32_t maxp;   // selected pages one CTA attends over at most: ceil(Kmax / C)
     int32_t bt_smem;  // 1: the units' block-table rows are copied to shared memory
+    int32_t NU;       // units per cluster: 1 or 2 (the kernel instantiation takes it too)
     int32_t n_new;  // appended tokens per batch entry (rows of new_k / new_v)
     int64_t n_phys;
     float scale_log2;  // sm_scale * log2(e)
@@ -260,8 +261,11 @@ cudaError_t launch_stability_rco(const StabilityParams& p, cudaStream_t stream);
 size_t stability_max_heads();  // largest L * Hkv the classification handles
 cudaError_t launch_decode_layer(DecodeParams p, int group_reduce, cudaStream_t stream);
 constexpr size_t kDSmemLimit = 220 * 1024;  // dynamic shared memory a decode_layer CTA may take
-size_t decode_layer_smem(int D, int T, int Pmax, int Kmax, int C, int G);  // dynamic shared memory of one CTA
-int decode_layer_cluster(const kvmm_shape& s);                 // CTAs per cluster for a shape
+struct DecodeGrid {
+    int nu;  // units per cluster (0: decode_layer takes the two-kernel path)
+    int c;   // CTAs per cluster
+};
+DecodeGrid decode_layer_grid(const kvmm_shape& s);  // the launch shape for a kvmm shape
 // the scoring kernel alone (page_score_topk without its selection kernel)
 cudaError_t launch_score_only(const ScoreParams& p, int group_reduce, cudaStream_t stream);
 cudaError_t launch_score_topk_mean(const ScoreParams& p, int group_reduce, cudaStream_t stream);  // mean-key rows

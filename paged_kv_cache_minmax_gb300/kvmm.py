@@ -20,7 +20,8 @@ ERR_NULL_BLOCK, ERR_OUT_OF_RANGE, ERR_TIMEOUT = 1, 2, 4
 NULL_BLOCK = -1
 
 EXPORTS = ("kv_minmax_update", "page_score_topk", "sparse_paged_decode_attn", "topk_promotion_diff",
-           "kvmm_workspace_size", "kvmm_auto_splits", "kvmm_decode_layer_cluster", "kvmm_status_string",
+           "kvmm_workspace_size", "kvmm_auto_splits", "kvmm_decode_layer_cluster", "kvmm_decode_layer_units",
+           "kvmm_status_string",
            "kvmm_last_cuda_error", "page_score_topk_static_scratch", "page_score_topk_attn", "decode_layer", "topk_history_record",
            "topk_stability_rco", "promote_pages", "block_table_update", "kv_meankey_update",
            "page_score_topk_mean")
@@ -96,6 +97,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.kvmm_auto_splits.restype = I32
     lib.kvmm_decode_layer_cluster.argtypes = [SP]
     lib.kvmm_decode_layer_cluster.restype = I32
+    lib.kvmm_decode_layer_units.argtypes = [SP]
+    lib.kvmm_decode_layer_units.restype = I32
     lib.kvmm_status_string.argtypes = [ctypes.c_int]
     lib.kvmm_status_string.restype = ctypes.c_char_p
     lib.kvmm_last_cuda_error.argtypes = []
@@ -146,6 +149,10 @@ def auto_splits(shape: Shape) -> int:
 
 def decode_layer_cluster(shape: Shape) -> int:
     return int(load().kvmm_decode_layer_cluster(ctypes.byref(shape)))
+
+
+def decode_layer_units(shape: Shape) -> int:
+    return int(load().kvmm_decode_layer_units(ctypes.byref(shape)))
 
 
 def alloc_workspace(shape: Shape, num_splits: int = 0, device="cuda") -> torch.Tensor:

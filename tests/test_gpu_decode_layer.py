@@ -187,16 +187,22 @@ def test_null_blocks_outside_the_selection_are_never_read():
     stats.check()
 
 
-def test_cluster_size_and_the_two_kernel_fallback():
-    """decode_layer's cluster size is one the device can hold, and a shape whose one-launch buffers exceed
-    shared memory (8192 pages a unit) runs the append and page_score_topk_attn instead, with the same results."""
+@pytest.mark.parametrize("pages", [8192, 12288])
+def test_launch_shape_and_long_units(pages):
+    """decode_layer's launch shape is one the device can hold: two units a cluster at the 8B shape, one
+    for a unit of 8192 pages (its scores no longer fit twice), and none at 12288 pages, where decode_layer
+    runs the append and page_score_topk_attn instead.  Either way it leaves what the separate calls leave."""
     bench_shape = kvmm.make_shape(8, 32, 32, 8, 128, 16, 2048, 128, 1)
+    assert kvmm.decode_layer_units(bench_shape) == 2
     assert 1 <= kvmm.decode_layer_cluster(bench_shape) <= 16
-    cfg = workloads.Config("long", B=1, L=1, Hq=4, Hkv=1, D=128, T=16, S=16 * 8192 - 3, K=96,
+    cfg = workloads.Config("long", B=1, L=1, Hq=4, Hkv=1, D=128, T=16, S=16 * pages - 3, K=96,
                            key_dist="outlier", n_planted=24, seed=83)
     a, b = twin_states(cfg)
     wl, st = a
-    assert kvmm.decode_layer_cluster(st.shape) == 0
+    if pages == 8192:
+        assert kvmm.decode_layer_units(st.shape) == 1 and kvmm.decode_layer_cluster(st.shape) >= 1
+    else:
+        assert kvmm.decode_layer_units(st.shape) == 0 and kvmm.decode_layer_cluster(st.shape) == 0
     nk, nv = workloads.step_tokens(wl, 0)
     sca, scb = run_both(a, b, 0, wl.q[0], nk[0], nv[0])
     assert st.read_err() == 0 and b[1].read_err() == 0
