@@ -360,50 +360,57 @@ __device__ __noinline__ int block_topk(const float* scores, int P, int K, int32_
         return P;
     }
     if (P <= 8 * THREADS) return block_topk_reg<THREADS, Group>(scores, P, K, sel, sc, ts, range);
-    // (the general path below finds the range itself)
 
-    // 1. scores to shared memory (16 loads in flight per thread), their range, an empty histogram
+    // 1. scores to shared memory (16 loads in flight per thread), their range, an empty histogram (a known
+    //    range: block_topk_prepare has emptied it, and the scores are in sc[] already)
     constexpr int kBatch = 16;
     float lo = FLT_MAX, hi = -FLT_MAX;
-    if (scores == nullptr) {
-        for (int i = tid; i < P; i += THREADS) {
-            lo = fminf(lo, sc[i]);
-            hi = fmaxf(hi, sc[i]);
-        }
-    }
-    for (int c0 = 0; scores != nullptr && c0 < P; c0 += THREADS * kBatch) {
-        float v[kBatch];
-#pragma unroll
-        for (int j = 0; j < kBatch; ++j) {
-            const int i = c0 + j * THREADS + tid;
-            v[j] = i < P ? __ldcg(scores + i) : 0.f;
-        }
-#pragma unroll
-        for (int j = 0; j < kBatch; ++j) {
-            const int i = c0 + j * THREADS + tid;
-            if (i < P) {
-                sc[i] = v[j];
-                lo = fminf(lo, v[j]);
-                hi = fmaxf(hi, v[j]);
+    float mn, mx;
+    if (range != nullptr && scores == nullptr) {
+        mn = topk_key_float(range[0]);
+        mx = topk_key_float(range[1]);
+    } else {
+        if (scores == nullptr) {
+            for (int i = tid; i < P; i += THREADS) {
+                lo = fminf(lo, sc[i]);
+                hi = fmaxf(hi, sc[i]);
             }
         }
-    }
-    for (int i = tid; i < kTopkBins; i += THREADS) ts.hist[i] = 0;
-    if (tid == 0) ts.ncand = 0;
+        for (int c0 = 0; scores != nullptr && c0 < P; c0 += THREADS * kBatch) {
+            float v[kBatch];
 #pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) {
-        lo = fminf(lo, __shfl_xor_sync(kFullMask, lo, off));
-        hi = fmaxf(hi, __shfl_xor_sync(kFullMask, hi, off));
-    }
-    if (lane == 0) {
-        ts.wmin[warp] = lo;
-        ts.wmax[warp] = hi;
-    }
-    Group::sync();
-    float mn = ts.wmin[0], mx = ts.wmax[0];
-    for (int w = 1; w < kWarps; ++w) {
-        mn = fminf(mn, ts.wmin[w]);
-        mx = fmaxf(mx, ts.wmax[w]);
+            for (int j = 0; j < kBatch; ++j) {
+                const int i = c0 + j * THREADS + tid;
+                v[j] = i < P ? __ldcg(scores + i) : 0.f;
+            }
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j) {
+                const int i = c0 + j * THREADS + tid;
+                if (i < P) {
+                    sc[i] = v[j];
+                    lo = fminf(lo, v[j]);
+                    hi = fmaxf(hi, v[j]);
+                }
+            }
+        }
+        for (int i = tid; i < kTopkBins; i += THREADS) ts.hist[i] = 0;
+        if (tid == 0) ts.ncand = 0;
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) {
+            lo = fminf(lo, __shfl_xor_sync(kFullMask, lo, off));
+            hi = fmaxf(hi, __shfl_xor_sync(kFullMask, hi, off));
+        }
+        if (lane == 0) {
+            ts.wmin[warp] = lo;
+            ts.wmax[warp] = hi;
+        }
+        Group::sync();
+        mn = ts.wmin[0];
+        mx = ts.wmax[0];
+        for (int w = 1; w < kWarps; ++w) {
+            mn = fminf(mn, ts.wmin[w]);
+            mx = fmaxf(mx, ts.wmax[w]);
+        }
     }
     if (!(mx > mn)) {  // every score equal: the K lowest pages win the ties
         for (int i = tid; i < K; i += THREADS) sel[i] = i;
