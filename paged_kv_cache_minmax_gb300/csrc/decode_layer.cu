@@ -83,6 +83,7 @@ struct DecodeShared {
     uint64_t full[kDCons][kDRingMax];  // a consumer warp's slot has landed
     uint64_t qbar;            // the query groups of the cluster's units
     uint64_t btbar;           // the units' block-table rows are in btab (bt_smem)
+    uint64_t cbar;            // two-level selection: every CTA's candidates are here
     uint64_t sbar[kDUnits];   // all of the unit's scores and its range are here (asynchronous remote stores
                               // and reductions, 4 bytes each)
     uint64_t selr[kDUnits];   // this CTA's share of the unit's pages is resolved
@@ -162,9 +163,16 @@ __device__ __forceinline__ bool mbar_wait_sleepy(uint64_t* bar, uint32_t parity,
     return true;
 }
 
+// Two-level selection: with one unit a cluster and more pages than one CTA's selection holds in registers,
+// each CTA selects the top K of the pages it scored, the cluster's candidates (at most C*K) are exchanged,
+// and each CTA selects the top K of those.  Every page of the unit's top K is in its own CTA's top K (fewer
+// than K pages of that share outrank it), and the candidates are packed in ascending page order, so the
+// result, ties to the lower page included, is the one-level selection's.
+__host__ __device__ inline bool d_two_level(int NU, int P, int C) { return NU == 1 && C > 1 && P > 8 * kDSelThreads; }
+
 // the shared-memory plan, identical on host and device
 struct DLayout {
-    size_t ring, part, qbuf, sbuf, bins, ts, selv, res, recv, btab, total;
+    size_t ring, part, qbuf, sbuf, bins, ts, selv, res, recv, btab, cand, total;
     int pstride, slice, recv_stride;
 };
 __host__ __device__ inline size_t d_align(size_t n) { return (n + 127) & ~static_cast<size_t>(127); }
@@ -185,7 +193,8 @@ __host__ __device__ inline DLayout d_layout(int D, int T, int Pmax, int Kmax, in
     l.res = d_align(l.selv + size_t(Kmax) * sizeof(int32_t));
     l.recv = d_align(l.res + size_t(NU) * maxp * 2 * sizeof(int32_t));
     l.btab = d_align(l.recv + size_t(NU) * l.recv_stride * sizeof(float));
-    l.total = d_align(l.btab + (bt ? size_t(NU) * Pmax * sizeof(int32_t) : 0));
+    l.cand = d_align(l.btab + (bt ? size_t(NU) * Pmax * sizeof(int32_t) : 0));
+    l.total = d_align(l.cand + (d_two_level(NU, Pmax, C) ? size_t(C) * Kmax * 8 : 0));
     return l;
 }
 
@@ -219,6 +228,8 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
     int2* res = reinterpret_cast<int2*>(smem + lay.res);
     float* recv = reinterpret_cast<float*>(smem + lay.recv);
     int32_t* btab = reinterpret_cast<int32_t*>(smem + lay.btab);
+    float* cand_s = reinterpret_cast<float*>(smem + lay.cand);  // two-level selection: C*Kmax scores, then pages
+    int32_t* cand_p = reinterpret_cast<int32_t*>(cand_s + size_t(C) * p.Kmax);
 
     const int tid = threadIdx.x;
     const int lane = tid & 31;
@@ -235,6 +246,7 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
             for (int b2 = 0; b2 < kDRingMax; ++b2) mbar_init(&sh.full[w][b2], 1);
         mbar_init(&sh.qbar, 1);
         mbar_init(&sh.btbar, 1);
+        mbar_init(&sh.cbar, 1);
         for (int j = 0; j < kDUnits; ++j) {
             mbar_init(&sh.sbar[j], 1);
             mbar_init(&sh.selr[j], 1);
@@ -350,6 +362,15 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
             // count negative; the pending arrival keeps the phase open until the count is set.
             const int e0 = static_cast<int>(rank) * lay.slice;
             const int own = max(0, min(n_out, e0 + lay.slice) - e0);
+            if (sh.ud[0].rescored && sh.ud[0].P > p.K && d_two_level(NU, sh.ud[0].P, C)) {
+                uint32_t n = 0;  // candidates: from every CTA min(K, pages it scored), 8 bytes each
+                for (int r = 0; r < C; ++r) {
+                    const int pr = static_cast<int>(static_cast<long long>(sh.ud[0].P) * (r + 1) / C) -
+                                   static_cast<int>(static_cast<long long>(sh.ud[0].P) * r / C);
+                    n += static_cast<uint32_t>(min(p.K, pr));
+                }
+                mbar_arrive_expect_tx(&sh.cbar, n * 8u);
+            }
             for (int j = 0; j < nunits; ++j) {
                 const DUnit& u = sh.ud[j];
                 mbar_arrive_expect_tx(&sh.sbar[j],
@@ -483,8 +504,32 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
                 // every score of the unit and its range are here (the histogram is cleared meanwhile)
                 block_topk_prepare<kDSelThreads, SelGroup>(ts);
                 if (!mbar_wait_sleepy(&sh.sbar[j], 0, aborting() ? kDAbortNs : kDWaitNs)) set_abort();
-                cnt = block_topk<kDSelThreads, SelGroup>(nullptr, u.P, p.K, selv, sbuf + size_t(j) * lay.pstride,
-                                                         bins, ts, sh.rkey[j]);
+                float* sj = sbuf + size_t(j) * lay.pstride;
+                if (u.P > p.K && d_two_level(NU, u.P, C)) {
+                    // this CTA's candidates: the top K of its share, to every CTA, after the earlier CTAs'
+                    const int n_l = block_topk<kDSelThreads, SelGroup>(nullptr, u.hi - u.lo, p.K, selv, sj + u.lo,
+                                                                       bins, ts, sh.rkey[j]);
+                    int off = 0, n_all = 0;
+                    for (int r = 0; r < C; ++r) {
+                        const int pr = static_cast<int>(static_cast<long long>(u.P) * (r + 1) / C) -
+                                       static_cast<int>(static_cast<long long>(u.P) * r / C);
+                        if (r < static_cast<int>(rank)) off += min(p.K, pr);
+                        n_all += min(p.K, pr);
+                    }
+                    for (int i = stid; i < n_l * C; i += kDSelThreads) {
+                        const int r = i / n_l, e = i - r * n_l;
+                        const int pg = u.lo + selv[e];
+                        st_async_f32(cand_s + off + e, &sh.cbar, static_cast<uint32_t>(r), sj[pg]);
+                        st_async_f32(cand_p + off + e, &sh.cbar, static_cast<uint32_t>(r), __int_as_float(pg));
+                    }
+                    SelGroup::sync();  // selv is read
+                    if (!mbar_wait_sleepy(&sh.cbar, 0, aborting() ? kDAbortNs : kDWaitNs)) set_abort();
+                    cnt = block_topk<kDSelThreads, SelGroup>(nullptr, n_all, p.K, selv, cand_s, bins, ts, nullptr);
+                    for (int i = stid; i < cnt; i += kDSelThreads) selv[i] = cand_p[selv[i]];  // positions -> pages
+                    SelGroup::sync();
+                } else {
+                    cnt = block_topk<kDSelThreads, SelGroup>(nullptr, u.P, p.K, selv, sj, bins, ts, sh.rkey[j]);
+                }
                 if (rank == 0) {
                     for (int i = stid; i < cnt; i += kDSelThreads) p.sel_idx[u.ufull * p.Kmax + i] = selv[i];
                     if (stid == 0) p.sel_cnt[u.ufull] = cnt;
