@@ -245,6 +245,20 @@ def reference_arm(args):
 # --------------------------------------------------------------------------- #
 # GPU arm                                                                      #
 # --------------------------------------------------------------------------- #
+def replica_seed(cfg, rank):
+    """Replicas: every rank decodes its own batch of the workload, seeded apart (no data-path collective)."""
+    return cfg.seed + 7919 * rank
+
+
+def max_over_ranks(value, dist, device):
+    """The slowest rank's time: a replica job ends when its last rank does (the value is unchanged alone)."""
+    if dist is None:
+        return value
+    t = torch.tensor([float(value)], device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t)
+
+
 def make_timing_events(n):
     try:
         return [torch.cuda.Event(enable_timing=True, external=True) for _ in range(n)], True
@@ -274,7 +288,7 @@ def gpu_arm(args):
         cfg = workloads.scaled(cfg, B=args.batch or cfg.B, L=args.layers or cfg.L)
     L = cfg.L_alloc  # a step rotates over the allocated layers
     # replicas: every rank decodes its own batch (seeded per rank); no collective on the data path
-    wl = workloads.generate(cfg, device="cuda", seed=cfg.seed + 7919 * rank)
+    wl = workloads.generate(cfg, device="cuda", seed=replica_seed(cfg, rank))
     splits = kvmm.auto_splits(kvmm.make_shape(cfg.B, L, cfg.Hq, cfg.Hkv, cfg.D, cfg.T, cfg.Pmax, cfg.K,
                                               wl.n_phys))
     st = DecodeState.for_workload(wl, num_splits=splits)
@@ -399,11 +413,7 @@ def gpu_arm(args):
             t1.record()
         stream.synchronize()
     torch.cuda.synchronize()
-    ms_total = t0.elapsed_time(t1)
-    if dist:
-        tt = torch.tensor([ms_total], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_total = float(tt)
+    ms_total = max_over_ranks(t0.elapsed_time(t1), dist, "cuda")
     err_word = st.read_err()
 
     if not external:  # eager instrumented step: per-launch durations on the launching stream
@@ -458,11 +468,7 @@ def gpu_arm(args):
             prom_host.copy_(st.promoted_cnt, non_blocking=True)
         e1.record()
     stream.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    if dist:
-        tt = torch.tensor([e2e_ms], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), dist, "cuda")
 
     if rank != 0:
         if dist:
