@@ -1219,13 +1219,13 @@ cudaError_t prepare_decode(void (*kernel)(DecodeParams), size_t smem)
 }  // namespace
 
 // the units' block-table rows go to shared memory when the launch still fits the limit with them
-bool decode_layer_bt(int D, int T, int Pmax, int Kmax, int C, int G, int NU)
+static bool decode_layer_bt(int D, int T, int Pmax, int Kmax, int C, int G, int NU)
 {
     const int maxp = (Kmax + C - 1) / C;
     return Pmax % 4 == 0 && d_layout(D, T, Pmax, Kmax, C, maxp, G, true, NU).total <= kDSmemLimit;
 }
 
-size_t decode_layer_smem(int D, int T, int Pmax, int Kmax, int C, int G, int NU)
+static size_t decode_layer_smem(int D, int T, int Pmax, int Kmax, int C, int G, int NU)
 {
     const int maxp = (Kmax + C - 1) / C;
     return d_layout(D, T, Pmax, Kmax, C, maxp, G, decode_layer_bt(D, T, Pmax, Kmax, C, G, NU), NU).total;
