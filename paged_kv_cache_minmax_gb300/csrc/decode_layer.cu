@@ -96,9 +96,6 @@ struct DecodeShared {
     int wcount[kDSelWarps];
     float mm[kDCons][8];
     float ml[kDCons][8];
-    float fw[kDCons][8];
-    float fc[kDMaxCluster][8];
-    float inv_l[8];
     uint32_t wide[kDUnits][128];   // per unit: key-ordered bounds of all rows below tok_end of the first
                                    // page the new tokens reach, [min | max], two channels a word (D <= 128)
     int wide_ok[kDUnits];          // those bounds are set (the page has a valid table entry)
@@ -594,30 +591,20 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
             const DUnit& u = sh.ud[j];
             if (!mbar_wait_sleepy(&sh.pready[j], 0, aborting() ? kDAbortNs : kDWaitNs)) set_abort();
             float* rj = recv + size_t(j) * lay.recv_stride;  // [C][16] (m, l), then [C][slice] outputs
-            if (stid < G) {
+            // four outputs of one head a thread; each thread weighs the warps' partials of its head itself, and
+            // one thread a head sends the head's (m, l) to every CTA
+            for (int e4 = 4 * stid; e4 < n_out; e4 += 4 * kDSelThreads) {
+                const int g = e4 / D;
                 float M = -INFINITY;
 #pragma unroll
-                for (int ww = 0; ww < kDCons; ++ww) M = fmaxf(M, sh.mm[ww][stid]);
+                for (int ww = 0; ww < kDCons; ++ww) M = fmaxf(M, sh.mm[ww][g]);
                 float L = 0.f;
-#pragma unroll
-                for (int ww = 0; ww < kDCons; ++ww) {
-                    const float mw2 = sh.mm[ww][stid];
-                    const float f = mw2 == -INFINITY ? 0.f : exp2f(mw2 - M);
-                    sh.fw[ww][stid] = f;
-                    L = fmaf(sh.ml[ww][stid], f, L);
-                }
-                for (int r = 0; r < C; ++r) {
-                    st_async_f32(rj + 16 * rank + stid, &sh.rbar[j], static_cast<uint32_t>(r), M);
-                    st_async_f32(rj + 16 * rank + 8 + stid, &sh.rbar[j], static_cast<uint32_t>(r), L);
-                }
-            }
-            SelGroup::sync();
-            for (int e4 = 4 * stid; e4 < n_out; e4 += 4 * kDSelThreads) {  // four outputs of one head a thread
-                const int g = e4 / D;
                 float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
                 for (int ww = 0; ww < kDCons; ++ww) {
-                    const float f = sh.fw[ww][g];
+                    const float mw2 = sh.mm[ww][g];
+                    const float f = mw2 == -INFINITY ? 0.f : exp2f(mw2 - M);
+                    L = fmaf(sh.ml[ww][g], f, L);
                     const float4 v =
                         *reinterpret_cast<const float4*>(part + size_t(ww) * G * (D + 4) + g * (D + 4) + (e4 - g * D));
                     O.x = fmaf(f, v.x, O.x);
@@ -628,37 +615,46 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
                 const int r = e4 / lay.slice;
                 st_async_v4_f32(rj + 16 * C + rank * lay.slice + (e4 - r * lay.slice), &sh.rbar[j],
                                 static_cast<uint32_t>(r), O.x, O.y, O.z, O.w);
+                if (e4 == g * D) {
+                    for (int rr = 0; rr < C; ++rr) {
+                        st_async_f32(rj + 16 * rank + g, &sh.rbar[j], static_cast<uint32_t>(rr), M);
+                        st_async_f32(rj + 16 * rank + 8 + g, &sh.rbar[j], static_cast<uint32_t>(rr), L);
+                    }
+                }
             }
             SelGroup::sync();  // the consumer warps' partials are read
             if (stid == 0 && j + 1 < nunits) mbar_arrive(&sh.pfree);
 
             if (!mbar_wait_sleepy(&sh.rbar[j], 0, aborting() ? kDAbortNs : kDWaitNs)) set_abort();
-            if (stid < G) {
-                float M = -INFINITY;
-                for (int c = 0; c < C; ++c) M = fmaxf(M, rj[16 * c + stid]);
-                float L = 0.f;
-                for (int c = 0; c < C; ++c) {
-                    const float mc = rj[16 * c + stid];
-                    const float f = mc == -INFINITY ? 0.f : exp2f(mc - M);
-                    sh.fc[c][stid] = f;
-                    L = fmaf(rj[16 * c + 8 + stid], f, L);
-                }
-                sh.inv_l[stid] = L > 0.f ? 1.f / L : 0.f;
-                if (rank == 0 && p.lse) {
-                    const size_t oi = static_cast<size_t>(u.b) * p.Hq + static_cast<size_t>(u.h) * G + stid;
-                    p.lse[oi] = L > 0.f ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
-                }
-            }
-            SelGroup::sync();
+            // this CTA's slice of the outputs from every CTA's partial: each thread weighs the partials of its
+            // head itself; rank 0 writes each head's lse
             const int e0 = static_cast<int>(rank) * lay.slice;
             const int e1 = min(n_out, e0 + lay.slice);
             const float* ro = rj + 16 * C;
             float* ob = p.out + (static_cast<size_t>(u.b) * p.Hq + static_cast<size_t>(u.h) * G) * D;
             for (int e = e0 + stid; e < e1; e += kDSelThreads) {
                 const int g = e / D;
-                float O = 0.f;
-                for (int c = 0; c < C; ++c) O = fmaf(sh.fc[c][g], ro[c * lay.slice + (e - e0)], O);
-                ob[e] = O * sh.inv_l[g];
+                float M = -INFINITY;
+                for (int c = 0; c < C; ++c) M = fmaxf(M, rj[16 * c + g]);
+                float L = 0.f, O = 0.f;
+                for (int c = 0; c < C; ++c) {
+                    const float mc = rj[16 * c + g];
+                    const float f = mc == -INFINITY ? 0.f : exp2f(mc - M);
+                    L = fmaf(rj[16 * c + 8 + g], f, L);
+                    O = fmaf(f, ro[c * lay.slice + (e - e0)], O);
+                }
+                ob[e] = O * (L > 0.f ? 1.f / L : 0.f);
+            }
+            if (rank == 0 && p.lse && stid < G) {
+                float M = -INFINITY;
+                for (int c = 0; c < C; ++c) M = fmaxf(M, rj[16 * c + stid]);
+                float L = 0.f;
+                for (int c = 0; c < C; ++c) {
+                    const float mc = rj[16 * c + stid];
+                    L = fmaf(rj[16 * c + 8 + stid], mc == -INFINITY ? 0.f : exp2f(mc - M), L);
+                }
+                const size_t oi = static_cast<size_t>(u.b) * p.Hq + static_cast<size_t>(u.h) * G + stid;
+                p.lse[oi] = L > 0.f ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
             }
             SelGroup::sync();
         }
