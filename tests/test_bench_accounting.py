@@ -1,0 +1,36 @@
+"""bench.py's byte accounting, the numerator of every GB/s and roofline figure it reports.
+
+Checked against the sizes the workloads fix: MinMax rows of every page of
+every rescored unit, K and V of every selected page, and small terms well
+under 1% at the full-size shapes.
+"""
+import bench
+from paged_kv_cache_minmax_gb300 import workloads
+
+
+def test_llama8b_32k_layer_step_moves_64_mib_of_metadata_and_64_mib_of_selected_kv():
+    cfg = workloads.CONFIGS[2]
+    b = bench.algorithmic_bytes(cfg)
+    units = cfg.B * cfg.Hkv  # 64
+    assert b["meta"] == units * cfg.P * 2 * cfg.D * 2 == 64 * 2**20
+    assert b["kv"] == units * cfg.K * cfg.T * cfg.D * 2 * 2 == 64 * 2**20
+    assert 0 < b["small"] < 0.01 * b["total"]
+    assert b["total"] == b["meta"] + b["kv"] + b["small"]
+    # one decode_layer launch: the metadata and pages, plus its own small terms
+    assert b["meta"] + b["kv"] < b["decode_launch"] < 1.01 * (b["meta"] + b["kv"])
+
+
+def test_the_rerank_schedule_counts_only_rescored_units_metadata():
+    cfg = workloads.CONFIGS[4]
+    all_units = cfg.B * cfg.Hkv
+    full = bench.algorithmic_bytes(cfg)
+    quarter = bench.algorithmic_bytes(cfg, rescored_units=all_units / 4)
+    assert quarter["kv"] == full["kv"]  # every unit attends over its selection every step
+    assert quarter["meta"] == full["meta"] / 4
+    assert quarter["total"] < full["total"]
+
+
+def test_k_at_least_p_selects_every_page():
+    cfg = workloads.scaled(workloads.CONFIGS[1], K=10**6)
+    b = bench.algorithmic_bytes(cfg)
+    assert b["kv"] == cfg.B * cfg.Hkv * cfg.P * cfg.T * cfg.D * 2 * 2

@@ -210,3 +210,11 @@ def test_launch_shape_and_long_units(pages):
     stats = parity.Stats()
     parity.check_unit(wl, st, 0, 0, 0, wl.q[0], sca, stats)
     stats.check()
+    # a step that rescores nothing keeps the selection (and skips the two-level exchange)
+    keep = torch.zeros(cfg.L, cfg.Hkv, dtype=torch.uint8, device="cuda")
+    before = st.sel_idx.clone()
+    nk1, nv1 = workloads.step_tokens(wl, 1)
+    sca, scb = run_both(a, b, 0, wl.q[0], nk1[0], nv1[0], mask=keep)
+    assert st.read_err() == 0 and b[1].read_err() == 0
+    assert torch.equal(st.sel_idx, before)
+    assert_same(a, b, sca, scb, 0)
