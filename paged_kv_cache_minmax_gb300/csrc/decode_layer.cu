@@ -10,31 +10,39 @@
 // only, found through [batch, layer, head, logical_block]).  The results
 // equal kv_minmax_update (appending) followed by page_score_topk_attn.
 //
-// Design (sm_103a).  A thread-block cluster of C CTAs owns two units (batch,
-// KV head).  Every CTA of it streams, in this order, its share of unit 0's
+// Design (sm_103a).  A thread-block cluster of C CTAs owns NU units (batch,
+// KV head): two, or one when two units' score buffers do not fit shared
+// memory (long sequences).  C is the most CTAs whose clusters are all resident
+// at once.  Every CTA of it streams, in this order, its share of unit 0's
 // MinMax rows, its share of unit 1's, its share of unit 0's selected K/V
-// pages, its share of unit 1's:
+// pages, its share of unit 1's (all bulk copies with an L2 evict-first
+// policy: each byte is read once):
 //   - 8 consumer warps each keep their own slots in flight (1-D bulk copies,
 //     TMA, one mbarrier per slot; two slots a warp for pages of 16 tokens, one
 //     for pages of 32).  A slot holds one page of K and V (an attention step)
 //     or the [min | max] rows of T consecutive pages (a score item): the same
 //     bytes.  A score item is scored on the tensor cores (mma.sync m16n8k16)
 //     and every score sent to every CTA of the cluster as an asynchronous
-//     remote store that completes on the receiver's mbarrier; a page of the
-//     item that receives new tokens first has its bounds widened by them.  An
-//     attention step runs S^T = K Q^T, the online softmax and O^T += V^T P^T
-//     with P as bf16 hi + lo.  At the end of a unit each warp leaves its
-//     softmax partial in shared memory and goes on with the next unit's
-//     pages, already in flight;
+//     remote store that completes on the receiver's mbarrier, as does each
+//     warp's range of the unit's scores (remote min/max reductions); a page of
+//     the item that receives new tokens first has its bounds widened by them.
+//     An attention step runs S^T = K Q^T, the online softmax (against a per-
+//     head reference raised only when a score exceeds it by 2^8) and
+//     O^T += V^T P^T with P as bf16 hi + lo.  At the end of a unit each warp
+//     leaves its softmax partial in shared memory and goes on with the next
+//     unit's pages, already in flight;
 //   - 8 selector warps first take the bounds of the rows a partly filled page
 //     already holds (for the consumer that widens it) and append the new
 //     tokens (rows, and the MinMax of the pages this CTA owns); then, as soon
-//     as all of a unit's scores have arrived, they select the unit's top K
-//     exactly (block_topk) and resolve this CTA's share of the pages through
-//     the block table -- unit 0's selection overlaps the streaming of unit 1's
-//     rows, unit 1's overlaps unit 0's attention -- and for each unit combine
-//     the consumer warps' partials into the CTA's, send every CTA its slice,
-//     and combine the slices they receive into out and lse.
+//     as all of a unit's scores and their range have arrived, they select the
+//     unit's top K exactly (block_topk; for one long unit a cluster, in two
+//     levels: each CTA's top K of its share, then the top K of those) and
+//     resolve this CTA's share of the pages through the block-table rows
+//     (copied to shared memory at the start when they fit) -- unit 0's
+//     selection overlaps the streaming of unit 1's rows, unit 1's overlaps
+//     unit 0's attention -- and for each unit combine the consumer warps'
+//     partials into the CTA's, send every CTA its slice (16-byte remote
+//     stores), and combine the slices they receive into out and lse.
 // All exchange stays on chip (asynchronous remote shared-memory stores and
 // mbarriers), with no fence on the way: a consumer attending over a page that
 // receives tokens takes those rows from new_k / new_v rather than waiting for
