@@ -399,8 +399,7 @@ def gpu_arm(args):
         dist.barrier()
     torch.cuda.synchronize()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    clocks = ClockSampler(local_rank, os.path.join(ROOT, "gpurun_out", "clocks.csv")
-                          if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else None)
+    clocks = ClockSampler(local_rank, args.clocks_log)
     with clocks:
         time.sleep(0.3)
         with torch.cuda.stream(stream):
@@ -837,6 +836,8 @@ def main():
     ap.add_argument("--config", type=int, default=2, choices=sorted(workloads.CONFIGS),
                     help="workload (default: the 8B-shape 32K-context decode step)")
     ap.add_argument("--no-graph", action="store_true", help="launch eagerly (for profilers)")
+    ap.add_argument("--clocks-log", default=None,
+                    help="also write the nvidia-smi clock samples of the timed region to this CSV file")
     ap.add_argument("--batch", type=int, default=0, help="override the batch (smaller profiling case)")
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (smaller profiling case)")
     ap.add_argument("--meankey", action="store_true",
