@@ -497,7 +497,7 @@ def gpu_arm(args):
         kernel_ms = {"score_topk_kernel": s_ms, "sparse_attn_kernel": a_ms}
     kernel_ms["per_layer_step_ms"] = ms_total / args.steps / L
     achieved = dom_bytes / (dom_ms / 1e3) / 1e9
-    traffic = load_traffic(dom)
+    traffic = load_traffic(dom, workloads.CONFIGS[args.config].name, cfg.B)
     clk = clocks.summary()
     line = {
         "metric": METRIC, "value": value, "unit": "layer-steps/s", "n_gpus": world, "steps": args.steps,
@@ -816,14 +816,16 @@ def meankey_arm(args):
         "device_err": st.read_err()}), flush=True)
 
 
-def load_traffic(kernel):
-    """dram bytes per launch of ``kernel`` from the committed ncu summary, if current."""
+def load_traffic(kernel, workload, batch):
+    """dram bytes per launch of ``kernel`` on ``workload`` from the committed ncu summaries, if one
+    was captured at that batch (a launch covers one layer, so the layer count does not matter)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         d = json.load(f)
-    return d.get(kernel)
+    rec = d.get(kernel, {}).get(workload)
+    return rec["bytes"] if rec and rec["batch"] == batch else None
 
 
 def main():

@@ -212,12 +212,17 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
     constexpr int kRing = d_ring(T);            // slots per consumer warp
     constexpr int kRowBytes = 4 * D;            // a page's [min | max] row
     constexpr int kPageBytes = 2 * T * D;       // a page's K (or V) block
-    constexpr int kSlot = 2 * kPageBytes;       // one page of K and V, or the rows of T pages
-    constexpr int kPiece = kSlot / kRowBytes;   // pages per score item
+    constexpr int kSlot = 2 * kPageBytes;       // an attention slot: one page of K and V
+    // the score phase cuts the same bytes into two slots of 16 pages' rows: a T = 32 warp's single
+    // attention slot would leave it copying and scoring one after the other
+    constexpr int kSRing = 2;                       // score slots per consumer warp
+    constexpr int kSSlot = kRing * kSlot / kSRing;  // the [min | max] rows of kSPiece pages
+    constexpr int kSPiece = kSSlot / kRowBytes;     // pages per score item
+    constexpr int kSGrp = kSPiece / 16;             // 16-page row groups of a score item
     constexpr int kMTiles = D / 16;
     constexpr int kR = (2 * D / 8) / 4;         // 16-byte chunk groups of a [min | max] row
-    static_assert(kPiece == 16 * kSub, "a score item is kSub groups of 16 pages");
-    static_assert(kRing <= kDRingMax, "slot count");
+    static_assert(kSGrp == 1 && kSPiece == 16, "a score item is one group of 16 pages");
+    static_assert(kRing <= kDRingMax && kSRing <= kDRingMax, "slot count");
     extern __shared__ __align__(1024) uint8_t smem[];
     __shared__ DecodeShared sh;
 
@@ -737,7 +742,7 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
         int nsl[kDUnits] = {0, 0};
         for (int j = 0; j < nunits; ++j) {
             const DUnit& u = sh.ud[j];
-            nsl[j] = u.rescored ? (u.hi - u.lo + kPiece - 1) / kPiece : 0;
+            nsl[j] = u.rescored ? (u.hi - u.lo + kSPiece - 1) / kSPiece : 0;
         }
         // advance (j, sl) to this warp's next score item; false when there is none
         auto next_score = [&](int& j, int& sl) {
@@ -751,15 +756,15 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
         auto issue_score = [&](int b2, int j, int sl) {
             const int lo = sh.ud[j].lo, hi = sh.ud[j].hi;
             const size_t ufull = sh.ud[j].ufull;
-            const int page0 = lo + sl * kPiece;
-            const int npg = min(kPiece, hi - page0);
+            const int page0 = lo + sl * kSPiece;
+            const int npg = min(kSPiece, hi - page0);
             if (lane == 0) mbar_arrive_expect_tx(&sh.full[w][b2], static_cast<uint32_t>(npg) * kRowBytes);
             __syncwarp();
             // each slot has its own copying lanes: a thread's bulk copies complete one after another
-            const int cl = lane - (kPiece / 8) * b2;
+            const int cl = lane - (kSPiece / 8) * b2;
             if (cl >= 0 && 8 * cl < npg) {  // lane cl copies rows 8cl .. 8cl+7
                 const int rows = min(8, npg - 8 * cl);
-                bulk_copy_g2s_hint(my_ring + size_t(b2) * kSlot + size_t(8 * cl) * kRowBytes,
+                bulk_copy_g2s_hint(my_ring + size_t(b2) * kSSlot + size_t(8 * cl) * kRowBytes,
                                    p.meta + (ufull * p.Pmax + page0 + 8 * cl) * 2 * D,
                                    static_cast<uint32_t>(rows) * kRowBytes, &sh.full[w][b2], stream_policy);
             }
@@ -835,7 +840,7 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
             float* orow = p.scores_out ? p.scores_out + static_cast<size_t>(cluster * NU + j) * p.Pmax + page0
                                        : nullptr;
 #pragma unroll
-            for (int grp = 0; grp < kSub; ++grp) {
+            for (int grp = 0; grp < kSGrp; ++grp) {
                 if (16 * grp < npg) {
                     const uint8_t* ra = slot + static_cast<size_t>(16 * grp + gid) * kRowBytes;
                     const uint8_t* rb = ra + 8 * kRowBytes;
@@ -893,20 +898,20 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
         {
             int ij = 0, isl = w - kDCons;  // the last issued item
             bool more = next_score(ij, isl);
-            for (int b = 0; b < kRing && more; ++b) {
+            for (int b = 0; b < kSRing && more; ++b) {
                 issue_score(b, ij, isl);
                 more = next_score(ij, isl);
             }
             // a slot is refilled as soon as it is consumed, and the slots are consumed in turn: in the
             // order they were filled
-            for (int b = 0; in_flight(b); b = (b + 1) % kRing) {
+            for (int b = 0; in_flight(b); b = (b + 1) % kSRing) {
                 const int j = b ? hj1 : hj0;
-                const int page0 = sh.ud[j].lo + (b ? hs1 : hs0) * kPiece;
-                const int npg = min(kPiece, sh.ud[j].hi - page0);
+                const int page0 = sh.ud[j].lo + (b ? hs1 : hs0) * kSPiece;
+                const int npg = min(kSPiece, sh.ud[j].hi - page0);
                 while (rj < j) flush_range();  // the units before j are done
                 land(b);
                 load_frags(j, false);
-                uint8_t* slot = my_ring + size_t(b) * kSlot;
+                uint8_t* slot = my_ring + size_t(b) * kSSlot;
                 const int pe = min(sh.ud[j].pe, page0 + npg);
                 for (int pg = max(sh.ud[j].pb, page0); pg < pe; ++pg)  // pages receiving new tokens
                     widen_page(j, pg, slot + size_t(pg - page0) * kRowBytes);

@@ -34,3 +34,14 @@ def test_k_at_least_p_selects_every_page():
     cfg = workloads.scaled(workloads.CONFIGS[1], K=10**6)
     b = bench.algorithmic_bytes(cfg)
     assert b["kv"] == cfg.B * cfg.Hkv * cfg.P * cfg.T * cfg.D * 2 * 2
+
+
+def test_measured_traffic_is_reported_only_for_the_captured_workload_and_batch():
+    name = workloads.CONFIGS[2].name
+    captured = bench.load_traffic("decode_layer", name, workloads.CONFIGS[2].B)
+    # the capture is one launch of that workload: within a few percent of its algorithmic bytes
+    launch = bench.algorithmic_bytes(workloads.CONFIGS[2])["decode_launch"]
+    assert captured is not None and launch <= captured < 1.05 * launch
+    assert bench.load_traffic("decode_layer", name, 4) is None  # another batch: another launch
+    assert bench.load_traffic("decode_layer", workloads.CONFIGS[5].name, workloads.CONFIGS[5].B) is None
+    assert bench.load_traffic("sparse_attn_kernel", name, workloads.CONFIGS[2].B) is None
