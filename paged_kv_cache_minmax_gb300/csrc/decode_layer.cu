@@ -18,10 +18,11 @@
 // pages, its share of unit 1's (all bulk copies with an L2 evict-first
 // policy: each byte is read once):
 //   - 8 consumer warps each keep their own slots in flight (1-D bulk copies,
-//     TMA, one mbarrier per slot; two slots a warp for pages of 16 tokens, one
-//     for pages of 32).  A slot holds one page of K and V (an attention step)
-//     or the [min | max] rows of T consecutive pages (a score item): the same
-//     bytes.  A score item is scored on the tensor cores (mma.sync m16n8k16)
+//     TMA, one mbarrier per slot).  An attention slot holds one page of K and
+//     V: two slots a warp for pages of 16 tokens, one for pages of 32.  The
+//     score phase cuts the same bytes into two slots of the [min | max] rows of
+//     16 consecutive pages (a score item), whatever the page size.  A score
+//     item is scored on the tensor cores (mma.sync m16n8k16)
 //     and every score sent to every CTA of the cluster as an asynchronous
 //     remote store that completes on the receiver's mbarrier, as does each
 //     warp's range of the unit's scores (remote min/max reductions); a page of
@@ -738,7 +739,7 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
             frag = want;
         };
 
-        // ---- 1. scores: this warp's items (T pages each) s = w, w + 8, ... of each rescored unit ----
+        // ---- 1. scores: this warp's items (16 pages each) s = w, w + 8, ... of each rescored unit ----
         int nsl[kDUnits] = {0, 0};
         for (int j = 0; j < nunits; ++j) {
             const DUnit& u = sh.ud[j];
