@@ -70,7 +70,7 @@ class Config:
 
     @property
     def L_alloc(self) -> int:
-        return self.layers_alloc or self.L
+        return min(self.layers_alloc, self.L) if self.layers_alloc else self.L
 
     def seq_lens(self) -> list[int]:
         if not self.ragged:
