@@ -37,11 +37,13 @@ def test_k_at_least_p_selects_every_page():
 
 
 def test_measured_traffic_is_reported_only_for_the_captured_workload_and_batch():
+    for c in (2, 3, 5):
+        cfg = workloads.CONFIGS[c]
+        captured = bench.load_traffic("decode_layer", cfg.name, cfg.B)
+        # each capture is one launch of its workload: within a few percent of its algorithmic bytes
+        launch = bench.algorithmic_bytes(cfg)["decode_launch"]
+        assert captured is not None and launch <= captured < 1.05 * launch, c
     name = workloads.CONFIGS[2].name
-    captured = bench.load_traffic("decode_layer", name, workloads.CONFIGS[2].B)
-    # the capture is one launch of that workload: within a few percent of its algorithmic bytes
-    launch = bench.algorithmic_bytes(workloads.CONFIGS[2])["decode_launch"]
-    assert captured is not None and launch <= captured < 1.05 * launch
     assert bench.load_traffic("decode_layer", name, 4) is None  # another batch: another launch
-    assert bench.load_traffic("decode_layer", workloads.CONFIGS[5].name, workloads.CONFIGS[5].B) is None
+    assert bench.load_traffic("decode_layer", workloads.CONFIGS[4].name, workloads.CONFIGS[4].B) is None
     assert bench.load_traffic("sparse_attn_kernel", name, workloads.CONFIGS[2].B) is None
