@@ -187,22 +187,29 @@ def test_null_blocks_outside_the_selection_are_never_read():
     stats.check()
 
 
-@pytest.mark.parametrize("pages", [8192, 12288])
-def test_launch_shape_and_long_units(pages):
+@pytest.mark.parametrize("pages,K,units", [(8192, 96, 1), (8192, 300, 1), (6000, 300, 1), (12288, 96, 0)])
+def test_launch_shape_and_long_units(pages, K, units):
     """decode_layer's launch shape is one the device can hold: two units a cluster at the 8B shape, one
-    for a unit of 8192 pages (its scores no longer fit twice), and none at 12288 pages, where decode_layer
-    runs the append and page_score_topk_attn instead.  Either way it leaves what the separate calls leave."""
+    for a unit of 6000 or 8192 pages (its scores no longer fit twice), and none at 12288 pages, where
+    decode_layer runs the append and page_score_topk_attn instead.  Either way it leaves what the separate
+    calls leave.  At K = 300 the selection takes the general top-K path (more than 2048 scores) at one of
+    its two levels: the first at 8192 pages (a CTA's share is larger), the second at 6000 pages (the
+    cluster's candidates are more)."""
     bench_shape = kvmm.make_shape(8, 32, 32, 8, 128, 16, 2048, 128, 1)
     assert kvmm.decode_layer_units(bench_shape) == 2
     assert 1 <= kvmm.decode_layer_cluster(bench_shape) <= 16
-    cfg = workloads.Config("long", B=1, L=1, Hq=4, Hkv=1, D=128, T=16, S=16 * pages - 3, K=96,
+    cfg = workloads.Config("long", B=1, L=1, Hq=4, Hkv=1, D=128, T=16, S=16 * pages - 3, K=K,
                            key_dist="outlier", n_planted=24, seed=83)
     a, b = twin_states(cfg)
     wl, st = a
-    if pages == 8192:
-        assert kvmm.decode_layer_units(st.shape) == 1 and kvmm.decode_layer_cluster(st.shape) >= 1
+    assert kvmm.decode_layer_units(st.shape) == units
+    if units:
+        assert kvmm.decode_layer_cluster(st.shape) >= 1
+        c = kvmm.decode_layer_cluster(st.shape)
+        if K == 300:
+            assert (pages + c - 1) // c > 2048 if pages == 8192 else c * K > 2048
     else:
-        assert kvmm.decode_layer_units(st.shape) == 0 and kvmm.decode_layer_cluster(st.shape) == 0
+        assert kvmm.decode_layer_cluster(st.shape) == 0
     nk, nv = workloads.step_tokens(wl, 0)
     sca, scb = run_both(a, b, 0, wl.q[0], nk[0], nv[0])
     assert st.read_err() == 0 and b[1].read_err() == 0
