@@ -324,11 +324,16 @@ def gpu_arm(args):
 
     path = args.path
     fused = path != "unfused"  # one timed launch group per layer (decode_layer, or scoring + attention)
+    # the layers' decode_layer calls follow one another on the stream, and none writes what the next reads
+    # of the cache state (its own layer's rows only; lengths and masks change between steps): each launch
+    # may stream its metadata while the previous one drains (KVMM_DECODE_EARLY_READS)
+    early_reads = not args.no_early_reads
 
     def decode_layer_call(l, mask=None):
         kvmm.decode_layer(st.shape, l, q_dev[l], nk_dev[l], nv_dev[l], 1, st.tok_begin, st.seq_len,
                           st.k_pool, st.v_pool, st.block_table, st.meta, st.seq_len, mask, st.K, st.sel_idx,
-                          st.sel_cnt, st.out[l], lse=st.lse[l], err=st.err, workspace=st.workspace)
+                          st.sel_cnt, st.out[l], lse=st.lse[l], err=st.err, workspace=st.workspace,
+                          early_reads=early_reads)
 
     def step(instrument, mask=None):
         main = torch.cuda.current_stream()
@@ -514,7 +519,9 @@ def gpu_arm(args):
                    "path": {"decode_layer": "decode_layer (append, score, select, attend: one launch)",
                             "fused": "kv_minmax_update + page_score_topk_attn (scoring kernel + selecting "
                                      "attention kernel)",
-                            "unfused": "kv_minmax_update + page_score_topk + sparse_paged_decode_attn"}[path]},
+                            "unfused": "kv_minmax_update + page_score_topk + sparse_paged_decode_attn"}[path],
+                   **({"decode_flags": "KVMM_DECODE_EARLY_READS" if early_reads else 0}
+                      if path == "decode_layer" else {})},
         "kv_gbs": kv_gbs, "pct_hbm_peak": kv_gbs / peak,
         "bytes_per_layer_step": acc["total"],
         "kernel_ms": kernel_ms,
@@ -850,6 +857,8 @@ def main():
                     help="time the promotion transfer from pinned host memory instead")
     ap.add_argument("--stability", action="store_true",
                     help="time head-stability profiling (history record, RCO and classification) instead")
+    ap.add_argument("--no-early-reads", action="store_true",
+                    help="decode_layer waits for the preceding kernel before any read (no KVMM_DECODE_EARLY_READS)")
     ap.add_argument("--path", default="decode_layer", choices=["decode_layer", "fused", "unfused"],
                     help="decode_layer (one launch per layer), fused (kv_minmax_update + page_score_topk_attn) "
                          "or unfused (kv_minmax_update + page_score_topk + sparse_paged_decode_attn)")

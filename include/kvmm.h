@@ -302,13 +302,29 @@ kvmm_status page_score_topk_attn(const kvmm_shape* shape, int32_t layer, const k
  * memory (long page tables), the call runs kv_minmax_update and then
  * page_score_topk_attn instead, which need workspace (as for page_score_topk;
  * otherwise workspace may be NULL and is not used).
+ *
+ * flags: 0, or KVMM_DECODE_EARLY_READS.  By default the launch reads nothing
+ * before the kernel launched just before it on the stream has finished
+ * (programmatic dependent launch lets it be scheduled meanwhile).  With
+ * KVMM_DECODE_EARLY_READS the caller guarantees that that kernel writes
+ * nothing this call reads of seq_len, tok_begin, tok_end, rescore_mask (the
+ * layer's row), block_table and meta (the layer's rows).  The launch then
+ * reads those while that kernel drains (the units' extents, their table
+ * rows, the first metadata rows) and waits for it before it reads q, new_k,
+ * new_v, the pools or the kept selections, and before it writes anything.
+ * A decode loop meets this when those arrays change only between steps or
+ * by this call itself: the layers' calls back to back, or the query
+ * projection just before.  Other bits return KVMM_INVALID_ARG.  The
+ * two-kernel fallback always waits.
  */
+#define KVMM_DECODE_EARLY_READS 1u
 kvmm_status decode_layer(const kvmm_shape* shape, int32_t layer, const kvmm_bf16* q, const kvmm_bf16* new_k,
                          const kvmm_bf16* new_v, int32_t n_new, const int32_t* tok_begin, const int32_t* tok_end,
                          kvmm_bf16* k_pool, kvmm_bf16* v_pool, const int32_t* block_table, kvmm_bf16* meta,
                          const int32_t* seq_len, const uint8_t* rescore_mask, int32_t K, int32_t group_reduce,
                          float sm_scale, int32_t* sel_idx, int32_t* sel_cnt, float* scores_out, float* out,
-                         float* lse, void* workspace, size_t workspace_bytes, int32_t* err, kvmm_stream stream);
+                         float* lse, void* workspace, size_t workspace_bytes, uint32_t flags, int32_t* err,
+                         kvmm_stream stream);
 
 /* ------------------------------------------------------------------------
  * The mean-key scorer: KVDrive's page representative, beside MinMax.

@@ -453,12 +453,14 @@ kvmm_status decode_layer(const kvmm_shape* shape, int32_t layer, const kvmm_bf16
                          kvmm_bf16* k_pool, kvmm_bf16* v_pool, const int32_t* block_table, kvmm_bf16* meta,
                          const int32_t* seq_len, const uint8_t* rescore_mask, int32_t K, int32_t group_reduce,
                          float sm_scale, int32_t* sel_idx, int32_t* sel_cnt, float* scores_out, float* out,
-                         float* lse, void* workspace, size_t workspace_bytes, int32_t* err, kvmm_stream stream)
+                         float* lse, void* workspace, size_t workspace_bytes, uint32_t flags, int32_t* err,
+                         kvmm_stream stream)
 {
     kvmm_status st = check_shape(shape);
     if (st != KVMM_OK) return st;
     const kvmm_shape& s = *shape;
     if (layer < 0 || layer >= s.L || K < 1 || K > s.Kmax || !std::isfinite(sm_scale)) return KVMM_INVALID_ARG;
+    if ((flags & ~KVMM_DECODE_EARLY_READS) != 0u) return KVMM_INVALID_ARG;
     if (group_reduce != 0 && group_reduce != 1) return KVMM_INVALID_ARG;
     if ((new_k == nullptr) != (new_v == nullptr)) return KVMM_INVALID_ARG;
     if (new_k != nullptr && (n_new < 1 || !req(new_k) || !req(new_v) || !req4(tok_begin) || !req4(tok_end)))
@@ -495,6 +497,7 @@ kvmm_status decode_layer(const kvmm_shape* shape, int32_t layer, const kvmm_bf16
     p.K = K;
     p.C = grid.c;
     p.NU = grid.nu;
+    p.early = (flags & KVMM_DECODE_EARLY_READS) != 0u ? 1 : 0;
     p.n_new = new_k != nullptr ? n_new : 0;
     p.n_phys = s.n_phys;
     p.scale_log2 = (sm_scale > 0.f ? sm_scale : 1.0f / std::sqrt(static_cast<float>(s.D))) * 1.4426950408889634f;

@@ -276,7 +276,12 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
     // anything reaches another CTA, and meanwhile the queries and the unit descriptors are fetched
     cluster_arrive();
     pdl_launch_dependents();
-    pdl_wait();  // every input may come from the preceding kernels
+    // Every input may come from the preceding kernels, and the caller may read what this one writes only
+    // after it.  With early cache reads the caller vouches that the preceding kernel writes none of the
+    // cache state (descriptors' inputs, block table, metadata): this launch then computes its units'
+    // descriptors, copies their table rows and starts streaming their metadata while that kernel drains,
+    // and every thread waits for it before it reads the queries or new rows or writes anything.
+    if (!p.early) pdl_wait();
 
     auto aborting = [&]() { return ld_volatile(&sh.abort_flag) != 0; };
     auto set_abort = [&]() {
@@ -289,7 +294,7 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
         return ok;
     };
 
-    if (tid == 0) {  // the query groups of the cluster's units
+    auto issue_q = [&]() {  // the query groups of the cluster's units (one thread)
         const uint32_t qbytes = static_cast<uint32_t>(G) * D * 2;
         mbar_arrive_expect_tx(&sh.qbar, qbytes * nunits);
         for (int j = 0; j < nunits; ++j) {
@@ -298,7 +303,8 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
             bulk_copy_g2s(qbuf + size_t(j) * 8 * D * 2,
                           p.q + (static_cast<size_t>(b) * p.Hq + static_cast<size_t>(h) * G) * D, qbytes, &sh.qbar);
         }
-    }
+    };
+    if (tid == 0 && !p.early) issue_q();
     if (tid < nunits) {  // this CTA's view of unit tid
         DUnit u;
         const int wunit = cluster * NU + tid;
@@ -388,6 +394,10 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
                                       u.rescored ? static_cast<uint32_t>(u.P) * 4u + static_cast<uint32_t>(C * kDCons * 8) : 0u);
                 mbar_arrive_expect_tx(&sh.rbar[j], static_cast<uint32_t>(C * (2 * G + own)) * 4u);
             }
+        }
+        if (p.early) {
+            pdl_wait();  // the preceding kernel is done: the queries and new rows are final
+            if (stid == 0) issue_q();
         }
         // 0. for the consumer warps, well before they need them: the finished bounds of the first page the
         //    new tokens reach, if this CTA scores it (all its rows below tok_end, old and new), and for a
@@ -903,6 +913,7 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
                 issue_score(b, ij, isl);
                 more = next_score(ij, isl);
             }
+            if (p.early) pdl_wait();  // before the new rows and any store
             // a slot is refilled as soon as it is consumed, and the slots are consumed in turn: in the
             // order they were filled
             for (int b = 0; in_flight(b); b = (b + 1) % kSRing) {

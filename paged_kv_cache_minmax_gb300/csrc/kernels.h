@@ -91,6 +91,7 @@ struct DecodeParams {
     int32_t maxp;   // selected pages one CTA attends over at most: ceil(Kmax / C)
     int32_t bt_smem;  // 1: the units' block-table rows are copied to shared memory
     int32_t NU;       // units per cluster: 1 or 2 (the kernel instantiation takes it too)
+    int32_t early;    // 1: the cache state is read before the preceding kernel has finished (KVMM_DECODE_EARLY_READS)
     int32_t n_new;  // appended tokens per batch entry (rows of new_k / new_v)
     int64_t n_phys;
     float scale_log2;  // sm_scale * log2(e)

@@ -17,6 +17,7 @@ from . import build as _build
 
 OK, INVALID_ARG, UNSUPPORTED_SHAPE, WORKSPACE_TOO_SMALL, CUDA_ERROR = range(5)
 ERR_NULL_BLOCK, ERR_OUT_OF_RANGE, ERR_TIMEOUT = 1, 2, 4
+DECODE_EARLY_READS = 1
 NULL_BLOCK = -1
 
 EXPORTS = ("kv_minmax_update", "page_score_topk", "sparse_paged_decode_attn", "topk_promotion_diff",
@@ -79,7 +80,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.page_score_topk_static_scratch.argtypes = [SP, I32, P, P, P, P, I32, I32, P, P, P, P, P]
     lib.page_score_topk_attn.argtypes = [SP, I32, P, P, P, P, P, P, P, I32, I32, F32, P, P, P, P, P, P, SZ, P, P]
     lib.decode_layer.argtypes = [SP, I32, P, P, P, I32, P, P, P, P, P, P, P, P, I32, I32, F32, P, P, P, P, P, P, SZ,
-                                 P, P]
+                                 ctypes.c_uint32, P, P]
     lib.topk_history_record.argtypes = [SP, I32, P, P, P, I32, I32, P, P, P, P, P]
     lib.topk_stability_rco.argtypes = [SP, P, P, P, I32, I32, I32, I32, F32, P, P, P, P, P]
     lib.promote_pages.argtypes = [SP, I32, P, P, P, P, P, P, P, P, P, P, P, P, P, I32, P, P]
@@ -260,8 +261,10 @@ def page_score_topk_attn(shape: Shape, layer: int, q, meta, k_pool, v_pool, bloc
 def decode_layer(shape: Shape, layer: int, q, new_k, new_v, n_new: int, tok_begin, tok_end, k_pool, v_pool,
                  block_table, meta, seq_len, rescore_mask, K: int, sel_idx, sel_cnt, out, lse=None, err=None,
                  scores_out=None, group_reduce: int = 0, sm_scale: float = 0.0, workspace=None,
-                 stream=None) -> None:
-    """Append (optional), score, select and attend for one layer in one launch."""
+                 stream=None, early_reads: bool = False) -> None:
+    """Append (optional), score, select and attend for one layer in one launch.  ``early_reads``: the
+    kernel launched just before on the stream writes nothing this call reads of seq_len, tok_begin,
+    tok_end, rescore_mask, block_table and meta (``KVMM_DECODE_EARLY_READS``)."""
     s = shape
     units = s.B * s.L * s.Hkv
     if (new_k is None) != (new_v is None):
@@ -285,6 +288,7 @@ def decode_layer(shape: Shape, layer: int, q, new_k, new_v, n_new: int, tok_begi
             _dev(out, "out", torch.float32, s.B * s.Hq * s.D),
             _dev(lse, "lse", torch.float32, s.B * s.Hq, optional=True),
             _dev(workspace, "workspace", torch.uint8, optional=True), 0 if workspace is None else workspace.numel(),
+            DECODE_EARLY_READS if early_reads else 0,
             _dev(err, "err", torch.int32, 1, optional=True), _stream(stream))
     _check("decode_layer", load().decode_layer(*args))
 

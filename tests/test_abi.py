@@ -91,6 +91,12 @@ def test_validation_rejects_before_any_launch(lib):
     assert lib.page_score_topk_attn(ctypes.byref(s), 0, *fa[:7], 9, *fa[8:]) == kvmm.INVALID_ARG
     assert lib.page_score_topk_attn(ctypes.byref(s), 0, *fa[:9], float("inf"), *fa[10:]) == kvmm.INVALID_ARG
     assert lib.page_score_topk_attn(ctypes.byref(s), 0, *fa[:16], 64, None, None) == kvmm.WORKSPACE_TOO_SMALL
+    # decode_layer: null query, an unknown flag bit
+    da = [fake, None, None, 0, None, None, fake, fake, fake, fake, fake, None, 8, 0, 0.0, fake, fake, None, fake,
+          None, None, 0]
+    assert lib.decode_layer(ctypes.byref(s), 0, None, *da[1:], 0, None, None) == kvmm.INVALID_ARG
+    assert lib.decode_layer(ctypes.byref(s), 0, *da, 2, None, None) == kvmm.INVALID_ARG
+    assert lib.decode_layer(ctypes.byref(s), 0, *da, kvmm.DECODE_EARLY_READS | 4, None, None) == kvmm.INVALID_ARG
     # diff: missing promoted list
     assert lib.topk_promotion_diff(ctypes.byref(s), 0, None, fake, fake, fake, fake, 1, None, fake, None, None,
                                    None, None, None) == kvmm.INVALID_ARG

@@ -226,3 +226,56 @@ def test_launch_shape_and_long_units(pages, K, units):
     assert st.read_err() == 0 and b[1].read_err() == 0
     assert torch.equal(st.sel_idx, before)
     assert_same(a, b, sca, scb, 0)
+
+
+EARLY_CASES = {
+    "llama-6-layers": scaled(CONFIGS[2], B=4, L=6, S=4096, K=32, n_planted=16, ragged=True),
+    "gqa5-t32": CASES["gqa5-t32"],
+    "odd-units": scaled(CASES["odd-units"], L=3),
+}
+
+
+@pytest.mark.parametrize("name", sorted(EARLY_CASES))
+def test_early_reads_leave_what_the_waiting_launch_leaves(name):
+    """KVMM_DECODE_EARLY_READS: the layers' launches back to back on one stream, each streaming its metadata
+    while the previous one drains, leave bit for bit what launches that wait for the previous one leave:
+    pools, MinMax, selections, outputs.  Odd layers take their queries from a kernel that writes them just
+    before the launch (the queries are read only after the wait), and the second step keeps the stable
+    heads' selections (read after the wait as well)."""
+    cfg = EARLY_CASES[name]
+    runs = []
+    for early in (True, False):
+        wl = workloads.generate(cfg, device="cuda")
+        st = DecodeState.for_workload(wl)
+        st.build_metadata()
+        nk, nv = workloads.step_tokens(wl, 0)
+        st.tok_begin.copy_(st.seq_len - 1)
+        qbuf = torch.empty_like(wl.q[0])
+        mask = (wl.unstable != 0).to(torch.uint8)
+        torch.cuda.synchronize()
+        for step in range(2):
+            for l in range(cfg.L_alloc):
+                q = wl.q[l]
+                if l % 2:
+                    qbuf.copy_(q)
+                    q = qbuf
+                kvmm.decode_layer(st.shape, l, q, nk[l], nv[l], 1, st.tok_begin, st.seq_len, st.k_pool,
+                                  st.v_pool, st.block_table, st.meta, st.seq_len, None if step == 0 else mask, st.K,
+                                  st.sel_idx, st.sel_cnt, st.out[l], lse=st.lse[l], err=st.err,
+                                  workspace=st.workspace, early_reads=early)
+        torch.cuda.synchronize()
+        assert st.read_err() == 0
+        runs.append((wl, st))
+    (wa, sa), (wb, sb) = runs
+    assert torch.equal(wa.k_pool, wb.k_pool) and torch.equal(wa.v_pool, wb.v_pool)
+    assert torch.equal(sa.meta, sb.meta)
+    assert torch.equal(sa.sel_cnt, sb.sel_cnt) and torch.equal(sa.sel_idx, sb.sel_idx)
+    assert torch.equal(sa.out, sb.out)
+    assert torch.equal(sa.lse, sb.lse)
+    # and the waiting launches match the oracle
+    stats = parity.Stats()
+    for l in range(cfg.L_alloc):
+        for bb in range(cfg.B):
+            for h in range(cfg.Hkv):
+                parity.check_unit(wb, sb, l, bb, h, wb.q[l], None, stats, check_meta=False)
+    stats.check()
