@@ -42,7 +42,7 @@ def test_measured_traffic_is_reported_only_for_the_captured_workload_and_batch()
         captured = bench.load_traffic("decode_layer", cfg.name, cfg.B)
         # each capture is one launch of its workload: within a few percent of its algorithmic bytes
         launch = bench.algorithmic_bytes(cfg)["decode_launch"]
-        assert captured is None or launch <= captured < 1.05 * launch, c
+        assert captured is not None and launch <= captured < 1.05 * launch, c
     name = workloads.CONFIGS[2].name
     assert bench.load_traffic("decode_layer", name, 4) is None  # another batch: another launch
     assert bench.load_traffic("decode_layer", workloads.CONFIGS[4].name, workloads.CONFIGS[4].B) is None
