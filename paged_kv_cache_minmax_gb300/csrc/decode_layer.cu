@@ -49,6 +49,11 @@
 // receives tokens takes those rows from new_k / new_v rather than waiting for
 // the selectors' pool writes, which are for later launches.  Every wait is
 // bounded (KVMM_ERR_TIMEOUT, then the kernel runs to its end).
+// Launched with programmatic dependent launch: a launch waits for the
+// preceding kernel before its first read, or, with early cache reads
+// (KVMM_DECODE_EARLY_READS), computes its units' extents, copies their table
+// rows and starts streaming their metadata first, and waits before it reads
+// the queries, new rows, pools or kept selections, or stores anything.
 #include <cfloat>
 #include <cmath>
 
