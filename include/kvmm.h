@@ -311,7 +311,9 @@ kvmm_status page_score_topk_attn(const kvmm_shape* shape, int32_t layer, const k
  * layer's row), block_table and meta (the layer's rows).  The launch then
  * reads those while that kernel drains (the units' extents, their table
  * rows, the first metadata rows) and waits for it before it reads q, new_k,
- * new_v, the pools or the kept selections, and before it writes anything.
+ * new_v, the pools or the kept selections, and before it writes anything
+ * but the error bits of out-of-range lengths or token ranges (atomic ORs
+ * into err).
  * A decode loop meets this when those arrays change only between steps or
  * by this call itself: the layers' calls back to back, or the query
  * projection just before.  Other bits return KVMM_INVALID_ARG.  The

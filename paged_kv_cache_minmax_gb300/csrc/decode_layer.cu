@@ -53,7 +53,8 @@
 // preceding kernel before its first read, or, with early cache reads
 // (KVMM_DECODE_EARLY_READS), computes its units' extents, copies their table
 // rows and starts streaming their metadata first, and waits before it reads
-// the queries, new rows, pools or kept selections, or stores anything.
+// the queries, new rows, pools or kept selections, or stores anything but
+// error bits (atomic ORs into err).
 #include <cfloat>
 #include <cmath>
 
@@ -282,10 +283,11 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
     cluster_arrive();
     pdl_launch_dependents();
     // Every input may come from the preceding kernels, and the caller may read what this one writes only
-    // after it.  With early cache reads the caller vouches that the preceding kernel writes none of the
-    // cache state (descriptors' inputs, block table, metadata): this launch then computes its units'
-    // descriptors, copies their table rows and starts streaming their metadata while that kernel drains,
-    // and every thread waits for it before it reads the queries or new rows or writes anything.
+    // after it.  With early cache reads the caller vouches that the preceding kernel writes nothing this
+    // launch reads of the cache state (descriptors' inputs, block-table rows, metadata rows): this launch
+    // then computes its units' descriptors, copies their table rows and starts streaming their metadata
+    // while that kernel drains, and every thread waits for it before it reads the queries or new rows or
+    // writes anything (error bits, ORed atomically into err, aside).
     if (!p.early) pdl_wait();
 
     auto aborting = [&]() { return ld_volatile(&sh.abort_flag) != 0; };
