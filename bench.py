@@ -191,23 +191,23 @@ def run_oracle_units(states, threads):
 
 
 def cpu_baseline(cfg, target_seconds=12.0):
+    """The oracle on the host cores over whole layer-steps: every (batch, KV head) unit of one layer, each
+    unit's own pages (no unit's data stays cached for the next layer-step), repeated for about
+    ``target_seconds`` of wall time."""
     import oracle
 
     oracle.build()
     threads = os.cpu_count() or 1
     units_per_layer = cfg.B * cfg.Hkv
-    states = oracle_layer_sample(cfg, min(units_per_layer, 16))
-    t1 = run_oracle_units(states, 1) / len(states)  # seconds of CPU per unit-step
-    reps = max(1, int(target_seconds / max(t1 * len(states), 1e-6)))
-    work = states * reps
-    wall = run_oracle_units(work, threads)
-    unit_steps = len(work)
-    ls_per_s = unit_steps / units_per_layer / wall
+    states = oracle_layer_sample(cfg, units_per_layer)
+    first = run_oracle_units(states, threads)  # one layer-step (also warms the code)
+    reps = max(1, int(target_seconds / max(first, 1e-6)))
+    wall = sum(run_oracle_units(states, threads) for _ in range(reps))
+    ls_per_s = reps / wall
     return {"value": ls_per_s, "unit": "layer-steps/s", "cores": threads, "kind": "oracle",
-            "sample": f"{unit_steps} unit-steps ({len(states)} distinct (batch, KV head) units of one layer of "
-                      f"{cfg.name}, each: append+MinMax, score all {cfg.P} pages, top-{cfg.K}, diff, attention) "
-                      f"on {threads} threads; {unit_steps / units_per_layer:.1f} layer-steps of work, "
-                      f"{t1 * unit_steps:.1f} s single-thread CPU"}
+            "sample": f"{reps} layer-steps of {cfg.name}, each all {units_per_layer} (batch, KV head) units of one "
+                      f"layer (per unit: append+MinMax, score all {cfg.P} pages, top-{cfg.K}, diff, attention), "
+                      f"on {threads} threads; {wall:.1f} s wall"}
 
 
 def reference_arm(args):
@@ -266,6 +266,196 @@ def make_timing_events(n):
         return [torch.cuda.Event(enable_timing=True) for _ in range(n)], False
 
 
+def decode_layer_call(st, l, q, nk, nv, early_reads, mask=None, tok_begin=None, seq_len=None):
+    """decode_layer for layer ``l`` as the bench launches it: one new token per sequence written at
+    ``tok_begin`` (the sequence's last position; ``seq_len`` counts it), every page of the rescored units
+    scored, K selected, attention over them."""
+    tb = st.tok_begin if tok_begin is None else tok_begin
+    sl = st.seq_len if seq_len is None else seq_len
+    kvmm = _kvmm()
+    kvmm.decode_layer(st.shape, l, q, nk, nv, 1, tb, sl, st.k_pool, st.v_pool, st.block_table, st.meta, sl, mask,
+                      st.K, st.sel_idx, st.sel_cnt, st.out[l], lse=st.lse[l], err=st.err, workspace=st.workspace,
+                      early_reads=early_reads)
+
+
+def decode_step(st, path, L, q, nk, nv, early_reads, side, forks, mask=None, ev=None, tok_begin=None,
+                seq_len=None, total_promoted=None):
+    """One decode step exactly as the bench times it.  Per layer l: decode_layer (path "decode_layer"), or
+    kv_minmax_update and then page_score_topk_attn ("fused") or page_score_topk and sparse_paged_decode_attn
+    ("unfused"); and topk_promotion_diff on the stream ``side``, forked after the layer's selection and joined
+    at the end of the step.  q [L][B][Hq][D], nk / nv [L][B][Hkv][1][D]; ``ev``: 4 events a layer bracketing
+    the selection (or decode) launch and the attention launch."""
+    kvmm = _kvmm()
+    main = torch.cuda.current_stream()
+    tb = st.tok_begin if tok_begin is None else tok_begin
+    sl = st.seq_len if seq_len is None else seq_len
+    tp = st.total_promoted if total_promoted is None else total_promoted
+    for l in range(L):
+        if path != "decode_layer":
+            kvmm.kv_minmax_update(st.shape, l, nk[l], nv[l], 1, tb, sl, st.k_pool, st.v_pool, st.block_table,
+                                  st.meta, st.err)
+        if ev is not None:
+            ev[4 * l].record()
+        if path == "decode_layer":  # append, score, select and attend in one launch
+            decode_layer_call(st, l, q[l], nk[l], nv[l], early_reads, mask, tb, sl)
+        elif path == "fused":  # scoring, then attention that selects its own pages
+            kvmm.page_score_topk_attn(st.shape, l, q[l], st.meta, st.k_pool, st.v_pool, st.block_table, sl, mask,
+                                      st.K, st.sel_idx, st.sel_cnt, st.out[l], st.workspace, lse=st.lse[l],
+                                      err=st.err)
+        else:
+            kvmm.page_score_topk(st.shape, l, q[l], st.meta, sl, mask, st.K, st.sel_idx, st.sel_cnt, st.workspace,
+                                 st.err)
+        if ev is not None:
+            ev[4 * l + 1].record()
+        forks[l].record(main)
+        side.wait_event(forks[l])
+        with torch.cuda.stream(side):
+            kvmm.topk_promotion_diff(st.shape, l, mask, st.prev_idx, st.prev_cnt, st.sel_idx, st.sel_cnt,
+                                     st.promoted, st.promoted_cnt, st.evicted, st.evicted_cnt, tp, commit=True,
+                                     err=st.err)
+        if path == "unfused":
+            if ev is not None:
+                ev[4 * l + 2].record()
+            kvmm.sparse_paged_decode_attn(st.shape, l, q[l], st.k_pool, st.v_pool, st.block_table, sl, st.sel_idx,
+                                          st.sel_cnt, st.out[l], st.workspace, lse=st.lse[l], err=st.err,
+                                          num_splits=st.num_splits)
+            if ev is not None:
+                ev[4 * l + 3].record()
+    main.wait_stream(side)
+
+
+def _kvmm():
+    from paged_kv_cache_minmax_gb300 import kvmm
+
+    return kvmm
+
+
+class MixEpisode:
+    """The stable/unstable workload's decode episode (64 steps): step t appends one token per sequence at
+    position S + t, with queries drifting as q_t = 0.9 q_{t-1} + 0.44 eps, and rescores every unit when
+    t % rerank_period == 0, else only the unstable heads' units (the others keep their selection).  Every
+    step's inputs sit in buffers of their own, so each step is one CUDA graph; after the last step the
+    episode starts over at position S (those tokens are written again with the same values)."""
+
+    def __init__(self, wl, st):
+        cfg = wl.cfg
+        self.E = cfg.steps
+        self.period = cfg.rerank_period
+        self.q = workloads.drift_queries(wl, self.E)  # [E, L, B, Hq, D]
+        toks = [workloads.step_tokens(wl, t) for t in range(self.E)]
+        self.nk = torch.stack([k for k, _ in toks]).contiguous()  # [E, L, B, Hkv, 1, D]
+        self.nv = torch.stack([v for _, v in toks]).contiguous()
+        base = wl.seq_len.clone()
+        self.seq = torch.stack([base + t + 1 for t in range(self.E)]).contiguous()  # [E, B], after the append
+        self.tb = (self.seq - 1).contiguous()
+        self.unstable = wl.unstable.contiguous()
+        self.prom = torch.zeros(self.E, dtype=torch.int32, device=wl.q.device)  # promoted pages per step
+
+    def rerank(self, t):
+        return t % self.period == 0
+
+    def mask(self, t):
+        return None if self.rerank(t) else self.unstable
+
+    def rescored_units(self, t, B):
+        return None if self.rerank(t) else int(self.unstable.sum()) * B
+
+
+def promotion_stats(ep, st, graphs, stream, K, B):
+    """One pass over the episode from an empty selection, step by step: the pages topk_promotion_diff lists
+    per step, split by rerank steps (every unit rescored) and the steps between (unstable heads only), and
+    by stable and unstable heads, as a fraction of the K pages of the units that were rescored."""
+    st.prev_cnt.zero_()
+    st.sel_cnt.zero_()
+    torch.cuda.synchronize()  # zeroed on the default stream; the steps replay on `stream`
+    unst = ep.unstable.bool()[None, :, :].expand(B, -1, -1)  # [B, L, Hkv]
+    per_step = []
+    acc = {"rerank_stable": [0, 0], "rerank_unstable": [0, 0], "between_unstable": [0, 0]}
+    for t in range(ep.E):
+        with torch.cuda.stream(stream):
+            graphs[t].replay()
+        stream.synchronize()
+        pc = st.promoted_cnt.clone()
+        per_step.append(int(pc.sum()))
+        if t == 0:
+            continue  # the first selection promotes every page: not a rerank of a running decode
+        if ep.rerank(t):
+            for key, sel in (("rerank_stable", ~unst), ("rerank_unstable", unst)):
+                acc[key][0] += int(pc[sel].sum())
+                acc[key][1] += int(sel.sum()) * K
+        else:
+            acc["between_unstable"][0] += int(pc[unst].sum())
+            acc["between_unstable"][1] += int(unst.sum()) * K
+    frac = {k: (v[0] / v[1] if v[1] else None) for k, v in acc.items()}
+    return {"promoted_per_step": per_step, "promoted_fraction_of_k": frac,
+            "how": "one episode from an empty selection, step by step; step 0 (the first selection) is left out "
+                   "of the fractions; a fraction is promoted pages / (rescored units x K)"}
+
+
+def time_graphs(graph_list, stream, reps):
+    """Mean ms of one replay of each graph: all replayed back to back ``reps`` times between two CUDA
+    events on ``stream`` (after three untimed rounds)."""
+    out = []
+    for g in graph_list:
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                g.replay()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record()
+            for _ in range(reps):
+                g.replay()
+            e1.record()
+        stream.synchronize()
+        out.append(e0.elapsed_time(e1) / reps)
+    return out
+
+
+def separate_calls_leg(st, cfg, L, q_dev, stream, reps, peak):
+    """page_score_topk alone, sparse_paged_decode_attn alone (over the selection the first leaves) and the
+    two back to back, each as L launches of one CUDA graph replayed back to back (every unit rescored, the
+    automatic split count).  Per launch: CUDA-event time and the algorithmic bytes of that call."""
+    kvmm = _kvmm()
+
+    def score(l):
+        kvmm.page_score_topk(st.shape, l, q_dev[l], st.meta, st.seq_len, None, st.K, st.sel_idx, st.sel_cnt,
+                             st.workspace, st.err)
+
+    def attn(l):
+        kvmm.sparse_paged_decode_attn(st.shape, l, q_dev[l], st.k_pool, st.v_pool, st.block_table, st.seq_len,
+                                      st.sel_idx, st.sel_cnt, st.out[l], st.workspace, lse=st.lse[l], err=st.err,
+                                      num_splits=st.num_splits)
+
+    with torch.cuda.stream(stream):
+        for l in range(L):
+            score(l)
+            attn(l)
+    stream.synchronize()
+    graphs = []
+    for body in ((score,), (attn,), (score, attn)):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for l in range(L):
+                for fn in body:
+                    fn(l)
+        graphs.append(g)
+    ms_s, ms_a, ms_p = (m / L for m in time_graphs(graphs, stream, reps))
+    b = algorithmic_bytes(cfg)
+
+    def rec(ms, nbytes):
+        gbs = nbytes / (ms / 1e3) / 1e9
+        return {"us_per_launch": ms * 1e3, "bytes_per_launch": nbytes, "gbs": gbs, "frac": gbs / peak}
+
+    both = b["score_launch"] + b["attn_launch"]
+    return {"page_score_topk": rec(ms_s, b["score_launch"]),
+            "sparse_paged_decode_attn": rec(ms_a, b["attn_launch"]),
+            "sum_of_alone": rec(ms_s + ms_a, both),
+            "back_to_back": rec(ms_p, both),
+            "how": f"{L} launches of each call (or {L} pairs) in one CUDA graph, replayed {reps} times between "
+                   "CUDA events on the launching stream; per launch = region / launches; bytes per launch: "
+                   "the call's metadata or selected K/V plus its small terms"}
+
+
 def gpu_arm(args):
     from paged_kv_cache_minmax_gb300 import build as kbuild
     from paged_kv_cache_minmax_gb300 import kvmm
@@ -289,114 +479,95 @@ def gpu_arm(args):
     L = cfg.L_alloc  # a step rotates over the allocated layers
     # replicas: every rank decodes its own batch (seeded per rank); no collective on the data path
     wl = workloads.generate(cfg, device="cuda", seed=replica_seed(cfg, rank))
-    splits = kvmm.auto_splits(kvmm.make_shape(cfg.B, L, cfg.Hq, cfg.Hkv, cfg.D, cfg.T, cfg.Pmax, cfg.K,
-                                              wl.n_phys))
+    shape = kvmm.make_shape(cfg.B, L, cfg.Hq, cfg.Hkv, cfg.D, cfg.T, cfg.Pmax, cfg.K, wl.n_phys)
+    splits = kvmm.auto_splits(shape)
     st = DecodeState.for_workload(wl, num_splits=splits)
     one_launch = True  # decode_layer runs its one-launch kernel (else its two-kernel fallback)
     if args.path == "decode_layer":
-        c_ctas = kvmm.decode_layer_cluster(kvmm.make_shape(cfg.B, L, cfg.Hq, cfg.Hkv, cfg.D, cfg.T, cfg.Pmax,
-                                                           cfg.K, wl.n_phys))
+        c_ctas = kvmm.decode_layer_cluster(shape)
         one_launch = c_ctas > 0
-        launch_shape = ({"units_per_cluster": kvmm.decode_layer_units(kvmm.make_shape(
-                             cfg.B, L, cfg.Hq, cfg.Hkv, cfg.D, cfg.T, cfg.Pmax, cfg.K, wl.n_phys)),
-                         "cluster_ctas": c_ctas} if one_launch else
+        launch_shape = ({"units_per_cluster": kvmm.decode_layer_units(shape), "cluster_ctas": c_ctas}
+                        if one_launch else
                         {"splits": splits, "decode_layer": "falls back to kv_minmax_update + page_score_topk_attn "
                                                            "(per-CTA buffers exceed shared memory)"})
     else:
         launch_shape = {"splits": splits}
-    # the rerank schedule: with an unstable share, a step rescores every unit every `rerank_period` steps and
-    # only the unstable heads' units otherwise (the others keep their selection)
-    mask_unstable = wl.unstable.contiguous() if cfg.unstable_frac > 0 else None
-    period = cfg.rerank_period if mask_unstable is not None else 1
-    st.build_metadata()
-    nk, nv = workloads.step_tokens(wl, 0)
-    # the current token sits at position seq_len - 1 and is rewritten every step
-    st.tok_begin.copy_(wl.seq_len - 1)
-    q_dev = wl.q.clone()
-    nk_dev, nv_dev = nk.clone(), nv.clone()
-    stream = torch.cuda.Stream()
-
-    ev_s, external = make_timing_events(4 * L)
-    # the promotion diff is not needed by attention: it runs on a side stream
-    # forked after each selection and joined at the end of the step
-    side = torch.cuda.Stream()
-    forks = [torch.cuda.Event() for _ in range(L)]
-
     path = args.path
-    fused = path != "unfused"  # one timed launch group per layer (decode_layer, or scoring + attention)
     # the layers' decode_layer calls follow one another on the stream, and none writes what the next reads
     # of the cache state (its own layer's rows only; lengths and masks change between steps): each launch
-    # may stream its metadata while the previous one drains (KVMM_DECODE_EARLY_READS)
-    early_reads = not args.no_early_reads
+    # may stream its metadata while the previous one drains (KVMM_DECODE_EARLY_READS).  With one allocated
+    # layer consecutive calls are for the same layer, and the earlier one writes the metadata row the later
+    # one would read early: the flag stays off there.
+    early_reads = not args.no_early_reads and L >= 2
+    st.build_metadata()
+    stream = torch.cuda.Stream()
+    side = torch.cuda.Stream()  # the promotion diff is not needed by attention: a side stream
+    forks = [torch.cuda.Event() for _ in range(L)]
+    ev_s, external = make_timing_events(4 * L)
 
-    def decode_layer_call(l, mask=None):
-        kvmm.decode_layer(st.shape, l, q_dev[l], nk_dev[l], nv_dev[l], 1, st.tok_begin, st.seq_len,
-                          st.k_pool, st.v_pool, st.block_table, st.meta, st.seq_len, mask, st.K, st.sel_idx,
-                          st.sel_cnt, st.out[l], lse=st.lse[l], err=st.err, workspace=st.workspace,
-                          early_reads=early_reads)
+    episode = cfg.steps > 0
+    if episode:
+        # the stable/unstable workload: a drifting decode episode, one graph per step
+        ep = MixEpisode(wl, st)
+        E = ep.E
 
-    def step(instrument, mask=None):
-        main = torch.cuda.current_stream()
-        for l in range(L):
-            if path != "decode_layer":
-                kvmm.kv_minmax_update(st.shape, l, nk_dev[l], nv_dev[l], 1, st.tok_begin, st.seq_len, st.k_pool,
-                                      st.v_pool, st.block_table, st.meta, st.err)
-            if instrument:
-                ev_s[4 * l].record()
-            if path == "decode_layer":  # append, score, select and attend in one launch
-                decode_layer_call(l, mask)
-            elif path == "fused":  # scoring, then attention that selects its own pages
-                st.select_attend(l, q_dev[l], rescore_mask=mask)
-            else:
-                st.select(l, q_dev[l], rescore_mask=mask)
-            if instrument:
-                ev_s[4 * l + 1].record()
-            forks[l].record(main)
-            side.wait_event(forks[l])
-            with torch.cuda.stream(side):
-                st.diff(l, rescore_mask=mask)
-            if not fused:
-                if instrument:
-                    ev_s[4 * l + 2].record()
-                st.attend(l, q_dev[l])
-                if instrument:
-                    ev_s[4 * l + 3].record()
-        main.wait_stream(side)
+        def step_inputs(t):
+            return dict(q=ep.q[t], nk=ep.nk[t], nv=ep.nv[t], mask=ep.mask(t), tok_begin=ep.tb[t],
+                        seq_len=ep.seq[t], total_promoted=ep.prom[t:t + 1])
+    else:
+        # one token per sequence at position seq_len - 1, written again every step with the same values
+        E = 1
+        nk0, nv0 = workloads.step_tokens(wl, 0)
+        st.tok_begin.copy_(wl.seq_len - 1)
+        q_dev, nk_dev, nv_dev = wl.q.clone(), nk0.clone(), nv0.clone()
+
+        def step_inputs(t):
+            return dict(q=q_dev, nk=nk_dev, nv=nv_dev)
+
+    def run_step(t, ev=None):
+        a = step_inputs(t)
+        decode_step(st, path, L, a["q"], a["nk"], a["nv"], early_reads, side, forks, mask=a.get("mask"), ev=ev,
+                    tok_begin=a.get("tok_begin"), seq_len=a.get("seq_len"), total_promoted=a.get("total_promoted"))
 
     torch.cuda.empty_cache()
+    torch.cuda.synchronize()  # the set-up ran on the default stream; everything below runs on `stream`
     with torch.cuda.stream(stream):
-        for _ in range(3):
-            step(False)
+        for t in range(min(3, E) if episode else 3):
+            run_step(t)
     stream.synchronize()
     if args.no_graph:  # eager launches (profiling): same kernels, host-issued every step
         external = False
 
         class _Eager:
-            def replay(self):
-                step(False)
+            def __init__(self, t):
+                self.t = t
 
-        graph, graph_instr = _Eager(), None
+            def replay(self):
+                run_step(self.t)
+
+        graphs = [_Eager(t) for t in range(E)]
+        graph_instr = None
     else:
-        graph = torch.cuda.CUDAGraph()
-        external = external and period == 1  # with a rerank schedule the roofline uses the graph below
+        graphs = []
+        for t in range(E):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                run_step(t)
+            graphs.append(g)
+        external = external and not episode  # the episode's roofline uses the graph below
         graph_instr = torch.cuda.CUDAGraph() if external else None
-        with torch.cuda.graph(graph, stream=stream):
-            step(False)
-        if mask_unstable is not None:  # the steps between reranks: only the unstable heads rescore
-            graph_u = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(graph_u, stream=stream):
-                step(False, mask_unstable)
         if external:
             with torch.cuda.graph(graph_instr, stream=stream):
-                step(True)
+                run_step(0, ev_s)
+    promotions = None
+    if episode:  # first, the episode once from an empty selection, counting promotions
+        promotions = promotion_stats(ep, st, graphs, stream, cfg.K, cfg.B)
     st.err.zero_()
-
-    def replay(i):  # step i of the rerank schedule
-        (graph if i % period == 0 or args.no_graph else graph_u).replay()
+    torch.cuda.synchronize()
 
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
-            replay(i)
+            graphs[i % E].replay()
     stream.synchronize()
 
     # ---- timed region (device-resident inputs) --------------------------------
@@ -405,15 +576,16 @@ def gpu_arm(args):
     torch.cuda.synchronize()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local_rank, args.clocks_log)
+    timed_steps = [(args.warmup + i) % E for i in range(args.steps)]
     with clocks:
         time.sleep(0.3)
         with torch.cuda.stream(stream):
             t0.record()
-            for i in range(args.steps):
+            for i, t in enumerate(timed_steps):
                 if external and i == args.steps - 1:
                     graph_instr.replay()  # the last step also stamps every kernel launch
                 else:
-                    replay(i)
+                    graphs[t].replay()
             t1.record()
         stream.synchronize()
     torch.cuda.synchronize()
@@ -422,38 +594,37 @@ def gpu_arm(args):
 
     if not external:  # eager instrumented step: per-launch durations on the launching stream
         with torch.cuda.stream(stream):
-            step(True)
+            run_step(0, ev_s)
         stream.synchronize()
     # the dominant kernel alone, in the bench's launch configuration: the L decode_layer launches of a step
-    # back to back in one graph (no event between launches, so programmatic dependent launch still lets
-    # each launch's CTAs be scheduled while its predecessor drains); per launch = region / launches
+    # (every unit rescored) back to back in one graph (no event between launches, so programmatic dependent
+    # launch still lets each launch's CTAs be scheduled while its predecessor drains); per launch = region /
+    # launches
     dl_ms = None
     if path == "decode_layer" and not args.no_graph:
+        a = step_inputs(0)
         g_dl = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g_dl, stream=stream):
             for l in range(L):
-                decode_layer_call(l)
-        reps = max(3, min(args.steps, 100))
-        d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            for _ in range(3):
-                g_dl.replay()
-            d0.record()
-            for _ in range(reps):
-                g_dl.replay()
-            d1.record()
-        stream.synchronize()
-        dl_ms = d0.elapsed_time(d1) / (reps * L)
+                decode_layer_call(st, l, a["q"][l], a["nk"][l], a["nv"][l], early_reads, None, a.get("tok_begin"),
+                                  a.get("seq_len"))
+        dl_ms = time_graphs([g_dl], stream, max(3, min(args.steps, 100)))[0] / L
     score_ms = [ev_s[4 * l].elapsed_time(ev_s[4 * l + 1]) for l in range(L)]
-    attn_ms = [ev_s[4 * l + 2].elapsed_time(ev_s[4 * l + 3]) for l in range(L)] if not fused else [0.0]
+    attn_ms = [ev_s[4 * l + 2].elapsed_time(ev_s[4 * l + 3]) for l in range(L)] if path == "unfused" else [0.0]
+    peak, peak_kind = peaks()
+    sep = None
+    if path == "decode_layer" and not episode and not args.no_graph and not args.no_separate_calls:
+        sep = separate_calls_leg(st, cfg, L, q_dev, stream, max(3, min(args.steps // 4, 50)), peak)
 
     # ---- end to end: host buffers in, host results out ------------------------
-    q_host = wl.q.cpu().pin_memory()
-    nk_host, nv_host = nk.cpu().pin_memory(), nv.cpu().pin_memory()
+    # every step copies that step's queries and new K/V rows from pinned host memory into the buffers its
+    # graph reads, replays the graph, and copies out, lse and the promoted counts to pinned host memory
+    in_dev = [(a["q"], a["nk"], a["nv"]) for a in (step_inputs(t) for t in range(E))]
+    in_host = [tuple(x.cpu().pin_memory() for x in trio) for trio in in_dev]
     out_host = torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory()
     lse_host = torch.empty(st.lse.shape, dtype=st.lse.dtype).pin_memory()
     prom_host = torch.empty(st.promoted_cnt.shape, dtype=torch.int32).pin_memory()
-    h2d = q_host.numel() * 2 + nk_host.numel() * 2 * 2
+    h2d = sum(x.numel() * x.element_size() for x in in_host[0])
     d2h = out_host.numel() * 4 + lse_host.numel() * 4 + prom_host.numel() * 4
     e2e_steps = max(3, min(args.steps, 200))
     if dist:
@@ -463,10 +634,10 @@ def gpu_arm(args):
     with torch.cuda.stream(stream):
         e0.record()
         for i in range(e2e_steps):
-            q_dev.copy_(q_host, non_blocking=True)
-            nk_dev.copy_(nk_host, non_blocking=True)
-            nv_dev.copy_(nv_host, non_blocking=True)
-            replay(i)
+            t = i % E
+            for d, h in zip(in_dev[t], in_host[t]):
+                d.copy_(h, non_blocking=True)
+            graphs[t].replay()
             out_host.copy_(st.out, non_blocking=True)
             lse_host.copy_(st.lse, non_blocking=True)
             prom_host.copy_(st.promoted_cnt, non_blocking=True)
@@ -479,20 +650,21 @@ def gpu_arm(args):
             dist.destroy_process_group()
         return
 
-    acc = acc_all = algorithmic_bytes(cfg)
-    if mask_unstable is not None:  # average over the schedule: every unit on a rerank step, else the unstable
-        n_u = float(wl.unstable.sum()) * cfg.B / L
-        acc = algorithmic_bytes(cfg, rescored_units=(cfg.B * cfg.Hkv + (period - 1) * n_u) / period)
+    acc_all = algorithmic_bytes(cfg)
+    if episode:  # the bytes of the steps actually timed: every unit on a rerank step, else the unstable heads'
+        tot = sum(algorithmic_bytes(cfg, rescored_units=ep.rescored_units(t, cfg.B))["total"] for t in timed_steps)
+        acc = {"total": tot / len(timed_steps)}
+    else:
+        acc = acc_all
     n_ls = args.steps * L * world
     secs = ms_total / 1e3
     value = n_ls / secs
     kv_gbs = acc["total"] * n_ls / secs / 1e9
-    peak, peak_kind = peaks()
     s_ms, a_ms = statistics.mean(score_ms), statistics.mean(attn_ms)
     if path == "decode_layer":
         dom, dom_ms, dom_bytes = "decode_layer", (dl_ms if dl_ms is not None else s_ms), acc_all["decode_launch"]
         kernel_ms = {"decode_layer": dom_ms, "decode_layer_event_bracketed": s_ms}
-    elif fused:
+    elif path == "fused":
         dom, dom_ms, dom_bytes = "page_score_topk_attn", s_ms, acc_all["fused_launch"]
         kernel_ms = {"page_score_topk_attn": s_ms}
     else:
@@ -504,6 +676,10 @@ def gpu_arm(args):
     achieved = dom_bytes / (dom_ms / 1e3) / 1e9
     traffic = load_traffic(dom, workloads.CONFIGS[args.config].name, cfg.B)
     clk = clocks.summary()
+    step_desc = (f"one decode step = {L} layer-steps, " + ("eager launches" if args.no_graph else "CUDA graph replay"))
+    if episode:
+        step_desc += (f"; steps cycle through a {E}-step episode (drifting queries, one appended token per step, "
+                      f"every unit rescored every {ep.period} steps and the unstable heads' units in between)")
     line = {
         "metric": METRIC, "value": value, "unit": "layer-steps/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_total / args.steps, "higher_is_better": True,
@@ -514,8 +690,7 @@ def gpu_arm(args):
                    "top_k_pages": cfg.K, **launch_shape, "parallelism": f"replicas x{world}",
                    "l2": f"inputs larger than L2 ({L * (acc_all['meta'] + acc_all['kv']) / 2**30:.1f} GiB of distinct "
                          "data per step, no flush)",
-                   "step": f"one decode step = {L} layer-steps, " + ("eager launches" if args.no_graph
-                                                                     else "CUDA graph replay"),
+                   "step": step_desc,
                    "path": {"decode_layer": "decode_layer (append, score, select, attend: one launch)",
                             "fused": "kv_minmax_update + page_score_topk_attn (scoring kernel + selecting "
                                      "attention kernel)",
@@ -529,8 +704,8 @@ def gpu_arm(args):
                      "frac": achieved / peak, "traffic": traffic, "kernel": dom,
                      "peak_source": f"{peak_kind} hbm_gbs (burst copy)",
                      "achieved_bytes_per_launch": dom_bytes, "launch_ms": dom_ms,
-                     "launch_timing": (f"CUDA events around {L}-launch graph replays of decode_layer alone, "
-                                       "back to back; per launch = region / launches"
+                     "launch_timing": (f"CUDA events around {L}-launch graph replays of decode_layer alone "
+                                       "(every unit rescored), back to back; per launch = region / launches"
                                        if dl_ms is not None else
                                        "CUDA events around each launch in the last timed step"
                                        if external else "CUDA events, eager instrumented step after timing")},
@@ -543,6 +718,13 @@ def gpu_arm(args):
         "clocks": clk,
         "device_err": err_word,
     }
+    if sep is not None:
+        line["separate_calls"] = sep
+    if promotions is not None:
+        line["promotions"] = promotions
+    par = load_parity(workloads.CONFIGS[args.config].name, launch_shape, early_reads)
+    if par is not None:
+        line["parity"] = par
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(cfg)
     print(json.dumps(line), flush=True)
@@ -580,6 +762,7 @@ def stability_arm(args):
         prof.record(state)
     # each call is captured in a CUDA graph and replayed, so the events time the device, not the host
     stream = torch.cuda.Stream()
+    torch.cuda.synchronize()  # the set-up above ran on the default stream
     e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
     reps = max(args.steps, 20)
     with torch.cuda.stream(stream):
@@ -657,6 +840,7 @@ def promote_arm(args):
     moved = torch.zeros(B, 1, Hkv, dtype=torch.int32, device="cuda")
     bytes_per_call = units * n_move * 2 * T * D * 2
     stream = torch.cuda.Stream()
+    torch.cuda.synchronize()  # the set-up above ran on the default stream
     results = {}
     for ctas in (4, 8, 16, 32, 64, 152):
         def pair():
@@ -717,6 +901,7 @@ def table_update_arm(args):
     val = torch.randint(-1, n_phys, (idx.numel(),), generator=gen, dtype=torch.int32).pin_memory()
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     stream = torch.cuda.Stream()
+    torch.cuda.synchronize()  # the set-up above ran on the default stream
 
     def timed(fn, reps):
         with torch.cuda.stream(stream):
@@ -774,6 +959,7 @@ def meankey_arm(args):
     sel_mk = torch.zeros_like(st.sel_idx)
     cnt_mk = torch.zeros_like(st.sel_cnt)
     stream = torch.cuda.Stream()
+    torch.cuda.synchronize()  # the set-up above ran on the default stream
 
     def timed(fn, reps):
         with torch.cuda.stream(stream):
@@ -823,6 +1009,28 @@ def meankey_arm(args):
         "device_err": st.read_err()}), flush=True)
 
 
+def load_parity(workload, launch_shape, early_reads):
+    """The GPU-versus-oracle parity record of ``workload`` at the benchmark's launch shape, written by the
+    ``-m gpu`` tests (tests/test_gpu_bench_shapes.py) into profiles/parity.json, with two checks: whether it
+    was taken with the current CUDA sources, and whether its launch shape and flags are the ones timed here."""
+    from paged_kv_cache_minmax_gb300 import build as kbuild
+
+    path = os.path.join(ROOT, "profiles", "parity.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    rec = d.get(workload)
+    if rec is None:
+        return None
+    out = dict(rec)
+    out["current_sources"] = rec.get("sources") == kbuild.source_digest()
+    mine = {k: launch_shape[k] for k in ("units_per_cluster", "cluster_ctas") if k in launch_shape}
+    out["launch_shape_matches"] = (rec.get("launch_shape") == mine and
+                                   bool(rec.get("early_reads")) == bool(early_reads))
+    return out
+
+
 def load_traffic(kernel, workload, batch):
     """dram bytes per launch of ``kernel`` on ``workload`` from the committed ncu summaries, if one
     was captured at that batch (a launch covers one layer, so the layer count does not matter)."""
@@ -857,6 +1065,8 @@ def main():
                     help="time the promotion transfer from pinned host memory instead")
     ap.add_argument("--stability", action="store_true",
                     help="time head-stability profiling (history record, RCO and classification) instead")
+    ap.add_argument("--no-separate-calls", action="store_true",
+                    help="skip timing page_score_topk and sparse_paged_decode_attn as separate calls")
     ap.add_argument("--no-early-reads", action="store_true",
                     help="decode_layer waits for the preceding kernel before any read (no KVMM_DECODE_EARLY_READS)")
     ap.add_argument("--path", default="decode_layer", choices=["decode_layer", "fused", "unfused"],

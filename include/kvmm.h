@@ -147,9 +147,9 @@ kvmm_status kv_minmax_update(const kvmm_shape* shape, int32_t layer, const kvmm_
  * method, 3": stable heads reuse their previous top-K between reranks).
  * scores_out, if not NULL, is [B][Hkv][Pmax] float and receives the fp32
  * scores of rescored units (pages >= P are not written).
- * workspace must hold kvmm_workspace_size(shape, 0) bytes, be zero-filled
- * before its first use, and not be modified by the caller between calls
- * (every call leaves its counters at zero again).
+ * workspace must hold kvmm_workspace_size(shape, 0) bytes of device memory;
+ * it needs no initialisation (the call writes every score it reads) and
+ * holds nothing between calls.
  * Requires 1 <= K <= Kmax; a sequence longer than Pmax*T sets
  * KVMM_ERR_OUT_OF_RANGE and is scored over its first Pmax pages.
  */
@@ -172,15 +172,17 @@ kvmm_status page_score_topk(const kvmm_shape* shape, int32_t layer, const kvmm_b
  * Same arguments, semantics and results as page_score_topk, minus
  * workspace / workspace_bytes.  The scratch is one fixed 4 MiB array in the
  * library's own device memory (every GPU that loads libkvmm holds it until
- * the process exits): up to 4096 (batch, KV head) units of a layer and
- * B * Hkv * Pmax <= 1,044,480 scores; a larger shape returns
- * KVMM_WORKSPACE_TOO_SMALL and nothing runs.  The first call on a device
- * looks up the array's device address and zeroes its counters on `stream`;
- * make that first call before any stream capture.  Every call on a device
- * shares the one array and leaves its last contents in it, so calls whose
- * kernels overlap on the GPU (different streams, or concurrent host
- * threads) race and give wrong selections; serialise them (calls on one
- * stream never overlap).
+ * the process exits): it takes B * Hkv * Pmax <= 1,048,576 scores; a larger
+ * shape returns KVMM_WORKSPACE_TOO_SMALL and nothing runs.  The first call
+ * on a device looks up the array's device address (cudaGetSymbolAddress,
+ * once per device, cached); make that first call before any stream
+ * capture.  The cached address belongs to the device's current context: a
+ * process that calls cudaDeviceReset on a device must not call this entry
+ * point on that device again.  Every call on a device shares the one array
+ * and leaves its last contents in it (nothing needs to start at zero: each
+ * call writes every score it reads), so calls whose kernels overlap on the
+ * GPU (different streams, or concurrent host threads) race and give wrong
+ * selections; serialise them (calls on one stream never overlap).
  */
 kvmm_status page_score_topk_static_scratch(const kvmm_shape* shape, int32_t layer, const kvmm_bf16* q,
                                            const kvmm_bf16* meta, const int32_t* seq_len,
@@ -306,18 +308,27 @@ kvmm_status page_score_topk_attn(const kvmm_shape* shape, int32_t layer, const k
  * flags: 0, or KVMM_DECODE_EARLY_READS.  By default the launch reads nothing
  * before the kernel launched just before it on the stream has finished
  * (programmatic dependent launch lets it be scheduled meanwhile).  With
- * KVMM_DECODE_EARLY_READS the caller guarantees that that kernel writes
- * nothing this call reads of seq_len, tok_begin, tok_end, rescore_mask (the
- * layer's row), block_table and meta (the layer's rows).  The launch then
- * reads those while that kernel drains (the units' extents, their table
- * rows, the first metadata rows) and waits for it before it reads q, new_k,
- * new_v, the pools or the kept selections, and before it writes anything
- * but the error bits of out-of-range lengths or token ranges (atomic ORs
- * into err).
- * A decode loop meets this when those arrays change only between steps or
- * by this call itself: the layers' calls back to back, or the query
- * projection just before.  Other bits return KVMM_INVALID_ARG.  The
- * two-kernel fallback always waits.
+ * KVMM_DECODE_EARLY_READS the caller guarantees that no kernel still running
+ * when this launch starts writes anything this call reads of seq_len,
+ * tok_begin, tok_end, rescore_mask (the layer's row), block_table and meta
+ * (the layer's rows).  The launch then reads those while that kernel drains
+ * (the units' extents, their table rows, the first metadata rows) and waits
+ * for it before it reads q, new_k, new_v, the pools or the kept selections,
+ * and before it writes anything but the error bits of out-of-range lengths
+ * or token ranges (atomic ORs into err).
+ * Every kvmm kernel lets the next launch start only after its own wait for
+ * its predecessor has returned, so when the kernel just before this call is
+ * a kvmm call (or a kernel launched without programmatic dependent launch),
+ * it is the only kernel that can still be running: the guarantee is then
+ * about that one kernel.  A decode loop meets it when those arrays change
+ * only between steps or by the call itself and consecutive decode_layer
+ * calls on the stream are for different layers (the layers of a step back
+ * to back, two or more layers), or when the query projection runs just
+ * before.  Two decode_layer calls for the SAME layer back to back (a
+ * one-layer loop) do not meet it: the first writes the metadata row of the
+ * page it appends to, which the second would read early; leave the flag off
+ * there.  Other bits return KVMM_INVALID_ARG.  The two-kernel fallback always
+ * waits.
  */
 #define KVMM_DECODE_EARLY_READS 1u
 kvmm_status decode_layer(const kvmm_shape* shape, int32_t layer, const kvmm_bf16* q, const kvmm_bf16* new_k,

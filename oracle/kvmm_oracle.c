@@ -38,7 +38,8 @@
  *   KVDrive, "Method details": each page's mean key is its representative
  *   in the index; the mean-key scorer ranks pages by q . mean.
  *
- * Readings taken where the pages are silent (each is listed in the design doc):
+ * Readings taken where the pages are silent (the plainest one the rest of
+ *   the pages supports; none of these points is printed on either page):
  *   - page score for one query head: sum_d max(q_d*min_d, q_d*max_d), the
  *     exact maximum of q.k over the box [min, max];
  *   - GQA: the KV head's score is the SUM of its query heads' scores

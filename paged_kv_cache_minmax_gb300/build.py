@@ -41,6 +41,22 @@ def _deps() -> list[str]:
         glob.glob(os.path.join(INCLUDE, "*.h")) + [os.path.abspath(__file__)]
 
 
+def source_digest() -> str:
+    """A short sha256 over the CUDA sources and the public header.  A record of results measured on the GPU
+    (the parity record of the benchmark's workloads) names the sources it was taken with, so a reader can tell
+    whether it still describes the current kernels."""
+    import hashlib
+
+    h = hashlib.sha256()
+    paths = sorted(_sources() + glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(CSRC, "*.cuh")))
+    paths += sorted(glob.glob(os.path.join(INCLUDE, "*.h")))
+    for p in paths:
+        h.update(os.path.relpath(p, ROOT).encode())
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
 def up_to_date() -> bool:
     if not os.path.exists(LIB_PATH):
         return False

@@ -68,7 +68,7 @@ int resolve_splits(const kvmm_shape& s, int32_t num_splits, bool select = false)
     return splits;
 }
 
-size_t score_ws_bytes(const kvmm_shape& s) { return kvmm::ws_counter_bytes(s) + kvmm::ws_scores_bytes(s); }
+size_t score_ws_bytes(const kvmm_shape& s) { return kvmm::ws_scores_bytes(s); }
 
 thread_local cudaError_t g_last_cuda_error = cudaSuccess;
 
@@ -197,8 +197,7 @@ static kvmm_status score_topk_call(const kvmm_shape* shape, int32_t layer, const
     p.sel_idx = sel_idx;
     p.sel_cnt = sel_cnt;
     p.scores_out = scores_out;
-    p.counters = static_cast<int32_t*>(workspace);
-    p.scores_ws = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + kvmm::ws_counter_bytes(s));
+    p.scores_ws = static_cast<float*>(workspace);
     p.err = err;
     return launched(mean ? kvmm::launch_score_topk_mean(p, group_reduce, reinterpret_cast<cudaStream_t>(stream))
                          : kvmm::launch_score_topk(p, group_reduce, reinterpret_cast<cudaStream_t>(stream)));
@@ -267,14 +266,11 @@ kvmm_status page_score_topk_static_scratch(const kvmm_shape* shape, int32_t laye
     if (!req(q) || !req(meta) || !req4(seq_len) || !req4(sel_idx) || !req4(sel_cnt) || !opt4(scores_out) ||
         !opt4(err))
         return KVMM_INVALID_ARG;
-    // the shape must fit the fixed scratch: counters region, then B*Hkv*Pmax scores
-    const size_t units = size_t(s.B) * s.Hkv;
-    if (units * sizeof(int32_t) > kvmm::kStaticScratchCounterBytes ||
-        kvmm::kStaticScratchCounterBytes + units * s.Pmax * sizeof(float) > kvmm::kStaticScratchBytes)
-        return KVMM_WORKSPACE_TOO_SMALL;
+    // the shape must fit the fixed scratch: B*Hkv*Pmax scores
+    if (size_t(s.B) * s.Hkv * s.Pmax * sizeof(float) > kvmm::kStaticScratchBytes) return KVMM_WORKSPACE_TOO_SMALL;
     void* scratch = nullptr;
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-    const cudaError_t se = kvmm::static_scratch_for_current_device(&scratch, cs);
+    const cudaError_t se = kvmm::static_scratch_for_current_device(&scratch);
     if (se != cudaSuccess) return launched(se);
     ScoreParams p{};
     p.B = s.B;
@@ -295,8 +291,7 @@ kvmm_status page_score_topk_static_scratch(const kvmm_shape* shape, int32_t laye
     p.sel_idx = sel_idx;
     p.sel_cnt = sel_cnt;
     p.scores_out = scores_out;
-    p.counters = static_cast<int32_t*>(scratch);
-    p.scores_ws = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + kvmm::kStaticScratchCounterBytes);
+    p.scores_ws = static_cast<float*>(scratch);
     p.err = err;
     return launched(kvmm::launch_score_topk(p, group_reduce, cs));
 }
@@ -385,7 +380,7 @@ kvmm_status page_score_topk_attn(const kvmm_shape* shape, int32_t layer, const k
                                         sm_scale, 0, out, lse, nullptr, 0, err, stream);
     }
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-    float* scores_ws = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + kvmm::ws_counter_bytes(s));
+    float* scores_ws = static_cast<float*>(workspace);
     ScoreParams sp{};
     sp.B = s.B;
     sp.L = s.L;
@@ -405,7 +400,6 @@ kvmm_status page_score_topk_attn(const kvmm_shape* shape, int32_t layer, const k
     sp.sel_idx = sel_idx;
     sp.sel_cnt = sel_cnt;
     sp.scores_out = scores_out;
-    sp.counters = static_cast<int32_t*>(workspace);
     sp.scores_ws = scores_ws;
     sp.err = err;
     const cudaError_t e = kvmm::launch_score_only(sp, group_reduce, cs);

@@ -225,6 +225,17 @@ __device__ __forceinline__ void red_async_minmax_u32(uint32_t* local, uint64_t* 
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// Every kvmm kernel lets its dependents be scheduled only after its own wait
+// has returned: in a chain A -> B -> C of these launches, C's CTAs then start
+// only once A has finished, so a launch that reads part of its inputs before
+// its wait (decode_layer with KVMM_DECODE_EARLY_READS) overlaps the kernel
+// launched just before it and no earlier one.
+__device__ __forceinline__ void pdl_wait_then_release()
+{
+    pdl_wait();
+    pdl_launch_dependents();
+}
+
 // ---------------------------------------------------------------------------
 // loads
 __device__ __forceinline__ uint4 ld_shared_v4(const void* p)

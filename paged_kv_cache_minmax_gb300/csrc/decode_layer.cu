@@ -281,14 +281,15 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
     // every CTA's barriers exist before the first remote arrival: the cluster barrier is passed before
     // anything reaches another CTA, and meanwhile the queries and the unit descriptors are fetched
     cluster_arrive();
-    pdl_launch_dependents();
     // Every input may come from the preceding kernels, and the caller may read what this one writes only
     // after it.  With early cache reads the caller vouches that the preceding kernel writes nothing this
     // launch reads of the cache state (descriptors' inputs, block-table rows, metadata rows): this launch
     // then computes its units' descriptors, copies their table rows and starts streaming their metadata
     // while that kernel drains, and every thread waits for it before it reads the queries or new rows or
-    // writes anything (error bits, ORed atomically into err, aside).
-    if (!p.early) pdl_wait();
+    // writes anything (error bits, ORed atomically into err, aside).  Either way a thread lets the next
+    // launch be scheduled only after its own wait, so the kernel before the preceding one has finished
+    // whenever a launch reads early.
+    if (!p.early) pdl_wait_then_release();
 
     auto aborting = [&]() { return ld_volatile(&sh.abort_flag) != 0; };
     auto set_abort = [&]() {
@@ -403,7 +404,7 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
             }
         }
         if (p.early) {
-            pdl_wait();  // the preceding kernel is done: the queries and new rows are final
+            pdl_wait_then_release();  // the preceding kernel is done: the queries and new rows are final
             if (stid == 0) issue_q();
         }
         // 0. for the consumer warps, well before they need them: the finished bounds of the first page the
@@ -920,7 +921,7 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
                 issue_score(b, ij, isl);
                 more = next_score(ij, isl);
             }
-            if (p.early) pdl_wait();  // before the new rows and any store
+            if (p.early) pdl_wait_then_release();  // before the new rows and any store
             // a slot is refilled as soon as it is consumed, and the slots are consumed in turn: in the
             // order they were filled
             for (int b = 0; in_flight(b); b = (b + 1) % kSRing) {

@@ -12,19 +12,14 @@
 
 namespace kvmm {
 
-// Workspace layout shared by the calls that take one: one int32 counter per
-// (b, kv_head) of the layer (reserved; left at zero), then the unit's page
-// scores, B*Hkv rows of Pmax fp32.
+// Workspace layout shared by the calls that take one: the units' page scores,
+// B*Hkv rows of Pmax fp32 (every call writes the scores it reads).
 inline size_t round256(size_t n) { return (n + 255) & ~static_cast<size_t>(255); }
-inline size_t ws_counter_bytes(const kvmm_shape& s)
-{
-    return round256(static_cast<size_t>(s.B) * s.Hkv * sizeof(int32_t));
-}
 inline size_t ws_scores_bytes(const kvmm_shape& s)
 {
     return round256(static_cast<size_t>(s.B) * s.Hkv * s.Pmax * sizeof(float));
 }
-inline size_t ws_total_bytes(const kvmm_shape& s) { return ws_counter_bytes(s) + ws_scores_bytes(s); }
+inline size_t ws_total_bytes(const kvmm_shape& s) { return ws_scores_bytes(s); }
 
 struct UpdateParams {
     int32_t B, L, Hkv, D, T, Pmax, layer, n_new;
@@ -49,7 +44,6 @@ struct ScoreParams {
     int32_t* sel_idx;
     int32_t* sel_cnt;
     float* scores_out;
-    int32_t* counters;  // workspace: [B*Hkv]
     float* scores_ws;   // workspace: [B*Hkv][Pmax]
     int32_t* err;
 };
@@ -272,12 +266,11 @@ cudaError_t launch_score_only(const ScoreParams& p, int group_reduce, cudaStream
 cudaError_t launch_score_topk_mean(const ScoreParams& p, int group_reduce, cudaStream_t stream);  // mean-key rows
 
 // Library-owned scratch of page_score_topk_static_scratch (score_topk.cu):
-// counters for up to kStaticScratchCounterBytes/4 units, then the scores.
+// the scores, laid out as in a caller workspace.
 constexpr size_t kStaticScratchBytes = size_t(4) << 20;
-constexpr size_t kStaticScratchCounterBytes = size_t(16) << 10;
 // Device address of that scratch on the current device; the first call on a
-// device resolves it and zeroes the counters on `stream`.
-cudaError_t static_scratch_for_current_device(void** ptr, cudaStream_t stream);
+// device looks it up (cudaGetSymbolAddress) and caches it.
+cudaError_t static_scratch_for_current_device(void** ptr);
 
 // Attention launch geometry for the current device.
 constexpr int kAttnMaxSplits = 16;                   // CTAs of a unit form one cluster

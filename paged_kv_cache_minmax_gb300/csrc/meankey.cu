@@ -21,8 +21,7 @@ template <int D>
 __global__ void __launch_bounds__(kMeanWarps * 32) meankey_kernel(const MeanParams p)
 {
     constexpr int kCh = D / 32;  // channels per lane
-    pdl_launch_dependents();
-    pdl_wait();
+    pdl_wait_then_release();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int h = blockIdx.x, b = blockIdx.y;
     const int page = blockIdx.z * kMeanWarps + warp;

@@ -42,8 +42,7 @@ __global__ void __launch_bounds__(kUpdWarps * 32) minmax_update_kernel(const Upd
     const int h = blockIdx.y;
     const int b = blockIdx.z;
     const int T = p.T;
-    pdl_launch_dependents();
-    pdl_wait();  // the pools, table and metadata may be in use by the previous kernel
+    pdl_wait_then_release();  // the pools, table and metadata may be in use by the previous kernel
 
     int tb = p.tok_begin[b];
     int te = p.tok_end[b];

@@ -27,8 +27,7 @@ constexpr int kPromoteBatch = 8;
 
 __global__ void __launch_bounds__(kPromoteThreads) promote_kernel(const PromoteParams p)
 {
-    pdl_launch_dependents();
-    pdl_wait();
+    pdl_wait_then_release();
     extern __shared__ int32_t pm[];
     int32_t* phys_s = pm;            // [Kmax] block of pair i (-1: the pair moves nothing)
     int32_t* page_s = pm + p.Kmax;   // [Kmax] promoted page of pair i

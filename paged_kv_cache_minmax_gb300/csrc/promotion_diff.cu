@@ -66,8 +66,7 @@ __global__ void __launch_bounds__(kDiffThreads) promotion_diff_kernel(const Diff
     const int b = blockIdx.y;
     const int tid = threadIdx.x;
     const size_t unit = (static_cast<size_t>(b) * p.L + p.layer) * p.Hkv + h;
-    pdl_launch_dependents();
-    pdl_wait();  // the current selection comes from the preceding kernels
+    pdl_wait_then_release();  // the current selection comes from the preceding kernels
 
     if (p.rescore_mask != nullptr && p.rescore_mask[p.layer * p.Hkv + h] == 0) {
         if (tid == 0) {

@@ -115,8 +115,7 @@ __global__ void __launch_bounds__(kScoreThreads) score_pages_kernel(const ScoreP
         fence_barrier_init();
     }
     __syncthreads();
-    pdl_launch_dependents();
-    pdl_wait();  // metadata and queries may come from the previous kernel
+    pdl_wait_then_release();  // metadata and queries may come from the previous kernel
 
     if (warp == kConsumerWarps) {
         // ---- producer ------------------------------------------------------
@@ -247,8 +246,7 @@ __global__ void __launch_bounds__(kTopkThreads) select_topk_kernel(const ScorePa
     __shared__ BlockTopkShared<kTopkThreads> ts;
     const int h = blockIdx.x;
     const int b = blockIdx.y;
-    pdl_launch_dependents();
-    pdl_wait();  // the scores are written by the scoring kernel
+    pdl_wait_then_release();  // the scores are written by the scoring kernel
 
     if (p.rescore_mask != nullptr && p.rescore_mask[p.layer * p.Hkv + h] == 0) return;
     const int P = unit_pages(p, b, false);
@@ -321,7 +319,7 @@ cudaError_t launch_score_only(const ScoreParams& p, int group_reduce, cudaStream
 // the module's device memory, so that call needs no workspace from its
 // caller and allocates nothing.  Every GPU that loads the library holds these
 // bytes until the process exits.  Layout as for a caller workspace: the
-// per-unit counters first, then the scores.
+// scores of every unit of the layer.
 namespace {
 __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
 
@@ -330,7 +328,7 @@ std::mutex g_static_mutex;
 void* g_static_ptr[kMaxDevices] = {};
 }  // namespace
 
-cudaError_t static_scratch_for_current_device(void** ptr, cudaStream_t stream)
+cudaError_t static_scratch_for_current_device(void** ptr)
 {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -339,12 +337,9 @@ cudaError_t static_scratch_for_current_device(void** ptr, cudaStream_t stream)
     std::lock_guard<std::mutex> lock(g_static_mutex);
     if (g_static_ptr[dev] == nullptr) {
         // first call on this device: resolve the array's device address (the
-        // host-side name is only a stand-in) and zero the counters, which
-        // every later call leaves at zero again
+        // host-side name is only a stand-in for it)
         void* addr = nullptr;
         e = cudaGetSymbolAddress(&addr, g_static_scratch);
-        if (e != cudaSuccess) return e;
-        e = cudaMemsetAsync(addr, 0, kStaticScratchCounterBytes, stream);
         if (e != cudaSuccess) return e;
         g_static_ptr[dev] = addr;
     }

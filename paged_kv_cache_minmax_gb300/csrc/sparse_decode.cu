@@ -134,8 +134,7 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const AttnPar
     if (tid < kAttnWarps * kSteps) mbar_init(&sh.bar[tid / kSteps][tid % kSteps], 1);
     if (tid == 0) mbar_init(&sh.bt_bar, 1);
     fence_barrier_init();
-    pdl_launch_dependents();
-    pdl_wait();  // every input may come from the preceding kernels
+    pdl_wait_then_release();  // every input may come from the preceding kernels
 
     // Q^T as B fragments: lane (gid, tig) holds head gid, 16-byte chunk 4r+tig
     uint32_t qf[D / 32][4];

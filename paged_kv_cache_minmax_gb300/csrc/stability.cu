@@ -56,8 +56,7 @@ __device__ __forceinline__ bool contains_sorted(const int32_t* list, int n, int3
 
 __global__ void __launch_bounds__(kRcoThreads) history_record_kernel(const StabilityParams p)
 {
-    pdl_launch_dependents();
-    pdl_wait();
+    pdl_wait_then_release();
     const int h = blockIdx.x, b = blockIdx.z;
     const int layer = p.layer >= 0 ? p.layer : static_cast<int>(blockIdx.y);
     const size_t u = (static_cast<size_t>(b) * p.L + layer) * p.Hkv + h;
@@ -93,8 +92,7 @@ __host__ __device__ inline bool rco_bitmaps(int n, int Pmax)
 
 __global__ void __launch_bounds__(kRcoThreads) rco_unit_kernel(const StabilityParams p)
 {
-    pdl_launch_dependents();
-    pdl_wait();
+    pdl_wait_then_release();
     extern __shared__ __align__(16) uint8_t rsm[];
     const int n = p.n;
     const bool bitmaps = rco_bitmaps(n, p.Pmax);
@@ -202,8 +200,7 @@ __device__ __forceinline__ unsigned long long order_key(double x)
 
 __global__ void __launch_bounds__(kClassifyThreads) stability_classify_kernel(const StabilityParams p)
 {
-    pdl_launch_dependents();
-    pdl_wait();
+    pdl_wait_then_release();
     extern __shared__ unsigned long long skey[];  // [L * Hkv] order keys of the stabilities
     const int n = p.L * p.Hkv;
     for (int i = threadIdx.x; i < n; i += kClassifyThreads) {

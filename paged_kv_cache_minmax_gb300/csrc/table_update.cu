@@ -20,8 +20,7 @@ constexpr int kUpdBatch = 8;
 
 __global__ void __launch_bounds__(kUpdThreads) table_update_kernel(const TableUpdateParams p)
 {
-    pdl_launch_dependents();
-    pdl_wait();
+    pdl_wait_then_release();
     const long long stride = static_cast<long long>(gridDim.x) * kUpdThreads;
     for (long long i0 = static_cast<long long>(blockIdx.x) * kUpdThreads + threadIdx.x; i0 < p.n;
          i0 += stride * kUpdBatch) {

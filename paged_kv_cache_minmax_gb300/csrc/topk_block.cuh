@@ -66,6 +66,15 @@ __device__ __forceinline__ uint32_t topk_order_key(float f)
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// bin of score v in [0, kTopkBins): floor((v - mn) * scale), monotone in v.  The clamps make every
+// input defined: a NaN score (unsupported input) lands in bin 0, where the ranking keeps the selection a
+// valid one (K distinct pages), with no promise on which of the tied or NaN pages win.
+__device__ __forceinline__ int topk_bin(float v, float mn, float scale)
+{
+    const float x = fminf(fmaxf((v - mn) * scale, 0.f), static_cast<float>(kTopkBins - 1));
+    return static_cast<int>(x);
+}
+
 // the float of an order key
 __device__ __forceinline__ float topk_key_float(uint32_t k)
 {
@@ -255,7 +264,7 @@ __device__ __noinline__ int block_topk_reg(const float* scores, int P, int K, in
     for (int e = 0; e < kPer; ++e) {
         b[e] = -1;
         if (i0 + e < P) {
-            b[e] = min(kTopkBins - 1, static_cast<int>((v[e] - mn) * scale));
+            b[e] = topk_bin(v[e], mn, scale);
             atomicAdd(&ts.hist[b[e]], 1);
         }
     }
@@ -425,7 +434,7 @@ __device__ __noinline__ int block_topk(const float* scores, int P, int K, int32_
 
     // 2. bucket every score: bin(s) = floor((s - mn) * scale) is monotone in s
     for (int i = tid; i < P; i += THREADS) {
-        const int bi = min(kTopkBins - 1, static_cast<int>((sc[i] - mn) * scale));
+        const int bi = topk_bin(sc[i], mn, scale);
         bin[i] = static_cast<int16_t>(bi);
         atomicAdd(&ts.hist[bi], 1);
     }

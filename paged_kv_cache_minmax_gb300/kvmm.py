@@ -262,9 +262,10 @@ def decode_layer(shape: Shape, layer: int, q, new_k, new_v, n_new: int, tok_begi
                  block_table, meta, seq_len, rescore_mask, K: int, sel_idx, sel_cnt, out, lse=None, err=None,
                  scores_out=None, group_reduce: int = 0, sm_scale: float = 0.0, workspace=None,
                  stream=None, early_reads: bool = False) -> None:
-    """Append (optional), score, select and attend for one layer in one launch.  ``early_reads``: the
-    kernel launched just before on the stream writes nothing this call reads of seq_len, tok_begin,
-    tok_end, rescore_mask, block_table and meta (``KVMM_DECODE_EARLY_READS``)."""
+    """Append (optional), score, select and attend for one layer in one launch.  ``early_reads``: no kernel
+    still running when this launch starts (after a kvmm call: that call alone) writes anything this call reads
+    of seq_len, tok_begin, tok_end, rescore_mask, block_table and meta (``KVMM_DECODE_EARLY_READS``); two
+    calls for the same layer back to back do not meet this."""
     s = shape
     units = s.B * s.L * s.Hkv
     if (new_k is None) != (new_v is None):

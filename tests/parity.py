@@ -96,6 +96,26 @@ def check_selection(s_gpu, s_orc, sel_gpu, K, stats: Stats):
         stats.ties += 1
 
 
+def check_selection_vs_oracle(s_orc, sel_gpu, K, stats: Stats):
+    """The GPU selection against the oracle's, without the GPU's scores: the two may differ only on pages
+    whose oracle score lies within the tie window of the oracle's K-th score (each such page is counted).
+    The selection must still be ascending, distinct and min(K, P) long."""
+    P = len(s_orc)
+    n = min(K, P)
+    sel = [int(x) for x in sel_gpu]
+    assert len(sel) == n, f"{len(sel)} pages selected, want {n}"
+    assert all(a < b for a, b in zip(sel, sel[1:])), "selection not strictly ascending"
+    assert all(0 <= x < P for x in sel), "selected page out of range"
+    if n == 0:
+        return
+    ref = oracle.topk(s_orc, K)
+    s_k = np.sort(s_orc)[::-1][n - 1]
+    for p in set(sel) ^ set(ref.tolist()):
+        assert abs(s_orc[p] - s_k) <= TIE_RTOL * max(abs(s_k), 1e-30), \
+            f"page {p} selected differently (score {s_orc[p]!r}, K-th {s_k!r})"
+        stats.ties += 1
+
+
 def compare_attention(out_gpu, lse_gpu, out_ref, lse_ref, stats: Stats):
     out_gpu = np.asarray(out_gpu, dtype=np.float64)
     d = np.abs(out_gpu - out_ref)
@@ -109,8 +129,10 @@ def compare_attention(out_gpu, lse_gpu, out_ref, lse_ref, stats: Stats):
 
 
 def check_unit(wl, st, layer, b, h, q, scores_gpu=None, stats: Stats | None = None, full=None,
-               check_meta=True, group_reduce=0):
-    """Compare one unit of one layer (after select + attend) with the oracle."""
+               check_meta=True, group_reduce=0, sel_vs_oracle=False):
+    """Compare one unit of one layer (after select + attend) with the oracle.  With ``scores_gpu`` the
+    selection is checked against the GPU's own scores and the oracle's; without them, ``sel_vs_oracle``
+    checks it against the oracle's selection from ``q`` (for a unit selected in this step)."""
     stats = stats or Stats()
     cfg = wl.cfg
     G, T = cfg.G, cfg.T
@@ -128,6 +150,8 @@ def check_unit(wl, st, layer, b, h, q, scores_gpu=None, stats: Stats | None = No
         s_o = oracle.unit_scores(qg, meta_o, P, group_reduce)
         s_g = scores_gpu[b, h, :P].double().cpu().numpy()
         check_selection(s_g, s_o, sel_g, st.K, stats)
+    elif sel_vs_oracle:
+        check_selection_vs_oracle(oracle.unit_scores(qg, meta_o, P, group_reduce), sel_g, st.K, stats)
     out_o, lse_o, _ = oracle.unit_sparse_attention(qg, kp, vp, T, row, seq, sel_g)
     out_g = st.out[layer, b, h * G:(h + 1) * G].cpu().numpy()
     lse_g = st.lse[layer, b, h * G:(h + 1) * G].cpu().numpy()

@@ -279,3 +279,55 @@ def test_early_reads_leave_what_the_waiting_launch_leaves(name):
             for h in range(cfg.Hkv):
                 parity.check_unit(wb, sb, l, bb, h, wb.q[l], None, stats, check_meta=False)
     stats.check()
+
+
+@pytest.mark.parametrize("L", [2, 3])
+def test_early_reads_across_growing_steps(L):
+    """Decode steps of L layers back to back, every launch appending one token at the end of its
+    sequences, so seq_len and tok_begin advance every step and the appends cross page boundaries.  Each
+    step's inputs sit in buffers of their own, filled before the first launch: no other kernel runs between
+    the launches, which form one chain of programmatic dependent launches.  A launch with early cache reads
+    then reads the metadata row that the same layer's launch one step earlier wrote; that launch is L
+    launches back, and only the launch just before may still run (every kvmm kernel lets the next one start
+    after its own wait).  The early and the waiting runs leave the same bytes, step by step, and the
+    waiting run matches the oracle."""
+    steps = 24
+    cfg = scaled(CONFIGS[2], B=4, L=L, S=4096 - 3, K=32, n_planted=16, ragged=True, steps=steps)
+    runs = []
+    for early in (True, False):
+        wl = workloads.generate(cfg, device="cuda")
+        st = DecodeState.for_workload(wl)
+        st.build_metadata()
+        qs = workloads.drift_queries(wl, steps)
+        toks = [workloads.step_tokens(wl, t) for t in range(steps)]
+        base = wl.seq_len.clone()
+        seq = torch.stack([base + t + 1 for t in range(steps)]).contiguous()  # [steps, B]: after the append
+        tb = (seq - 1).contiguous()
+        outs = torch.zeros(steps, L, cfg.B, cfg.Hq, cfg.D, device="cuda")
+        lses = torch.zeros(steps, L, cfg.B, cfg.Hq, device="cuda")
+        torch.cuda.synchronize()
+        for t in range(steps):
+            nk, nv = toks[t]
+            for l in range(L):
+                kvmm.decode_layer(st.shape, l, qs[t, l], nk[l], nv[l], 1, tb[t], seq[t], st.k_pool, st.v_pool,
+                                  st.block_table, st.meta, seq[t], None, st.K, st.sel_idx, st.sel_cnt, outs[t, l],
+                                  lse=lses[t, l], err=st.err, workspace=st.workspace, early_reads=early)
+        torch.cuda.synchronize()
+        assert st.read_err() == 0
+        wl.seq_len.copy_(seq[-1])
+        st.out.copy_(outs[-1])
+        st.lse.copy_(lses[-1])
+        runs.append((wl, st, outs, lses, qs))
+    (wa, sa, oa, la, _), (wb, sb, ob, lb, qb) = runs
+    assert torch.equal(wa.k_pool, wb.k_pool) and torch.equal(wa.v_pool, wb.v_pool)
+    assert torch.equal(sa.meta, sb.meta)
+    assert torch.equal(sa.sel_cnt, sb.sel_cnt) and torch.equal(sa.sel_idx, sb.sel_idx)
+    for t in range(steps):
+        assert torch.equal(oa[t], ob[t]), f"step {t}: outputs differ"
+        assert torch.equal(la[t], lb[t]), f"step {t}: lse differs"
+    stats = parity.Stats()
+    for l in range(L):
+        for bb in range(cfg.B):
+            for h in range(cfg.Hkv):
+                parity.check_unit(wb, sb, l, bb, h, qb[-1, l], None, stats, sel_vs_oracle=True)
+    stats.check()

@@ -94,7 +94,8 @@ def test_fused_matches_oracle_and_separate_calls(name):
 
 
 def test_repeated_launches_on_one_workspace():
-    """Consecutive launches with changing queries: counters and the ready generation carry over."""
+    """Consecutive launches with changing queries on one workspace: every launch leaves what the separate
+    calls leave."""
     cfg = CASES["llama-ragged"]
     wl, fused, sep = fused_states(cfg)
     qs = workloads.drift_queries(wl, 6)
@@ -105,9 +106,6 @@ def test_repeated_launches_on_one_workspace():
             assert fused.read_err() == 0
             assert_same_selection(fused, sep, sf, ss)
             assert (fused.out[l] - sep.out[l]).abs().max().item() <= 2e-5
-    # the workspace's counter region is left at zero
-    ctrl = fused.workspace.view(torch.int32)[: cfg.B * cfg.Hkv]
-    assert int(ctrl.abs().sum()) == 0
 
 
 def test_partial_rescore_mask_keeps_stable_selections():
