@@ -414,17 +414,20 @@ def time_graphs(graph_list, stream, reps):
 def separate_calls_leg(st, cfg, L, q_dev, stream, reps, peak):
     """page_score_topk alone, sparse_paged_decode_attn alone (over the selection the first leaves) and the
     two back to back, each as L launches of one CUDA graph replayed back to back (every unit rescored, the
-    automatic split count).  Per launch: CUDA-event time and the algorithmic bytes of that call."""
+    automatic split count).  Per launch: CUDA-event time and the algorithmic bytes of that call.  Both calls
+    read early (KVMM_EARLY_READS): in every sequence timed here the launch before writes nothing they read
+    early (scoring writes selections and scores; attention writes outputs; neither writes lengths, masks,
+    tables or metadata)."""
     kvmm = _kvmm()
 
     def score(l):
         kvmm.page_score_topk(st.shape, l, q_dev[l], st.meta, st.seq_len, None, st.K, st.sel_idx, st.sel_cnt,
-                             st.workspace, st.err)
+                             st.workspace, st.err, early_reads=True)
 
     def attn(l):
         kvmm.sparse_paged_decode_attn(st.shape, l, q_dev[l], st.k_pool, st.v_pool, st.block_table, st.seq_len,
                                       st.sel_idx, st.sel_cnt, st.out[l], st.workspace, lse=st.lse[l], err=st.err,
-                                      num_splits=st.num_splits)
+                                      num_splits=st.num_splits, early_reads=True)
 
     with torch.cuda.stream(stream):
         for l in range(L):
@@ -451,6 +454,7 @@ def separate_calls_leg(st, cfg, L, q_dev, stream, reps, peak):
             "sparse_paged_decode_attn": rec(ms_a, b["attn_launch"]),
             "sum_of_alone": rec(ms_s + ms_a, both),
             "back_to_back": rec(ms_p, both),
+            "flags": "KVMM_EARLY_READS",
             "how": f"{L} launches of each call (or {L} pairs) in one CUDA graph, replayed {reps} times between "
                    "CUDA events on the launching stream; per launch = region / launches; bytes per launch: "
                    "the call's metadata or selected K/V plus its small terms"}
@@ -481,7 +485,7 @@ def gpu_arm(args):
     wl = workloads.generate(cfg, device="cuda", seed=replica_seed(cfg, rank))
     shape = kvmm.make_shape(cfg.B, L, cfg.Hq, cfg.Hkv, cfg.D, cfg.T, cfg.Pmax, cfg.K, wl.n_phys)
     splits = kvmm.auto_splits(shape)
-    st = DecodeState.for_workload(wl, num_splits=splits)
+    st = DecodeState.for_workload(wl)  # automatic split count (0): the clustered attention kernel
     one_launch = True  # decode_layer runs its one-launch kernel (else its two-kernel fallback)
     if args.path == "decode_layer":
         c_ctas = kvmm.decode_layer_cluster(shape)

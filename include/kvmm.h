@@ -152,12 +152,22 @@ kvmm_status kv_minmax_update(const kvmm_shape* shape, int32_t layer, const kvmm_
  * holds nothing between calls.
  * Requires 1 <= K <= Kmax; a sequence longer than Pmax*T sets
  * KVMM_ERR_OUT_OF_RANGE and is scored over its first Pmax pages.
+ * The work is one launch: a cluster of CTAs streams a pair of units'
+ * metadata, scores it and selects on chip (the workspace is not touched);
+ * shapes whose per-unit buffers do not fit one CTA (beyond about 9,500
+ * pages) run a scoring kernel and a selection kernel through the workspace.
+ * flags: 0, or KVMM_EARLY_READS: the caller guarantees that no kernel still
+ * running when this launch starts writes seq_len, the layer's rescore_mask
+ * row or its metadata rows (after a kvmm call, the guarantee is about that
+ * call alone; see decode_layer).  The launch then starts streaming the
+ * metadata while that kernel drains, and waits for it before it reads q or
+ * writes anything but error bits.  The two-kernel fallback always waits.
  */
 kvmm_status page_score_topk(const kvmm_shape* shape, int32_t layer, const kvmm_bf16* q,
                             const kvmm_bf16* meta, const int32_t* seq_len,
                             const uint8_t* rescore_mask, int32_t K, int32_t group_reduce,
                             int32_t* sel_idx, int32_t* sel_cnt, float* scores_out,
-                            void* workspace, size_t workspace_bytes, int32_t* err,
+                            void* workspace, size_t workspace_bytes, uint32_t flags, int32_t* err,
                             kvmm_stream stream);
 
 /* ------------------------------------------------------------------------
@@ -205,23 +215,34 @@ kvmm_status page_score_topk_static_scratch(const kvmm_shape* shape, int32_t laye
  *     out[b][g]  = sum_t exp(z_t - m) v_t / sum_t exp(z_t - m),  m = max_t z_t
  *     lse[b][g]  = m + log(sum_t exp(z_t - m))
  * accumulated in fp32.  sm_scale <= 0 means 1/sqrt(D).  A unit with no
- * valid token yields out = 0 and lse = -inf.  The selection is split over
- * num_splits CTAs per unit, which form one thread-block cluster and merge
- * their partial results by log-sum-exp in distributed shared memory
- * (0 = chosen from the GPU's SM count; explicit values are clamped to
- * [1, min(16, Kmax)], and a value the device cannot co-schedule returns
- * KVMM_UNSUPPORTED_SHAPE).  A selected page whose entry is null or out of
- * range, or whose index is >= the unit's page count, sets its error bit and
- * contributes nothing.  lse may be NULL.  workspace / workspace_bytes are
- * not used by this call (kept for the stable signature) and may be NULL / 0.
+ * valid token yields out = 0 and lse = -inf.  Each unit's selection is
+ * split over the CTAs of one thread-block cluster, which merge their
+ * partial results by log-sum-exp in distributed shared memory.  With
+ * num_splits = 0 the launch shape is automatic: two units share a cluster
+ * as large as the GPU holds in one wave (kvmm_auto_splits gives its CTAs
+ * per unit), and a unit's pages stream into the slots the previous unit's
+ * pages free.  An explicit num_splits runs one unit a cluster of that many
+ * CTAs (clamped to [1, min(16, Kmax)]; a value the device cannot co-schedule
+ * returns KVMM_UNSUPPORTED_SHAPE).  A selected page whose entry is null or
+ * out of range, or whose index is >= the unit's page count, sets its error
+ * bit and contributes nothing.  lse may be NULL.  workspace /
+ * workspace_bytes are not used by this call (kept for the stable signature)
+ * and may be NULL / 0.
+ * flags: 0, or KVMM_EARLY_READS (automatic launch shape only): the caller
+ * guarantees that no kernel still running when this launch starts writes
+ * seq_len or the layer's block-table rows.  The launch then computes its
+ * units' extents and copies their table rows while that kernel drains, and
+ * waits for it before it reads q, the selections or the pools.  A
+ * page_score_topk just before writes only selections and scores, so a
+ * decode loop may set the flag whenever the table changes between steps.
  */
 kvmm_status sparse_paged_decode_attn(const kvmm_shape* shape, int32_t layer, const kvmm_bf16* q,
                                      const kvmm_bf16* k_pool, const kvmm_bf16* v_pool,
                                      const int32_t* block_table, const int32_t* seq_len,
                                      const int32_t* sel_idx, const int32_t* sel_cnt,
                                      float sm_scale, int32_t num_splits, float* out, float* lse,
-                                     void* workspace, size_t workspace_bytes, int32_t* err,
-                                     kvmm_stream stream);
+                                     void* workspace, size_t workspace_bytes, uint32_t flags,
+                                     int32_t* err, kvmm_stream stream);
 
 /* ------------------------------------------------------------------------
  * topk_promotion_diff -- after a rerank, list the pages that entered and
@@ -330,7 +351,8 @@ kvmm_status page_score_topk_attn(const kvmm_shape* shape, int32_t layer, const k
  * there.  Other bits return KVMM_INVALID_ARG.  The two-kernel fallback always
  * waits.
  */
-#define KVMM_DECODE_EARLY_READS 1u
+#define KVMM_EARLY_READS 1u
+#define KVMM_DECODE_EARLY_READS KVMM_EARLY_READS
 kvmm_status decode_layer(const kvmm_shape* shape, int32_t layer, const kvmm_bf16* q, const kvmm_bf16* new_k,
                          const kvmm_bf16* new_v, int32_t n_new, const int32_t* tok_begin, const int32_t* tok_end,
                          kvmm_bf16* k_pool, kvmm_bf16* v_pool, const int32_t* block_table, kvmm_bf16* meta,

@@ -103,7 +103,8 @@ const char* kvmm_last_cuda_error(void)
 int32_t kvmm_auto_splits(const kvmm_shape* shape)
 {
     if (check_shape(shape) != KVMM_OK) return 0;
-    return resolve_splits(*shape, 0);
+    const kvmm::DecodeGrid g = kvmm::decode_layer_grid(*shape, kvmm::kPhAttend);
+    return g.nu > 0 ? g.c : resolve_splits(*shape, 0);
 }
 
 int32_t kvmm_decode_layer_cluster(const kvmm_shape* shape)
@@ -162,12 +163,35 @@ kvmm_status kv_minmax_update(const kvmm_shape* shape, int32_t layer, const kvmm_
     return launched(kvmm::launch_minmax_update(p, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+// the shape part of the clustered decode kernel's parameters; the caller sets the arrays
+static kvmm::DecodeParams decode_params(const kvmm_shape& s, int32_t layer, int32_t K, const kvmm::DecodeGrid& g,
+                                        float sm_scale)
+{
+    kvmm::DecodeParams p{};
+    p.B = s.B;
+    p.L = s.L;
+    p.Hq = s.Hq;
+    p.Hkv = s.Hkv;
+    p.G = s.Hq / s.Hkv;
+    p.D = s.D;
+    p.T = s.T;
+    p.Pmax = s.Pmax;
+    p.Kmax = s.Kmax;
+    p.layer = layer;
+    p.K = K;
+    p.C = g.c;
+    p.NU = g.nu;
+    p.n_phys = s.n_phys;
+    p.scale_log2 = (sm_scale > 0.f ? sm_scale : 1.0f / std::sqrt(static_cast<float>(s.D))) * 1.4426950408889634f;
+    return p;
+}
+
 // page_score_topk and page_score_topk_mean: the same arguments, MinMax bounds or mean keys as rows
 static kvmm_status score_topk_call(const kvmm_shape* shape, int32_t layer, const kvmm_bf16* q,
                                    const kvmm_bf16* meta, const int32_t* seq_len, const uint8_t* rescore_mask,
                                    int32_t K, int32_t group_reduce, int32_t* sel_idx, int32_t* sel_cnt,
-                                   float* scores_out, void* workspace, size_t workspace_bytes, int32_t* err,
-                                   kvmm_stream stream, bool mean)
+                                   float* scores_out, void* workspace, size_t workspace_bytes, uint32_t flags,
+                                   int32_t* err, kvmm_stream stream, bool mean)
 {
     kvmm_status st = check_shape(shape);
     if (st != KVMM_OK) return st;
@@ -178,6 +202,26 @@ static kvmm_status score_topk_call(const kvmm_shape* shape, int32_t layer, const
         !req(workspace) || !opt4(err))
         return KVMM_INVALID_ARG;
     if (workspace_bytes < score_ws_bytes(s)) return KVMM_WORKSPACE_TOO_SMALL;
+    if ((flags & ~KVMM_EARLY_READS) != 0u) return KVMM_INVALID_ARG;
+    if (!mean) {
+        // MinMax rows: one launch of the clustered kernel's scoring phase (scores exchanged and selected on
+        // chip; the workspace is not touched), when the units' score buffers fit a CTA
+        const kvmm::DecodeGrid g = kvmm::decode_layer_grid(s, kvmm::kPhScore);
+        if (g.nu > 0) {
+            kvmm::DecodeParams dp = decode_params(s, layer, K, g, 0.f);
+            dp.early = (flags & KVMM_EARLY_READS) != 0u ? 1 : 0;
+            dp.q = q;
+            dp.meta = const_cast<kvmm_bf16*>(meta);  // read only: this phase appends nothing
+            dp.seq_len = seq_len;
+            dp.rescore_mask = rescore_mask;
+            dp.sel_idx = sel_idx;
+            dp.sel_cnt = sel_cnt;
+            dp.scores_out = scores_out;
+            dp.err = err;
+            return launched(kvmm::launch_decode_layer(dp, group_reduce, kvmm::kPhScore,
+                                                      reinterpret_cast<cudaStream_t>(stream)));
+        }
+    }
     ScoreParams p{};
     p.B = s.B;
     p.L = s.L;
@@ -207,11 +251,11 @@ kvmm_status page_score_topk(const kvmm_shape* shape, int32_t layer, const kvmm_b
                             const kvmm_bf16* meta, const int32_t* seq_len,
                             const uint8_t* rescore_mask, int32_t K, int32_t group_reduce,
                             int32_t* sel_idx, int32_t* sel_cnt, float* scores_out,
-                            void* workspace, size_t workspace_bytes, int32_t* err,
+                            void* workspace, size_t workspace_bytes, uint32_t flags, int32_t* err,
                             kvmm_stream stream)
 {
     return score_topk_call(shape, layer, q, meta, seq_len, rescore_mask, K, group_reduce, sel_idx, sel_cnt,
-                           scores_out, workspace, workspace_bytes, err, stream, false);
+                           scores_out, workspace, workspace_bytes, flags, err, stream, false);
 }
 
 kvmm_status page_score_topk_mean(const kvmm_shape* shape, int32_t layer, const kvmm_bf16* q,
@@ -221,7 +265,7 @@ kvmm_status page_score_topk_mean(const kvmm_shape* shape, int32_t layer, const k
                                  kvmm_stream stream)
 {
     return score_topk_call(shape, layer, q, mean, seq_len, rescore_mask, K, group_reduce, sel_idx, sel_cnt,
-                           scores_out, workspace, workspace_bytes, err, stream, true);
+                           scores_out, workspace, workspace_bytes, 0u, err, stream, true);
 }
 
 kvmm_status kv_meankey_update(const kvmm_shape* shape, int32_t layer, const int32_t* tok_begin,
@@ -301,8 +345,8 @@ kvmm_status sparse_paged_decode_attn(const kvmm_shape* shape, int32_t layer, con
                                      const int32_t* block_table, const int32_t* seq_len,
                                      const int32_t* sel_idx, const int32_t* sel_cnt,
                                      float sm_scale, int32_t num_splits, float* out, float* lse,
-                                     void* workspace, size_t workspace_bytes, int32_t* err,
-                                     kvmm_stream stream)
+                                     void* workspace, size_t workspace_bytes, uint32_t flags,
+                                     int32_t* err, kvmm_stream stream)
 {
     kvmm_status st = check_shape(shape);
     if (st != KVMM_OK) return st;
@@ -313,6 +357,27 @@ kvmm_status sparse_paged_decode_attn(const kvmm_shape* shape, int32_t layer, con
         return KVMM_INVALID_ARG;
     (void)workspace;
     (void)workspace_bytes;
+    if ((flags & ~KVMM_EARLY_READS) != 0u) return KVMM_INVALID_ARG;
+    if (num_splits == 0) {
+        // automatic: one launch of the clustered kernel's attention phase over the kept selections (units
+        // share clusters; a unit's pages follow the previous unit's in the same slots), when it fits
+        const kvmm::DecodeGrid g = kvmm::decode_layer_grid(s, kvmm::kPhAttend);
+        if (g.nu > 0) {
+            kvmm::DecodeParams dp = decode_params(s, layer, s.Kmax, g, sm_scale);
+            dp.early = (flags & KVMM_EARLY_READS) != 0u ? 1 : 0;
+            dp.q = q;
+            dp.k_pool = const_cast<kvmm_bf16*>(k_pool);  // read only: this phase appends nothing
+            dp.v_pool = const_cast<kvmm_bf16*>(v_pool);
+            dp.block_table = block_table;
+            dp.seq_len = seq_len;
+            dp.sel_idx = const_cast<int32_t*>(sel_idx);  // read only: the kept selections
+            dp.sel_cnt = const_cast<int32_t*>(sel_cnt);
+            dp.out = out;
+            dp.lse = lse;
+            dp.err = err;
+            return launched(kvmm::launch_decode_layer(dp, 0, kvmm::kPhAttend, reinterpret_cast<cudaStream_t>(stream)));
+        }
+    }
     const int splits = resolve_splits(s, num_splits);
     if (num_splits > 0 && splits > kvmm::attention_max_splits(s)) return KVMM_UNSUPPORTED_SHAPE;
     const int max_pages = (s.Kmax + splits - 1) / splits;  // selected pages one CTA may hold
@@ -374,10 +439,10 @@ kvmm_status page_score_topk_attn(const kvmm_shape* shape, int32_t layer, const k
     if (bt_offset + (bt_prefetch ? size_t(s.Pmax) * 4 : 0) > 200 * 1024) {
         // the selection does not fit the attention CTA's shared memory: separate kernels
         st = page_score_topk(shape, layer, q, meta, seq_len, rescore_mask, K, group_reduce, sel_idx, sel_cnt,
-                             scores_out, workspace, workspace_bytes, err, stream);
+                             scores_out, workspace, workspace_bytes, 0u, err, stream);
         if (st != KVMM_OK) return st;
         return sparse_paged_decode_attn(shape, layer, q, k_pool, v_pool, block_table, seq_len, sel_idx, sel_cnt,
-                                        sm_scale, 0, out, lse, nullptr, 0, err, stream);
+                                        sm_scale, 0, out, lse, nullptr, 0, 0u, err, stream);
     }
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     float* scores_ws = static_cast<float*>(workspace);
@@ -512,7 +577,7 @@ kvmm_status decode_layer(const kvmm_shape* shape, int32_t layer, const kvmm_bf16
     p.out = out;
     p.lse = lse;
     p.err = err;
-    return launched(kvmm::launch_decode_layer(p, group_reduce, cs));
+    return launched(kvmm::launch_decode_layer(p, group_reduce, kvmm::kPhBoth, cs));
 }
 
 kvmm_status topk_promotion_diff(const kvmm_shape* shape, int32_t layer,

@@ -254,13 +254,18 @@ cudaError_t launch_meankey(const MeanParams& p, cudaStream_t stream);
 cudaError_t launch_history_record(const StabilityParams& p, cudaStream_t stream);
 cudaError_t launch_stability_rco(const StabilityParams& p, cudaStream_t stream);
 size_t stability_max_heads();  // largest L * Hkv the classification handles
-cudaError_t launch_decode_layer(DecodeParams p, int group_reduce, cudaStream_t stream);
+// The phases a launch of the decode kernel runs: decode_layer runs both; page_score_topk runs the first
+// alone (score and select), sparse_paged_decode_attn the second (attend over kept selections).
+constexpr int kPhScore = 1;   // score every page of the rescored units, select their top K
+constexpr int kPhAttend = 2;  // attend over the selected pages and merge the partials
+constexpr int kPhBoth = kPhScore | kPhAttend;
+cudaError_t launch_decode_layer(DecodeParams p, int group_reduce, int ph, cudaStream_t stream);
 constexpr size_t kDSmemLimit = 220 * 1024;  // dynamic shared memory a decode_layer CTA may take
 struct DecodeGrid {
-    int nu;  // units per cluster (0: decode_layer takes the two-kernel path)
+    int nu;  // units per cluster (0: the shape's buffers do not fit; the caller takes another path)
     int c;   // CTAs per cluster
 };
-DecodeGrid decode_layer_grid(const kvmm_shape& s);  // the launch shape for a kvmm shape
+DecodeGrid decode_layer_grid(const kvmm_shape& s, int ph = kPhBoth);  // the launch shape for a kvmm shape
 // the scoring kernel alone (page_score_topk without its selection kernel)
 cudaError_t launch_score_only(const ScoreParams& p, int group_reduce, cudaStream_t stream);
 cudaError_t launch_score_topk_mean(const ScoreParams& p, int group_reduce, cudaStream_t stream);  // mean-key rows

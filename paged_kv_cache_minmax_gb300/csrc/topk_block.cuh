@@ -32,7 +32,7 @@ struct BlockTopkShared {
     static_assert(THREADS % 32 == 0 && kTopkBins % THREADS == 0 && THREADS <= kTopkBins,
                   "the bins are split evenly over the block's threads");
     static constexpr int kWarps = THREADS / 32;
-    int hist[kTopkBins];
+    alignas(16) int hist[kTopkBins];
     int cand[kTopkCandMax];
     float wmin[kWarps];
     float wmax[kWarps];
@@ -73,6 +73,25 @@ __device__ __forceinline__ int topk_bin(float v, float mn, float scale)
 {
     const float x = fminf(fmaxf((v - mn) * scale, 0.f), static_cast<float>(kTopkBins - 1));
     return static_cast<int>(x);
+}
+
+// the sum of N consecutive histogram bins from `h` (16-byte aligned when N is a multiple of 4: then in
+// 16-byte loads, free of the bank conflicts a thread stride of N words gives 4-byte loads)
+template <int N>
+__device__ __forceinline__ int topk_bin_sum(const int* h)
+{
+    int sum = 0;
+    if constexpr (N % 4 == 0) {
+#pragma unroll
+        for (int j = 0; j < N; j += 4) {
+            const int4 w = *reinterpret_cast<const int4*>(h + j);
+            sum += (w.x + w.y) + (w.z + w.w);
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < N; ++j) sum += h[j];
+    }
+    return sum;
 }
 
 // the float of an order key
@@ -203,12 +222,21 @@ __device__ __noinline__ int block_topk_reg(const float* scores, int P, int K, in
     const int warp = tid >> 5;
     const int i0 = kPer * tid;
 
-    // 1. this thread's scores, their range, an empty histogram
+    // 1. this thread's scores, their range, an empty histogram.  From shared memory a thread's 8 consecutive
+    //    scores are two 16-byte loads when they are aligned (eight 4-byte loads at a 32-byte stride would
+    //    hit the same four banks 8 times)
     float v[kPer];
+    if (scores == nullptr && i0 + kPer <= P && (reinterpret_cast<uintptr_t>(sc) & 15u) == 0u) {
+        const float4 a = *reinterpret_cast<const float4*>(sc + i0);
+        const float4 c = *reinterpret_cast<const float4*>(sc + i0 + 4);
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+        v[4] = c.x; v[5] = c.y; v[6] = c.z; v[7] = c.w;
+    } else {
 #pragma unroll
-    for (int e = 0; e < kPer; ++e) {
-        const int i = i0 + e;
-        v[e] = i < P ? (scores != nullptr ? __ldcg(scores + i) : sc[i]) : 0.f;
+        for (int e = 0; e < kPer; ++e) {
+            const int i = i0 + e;
+            v[e] = i < P ? (scores != nullptr ? __ldcg(scores + i) : sc[i]) : 0.f;
+        }
     }
     uint32_t* winbits = reinterpret_cast<uint32_t*>(ts.rhist);  // bit i: page i of the threshold bin wins
     static_assert(8 * THREADS / 32 <= 256, "the winner bitmask fits the radix histogram");
@@ -272,9 +300,7 @@ __device__ __noinline__ int block_topk_reg(const float* scores, int P, int K, in
 
     // 3. the bin holding the K-th largest score: suffix sums over bins
     constexpr int kBinsPerThread = kTopkBins / THREADS;
-    int local = 0;
-#pragma unroll
-    for (int j = 0; j < kBinsPerThread; ++j) local += ts.hist[kBinsPerThread * tid + j];
+    const int local = topk_bin_sum<kBinsPerThread>(ts.hist + kBinsPerThread * tid);
     int incl = local;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -442,9 +468,7 @@ __device__ __noinline__ int block_topk(const float* scores, int P, int K, int32_
 
     // 3. the bin holding the K-th largest score: suffix sums over bins
     constexpr int kBinsPerThread = kTopkBins / THREADS;
-    int local = 0;
-#pragma unroll
-    for (int j = 0; j < kBinsPerThread; ++j) local += ts.hist[kBinsPerThread * tid + j];
+    const int local = topk_bin_sum<kBinsPerThread>(ts.hist + kBinsPerThread * tid);
     int incl = local;  // inclusive suffix within the warp (lanes >= this one)
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {

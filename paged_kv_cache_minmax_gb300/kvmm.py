@@ -17,7 +17,7 @@ from . import build as _build
 
 OK, INVALID_ARG, UNSUPPORTED_SHAPE, WORKSPACE_TOO_SMALL, CUDA_ERROR = range(5)
 ERR_NULL_BLOCK, ERR_OUT_OF_RANGE, ERR_TIMEOUT = 1, 2, 4
-DECODE_EARLY_READS = 1
+EARLY_READS = DECODE_EARLY_READS = 1
 NULL_BLOCK = -1
 
 EXPORTS = ("kv_minmax_update", "page_score_topk", "sparse_paged_decode_attn", "topk_promotion_diff",
@@ -74,8 +74,9 @@ def load(path: str | None = None) -> ctypes.CDLL:
     P, I32, F32, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float, ctypes.c_size_t
     SP = ctypes.POINTER(Shape)
     lib.kv_minmax_update.argtypes = [SP, I32, P, P, I32, P, P, P, P, P, P, P, P]
-    lib.page_score_topk.argtypes = [SP, I32, P, P, P, P, I32, I32, P, P, P, P, SZ, P, P]
-    lib.sparse_paged_decode_attn.argtypes = [SP, I32, P, P, P, P, P, P, P, F32, I32, P, P, P, SZ, P, P]
+    U32 = ctypes.c_uint32
+    lib.page_score_topk.argtypes = [SP, I32, P, P, P, P, I32, I32, P, P, P, P, SZ, U32, P, P]
+    lib.sparse_paged_decode_attn.argtypes = [SP, I32, P, P, P, P, P, P, P, F32, I32, P, P, P, SZ, U32, P, P]
     lib.topk_promotion_diff.argtypes = [SP, I32, P, P, P, P, P, I32, P, P, P, P, P, P, P]
     lib.page_score_topk_static_scratch.argtypes = [SP, I32, P, P, P, P, I32, I32, P, P, P, P, P]
     lib.page_score_topk_attn.argtypes = [SP, I32, P, P, P, P, P, P, P, I32, I32, F32, P, P, P, P, P, P, SZ, P, P]
@@ -183,7 +184,10 @@ def kv_minmax_update(shape: Shape, layer: int, new_k, new_v, n_new: int, tok_beg
 
 
 def page_score_topk(shape: Shape, layer: int, q, meta, seq_len, rescore_mask, K: int, sel_idx, sel_cnt,
-                    workspace, err=None, scores_out=None, group_reduce: int = 0, stream=None) -> None:
+                    workspace, err=None, scores_out=None, group_reduce: int = 0, stream=None,
+                    early_reads: bool = False) -> None:
+    """Score and select for one layer.  ``early_reads``: no kernel still running when this launch starts
+    writes seq_len, the layer's rescore_mask row or its metadata rows (``KVMM_EARLY_READS``)."""
     s = shape
     units = s.B * s.L * s.Hkv
     args = (ctypes.byref(s), layer, _dev(q, "q", torch.bfloat16, s.B * s.Hq * s.D),
@@ -192,7 +196,7 @@ def page_score_topk(shape: Shape, layer: int, q, meta, seq_len, rescore_mask, K:
             _dev(rescore_mask, "rescore_mask", torch.uint8, s.L * s.Hkv, optional=True), K, group_reduce,
             _dev(sel_idx, "sel_idx", torch.int32, units * s.Kmax), _dev(sel_cnt, "sel_cnt", torch.int32, units),
             _dev(scores_out, "scores_out", torch.float32, s.B * s.Hkv * s.Pmax, optional=True),
-            _dev(workspace, "workspace", torch.uint8), workspace.numel(),
+            _dev(workspace, "workspace", torch.uint8), workspace.numel(), EARLY_READS if early_reads else 0,
             _dev(err, "err", torch.int32, 1, optional=True), _stream(stream))
     _check("page_score_topk", load().page_score_topk(*args))
 
@@ -218,7 +222,9 @@ def page_score_topk_static_scratch(shape: Shape, layer: int, q, meta, seq_len, r
 
 def sparse_paged_decode_attn(shape: Shape, layer: int, q, k_pool, v_pool, block_table, seq_len, sel_idx, sel_cnt,
                              out, workspace, lse=None, err=None, sm_scale: float = 0.0, num_splits: int = 0,
-                             stream=None) -> None:
+                             stream=None, early_reads: bool = False) -> None:
+    """Attention over the kept selections of one layer.  ``early_reads`` (automatic split count only): no
+    kernel still running when this launch starts writes seq_len or the layer's block-table rows."""
     s = shape
     units = s.B * s.L * s.Hkv
     args = (ctypes.byref(s), layer, _dev(q, "q", torch.bfloat16, s.B * s.Hq * s.D),
@@ -230,7 +236,7 @@ def sparse_paged_decode_attn(shape: Shape, layer: int, q, k_pool, v_pool, block_
             float(sm_scale), num_splits, _dev(out, "out", torch.float32, s.B * s.Hq * s.D),
             _dev(lse, "lse", torch.float32, s.B * s.Hq, optional=True),
             _dev(workspace, "workspace", torch.uint8, optional=True),
-            0 if workspace is None else workspace.numel(),
+            0 if workspace is None else workspace.numel(), EARLY_READS if early_reads else 0,
             _dev(err, "err", torch.int32, 1, optional=True), _stream(stream))
     _check("sparse_paged_decode_attn", load().sparse_paged_decode_attn(*args))
 

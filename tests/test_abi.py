@@ -64,17 +64,19 @@ def test_validation_rejects_before_any_launch(lib):
     fake = P(0x10000)  # aligned, never dereferenced: validation fails first
     bad_align = P(0x10002)
     # null pointers
-    assert lib.page_score_topk(ctypes.byref(s), 0, None, None, None, None, 8, 0, None, None, None, None, 0, None,
-                               None) == kvmm.INVALID_ARG
+    assert lib.page_score_topk(ctypes.byref(s), 0, None, None, None, None, 8, 0, None, None, None, None, 0, 0,
+                               None, None) == kvmm.INVALID_ARG
     # K out of range, layer out of range, bad group flag
-    args = [fake, fake, fake, None, 8, 0, fake, fake, None, fake, 1 << 20, None, None]
+    args = [fake, fake, fake, None, 8, 0, fake, fake, None, fake, 1 << 20, 0, None, None]
     assert lib.page_score_topk(ctypes.byref(s), 0, *args[:4], 9, *args[5:]) == kvmm.INVALID_ARG
     assert lib.page_score_topk(ctypes.byref(s), 1, *args) == kvmm.INVALID_ARG
     assert lib.page_score_topk(ctypes.byref(s), 0, *args[:5], 2, *args[6:]) == kvmm.INVALID_ARG
     # misaligned bf16 array
     assert lib.page_score_topk(ctypes.byref(s), 0, bad_align, *args[1:]) == kvmm.INVALID_ARG
     # workspace too small
-    assert lib.page_score_topk(ctypes.byref(s), 0, *args[:9], fake, 16, None, None) == kvmm.WORKSPACE_TOO_SMALL
+    assert lib.page_score_topk(ctypes.byref(s), 0, *args[:9], fake, 16, 0, None, None) == kvmm.WORKSPACE_TOO_SMALL
+    # an unknown flag bit
+    assert lib.page_score_topk(ctypes.byref(s), 0, *args[:11], 2, None, None) == kvmm.INVALID_ARG
     # unsupported shape
     s2 = kvmm.make_shape(1, 1, 4, 1, 80, 16, 64, 8, 64)
     assert lib.page_score_topk(ctypes.byref(s2), 0, *args) == kvmm.UNSUPPORTED_SHAPE
@@ -83,7 +85,9 @@ def test_validation_rejects_before_any_launch(lib):
                                 None) == kvmm.INVALID_ARG
     # attention: non-finite scale
     assert lib.sparse_paged_decode_attn(ctypes.byref(s), 0, fake, fake, fake, fake, fake, fake, fake,
-                                        float("nan"), 1, fake, None, None, 0, None, None) == kvmm.INVALID_ARG
+                                        float("nan"), 1, fake, None, None, 0, 0, None, None) == kvmm.INVALID_ARG
+    assert lib.sparse_paged_decode_attn(ctypes.byref(s), 0, fake, fake, fake, fake, fake, fake, fake,
+                                        0.0, 0, fake, None, None, 0, 8, None, None) == kvmm.INVALID_ARG
     # fused select + attend: null pointers, bad K, non-finite scale, small workspace
     fa = [fake, fake, fake, fake, fake, fake, None, 8, 0, 0.0, fake, fake, None, fake, None, fake, 1 << 20, None,
           None]

@@ -88,8 +88,7 @@ def test_bench_step_matches_oracle(cfg_id):
     cfg = CONFIGS[cfg_id]
     L = cfg.L_alloc
     wl = workloads.generate(cfg, device="cuda", seed=bench.replica_seed(cfg, 0))
-    st = DecodeState.for_workload(wl, num_splits=kvmm.auto_splits(kvmm.make_shape(
-        cfg.B, L, cfg.Hq, cfg.Hkv, cfg.D, cfg.T, cfg.Pmax, cfg.K, wl.n_phys)))
+    st = DecodeState.for_workload(wl)
     shape = launch_shape(st)
     assert shape["cluster_ctas"] >= 1 and shape["units_per_cluster"] >= 1, "decode_layer falls back"
     st.build_metadata()

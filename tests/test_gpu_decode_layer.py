@@ -331,3 +331,43 @@ def test_early_reads_across_growing_steps(L):
             for h in range(cfg.Hkv):
                 parity.check_unit(wb, sb, l, bb, h, qb[-1, l], None, stats, sel_vs_oracle=True)
     stats.check()
+
+
+@pytest.mark.parametrize("name", ["llama-6-layers", "gqa5-t32", "odd-units"])
+def test_separate_calls_with_early_reads(name):
+    """page_score_topk and sparse_paged_decode_attn (automatic launch shape) back to back for every layer over
+    two steps with drifting queries, with KVMM_EARLY_READS on both (each launch's predecessor writes only
+    selections, scores or outputs) and without: the same selections, scores and outputs bit for bit, and the
+    waiting run matches the oracle."""
+    cfg = EARLY_CASES[name]
+    runs = []
+    for early in (True, False):
+        wl = workloads.generate(cfg, device="cuda")
+        st = DecodeState.for_workload(wl)
+        st.build_metadata()
+        qs = workloads.drift_queries(wl, 2)
+        sc = torch.zeros(2, cfg.L_alloc, cfg.B, cfg.Hkv, cfg.Pmax, device="cuda")
+        outs = torch.zeros(2, cfg.L_alloc, cfg.B, cfg.Hq, cfg.D, device="cuda")
+        torch.cuda.synchronize()
+        for step in range(2):
+            for l in range(cfg.L_alloc):
+                kvmm.page_score_topk(st.shape, l, qs[step, l], st.meta, st.seq_len, None, st.K, st.sel_idx,
+                                     st.sel_cnt, st.workspace, st.err, scores_out=sc[step, l], early_reads=early)
+                kvmm.sparse_paged_decode_attn(st.shape, l, qs[step, l], st.k_pool, st.v_pool, st.block_table,
+                                              st.seq_len, st.sel_idx, st.sel_cnt, outs[step, l], st.workspace,
+                                              lse=st.lse[l], err=st.err, early_reads=early)
+        torch.cuda.synchronize()
+        assert st.read_err() == 0
+        st.out.copy_(outs[1])
+        runs.append((wl, st, sc, outs, qs))
+    (wa, sa, sca, oa, _), (wb, sb, scb, ob, qb) = runs
+    assert torch.equal(sa.sel_cnt, sb.sel_cnt) and torch.equal(sa.sel_idx, sb.sel_idx)
+    assert torch.equal(sca, scb)
+    assert torch.equal(oa, ob)
+    assert torch.equal(sa.lse, sb.lse)
+    stats = parity.Stats()
+    for l in range(cfg.L_alloc):
+        for bb in range(cfg.B):
+            for h in range(cfg.Hkv):
+                parity.check_unit(wb, sb, l, bb, h, qb[1, l], scb[1, l], stats)
+    stats.check()

@@ -120,7 +120,7 @@ def test_split_count_invariance():
     cfg = SMALL["llama-ragged"]
     wl = workloads.generate(cfg, device="cuda")
     outs = []
-    for splits in (1, 2, 4, 8, 32):
+    for splits in (1, 2, 4, 8, 32, 0):  # explicit counts: one unit a cluster; 0: the clustered kernel
         st = DecodeState.for_workload(wl, num_splits=splits)
         st.build_metadata()
         run_all_layers(wl, st, scores=False)
