@@ -358,7 +358,9 @@ class MixEpisode:
         return None if self.rerank(t) else self.unstable
 
     def rescored_units(self, t, B):
-        return None if self.rerank(t) else int(self.unstable.sum()) * B
+        """Units of one layer-step rescored at step t (None: all): on average over the layers, the batch times
+        the unstable heads of a layer."""
+        return None if self.rerank(t) else float(self.unstable.sum()) * B / self.unstable.shape[0]
 
 
 def promotion_stats(ep, st, graphs, stream, K, B):

@@ -1227,13 +1227,20 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
             l0 = l1 = 0.f;
         }
         }  // kAttend
-        // only after a time-out can a slot still be in flight here: let it land before the CTA exits
+        // No copy into this CTA's shared memory may still be in flight when it exits.  Only after a time-out
+        // can a slot be: it gets the full limit to land, whatever happened before.  The query groups' copy
+        // is waited for by the warps that use them, so when no consumer warp had work, warp 0 waits for it.
         for (int bb = 0; bb < kRing; ++bb)
-            if (in_flight(bb)) land(bb);
+            if (in_flight(bb) && !__all_sync(kFullMask, mbar_wait_bounded(&sh.full[w][bb], (par >> bb) & 1u, kDWaitNs)) &&
+                lane == 0)
+                set_abort();
+        if (w == 0 && !__all_sync(kFullMask, mbar_wait_bounded(&sh.qbar, 0, kDWaitNs)) && lane == 0) set_abort();
     }
     // No final cluster barrier: every access another CTA makes to this one's shared memory is an
     // asynchronous store counted by one of this CTA's mbarriers (scores, partials), and the selector
-    // warps have waited for all of them by now.
+    // warps have waited for all of them by now -- unless one of those waits timed out (KVMM_ERR_TIMEOUT),
+    // after which a peer's late store may still be on its way: the time-outs turn a hang into an error,
+    // they do not make the launch's results or its exit safe.
 }
 
 }  // namespace dl

@@ -47,3 +47,23 @@ def test_measured_traffic_is_reported_only_for_the_captured_workload_and_batch()
     assert bench.load_traffic("decode_layer", name, 4) is None  # another batch: another launch
     assert bench.load_traffic("decode_layer", workloads.CONFIGS[4].name, workloads.CONFIGS[4].B) is None
     assert bench.load_traffic("sparse_attn_kernel", name, workloads.CONFIGS[2].B) is None
+
+
+def test_the_mix_episode_counts_the_units_each_step_rescores():
+    """The stable/unstable episode: every unit on a rerank step, else the batch times a layer's unstable heads
+    (on average over the layers); a layer-step's bytes follow."""
+    cfg = workloads.scaled(workloads.CONFIGS[4], B=2, L=4, S=256, K=8, steps=32, n_planted=4)
+    wl = workloads.generate(cfg, device="cpu")
+    ep = bench.MixEpisode(wl, None)
+    n_unstable = int(wl.unstable.sum())
+    assert n_unstable == round(0.25 * cfg.L * cfg.Hkv)
+    assert ep.rerank(0) and ep.rerank(16) and not ep.rerank(1)
+    assert ep.mask(0) is None and ep.mask(5) is ep.unstable
+    assert ep.rescored_units(0, cfg.B) is None
+    assert ep.rescored_units(3, cfg.B) == cfg.B * n_unstable / cfg.L
+    between = bench.algorithmic_bytes(cfg, rescored_units=ep.rescored_units(3, cfg.B))
+    full = bench.algorithmic_bytes(cfg)
+    assert between["meta"] == full["meta"] * n_unstable / (cfg.L * cfg.Hkv)
+    # the episode's inputs: one appended token per step at the sequence's end
+    assert ep.seq.shape == (cfg.steps, cfg.B) and int(ep.seq[0, 0]) == cfg.S + 1
+    assert ep.tb[5].tolist() == (ep.seq[5] - 1).tolist()
