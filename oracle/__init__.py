@@ -77,6 +77,10 @@ def _load():
         lib.oracle_unit_mean_scores.restype = None
         lib.oracle_unit_page_mass.argtypes = [P, I32, I32, I32, P, I64, P, I32, D, P]
         lib.oracle_unit_page_mass.restype = I32
+        lib.oracle_centroid_build.argtypes = [P, I32, I32, I32, I32, P, P, P, P]
+        lib.oracle_centroid_build.restype = I32
+        lib.oracle_centroid_select.argtypes = [P, I32, I32, P, I32, P, I32, P, P, I32, I32, I32, P, P, P, P, P, P]
+        lib.oracle_centroid_select.restype = I32
         lib.oracle_rco.argtypes = [P, I32, P, I32, I32]
         lib.oracle_rco.restype = D
         lib.oracle_unit_stability.argtypes = [P, P, P, I32, I32, I32]
@@ -205,6 +209,46 @@ def unit_mean_scores(q, mean, P, group_reduce=0) -> np.ndarray:
     out = np.zeros(max(P, 1), dtype=np.float64)
     _load().oracle_unit_mean_scores(_ptr(q), G, D, _ptr(mean), int(P), int(group_reduce), _ptr(out))
     return out[:P].copy()
+
+
+def centroid_build(mean, R, n_iter):
+    """KVDrive's centroid level over a unit's pages' mean keys ``mean`` (uint16 bf16 bits [P, D]): Lloyd's
+    k-means from spatial blocks of R pages, n_iter iterations.  Returns (cent [n_c, D] uint16, assign [P],
+    off [n_c + 1], members [P]) -- the pages of centroid j are members[off[j]:off[j+1]], ascending."""
+    mean = _u16(mean)
+    P, D = mean.shape
+    n_c = (P + R - 1) // R
+    cent = np.zeros((max(n_c, 1), D), dtype=np.uint16)
+    assign = np.zeros(max(P, 1), dtype=np.int32)
+    off = np.zeros(n_c + 1, dtype=np.int32)
+    members = np.zeros(max(P, 1), dtype=np.int32)
+    got = _load().oracle_centroid_build(_ptr(mean), P, D, int(R), int(n_iter), _ptr(cent), _ptr(assign), _ptr(off),
+                                        _ptr(members))
+    assert got == n_c
+    return cent[:n_c].copy(), assign[:P].copy(), off, members[:P].copy()
+
+
+def centroid_select(q, mean, cent, off, members, M, K, group_reduce=0):
+    """The two-level search of one unit: score the centroids, expand the M best, keep the K best of their
+    pages.  Returns a dict: cs (centroid scores), chosen (centroids, ascending), cand (their pages, ascending),
+    ps (the candidates' scores), sel (the selection, ascending)."""
+    q, mean, cent = _u16(q), _u16(mean), _u16(cent)
+    off, members = _i32(off), _i32(members)
+    G, D = q.shape
+    P = mean.shape[0]
+    n_c = len(off) - 1
+    cs = np.zeros(max(n_c, 1), dtype=np.float64)
+    chosen = np.zeros(max(n_c, 1), dtype=np.int32)
+    cand = np.zeros(max(P, 1), dtype=np.int32)
+    ps = np.zeros(max(P, 1), dtype=np.float64)
+    sel = np.zeros(max(P, 1), dtype=np.int32)
+    n_cand = ctypes.c_int32(0)
+    cnt = _load().oracle_centroid_select(_ptr(q), G, D, _ptr(mean), P, _ptr(cent), n_c, _ptr(off), _ptr(members),
+                                         int(M), int(K), int(group_reduce), _ptr(cs), _ptr(chosen), _ptr(cand),
+                                         ctypes.addressof(n_cand), _ptr(ps), _ptr(sel))
+    n = n_cand.value
+    return {"cs": cs[:n_c].copy(), "chosen": chosen[:min(M, n_c)].copy(), "cand": cand[:n].copy(),
+            "ps": ps[:n].copy(), "sel": sel[:cnt].copy()}
 
 
 def unit_page_mass(q, k_pool, T, bt_row, seq_len, scale=0.0) -> np.ndarray:

@@ -628,3 +628,111 @@ int32_t oracle_unit_page_mass(const uint16_t* q, int32_t G, int32_t D, int32_t T
     free(row);
     return err;
 }
+
+/* ------------------------------------------------------------------------
+ * The centroid level of KVDrive's index ("Method details": each page's mean
+ * key is its representative, and higher-level centroids group similar pages;
+ * "the trade-off between block size and centroid count": the centroid count
+ * is proportional to the context, and the grouping is by similarity, with
+ * half the centroids a spatial blocking of the pages needs).  The page names
+ * no clustering algorithm.  The reading taken: Lloyd's k-means over a unit's
+ * pages' mean keys, started from spatial blocks of R consecutive pages
+ * (n_c = ceil(P / R) centroids; n_iter = 0 leaves the spatial blocks), with
+ *   - the assignment: page p joins the centroid j of least squared Euclidean
+ *     distance sum_d (m_pd - c_jd)^2, ties to the lower j;
+ *   - the update: c_j = bf16 nearest-even of (the fp32 sum of its members'
+ *     mean keys in page order) / (their count); a centroid left with no
+ *     member keeps its value.
+ * Both steps are decisions or stored codes, so they are taken in the
+ * precision and order the GPU kernel uses: the distance accumulates
+ * fmaf(x, x, acc) over d = 0 .. D-1 in fp32 with x = m_pd - c_jd, the sum
+ * adds the members in page order in fp32, and the quotient is an fp32
+ * division.  The search then scores the centroids like pages (q . c, the
+ * group reduced by sum or max, in double), expands the M best centroids
+ * (ties to the lower centroid) into their member pages, and keeps the K
+ * best of those pages by their mean-key scores (ties to the lower page),
+ * ascending.
+ */
+static void centroid_update(const uint16_t* mean, int32_t P, int32_t D, int32_t n_c, const int32_t* assign,
+                            uint16_t* cent, int32_t* off, int32_t* members)
+{
+    for (int32_t j = 0; j <= n_c; ++j) off[j] = 0;
+    for (int32_t p = 0; p < P; ++p) off[assign[p] + 1] += 1;
+    for (int32_t j = 0; j < n_c; ++j) off[j + 1] += off[j];
+    int32_t* fill = (int32_t*)malloc(sizeof(int32_t) * (size_t)(n_c > 0 ? n_c : 1));
+    for (int32_t j = 0; j < n_c; ++j) fill[j] = off[j];
+    for (int32_t p = 0; p < P; ++p) members[fill[assign[p]]++] = p; /* page order within a group */
+    free(fill);
+    for (int32_t j = 0; j < n_c; ++j) {
+        const int32_t n = off[j + 1] - off[j];
+        if (n == 0) continue; /* keeps its value */
+        for (int32_t d = 0; d < D; ++d) {
+            float acc = 0.0f;
+            for (int32_t k = off[j]; k < off[j + 1]; ++k) acc += (float)bf16_value(mean[(int64_t)members[k] * D + d]);
+            cent[(int64_t)j * D + d] = bf16_round_nearest_even(acc / (float)n);
+        }
+    }
+}
+
+static void centroid_assign(const uint16_t* mean, int32_t P, int32_t D, int32_t n_c, const uint16_t* cent,
+                            int32_t* assign)
+{
+    for (int32_t p = 0; p < P; ++p) {
+        float best = 0.0f;
+        int32_t arg = 0;
+        for (int32_t j = 0; j < n_c; ++j) {
+            float acc = 0.0f;
+            for (int32_t d = 0; d < D; ++d) {
+                const float x = (float)bf16_value(mean[(int64_t)p * D + d]) - (float)bf16_value(cent[(int64_t)j * D + d]);
+                acc = fmaf(x, x, acc);
+            }
+            if (j == 0 || acc < best) {
+                best = acc;
+                arg = j;
+            }
+        }
+        assign[p] = arg;
+    }
+}
+
+/* Builds a unit's centroids from its P pages' mean keys mean[P][D]: cent[n_c][D], assign[P], off[n_c + 1]
+ * and members[P] (the pages of centroid j are members[off[j] .. off[j+1]), ascending).  Returns n_c. */
+int32_t oracle_centroid_build(const uint16_t* mean, int32_t P, int32_t D, int32_t R, int32_t n_iter, uint16_t* cent,
+                              int32_t* assign, int32_t* off, int32_t* members)
+{
+    const int32_t n_c = (P + R - 1) / R;
+    for (int32_t p = 0; p < P; ++p) assign[p] = p / R; /* spatial blocks */
+    centroid_update(mean, P, D, n_c, assign, cent, off, members);
+    for (int32_t it = 0; it < n_iter; ++it) {
+        centroid_assign(mean, P, D, n_c, cent, assign);
+        centroid_update(mean, P, D, n_c, assign, cent, off, members);
+    }
+    return n_c;
+}
+
+/* The two-level search of one unit: centroid scores cs[n_c]; the M best centroids; their member pages
+ * (cand[0 .. *n_cand), ascending; pages < P) with their mean-key scores ps[*n_cand]; the K best of those
+ * pages into sel (ascending).  Returns the selection's size. */
+int32_t oracle_centroid_select(const uint16_t* q, int32_t G, int32_t D, const uint16_t* mean, int32_t P,
+                               const uint16_t* cent, int32_t n_c, const int32_t* off, const int32_t* members, int32_t M,
+                               int32_t K, int32_t group_reduce, double* cs, int32_t* chosen, int32_t* cand,
+                               int32_t* n_cand, double* ps, int32_t* sel)
+{
+    oracle_unit_mean_scores(q, G, D, cent, n_c, group_reduce, cs);
+    const int32_t nm = oracle_topk(cs, n_c, M, chosen);
+    uint8_t* take = (uint8_t*)calloc((size_t)(P > 0 ? P : 1), 1);
+    for (int32_t i = 0; i < nm; ++i)
+        for (int32_t k = off[chosen[i]]; k < off[chosen[i] + 1]; ++k) take[members[k]] = 1;
+    int32_t n = 0;
+    for (int32_t p = 0; p < P; ++p)
+        if (take[p]) cand[n++] = p;
+    free(take);
+    *n_cand = n;
+    uint16_t* rows = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)(n > 0 ? n : 1) * (size_t)D);
+    for (int32_t i = 0; i < n; ++i) memcpy(rows + (int64_t)i * D, mean + (int64_t)cand[i] * D, sizeof(uint16_t) * (size_t)D);
+    oracle_unit_mean_scores(q, G, D, rows, n, group_reduce, ps);
+    free(rows);
+    const int32_t cnt = oracle_topk(ps, n, K, sel); /* positions, ascending */
+    for (int32_t i = 0; i < cnt; ++i) sel[i] = cand[sel[i]];
+    return cnt;
+}

@@ -12,7 +12,8 @@ import tempfile
 import pytest
 
 import oracle
-from tests import test_oracle_meankey, test_oracle_pins as pins, test_oracle_promote, test_oracle_stability
+from tests import (test_oracle_centroid, test_oracle_meankey, test_oracle_pins as pins, test_oracle_promote,
+                   test_oracle_stability)
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "kvmm_oracle.c")
 
@@ -55,9 +56,23 @@ MUTATIONS = {
     "meankey-truncates": ("    u += 0x7fffu + lsb;\n", ""),
     "page-mass-skips-the-softmax-max": ("mass[(int64_t)g * P + t / T] += exp(z[t] - m) / denom;",
                                         "mass[(int64_t)g * P + t / T] += exp(z[t]) / denom;"),
+    # centroid level
+    "centroid-assign-takes-the-farthest": ("if (j == 0 || acc < best) {", "if (j == 0 || acc > best) {"),
+    "centroid-assign-ties-to-the-higher": ("if (j == 0 || acc < best) {", "if (j == 0 || acc <= best) {"),
+    "centroid-update-divides-by-the-block": ("bf16_round_nearest_even(acc / (float)n);\n        }\n    }\n}",
+                                             "bf16_round_nearest_even(acc / 4.0f);\n        }\n    }\n}"),
+    "centroid-update-skips-the-first-member": ("for (int32_t k = off[j]; k < off[j + 1]; ++k) acc +=",
+                                               "for (int32_t k = off[j] + 1; k < off[j + 1]; ++k) acc +="),
+    "centroid-blocks-off-by-one": ("for (int32_t p = 0; p < P; ++p) assign[p] = p / R;",
+                                   "for (int32_t p = 0; p < P; ++p) assign[p] = (p + 1) / R < (P + R - 1) / R ? (p + 1) / R : p / R;"),
+    "centroid-search-expands-one-fewer": ("for (int32_t i = 0; i < nm; ++i)\n        for (int32_t k = off[chosen[i]]",
+                                          "for (int32_t i = 0; i + 1 < nm; ++i)\n        for (int32_t k = off[chosen[i]]"),
+    "centroid-distance-drops-a-channel": ("            for (int32_t d = 0; d < D; ++d) {\n                const float x =",
+                                          "            for (int32_t d = 1; d < D; ++d) {\n                const float x ="),
 }
 
-PIN_TESTS = [getattr(m, n) for m in (pins, test_oracle_stability, test_oracle_promote, test_oracle_meankey)
+PIN_TESTS = [getattr(m, n) for m in (pins, test_oracle_stability, test_oracle_promote, test_oracle_meankey,
+                                     test_oracle_centroid)
              for n in dir(m) if n.startswith("test_")]
 
 
