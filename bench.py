@@ -1015,6 +1015,93 @@ def meankey_arm(args):
         "device_err": st.read_err()}), flush=True)
 
 
+def centroid_arm(args):
+    """KVDrive's centroid level at the 8B-32K shape (one layer, 64 units, K = 128): the index build and the
+    two-level selection for a spatial blocking (R = 4 pages a centroid, no iteration) and for the k-means
+    grouping with half the centroids (R = 8, 3 Lloyd iterations), each expanding M = 4K / R centroids (about
+    4K pages); beside MinMax and the flat mean-key scorer.  Times are CUDA-graph replays; over a sample of
+    units, the dense attention mass each selection captures (oracle, fp64), next to the best possible: the K
+    pages of most mass."""
+    import oracle
+    from paged_kv_cache_minmax_gb300 import build as kbuild
+    from paged_kv_cache_minmax_gb300 import kvmm
+    from paged_kv_cache_minmax_gb300.runtime import DecodeState
+    from paged_kv_cache_minmax_gb300.workloads import bf16_bits
+
+    kbuild.build_library()
+    kvmm.load()
+    oracle.build()
+    cfg = workloads.scaled(CFG, L=1)
+    wl = workloads.generate(cfg, device="cuda")
+    st = DecodeState.for_workload(wl)
+    st.build_metadata()
+    shape = st.shape
+    mean = torch.zeros(cfg.B, 1, cfg.Hkv, cfg.Pmax, cfg.D, dtype=torch.bfloat16, device="cuda")
+    kvmm.kv_meankey_update(shape, 0, None, wl.seq_len, wl.k_pool, wl.block_table, mean, err=st.err)
+    torch.cuda.synchronize()
+    stream = torch.cuda.Stream()
+    reps = max(10, min(args.steps, 200))
+
+    def timed(fn):
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                fn()
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+        return time_graphs([g], stream, reps)[0] * 1e3
+
+    sels = {}
+    times = {}
+
+    def new_sel():
+        return torch.zeros_like(st.sel_idx), torch.zeros_like(st.sel_cnt)
+
+    sels["minmax"] = new_sel()
+    times["minmax_score_topk_us"] = timed(lambda: kvmm.page_score_topk(
+        shape, 0, wl.q[0], st.meta, wl.seq_len, None, cfg.K, *sels["minmax"], st.workspace, st.err))
+    sels["meankey"] = new_sel()
+    times["meankey_score_topk_us"] = timed(lambda: kvmm.page_score_topk_mean(
+        shape, 0, wl.q[0], mean, wl.seq_len, None, cfg.K, *sels["meankey"], st.workspace, st.err))
+    variants = {"spatial_r4": (4, 0), "kmeans_r8_it3": (8, 3)}
+    index_bytes = {}
+    for name, (R, n_iter) in variants.items():
+        cmax = kvmm.centroid_rows(shape, R)
+        cent = torch.zeros(cfg.B, 1, cfg.Hkv, cmax, cfg.D, dtype=torch.bfloat16, device="cuda")
+        assign = torch.zeros(cfg.B, 1, cfg.Hkv, cfg.Pmax, dtype=torch.int32, device="cuda")
+        off = torch.zeros(cfg.B, 1, cfg.Hkv, cmax + 1, dtype=torch.int32, device="cuda")
+        members = torch.zeros_like(assign)
+        times[name + "_build_us"] = timed(lambda: kvmm.kv_centroid_build(
+            shape, 0, mean, wl.seq_len, R, n_iter, cent, assign, off, members, err=st.err))
+        sels[name] = new_sel()
+        M = max(1, 4 * cfg.K // R)
+        times[name + "_select_us"] = timed(lambda: kvmm.page_score_topk_centroid(
+            shape, 0, wl.q[0], mean, wl.seq_len, R, cent, off, members, None, M, cfg.K, *sels[name], err=st.err))
+        index_bytes[name] = {"centroids": cfg.B * cfg.Hkv * ((cfg.P + R - 1) // R) * cfg.D * 2, "M": M,
+                             "pages_expanded": M * R}
+    torch.cuda.synchronize()
+    kp, qb = bf16_bits(wl.k_pool).reshape(-1, cfg.T, cfg.D), bf16_bits(wl.q[0])
+    captured = {k: [] for k in list(sels) + ["best"]}
+    sample = [(b, h) for b in range(cfg.B) for h in range(0, cfg.Hkv, 4)][:max(2, min(16, args.steps))]
+    for b, h in sample:
+        row = wl.block_table[b, 0, h].cpu().numpy()
+        seq = int(wl.seq_len[b])
+        mass = oracle.unit_page_mass(qb[b, h * cfg.G:(h + 1) * cfg.G], kp, cfg.T, row, seq).mean(axis=0)
+        for name, (sel, cnt) in sels.items():
+            pages = sel[b, 0, h, :int(cnt[b, 0, h])].cpu().numpy()
+            captured[name].append(float(mass[pages].sum()))
+        captured["best"].append(float(np.sort(mass)[::-1][:cfg.K].sum()))
+    print(json.dumps({
+        "metric": "KVDrive centroid index: build and two-level selection time; dense attention mass captured",
+        "unit": "us", "higher_is_better": False, "times_us": times, "index": index_bytes,
+        "attention_mass_captured_mean": {k: float(np.mean(v)) for k, v in captured.items()},
+        "attention_mass_captured_min": {k: float(np.min(v)) for k, v in captured.items()},
+        "config": {"workload": cfg.name, "units": cfg.B * cfg.Hkv, "top_k": cfg.K, "pages": cfg.P,
+                   "sampled_units": len(sample), "keys": cfg.key_dist, "planted_pages": cfg.n_planted},
+        "device_err": st.read_err()}), flush=True)
+
+
 def load_parity(workload, launch_shape, early_reads):
     """The GPU-versus-oracle parity record of ``workload`` at the benchmark's launch shape, written by the
     ``-m gpu`` tests (tests/test_gpu_bench_shapes.py) into profiles/parity.json, with two checks: whether it
@@ -1065,6 +1152,8 @@ def main():
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (smaller profiling case)")
     ap.add_argument("--meankey", action="store_true",
                     help="compare the mean-key scorer with MinMax (time, attention mass captured) instead")
+    ap.add_argument("--centroid", action="store_true",
+                    help="time KVDrive's centroid index (build, two-level selection) and compare attention mass")
     ap.add_argument("--table-update", action="store_true",
                     help="time dirty-tracked block-table synchronisation instead")
     ap.add_argument("--promote", action="store_true",
@@ -1090,6 +1179,8 @@ def main():
         table_update_arm(args)
     elif args.meankey:
         meankey_arm(args)
+    elif args.centroid:
+        centroid_arm(args)
     else:
         gpu_arm(args)
 

@@ -391,6 +391,58 @@ kvmm_status page_score_topk_mean(const kvmm_shape* shape, int32_t layer, const k
                                  kvmm_stream stream);
 
 /* ------------------------------------------------------------------------
+ * The centroid level of KVDrive's index over the pages' mean keys.
+ *
+ * KVDrive, "Method details": each page's mean key is its representative and
+ * higher-level centroids group similar pages; "the trade-off between block
+ * size and centroid count": the centroid count is kept proportional to the
+ * context (a fixed number of pages per centroid), and the grouping by
+ * similarity matches a spatial blocking's accuracy with half the centroids.
+ * The page names no clustering algorithm.  The one built here, per unit:
+ * Lloyd's k-means over the unit's P pages' mean keys, started from spatial
+ * blocks (page p in centroid p / R, n_c = ceil(P / R) centroids):
+ *   - assignment: a page joins the centroid of least squared Euclidean
+ *     distance, accumulated as fmaf(x, x, acc) in fp32 over the channels in
+ *     order (x = mean - centroid), ties to the lower centroid;
+ *   - update: a centroid becomes the bf16 (nearest even) of the fp32 mean of
+ *     its pages' mean keys, summed in page order; one with no page keeps its
+ *     value.
+ *
+ * kv_centroid_build -- the spatial blocks, then n_iter Lloyd iterations
+ * (0 <= n_iter <= 64; 0 leaves the spatial blocking), for every unit of
+ * `layer`.  mean [B][L][Hkv][Pmax][D] as kv_meankey_update writes it.
+ * Outputs, with Cmax = ceil(Pmax / R):
+ *   cent       [B][L][Hkv][Cmax][D] bf16   the centroids (rows >= n_c untouched)
+ *   assign     [B][L][Hkv][Pmax]    int32  each page's centroid (pages >= P untouched)
+ *   member_off [B][L][Hkv][Cmax + 1] int32 centroid j's pages are
+ *   members    [B][L][Hkv][Pmax]    int32  members[member_off[j] .. member_off[j + 1]), ascending
+ * Requires 1 <= R <= Pmax; shapes whose per-unit buffers do not fit a CTA
+ * (about Pmax + Cmax > 56,000) return KVMM_UNSUPPORTED_SHAPE.
+ */
+kvmm_status kv_centroid_build(const kvmm_shape* shape, int32_t layer, const kvmm_bf16* mean, const int32_t* seq_len,
+                              int32_t R, int32_t n_iter, kvmm_bf16* cent, int32_t* assign, int32_t* member_off,
+                              int32_t* members, int32_t* err, kvmm_stream stream);
+
+/* page_score_topk_centroid -- the two-level selection over the index: score
+ * the unit's n_c centroids like pages (q_g . c, the group summed or, with
+ * group_reduce = 1, maxed; fp32), expand the M best (ties to the lower
+ * centroid; all when M >= n_c), score the pages of those centroids by their
+ * mean keys the same way, and keep the K best of those pages (ties to the
+ * lower page) in sel_idx, ascending, with their count in sel_cnt.
+ * rescore_mask as for page_score_topk (units not rescored keep their
+ * selection).  R is the build's.  centroid_scores_out [B][Hkv][Cmax] and
+ * scores_out [B][Hkv][Pmax] (written for the expanded pages only) may be
+ * NULL.  Requires 1 <= M, 1 <= K <= Kmax; shapes whose selection buffers do
+ * not fit a CTA (Pmax beyond about 16,000) return KVMM_UNSUPPORTED_SHAPE.
+ */
+kvmm_status page_score_topk_centroid(const kvmm_shape* shape, int32_t layer, const kvmm_bf16* q,
+                                     const kvmm_bf16* mean, const int32_t* seq_len, int32_t R, const kvmm_bf16* cent,
+                                     const int32_t* member_off, const int32_t* members, const uint8_t* rescore_mask,
+                                     int32_t M, int32_t K, int32_t group_reduce, int32_t* sel_idx, int32_t* sel_cnt,
+                                     float* centroid_scores_out, float* scores_out, int32_t* err,
+                                     kvmm_stream stream);
+
+/* ------------------------------------------------------------------------
  * block_table_update -- apply the changed entries of the head-level block
  * table: block_table[idx[i]] = val[i], i = 0 .. n-1.
  *

@@ -296,6 +296,82 @@ kvmm_status kv_meankey_update(const kvmm_shape* shape, int32_t layer, const int3
     return launched(kvmm::launch_meankey(p, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+static kvmm::CentroidParams centroid_params(const kvmm_shape& s, int32_t layer, int32_t R)
+{
+    kvmm::CentroidParams p{};
+    p.B = s.B;
+    p.L = s.L;
+    p.Hq = s.Hq;
+    p.Hkv = s.Hkv;
+    p.G = s.Hq / s.Hkv;
+    p.D = s.D;
+    p.T = s.T;
+    p.Pmax = s.Pmax;
+    p.Kmax = s.Kmax;
+    p.layer = layer;
+    p.R = R;
+    p.Cmax = (s.Pmax + R - 1) / R;
+    return p;
+}
+
+kvmm_status kv_centroid_build(const kvmm_shape* shape, int32_t layer, const kvmm_bf16* mean, const int32_t* seq_len,
+                              int32_t R, int32_t n_iter, kvmm_bf16* cent, int32_t* assign, int32_t* member_off,
+                              int32_t* members, int32_t* err, kvmm_stream stream)
+{
+    kvmm_status st = check_shape(shape);
+    if (st != KVMM_OK) return st;
+    const kvmm_shape& s = *shape;
+    if (layer < 0 || layer >= s.L || R < 1 || R > s.Pmax || n_iter < 0 || n_iter > 64) return KVMM_INVALID_ARG;
+    if (!req(mean) || !req4(seq_len) || !req(cent) || !req4(assign) || !req4(member_off) || !req4(members) ||
+        !opt4(err))
+        return KVMM_INVALID_ARG;
+    kvmm::CentroidParams p = centroid_params(s, layer, R);
+    if (kvmm::centroid_update_smem(s.Pmax, p.Cmax) > kvmm::kDSmemLimit) return KVMM_UNSUPPORTED_SHAPE;
+    p.mean = mean;
+    p.seq_len = seq_len;
+    p.cent = cent;
+    p.assign = assign;
+    p.member_off = member_off;
+    p.members = members;
+    p.err = err;
+    return launched(kvmm::launch_centroid_build(p, n_iter, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+kvmm_status page_score_topk_centroid(const kvmm_shape* shape, int32_t layer, const kvmm_bf16* q,
+                                     const kvmm_bf16* mean, const int32_t* seq_len, int32_t R, const kvmm_bf16* cent,
+                                     const int32_t* member_off, const int32_t* members, const uint8_t* rescore_mask,
+                                     int32_t M, int32_t K, int32_t group_reduce, int32_t* sel_idx, int32_t* sel_cnt,
+                                     float* centroid_scores_out, float* scores_out, int32_t* err,
+                                     kvmm_stream stream)
+{
+    kvmm_status st = check_shape(shape);
+    if (st != KVMM_OK) return st;
+    const kvmm_shape& s = *shape;
+    if (layer < 0 || layer >= s.L || R < 1 || R > s.Pmax || M < 1 || K < 1 || K > s.Kmax) return KVMM_INVALID_ARG;
+    if (group_reduce != 0 && group_reduce != 1) return KVMM_INVALID_ARG;
+    if (!req(q) || !req(mean) || !req4(seq_len) || !req(cent) || !req4(member_off) || !req4(members) ||
+        !req4(sel_idx) || !req4(sel_cnt) || !opt4(centroid_scores_out) || !opt4(scores_out) || !opt4(err))
+        return KVMM_INVALID_ARG;
+    kvmm::CentroidParams p = centroid_params(s, layer, R);
+    p.M = M < p.Cmax ? M : p.Cmax;
+    p.K = K;
+    if (kvmm::centroid_select_smem(s.D, p.G, s.Pmax, p.Cmax, K, p.M) > kvmm::kDSmemLimit)
+        return KVMM_UNSUPPORTED_SHAPE;
+    p.q = q;
+    p.mean = mean;
+    p.seq_len = seq_len;
+    p.rescore_mask = rescore_mask;
+    p.cent = const_cast<kvmm_bf16*>(cent);  // read only here
+    p.member_off = const_cast<int32_t*>(member_off);
+    p.members = const_cast<int32_t*>(members);
+    p.sel_idx = sel_idx;
+    p.sel_cnt = sel_cnt;
+    p.centroid_scores_out = centroid_scores_out;
+    p.scores_out = scores_out;
+    p.err = err;
+    return launched(kvmm::launch_centroid_select(p, group_reduce, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 kvmm_status page_score_topk_static_scratch(const kvmm_shape* shape, int32_t layer, const kvmm_bf16* q,
                                            const kvmm_bf16* meta, const int32_t* seq_len,
                                            const uint8_t* rescore_mask, int32_t K, int32_t group_reduce,

@@ -226,6 +226,32 @@ struct PromoteParams {
     int32_t* err;
 };
 
+// kv_centroid_build / page_score_topk_centroid (centroid.cu)
+struct CentroidParams {
+    int32_t B, L, Hq, Hkv, G, D, T, Pmax, layer;
+    int32_t R;       // pages per initial spatial block
+    int32_t Cmax;    // centroids a unit holds at most: ceil(Pmax / R)
+    int32_t M, K;    // centroids expanded, pages selected
+    int32_t Kmax;    // row length of sel_idx
+    const kvmm_bf16* mean;       // [B][L][Hkv][Pmax][D]
+    const int32_t* seq_len;      // [B]
+    const uint8_t* rescore_mask; // [L][Hkv] or null
+    const kvmm_bf16* q;          // [B][Hq][D]
+    kvmm_bf16* cent;             // [B][L][Hkv][Cmax][D]
+    int32_t* assign;             // [B][L][Hkv][Pmax]
+    int32_t* member_off;         // [B][L][Hkv][Cmax + 1]
+    int32_t* members;            // [B][L][Hkv][Pmax]
+    int32_t* sel_idx;
+    int32_t* sel_cnt;
+    float* centroid_scores_out;  // [B][Hkv][Cmax] or null
+    float* scores_out;           // [B][Hkv][Pmax] or null
+    int32_t* err;
+};
+cudaError_t launch_centroid_build(const CentroidParams& p, int n_iter, cudaStream_t stream);
+cudaError_t launch_centroid_select(const CentroidParams& p, int group_reduce, cudaStream_t stream);
+size_t centroid_select_smem(int D, int G, int Pmax, int Cmax, int K, int M);  // dynamic shared memory of the selection
+size_t centroid_update_smem(int Pmax, int Cmax);                             // ... and of the update
+
 // topk_history_record / topk_stability_rco
 struct StabilityParams {
     int B, L, Hkv, T, Pmax, Kmax;

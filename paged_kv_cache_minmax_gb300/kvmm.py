@@ -25,7 +25,7 @@ EXPORTS = ("kv_minmax_update", "page_score_topk", "sparse_paged_decode_attn", "t
            "kvmm_status_string",
            "kvmm_last_cuda_error", "page_score_topk_static_scratch", "page_score_topk_attn", "decode_layer", "topk_history_record",
            "topk_stability_rco", "promote_pages", "block_table_update", "kv_meankey_update",
-           "page_score_topk_mean")
+           "page_score_topk_mean", "kv_centroid_build", "page_score_topk_centroid")
 
 
 class KvmmError(RuntimeError):
@@ -88,10 +88,12 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.block_table_update.argtypes = [SP, P, P, I32, P, P, P]
     lib.kv_meankey_update.argtypes = [SP, I32, P, P, P, P, P, P, P]
     lib.page_score_topk_mean.argtypes = [SP, I32, P, P, P, P, I32, I32, P, P, P, P, SZ, P, P]
+    lib.kv_centroid_build.argtypes = [SP, I32, P, P, I32, I32, P, P, P, P, P, P]
+    lib.page_score_topk_centroid.argtypes = [SP, I32, P, P, P, I32, P, P, P, P, I32, I32, I32, P, P, P, P, P, P]
     for f in ("kv_minmax_update", "page_score_topk", "sparse_paged_decode_attn", "topk_promotion_diff",
               "page_score_topk_static_scratch", "page_score_topk_attn", "decode_layer", "topk_history_record",
               "topk_stability_rco", "promote_pages", "block_table_update", "kv_meankey_update",
-              "page_score_topk_mean"):
+              "page_score_topk_mean", "kv_centroid_build", "page_score_topk_centroid"):
         getattr(lib, f).restype = ctypes.c_int
     lib.kvmm_workspace_size.argtypes = [SP, I32]
     lib.kvmm_workspace_size.restype = SZ
@@ -425,3 +427,45 @@ def page_score_topk_mean(shape: Shape, layer: int, q, mean, seq_len, rescore_mas
             _dev(err, "err", torch.int32, 1, optional=True), _stream(stream))
     _check("page_score_topk_mean", load().page_score_topk_mean(*args))
 
+
+def centroid_rows(shape: Shape, R: int) -> int:
+    """Cmax = ceil(Pmax / R): the centroid rows a unit holds at most."""
+    return (shape.Pmax + R - 1) // R
+
+
+def kv_centroid_build(shape: Shape, layer: int, mean, seq_len, R: int, n_iter: int, cent, assign, member_off, members,
+                      err=None, stream=None) -> None:
+    """KVDrive's centroid level over the layer's pages' mean keys: spatial blocks of R pages, then n_iter Lloyd
+    iterations.  cent [B,L,Hkv,Cmax,D] bf16, assign [B,L,Hkv,Pmax], member_off [B,L,Hkv,Cmax+1],
+    members [B,L,Hkv,Pmax] int32 (Cmax = ceil(Pmax / R))."""
+    s = shape
+    units = s.B * s.L * s.Hkv
+    cmax = centroid_rows(s, R)
+    args = (ctypes.byref(s), layer, _dev(mean, "mean", torch.bfloat16, units * s.Pmax * s.D),
+            _dev(seq_len, "seq_len", torch.int32, s.B), int(R), int(n_iter),
+            _dev(cent, "cent", torch.bfloat16, units * cmax * s.D), _dev(assign, "assign", torch.int32, units * s.Pmax),
+            _dev(member_off, "member_off", torch.int32, units * (cmax + 1)),
+            _dev(members, "members", torch.int32, units * s.Pmax), _dev(err, "err", torch.int32, 1, optional=True),
+            _stream(stream))
+    _check("kv_centroid_build", load().kv_centroid_build(*args))
+
+
+def page_score_topk_centroid(shape: Shape, layer: int, q, mean, seq_len, R: int, cent, member_off, members,
+                             rescore_mask, M: int, K: int, sel_idx, sel_cnt, err=None, centroid_scores_out=None,
+                             scores_out=None, group_reduce: int = 0, stream=None) -> None:
+    """The two-level selection: score the centroids, expand the M best, keep the K best of their pages."""
+    s = shape
+    units = s.B * s.L * s.Hkv
+    cmax = centroid_rows(s, R)
+    args = (ctypes.byref(s), layer, _dev(q, "q", torch.bfloat16, s.B * s.Hq * s.D),
+            _dev(mean, "mean", torch.bfloat16, units * s.Pmax * s.D), _dev(seq_len, "seq_len", torch.int32, s.B),
+            int(R), _dev(cent, "cent", torch.bfloat16, units * cmax * s.D),
+            _dev(member_off, "member_off", torch.int32, units * (cmax + 1)),
+            _dev(members, "members", torch.int32, units * s.Pmax),
+            _dev(rescore_mask, "rescore_mask", torch.uint8, s.L * s.Hkv, optional=True), int(M), int(K),
+            int(group_reduce), _dev(sel_idx, "sel_idx", torch.int32, units * s.Kmax),
+            _dev(sel_cnt, "sel_cnt", torch.int32, units),
+            _dev(centroid_scores_out, "centroid_scores_out", torch.float32, s.B * s.Hkv * cmax, optional=True),
+            _dev(scores_out, "scores_out", torch.float32, s.B * s.Hkv * s.Pmax, optional=True),
+            _dev(err, "err", torch.int32, 1, optional=True), _stream(stream))
+    _check("page_score_topk_centroid", load().page_score_topk_centroid(*args))
