@@ -873,9 +873,33 @@ def promote_arm(args):
         us = e0.elapsed_time(e1) * 1e3 / (2 * reps)
         results[str(ctas)] = {"us_per_call": us, "gbs": bytes_per_call / (us * 1e-6) / 1e9}
     ok = int(err.item()) == 0 and int(moved.min()) == n_move
+
+    # baselines of the same bytes: one cudaMemcpyAsync per promoted page's keys and one per its values (into
+    # the blocks the kernel uses), and one contiguous copy of that many bytes from pinned memory
+    def copies():
+        for b in range(B):
+            for h in range(Hkv):
+                for i in range(n_move):
+                    phys = (b * Hkv + h) * K + i
+                    k_pool[phys].copy_(host_k[b, 0, h, K + i], non_blocking=True)
+                    v_pool[phys].copy_(host_v[b, 0, h, K + i], non_blocking=True)
+    big_h = torch.empty(bytes_per_call // 2, dtype=torch.bfloat16).pin_memory()
+    big_d = torch.empty(bytes_per_call // 2, dtype=torch.bfloat16, device="cuda")
+    baselines = {}
+    for name, fn, r in (("memcpy_per_page", copies, 5), ("memcpy_contiguous", lambda: big_d.copy_(big_h, non_blocking=True),
+                                                         max(10, min(args.steps, 100)))):
+        with torch.cuda.stream(stream):
+            fn()
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+        us = time_graphs([g], stream, r)[0] * 1e3
+        baselines[name] = {"us_per_call": us, "gbs": bytes_per_call / (us * 1e-6) / 1e9}
     print(json.dumps({
         "metric": "promotion transfer: K/V moved from pinned host memory into recycled blocks", "unit": "GB/s",
         "higher_is_better": True, "bytes_per_call": bytes_per_call, "by_max_ctas": results,
+        "baselines": baselines,
         "config": {"workload": cfg.name, "units": units, "pages_per_unit": n_move, "top_k": K,
                    "page_bytes_kv": 2 * T * D * 2, "host_store": "pinned (cudaHostAlloc through torch)"},
         "device_err": int(err.item()), "all_moved": ok}), flush=True)
