@@ -119,6 +119,20 @@ __device__ __forceinline__ void bulk_copy_g2s_hint(void* dst, const void* src, u
         : "memory");
 }
 
+// 3-D tensor copy (TMA) global -> shared of the box at coordinates (c0, c1, c2) of the tensor map at `tmap`
+// (the generic address of a __grid_constant__ kernel parameter), completing the box's bytes of transaction
+// on `bar`, with an L2 cache policy for the source lines.  c0 times the element size must be a multiple of
+// 16 bytes; the destination is aligned as the map's swizzle requires (1024 bytes for the 128-byte swizzle).
+__device__ __forceinline__ void tma_load_3d_hint(void* dst, const void* tmap, int c0, int c1, int c2, uint64_t* bar,
+                                                 uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, %3, "
+        "%4}], [%5], %6;" ::"r"(smem_addr(dst)),
+        "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar)
 {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");

@@ -5,6 +5,10 @@
 // FlexiCache (MLSys'26 blog summary), "Core method, 2. MinMax-metadata page
 // scoring" and "Core method, 1. Stability-differentiated placement" /
 // "System design, head-level block table".
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
 #include "decode_layer.cuh"
 
 namespace kvmm {
@@ -101,6 +105,8 @@ DecodeGrid decode_layer_grid(const kvmm_shape& s, int ph)
             return c.g;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     DecodeGrid g{0, 0};
+    // a score item's tensor copy addresses its first row by a signed 32-bit coordinate
+    if (static_cast<long long>(s.B) * s.L * s.Hkv * s.Pmax > 0x7fffffffLL) return g;
     for (int nu = dl::kDUnits; nu >= 1 && g.nu == 0; --nu) {
         DecodeKernel kernel = decode_kernel_for(s.D, s.T, 0, nu, ph);  // both reductions: same resources
         const int clusters = (units + nu - 1) / nu;
@@ -134,9 +140,43 @@ DecodeGrid decode_layer_grid(const kvmm_shape& s, int ph)
     return g;
 }
 
+// The tensor map of the metadata for the score items' tensor copies: a 3-D tensor of 16-bit elements,
+// {64 (one 128-byte line), 2D / 64 lines of a [min | max] row, B * L * Hkv * Pmax rows}, read in boxes of
+// {64, 2D / 64, 16 rows} with the 128-byte swizzle; rows past the end read as zeros.  The encoder is the
+// driver's, reached through the runtime.
+static cudaError_t meta_tensor_map(CUtensorMap* m, const DecodeParams& p)
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    if (encode == nullptr) return cudaErrorNotSupported;
+    const cuuint64_t lines = static_cast<cuuint64_t>(2 * p.D / 64);
+    const cuuint64_t rows = static_cast<cuuint64_t>(p.B) * p.L * p.Hkv * p.Pmax;
+    const cuuint64_t dims[3] = {64, lines, rows};
+    const cuuint64_t strides[2] = {128, lines * 128};
+    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(lines), 16};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, p.meta, dims, strides, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 cudaError_t launch_decode_layer(DecodeParams p, int group_reduce, int ph, cudaStream_t stream)
 {
     DecodeKernel kernel = decode_kernel_for(p.D, p.T, group_reduce, p.NU, ph);
+    CUtensorMap tmeta{};  // the attention phase alone reads no metadata: left empty
+    if (ph & kPhScore) {
+        const cudaError_t e = meta_tensor_map(&tmeta, p);
+        if (e != cudaSuccess) return e;
+    }
     p.maxp = (p.Kmax + p.C - 1) / p.C;
     p.bt_smem = decode_layer_bt(p.D, p.T, p.Pmax, p.Kmax, p.C, p.G, p.NU, ph) ? 1 : 0;
     const size_t smem = decode_layer_smem(p.D, p.T, p.Pmax, p.Kmax, p.C, p.G, p.NU, ph);
@@ -144,7 +184,7 @@ cudaError_t launch_decode_layer(DecodeParams p, int group_reduce, int ph, cudaSt
     if (e != cudaSuccess) return e;
     const int clusters = (p.B * p.Hkv + p.NU - 1) / p.NU;
     return launch_pdl_cluster(kernel, dim3(static_cast<unsigned>(clusters * p.C)), dim3(dl::kDThreads), smem,
-                              stream, static_cast<unsigned>(p.C), p);
+                              stream, static_cast<unsigned>(p.C), p, tmeta);
 }
 
 }  // namespace kvmm

@@ -196,6 +196,16 @@ __host__ __device__ inline bool d_all_select(int ph, int NU, int P, int C)
     return (ph & kPhAttend) != 0 || d_two_level(NU, P, C);
 }
 
+// Where a unit's scores and score range go: to every CTA of the cluster (each selects from all of them), to
+// rank 0 alone (it alone selects), or to the scoring CTA itself (two levels: each CTA's first level reads
+// only the pages it scored and their range, the second only the candidates the CTAs exchange).
+enum DScoreDest { kDestAll = 0, kDestRank0 = 1, kDestOwn = 2 };
+__host__ __device__ inline int d_score_dest(int ph, int NU, int P, int C)
+{
+    if (d_two_level(NU, P, C)) return kDestOwn;
+    return (ph & kPhAttend) != 0 ? kDestAll : kDestRank0;
+}
+
 // the shared-memory plan, identical on host and device
 struct DLayout {
     size_t ring, part, qbuf, sbuf, bins, ts, selv, res, recv, btab, cand, total;
@@ -229,7 +239,8 @@ __host__ __device__ inline DLayout d_layout(int D, int T, int Pmax, int Kmax, in
 
 // ---------------------------------------------------------------------------
 template <int D, int T, int MODE, int NU, int PH>
-__global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const DecodeParams p)
+__global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const DecodeParams p,
+                                                                     const __grid_constant__ CUtensorMap tmeta)
 {
     static_assert(NU >= 1 && NU <= kDUnits, "units per cluster");
     static_assert(PH == kPhScore || PH == kPhAttend || PH == kPhBoth, "phases");
@@ -249,6 +260,11 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
     constexpr int kMTiles = D / 16;
     constexpr int kR = (2 * D / 8) / 4;         // 16-byte chunk groups of a [min | max] row
     static_assert(kSGrp == 1 && kSPiece == 16, "a score item is one group of 16 pages");
+    // A score item arrives by one tensor copy (TMA) with the 128-byte swizzle: a page's [min | max] row is
+    // kLines 128-byte lines, and 16-byte unit u of line l sits at unit u ^ (l & 7) of it, so the fragment loads
+    // of rows gid and gid + 1 (512 bytes apart, on the same banks) fall on different banks.
+    constexpr int kLines = kRowBytes / 128;
+    static_assert(kSSlot == kSPiece * kRowBytes && kSSlot % 1024 == 0, "a score slot is one swizzled box");
     static_assert(kRing <= kDRingMax && kSRing <= kDRingMax, "slot count");
     extern __shared__ __align__(1024) uint8_t smem[];
     __shared__ DecodeShared sh;
@@ -418,9 +434,14 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
             }
             for (int j = 0; j < nunits; ++j) {
                 const DUnit& u = sh.ud[j];
-                const bool here = u.rescored && (rank == 0 || d_all_select(PH, NU, u.P, C));
-                mbar_arrive_expect_tx(&sh.sbar[j],
-                                      here ? static_cast<uint32_t>(u.P) * 4u + static_cast<uint32_t>(C * kDCons * 8) : 0u);
+                // every score of the unit and every warp's range, or this CTA's own (two levels), or none
+                const int dest = d_score_dest(PH, NU, u.P, C);
+                uint32_t bytes = 0u;
+                if (u.rescored && dest == kDestOwn)
+                    bytes = static_cast<uint32_t>(u.hi - u.lo) * 4u + static_cast<uint32_t>(kDCons * 8);
+                else if (u.rescored && (dest == kDestAll || rank == 0))
+                    bytes = static_cast<uint32_t>(u.P) * 4u + static_cast<uint32_t>(C * kDCons * 8);
+                mbar_arrive_expect_tx(&sh.sbar[j], bytes);
                 if (kAttend) mbar_arrive_expect_tx(&sh.rbar[j], static_cast<uint32_t>(C * (2 * G + own)) * 4u);
             }
         }
@@ -800,24 +821,24 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
             return j < nunits;
         };
         auto issue_score = [&](int b2, int j, int sl) {
-            const int lo = sh.ud[j].lo, hi = sh.ud[j].hi;
-            const size_t ufull = sh.ud[j].ufull;
-            const int page0 = lo + sl * kSPiece;
-            const int npg = min(kSPiece, hi - page0);
-            if (lane == 0) mbar_arrive_expect_tx(&sh.full[w][b2], static_cast<uint32_t>(npg) * kRowBytes);
-            __syncwarp();
-            // each slot has its own copying lanes: a thread's bulk copies complete one after another
-            const int cl = lane - (kSPiece / 8) * b2;
-            if (cl >= 0 && 8 * cl < npg) {  // lane cl copies rows 8cl .. 8cl+7
-                const int rows = min(8, npg - 8 * cl);
-                bulk_copy_g2s_hint(my_ring + size_t(b2) * kSSlot + size_t(8 * cl) * kRowBytes,
-                                   p.meta + (ufull * p.Pmax + page0 + 8 * cl) * 2 * D,
-                                   static_cast<uint32_t>(rows) * kRowBytes, &sh.full[w][b2], stream_policy);
+            const int page0 = sh.ud[j].lo + sl * kSPiece;
+            // the 16 rows from page0 in one tensor copy, whole (rows past the unit's pages are read and not
+            // used; rows past the array's end arrive as zeros), issued by the slot's own lane: a thread's bulk
+            // copies complete one after another
+            if (lane == b2) {
+                mbar_arrive_expect_tx(&sh.full[w][b2], static_cast<uint32_t>(kSSlot));
+                tma_load_3d_hint(my_ring + size_t(b2) * kSSlot, &tmeta, 0, 0,
+                                 static_cast<int>(sh.ud[j].ufull * p.Pmax + page0), &sh.full[w][b2], stream_policy);
             }
             set_slot(b2, j, sl);
         };
-        // page `pg` of unit j receives tokens in this launch: its bounds in `staged` (the page's
-        // [min | max] row in shared memory) become those of all its rows below tok_end.  The selector warps
+        // the byte offset in a score slot of 16-byte unit u of page row pr (see kLines)
+        auto sw_off = [](int pr, int u) {
+            const int line = pr * kLines + (u >> 3);
+            return line * 128 + (((u & 7) ^ (line & 7)) << 4);
+        };
+        // page `pg` of unit j receives tokens in this launch: its bounds in row pr of the score slot (the
+        // page's [min | max] row in shared memory, swizzled) become those of all its rows below tok_end.  The selector warps
         // have them ready for the first such page; a later page of a multi-token append holds new rows
         // only.  (The selector warps write the rows and the metadata; a page they skip -- null or
         // out-of-range table entry -- keeps its bounds here too.)
@@ -828,13 +849,13 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
                 have_prep = true;
             }
         };
-        auto widen_page = [&](int j, int pg, uint8_t* staged) {
+        auto widen_page = [&](int j, int pg, uint8_t* slot, int pr) {  // pr: the page's row in the slot
             const DUnit& u = sh.ud[j];
             if (pg == u.tb / T) {
                 wait_prep();
                 if (sh.wide_ok[j] && lane < D / 4) {
                     const uint32_t* wv = sh.wide[j] + 4 * lane;
-                    *reinterpret_cast<uint4*>(staged + 16 * lane) =
+                    *reinterpret_cast<uint4*>(slot + sw_off(pr, lane)) =
                         make_uint4(from_key2(wv[0]), from_key2(wv[1]), from_key2(wv[2]), from_key2(wv[3]));
                 }
                 __syncwarp();
@@ -859,7 +880,7 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
                     for (int i = 0; i < 4; ++i)
                         acc[i] = half == 0 ? __vminu2(acc[i], k4[i]) : __vmaxu2(acc[i], k4[i]);
                 }
-                *reinterpret_cast<uint4*>(staged + half * 2 * D + 16 * sub) =
+                *reinterpret_cast<uint4*>(slot + sw_off(pr, half * (D / 8) + sub)) =
                     make_uint4(from_key2(acc[0]), from_key2(acc[1]), from_key2(acc[2]), from_key2(acc[3]));
             }
             __syncwarp();
@@ -872,10 +893,11 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
             if (sh.ud[rj].rescored) {
                 kmin = __reduce_min_sync(kFullMask, kmin);
                 kmax = __reduce_max_sync(kFullMask, kmax);
-                const int to = d_all_select(PH, NU, sh.ud[rj].P, C) ? C : 1;  // the CTAs that select the unit
-                if (lane < to) {
-                    red_async_minmax_u32<false>(&sh.rkey[rj][0], &sh.sbar[rj], static_cast<uint32_t>(lane), kmin);
-                    red_async_minmax_u32<true>(&sh.rkey[rj][1], &sh.sbar[rj], static_cast<uint32_t>(lane), kmax);
+                const int dest = d_score_dest(PH, NU, sh.ud[rj].P, C);  // the CTAs that select from the range
+                if (dest == kDestAll ? lane < C : lane == 0) {
+                    const uint32_t r = dest == kDestAll ? static_cast<uint32_t>(lane) : dest == kDestOwn ? rank : 0u;
+                    red_async_minmax_u32<false>(&sh.rkey[rj][0], &sh.sbar[rj], r, kmin);
+                    red_async_minmax_u32<true>(&sh.rkey[rj][1], &sh.sbar[rj], r, kmax);
                 }
             }
             kmin = 0xffffffffu;
@@ -889,16 +911,18 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
 #pragma unroll
             for (int grp = 0; grp < kSGrp; ++grp) {
                 if (16 * grp < npg) {
-                    const uint8_t* ra = slot + static_cast<size_t>(16 * grp + gid) * kRowBytes;
-                    const uint8_t* rb = ra + 8 * kRowBytes;
+                    // rows gid and gid + 8 share their swizzle (8 rows apart is a multiple of 8 lines)
+                    const uint8_t* ra = slot;
+                    const uint8_t* rb = slot + 8 * kRowBytes;
                     // four independent accumulation chains (even / odd r, low / high half of the chunk); the scoring
                     // kernels of every path sum them in this same order, so their scores agree bit for bit
                     float c[4] = {0.f, 0.f, 0.f, 0.f}, c2[4] = {0.f, 0.f, 0.f, 0.f};
                     float c3[4] = {0.f, 0.f, 0.f, 0.f}, c4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                     for (int r = 0; r < kR; ++r) {
-                        const uint4 ka = ld_shared_v4(ra + 16 * (4 * r + tig));
-                        const uint4 kb = ld_shared_v4(rb + 16 * (4 * r + tig));
+                        const int o = sw_off(16 * grp + gid, 4 * r + tig);
+                        const uint4 ka = ld_shared_v4(ra + o);
+                        const uint4 kb = ld_shared_v4(rb + o);
                         mma_bf16_16816((r & 1) ? c3 : c, ka.x, kb.x, ka.y, kb.y, wf[r][0], wf[r][1]);
                         mma_bf16_16816((r & 1) ? c4 : c2, ka.z, kb.z, ka.w, kb.w, wf[r][2], wf[r][3]);
                     }
@@ -931,10 +955,16 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
                         kmin = min(kmin, topk_order_key(s_hi));
                         kmax = max(kmax, topk_order_key(s_hi));
                     }
-                    const int to = d_all_select(PH, NU, sh.ud[j].P, C) ? C : 1;  // the CTAs that select the unit
-                    for (int r = tig; r < to; r += 4) {
-                        if (r0 < npg) st_async_f32(sb + r0, &sh.sbar[j], static_cast<uint32_t>(r), s_lo);
-                        if (r0 + 8 < npg) st_async_f32(sb + r0 + 8, &sh.sbar[j], static_cast<uint32_t>(r), s_hi);
+                    const int dest = d_score_dest(PH, NU, sh.ud[j].P, C);  // the CTAs that select the unit
+                    if (dest == kDestAll) {
+                        for (int r = tig; r < C; r += 4) {
+                            if (r0 < npg) st_async_f32(sb + r0, &sh.sbar[j], static_cast<uint32_t>(r), s_lo);
+                            if (r0 + 8 < npg) st_async_f32(sb + r0 + 8, &sh.sbar[j], static_cast<uint32_t>(r), s_hi);
+                        }
+                    } else if (tig == 0) {
+                        const uint32_t r = dest == kDestOwn ? rank : 0u;
+                        if (r0 < npg) st_async_f32(sb + r0, &sh.sbar[j], r, s_lo);
+                        if (r0 + 8 < npg) st_async_f32(sb + r0 + 8, &sh.sbar[j], r, s_hi);
                     }
                     if (orow && tig == 0) {
                         if (r0 < npg) orow[r0] = s_lo;
@@ -965,7 +995,7 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
                 uint8_t* slot = my_ring + size_t(b) * kSSlot;
                 const int pe = min(sh.ud[j].pe, page0 + npg);
                 for (int pg = max(sh.ud[j].pb, page0); pg < pe; ++pg)  // pages receiving new tokens
-                    widen_page(j, pg, slot + size_t(pg - page0) * kRowBytes);
+                    widen_page(j, pg, slot, pg - page0);
                 score_slot(slot, j, page0, npg);
                 __syncwarp();
                 fence_proxy_async_shared();  // this slot's reads, then the next copy into it
@@ -1247,7 +1277,7 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
 
 // the decode kernel for a shape's (D, T, group reduction, units per cluster), one function per phase set,
 // each in its own translation unit
-using DecodeKernel = void (*)(DecodeParams);
+using DecodeKernel = void (*)(DecodeParams, CUtensorMap);
 DecodeKernel decode_kernel_both(int D, int T, int mode, int nu);    // decode_layer.cu
 DecodeKernel decode_kernel_score(int D, int T, int mode, int nu);   // decode_score.cu
 DecodeKernel decode_kernel_attend(int D, int T, int nu);            // decode_attend.cu

@@ -6,6 +6,7 @@
 #include <cstdint>
 #include <utility>
 
+#include <cuda.h>  // CUtensorMap (the type only; the encoder is reached through the runtime)
 #include <cuda_runtime.h>
 
 #include "kvmm.h"
