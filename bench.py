@@ -447,13 +447,16 @@ def separate_calls_leg(st, cfg, L, q_dev, stream, reps, peak):
     ms_s, ms_a, ms_p = (m / L for m in time_graphs(graphs, stream, reps))
     b = algorithmic_bytes(cfg)
 
-    def rec(ms, nbytes):
+    def rec(ms, nbytes, kernel=None):
         gbs = nbytes / (ms / 1e3) / 1e9
-        return {"us_per_launch": ms * 1e3, "bytes_per_launch": nbytes, "gbs": gbs, "frac": gbs / peak}
+        out = {"us_per_launch": ms * 1e3, "bytes_per_launch": nbytes, "gbs": gbs, "frac": gbs / peak}
+        if kernel is not None:  # DRAM bytes of one launch from the committed ncu capture, if there is one
+            out["traffic"] = load_traffic(kernel, cfg.name, cfg.B)
+        return out
 
     both = b["score_launch"] + b["attn_launch"]
-    return {"page_score_topk": rec(ms_s, b["score_launch"]),
-            "sparse_paged_decode_attn": rec(ms_a, b["attn_launch"]),
+    return {"page_score_topk": rec(ms_s, b["score_launch"], "page_score_topk"),
+            "sparse_paged_decode_attn": rec(ms_a, b["attn_launch"], "sparse_paged_decode_attn"),
             "sum_of_alone": rec(ms_s + ms_a, both),
             "back_to_back": rec(ms_p, both),
             "flags": "KVMM_EARLY_READS",
