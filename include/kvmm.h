@@ -279,20 +279,22 @@ kvmm_status topk_promotion_diff(const kvmm_shape* shape, int32_t layer,
  * FlexiCache, "Core method, 2. MinMax-metadata page scoring" (score every
  * page from its key bounds, keep the top-K per layer and KV head) and
  * "Core method, 1" / "System design, head-level block table" (attend over
- * the selected pages only, through the head-level table).  Two kernels
- * instead of three: the scoring kernel, then the attention kernel, whose
- * CTAs select their unit's pages from the scores themselves (every CTA of a
- * unit's cluster computes the same exact top-K in shared memory) before
- * streaming them, so the separate selection kernel and its round trip
- * through global memory drop out.
+ * the selected pages only, through the head-level table).  One launch of
+ * the clustered kernel decode_layer runs, with nothing appended: a cluster
+ * streams its units' metadata, scores and selects on chip, then streams the
+ * selected pages.  Shapes whose per-unit buffers do not fit that kernel
+ * (long page tables) run two kernels instead: the scoring kernel, then an
+ * attention kernel whose CTAs select their unit's pages from the scores
+ * themselves before streaming them.
  *
  * Arguments, layouts and results are those of the two calls: sel_idx /
  * sel_cnt / scores_out of rescored units as page_score_topk writes them (the
  * others keep their selection, which the attention then uses), and out /
  * lse as sparse_paged_decode_attn writes them with its automatic split
- * count.  workspace as for page_score_topk.  When the selection does not fit
- * the attention CTA's shared memory (Pmax beyond about 30,000 pages), the
- * call runs page_score_topk and then sparse_paged_decode_attn (same results).
+ * count.  workspace as for page_score_topk (the one-launch kernel does not
+ * touch it).  When the selection does not fit the attention CTA's shared
+ * memory either (Pmax beyond about 30,000 pages), the call runs
+ * page_score_topk and then sparse_paged_decode_attn (same results).
  */
 kvmm_status page_score_topk_attn(const kvmm_shape* shape, int32_t layer, const kvmm_bf16* q,
                                  const kvmm_bf16* meta, const kvmm_bf16* k_pool, const kvmm_bf16* v_pool,

@@ -505,6 +505,29 @@ kvmm_status page_score_topk_attn(const kvmm_shape* shape, int32_t layer, const k
         !opt4(err))
         return KVMM_INVALID_ARG;
     if (workspace_bytes < score_ws_bytes(s)) return KVMM_WORKSPACE_TOO_SMALL;
+    {
+        // one launch of the clustered kernel with both phases and nothing appended: decode_layer without new
+        // rows, which leaves what the two calls leave
+        const kvmm::DecodeGrid g = kvmm::decode_layer_grid(s, kvmm::kPhBoth);
+        if (g.nu > 0) {
+            kvmm::DecodeParams dp = decode_params(s, layer, K, g, sm_scale);
+            dp.q = q;
+            dp.k_pool = const_cast<kvmm_bf16*>(k_pool);  // read only: nothing is appended
+            dp.v_pool = const_cast<kvmm_bf16*>(v_pool);
+            dp.block_table = block_table;
+            dp.meta = const_cast<kvmm_bf16*>(meta);
+            dp.seq_len = seq_len;
+            dp.rescore_mask = rescore_mask;
+            dp.sel_idx = sel_idx;
+            dp.sel_cnt = sel_cnt;
+            dp.scores_out = scores_out;
+            dp.out = out;
+            dp.lse = lse;
+            dp.err = err;
+            return launched(kvmm::launch_decode_layer(dp, group_reduce, kvmm::kPhBoth,
+                                                      reinterpret_cast<cudaStream_t>(stream)));
+        }
+    }
     const size_t scratch = kvmm::attention_select_scratch(s.Pmax, s.Kmax);
     const int splits = resolve_splits(s, 0, true);
     const int max_pages = (s.Kmax + splits - 1) / splits;

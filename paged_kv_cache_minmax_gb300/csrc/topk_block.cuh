@@ -298,9 +298,21 @@ __device__ __noinline__ int block_topk_reg(const float* scores, int P, int K, in
     }
     Group::sync();
 
-    // 3. the bin holding the K-th largest score: suffix sums over bins
+    // 3. the bin holding the K-th largest score: suffix sums over bins (a thread's bins stay in registers
+    //    for the search)
     constexpr int kBinsPerThread = kTopkBins / THREADS;
-    const int local = topk_bin_sum<kBinsPerThread>(ts.hist + kBinsPerThread * tid);
+    static_assert(kBinsPerThread % 4 == 0, "a thread's bins are whole 16-byte words");
+    int hb[kBinsPerThread];
+    int local = 0;
+#pragma unroll
+    for (int j = 0; j < kBinsPerThread; j += 4) {
+        const int4 h4 = *reinterpret_cast<const int4*>(&ts.hist[kBinsPerThread * tid + j]);
+        hb[j] = h4.x;
+        hb[j + 1] = h4.y;
+        hb[j + 2] = h4.z;
+        hb[j + 3] = h4.w;
+        local += (h4.x + h4.y) + (h4.z + h4.w);
+    }
     int incl = local;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -313,15 +325,16 @@ __device__ __noinline__ int block_topk_reg(const float* scores, int P, int K, in
     for (int w = warp + 1; w < kWarps; ++w) above += ts.wsum[w];
     if (above < K && K <= above + local) {
         int acc = above;
+#pragma unroll
         for (int j = kBinsPerThread - 1; j >= 0; --j) {
-            const int bj = kBinsPerThread * tid + j;
-            if (acc + ts.hist[bj] >= K) {
-                ts.tb = bj;
+            if (acc >= 0 && acc + hb[j] >= K) {
+                ts.tb = kBinsPerThread * tid + j;
                 ts.need = K - acc;
-                ts.cbin = ts.hist[bj];
-                break;
+                ts.cbin = hb[j];
+                acc = -1;  // found
+            } else if (acc >= 0) {
+                acc += hb[j];
             }
-            acc += ts.hist[bj];
         }
     }
     Group::sync();
@@ -331,28 +344,36 @@ __device__ __noinline__ int block_topk_reg(const float* scores, int P, int K, in
         return K;
     }
 
-    // 4. rank the threshold bin's pages exactly (value descending, page ascending), one per thread
-#pragma unroll
-    for (int e = 0; e < kPer; ++e)
-        if (b[e] == tb) ts.cand[atomicAdd(&ts.ncand, 1)] = i0 + e;
-    Group::sync();
-    for (int t = tid; t < cbin; t += THREADS) {
-        const int i = ts.cand[t];
-        const float s = sc[i];
-        int rank = 0;
-        for (int j = 0; j < cbin; ++j) {
-            const int i2 = ts.cand[j];
-            const float s2 = sc[i2];
-            rank += (s2 > s) || (s2 == s && i2 < i);
-        }
-        if (rank < need) atomicOr(&winbits[i >> 5], 1u << (i & 31));
-    }
-    Group::sync();
-    const uint32_t tw = winbits[i0 >> 5] >> (i0 & 31);  // this thread's 8 pages share one word
     uint32_t win = 0u;
+    if (need == cbin) {
+        // every score of the threshold bin wins (the common case: about one score a bin near the K-th): no
+        // ranking
 #pragma unroll
-    for (int e = 0; e < kPer; ++e)
-        if (b[e] > tb || (b[e] == tb && ((tw >> e) & 1u))) win |= 1u << e;
+        for (int e = 0; e < kPer; ++e)
+            if (b[e] >= tb) win |= 1u << e;
+    } else {
+        // 4. rank the threshold bin's pages exactly (value descending, page ascending), one per thread
+#pragma unroll
+        for (int e = 0; e < kPer; ++e)
+            if (b[e] == tb) ts.cand[atomicAdd(&ts.ncand, 1)] = i0 + e;
+        Group::sync();
+        for (int t = tid; t < cbin; t += THREADS) {
+            const int i = ts.cand[t];
+            const float s = sc[i];
+            int rank = 0;
+            for (int j = 0; j < cbin; ++j) {
+                const int i2 = ts.cand[j];
+                const float s2 = sc[i2];
+                rank += (s2 > s) || (s2 == s && i2 < i);
+            }
+            if (rank < need) atomicOr(&winbits[i >> 5], 1u << (i & 31));
+        }
+        Group::sync();
+        const uint32_t tw = winbits[i0 >> 5] >> (i0 & 31);  // this thread's 8 pages share one word
+#pragma unroll
+        for (int e = 0; e < kPer; ++e)
+            if (b[e] > tb || (b[e] == tb && ((tw >> e) & 1u))) win |= 1u << e;
+    }
 
     // 5. ordered compaction: thread t's winners follow those of threads below t
     const int mine = __popc(win);
