@@ -1152,15 +1152,20 @@ def load_parity(workload, launch_shape, early_reads):
 
 
 def load_traffic(kernel, workload, batch):
-    """dram bytes per launch of ``kernel`` on ``workload`` from the committed ncu summaries, if one
-    was captured at that batch (a launch covers one layer, so the layer count does not matter)."""
+    """dram bytes per launch of ``kernel`` on ``workload`` from the committed ncu summaries, if one was
+    captured at that batch (a launch covers one layer, so the layer count does not matter) with the current
+    CUDA sources: a capture of an earlier kernel no longer describes this one."""
+    from paged_kv_cache_minmax_gb300 import build as kbuild
+
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         d = json.load(f)
     rec = d.get(kernel, {}).get(workload)
-    return rec["bytes"] if rec and rec["batch"] == batch else None
+    if not rec or rec["batch"] != batch or rec.get("sources") != kbuild.source_digest():
+        return None
+    return rec["bytes"]
 
 
 def main():

@@ -99,14 +99,15 @@ DecodeGrid decode_layer_grid(const kvmm_shape& s, int ph)
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     const int units = s.B * s.Hkv, G = s.Hq / s.Hkv;
+    DecodeGrid g{0, 0};
+    // a score item's tensor copy addresses its first row by a signed 32-bit coordinate (checked before the
+    // cache, which does not key on the layer count)
+    if (static_cast<long long>(s.B) * s.L * s.Hkv * s.Pmax > 0x7fffffffLL) return g;
     for (const auto& c : cache)
         if (c.g.nu > 0 && c.dev == dev && c.D == s.D && c.T == s.T && c.Pmax == s.Pmax && c.Kmax == s.Kmax &&
             c.units == units && c.G == G && c.ph == ph)
             return c.g;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    DecodeGrid g{0, 0};
-    // a score item's tensor copy addresses its first row by a signed 32-bit coordinate
-    if (static_cast<long long>(s.B) * s.L * s.Hkv * s.Pmax > 0x7fffffffLL) return g;
     for (int nu = dl::kDUnits; nu >= 1 && g.nu == 0; --nu) {
         DecodeKernel kernel = decode_kernel_for(s.D, s.T, 0, nu, ph);  // both reductions: same resources
         const int clusters = (units + nu - 1) / nu;

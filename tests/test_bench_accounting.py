@@ -36,17 +36,33 @@ def test_k_at_least_p_selects_every_page():
     assert b["kv"] == cfg.B * cfg.Hkv * cfg.P * cfg.T * cfg.D * 2 * 2
 
 
-def test_measured_traffic_is_reported_only_for_the_captured_workload_and_batch():
+def test_measured_traffic_is_reported_only_for_the_captured_workload_batch_and_sources(tmp_path, monkeypatch):
+    import json
+    import os
+
+    from paged_kv_cache_minmax_gb300 import build as kbuild
+
+    # the committed captures: one launch of each workload, within a few percent of its algorithmic bytes
+    with open(os.path.join(bench.ROOT, "profiles", "traffic.json")) as f:
+        committed = json.load(f)
     for c in (2, 3, 5):
         cfg = workloads.CONFIGS[c]
-        captured = bench.load_traffic("decode_layer", cfg.name, cfg.B)
-        # each capture is one launch of its workload: within a few percent of its algorithmic bytes
+        rec = committed["decode_layer"][cfg.name]
         launch = bench.algorithmic_bytes(cfg)["decode_launch"]
-        assert captured is not None and launch <= captured < 1.05 * launch, c
+        assert rec["batch"] == cfg.B and launch <= rec["bytes"] < 1.05 * launch, c
+    # the gate: the workload, its batch and the sources the capture was taken with
     name = workloads.CONFIGS[2].name
+    B = workloads.CONFIGS[2].B
+    (tmp_path / "profiles").mkdir()
+    with open(tmp_path / "profiles" / "traffic.json", "w") as f:
+        json.dump({"decode_layer": {name: {"batch": B, "bytes": 123, "sources": kbuild.source_digest()}},
+                   "page_score_topk": {name: {"batch": B, "bytes": 456, "sources": "0000000000000000"}}}, f)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.load_traffic("decode_layer", name, B) == 123
     assert bench.load_traffic("decode_layer", name, 4) is None  # another batch: another launch
     assert bench.load_traffic("decode_layer", workloads.CONFIGS[4].name, workloads.CONFIGS[4].B) is None
-    assert bench.load_traffic("sparse_attn_kernel", name, workloads.CONFIGS[2].B) is None
+    assert bench.load_traffic("sparse_attn_kernel", name, B) is None
+    assert bench.load_traffic("page_score_topk", name, B) is None  # taken with other sources
 
 
 def test_the_mix_episode_counts_the_units_each_step_rescores():
