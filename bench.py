@@ -6,9 +6,9 @@ budget 128 pages): per layer, append the new token and refresh its page's
 MinMax, score every page, select the top-K and attend over the selected
 pages -- decode_layer, one launch -- and list promoted pages
 (topk_promotion_diff, on a side stream).  --path fused runs
-kv_minmax_update and page_score_topk_attn (scoring kernel, then the attention
-kernel that selects its own pages) instead; --path unfused runs
-kv_minmax_update, page_score_topk and sparse_paged_decode_attn.  A
+kv_minmax_update and page_score_topk_attn (one launch that scores, selects
+and attends) instead; --path unfused runs kv_minmax_update, page_score_topk
+and sparse_paged_decode_attn.  A
 layer-step is one layer of that step for the whole batch.
 
 Inputs are seeded synthetic tensors resident in HBM (32 GiB of K/V, 2 GiB of
@@ -492,6 +492,7 @@ def gpu_arm(args):
     splits = kvmm.auto_splits(shape)
     st = DecodeState.for_workload(wl)  # automatic split count (0): the clustered attention kernel
     one_launch = True  # decode_layer runs its one-launch kernel (else its two-kernel fallback)
+    clustered = kvmm.decode_layer_cluster(shape) > 0  # the shape fits the clustered decode kernel
     if args.path == "decode_layer":
         c_ctas = kvmm.decode_layer_cluster(shape)
         one_launch = c_ctas > 0
@@ -701,8 +702,8 @@ def gpu_arm(args):
                          "data per step, no flush)",
                    "step": step_desc,
                    "path": {"decode_layer": "decode_layer (append, score, select, attend: one launch)",
-                            "fused": "kv_minmax_update + page_score_topk_attn (scoring kernel + selecting "
-                                     "attention kernel)",
+                            "fused": "kv_minmax_update + page_score_topk_attn (score, select, attend: one "
+                                     "launch)",
                             "unfused": "kv_minmax_update + page_score_topk + sparse_paged_decode_attn"}[path],
                    **({"decode_flags": "KVMM_DECODE_EARLY_READS" if early_reads else 0}
                       if path == "decode_layer" else {})},
@@ -721,9 +722,12 @@ def gpu_arm(args):
         "e2e": {"value": e2e_steps * L * world / (e2e_ms / 1e3), "unit": "layer-steps/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "how": "pinned host q/new K,V -> device, graph replay, out/lse/promoted counts -> pinned host"},
-        # per layer: decode_layer, diff; or update, score, selecting attention, diff (fused); or update,
-        # score, top-K, diff, attention (unfused)
-        "gpu_launches": {"decode_layer": 2 if one_launch else 4, "fused": 4, "unfused": 5}[path] * L * args.steps,
+        # per layer: decode_layer, diff; or update, page_score_topk_attn, diff (fused); or update, scoring,
+        # attention, diff (unfused).  Where the clustered kernel does not fit the shape, decode_layer falls back
+        # to update + the two-kernel fused path, the fused call to a scoring and a selecting attention kernel,
+        # and page_score_topk to a scoring and a selection kernel
+        "gpu_launches": {"decode_layer": 2 if one_launch else 4, "fused": 3 if clustered else 4,
+                         "unfused": 4 if clustered else 5}[path] * L * args.steps,
         "clocks": clk,
         "device_err": err_word,
     }
