@@ -80,14 +80,47 @@ static size_t decode_layer_smem(int D, int T, int Pmax, int Kmax, int C, int G, 
         .total;
 }
 
-// Units per cluster and CTAs per cluster.  Two units a cluster when their buffers fit shared memory, else
-// one (long sequences: a unit's scores take 4 bytes a page), else none ({0, 0}: the two-kernel path).  The
-// cluster size is as many CTAs as the SMs allow for one wave of all the launch's clusters.  Clusters are
-// placed within a GPC, so SMs / clusters can overestimate; the occupancy query decides (a launch whose
-// clusters do not all fit at once runs in two waves).  The query must leave room for an eighth more
-// clusters: with programmatic dependent launch the next launch's first clusters take the SMs this one
-// leaves free before it ends, and a launch that needs every cluster place the GPU has was measured to
-// run part of its grid in a second wave.  Cached per device and shape.
+// Whether `clusters` clusters of c CTAs of `kernel` all fit the GPU at once, with room for an eighth more:
+// with programmatic dependent launch the next launch's first clusters take the SMs this one leaves free
+// before it ends, and a launch that needs every cluster place the GPU has was measured to run part of its
+// grid in a second wave.  Clusters are placed within a GPC, so SMs / c overestimates; the occupancy query
+// decides.
+static bool one_wave(DecodeKernel kernel, size_t smem, int c, int clusters, int sms)
+{
+    int n = 0;
+    if (c == 1) {
+        int per_sm = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, dl::kDThreads, smem) != cudaSuccess) {
+            cudaGetLastError();
+            return false;
+        }
+        n = per_sm * sms;
+    } else {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(clusters * c));
+        cfg.blockDim = dim3(dl::kDThreads);
+        cfg.dynamicSmemBytes = smem;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = static_cast<unsigned>(c);
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) {
+            cudaGetLastError();
+            return false;
+        }
+    }
+    return n >= clusters + (clusters + 7) / 8;
+}
+
+// Units per cluster and CTAs per cluster.  For each unit count a cluster (two when there are two units, then
+// one), the largest cluster whose buffers fit shared memory and whose clusters fit one wave; of those, the
+// one with more CTAs in all, two units a cluster on a tie (one unit's selection then overlaps the other's
+// streaming).  Measured at the 128K shape: clusters of 4 over one unit each (128 CTAs) 40.5 us a launch, of
+// 6 over two (96 CTAs) 43.9 us.  When no shape fits one wave, two units a cluster if their buffers fit,
+// else one; none at all ({0, 0}) sends the caller to the two-kernel path.  Cached per device and shape.
 DecodeGrid decode_layer_grid(const kvmm_shape& s, int ph)
 {
     struct Choice {
@@ -108,34 +141,34 @@ DecodeGrid decode_layer_grid(const kvmm_shape& s, int ph)
             c.units == units && c.G == G && c.ph == ph)
             return c.g;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    for (int nu = dl::kDUnits; nu >= 1 && g.nu == 0; --nu) {
+    long long best_ctas = 0;
+    bool best_wave = false;
+    // two units a cluster only when there are two: one unit in a two-unit layout has half the room
+    for (int nu = units < dl::kDUnits ? 1 : dl::kDUnits; nu >= 1; --nu) {
         DecodeKernel kernel = decode_kernel_for(s.D, s.T, 0, nu, ph);  // both reductions: same resources
         const int clusters = (units + nu - 1) / nu;
-        int c = sms / clusters;
-        if (c > kDMaxCluster) c = kDMaxCluster;
-        if (c < 1) c = 1;
-        for (; c > 1; --c) {
+        int c0 = sms / clusters;
+        if (c0 > kDMaxCluster) c0 = kDMaxCluster;
+        if (c0 < 1) c0 = 1;
+        int found = 0;
+        bool wave = false;
+        for (int c = c0; c >= 1 && !wave; --c) {
             const size_t smem = decode_layer_smem(s.D, s.T, s.Pmax, s.Kmax, c, G, nu, ph);
             if (smem > kDSmemLimit || prepare_decode(kernel, smem) != cudaSuccess) continue;
-            cudaLaunchConfig_t cfg = {};
-            cfg.gridDim = dim3(static_cast<unsigned>(clusters * c));
-            cfg.blockDim = dim3(dl::kDThreads);
-            cfg.dynamicSmemBytes = smem;
-            cudaLaunchAttribute attr[1];
-            attr[0].id = cudaLaunchAttributeClusterDimension;
-            attr[0].val.clusterDim.x = static_cast<unsigned>(c);
-            attr[0].val.clusterDim.y = 1;
-            attr[0].val.clusterDim.z = 1;
-            cfg.attrs = attr;
-            cfg.numAttrs = 1;
-            int n = 0;
-            if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) {
-                cudaGetLastError();
-                continue;
+            if (one_wave(kernel, smem, c, clusters, sms)) {
+                found = c;
+                wave = true;
+            } else if (found == 0 && c == 1) {
+                found = 1;  // more clusters than one wave holds: single CTAs, as many waves as it takes
             }
-            if (n >= clusters + (clusters + 7) / 8) break;
         }
-        if (decode_layer_smem(s.D, s.T, s.Pmax, s.Kmax, c, G, nu, ph) <= kDSmemLimit) g = {nu, c};
+        if (found == 0) continue;
+        const long long ctas = static_cast<long long>(clusters) * found;
+        if (g.nu == 0 || (wave && !best_wave) || (wave && best_wave && ctas > best_ctas)) {
+            g = {nu, found};
+            best_ctas = ctas;
+            best_wave = wave;
+        }
     }
     if (g.nu > 0) cache[next++ % 8] = {dev, s.D, s.T, s.Pmax, s.Kmax, units, G, ph, g};
     return g;

@@ -104,7 +104,7 @@ struct DecodeShared {
     uint64_t full[kDCons][kDRingMax];  // a consumer warp's slot has landed
     uint64_t qbar;            // the query groups of the cluster's units
     uint64_t btbar;           // the units' block-table rows are in btab (bt_smem)
-    uint64_t cbar;            // two-level selection: every CTA's candidates are here
+    uint64_t cbar[kDUnits];   // two-level selection: every CTA's candidates of the unit are here
     uint64_t sbar[kDUnits];   // all of the unit's scores and its range are here (asynchronous remote stores
                               // and reductions, 4 bytes each)
     uint64_t selr[kDUnits];   // this CTA's share of the unit's pages is resolved
@@ -181,28 +181,35 @@ __device__ __forceinline__ bool mbar_wait_sleepy(uint64_t* bar, uint32_t parity,
     return true;
 }
 
-// Two-level selection: with one unit a cluster and more pages than one CTA's selection holds in registers,
-// each CTA selects the top K of the pages it scored, the cluster's candidates (at most C*K) are exchanged,
-// and each CTA selects the top K of those.  Every page of the unit's top K is in its own CTA's top K (fewer
-// than K pages of that share outrank it), and the candidates are packed in ascending page order, so the
-// result, ties to the lower page included, is the one-level selection's.
-__host__ __device__ inline bool d_two_level(int NU, int P, int C) { return NU == 1 && C > 1 && P > 8 * kDSelThreads; }
+// Two-level selection: with one unit a cluster, when a unit may have more pages than one CTA's selection holds
+// in registers (a launch whose Pmax is above that, with clusters of more than one CTA), each CTA selects the
+// top K of the pages it scored, the cluster's candidates (at most C*K) are exchanged, and each CTA selects the
+// top K of those.  Every page of the unit's top K is in its own CTA's top K (fewer than K pages of that share
+// outrank it), and the candidates are packed in ascending page order, so the result, ties to the lower page
+// included, is the one-level selection's -- for every unit of the launch, whatever its own page count.  A CTA
+// then keeps only the scores of its own share.  Two units a cluster always select in one level: a compile-time
+// fact that keeps that kernel free of the two-level code (measured: the runtime test alone cost it 0.9 us a
+// launch at the 8B shape), and at long contexts one unit a cluster was the faster launch anyway.
+__host__ __device__ inline bool d_two_level(int NU, int Pmax, int C)
+{
+    return NU == 1 && C > 1 && Pmax > 8 * kDSelThreads;
+}
 
 // Which CTAs of the cluster select a unit (and so receive its scores and range): every one when the launch
 // also attends (each resolves its share of the selection) or selects in two levels; in a launch that only
 // scores and selects, rank 0 alone, which writes the selection, so that the other CTAs leave after scoring.
-__host__ __device__ inline bool d_all_select(int ph, int NU, int P, int C)
+__host__ __device__ inline bool d_all_select(int ph, int NU, int Pmax, int C)
 {
-    return (ph & kPhAttend) != 0 || d_two_level(NU, P, C);
+    return (ph & kPhAttend) != 0 || d_two_level(NU, Pmax, C);
 }
 
 // Where a unit's scores and score range go: to every CTA of the cluster (each selects from all of them), to
 // rank 0 alone (it alone selects), or to the scoring CTA itself (two levels: each CTA's first level reads
 // only the pages it scored and their range, the second only the candidates the CTAs exchange).
 enum DScoreDest { kDestAll = 0, kDestRank0 = 1, kDestOwn = 2 };
-__host__ __device__ inline int d_score_dest(int ph, int NU, int P, int C)
+__host__ __device__ inline int d_score_dest(int ph, int NU, int Pmax, int C)
 {
-    if (d_two_level(NU, P, C)) return kDestOwn;
+    if (d_two_level(NU, Pmax, C)) return kDestOwn;
     return (ph & kPhAttend) != 0 ? kDestAll : kDestRank0;
 }
 
@@ -218,8 +225,10 @@ __host__ __device__ inline DLayout d_layout(int D, int T, int Pmax, int Kmax, in
                                             int ph)
 {
     const bool sc = (ph & kPhScore) != 0, at = (ph & kPhAttend) != 0;
+    const bool two = sc && d_two_level(NU, Pmax, C);
+    const int share = (Pmax + C - 1) / C;  // pages a CTA scores at most
     DLayout l{};
-    l.pstride = (Pmax + 3) & ~3;
+    l.pstride = ((two ? share : Pmax) + 3) & ~3;  // per unit: its scores, or this CTA's share of them
     l.slice = ((G * D + C - 1) / C + 3) & ~3;  // outputs a CTA combines: a multiple of 4 (16-byte stores)
     l.recv_stride = 16 * C + l.slice * C;
     l.ring = 0;
@@ -227,13 +236,14 @@ __host__ __device__ inline DLayout d_layout(int D, int T, int Pmax, int Kmax, in
     l.qbuf = d_align(l.part + (at ? size_t(kDCons) * G * (D + 4) * sizeof(float) : 0));
     l.sbuf = d_align(l.qbuf + size_t(NU) * 8 * D * 2);
     l.bins = d_align(l.sbuf + (sc ? size_t(NU) * l.pstride * sizeof(float) : 0));
-    l.ts = d_align(l.bins + (sc ? size_t(Pmax) * sizeof(int16_t) : 0));
+    // bins: one per score the general top-K path ranks (a share, or the cluster's candidates, in two levels)
+    l.ts = d_align(l.bins + (sc ? size_t(two ? (share > C * Kmax ? share : C * Kmax) : Pmax) * sizeof(int16_t) : 0));
     l.selv = d_align(l.ts + (sc ? sizeof(BlockTopkShared<kDSelThreads>) : 0));
     l.res = d_align(l.selv + (sc ? size_t(Kmax) * sizeof(int32_t) : 0));
     l.recv = d_align(l.res + (at ? size_t(NU) * maxp * 2 * sizeof(int32_t) : 0));
     l.btab = d_align(l.recv + (at ? size_t(NU) * l.recv_stride * sizeof(float) : 0));
     l.cand = d_align(l.btab + (at && bt ? size_t(NU) * Pmax * sizeof(int32_t) : 0));
-    l.total = d_align(l.cand + (sc && d_two_level(NU, Pmax, C) ? size_t(C) * Kmax * 8 : 0));
+    l.total = d_align(l.cand + (two ? size_t(NU) * C * Kmax * 8 : 0));
     return l;
 }
 
@@ -281,8 +291,8 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
     int2* res = reinterpret_cast<int2*>(smem + lay.res);
     float* recv = reinterpret_cast<float*>(smem + lay.recv);
     int32_t* btab = reinterpret_cast<int32_t*>(smem + lay.btab);
-    float* cand_s = reinterpret_cast<float*>(smem + lay.cand);  // two-level selection: C*Kmax scores, then pages
-    int32_t* cand_p = reinterpret_cast<int32_t*>(cand_s + size_t(C) * p.Kmax);
+    // two-level selection, per unit: C*Kmax candidate scores, then their pages
+    float* cand = reinterpret_cast<float*>(smem + lay.cand);
 
     const int tid = threadIdx.x;
     const int lane = tid & 31;
@@ -299,8 +309,8 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
             for (int b2 = 0; b2 < kDRingMax; ++b2) mbar_init(&sh.full[w][b2], 1);
         mbar_init(&sh.qbar, 1);
         mbar_init(&sh.btbar, 1);
-        mbar_init(&sh.cbar, 1);
         for (int j = 0; j < kDUnits; ++j) {
+            mbar_init(&sh.cbar[j], 1);
             mbar_init(&sh.sbar[j], 1);
             mbar_init(&sh.selr[j], 1);
             mbar_init(&sh.rbar[j], 1);
@@ -423,19 +433,21 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
             // count negative; the pending arrival keeps the phase open until the count is set.
             const int e0 = static_cast<int>(rank) * lay.slice;
             const int own = max(0, min(n_out, e0 + lay.slice) - e0);
-            if (sh.ud[0].rescored && sh.ud[0].P > p.K && d_two_level(NU, sh.ud[0].P, C)) {
+            for (int j = 0; j < nunits; ++j) {
+                const DUnit& u = sh.ud[j];
+                if (!(u.rescored && u.P > p.K && d_two_level(NU, p.Pmax, C))) continue;
                 uint32_t n = 0;  // candidates: from every CTA min(K, pages it scored), 8 bytes each
                 for (int r = 0; r < C; ++r) {
-                    const int pr = static_cast<int>(static_cast<long long>(sh.ud[0].P) * (r + 1) / C) -
-                                   static_cast<int>(static_cast<long long>(sh.ud[0].P) * r / C);
+                    const int pr = static_cast<int>(static_cast<long long>(u.P) * (r + 1) / C) -
+                                   static_cast<int>(static_cast<long long>(u.P) * r / C);
                     n += static_cast<uint32_t>(min(p.K, pr));
                 }
-                mbar_arrive_expect_tx(&sh.cbar, n * 8u);
+                mbar_arrive_expect_tx(&sh.cbar[j], n * 8u);
             }
             for (int j = 0; j < nunits; ++j) {
                 const DUnit& u = sh.ud[j];
                 // every score of the unit and every warp's range, or this CTA's own (two levels), or none
-                const int dest = d_score_dest(PH, NU, u.P, C);
+                const int dest = d_score_dest(PH, NU, p.Pmax, C);
                 uint32_t bytes = 0u;
                 if (u.rescored && dest == kDestOwn)
                     bytes = static_cast<uint32_t>(u.hi - u.lo) * 4u + static_cast<uint32_t>(kDCons * 8);
@@ -572,14 +584,16 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
             int cnt;
             const int32_t* src;
             if (kScore && u.rescored) {
-                if (rank != 0 && !d_all_select(PH, NU, u.P, C)) continue;  // rank 0 selects this unit alone
+                if (rank != 0 && !d_all_select(PH, NU, p.Pmax, C)) continue;  // rank 0 selects this unit alone
                 // every score of the unit and its range are here (the histogram is cleared meanwhile)
                 block_topk_prepare<kDSelThreads, SelGroup>(ts);
                 if (!mbar_wait_sleepy(&sh.sbar[j], 0, aborting() ? kDAbortNs : kDWaitNs)) set_abort();
-                float* sj = sbuf + size_t(j) * lay.pstride;
-                if (u.P > p.K && d_two_level(NU, u.P, C)) {
+                float* sj = sbuf + size_t(j) * lay.pstride;  // the unit's scores, or this CTA's share of them
+                if (u.P > p.K && d_two_level(NU, p.Pmax, C)) {
+                    float* cand_s = cand + size_t(j) * 2 * C * p.Kmax;
+                    int32_t* cand_p = reinterpret_cast<int32_t*>(cand_s + size_t(C) * p.Kmax);
                     // this CTA's candidates: the top K of its share, to every CTA, after the earlier CTAs'
-                    const int n_l = block_topk<kDSelThreads, SelGroup>(nullptr, u.hi - u.lo, p.K, selv, sj + u.lo,
+                    const int n_l = block_topk<kDSelThreads, SelGroup>(nullptr, u.hi - u.lo, p.K, selv, sj,
                                                                        bins, ts, sh.rkey[j]);
                     int off = 0, n_all = 0;
                     for (int r = 0; r < C; ++r) {
@@ -590,12 +604,12 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
                     }
                     for (int i = stid; i < n_l * C; i += kDSelThreads) {
                         const int r = i / n_l, e = i - r * n_l;
-                        const int pg = u.lo + selv[e];
-                        st_async_f32(cand_s + off + e, &sh.cbar, static_cast<uint32_t>(r), sj[pg]);
-                        st_async_f32(cand_p + off + e, &sh.cbar, static_cast<uint32_t>(r), __int_as_float(pg));
+                        st_async_f32(cand_s + off + e, &sh.cbar[j], static_cast<uint32_t>(r), sj[selv[e]]);
+                        st_async_f32(cand_p + off + e, &sh.cbar[j], static_cast<uint32_t>(r),
+                                     __int_as_float(u.lo + selv[e]));
                     }
                     SelGroup::sync();  // selv is read
-                    if (!mbar_wait_sleepy(&sh.cbar, 0, aborting() ? kDAbortNs : kDWaitNs)) set_abort();
+                    if (!mbar_wait_sleepy(&sh.cbar[j], 0, aborting() ? kDAbortNs : kDWaitNs)) set_abort();
                     cnt = block_topk<kDSelThreads, SelGroup>(nullptr, n_all, p.K, selv, cand_s, bins, ts, nullptr);
                     for (int i = stid; i < cnt; i += kDSelThreads) selv[i] = cand_p[selv[i]];  // positions -> pages
                     SelGroup::sync();
@@ -893,7 +907,7 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
             if (sh.ud[rj].rescored) {
                 kmin = __reduce_min_sync(kFullMask, kmin);
                 kmax = __reduce_max_sync(kFullMask, kmax);
-                const int dest = d_score_dest(PH, NU, sh.ud[rj].P, C);  // the CTAs that select from the range
+                const int dest = d_score_dest(PH, NU, p.Pmax, C);  // the CTAs that select from the range
                 if (dest == kDestAll ? lane < C : lane == 0) {
                     const uint32_t r = dest == kDestAll ? static_cast<uint32_t>(lane) : dest == kDestOwn ? rank : 0u;
                     red_async_minmax_u32<false>(&sh.rkey[rj][0], &sh.sbar[rj], r, kmin);
@@ -955,16 +969,19 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
                         kmin = min(kmin, topk_order_key(s_hi));
                         kmax = max(kmax, topk_order_key(s_hi));
                     }
-                    const int dest = d_score_dest(PH, NU, sh.ud[j].P, C);  // the CTAs that select the unit
+                    const int dest = d_score_dest(PH, NU, p.Pmax, C);  // the CTAs that select the unit
                     if (dest == kDestAll) {
                         for (int r = tig; r < C; r += 4) {
                             if (r0 < npg) st_async_f32(sb + r0, &sh.sbar[j], static_cast<uint32_t>(r), s_lo);
                             if (r0 + 8 < npg) st_async_f32(sb + r0 + 8, &sh.sbar[j], static_cast<uint32_t>(r), s_hi);
                         }
                     } else if (tig == 0) {
+                        // rank 0 keeps the unit's scores by page; a CTA selecting in two levels, its share by
+                        // page - lo
                         const uint32_t r = dest == kDestOwn ? rank : 0u;
-                        if (r0 < npg) st_async_f32(sb + r0, &sh.sbar[j], r, s_lo);
-                        if (r0 + 8 < npg) st_async_f32(sb + r0 + 8, &sh.sbar[j], r, s_hi);
+                        float* so = dest == kDestOwn ? sb - sh.ud[j].lo : sb;
+                        if (r0 < npg) st_async_f32(so + r0, &sh.sbar[j], r, s_lo);
+                        if (r0 + 8 < npg) st_async_f32(so + r0 + 8, &sh.sbar[j], r, s_hi);
                     }
                     if (orow && tig == 0) {
                         if (r0 < npg) orow[r0] = s_lo;

@@ -187,14 +187,14 @@ def test_null_blocks_outside_the_selection_are_never_read():
     stats.check()
 
 
-@pytest.mark.parametrize("pages,K,units", [(8192, 96, 1), (8192, 300, 1), (6000, 300, 1), (12288, 96, 0)])
-def test_launch_shape_and_long_units(pages, K, units):
-    """decode_layer's launch shape is one the device can hold: two units a cluster at the 8B shape, one
-    for a unit of 6000 or 8192 pages (its scores no longer fit twice), and none at 12288 pages, where
-    decode_layer runs the append and page_score_topk_attn instead.  Either way it leaves what the separate
-    calls leave.  At K = 300 the selection takes the general top-K path (more than 2048 scores) at one of
-    its two levels: the first at 8192 pages (a CTA's share is larger), the second at 6000 pages (the
-    cluster's candidates are more)."""
+@pytest.mark.parametrize("pages,K,clustered", [(8192, 96, True), (8192, 300, True), (6000, 300, True),
+                                               (12288, 96, True), (16384, 1500, False)])
+def test_launch_shape_and_long_units(pages, K, clustered):
+    """decode_layer's launch shape is one the device can hold: two units a cluster at the 8B shape; for one
+    long unit (6000 to 12288 pages) a cluster that selects in two levels, each CTA keeping the scores of its
+    own share; and none at 16384 pages with K = 1500 (the candidates no longer fit), where decode_layer runs
+    the append and page_score_topk_attn instead.  Either way it leaves what the separate calls leave.  At
+    K = 300 the selection takes the general top-K path (more than 2048 scores) at one of its two levels."""
     bench_shape = kvmm.make_shape(8, 32, 32, 8, 128, 16, 2048, 128, 1)
     assert kvmm.decode_layer_units(bench_shape) == 2
     assert 1 <= kvmm.decode_layer_cluster(bench_shape) <= 16
@@ -202,15 +202,14 @@ def test_launch_shape_and_long_units(pages, K, units):
                            key_dist="outlier", n_planted=24, seed=83)
     a, b = twin_states(cfg)
     wl, st = a
-    assert kvmm.decode_layer_units(st.shape) == units
-    if units:
-        assert kvmm.decode_layer_cluster(st.shape) >= 1
+    if clustered:
+        assert kvmm.decode_layer_units(st.shape) == 1  # one unit: a one-unit layout
         c = kvmm.decode_layer_cluster(st.shape)
-        if K == 300:  # two levels (C > 1), one of them over more than 2048 scores
-            assert c > 1
-            assert (pages + c - 1) // c > 2048 if pages == 8192 else c * K > 2048
+        assert c > 1  # two levels
+        if K == 300:  # one level over more than 2048 scores: a CTA's share, or the cluster's candidates
+            assert max((pages + c - 1) // c, c * K) > 2048
     else:
-        assert kvmm.decode_layer_cluster(st.shape) == 0
+        assert kvmm.decode_layer_units(st.shape) == 0 and kvmm.decode_layer_cluster(st.shape) == 0
     nk, nv = workloads.step_tokens(wl, 0)
     sca, scb = run_both(a, b, 0, wl.q[0], nk[0], nv[0])
     assert st.read_err() == 0 and b[1].read_err() == 0
