@@ -212,8 +212,8 @@ __device__ __noinline__ void block_radix_topk(const float* sc, int P, int K, int
 // (the radix histogram's space) that their owners read back.  Same bins, same
 // threshold, same result.
 template <int THREADS, class Group = CtaGroup>
-__device__ __noinline__ int block_topk_reg(const float* scores, int P, int K, int32_t* sel, float* sc,
-                              BlockTopkShared<THREADS>& ts, const uint32_t* range)
+__device__ __forceinline__ int block_topk_reg_body(const float* scores, int P, int K, int32_t* sel, float* sc,
+                                                   BlockTopkShared<THREADS>& ts, const uint32_t* range)
 {
     constexpr int kPer = 8;
     constexpr int kWarps = THREADS / 32;
@@ -394,6 +394,14 @@ __device__ __noinline__ int block_topk_reg(const float* scores, int P, int K, in
     return K;
 }
 
+// the register path as a call (one copy of its code, however many call sites)
+template <int THREADS, class Group = CtaGroup>
+__device__ __noinline__ int block_topk_reg(const float* scores, int P, int K, int32_t* sel, float* sc,
+                                           BlockTopkShared<THREADS>& ts, const uint32_t* range)
+{
+    return block_topk_reg_body<THREADS, Group>(scores, P, K, sel, sc, ts, range);
+}
+
 // Selects the top K of the P scores at `scores` (global memory, read through
 // L2; or null when sc[] already holds them) into sel[] (shared or global
 // memory) and returns the count, min(K, P).  sc (P floats) and bin (P int16)
@@ -556,6 +564,17 @@ __device__ __noinline__ int block_topk(const float* scores, int P, int K, int32_
         if (bin[i] > tb) sel[pos++] = i;
     Group::sync();
     return K;
+}
+
+// block_topk with its register path inlined at the call site (the general path stays a call): for a caller
+// with a single call site on a latency-critical path, where the two calls' overhead shows
+template <int THREADS, class Group = CtaGroup>
+__device__ __forceinline__ int block_topk_inline(const float* scores, int P, int K, int32_t* sel, float* sc,
+                                                 int16_t* bin, BlockTopkShared<THREADS>& ts,
+                                                 const uint32_t* range = nullptr)
+{
+    if (K < P && P <= 8 * THREADS) return block_topk_reg_body<THREADS, Group>(scores, P, K, sel, sc, ts, range);
+    return block_topk<THREADS, Group>(scores, P, K, sel, sc, bin, ts, range);
 }
 
 }  // namespace kvmm
