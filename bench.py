@@ -627,15 +627,26 @@ def gpu_arm(args):
         sep = separate_calls_leg(st, cfg, L, q_dev, stream, max(3, min(args.steps // 4, 50)), peak)
 
     # ---- end to end: host buffers in, host results out ------------------------
-    # every step copies that step's queries and new K/V rows from pinned host memory into the buffers its
-    # graph reads, replays the graph, and copies out, lse and the promoted counts to pinned host memory
+    # every step copies that step's queries and new K/V rows from pinned host memory, replays its graph, and
+    # copies out, lse and the promoted counts to pinned host memory -- overlapped with the compute, as a decode
+    # loop runs it: step i+1's inputs cross the link into a staging buffer on a copy stream while step i
+    # computes, and step i's results are copied on the device into a staging buffer that a second stream reads
+    # back while step i+1 computes.  Two staging sets alternate; events keep each set from being overwritten
+    # before it is read.  The on-device copies into the graph's input buffers and out of its outputs run on
+    # the compute stream (a few MB each, at HBM rate).
     in_dev = [(a["q"], a["nk"], a["nv"]) for a in (step_inputs(t) for t in range(E))]
     in_host = [tuple(x.cpu().pin_memory() for x in trio) for trio in in_dev]
-    out_host = torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory()
-    lse_host = torch.empty(st.lse.shape, dtype=st.lse.dtype).pin_memory()
-    prom_host = torch.empty(st.promoted_cnt.shape, dtype=torch.int32).pin_memory()
+    out_dev = (st.out, st.lse, st.promoted_cnt)
+    out_host = tuple(torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in out_dev)
+    in_stage = [tuple(torch.empty_like(x) for x in in_dev[0]) for _ in range(2)]
+    out_stage = [tuple(torch.empty_like(x) for x in out_dev) for _ in range(2)]
     h2d = sum(x.numel() * x.element_size() for x in in_host[0])
-    d2h = out_host.numel() * 4 + lse_host.numel() * 4 + prom_host.numel() * 4
+    d2h = sum(x.numel() * x.element_size() for x in out_host)
+    h2d_stream, d2h_stream = torch.cuda.Stream(), torch.cuda.Stream()
+    in_ready = [torch.cuda.Event() for _ in range(2)]
+    in_free = [torch.cuda.Event() for _ in range(2)]
+    out_ready = [torch.cuda.Event() for _ in range(2)]
+    out_free = [torch.cuda.Event() for _ in range(2)]
     e2e_steps = max(3, min(args.steps, 200))
     if dist:
         dist.barrier()
@@ -643,14 +654,32 @@ def gpu_arm(args):
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         e0.record()
-        for i in range(e2e_steps):
-            t = i % E
-            for d, h in zip(in_dev[t], in_host[t]):
+    h2d_stream.wait_stream(stream)  # every copy of the timed region starts after e0
+    d2h_stream.wait_stream(stream)
+    for i in range(e2e_steps):
+        t, b = i % E, i % 2
+        with torch.cuda.stream(h2d_stream):  # host -> staging set b, once step i - 2 has taken it
+            h2d_stream.wait_event(in_free[b])
+            for d, h in zip(in_stage[b], in_host[t]):
                 d.copy_(h, non_blocking=True)
+            in_ready[b].record()
+        with torch.cuda.stream(stream):
+            stream.wait_event(in_ready[b])
+            for d, sg in zip(in_dev[t], in_stage[b]):
+                d.copy_(sg, non_blocking=True)
+            in_free[b].record()
             graphs[t].replay()
-            out_host.copy_(st.out, non_blocking=True)
-            lse_host.copy_(st.lse, non_blocking=True)
-            prom_host.copy_(st.promoted_cnt, non_blocking=True)
+            stream.wait_event(out_free[b])  # step i - 2's results have left staging set b
+            for sg, d in zip(out_stage[b], out_dev):
+                sg.copy_(d, non_blocking=True)
+            out_ready[b].record()
+        with torch.cuda.stream(d2h_stream):
+            d2h_stream.wait_event(out_ready[b])
+            for h, sg in zip(out_host, out_stage[b]):
+                h.copy_(sg, non_blocking=True)
+            out_free[b].record()
+    with torch.cuda.stream(stream):
+        stream.wait_stream(d2h_stream)
         e1.record()
     stream.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), dist, "cuda")
@@ -721,7 +750,9 @@ def gpu_arm(args):
                                        if external else "CUDA events, eager instrumented step after timing")},
         "e2e": {"value": e2e_steps * L * world / (e2e_ms / 1e3), "unit": "layer-steps/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "how": "pinned host q/new K,V -> device, graph replay, out/lse/promoted counts -> pinned host"},
+                "how": "every step: pinned host q/new K,V -> device (copy stream, overlapping the previous step), "
+                       "graph replay, out/lse/promoted counts -> pinned host (second stream, overlapping the next "
+                       "step); two staging sets"},
         # per layer: decode_layer, diff; or update, page_score_topk_attn, diff (fused); or update, scoring,
         # attention, diff (unfused).  Where the clustered kernel does not fit the shape, decode_layer falls back
         # to update + the two-kernel fused path, the fused call to a scoring and a selecting attention kernel,
