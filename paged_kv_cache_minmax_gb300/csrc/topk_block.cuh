@@ -36,7 +36,7 @@ struct BlockTopkShared {
     int cand[kTopkCandMax];
     float wmin[kWarps];
     float wmax[kWarps];
-    int wsum[kWarps];
+    alignas(16) int wsum[kWarps];  // read whole, 16 bytes at a time, when kWarps is a multiple of 4
     int rhist[256];
     int ncand;
     int tb;
@@ -45,6 +45,26 @@ struct BlockTopkShared {
     int digit;
     int remaining;
 };
+
+// the sum of the per-warp counts ts.wsum[w] over the warps w with lo <= w < hi, every count read in one pass
+// (16-byte loads when the warp count allows) instead of one dependent load a warp
+template <int WARPS>
+__device__ __forceinline__ int topk_wsum_range(const int* wsum, int lo, int hi)
+{
+    int s = 0;
+    if constexpr (WARPS % 4 == 0) {
+#pragma unroll
+        for (int w = 0; w < WARPS; w += 4) {
+            const int4 c = *reinterpret_cast<const int4*>(wsum + w);
+            s += (w >= lo && w < hi ? c.x : 0) + (w + 1 >= lo && w + 1 < hi ? c.y : 0) +
+                 (w + 2 >= lo && w + 2 < hi ? c.z : 0) + (w + 3 >= lo && w + 3 < hi ? c.w : 0);
+        }
+    } else {
+#pragma unroll
+        for (int w = 0; w < WARPS; ++w) s += w >= lo && w < hi ? wsum[w] : 0;
+    }
+    return s;
+}
 
 // The threads that run one selection: the whole CTA, or a group of N threads
 // (whole warps) starting at thread FIRST that synchronises on named barrier BAR.
@@ -321,21 +341,24 @@ __device__ __forceinline__ int block_topk_reg_body(const float* scores, int P, i
     }
     if (lane == 0) ts.wsum[warp] = incl;
     Group::sync();
-    int above = incl - local;
-    for (int w = warp + 1; w < kWarps; ++w) above += ts.wsum[w];
+    const int above = incl - local + topk_wsum_range<kWarps>(ts.wsum, warp + 1, kWarps);
     if (above < K && K <= above + local) {
-        int acc = above;
+        // the K-th largest score lies in this thread's bins: the highest bin j whose count together with the
+        // counts above it reaches K (suffix sums, then predicated selects: no early exit, no indexing)
+        int suf = above;  // scores in bins above j
+        int tj = 0, tneed = 0, tcnt = 0;
 #pragma unroll
         for (int j = kBinsPerThread - 1; j >= 0; --j) {
-            if (acc >= 0 && acc + hb[j] >= K) {
-                ts.tb = kBinsPerThread * tid + j;
-                ts.need = K - acc;
-                ts.cbin = hb[j];
-                acc = -1;  // found
-            } else if (acc >= 0) {
-                acc += hb[j];
+            if (suf < K && suf + hb[j] >= K) {
+                tj = j;
+                tneed = K - suf;
+                tcnt = hb[j];
             }
+            suf += hb[j];
         }
+        ts.tb = kBinsPerThread * tid + tj;
+        ts.need = tneed;
+        ts.cbin = tcnt;
     }
     Group::sync();
     const int tb = ts.tb, need = ts.need, cbin = ts.cbin;
@@ -385,8 +408,7 @@ __device__ __forceinline__ int block_topk_reg_body(const float* scores, int P, i
     }
     if (lane == 31) ts.wsum[warp] = pre;
     Group::sync();
-    int pos = pre - mine;
-    for (int w = 0; w < warp; ++w) pos += ts.wsum[w];
+    int pos = pre - mine + topk_wsum_range<kWarps>(ts.wsum, 0, warp);
 #pragma unroll
     for (int e = 0; e < kPer; ++e)
         if ((win >> e) & 1u) sel[pos++] = i0 + e;
@@ -506,8 +528,7 @@ __device__ __noinline__ int block_topk(const float* scores, int P, int K, int32_
     }
     if (lane == 0) ts.wsum[warp] = incl;
     Group::sync();
-    int above = incl - local;
-    for (int w = warp + 1; w < kWarps; ++w) above += ts.wsum[w];
+    const int above = incl - local + topk_wsum_range<kWarps>(ts.wsum, warp + 1, kWarps);
     if (above < K && K <= above + local) {
         int acc = above;
         for (int j = kBinsPerThread - 1; j >= 0; --j) {
@@ -558,8 +579,7 @@ __device__ __noinline__ int block_topk(const float* scores, int P, int K, int32_
     }
     if (lane == 31) ts.wsum[warp] = pre;
     Group::sync();
-    int pos = pre - mine;
-    for (int w = 0; w < warp; ++w) pos += ts.wsum[w];
+    int pos = pre - mine + topk_wsum_range<kWarps>(ts.wsum, 0, warp);
     for (int i = i0; i < i1; ++i)
         if (bin[i] > tb) sel[pos++] = i;
     Group::sync();
