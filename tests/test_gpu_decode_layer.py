@@ -227,6 +227,37 @@ def test_launch_shape_and_long_units(pages, K, clustered):
     assert_same(a, b, sca, scb, 0)
 
 
+def test_two_level_launch_with_short_units():
+    """Two-level selection is chosen per launch (Pmax above a CTA's register-path capacity), so the short units
+    of a long launch select in two levels too: a unit of 151 pages over 16 CTAs (shares of 9 or 10 pages, each
+    CTA's candidates its whole share), one of 51 pages and one of a single page (fewer pages than K: every
+    page), beside a unit of 8192 pages.  decode_layer leaves what the separate calls leave, and each unit
+    matches the oracle."""
+    cfg = workloads.Config("mixed-long", B=4, L=1, Hq=4, Hkv=1, D=128, T=16, S=16 * 8192 - 3, K=96,
+                           key_dist="outlier", n_planted=24, seed=85)
+    lens = [16 * 8192 - 3, 150 * 16 + 7, 50 * 16 + 5, 1]
+    out = []
+    for _ in range(2):
+        wl = workloads.generate(cfg, device="cuda")
+        wl.seq_len.copy_(torch.tensor(lens, dtype=torch.int32, device="cuda"))
+        st = DecodeState.for_workload(wl)
+        st.build_metadata()
+        out.append((wl, st))
+    torch.cuda.synchronize()
+    a, b = out
+    wl, st = a
+    assert kvmm.decode_layer_units(st.shape) == 1 and kvmm.decode_layer_cluster(st.shape) > 1  # two levels
+    nk, nv = workloads.step_tokens(wl, 0)
+    sca, scb = run_both(a, b, 0, wl.q[0], nk[0], nv[0])
+    assert st.read_err() == 0 and b[1].read_err() == 0
+    assert_same(a, b, sca, scb, 0)
+    assert st.sel_cnt[:, 0, 0].tolist() == [96, 96, 51, 1]
+    stats = parity.Stats()
+    for bb in range(cfg.B):
+        parity.check_unit(wl, st, 0, bb, 0, wl.q[0], sca, stats)
+    stats.check()
+
+
 EARLY_CASES = {
     "llama-6-layers": scaled(CONFIGS[2], B=4, L=6, S=4096, K=32, n_planted=16, ragged=True),
     "gqa5-t32": CASES["gqa5-t32"],
