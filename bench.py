@@ -316,9 +316,11 @@ def decode_step(st, path, L, q, nk, nv, early_reads, side, forks, mask=None, ev=
         if path == "unfused":
             if ev is not None:
                 ev[4 * l + 2].record()
+            # early reads: the scoring call just before writes selections and scores only (it reads early
+            # nothing itself: the update before it writes the metadata rows it scores)
             kvmm.sparse_paged_decode_attn(st.shape, l, q[l], st.k_pool, st.v_pool, st.block_table, sl, st.sel_idx,
                                           st.sel_cnt, st.out[l], st.workspace, lse=st.lse[l], err=st.err,
-                                          num_splits=st.num_splits)
+                                          num_splits=st.num_splits, early_reads=early_reads)
             if ev is not None:
                 ev[4 * l + 3].record()
     main.wait_stream(side)
@@ -707,10 +709,10 @@ def gpu_arm(args):
         dom, dom_ms, dom_bytes = "page_score_topk_attn", s_ms, acc_all["fused_launch"]
         kernel_ms = {"page_score_topk_attn": s_ms}
     else:
-        dom = "sparse_attn_kernel" if a_ms >= s_ms else "score_topk_kernel"
+        dom = "sparse_paged_decode_attn" if a_ms >= s_ms else "page_score_topk"
         dom_ms = max(a_ms, s_ms)
         dom_bytes = acc_all["attn_launch"] if a_ms >= s_ms else acc_all["score_launch"]
-        kernel_ms = {"score_topk_kernel": s_ms, "sparse_attn_kernel": a_ms}
+        kernel_ms = {"page_score_topk": s_ms, "sparse_paged_decode_attn": a_ms}
     kernel_ms["per_layer_step_ms"] = ms_total / args.steps / L
     achieved = dom_bytes / (dom_ms / 1e3) / 1e9
     traffic = load_traffic(dom, workloads.CONFIGS[args.config].name, cfg.B)
