@@ -118,8 +118,11 @@ static bool one_wave(DecodeKernel kernel, size_t smem, int c, int clusters, int 
 // Units per cluster and CTAs per cluster.  For each unit count a cluster (two when there are two units, then
 // one), the largest cluster whose buffers fit shared memory and whose clusters fit one wave; of those, the
 // one with more CTAs in all, two units a cluster on a tie (one unit's selection then overlaps the other's
-// streaming).  Measured at the 128K shape: clusters of 4 over one unit each (128 CTAs) 40.5 us a launch, of
-// 6 over two (96 CTAs) 43.9 us.  When no shape fits one wave, two units a cluster if their buffers fit,
+// streaming) -- except in a launch that only attends, which takes one unit a cluster on a tie when its
+// clusters keep two CTAs or more.  Measured at the 128K shape: clusters of 4 over one unit each (128 CTAs)
+// 40.5 us a launch, of 6 over two (96 CTAs) 43.9 us; attention alone at the 8B shape: one unit in clusters of
+// 2, 15.6 us, two in clusters of 4, 16.4 us; at the GQA-5 shape single-CTA clusters 27.4 us against two units
+// in clusters of 2, 27.3 us.  When no shape fits one wave, two units a cluster if their buffers fit,
 // else one; none at all ({0, 0}) sends the caller to the two-kernel path.  Cached per device and shape.
 DecodeGrid decode_layer_grid(const kvmm_shape& s, int ph)
 {
@@ -164,7 +167,10 @@ DecodeGrid decode_layer_grid(const kvmm_shape& s, int ph)
         }
         if (found == 0) continue;
         const long long ctas = static_cast<long long>(clusters) * found;
-        if (g.nu == 0 || (wave && !best_wave) || (wave && best_wave && ctas > best_ctas)) {
+        // a launch that only attends has no selection to overlap, and each unit's merge spans the cluster: on a
+        // tie it takes one unit a cluster, unless that leaves single-CTA clusters
+        const bool tie_to_one = ph == kPhAttend && nu == 1 && found > 1 && ctas == best_ctas;
+        if (g.nu == 0 || (wave && !best_wave) || (wave && best_wave && (ctas > best_ctas || tie_to_one))) {
             g = {nu, found};
             best_ctas = ctas;
             best_wave = wave;
