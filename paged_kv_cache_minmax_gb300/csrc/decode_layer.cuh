@@ -459,7 +459,10 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
         }
         if (p.early) {
             pdl_wait_then_release();  // the preceding kernel is done: the queries and new rows are final
-            if (stid == 0) issue_q();
+            // a launch that only attends has consumer warp 0 copy the queries: the resolution that the first
+            // page copies wait for does not stall behind issuing them (attention alone at the 8B shape: 15.52
+            // -> 15.45 us)
+            if (kScore && stid == 0) issue_q();
         }
         // 0. for the consumer warps, well before they need them: the finished bounds of the first page the
         //    new tokens reach, if this CTA scores it (all its rows below tok_end, old and new), and for a
@@ -997,7 +1000,10 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_layer_kernel(const Decode
             }
         };
         if constexpr (!kScore) {
-            if (p.early) pdl_wait_then_release();  // before the kept selections, the pools and any store
+            if (p.early) {
+                pdl_wait_then_release();  // before the queries, the kept selections, the pools and any store
+                if (w == 0 && lane == 0) issue_q();
+            }
         } else {
             int ij = 0, isl = w - kDCons;  // the last issued item
             bool more = next_score(ij, isl);
