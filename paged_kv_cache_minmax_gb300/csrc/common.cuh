@@ -138,12 +138,6 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar)
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
-// named barrier over `threads` threads (a multiple of 32) of the CTA
-__device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t threads)
-{
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
-}
-
 // ---------------------------------------------------------------------------
 // thread-block clusters and distributed shared memory
 __device__ __forceinline__ uint32_t cluster_ctarank()
@@ -163,17 +157,6 @@ __device__ __forceinline__ void cluster_sync()
 // the two halves of cluster_sync, for work that needs neither in between
 __device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
 __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
-
-// load a float from the shared memory of CTA `rank` of the cluster, at the
-// address that `local` has in this CTA's shared memory
-__device__ __forceinline__ float ld_dsmem_f32(const void* local, uint32_t rank)
-{
-    uint32_t remote;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(local)), "r"(rank));
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
-    return v;
-}
 
 // store a float into the shared memory of CTA `rank` of the cluster, at the
 // address that `local` has in this CTA's shared memory (visible to that CTA
