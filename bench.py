@@ -204,7 +204,12 @@ def cpu_baseline(cfg, target_seconds=12.0):
     reps = max(1, int(target_seconds / max(first, 1e-6)))
     wall = sum(run_oracle_units(states, threads) for _ in range(reps))
     ls_per_s = reps / wall
+    one = run_oracle_units(states, 1)  # the same layer-step on one thread
+    b = algorithmic_bytes(cfg)
     return {"value": ls_per_s, "unit": "layer-steps/s", "cores": threads, "kind": "oracle",
+            "gbs": b["total"] * ls_per_s / 1e9,
+            "one_thread": {"value": 1.0 / one, "unit": "layer-steps/s", "gbs": b["total"] / one / 1e9,
+                           "sample": "one layer-step on one thread"},
             "sample": f"{reps} layer-steps of {cfg.name}, each all {units_per_layer} (batch, KV head) units of one "
                       f"layer (per unit: append+MinMax, score all {cfg.P} pages, top-{cfg.K}, diff, attention), "
                       f"on {threads} threads; {wall:.1f} s wall"}
